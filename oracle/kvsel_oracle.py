@@ -1,0 +1,292 @@
+"""fp64 CPU oracle for window-attention KV selection.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the library calls this module; only the
+tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py``
+use it.  It shares no code with the CUDA path and imports nothing from it.
+
+Each function writes out the plain definition of one step, in float64, with
+numpy (a matrix product and a sort are the only library primitives used).
+Inputs arrive as bf16 values (from the workload generator) and are decoded to
+float64 exactly.
+
+Sources (page title, then the section / equation the step follows):
+
+* ClusterAttn: KV Cache Compression under Intrinsic Attention Clustering (ACL
+  2025), 'Background and key observations' (背景知识与关键观察): the feature
+  aggregation equations W_win = Q[:, -L_win:] K^T, the window mask M_win, the
+  softmax A^m_win and the column sum P = sum over the window rows of
+  A^m_win[:, i, :L_pre]; 'Method details' (方法细节): the compressed prefix is
+  concatenated with the full observation window.
+* CLAA: cross-layer attention aggregation (2026), 'Three representative
+  token-ranking methods' (FastKV) and 'Three design decisions', decision 2:
+  post-softmax window probabilities summed over the window queries and heads;
+  decision 3 (Eq. 6): per-token aggregation across layers; 'Oracle
+  construction': 1-D pooling with kernel 7 after the aggregation.
+* DELTA: Dynamic Layer-Aware Token Attention (ACL 2026 Findings), 'Key
+  designs' 2 and 3: token score = max over heads, page score over the P = 16
+  tokens of a page, last L pages kept plus the top K - L of the remaining pages.
+* LookaheadKV (2026), 'Background: KL divergence and ListNet': L1
+  normalisation s / ||s||_1 of importance scores.
+* CompactAttention: Accelerating Chunked Prefill with Block-Union KV Selection,
+  'Core method' and 'Method steps' (2): Q-block union, intra-group union and
+  the per-group table T_{b,g} = { j | G_{b,g,j} = 1 }.
+
+Readings taken where the pages are silent or garbled (each is also listed in
+the design notes):
+
+* The window mask is additive-causal: window row j (absolute position L + j)
+  sees every prefix key and window keys 0..j; the softmax runs over that full
+  row; only prefix columns t < L are emitted.
+* Scale is 1/sqrt(d) (the standard attention scale the CLAA page names).
+* Query head h belongs to KV head g = h // (H_q / H_kv).
+* Max-over-heads with W > 1 is max_h (sum_j p): the column mass of each head
+  first, then the max over the heads of the group.
+* Pooling is max-pooling, centred, stride 1, same length, out-of-range
+  neighbours ignored, over prefix columns only.
+* A page's score reduces the pooled token scores of its tokens (max by
+  default, sum as the DELTA page prints it); the last page may be partial.
+* Ranking is by (score descending, index ascending).
+* Selected entries are returned in ascending original position, then the
+  observation window (token mode) or its pages (page mode) is appended.
+* Cross-layer: each layer's group score is L1-normalised over t < L, then the
+  mean over an inclusive layer range is taken, then pooled.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+
+def _f64(x) -> np.ndarray:
+    """bf16 / fp32 torch tensor or array -> float64 ndarray (exact)."""
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu")
+        if str(x.dtype) == "torch.bfloat16":
+            x = x.float()
+        return x.double().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+# --------------------------------------------------------------------------- scoring
+
+def window_logits(q: np.ndarray, k: np.ndarray) -> np.ndarray:
+    """z[r, t] = <q_r, k_t> / sqrt(d) for every window query row r and key t.
+
+    ClusterAttn 'Background and key observations', W_win = Q[:, -L_win:] K^T,
+    with the 1/sqrt(d_k) scale of standard attention.
+    q: [R, d] float64, k: [N, d] float64 -> [R, N].
+    """
+    d = q.shape[-1]
+    return (q @ k.T) / np.sqrt(d)
+
+
+def window_mask(L: int, W: int) -> np.ndarray:
+    """visible[j, t] for window row j and key t < L + W: all prefix keys, window keys 0..j."""
+    t = np.arange(L + W)[None, :]
+    j = np.arange(W)[:, None]
+    return t <= L + j
+
+
+def window_probs(q_group: np.ndarray, k_head: np.ndarray, L: int) -> np.ndarray:
+    """A^m_win: masked softmax rows of one GQA group.
+
+    q_group: [G, W, d] window queries of the G query heads that share KV head
+    k_head: [L + W, d].  Returns p [G, W, L + W]; each row sums to one over
+    its visible keys and is zero on masked ones.
+    """
+    G, W, d = q_group.shape
+    z = window_logits(q_group.reshape(G * W, d), k_head).reshape(G, W, L + W)
+    vis = window_mask(L, W)[None, :, :]
+    z = np.where(vis, z, -np.inf)
+    m = z.max(axis=-1, keepdims=True)
+    e = np.exp(z - m)
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def column_mass(p: np.ndarray, L: int) -> np.ndarray:
+    """P: column sum over the window rows, restricted to prefix columns :L.  [G, W, N] -> [G, L]."""
+    return p[:, :, :L].sum(axis=1)
+
+
+def group_reduce(c: np.ndarray, mode: str) -> np.ndarray:
+    """Reduce the per-head column mass [G, L] over the heads of one group: 'sum' or 'max'."""
+    if mode == "sum":
+        return c.sum(axis=0)
+    if mode == "max":
+        return c.max(axis=0)
+    raise ValueError(mode)
+
+
+def group_scores(q_group, k_head, L: int, mode: str) -> np.ndarray:
+    """s[t], t < L, for one (layer, KV head): probabilities -> column mass -> group reduce."""
+    return group_reduce(column_mass(window_probs(q_group, k_head, L), L), mode)
+
+
+def max_pool(s: np.ndarray, k: int) -> np.ndarray:
+    """u[t] = max of s over [t - r, t + r] intersected with [0, len), r = (k - 1) / 2 (last axis)."""
+    if k % 2 != 1 or k < 1:
+        raise ValueError("pool width must be odd")
+    r = (k - 1) // 2
+    n = s.shape[-1]
+    out = s.copy()
+    for off in range(1, r + 1):
+        if off >= n:
+            break
+        out[..., :-off] = np.maximum(out[..., :-off], s[..., off:])
+        out[..., off:] = np.maximum(out[..., off:], s[..., :-off])
+    return out
+
+
+def page_reduce(u: np.ndarray, P: int, mode: str = "max") -> np.ndarray:
+    """U[p] over the tokens [pP, min((p+1)P, L)) of each page (last axis; last page may be partial)."""
+    n = u.shape[-1]
+    n_pages = -(-n // P)
+    pad = n_pages * P - n
+    fill = -np.inf if mode == "max" else 0.0
+    x = np.concatenate([u, np.full(u.shape[:-1] + (pad,), fill)], axis=-1)
+    x = x.reshape(u.shape[:-1] + (n_pages, P))
+    if mode == "max":
+        return x.max(axis=-1)
+    if mode == "sum":
+        return x.sum(axis=-1)
+    raise ValueError(mode)
+
+
+def l1_normalise(s: np.ndarray) -> np.ndarray:
+    """s / ||s||_1 along the last axis (LookaheadKV's normalisation of importance scores)."""
+    return s / np.abs(s).sum(axis=-1, keepdims=True)
+
+
+def cross_layer_mean(s_layers: np.ndarray, lo: int, hi: int) -> np.ndarray:
+    """Mean over layers lo..hi (inclusive) of the L1-normalised scores.  s_layers: [n_layers, ..., L]."""
+    return l1_normalise(s_layers[lo:hi + 1]).mean(axis=0)
+
+
+# --------------------------------------------------------------------------- selection
+
+def rank(scores: np.ndarray) -> np.ndarray:
+    """Positions ordered by (score descending, index ascending), by a full stable sort."""
+    n = scores.shape[-1]
+    return np.lexsort((np.arange(n), -scores))
+
+
+def select_tokens(u: np.ndarray, k: int, L: int, W: int) -> np.ndarray:
+    """Top-k prefix tokens of one row, ascending, followed by the window positions L..L+W-1."""
+    top = np.sort(rank(u[:L])[:k])
+    return np.concatenate([top, np.arange(L, L + W)]).astype(np.int64)
+
+
+def select_pages(U: np.ndarray, k: int, n_recent: int, L: int, W: int, P: int) -> np.ndarray:
+    """DELTA page rule for one row, then the window's pages.
+
+    The last ``n_recent`` prefix pages are always kept; the top k of the
+    remaining prefix pages are added; the result is sorted ascending and the
+    pages holding window tokens beyond the prefix pages are appended.
+    """
+    n_pages = -(-L // P)
+    cand = n_pages - n_recent
+    top = rank(U[:cand])[:k]
+    keep = np.sort(np.concatenate([top, np.arange(cand, n_pages)]))
+    wpages = np.arange(n_pages, -(-(L + W) // P))
+    return np.concatenate([keep, wpages]).astype(np.int64)
+
+
+def gather_rows(x: np.ndarray, idx: np.ndarray, page_size: int = 1) -> np.ndarray:
+    """Rows of x [N, d] at idx (token mode) or the P rows of each page (page mode); rows past N are 0."""
+    if page_size == 1:
+        return x[idx]
+    rows = (idx[:, None] * page_size + np.arange(page_size)[None, :]).reshape(-1)
+    out = np.zeros((rows.size,) + x.shape[1:], dtype=x.dtype)
+    ok = rows < x.shape[0]
+    out[ok] = x[rows[ok]]
+    return out
+
+
+# --------------------------------------------------------------------------- block union
+
+def block_union(mask: np.ndarray, h_kv: int, n_kv: int):
+    """Per-group KV block list of one (sequence, layer).
+
+    mask: [H_q, n_qblk, >= n_kv] of 0/1.  Q-block union Mbar[h, j] = OR_i M[h, i, j];
+    intra-group union G[g, j] = OR over h in group g of Mbar[h, j]; T_g = { j : G[g, j] = 1 }.
+    Returns a list of h_kv ascending int arrays.
+    """
+    H = mask.shape[0]
+    Gsz = H // h_kv
+    out = []
+    for g in range(h_kv):
+        hit = np.zeros(n_kv, dtype=bool)
+        for h in range(g * Gsz, (g + 1) * Gsz):
+            for i in range(mask.shape[1]):
+                hit |= mask[h, i, :n_kv] != 0
+        out.append(np.nonzero(hit)[0].astype(np.int64))
+    return out
+
+
+def block_union_csr(mask: np.ndarray, h_kv: int, n_kv: list):
+    """CSR over rows (b, layer, g): kv_indptr [B*layers*h_kv + 1], kv_indices.  mask: [B, layers, H_q, n_qblk, nmax]."""
+    lists = []
+    for b in range(mask.shape[0]):
+        for layer in range(mask.shape[1]):
+            lists.extend(block_union(mask[b, layer], h_kv, n_kv[b]))
+    indptr = np.zeros(len(lists) + 1, dtype=np.int64)
+    indptr[1:] = np.cumsum([len(x) for x in lists])
+    indices = np.concatenate(lists) if lists else np.zeros(0, dtype=np.int64)
+    return indptr, indices
+
+
+# --------------------------------------------------------------------------- whole workload
+
+def score_unit(q_layer, k_layer, g: int, G: int, L: int, mode: str) -> np.ndarray:
+    """Raw group scores of (layer, KV head g): q_layer [H_q, W, d], k_layer [H_kv, L+W, d] (any dtype)."""
+    qg = _f64(q_layer[g * G:(g + 1) * G])
+    kh = _f64(k_layer[g])
+    return group_scores(qg, kh, L, mode)
+
+
+def run_sequence(w, q, k, v=None, with_gather: bool = True, layers=None):
+    """Every output of the path for one sequence of workload ``w`` (an object with the
+    Workload fields).  q [n_layers, H_q, W, d], k/v [n_layers, H_kv, L+W, d].
+
+    Returns a dict: 'raw' [n_layers, H_kv, L] group scores, 'pooled' (per layer
+    or, with a layer range, [H_kv, L] after the cross-layer mean), 'pages'
+    [.., n_pages] in page mode, 'idx' selected positions (or pages), and, with
+    ``with_gather``, 'k_c' / 'v_c' compacted rows.
+    """
+    L = int(k.shape[2]) - w.window
+    W, G, Hkv = w.window, w.h_q // w.h_kv, w.h_kv
+    layers = range(w.n_layers) if layers is None else layers
+    raw = np.stack([np.stack([score_unit(q[l], k[l], g, G, L, w.group_reduce) for g in range(Hkv)])
+                    for l in layers])
+    out = {"raw": raw}
+    if w.layer_range is not None:
+        lo, hi = w.layer_range
+        s = cross_layer_mean(raw, lo, hi)                       # [H_kv, L]
+        u = max_pool(s, w.pool_k)
+        idx = np.stack([select_tokens(u[g], w.k_keep, L, W) for g in range(Hkv)])
+        out.update(combined=s, pooled=u, idx=idx)
+    else:
+        u = max_pool(raw, w.pool_k)                              # [layers, H_kv, L]
+        out["pooled"] = u
+        if w.page_size == 1:
+            idx = np.stack([np.stack([select_tokens(u[i, g], w.k_keep, L, W) for g in range(Hkv)])
+                            for i in range(u.shape[0])])
+        else:
+            U = page_reduce(u, w.page_size, w.page_reduce)
+            out["pages"] = U
+            idx = np.stack([np.stack([select_pages(U[i, g], w.k_keep, w.n_recent, L, W, w.page_size)
+                                      for g in range(Hkv)]) for i in range(u.shape[0])])
+        out["idx"] = idx
+    if with_gather and v is not None:
+        P = w.page_size
+        kc, vc = [], []
+        for i, l in enumerate(layers):
+            kl, vl = [], []
+            for g in range(Hkv):
+                ii = out["idx"][g] if w.layer_range is not None else out["idx"][i, g]
+                kl.append(gather_rows(_f64(k[l, g]), ii, P))
+                vl.append(gather_rows(_f64(v[l, g]), ii, P))
+            kc.append(np.stack(kl)); vc.append(np.stack(vl))
+        out["k_c"] = np.stack(kc)
+        out["v_c"] = np.stack(vc)
+    return out

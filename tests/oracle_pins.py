@@ -1,0 +1,304 @@
+"""Pins for the fp64 oracle: checks against facts fixed outside the oracle itself.
+
+Each ``check_*`` takes the oracle module (or a mutated copy of it) and raises
+AssertionError when the oracle disagrees with:
+
+* an independent library routine computing the same quantity
+  (torch's scaled_dot_product_attention with identity values returns the
+  masked softmax probabilities, and its ``enable_gqa`` fixes the query-head
+  to KV-head map; scipy's softmax for the one-row case);
+* closed forms (identical keys; a hand-worked 4-key example);
+* invariants (softmax rows sum to one, so each head's column mass over all
+  visible columns is exactly W; L1-normalised scores sum to one);
+* brute force on tiny inputs (subset enumeration for top-k with ties, loop
+  definitions of pooling, page reduction and the block unions).
+
+``tests/test_oracle_pins.py`` runs them on the oracle; ``tests/test_oracle_mutants.py``
+plants plausible mistakes in copies of the oracle and checks that some pin fails.
+"""
+
+from __future__ import annotations
+
+import itertools
+import math
+
+import numpy as np
+import torch
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _bf16_values(a: np.ndarray) -> np.ndarray:
+    """Round float64 values to bf16 and back, so inputs look like the workloads'."""
+    return torch.from_numpy(a).to(torch.bfloat16).double().numpy()
+
+
+# --------------------------------------------------------------------------- scoring pins
+
+def check_probs_match_sdpa(o):
+    """Group scores and probabilities equal torch SDPA's attention weights (identity values, GQA map)."""
+    rng = _rng(1)
+    Hq, Hkv, W, L, d = 6, 2, 5, 13, 8
+    G = Hq // Hkv
+    q = _bf16_values(rng.standard_normal((Hq, W, d)) * 1.7)
+    k = _bf16_values(rng.standard_normal((Hkv, L + W, d)) * 1.3)
+    N = L + W
+    # attention weights = SDPA(q, k, V = I): output row r is the probability row of query r
+    vis = torch.zeros((W, N), dtype=torch.bool)
+    for j in range(W):
+        vis[j, : L + j + 1] = True            # window row j at position L + j sees keys 0 .. L + j
+    eye = torch.eye(N, dtype=torch.float64).expand(Hkv, N, N)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[None], torch.from_numpy(k)[None], eye[None],
+        attn_mask=vis, enable_gqa=True)[0].numpy()           # [Hq, W, N]
+    for mode in ("sum", "max"):
+        for g in range(Hkv):
+            s = o.score_unit(q, k, g, G, L, mode)
+            heads = ref[g * G:(g + 1) * G, :, :L].sum(axis=1)     # column mass per head
+            want = heads.sum(axis=0) if mode == "sum" else heads.max(axis=0)
+            np.testing.assert_allclose(s, want, rtol=1e-12, atol=1e-15)
+    for g in range(Hkv):
+        p = o.window_probs(q[g * G:(g + 1) * G], k[g], L)
+        np.testing.assert_allclose(p, ref[g * G:(g + 1) * G], rtol=1e-12, atol=1e-15)
+
+
+def check_row_mass_invariant(o):
+    """Each softmax row sums to one, so a head's mass over all visible columns is W, and the prefix part is below it."""
+    rng = _rng(2)
+    G, W, L, d = 3, 7, 40, 16
+    q = rng.standard_normal((G, W, d)) * 2.0
+    k = rng.standard_normal((L + W, d))
+    p = o.window_probs(q, k, L)
+    np.testing.assert_allclose(p.sum(axis=-1), 1.0, rtol=0, atol=1e-12)
+    assert np.all(p[:, np.arange(W)[:, None] < np.arange(L + W)[None, :] - L] == 0.0)
+    c = o.column_mass(p, L)
+    assert c.shape == (G, L)
+    total = c.sum(axis=1) + p[:, :, L:].sum(axis=(1, 2))
+    np.testing.assert_allclose(total, W, rtol=0, atol=1e-10)
+    s = o.group_reduce(c, "sum")
+    assert s.sum() <= G * W + 1e-9
+
+
+def check_identical_keys_closed_form(o):
+    """All keys equal: row j has L + j + 1 equal logits, so c[h, t] = sum_j 1 / (L + j + 1) for every prefix t."""
+    rng = _rng(3)
+    G, W, L, d = 2, 6, 30, 8
+    q = rng.standard_normal((G, W, d))
+    k = np.tile(rng.standard_normal((1, d)), (L + W, 1))
+    want = sum(1.0 / (L + j + 1) for j in range(W))
+    for mode, factor in (("sum", G), ("max", 1)):
+        s = o.group_scores(q, k, L, mode)
+        np.testing.assert_allclose(s, factor * want, rtol=1e-12)
+    u = o.max_pool(o.group_scores(q, k, L, "sum"), 7)
+    np.testing.assert_allclose(u, G * want, rtol=1e-12)
+    # ties everywhere: the first k positions win, then the window follows
+    idx = o.select_tokens(u, 5, L, W)
+    assert list(idx) == list(range(5)) + list(range(L, L + W))
+
+
+def check_hand_worked_example(o):
+    """d = 4 (scale 1/2), L = 2, W = 2, one head.
+
+    q_0 = (2 ln 2, 0, 0, 0), q_1 = 0; k_0 = (1, 0, 0, 0), k_1 = k_2 = k_3 = 0.
+    Row 0 sees keys 0..2 with logits (ln 2, 0, 0): p = (2, 1, 1) / 4.
+    Row 1 sees keys 0..3, all logits 0: p = 1/4 each.
+    Column mass over the prefix: c_0 = 1/2 + 1/4 = 3/4, c_1 = 1/4 + 1/4 = 1/2.
+    """
+    q = np.zeros((1, 2, 4)); q[0, 0, 0] = 2.0 * math.log(2.0)
+    k = np.zeros((4, 4)); k[0, 0] = 1.0
+    p = o.window_probs(q, k, 2)
+    np.testing.assert_allclose(p[0, 0], [0.5, 0.25, 0.25, 0.0], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(p[0, 1], [0.25] * 4, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(o.group_scores(q, k, 2, "sum"), [0.75, 0.5], rtol=0, atol=1e-15)
+
+
+def check_one_row_textbook(o):
+    """W = 1, G = 1, no pooling: the scores are one softmax row over L + 1 keys (scipy), first L entries."""
+    from scipy.special import softmax
+    rng = _rng(4)
+    L, d = 25, 12
+    q = rng.standard_normal((1, 1, d)) * 3.0
+    k = rng.standard_normal((L + 1, d))
+    z = np.array([sum(q[0, 0, c] * k[t, c] for c in range(d)) / math.sqrt(d) for t in range(L + 1)])
+    want = softmax(z)[:L]
+    np.testing.assert_allclose(o.group_scores(q, k, L, "sum"), want, rtol=1e-12)
+    np.testing.assert_allclose(o.group_scores(q, k, L, "max"), want, rtol=1e-12)
+
+
+def check_planted_key_first(o):
+    """A prefix key 8 sqrt(d) along the mean window-query direction ranks first and is always selected."""
+    rng = _rng(5)
+    G, W, L, d = 4, 8, 200, 32
+    q = rng.standard_normal((G, W, d))
+    k = rng.standard_normal((L + W, d))
+    u = q.reshape(-1, d).mean(axis=0)
+    u /= np.linalg.norm(u)
+    for pos in (0, 77, L - 1):
+        kk = k.copy()
+        kk[pos] = 8.0 * math.sqrt(d) * u
+        for mode in ("sum", "max"):
+            s = o.group_scores(q, kk, L, mode)
+            assert int(np.argmax(s)) == pos
+            assert o.rank(s)[0] == pos
+            idx = o.select_tokens(o.max_pool(s, 1), 1, L, W)
+            assert idx[0] == pos
+
+
+# --------------------------------------------------------------------------- pooling / pages
+
+def _pool_loop(s, k):
+    r = (k - 1) // 2
+    n = len(s)
+    return np.array([max(s[max(0, t - r):min(n, t + r + 1)]) for t in range(n)])
+
+
+def check_pool_definition(o):
+    """Max-pool equals its loop definition; a single spike widens to exactly 2r + 1 positions (clipped at the ends)."""
+    rng = _rng(6)
+    for n in (1, 2, 3, 7, 8, 50):
+        s = rng.random(n)
+        for kk in (1, 3, 7, 9):
+            np.testing.assert_array_equal(o.max_pool(s, kk), _pool_loop(s, kk))
+    for pos in (0, 2, 10, 19):
+        s = np.zeros(20); s[pos] = 1.0
+        u = o.max_pool(s, 7)
+        assert list(np.nonzero(u)[0]) == list(range(max(0, pos - 3), min(20, pos + 4)))
+    s = rng.random((3, 4, 33))
+    np.testing.assert_array_equal(o.max_pool(s, 7)[1, 2], _pool_loop(s[1, 2], 7))
+
+
+def check_page_reduce_definition(o):
+    """Page max / sum over P consecutive tokens, the last page partial."""
+    rng = _rng(7)
+    for n in (16, 17, 31, 48, 5):
+        u = rng.random(n)
+        P = 16
+        n_pages = -(-n // P)
+        want_max = [max(u[p * P:min(n, (p + 1) * P)]) for p in range(n_pages)]
+        want_sum = [sum(u[p * P:min(n, (p + 1) * P)]) for p in range(n_pages)]
+        np.testing.assert_array_equal(o.page_reduce(u, P, "max"), want_max)
+        np.testing.assert_allclose(o.page_reduce(u, P, "sum"), want_sum, rtol=1e-15)
+
+
+# --------------------------------------------------------------------------- selection
+
+def _brute_topk(scores, k):
+    """Best k-subset: max score sum, then the lexicographically smallest ascending index tuple."""
+    best = None
+    for sub in itertools.combinations(range(len(scores)), k):
+        key = (-sum(scores[list(sub)]), sub)
+        if best is None or key < best:
+            best = key
+    return list(best[1])
+
+
+def check_topk_brute_force(o):
+    """Sort-based top-k with ties to the lower index equals subset enumeration (exact sums on 1/8 levels)."""
+    rng = _rng(8)
+    for trial in range(40):
+        n = int(rng.integers(1, 12))
+        s = rng.integers(0, 4, n) * 0.125
+        for k in range(1, min(n, 4) + 1):
+            got = list(o.select_tokens(s, k, n, 0))
+            assert got == _brute_topk(s, k), (s, k, got)
+    # the window is appended after the ascending selection
+    s = np.array([0.0, 3.0, 1.0, 3.0, 2.0])
+    assert list(o.select_tokens(s, 2, 5, 3)) == [1, 3, 5, 6, 7]
+
+
+def check_page_selection_rule(o):
+    """Recency pages always kept, the top k of the other prefix pages by brute force, then window pages."""
+    rng = _rng(9)
+    P, W = 4, 8
+    for trial in range(30):
+        L = int(rng.integers(9, 40))
+        n_pages = -(-L // P)
+        n_recent = int(rng.integers(1, 3))
+        cand = n_pages - n_recent
+        k = int(rng.integers(1, min(cand, 3) + 1))
+        U = rng.integers(0, 3, n_pages) * 0.5
+        got = list(o.select_pages(U, k, n_recent, L, W, P))
+        top = _brute_topk(U[:cand], k)
+        want = sorted(top + list(range(cand, n_pages)))
+        wp = list(range(n_pages, -(-(L + W) // P)))
+        assert got == want + wp, (L, n_recent, k, U, got)
+        if L % P == 0:
+            assert len(got) == k + n_recent + W // P
+
+
+def check_gather(o):
+    rng = _rng(10)
+    x = rng.standard_normal((37, 5))
+    idx = np.array([0, 3, 36])
+    np.testing.assert_array_equal(o.gather_rows(x, idx), x[[0, 3, 36]])
+    pg = o.gather_rows(x, np.array([1, 9]), 4)
+    np.testing.assert_array_equal(pg[:4], x[4:8])
+    np.testing.assert_array_equal(pg[4], x[36])
+    np.testing.assert_array_equal(pg[5:], 0.0)
+
+
+# --------------------------------------------------------------------------- cross-layer
+
+def check_l1_cross_layer(o):
+    """L1-normalised rows sum to one; the layer mean sums to one; scaling one layer changes nothing."""
+    rng = _rng(11)
+    s = rng.random((6, 3, 50)) * rng.random((6, 3, 1)) * 10
+    S = o.cross_layer_mean(s, 1, 4)
+    np.testing.assert_allclose(S.sum(axis=-1), 1.0, rtol=1e-13)
+    s2 = s.copy(); s2[2] *= 37.0; s2[0] *= 5.0; s2[5] *= 0.01
+    np.testing.assert_allclose(o.cross_layer_mean(s2, 1, 4), S, rtol=1e-13)
+    # a layer outside the range does not matter; a layer inside it does
+    s3 = s.copy(); s3[5] = rng.random((3, 50))
+    np.testing.assert_allclose(o.cross_layer_mean(s3, 1, 4), S, rtol=1e-13)
+    s4 = s.copy(); s4[4] = rng.random((3, 50))
+    assert np.abs(o.cross_layer_mean(s4, 1, 4) - S).max() > 1e-6
+    # with identical normalised layers the mean is that layer
+    one = rng.random((1, 2, 9))
+    same = np.concatenate([one * c for c in (1.0, 2.0, 3.0)])
+    np.testing.assert_allclose(o.cross_layer_mean(same, 0, 2), one[0] / one[0].sum(-1, keepdims=True), rtol=1e-13)
+
+
+# --------------------------------------------------------------------------- block union
+
+def check_block_union(o):
+    """CSR equals the OR over (Q block, head in group) by array reduction; minimal and complete."""
+    rng = _rng(12)
+    B, Lyr, Hq, Hkv, nq, nmax = 3, 2, 8, 2, 5, 23
+    n_kv = [23, 9, 17]
+    M = (rng.random((B, Lyr, Hq, nq, nmax)) < 0.08).astype(np.uint8)
+    indptr, indices = o.block_union_csr(M, Hkv, n_kv)
+    G = Hq // Hkv
+    row = 0
+    for b in range(B):
+        for layer in range(Lyr):
+            for g in range(Hkv):
+                block = M[b, layer, g * G:(g + 1) * G, :, :n_kv[b]]
+                want = np.nonzero(block.any(axis=(0, 1)))[0]
+                got = indices[indptr[row]:indptr[row + 1]]
+                np.testing.assert_array_equal(got, want)
+                for j in got:           # minimal: every listed block was selected by some (h, i)
+                    assert block[:, :, j].any()
+                for h, i, j in zip(*np.nonzero(block)):   # complete: every selected block is listed
+                    assert j in got
+                assert np.all(np.diff(got) > 0)
+                row += 1
+    assert row == B * Lyr * Hkv and indptr[-1] == len(indices)
+
+
+ALL_CHECKS = [
+    check_probs_match_sdpa,
+    check_row_mass_invariant,
+    check_identical_keys_closed_form,
+    check_hand_worked_example,
+    check_one_row_textbook,
+    check_planted_key_first,
+    check_pool_definition,
+    check_page_reduce_definition,
+    check_topk_brute_force,
+    check_page_selection_rule,
+    check_gather,
+    check_l1_cross_layer,
+    check_block_union,
+]

@@ -1,0 +1,162 @@
+"""Plant plausible mistakes in fresh copies of the oracle: every one must fail some pin.
+
+This shows the pins are strong enough that a dropped term, a wrong sign or
+index, or a swapped operand anywhere in the oracle would be caught.
+"""
+
+import importlib.util
+import os
+
+import numpy as np
+import pytest
+
+from tests import oracle_pins as pins
+
+ORACLE_PATH = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                           "oracle", "kvsel_oracle.py")
+
+
+def fresh_oracle():
+    spec = importlib.util.spec_from_file_location("kvsel_oracle_mutant", ORACLE_PATH)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def _no_scale(o):
+    o.window_logits = lambda q, k: q @ k.T
+
+
+def _mask_off_by_one(o):
+    def window_mask(L, W):
+        return np.arange(L + W)[None, :] < L + np.arange(W)[:, None]
+    o.window_mask = window_mask
+
+
+def _prefix_only_softmax(o):
+    def window_mask(L, W):
+        return np.broadcast_to(np.arange(L + W)[None, :] < L, (W, L + W))
+    o.window_mask = window_mask
+
+
+def _mass_max_over_rows(o):
+    o.column_mass = lambda p, L: p[:, :, :L].max(axis=1)
+
+
+def _mass_includes_window_shift(o):
+    o.column_mass = lambda p, L: p[:, :, 1:L + 1].sum(axis=1)
+
+
+def _wrong_group_map(o):
+    orig = o.group_scores
+
+    def score_unit(q_layer, k_layer, g, G, L, mode):
+        Hkv = q_layer.shape[0] // G
+        return orig(o._f64(q_layer[g::Hkv]), o._f64(k_layer[g]), L, mode)
+    o.score_unit = score_unit
+
+
+def _reduce_swapped(o):
+    orig = o.group_reduce
+    o.group_reduce = lambda c, mode: orig(c, "max" if mode == "sum" else "sum")
+
+
+def _transposed_rows(o):
+    """Window rows reversed against the mask (row j paired with the mask of row W-1-j)."""
+    orig = o.window_probs
+
+    def window_probs(q_group, k_head, L):
+        return orig(q_group[:, ::-1], k_head, L)
+    o.window_probs = window_probs
+
+
+def _pool_radius(o):
+    orig = o.max_pool
+    o.max_pool = lambda s, k: orig(s, k + 2) if k > 1 else orig(s, k)
+
+
+def _pool_one_sided(o):
+    def max_pool(s, k):
+        r = (k - 1) // 2
+        out = s.copy()
+        for off in range(1, r + 1):
+            if off < s.shape[-1]:
+                out[..., :-off] = np.maximum(out[..., :-off], s[..., off:])
+        return out
+    o.max_pool = max_pool
+
+
+def _page_sum_for_max(o):
+    orig = o.page_reduce
+    o.page_reduce = lambda u, P, mode="max": orig(u, P, "sum")
+
+
+def _tie_to_higher(o):
+    def rank(scores):
+        n = scores.shape[-1]
+        return np.lexsort((-np.arange(n), -scores))
+    o.rank = rank
+
+
+def _rank_ascending(o):
+    def rank(scores):
+        n = scores.shape[-1]
+        return np.lexsort((np.arange(n), scores))
+    o.rank = rank
+
+
+def _recency_off_by_one(o):
+    orig = o.select_pages
+    o.select_pages = lambda U, k, n_recent, L, W, P: orig(U, k, n_recent + 1, L, W, P)[1:]
+
+
+def _no_l1(o):
+    o.l1_normalise = lambda s: s
+
+
+def _layer_range_exclusive(o):
+    o.cross_layer_mean = lambda s, lo, hi: o.l1_normalise(s[lo:hi]).mean(axis=0)
+
+
+def _union_wrong_group(o):
+    def block_union(mask, h_kv, n_kv):
+        out = []
+        for g in range(h_kv):
+            hit = np.zeros(n_kv, dtype=bool)
+            for h in range(g, mask.shape[0], h_kv):
+                hit |= (mask[h, :, :n_kv] != 0).any(axis=0)
+            out.append(np.nonzero(hit)[0])
+        return out
+    o.block_union = block_union
+
+
+def _union_first_qblock_only(o):
+    def block_union(mask, h_kv, n_kv):
+        G = mask.shape[0] // h_kv
+        return [np.nonzero((mask[g * G:(g + 1) * G, 0, :n_kv] != 0).any(axis=0))[0] for g in range(h_kv)]
+    o.block_union = block_union
+
+
+def _gather_page_offset(o):
+    orig = o.gather_rows
+    o.gather_rows = lambda x, idx, page_size=1: orig(x, idx + (1 if page_size > 1 else 0), page_size)
+
+
+MUTANTS = [_no_scale, _mask_off_by_one, _prefix_only_softmax, _mass_max_over_rows,
+           _mass_includes_window_shift, _wrong_group_map, _reduce_swapped, _transposed_rows,
+           _pool_radius, _pool_one_sided, _page_sum_for_max, _tie_to_higher, _rank_ascending,
+           _recency_off_by_one, _no_l1, _layer_range_exclusive, _union_wrong_group,
+           _union_first_qblock_only, _gather_page_offset]
+
+
+@pytest.mark.parametrize("mutate", MUTANTS, ids=lambda m: m.__name__.strip("_"))
+def test_mutant_is_caught(mutate):
+    o = fresh_oracle()
+    mutate(o)
+    failed = []
+    for check in pins.ALL_CHECKS:
+        try:
+            check(o)
+        except Exception:          # an assertion, or a shape error the mistake causes
+            failed.append(check.__name__)
+    assert failed, f"no pin catches mutant {mutate.__name__}"
