@@ -1,0 +1,95 @@
+// Internal declarations shared by the translation units of libkvsel.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "kvsel.h"
+
+namespace kvsel {
+
+// Error word at the start of every workspace (device side).
+struct DeviceError {
+  uint32_t code;       // 0 = none, else a kvsel_status value
+  uint32_t where;      // kernel-specific detail (first failure wins)
+  uint32_t pad[62];
+};
+static_assert(sizeof(DeviceError) == 256, "error header is one 256-byte line");
+
+__device__ __forceinline__ void set_device_error(DeviceError* e, uint32_t code, uint32_t where) {
+  if (e == nullptr) return;
+  if (atomicCAS(&e->code, 0u, code) == 0u) atomicExch(&e->where, where);
+}
+
+// Per-sequence geometry of one call (lives in kernel parameters).
+struct SeqInfo {
+  int32_t L;            // prefix length L_b
+  int32_t n_keys;       // L_b + W
+  int64_t k_off;        // element offset of the sequence's K / V block
+  int64_t s_off;        // element offset of its token scores ([layers][h_kv][L_b])
+  int64_t p_off;        // element offset of its page scores ([layers][h_kv][ceil(L_b/P)])
+  int32_t item0;        // first work item of this sequence in the current launch
+  int32_t n_seg;        // segments per (layer, KV head) unit in the current launch
+  int64_t part_off;     // index of its first (unit, segment) partial record
+  int32_t unit0;        // global index of its first (layer, KV head) unit
+  int32_t aux;          // launch-specific (KV blocks for the page table)
+};
+
+struct SeqTable {
+  int32_t batch;
+  int32_t n_items;
+  SeqInfo s[KVSEL_MAX_BATCH];
+};
+
+__device__ __forceinline__ int find_seq(const SeqTable& t, int item) {
+  int b = 0;
+  while (b + 1 < t.batch && t.s[b + 1].item0 <= item) ++b;
+  return b;
+}
+
+// Problem description handed to every scoring kernel.
+struct ScoreShape {
+  int32_t n_layers, h_q, h_kv, d, W, G, R;   // R = G * W rows per unit
+  int32_t group_reduce, pool_k, page_size, page_reduce;
+  int32_t seg1, seg2;                        // keys per pass-1 / pass-2 segment
+  float scale_log2;                          // log2(e) / sqrt(d)
+};
+
+// ---- launch plumbing (kvsel_api.cu) ------------------------------------------------
+struct TraceScope {
+  TraceScope(const char* name, cudaStream_t s);
+  ~TraceScope();
+  const char* name;
+  cudaStream_t stream;
+  cudaEvent_t start;
+  bool on;
+};
+void count_launch();
+cudaError_t set_smem(const void* func, size_t bytes);
+
+inline kvsel_status launch_status() {
+  count_launch();
+  return cudaGetLastError() == cudaSuccess ? KVSEL_OK : KVSEL_ERR_CUDA;
+}
+
+// ---- kernel launchers ---------------------------------------------------------------
+kvsel_status launch_score(const ScoreShape& sh, const SeqTable& t1, const SeqTable& t2,
+                          const void* q, const void* k, float* scores, float* page_scores,
+                          float* lse, float2* part, DeviceError* err, cudaStream_t s);
+
+kvsel_status launch_topk(const kvsel_desc& desc, const SeqTable& t, int layers, int k, int n_recent,
+                         const float* scores, int32_t* idx, cudaStream_t s);
+
+kvsel_status launch_combine_layers(const kvsel_desc& desc, const SeqTable& t, const float* scores,
+                                   int lo, int hi, float* norms, float* combined, cudaStream_t s);
+
+kvsel_status launch_compact(const kvsel_desc& desc, const SeqTable& t, const void* k, const void* v,
+                            const int32_t* idx, int idx_layers, int n_sel, void* k_out, void* v_out,
+                            DeviceError* err, cudaStream_t s);
+
+kvsel_status launch_pagetable(const kvsel_desc& desc, const SeqTable& t, const uint8_t* mask,
+                              int n_qblk, int n_kvblk_max, int32_t* counts, int32_t* kv_indptr,
+                              int32_t* kv_indices, cudaStream_t s);
+
+}  // namespace kvsel

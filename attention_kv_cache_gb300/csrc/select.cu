@@ -1,0 +1,255 @@
+// Top-k selection with ties to the lower index, recency / window append, and the
+// cross-layer L1-normalised mean.
+//
+// Top-k: one CTA per (sequence, layer, KV head) row.  Scores map to order-
+// preserving uint32 keys; a 4-pass 8-bit radix select finds the k-th largest
+// key T and how many keys equal to T are taken (krem).  Then one ordered pass
+// emits every index with key > T and the first krem indices with key == T, in
+// ascending index order, which is exactly the first k of the ranking by
+// (score descending, index ascending) sorted back into position order
+// (DELTA, 'Key designs' 2; ClusterAttn, 'Method details').
+#include "internal.cuh"
+
+namespace kvsel {
+namespace {
+
+constexpr int kTopkThreads = 1024;
+constexpr int kSmemKeysMax = 40960;   // rows up to this length are staged in shared memory
+
+__device__ __forceinline__ uint32_t f2key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;                  // -0 ranks equal to +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Exclusive prefix sum over the block of a 64-bit value; *total gets the block sum.
+__device__ unsigned long long block_scan_u64(unsigned long long v, unsigned long long* sh32,
+                                             unsigned long long* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  unsigned long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh32[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    const int nw = blockDim.x >> 5;
+    unsigned long long w = lane < nw ? sh32[lane] : 0ull;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    sh32[lane] = w;
+  }
+  __syncthreads();
+  const unsigned long long before = (wid > 0 ? sh32[wid - 1] : 0ull) + x - v;
+  *total = sh32[(blockDim.x >> 5) - 1];
+  __syncthreads();
+  return before;
+}
+
+struct TopkArgs {
+  const float* scores;
+  int32_t* idx;
+  int32_t layers, h_kv, k, n_recent, P, W, n_sel;
+};
+
+template <bool SMEM>
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constant__ TopkArgs a,
+                                                            const __grid_constant__ SeqTable t) {
+  extern __shared__ __align__(16) uint32_t keys_sm[];
+  __shared__ uint32_t hist[256];
+  __shared__ unsigned long long scan_sh[32];
+  __shared__ uint32_t sel_digit, sel_gt;
+
+  const int row = blockIdx.x;
+  const int rows_per_seq = a.layers * a.h_kv;
+  const int b = row / rows_per_seq;
+  const int lg = row % rows_per_seq;
+  const SeqInfo& si = t.s[b];
+  const int n = a.P == 1 ? si.L : (si.L + a.P - 1) / a.P;
+  const int n_cand = n - a.n_recent;
+  const float* src = a.scores + (a.P == 1 ? si.s_off : si.p_off) + (int64_t)lg * n;
+  int32_t* out = a.idx + (int64_t)row * a.n_sel;
+  const int tid = threadIdx.x;
+
+  if (SMEM)
+    for (int i = tid; i < n_cand; i += kTopkThreads) keys_sm[i] = f2key(src[i]);
+  __syncthreads();
+  auto key_at = [&](int i) -> uint32_t { return SMEM ? keys_sm[i] : f2key(src[i]); };
+
+  uint32_t prefix = 0, pmask = 0;
+  uint32_t krem = (uint32_t)a.k;
+  if (a.k > 0) {
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      if (tid < 256) hist[tid] = 0;
+      __syncthreads();
+      for (int base = 0; base < n_cand; base += kTopkThreads) {
+        const int i = base + tid;
+        uint32_t key = 0;
+        bool ok = false;
+        if (i < n_cand) {
+          key = key_at(i);
+          ok = (key & pmask) == prefix;
+        }
+        const unsigned m = __ballot_sync(0xffffffffu, ok);
+        if (ok) {
+          const uint32_t digit = (key >> shift) & 255u;
+          const unsigned peers = __match_any_sync(m, digit);
+          if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(peers));
+        }
+      }
+      __syncthreads();
+      // digits from the top: count of candidates whose digit is above d
+      const uint32_t d = 255u - (uint32_t)tid;
+      const unsigned long long c = tid < 256 ? hist[d] : 0ull;
+      unsigned long long tot;
+      const unsigned long long above = block_scan_u64(c, scan_sh, &tot);
+      if (tid < 256 && above < krem && krem <= above + c) {
+        sel_digit = d;
+        sel_gt = (uint32_t)above;
+      }
+      __syncthreads();
+      prefix |= sel_digit << shift;
+      pmask |= 255u << shift;
+      krem -= sel_gt;
+      __syncthreads();
+    }
+    // ordered emission: every key > T, then the first krem keys == T
+    const uint32_t T = prefix;
+    const int chunk = (n_cand + kTopkThreads - 1) / kTopkThreads;
+    const int beg = min(n_cand, tid * chunk), end = min(n_cand, beg + chunk);
+    uint32_t gt = 0, eq = 0;
+    for (int i = beg; i < end; ++i) {
+      const uint32_t key = key_at(i);
+      gt += key > T;
+      eq += key == T;
+    }
+    unsigned long long tot;
+    const unsigned long long pre = block_scan_u64(((unsigned long long)gt << 32) | eq, scan_sh, &tot);
+    const uint32_t gt_before = (uint32_t)(pre >> 32), eq_before = (uint32_t)(pre & 0xffffffffu);
+    uint32_t pos = gt_before + min(eq_before, krem);
+    uint32_t eq_seen = eq_before;
+    for (int i = beg; i < end; ++i) {
+      const uint32_t key = key_at(i);
+      if (key > T) {
+        out[pos++] = i;
+      } else if (key == T) {
+        if (eq_seen < krem) out[pos++] = i;
+        ++eq_seen;
+      }
+    }
+  }
+  // recency pages and window pages (page mode) or window tokens (token mode) follow n_cand
+  for (int i = tid; i < a.n_sel - a.k; i += kTopkThreads) out[a.k + i] = n_cand + i;
+}
+
+// ------------------------------------------------------------------------ cross-layer mean
+constexpr int kCombThreads = 256;
+constexpr int kCombChunk = 1024;
+
+__global__ void __launch_bounds__(kCombThreads) layer_norms(const float* scores, float* norms,
+                                                            const __grid_constant__ SeqTable t, int n_layers,
+                                                            int h_kv) {
+  __shared__ float red[kCombThreads];
+  const int row = blockIdx.x;                       // (b, layer, g)
+  const int per_seq = n_layers * h_kv;
+  const int b = row / per_seq, lg = row % per_seq;
+  const SeqInfo& si = t.s[b];
+  const float* s = scores + si.s_off + (int64_t)lg * si.L;
+  float acc = 0.f;
+  for (int i = threadIdx.x; i < si.L; i += kCombThreads) acc += fabsf(s[i]);
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = kCombThreads / 2; w > 0; w >>= 1) {
+    if ((int)threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) norms[row] = red[0];
+}
+
+__global__ void __launch_bounds__(kCombThreads) layer_mean_pool(const float* scores, const float* norms,
+                                                                float* combined,
+                                                                const __grid_constant__ SeqTable t,
+                                                                int n_layers, int h_kv, int lo, int hi,
+                                                                int pool_k) {
+  __shared__ float S[kCombChunk + 64];
+  const int b = blockIdx.z, g = blockIdx.y;
+  const SeqInfo& si = t.s[b];
+  const int a0 = blockIdx.x * kCombChunk;
+  if (a0 >= si.L) return;
+  const int a1 = min(si.L, a0 + kCombChunk);
+  const int pr = (pool_k - 1) / 2;
+  const int ea = max(0, a0 - pr), eb = min(si.L, a1 + pr);
+  const float inv_n = 1.0f / (float)(hi - lo + 1);
+  for (int tt = ea + threadIdx.x; tt < eb; tt += kCombThreads) {
+    float acc = 0.f;
+    for (int layer = lo; layer <= hi; ++layer) {
+      const int64_t row = ((int64_t)b * n_layers + layer) * h_kv + g;
+      const float v = scores[si.s_off + ((int64_t)layer * h_kv + g) * si.L + tt];
+      acc += v / norms[row];
+    }
+    S[tt - ea] = acc * inv_n;
+  }
+  __syncthreads();
+  float* out = combined + si.s_off / n_layers + (int64_t)g * si.L;
+  for (int tt = a0 + threadIdx.x; tt < a1; tt += kCombThreads) {
+    const int l0 = max(tt - pr, ea), l1 = min(tt + pr, eb - 1);
+    float u = S[l0 - ea];
+    for (int x = l0 + 1; x <= l1; ++x) u = fmaxf(u, S[x - ea]);
+    out[tt] = u;
+  }
+}
+
+}  // namespace
+
+kvsel_status launch_topk(const kvsel_desc& d, const SeqTable& t, int layers, int k, int n_recent,
+                         const float* scores, int32_t* idx, cudaStream_t s) {
+  TopkArgs a;
+  a.scores = scores;
+  a.idx = idx;
+  a.layers = layers;
+  a.h_kv = d.h_kv;
+  a.k = k;
+  a.n_recent = n_recent;
+  a.P = d.page_size;
+  a.W = d.window;
+  a.n_sel = d.page_size == 1 ? k + d.window : k + n_recent + d.window / d.page_size;
+  int64_t nmax = 0;
+  for (int b = 0; b < d.batch; ++b) {
+    const int64_t n = d.page_size == 1 ? d.prefix_lens[b] : (d.prefix_lens[b] + d.page_size - 1) / d.page_size;
+    nmax = n > nmax ? n : nmax;
+  }
+  const int rows = d.batch * layers * d.h_kv;
+  TraceScope ts("topk_radix", s);
+  if (nmax <= kSmemKeysMax) {
+    const size_t smem = (size_t)nmax * sizeof(uint32_t);
+    if (set_smem((const void*)topk_kernel<true>, smem) != cudaSuccess) return KVSEL_ERR_CUDA;
+    topk_kernel<true><<<rows, kTopkThreads, smem, s>>>(a, t);
+  } else {
+    topk_kernel<false><<<rows, kTopkThreads, 0, s>>>(a, t);
+  }
+  return launch_status();
+}
+
+kvsel_status launch_combine_layers(const kvsel_desc& d, const SeqTable& t, const float* scores, int lo, int hi,
+                                   float* norms, float* combined, cudaStream_t s) {
+  kvsel_status st;
+  {
+    TraceScope ts("layer_norms", s);
+    layer_norms<<<d.batch * d.n_layers * d.h_kv, kCombThreads, 0, s>>>(scores, norms, t, d.n_layers, d.h_kv);
+    if ((st = launch_status()) != KVSEL_OK) return st;
+  }
+  int64_t lmax = 0;
+  for (int b = 0; b < d.batch; ++b) lmax = d.prefix_lens[b] > lmax ? d.prefix_lens[b] : lmax;
+  dim3 grid((unsigned)((lmax + kCombChunk - 1) / kCombChunk), d.h_kv, d.batch);
+  TraceScope ts("layer_mean_pool", s);
+  layer_mean_pool<<<grid, kCombThreads, 0, s>>>(scores, norms, combined, t, d.n_layers, d.h_kv, lo, hi, d.pool_k);
+  return launch_status();
+}
+
+}  // namespace kvsel

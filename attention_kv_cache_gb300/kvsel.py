@@ -1,0 +1,183 @@
+"""Thin ctypes binding of libkvsel.so (include/kvsel.h).
+
+Argument marshalling only: every computation runs in the library's CUDA
+kernels.  Functions keep the C names; tensors are passed by ``data_ptr()`` and
+the stream is torch's current CUDA stream unless one is given.  A non-OK
+status raises ``KvselError``.  If the library has not been built, importing
+this module raises: there is no other implementation to fall back to.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "_build", "libkvsel.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = range(7)
+REDUCE_SUM, REDUCE_MAX = 0, 1
+MAX_BATCH, MAX_WINDOW, MAX_ROWS, MAX_PAGE, WS_ALIGN = 128, 64, 256, 256, 256
+
+
+class KvselError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+class Desc(ctypes.Structure):
+    _fields_ = [
+        ("n_layers", ctypes.c_int32),
+        ("h_q", ctypes.c_int32),
+        ("h_kv", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("window", ctypes.c_int32),
+        ("batch", ctypes.c_int32),
+        ("prefix_lens", ctypes.POINTER(ctypes.c_int64)),
+        ("group_reduce", ctypes.c_int32),
+        ("pool_k", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("page_reduce", ctypes.c_int32),
+    ]
+
+
+class TraceEntry(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int64), ("ms", ctypes.c_double)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with attention_kv_cache_gb300.build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, I64, SZ, VP = ctypes.POINTER, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p
+    D = P(Desc)
+    sig = {
+        "kvsel_workspace_size": (I32, [D, P(SZ)]),
+        "kvsel_score": (I32, [D, VP, VP, VP, VP, VP, SZ, VP]),
+        "kvsel_combine_layers": (I32, [D, VP, I32, I32, VP, VP, SZ, VP]),
+        "kvsel_topk": (I32, [D, VP, I32, I32, I32, VP, VP, SZ, VP]),
+        "kvsel_compact": (I32, [D, VP, VP, VP, I32, I32, VP, VP, VP, VP]),
+        "kvsel_pagetable": (I32, [D, VP, I32, I32, P(I32), VP, VP, VP, SZ, VP]),
+        "kvsel_read_device_error": (I32, [VP, VP]),
+        "kvsel_status_string": (ctypes.c_char_p, [I32]),
+        "kvsel_version": (ctypes.c_char_p, []),
+        "kvsel_trace_enable": (None, [I32]),
+        "kvsel_trace_read": (I32, [P(TraceEntry), I32, P(I32)]),
+        "kvsel_launch_count": (I64, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+_lib = _load()
+EXPORTED = ("kvsel_workspace_size", "kvsel_score", "kvsel_combine_layers", "kvsel_topk", "kvsel_compact",
+            "kvsel_pagetable", "kvsel_read_device_error", "kvsel_status_string", "kvsel_version",
+            "kvsel_trace_enable", "kvsel_trace_read", "kvsel_launch_count")
+
+
+def status_string(status: int) -> str:
+    return _lib.kvsel_status_string(status).decode()
+
+
+def version() -> str:
+    return _lib.kvsel_version().decode()
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise KvselError(status, what)
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def make_desc(*, n_layers: int, h_q: int, h_kv: int, head_dim: int, window: int,
+              prefix_lens: Sequence[int], group_reduce: int = REDUCE_SUM, pool_k: int = 7,
+              page_size: int = 1, page_reduce: int = REDUCE_MAX) -> Desc:
+    """A descriptor; it keeps its own host copy of prefix_lens alive."""
+    lens = (ctypes.c_int64 * len(prefix_lens))(*[int(x) for x in prefix_lens])
+    d = Desc(n_layers, h_q, h_kv, head_dim, window, len(prefix_lens), lens, group_reduce, pool_k,
+             page_size, page_reduce)
+    d._lens = lens
+    return d
+
+
+def kvsel_workspace_size(desc: Desc) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.kvsel_workspace_size(ctypes.byref(desc), ctypes.byref(n)), "kvsel_workspace_size")
+    return n.value
+
+
+def kvsel_score(desc, q, k, scores, page_scores, ws, ws_bytes: Optional[int] = None, stream=None):
+    nb = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    _check(_lib.kvsel_score(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(scores), _ptr(page_scores), _ptr(ws),
+                            nb, _stream(stream)), "kvsel_score")
+
+
+def kvsel_combine_layers(desc, scores, layer_lo: int, layer_hi: int, combined, ws, ws_bytes=None, stream=None):
+    nb = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    _check(_lib.kvsel_combine_layers(ctypes.byref(desc), _ptr(scores), layer_lo, layer_hi, _ptr(combined),
+                                     _ptr(ws), nb, _stream(stream)), "kvsel_combine_layers")
+
+
+def kvsel_topk(desc, scores, layers: int, k: int, n_recent: int, idx_out, ws, ws_bytes=None, stream=None):
+    nb = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    _check(_lib.kvsel_topk(ctypes.byref(desc), _ptr(scores), layers, k, n_recent, _ptr(idx_out), _ptr(ws), nb,
+                           _stream(stream)), "kvsel_topk")
+
+
+def kvsel_compact(desc, k, v, idx, idx_layers: int, n_sel: int, k_out, v_out, ws=None, stream=None):
+    _check(_lib.kvsel_compact(ctypes.byref(desc), _ptr(k), _ptr(v), _ptr(idx), idx_layers, n_sel, _ptr(k_out),
+                              _ptr(v_out), _ptr(ws), _stream(stream)), "kvsel_compact")
+
+
+def kvsel_pagetable(desc, mask, n_qblk: int, n_kvblk_max: int, n_kvblk: Sequence[int], kv_indptr, kv_indices,
+                    ws, ws_bytes=None, stream=None):
+    nb = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    nk = (ctypes.c_int32 * len(n_kvblk))(*[int(x) for x in n_kvblk])
+    _check(_lib.kvsel_pagetable(ctypes.byref(desc), _ptr(mask), n_qblk, n_kvblk_max, nk, _ptr(kv_indptr),
+                                _ptr(kv_indices), _ptr(ws), nb, _stream(stream)), "kvsel_pagetable")
+
+
+def kvsel_read_device_error(ws, stream=None) -> int:
+    """Status recorded by the device in the workspace's error word (clears it)."""
+    return _lib.kvsel_read_device_error(_ptr(ws), _stream(stream))
+
+
+def kvsel_trace_enable(on: bool):
+    _lib.kvsel_trace_enable(1 if on else 0)
+
+
+def kvsel_trace_read() -> dict:
+    n = ctypes.c_int32(0)
+    buf = (TraceEntry * 64)()
+    _check(_lib.kvsel_trace_read(buf, 64, ctypes.byref(n)), "kvsel_trace_read")
+    return {buf[i].name.decode(): (buf[i].launches, buf[i].ms) for i in range(min(n.value, 64))}
+
+
+def kvsel_launch_count() -> int:
+    return _lib.kvsel_launch_count()
+
+
+def raw_call(name: str, *args) -> int:
+    """The C function itself (status returned, nothing raised), for argument-check tests."""
+    return getattr(_lib, name)(*args)

@@ -1,0 +1,210 @@
+/*
+ * kvsel — window-attention prompt-token scoring and top-k KV selection on one GPU.
+ *
+ * C ABI of libkvsel.so.  Every pointer argument is caller-owned; device
+ * pointers are marked [device], host pointers [host].  No call allocates or
+ * frees device memory and no call synchronises a stream except
+ * kvsel_read_device_error() and kvsel_trace_read().  Calls are asynchronous
+ * on the stream passed in; the library keeps no per-call state, so calls with
+ * distinct workspaces may run concurrently from several host threads.
+ *
+ * Arguments are checked on the host before any launch; a rejected call
+ * returns a status and launches nothing.  A launch failure returns
+ * KVSEL_ERR_CUDA.  Errors that only the device can see (a bounded wait that
+ * ran out, an index out of range) are recorded in an error word at the start
+ * of the workspace and read back with kvsel_read_device_error().
+ *
+ * Layouts (bf16 = IEEE bfloat16 bit pattern in uint16 storage, row-major,
+ * sequences of a batch packed one after another in batch order):
+ *   q            [batch][n_layers][h_q][W][d]                     bf16
+ *   k, v         per sequence b: [n_layers][h_kv][L_b + W][d]     bf16
+ *   scores       per sequence b: [n_layers][h_kv][L_b]            fp32
+ *   page_scores  per sequence b: [n_layers][h_kv][ceil(L_b / P)]  fp32
+ * Key row t of sequence b is absolute prompt position t: rows 0..L_b-1 are
+ * the prefix, rows L_b..L_b+W-1 the observation window whose queries are q.
+ * Query head h reads KV head g = h / (h_q / h_kv).
+ */
+#ifndef KVSEL_H
+#define KVSEL_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define KVSEL_API __attribute__((visibility("default")))
+#else
+#define KVSEL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KVSEL_OK = 0,
+  KVSEL_ERR_INVALID_ARG = 1,   /* null pointer, bad size, inconsistent shape */
+  KVSEL_ERR_UNSUPPORTED = 2,   /* valid request outside what the kernels implement */
+  KVSEL_ERR_WORKSPACE = 3,     /* workspace null, misaligned or smaller than kvsel_workspace_size() */
+  KVSEL_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
+  KVSEL_ERR_TIMEOUT = 5,       /* a bounded device-side wait gave up */
+  KVSEL_ERR_DEVICE = 6         /* the device found an index out of range */
+} kvsel_status;
+
+enum { KVSEL_REDUCE_SUM = 0, KVSEL_REDUCE_MAX = 1 };
+
+#define KVSEL_MAX_BATCH 128
+#define KVSEL_MAX_WINDOW 64
+#define KVSEL_MAX_ROWS 256          /* (h_q / h_kv) * window */
+#define KVSEL_MAX_PAGE 256
+#define KVSEL_WS_ALIGN 256          /* required workspace alignment in bytes */
+
+/* Shape and reduction modes shared by every call. */
+typedef struct {
+  int32_t n_layers;            /* >= 1 */
+  int32_t h_q;                 /* query heads, multiple of h_kv */
+  int32_t h_kv;                /* KV heads >= 1 */
+  int32_t head_dim;            /* d: 64 or 128 */
+  int32_t window;              /* W: 1 .. KVSEL_MAX_WINDOW; (h_q / h_kv) * W <= KVSEL_MAX_ROWS */
+  int32_t batch;               /* sequences: 1 .. KVSEL_MAX_BATCH */
+  const int64_t* prefix_lens;  /* [host] [batch] prefix lengths L_b >= 1, L_b + W < 2^31 */
+  int32_t group_reduce;        /* KVSEL_REDUCE_SUM or KVSEL_REDUCE_MAX over the query heads of a group */
+  int32_t pool_k;              /* odd max-pool width, 1 (none) .. 63 */
+  int32_t page_size;           /* P: 1 = token mode, 2 .. KVSEL_MAX_PAGE = page mode */
+  int32_t page_reduce;         /* KVSEL_REDUCE_MAX or KVSEL_REDUCE_SUM over the tokens of a page */
+} kvsel_desc;
+
+/* Bytes of device workspace the calls below need for this descriptor (any of them). */
+KVSEL_API kvsel_status kvsel_workspace_size(const kvsel_desc* desc, size_t* bytes);
+
+/*
+ * kvsel_score — window-query attention scores of every prefix token.
+ *
+ * ClusterAttn: KV Cache Compression under Intrinsic Attention Clustering,
+ * 'Background and key observations', feature aggregation: the W window
+ * queries attend to all prompt keys through a causal mask inside the window
+ * (row j sees prefix keys and window keys 0..j), QK^T / sqrt(d), softmax over
+ * the full row, then the post-softmax mass is summed over the window rows for
+ * each prefix column.  The per-head column mass is reduced over the query
+ * heads of each GQA group (sum as in CLAA's FastKV-style window scoring,
+ * max as in DELTA's head-aware scoring), max-pooled with width pool_k over
+ * prefix positions (CLAA, 'Oracle construction': 1-D pooling, kernel 7), and,
+ * in page mode, reduced to page scores over P consecutive tokens (DELTA,
+ * 'Key designs' 2 and 3).
+ *
+ *   q, k         [device] bf16, layouts above; 16-byte aligned
+ *   scores       [device] fp32 out: pooled token scores (raw group scores when pool_k == 1)
+ *   page_scores  [device] fp32 out in page mode (may be NULL in token mode)
+ *   ws           [device] workspace of ws_bytes >= kvsel_workspace_size(), KVSEL_WS_ALIGN aligned
+ */
+KVSEL_API kvsel_status kvsel_score(const kvsel_desc* desc, const void* q, const void* k,
+                         float* scores, float* page_scores,
+                         void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * kvsel_combine_layers — cross-layer aggregation of raw group scores.
+ *
+ * Each layer's scores of a (sequence, KV head) row are L1-normalised over the
+ * prefix (LookaheadKV, 'KL divergence and ListNet': s / ||s||_1), the mean is
+ * taken over layers layer_lo..layer_hi inclusive (CLAA, decision 3: one score
+ * per token aggregated over several layers), and the result is max-pooled
+ * with desc->pool_k.
+ *
+ *   scores    [device] fp32 raw group scores (kvsel_score with pool_k = 1), layout above
+ *   combined  [device] fp32 out, per sequence b: [h_kv][L_b]
+ *   ws        [device] workspace (holds the per-layer L1 norms)
+ */
+KVSEL_API kvsel_status kvsel_combine_layers(const kvsel_desc* desc, const float* scores,
+                                  int32_t layer_lo, int32_t layer_hi, float* combined,
+                                  void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * kvsel_topk — top-k selection per (sequence, layer, KV head) row, ties to the lower index.
+ *
+ * Token mode (desc->page_size == 1): the k prefix tokens of highest score,
+ * in ascending position, then the window positions L_b .. L_b+W-1 (ClusterAttn,
+ * 'Method details': the compressed prefix is joined with the window).
+ * Page mode: the last n_recent prefix pages are kept and the k highest-scoring
+ * of the other prefix pages are added (DELTA, 'Key designs' 2: recency pages
+ * union top pages of the rest), in ascending order, then the W / P pages of
+ * the window.  Page mode requires W % P == 0, and n_recent >= 1 when
+ * L_b % P != 0 (so the page shared by prefix and window is kept once).
+ *
+ *   scores   [device] fp32 per sequence b: [layers][h_kv][n] with n = L_b (token mode)
+ *            or ceil(L_b / P) (page mode); layers = desc->n_layers, or 1 for the
+ *            output of kvsel_combine_layers
+ *   idx_out  [device] int32 out [batch][layers][h_kv][n_sel], n_sel = k + W (token)
+ *            or k + n_recent + W / P (page): token positions or page numbers
+ */
+KVSEL_API kvsel_status kvsel_topk(const kvsel_desc* desc, const float* scores, int32_t layers,
+                        int32_t k, int32_t n_recent, int32_t* idx_out,
+                        void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * kvsel_compact — gather the kept K and V rows into a compacted cache.
+ *
+ * CLAA, 'Complete flow and cost': each layer's cache keeps only the K and V
+ * rows of the selected tokens; ClusterAttn, 'Method details', keeps the window
+ * rows with them.  Token mode copies row idx[r]; page mode copies the P rows
+ * of page idx[r] (rows past L_b + W are written as zero).  A bit copy:
+ * outputs equal inputs exactly.
+ *
+ *   k, v          [device] bf16 caches, layout above
+ *   idx           [device] int32 [batch][idx_layers][h_kv][n_sel] as written by kvsel_topk;
+ *                 idx_layers == 1 applies one selection to every layer
+ *   k_out, v_out  [device] bf16 out [batch][n_layers][h_kv][n_sel * P][d]
+ *   ws            [device] workspace or NULL; an index out of range is not
+ *                 followed, its row is zeroed and, with ws, KVSEL_ERR_DEVICE is
+ *                 recorded in the error word
+ */
+KVSEL_API kvsel_status kvsel_compact(const kvsel_desc* desc, const void* k, const void* v,
+                           const int32_t* idx, int32_t idx_layers, int32_t n_sel,
+                           void* k_out, void* v_out, void* ws, cudaStream_t stream);
+
+/*
+ * kvsel_pagetable — per-group KV block table from a 2-D block mask.
+ *
+ * CompactAttention: Accelerating Chunked Prefill with Block-Union KV
+ * Selection, 'Method steps' (2): Q-block union Mbar[b,h,j] = OR_i M[b,h,i,j],
+ * intra-group union G[b,g,j] = OR over the heads h of group g, and
+ * T[b,g] = { j : G[b,g,j] = 1 } in ascending order, written as CSR
+ * (kv_indptr / kv_indices) over rows (b, layer, g).
+ *
+ *   mask        [device] uint8 [batch][n_layers][h_q][n_qblk][n_kvblk_max], nonzero = selected
+ *   n_kvblk     [host] [batch] KV blocks of each sequence (<= n_kvblk_max); mask
+ *               entries at j >= n_kvblk[b] are ignored
+ *   kv_indptr   [device] int32 out [batch * n_layers * h_kv + 1]
+ *   kv_indices  [device] int32 out, capacity batch * n_layers * h_kv * n_kvblk_max
+ */
+KVSEL_API kvsel_status kvsel_pagetable(const kvsel_desc* desc, const uint8_t* mask, int32_t n_qblk,
+                             int32_t n_kvblk_max, const int32_t* n_kvblk,
+                             int32_t* kv_indptr, int32_t* kv_indices,
+                             void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Reads (stream-synchronising) and clears the device error word of a workspace. */
+KVSEL_API kvsel_status kvsel_read_device_error(void* ws, cudaStream_t stream);
+
+KVSEL_API const char* kvsel_status_string(kvsel_status status);
+KVSEL_API const char* kvsel_version(void);
+
+/*
+ * Tracing.  With tracing on, every kernel launch of the library is bracketed
+ * by CUDA events on its stream; kvsel_trace_read() synchronises those events
+ * and returns, per kernel name, the launches and the summed milliseconds since
+ * the last read.  kvsel_launch_count() counts every kernel launch since load.
+ */
+typedef struct {
+  char name[48];
+  int64_t launches;
+  double ms;
+} kvsel_trace_entry;
+
+KVSEL_API void kvsel_trace_enable(int32_t on);
+KVSEL_API kvsel_status kvsel_trace_read(kvsel_trace_entry* out, int32_t capacity, int32_t* n_out);
+KVSEL_API int64_t kvsel_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVSEL_H */

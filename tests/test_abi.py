@@ -1,0 +1,98 @@
+"""The C-ABI library loads, exports every declared symbol and rejects bad arguments on the host (no GPU)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from attention_kv_cache_gb300 import kvsel as K
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    with open(os.path.join(ROOT, "include", "kvsel.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"KVSEL_API[^;(]*?\b(kvsel_\w+)\s*\(", text, flags=re.S)))
+
+
+def test_header_declares_the_four_operations():
+    names = declared_symbols()
+    for op in ("kvsel_score", "kvsel_topk", "kvsel_compact", "kvsel_pagetable", "kvsel_combine_layers"):
+        assert op in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(K.LIB_PATH)
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert set(declared_symbols()) == set(K.EXPORTED)
+    assert "sm_103a" in K.version()
+    assert K.status_string(K.ERR_WORKSPACE).startswith("workspace")
+
+
+def _desc(**kw):
+    base = dict(n_layers=2, h_q=8, h_kv=2, head_dim=128, window=32, prefix_lens=[1000])
+    base.update(kw)
+    return K.make_desc(**base)
+
+
+def test_workspace_size_grows_with_length():
+    a = K.kvsel_workspace_size(_desc(prefix_lens=[1000]))
+    b = K.kvsel_workspace_size(_desc(prefix_lens=[100000]))
+    c = K.kvsel_workspace_size(_desc(prefix_lens=[1000, 5000, 70000]))
+    assert 0 < a < b and c > a and a % K.WS_ALIGN == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=96), K.ERR_UNSUPPORTED),
+    (dict(h_q=6, h_kv=4), K.ERR_INVALID_ARG),
+    (dict(window=0), K.ERR_INVALID_ARG),
+    (dict(window=65), K.ERR_INVALID_ARG),
+    (dict(h_q=32, h_kv=2, window=32), K.ERR_UNSUPPORTED),      # 16 heads x 32 rows > 256
+    (dict(pool_k=4), K.ERR_INVALID_ARG),
+    (dict(pool_k=65), K.ERR_INVALID_ARG),
+    (dict(page_size=0), K.ERR_INVALID_ARG),
+    (dict(page_size=512), K.ERR_INVALID_ARG),
+    (dict(prefix_lens=[0]), K.ERR_INVALID_ARG),
+    (dict(prefix_lens=[2 ** 31]), K.ERR_INVALID_ARG),
+    (dict(prefix_lens=[10] * 129), K.ERR_INVALID_ARG),
+    (dict(group_reduce=2), K.ERR_INVALID_ARG),
+])
+def test_bad_descriptor_rejected(kw, status):
+    d = _desc(**kw)
+    n = ctypes.c_size_t(0)
+    assert K.raw_call("kvsel_workspace_size", ctypes.byref(d), ctypes.byref(n)) == status
+    # the same check runs before any launch in every entry point (null stream: nothing is touched)
+    assert K.raw_call("kvsel_score", ctypes.byref(d), 16, 16, 16, 16, 256, 1 << 40, None) == status
+
+
+def test_null_and_misaligned_pointers_rejected():
+    d = _desc()
+    ws = K.kvsel_workspace_size(d)
+    assert K.raw_call("kvsel_score", ctypes.byref(d), None, 16, 16, None, 256, ws, None) == K.ERR_INVALID_ARG
+    assert K.raw_call("kvsel_score", ctypes.byref(d), 8, 16, 16, None, 256, ws, None) == K.ERR_INVALID_ARG
+    assert K.raw_call("kvsel_score", ctypes.byref(d), 16, 16, 16, None, None, ws, None) == K.ERR_WORKSPACE
+    assert K.raw_call("kvsel_score", ctypes.byref(d), 16, 16, 16, None, 128, ws, None) == K.ERR_WORKSPACE
+    assert K.raw_call("kvsel_score", ctypes.byref(d), 16, 16, 16, None, 256, ws - 1, None) == K.ERR_WORKSPACE
+    dp = _desc(page_size=16)
+    assert K.raw_call("kvsel_score", ctypes.byref(dp), 16, 16, 16, None, 256, 1 << 40, None) == K.ERR_INVALID_ARG
+    assert K.raw_call("kvsel_compact", ctypes.byref(d), 16, 16, 16, 1, 10, 16, 8, None, None) == K.ERR_INVALID_ARG
+    assert K.raw_call("kvsel_compact", ctypes.byref(d), 16, 16, 16, 3, 10, 16, 16, None, None) == K.ERR_INVALID_ARG
+
+
+def test_selection_arguments_rejected():
+    d = _desc(prefix_lens=[100])
+    big = 1 << 40
+    assert K.raw_call("kvsel_topk", ctypes.byref(d), 16, 2, 101, 0, 16, 256, big, None) == K.ERR_INVALID_ARG
+    assert K.raw_call("kvsel_topk", ctypes.byref(d), 16, 2, 5, 1, 16, 256, big, None) == K.ERR_INVALID_ARG
+    assert K.raw_call("kvsel_topk", ctypes.byref(d), 16, 3, 5, 0, 16, 256, big, None) == K.ERR_INVALID_ARG
+    dp = _desc(prefix_lens=[100], page_size=16)          # 7 pages, the last one partial
+    assert K.raw_call("kvsel_topk", ctypes.byref(dp), 16, 2, 3, 0, 16, 256, big, None) == K.ERR_INVALID_ARG
+    assert K.raw_call("kvsel_topk", ctypes.byref(dp), 16, 2, 7, 1, 16, 256, big, None) == K.ERR_INVALID_ARG
+    dw = _desc(prefix_lens=[96], page_size=16, window=24)  # window not a whole number of pages
+    assert K.raw_call("kvsel_topk", ctypes.byref(dw), 16, 2, 2, 1, 16, 256, big, None) == K.ERR_UNSUPPORTED
+    nk = (ctypes.c_int32 * 1)(9)
+    assert K.raw_call("kvsel_pagetable", ctypes.byref(d), 16, 4, 8, nk, 16, 16, 256, big, None) == K.ERR_INVALID_ARG
+    assert K.raw_call("kvsel_combine_layers", ctypes.byref(d), 16, 1, 2, 16, 256, big, None) == K.ERR_INVALID_ARG
