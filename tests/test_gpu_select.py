@@ -1,0 +1,105 @@
+"""Selection, gather and page-table kernels alone, on seeded inputs: bit-exact against the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+from attention_kv_cache_gb300 import synth as S
+from oracle import kvsel_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+def _ws(K, desc, cuda):
+    n = K.kvsel_workspace_size(desc)
+    buf = torch.zeros(n + K.WS_ALIGN, dtype=torch.uint8, device=cuda)
+    off = (-buf.data_ptr()) % K.WS_ALIGN
+    return buf[off:off + n]
+
+
+@pytest.mark.parametrize("rows,n,k,ties", [(3, 100, 7, True), (5, 4097, 1000, True), (2, 33000, 1024, False),
+                                           (2, 50000, 4096, True), (4, 300, 300, True), (2, 64, 0, False),
+                                           (3, 70000, 1, True)])
+def test_topk_token_mode_exact(rows, n, k, ties, cuda):
+    """Top-k with ties to the lower index, both decided in fp32 (the kernel's precision)."""
+    from attention_kv_cache_gb300 import kvsel as K
+    W = 3
+    s = S.random_scores(rows, n, seed=rows * 1000 + n, ties=ties)
+    desc = K.make_desc(n_layers=rows, h_q=1, h_kv=1, head_dim=128, window=W, prefix_lens=[n])
+    idx = torch.full((rows, k + W), -7, dtype=torch.int32, device=cuda)
+    ws = _ws(K, desc, cuda)
+    K.kvsel_topk(desc, s.to(cuda), rows, k, 0, idx, ws)
+    got = idx.cpu().numpy()
+    for r in range(rows):
+        want = O.select_tokens(s[r].double().numpy(), k, n, W)
+        np.testing.assert_array_equal(got[r], want)
+
+
+@pytest.mark.parametrize("L,P,k,n_recent,W", [(8192, 16, 128, 4, 32), (8200, 16, 50, 1, 16), (1000, 8, 3, 2, 8),
+                                               (131072, 16, 128, 4, 32)])
+def test_topk_page_mode_exact(L, P, k, n_recent, W, cuda):
+    from attention_kv_cache_gb300 import kvsel as K
+    n_pages = -(-L // P)
+    rows = 3
+    s = S.random_scores(rows, n_pages, seed=L + P, ties=True)
+    desc = K.make_desc(n_layers=rows, h_q=1, h_kv=1, head_dim=128, window=W, prefix_lens=[L], page_size=P)
+    n_sel = k + n_recent + W // P
+    idx = torch.full((rows, n_sel), -7, dtype=torch.int32, device=cuda)
+    K.kvsel_topk(desc, s.to(cuda), rows, k, n_recent, idx, _ws(K, desc, cuda))
+    got = idx.cpu().numpy()
+    for r in range(rows):
+        want = O.select_pages(s[r].double().numpy(), k, n_recent, L, W, P)
+        np.testing.assert_array_equal(got[r], want)
+
+
+@pytest.mark.parametrize("P", [1, 16])
+def test_compact_bit_exact_and_bounds(P, cuda):
+    from attention_kv_cache_gb300 import kvsel as K
+    w = S.Workload("gather", 95, 3, 4, 2, 128, 16, (999,), k_keep=20, page_size=P, n_recent=1 if P > 1 else 0)
+    inp = S.make_inputs(w, "cpu")
+    n_keys = 999 + 16
+    lim = n_keys if P == 1 else -(-n_keys // P)
+    g = torch.Generator().manual_seed(3)
+    n_sel = 23
+    idx = torch.randint(0, lim, (1, w.n_layers, w.h_kv, n_sel), generator=g, dtype=torch.int32)
+    desc = K.make_desc(n_layers=w.n_layers, h_q=w.h_q, h_kv=w.h_kv, head_dim=128, window=16, prefix_lens=[999],
+                       page_size=P)
+    kd, vd = inp.k[0].to(cuda), inp.v[0].to(cuda)
+    ko = torch.empty((1, w.n_layers, w.h_kv, n_sel * P, 128), dtype=torch.bfloat16, device=cuda)
+    vo = torch.empty_like(ko)
+    ws = _ws(K, desc, cuda)
+    K.kvsel_compact(desc, kd, vd, idx.to(cuda), w.n_layers, n_sel, ko, vo, ws)
+    assert K.kvsel_read_device_error(ws) == K.OK
+    for layer in range(w.n_layers):
+        for h in range(w.h_kv):
+            want_k = O.gather_rows(inp.k[0][layer, h].float().numpy(), idx[0, layer, h].numpy().astype(np.int64), P)
+            want_v = O.gather_rows(inp.v[0][layer, h].float().numpy(), idx[0, layer, h].numpy().astype(np.int64), P)
+            np.testing.assert_array_equal(ko[0, layer, h].float().cpu().numpy(), want_k)
+            np.testing.assert_array_equal(vo[0, layer, h].float().cpu().numpy(), want_v)
+    # an index out of range is not followed: its rows are zero and the error word says so
+    bad = idx.clone()
+    bad[0, 1, 0, 5] = lim
+    bad[0, 2, 1, 0] = -1
+    K.kvsel_compact(desc, kd, vd, bad.to(cuda), w.n_layers, n_sel, ko, vo, ws)
+    assert K.kvsel_read_device_error(ws) == K.ERR_DEVICE
+    assert K.kvsel_read_device_error(ws) == K.OK            # reading clears it
+    assert torch.all(ko[0, 1, 0, 5 * P:6 * P] == 0) and torch.all(ko[0, 2, 1, 0:P] == 0)
+
+
+def test_pagetable_full_size_ragged(cuda):
+    """Block union over the ragged batch's full mask (8 sequences, 32 layers, 16 Q blocks)."""
+    from attention_kv_cache_gb300 import kvsel as K
+    w = S.RAGGED_B8
+    M, n_kv = S.block_mask(w, "cpu")
+    desc = K.make_desc(n_layers=w.n_layers, h_q=w.h_q, h_kv=w.h_kv, head_dim=128, window=w.window,
+                       prefix_lens=w.prefix_lens)
+    rows = w.batch * w.n_layers * w.h_kv
+    nmax = M.shape[-1]
+    indptr = torch.empty(rows + 1, dtype=torch.int32, device=cuda)
+    indices = torch.full((rows * nmax,), -1, dtype=torch.int32, device=cuda)
+    K.kvsel_pagetable(desc, M.to(cuda), M.shape[3], nmax, n_kv, indptr, indices, _ws(K, desc, cuda))
+    ref_ptr, ref_idx = O.block_union_csr(M.numpy(), w.h_kv, n_kv)
+    np.testing.assert_array_equal(indptr.cpu().numpy(), ref_ptr)
+    np.testing.assert_array_equal(indices.cpu().numpy()[: ref_ptr[-1]], ref_idx)
+    density = M.float().mean().item()
+    assert 0.05 < density < 0.2
