@@ -146,42 +146,67 @@ class Inputs:
 
 
 def _cluster_starts(w: Workload, L: int, gen: torch.Generator, device) -> torch.Tensor:
-    """Non-overlapping run starts: one run inside each of n_clusters equal slots of [0, L)."""
+    """Non-overlapping run starts: one run inside each of n_clusters equal slots of [0, L).  [1, h_kv, n]."""
     n = w.n_clusters
     slot = L // n
     if slot < w.cluster_len:
         raise ValueError("prefix too short for the planted clusters")
-    off = torch.randint(0, slot - w.cluster_len + 1, (w.n_layers, w.h_kv, n), generator=gen, device=device)
+    off = torch.randint(0, slot - w.cluster_len + 1, (1, w.h_kv, n), generator=gen, device=device)
     base = torch.arange(n, device=device) * slot
     return base + off
 
 
-def _one_sequence(w: Workload, b: int, device, gen: torch.Generator):
+def _layer_generator(w: Workload, b: int, layer: int, device) -> torch.Generator:
+    """Each (sequence, layer) draws from its own stream, so any layer can be regenerated alone."""
+    return torch.Generator(device=device).manual_seed(w.seed * 1_000_003 + b * 10_007 + layer + 1)
+
+
+def make_queries(w: Workload, b: int, device="cpu") -> torch.Tensor:
+    """Window queries of sequence b: [n_layers, h_q, W, d] bf16."""
+    gen = torch.Generator(device=device).manual_seed(w.seed * 1_000_003 + b * 10_007)
+    q32 = torch.randn((w.n_layers, w.h_q, w.window, w.head_dim), generator=gen, device=device,
+                      dtype=torch.float32)
+    return q32.to(torch.bfloat16)
+
+
+def make_layer(w: Workload, b: int, layer: int, q: torch.Tensor, device="cpu"):
+    """K, V ([h_kv, L_b + W, d] bf16) and the planted run starts ([h_kv, n_clusters]) of one layer.
+
+    ``q`` is the sequence's query tensor from make_queries (the cluster
+    direction is the mean of each group's window queries of this layer).
+    """
     L, W, d = w.prefix_lens[b], w.window, w.head_dim
     n = L + W
-    q32 = torch.randn((w.n_layers, w.h_q, W, d), generator=gen, device=device, dtype=torch.float32)
-    q = q32.to(torch.bfloat16)
-    k = torch.empty((w.n_layers, w.h_kv, n, d), device=device, dtype=torch.bfloat16)
-    v = torch.empty((w.n_layers, w.h_kv, n, d), device=device, dtype=torch.bfloat16)
-    starts = (_cluster_starts(w, L, gen, device) if w.n_clusters else
-              torch.zeros((w.n_layers, w.h_kv, 0), dtype=torch.long, device=device))
-    G = w.group
-    span = torch.arange(w.cluster_len, device=device)
+    gen = _layer_generator(w, b, layer, device)
+    k32 = torch.randn((w.h_kv, n, d), generator=gen, device=device, dtype=torch.float32)
+    starts = torch.zeros((w.h_kv, 0), dtype=torch.long, device=device)
+    if w.n_clusters:
+        starts = _cluster_starts(w, L, gen, device)[0]
+        G = w.group
+        qg = q[layer].to(device).float().reshape(w.h_kv, G * W, d)
+        u = qg.mean(dim=1)
+        u = u / u.norm(dim=-1, keepdim=True).clamp_min(1e-30)
+        shift = 1.5 * math.sqrt(d) * u                                       # [h_kv, d]
+        span = torch.arange(w.cluster_len, device=device)
+        rows = (starts[:, :, None] + span).reshape(w.h_kv, -1)               # [h_kv, n_clusters * 64]
+        idx = rows[:, :, None].expand(-1, -1, d)
+        k32.scatter_add_(1, idx, shift[:, None, :].expand(-1, rows.shape[1], -1).contiguous())
+    k = k32.to(torch.bfloat16)
+    del k32
+    v = torch.randn((w.h_kv, n, d), generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+    return k, v, starts
+
+
+def _one_sequence(w: Workload, b: int, device):
+    q = make_queries(w, b, device)
+    n = w.prefix_lens[b] + w.window
+    k = torch.empty((w.n_layers, w.h_kv, n, w.head_dim), device=device, dtype=torch.bfloat16)
+    v = torch.empty_like(k)
+    starts = []
     for layer in range(w.n_layers):
-        # one layer at a time keeps the fp32 staging buffer small (537 MB at L = 128K)
-        k32 = torch.randn((w.h_kv, n, d), generator=gen, device=device, dtype=torch.float32)
-        if w.n_clusters:
-            qg = q[layer].float().reshape(w.h_kv, G * W, d)
-            u = qg.mean(dim=1)
-            u = u / u.norm(dim=-1, keepdim=True).clamp_min(1e-30)
-            shift = 1.5 * math.sqrt(d) * u                             # [h_kv, d]
-            rows = (starts[layer][:, :, None] + span).reshape(w.h_kv, -1)  # [h_kv, n_clusters*64]
-            idx = rows[:, :, None].expand(-1, -1, d)
-            k32.scatter_add_(1, idx, shift[:, None, :].expand(-1, rows.shape[1], -1).contiguous())
-        k[layer] = k32.to(torch.bfloat16)
-        v[layer] = torch.randn((w.h_kv, n, d), generator=gen, device=device,
-                               dtype=torch.float32).to(torch.bfloat16)
-    return q, k, v, starts
+        k[layer], v[layer], st = make_layer(w, b, layer, q, device)
+        starts.append(st)
+    return q, k, v, torch.stack(starts)
 
 
 def block_mask(w: Workload, device="cpu") -> tuple:
@@ -220,10 +245,9 @@ def block_mask(w: Workload, device="cpu") -> tuple:
 
 def make_inputs(w: Workload, device="cpu", with_mask: Optional[bool] = None) -> Inputs:
     """All tensors of workload ``w`` on ``device`` (a torch device string)."""
-    gen = torch.Generator(device=device).manual_seed(w.seed)
     qs, ks, vs, cs = [], [], [], []
     for b in range(w.batch):
-        q, k, v, c = _one_sequence(w, b, device, gen)
+        q, k, v, c = _one_sequence(w, b, device)
         qs.append(q); ks.append(k); vs.append(v); cs.append(c)
     mask = n_kv = None
     if (w.block_union if with_mask is None else with_mask):
