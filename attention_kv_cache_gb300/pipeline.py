@@ -26,6 +26,8 @@ def desc_for(w, pool_k: Optional[int] = None):
 def pack(inputs, device="cuda"):
     """Packed device tensors in the library's layouts: q [B, layers, h_q, W, d]; k, v flat (sequences back to back)."""
     q = torch.stack([x for x in inputs.q]).to(device).contiguous()
+    if len(inputs.k) == 1:                       # one sequence: a view, no second copy
+        return q, inputs.k[0].to(device).reshape(-1), inputs.v[0].to(device).reshape(-1)
     k = torch.cat([x.reshape(-1) for x in inputs.k]).to(device)
     v = torch.cat([x.reshape(-1) for x in inputs.v]).to(device)
     return q, k, v

@@ -1,0 +1,389 @@
+#!/usr/bin/env python
+"""Throughput of the window-attention KV selection path on GB300.
+
+One step = the whole path over one batch of the workload: kvsel_score,
+[kvsel_combine_layers], kvsel_topk, kvsel_compact (and kvsel_pagetable when
+the workload has a block mask).  Default workload: LLaMA-3.1-8B shape, 32
+layers, 32 / 8 heads, d = 128, 128K-token prefix, W = 32, max over the group,
+page max P = 16, top 128 pages + 4 recent pages, compacted K/V.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU
+oracle on the same metric instead (a bounded sample of the workload per step).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefix tokens scored+selected/s (per layer, 128K ctx); % of HBM/TC roofline"
+DEFAULT_WORKLOAD = "llama8b_32l_h32x8_d128_L131072_W32_paged16"
+HBM_FALLBACK_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="kvsel", choices=["kvsel", "reference"])
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--cpu-units", type=int, default=0,
+                   help="(layer, KV head) units in the CPU-baseline sample (default: one per host core)")
+    p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) leg
+
+def _oracle_unit(args):
+    """The oracle's whole path for one (layer, KV head) unit; returns seconds spent."""
+    wd, q_group, k_unit, v_unit = args
+    from oracle import kvsel_oracle as O
+    t0 = time.perf_counter()
+    L, W, P = wd["L"], wd["W"], wd["P"]
+    s = O.group_scores(O._f64(q_group), O._f64(k_unit), L, wd["reduce"])
+    u = O.max_pool(s, wd["pool_k"])
+    if P > 1:
+        U = O.page_reduce(u, P, wd["page_reduce"])
+        sel = O.select_pages(U, wd["k"], wd["n_recent"], L, W, P)
+    else:
+        sel = O.select_tokens(u, wd["k"], L, W)
+    O.gather_rows(O._f64(k_unit), sel, P)
+    O.gather_rows(O._f64(v_unit), sel, P)
+    return time.perf_counter() - t0
+
+
+def _pool_init():
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    os.environ["OMP_NUM_THREADS"] = "1"
+
+
+def oracle_rate(w, units, pool, cores):
+    """Prefix tokens per second per layer of the oracle over ``units`` = [(q_group, k_unit, v_unit)]."""
+    wd = dict(L=w.prefix_lens[0], W=w.window, P=w.page_size, G=w.group, h_kv=w.h_kv, reduce=w.group_reduce,
+              pool_k=w.pool_k, page_reduce=w.page_reduce, k=w.k_keep, n_recent=w.n_recent)
+    t0 = time.perf_counter()
+    pool.map(_oracle_unit, [(wd, q, k, v) for (q, k, v) in units], chunksize=1)
+    wall = time.perf_counter() - t0
+    tokens_layers = len(units) / w.h_kv * w.prefix_lens[0]
+    return tokens_layers / wall, wall
+
+
+def make_pool(cores):
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    os.environ["OMP_NUM_THREADS"] = "1"
+    ctx = mp.get_context("spawn")
+    pool = ctx.Pool(cores, initializer=_pool_init)
+    pool.map(time.sleep, [0.0] * cores)       # start the workers before timing
+    return pool
+
+
+# ----------------------------------------------------------------------------- measurement helpers
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return HBM_FALLBACK_GBS, "fallback"
+
+
+CLOCK_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+                "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                "clocks_event_reasons.sw_power_cap")
+REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    def __init__(self, index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(REASONS, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_bytes(w, n_sel_rows):
+    """Algorithmic HBM bytes of one launch of each kernel (the whole workload per launch)."""
+    d, W = w.head_dim, w.window
+    units = [(w.n_layers * w.h_kv, L) for L in w.prefix_lens]
+    q_bytes = w.batch * w.n_layers * w.h_q * W * d * 2
+    k_all = sum(u * (L + W) * d * 2 for u, L in units)
+    k_prefix = sum(u * L * d * 2 for u, L in units)
+    score_w = sum(u * L * 4 for u, L in units)
+    P = w.page_size
+    page_w = sum(u * (-(-L // P)) * 4 for u, L in units) if P > 1 else 0
+    sel_read = page_w if P > 1 else score_w
+    idx_w = w.batch * w.n_layers * w.h_kv * w.n_sel() * 4
+    gather = 2 * 2 * w.batch * w.n_layers * w.h_kv * n_sel_rows * d * 2
+    return {
+        "score_pass1_simt": k_all + q_bytes,
+        "score_pass2_simt": k_prefix + q_bytes + score_w + page_w,
+        "topk_radix": sel_read + idx_w,
+        "kv_compact": gather + idx_w,
+    }
+
+
+def traffic_record(kernel):
+    """dram bytes per launch from the committed ncu summary, if taken on the kernel's current source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and parts[0] == kernel and not line.startswith("#"):
+                src, digest = parts[2].split(":")
+                with open(os.path.join(ROOT, "attention_kv_cache_gb300", "csrc", src), "rb") as g:
+                    if hashlib.sha256(g.read()).hexdigest()[:12] != digest:
+                        return None
+                return float(parts[1])
+    return None
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- the CUDA path
+
+def run_kvsel(args):
+    import torch
+    from attention_kv_cache_gb300 import kvsel as K
+    from attention_kv_cache_gb300 import synth as S
+    from attention_kv_cache_gb300.pipeline import Pipeline, pack
+
+    rank, world, local = dist_setup()
+    w = S.by_name(args.workload)
+    n_cpu_units = args.cpu_units or (os.cpu_count() or 1)
+    cores = min(os.cpu_count() or 1, n_cpu_units)
+    pool = make_pool(cores) if (rank == 0 and world == 1 and not args.no_cpu) else None  # before any GPU call
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    inp = S.make_inputs(w, str(dev))
+    q, k, v = pack(inp, dev)
+    mask = inp.mask
+    nkv = inp.n_kvblk
+    pipe = Pipeline(w, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        pipe.run(q, k, v, mask, nkv)
+    torch.cuda.synchronize()
+    assert K.kvsel_read_device_error(pipe.ws) == K.OK
+
+    # ---- timed region: inputs (K/V) are far larger than L2, so every step streams them from HBM
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    K.kvsel_trace_enable(True)
+    K.kvsel_trace_read()
+    n0 = K.kvsel_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        pipe.run(q, k, v, mask, nkv)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = K.kvsel_launch_count() - n0
+    trace = K.kvsel_trace_read()
+    K.kvsel_trace_enable(False)
+    clocks = sampler.stop()
+    barrier(world)
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    assert K.kvsel_read_device_error(pipe.ws) == K.OK
+
+    tokens_per_step = sum(L for L in w.prefix_lens) * w.n_layers
+    value = world * tokens_per_step * args.steps / (ms / 1e3)
+
+    # ---- roofline of the dominant kernel (largest share of the timed region)
+    name, (n_launch, k_ms) = max(trace.items(), key=lambda kv: kv[1][1])
+    bytes_per_launch = kernel_bytes(w, pipe.n_sel * w.page_size).get(name)
+    peak, peak_src = measured_peaks()
+    roof = None
+    if bytes_per_launch is not None:
+        achieved = bytes_per_launch / (k_ms / n_launch / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": name, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                "traffic": traffic_record(name), "algorithmic_bytes": bytes_per_launch,
+                "share": round(k_ms / sum(x[1] for x in trace.values()), 4)}
+
+    # ---- end to end through the C ABI with host buffers (copies inside the timed region)
+    e2e = None
+    if not args.no_e2e:
+        qh = q.cpu().pin_memory()
+        kh = torch.empty(k.shape, dtype=k.dtype, pin_memory=True)
+        kh.copy_(k)
+        vh = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+        vh.copy_(v)
+        outs = [pipe.idx, pipe.k_out, pipe.v_out] + ([pipe.kv_indptr, pipe.kv_indices] if mask is not None else [])
+        outs_h = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+        mask_h = mask.cpu().pin_memory() if mask is not None else None
+
+        def e2e_step():
+            q.copy_(qh, non_blocking=True)
+            k.copy_(kh, non_blocking=True)
+            v.copy_(vh, non_blocking=True)
+            if mask is not None:
+                mask.copy_(mask_h, non_blocking=True)
+            pipe.run(q, k, v, mask, nkv)
+            for o, oh in zip(outs, outs_h):
+                oh.copy_(o, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        h2d = q.numel() * 2 + k.numel() * 2 + v.numel() * 2 + (mask.numel() if mask is not None else 0)
+        d2h = sum(o.numel() * o.element_size() for o in outs)
+        e2e = {"value": world * tokens_per_step * args.e2e_steps / (ems / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps}
+
+    # ---- CPU baseline: the oracle on a bounded sample of the same workload (rank 0, N = 1)
+    cpu = None
+    if pool is not None:
+        units = []
+        G = w.group
+        for i in range(n_cpu_units):
+            layer, g = divmod(i, w.h_kv)
+            layer %= w.n_layers
+            units.append((inp.q[0][layer, g * G:(g + 1) * G].cpu(), inp.k[0][layer, g].cpu(), inp.v[0][layer, g].cpu()))
+        rate, wall = oracle_rate(w, units, pool, cores)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{len(units)} (layer, KV head) units of the same workload ({len(units) / w.h_kv:g} layers), "
+                         f"full path per unit, {wall:.1f} s wall on {cores} worker processes (1 BLAS thread each)"}
+        pool.close()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 inputs, f32 arithmetic", "data": "synthetic",
+            "config": {"workload": w.name, "layers": w.n_layers, "h_q": w.h_q, "h_kv": w.h_kv, "d": w.head_dim,
+                       "prefix_len": list(w.prefix_lens), "window": w.window, "group_reduce": w.group_reduce,
+                       "pool_k": w.pool_k, "page_size": w.page_size, "k_keep": w.k_keep, "n_recent": w.n_recent,
+                       "l2": "inputs exceed L2 (K+V %.1f GB per step)" % ((k.numel() + v.numel()) * 2 / 1e9),
+                       "parallelism": f"replicas x{world}"},
+            "clocks": clocks, "gpu_launches": launches, "kernels": {n: {"launches": c, "ms": round(t, 3)}
+                                                                   for n, (c, t) in trace.items()},
+            "roofline": roof, "e2e": e2e, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- the oracle arm
+
+def run_reference(args):
+    """The fp64 oracle on the host cores: each step is one (layer, KV head) unit of the workload (the
+    path's smallest independent piece), and the steps run concurrently on one worker process per core."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from attention_kv_cache_gb300 import synth as S
+    w = S.by_name(args.workload)
+    cores = min(os.cpu_count() or 1, max(1, args.steps))
+    pool = make_pool(cores)
+    q = S.make_queries(w, 0, "cpu")
+    kk, vv, _ = S.make_layer(w, 0, 0, q, "cpu")
+    G = w.group
+    units = [(q[0, g * G:(g + 1) * G], kk[g], vv[g]) for g in range(w.h_kv)]
+    if args.warmup > 0:
+        oracle_rate(w, [units[i % len(units)] for i in range(min(args.warmup, cores))], pool, cores)
+    value, wall = oracle_rate(w, [units[i % len(units)] for i in range(args.steps)], pool, cores)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name,
+                   "sample_per_step": "one (layer, KV head) unit: scores, pooling, page scores, selection, gather"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} units of layer 0 (cycled over its {w.h_kv} KV heads), "
+                                   f"{wall:.1f} s wall on {cores} worker processes"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    pool.close()
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_kvsel(a)
