@@ -7,7 +7,6 @@ this module only allocates device memory and orders the calls on one stream.
 
 from __future__ import annotations
 
-import dataclasses
 from typing import Optional
 
 import torch
@@ -31,19 +30,6 @@ def pack(inputs, device="cuda"):
     k = torch.cat([x.reshape(-1) for x in inputs.k]).to(device)
     v = torch.cat([x.reshape(-1) for x in inputs.v]).to(device)
     return q, k, v
-
-
-@dataclasses.dataclass
-class Buffers:
-    ws: torch.Tensor
-    scores: torch.Tensor
-    page_scores: Optional[torch.Tensor]
-    combined: Optional[torch.Tensor]
-    idx: torch.Tensor
-    k_out: torch.Tensor
-    v_out: torch.Tensor
-    kv_indptr: Optional[torch.Tensor] = None
-    kv_indices: Optional[torch.Tensor] = None
 
 
 class Pipeline:
