@@ -56,6 +56,7 @@ def _load():
     sig = {
         "kvsel_workspace_size": (I32, [D, P(SZ)]),
         "kvsel_score": (I32, [D, VP, VP, VP, VP, VP, SZ, VP]),
+        "kvsel_score_noalloc": (I32, [D, VP, VP, VP, VP, VP]),
         "kvsel_combine_layers": (I32, [D, VP, I32, I32, VP, VP, SZ, VP]),
         "kvsel_topk": (I32, [D, VP, I32, I32, I32, VP, VP, SZ, VP]),
         "kvsel_compact": (I32, [D, VP, VP, VP, I32, I32, VP, VP, VP, VP]),
@@ -75,8 +76,8 @@ def _load():
 
 
 _lib = _load()
-EXPORTED = ("kvsel_workspace_size", "kvsel_score", "kvsel_combine_layers", "kvsel_topk", "kvsel_compact",
-            "kvsel_pagetable", "kvsel_read_device_error", "kvsel_status_string", "kvsel_version",
+EXPORTED = ("kvsel_workspace_size", "kvsel_score", "kvsel_score_noalloc", "kvsel_combine_layers", "kvsel_topk",
+            "kvsel_compact", "kvsel_pagetable", "kvsel_read_device_error", "kvsel_status_string", "kvsel_version",
             "kvsel_trace_enable", "kvsel_trace_read", "kvsel_launch_count")
 
 
@@ -131,6 +132,15 @@ def kvsel_score(desc, q, k, scores, page_scores, ws, ws_bytes: Optional[int] = N
     nb = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
     _check(_lib.kvsel_score(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(scores), _ptr(page_scores), _ptr(ws),
                             nb, _stream(stream)), "kvsel_score")
+
+
+def kvsel_score_noalloc(desc, q, k, scores, page_scores, stream=None):
+    """kvsel_score with the library's built-in scratch (no workspace argument, nothing allocated)."""
+    _check(_lib.kvsel_score_noalloc(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(scores), _ptr(page_scores),
+                                    _stream(stream)), "kvsel_score_noalloc")
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 def kvsel_combine_layers(desc, scores, layer_lo: int, layer_hi: int, combined, ws, ws_bytes=None, stream=None):

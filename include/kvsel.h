@@ -181,6 +181,30 @@ KVSEL_API kvsel_status kvsel_pagetable(const kvsel_desc* desc, const uint8_t* ma
                              int32_t* kv_indptr, int32_t* kv_indices,
                              void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/*
+ * kvsel_score_noalloc — kvsel_score for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this call; it exists for callers with no
+ * way to obtain a workspace: a plugin inside a host program that owns all of
+ * the GPU's memory, or a latency-critical caller that must not pay
+ * cudaMalloc's device-wide synchronisation.  It computes exactly what
+ * kvsel_score computes, with the scratch of the two scoring passes in an
+ * array inside the library of KVSEL_NOALLOC_SCRATCH_BYTES, which every GPU
+ * that loads the library holds until the process exits.  It allocates and
+ * frees nothing.
+ *
+ * The first call made while a device is current looks up that array's device
+ * address (cudaGetSymbolAddress) and caches it; make that first call before
+ * any stream capture.  The stream must belong to the current device.  All
+ * calls share the one array: calls whose work overlaps on the GPU (two
+ * streams, or two host threads) race and give undefined results.  A
+ * descriptor whose kvsel_workspace_size() exceeds KVSEL_NOALLOC_SCRATCH_BYTES
+ * is rejected with KVSEL_ERR_WORKSPACE before anything is launched.
+ */
+#define KVSEL_NOALLOC_SCRATCH_BYTES (32u << 20)
+KVSEL_API kvsel_status kvsel_score_noalloc(const kvsel_desc* desc, const void* q, const void* k,
+                                           float* scores, float* page_scores, cudaStream_t stream);
+
 /* Reads (stream-synchronising) and clears the device error word of a workspace. */
 KVSEL_API kvsel_status kvsel_read_device_error(void* ws, cudaStream_t stream);
 
