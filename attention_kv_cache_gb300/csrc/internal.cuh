@@ -48,6 +48,9 @@ __device__ __forceinline__ int find_seq(const SeqTable& t, int item) {
   return b;
 }
 
+// Keys per pass-1 segment (fixes the size of the per-segment partials in the workspace).
+constexpr int64_t kScoreSeg1 = 2048;
+
 // Problem description handed to every scoring kernel.
 struct ScoreShape {
   int32_t n_layers, h_q, h_kv, d, W, G, R;   // R = G * W rows per unit
@@ -74,9 +77,35 @@ inline kvsel_status launch_status() {
 }
 
 // ---- kernel launchers ---------------------------------------------------------------
-kvsel_status launch_score(const ScoreShape& sh, const SeqTable& t1, const SeqTable& t2,
-                          const void* q, const void* k, float* scores, float* page_scores,
-                          float* lse, float2* part, DeviceError* err, cudaStream_t s);
+// Scoring: launch_score (score_tc.cu) picks the tensor-core kernels for the shapes they
+// cover and the CUDA-core kernels otherwise.  `base` carries the per-sequence geometry;
+// the launchers add their own work-item tables.
+kvsel_status launch_score(const ScoreShape& sh, const SeqTable& base, const void* q, const void* k,
+                          float* scores, float* page_scores, float* lse, float2* part, DeviceError* err,
+                          cudaStream_t s);
+kvsel_status launch_score_simt(const ScoreShape& sh, const SeqTable& t1, const SeqTable& t2,
+                               const void* q, const void* k, float* scores, float* page_scores,
+                               float* lse, float2* part, DeviceError* err, cudaStream_t s);
+kvsel_status launch_lse_combine(const ScoreShape& sh, const SeqTable& t1, float2* part, float* lse,
+                                cudaStream_t s);
+
+// Work items: n_seg = ceil(len_b / seg) segments for each (layer, KV head) unit of sequence b,
+// where len_b is L_b + W (pass 1) or L_b (pass 2).
+inline SeqTable with_items(const SeqTable& base, int64_t units_per_seq, int64_t seg, bool include_window,
+                           int32_t window) {
+  SeqTable t = base;
+  int64_t item = 0;
+  for (int b = 0; b < t.batch; ++b) {
+    const int64_t len = (int64_t)t.s[b].L + (include_window ? window : 0);
+    const int64_t ns = (len + seg - 1) / seg;
+    t.s[b].item0 = (int32_t)item;
+    t.s[b].n_seg = (int32_t)ns;
+    t.s[b].part_off = item;
+    item += units_per_seq * ns;
+  }
+  t.n_items = (int32_t)item;
+  return t;
+}
 
 kvsel_status launch_topk(const kvsel_desc& desc, const SeqTable& t, int layers, int k, int n_recent,
                          const float* scores, int32_t* idx, cudaStream_t s);

@@ -74,10 +74,7 @@ static inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 static int64_t total_units(const kvsel_desc& d) { return (int64_t)d.batch * d.n_layers * d.h_kv; }
-static int64_t seg1_len(const kvsel_desc&) { return 2048; }
-static int64_t seg2_len(const kvsel_desc& d) { return (int64_t)d.page_size * cdiv(1024, d.page_size); }
-static int64_t nseg1(const kvsel_desc& d, int b) { return cdiv(d.prefix_lens[b] + d.window, seg1_len(d)); }
-static int64_t nseg2(const kvsel_desc& d, int b) { return cdiv(d.prefix_lens[b], seg2_len(d)); }
+static int64_t nseg1(const kvsel_desc& d, int b) { return cdiv(d.prefix_lens[b] + d.window, kScoreSeg1); }
 
 struct WsLayout {
   size_t lse_off, part_off, norm_off, cnt_off, total;
@@ -151,20 +148,6 @@ static SeqTable make_table(const kvsel_desc& d, int32_t layers_in_scores) {
   return t;
 }
 
-// Work items of a launch: n_seg(b) segments for every (layer, KV head) unit of sequence b.
-static void set_items(SeqTable& t, const kvsel_desc& d, int64_t (*nseg)(const kvsel_desc&, int)) {
-  int64_t item = 0;
-  const int64_t units_per_seq = (int64_t)d.n_layers * d.h_kv;
-  for (int b = 0; b < t.batch; ++b) {
-    const int64_t ns = nseg(d, b);
-    t.s[b].item0 = (int32_t)item;
-    t.s[b].n_seg = (int32_t)ns;
-    t.s[b].part_off = item;
-    item += units_per_seq * ns;
-  }
-  t.n_items = (int32_t)item;
-}
-
 }  // namespace kvsel
 
 using namespace kvsel;
@@ -205,23 +188,18 @@ kvsel_status kvsel_score(const kvsel_desc* desc, const void* q, const void* k, f
   if (d.page_size > 1 && page_scores == nullptr) return KVSEL_ERR_INVALID_ARG;
   if ((st = check_ws(d, ws, ws_bytes)) != KVSEL_OK) return st;
   const WsLayout w = ws_layout(d);
-  char* base = static_cast<char*>(ws);
+  auto ws_base = [](void* p) { return static_cast<char*>(p); };
 
   ScoreShape sh;
   sh.n_layers = d.n_layers; sh.h_q = d.h_q; sh.h_kv = d.h_kv; sh.d = d.head_dim; sh.W = d.window;
   sh.G = d.h_q / d.h_kv; sh.R = sh.G * d.window;
   sh.group_reduce = d.group_reduce; sh.pool_k = d.pool_k; sh.page_size = d.page_size;
   sh.page_reduce = d.page_reduce;
-  sh.seg1 = (int32_t)seg1_len(d);
-  sh.seg2 = (int32_t)seg2_len(d);
+  sh.seg1 = sh.seg2 = 0;    // set by the launcher
   sh.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.head_dim));
-
-  SeqTable t1 = make_table(d, d.n_layers);
-  SeqTable t2 = t1;
-  set_items(t1, d, nseg1);
-  set_items(t2, d, nseg2);
-  return launch_score(sh, t1, t2, q, k, scores, page_scores, reinterpret_cast<float*>(base + w.lse_off),
-                      reinterpret_cast<float2*>(base + w.part_off), reinterpret_cast<DeviceError*>(base),
+  const SeqTable base = make_table(d, d.n_layers);
+  return launch_score(sh, base, q, k, scores, page_scores, reinterpret_cast<float*>(ws_base(ws) + w.lse_off),
+                      reinterpret_cast<float2*>(ws_base(ws) + w.part_off), reinterpret_cast<DeviceError*>(ws),
                       stream);
 }
 

@@ -309,9 +309,9 @@ kvsel_status run_d(const ScoreArgs& args, const SeqTable& t1, const SeqTable& t2
 
 }  // namespace
 
-kvsel_status launch_score(const ScoreShape& sh, const SeqTable& t1, const SeqTable& t2, const void* q,
-                          const void* k, float* scores, float* page_scores, float* lse, float2* part,
-                          DeviceError* err, cudaStream_t s) {
+kvsel_status launch_score_simt(const ScoreShape& sh, const SeqTable& t1, const SeqTable& t2, const void* q,
+                               const void* k, float* scores, float* page_scores, float* lse, float2* part,
+                               DeviceError* err, cudaStream_t s) {
   ScoreArgs args;
   args.sh = sh;
   args.q = static_cast<const __nv_bfloat16*>(q);
@@ -323,6 +323,17 @@ kvsel_status launch_score(const ScoreShape& sh, const SeqTable& t1, const SeqTab
   args.err = err;
   if (t1.n_items <= 0 || t2.n_items <= 0) return KVSEL_ERR_INVALID_ARG;
   return sh.d == 64 ? run_d<64>(args, t1, t2, s) : run_d<128>(args, t1, t2, s);
+}
+
+kvsel_status launch_lse_combine(const ScoreShape& sh, const SeqTable& t1, float2* part, float* lse, cudaStream_t s) {
+  ScoreArgs args{};
+  args.sh = sh;
+  args.part = part;
+  args.lse = lse;
+  const int64_t n_rows = (int64_t)t1.batch * sh.n_layers * sh.h_kv * sh.R;
+  TraceScope ts("score_lse_combine", s);
+  score_lse_combine<<<(unsigned)((n_rows + kThreads - 1) / kThreads), kThreads, 0, s>>>(args, t1, n_rows);
+  return launch_status();
 }
 
 }  // namespace kvsel

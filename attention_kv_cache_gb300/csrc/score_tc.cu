@@ -1,0 +1,647 @@
+// Window-attention scoring on the 5th-generation tensor cores (tcgen05 / TMEM), sm_103a.
+//
+// Same two passes as the CUDA-core version (ClusterAttn, 'Background and key
+// observations': masked window softmax over the full row, column sum over the
+// window rows for prefix columns), with the logits of each 128-key tile made
+// by UMMA from TMA-staged operands:
+//
+//   pass 1  rows on TMEM lanes:  D[128 rows x 128 keys] = Q · K_tileᵀ; each
+//           epilogue thread owns one window row and keeps an online max / sum.
+//   pass 2  keys on TMEM lanes:  D[128 keys x RT rows] = K_tile · Qᵀ; each
+//           epilogue thread owns one key and sums 2^(z·log2e/√d − lse) over the
+//           rows of each head in registers (no cross-lane reduction), then the
+//           group reduce, max-pool and page reduce run on the segment in smem.
+//
+// Persistent CTAs (one per SM), each walking a contiguous range of (unit,
+// segment) work items.  Warp roles: warp 0 issues TMA (Q once per unit, K
+// tiles through an NK-stage ring), warp 1 owns TMEM and issues UMMA into a
+// ring of TMEM accumulators, warps 2..9 are the epilogue.  All hand-offs are
+// mbarriers with bounded waits; a wait that gives up records
+// KVSEL_ERR_TIMEOUT in the workspace error word and the CTA unwinds.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "internal.cuh"
+#include "sm100.cuh"
+
+namespace kvsel {
+namespace {
+
+using namespace sm100;
+
+constexpr int kTileKeys = 128;
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kThreadsTc = 32 * (2 + kEpiWarps);
+constexpr int kSeg2Max = 8192;     // prefix keys per pass-2 segment (rounded down to whole pages)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kEpiBarrier = 1;   // named barrier id of the epilogue warps
+
+enum : uint32_t { kWhereProducer = 1, kWhereMma = 2, kWhereEpilogue = 3, kWhereDrain = 4 };
+
+// Shared-memory plan (offsets from a 1024-byte aligned base).
+template <int RT, int D, int NK>
+struct Plan {
+  static constexpr int kDBlocks = D / 64;                   // 128-byte swizzle atoms along d
+  static constexpr uint32_t kQBlock = RT * 128;             // one d-block of Q: RT rows x 128 B
+  static constexpr uint32_t kQBytes = kQBlock * kDBlocks;
+  static constexpr uint32_t kKBlock = kTileKeys * 128;      // one d-block of a K tile
+  static constexpr uint32_t kKBytes = kKBlock * kDBlocks;
+  static constexpr uint32_t kQOff = 0;
+  static constexpr uint32_t kKOff = kQOff + kQBytes;
+  static constexpr uint32_t kSsOff = kKOff + NK * kKBytes;                 // pass-2 segment scores
+  static constexpr uint32_t kSsFloats = kSeg2Max + 128;
+  static constexpr uint32_t kLseOff = kSsOff + kSsFloats * 4;             // pass-2 row lse (RT floats)
+  static constexpr uint32_t kRedOff = kLseOff + RT * 4;                   // pass-1 (m, l) exchange
+  static constexpr uint32_t kNT = kTmemCols / RT;                         // TMEM accumulator stages
+  static constexpr uint32_t kBarOff = kRedOff + 128 * 8;
+  // barriers: full[NK], empty[NK], tfull[NT], tempty[NT], q_full, q_empty, drain
+  static constexpr uint32_t kNumBars = 2 * NK + 2 * kNT + 3;
+  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;            // tmem slot, abort flag
+  static constexpr uint32_t kBytes = kMiscOff + 16;
+  static constexpr size_t kSmem = kBytes + 1024;                          // + alignment slack
+  static_assert(kSmem <= 227 * 1024, "shared memory plan too large");
+};
+
+struct TcArgs {
+  ScoreShape sh;
+  float* scores;
+  float* page_scores;
+  float* lse;
+  float2* part;
+  DeviceError* err;
+};
+
+// Geometry of one work item.
+struct Item {
+  int b, ul, seg, layer, g;
+  int unit;            // global (sequence, layer, KV head) unit index
+  int L, n_keys;
+  int32_t q_row0;      // first Q row of the unit's group in the 2-D Q view
+  int32_t k_row0;      // first K row of the unit in the 2-D K view
+  int ta, tb;          // key range whose tiles are processed
+  int a0, a1;          // pass 2: prefix range whose scores are emitted
+};
+
+template <bool PASS2>
+__device__ __forceinline__ Item decode(const SeqTable& t, const ScoreShape& sh, int item) {
+  Item it;
+  it.b = find_seq(t, item);
+  const SeqInfo& si = t.s[it.b];
+  const int local = item - si.item0;
+  it.ul = local / si.n_seg;
+  it.seg = local % si.n_seg;
+  it.layer = it.ul / sh.h_kv;
+  it.g = it.ul % sh.h_kv;
+  it.unit = si.unit0 + it.ul;
+  it.L = si.L;
+  it.n_keys = si.n_keys;
+  it.q_row0 = (int32_t)((((int64_t)it.b * sh.n_layers + it.layer) * sh.h_q + (int64_t)it.g * sh.G) * sh.W);
+  it.k_row0 = (int32_t)(si.k_off / sh.d + ((int64_t)it.layer * sh.h_kv + it.g) * si.n_keys);
+  if (!PASS2) {
+    it.ta = it.seg * sh.seg1;
+    it.tb = min(si.n_keys, it.ta + sh.seg1);
+    it.a0 = it.a1 = 0;
+  } else {
+    const int pr = (sh.pool_k - 1) / 2;
+    it.a0 = it.seg * sh.seg2;
+    it.a1 = min(si.L, it.a0 + sh.seg2);
+    it.ta = max(0, it.a0 - pr);
+    it.tb = min(si.L, it.a1 + pr);
+  }
+  return it;
+}
+
+__device__ __forceinline__ int item_begin(int n_items) {
+  return (int)(((int64_t)blockIdx.x * n_items) / gridDim.x);
+}
+__device__ __forceinline__ int item_end(int n_items) {
+  return (int)(((int64_t)(blockIdx.x + 1) * n_items) / gridDim.x);
+}
+
+__device__ __forceinline__ bool aborted(const volatile uint32_t* flag) { return *flag != 0; }
+
+__device__ __forceinline__ void fail(const TcArgs& a, volatile uint32_t* flag, uint32_t where) {
+  set_device_error(a.err, KVSEL_ERR_TIMEOUT, where);
+  *flag = 1;
+}
+
+// ---------------------------------------------------------------- producer (one thread)
+template <bool PASS2, int RT, int D, int NK>
+__device__ void produce(const CUtensorMap* tq, const CUtensorMap* tk, const TcArgs& a, const SeqTable& t,
+                        uint32_t base, volatile uint32_t* flag) {
+  using P = Plan<RT, D, NK>;
+  const uint32_t bars = base + P::kBarOff;
+  auto full = [&](int s) { return bars + 8u * s; };
+  auto empty = [&](int s) { return bars + 8u * (NK + s); };
+  const uint32_t q_full = bars + 8u * (2 * NK + 2 * P::kNT);
+  const uint32_t q_empty = q_full + 8;
+  tma_prefetch_desc(tq);
+  tma_prefetch_desc(tk);
+  int ks = 0;
+  uint32_t kph = 0, qph = 0;
+  uint32_t n_fills = 0, n_q = 0;
+  int prev_unit = -1;
+  const int i1 = item_end(t.n_items);
+  for (int item = item_begin(t.n_items); item < i1 && !aborted(flag); ++item) {
+    const Item it = decode<PASS2>(t, a.sh, item);
+    if (it.unit != prev_unit) {
+      if (!mbar_wait(q_empty, qph ^ 1)) { fail(a, flag, kWhereProducer); break; }
+      mbar_expect_tx(q_full, P::kQBytes);
+#pragma unroll
+      for (int db = 0; db < P::kDBlocks; ++db)
+#pragma unroll
+        for (int m = 0; m < RT / 128; ++m)
+          tma_load_2d(base + P::kQOff + db * P::kQBlock + m * 16384, tq, db * 64, it.q_row0 + m * 128, q_full);
+      qph ^= 1;
+      ++n_q;
+      prev_unit = it.unit;
+    }
+    bool ok = true;
+    for (int t0 = it.ta; t0 < it.tb; t0 += kTileKeys) {
+      if (!mbar_wait(empty(ks), kph ^ 1)) { ok = false; break; }
+      mbar_expect_tx(full(ks), P::kKBytes);
+      const uint32_t dst = base + P::kKOff + ks * P::kKBytes;
+#pragma unroll
+      for (int db = 0; db < P::kDBlocks; ++db)
+        tma_load_2d(dst + db * P::kKBlock, tk, db * 64, it.k_row0 + t0, full(ks));
+      ++n_fills;
+      if (++ks == NK) { ks = 0; kph ^= 1; }
+    }
+    if (!ok) { fail(a, flag, kWhereProducer); break; }
+  }
+  // Loads still in flight (possible only after an abort) must land before the CTA exits:
+  // wait for the phase of each stage's last fill (returns at once when already complete).
+  for (int s = 0; s < NK; ++s) {
+    if (n_fills > (uint32_t)s) {
+      const uint32_t cnt = (n_fills - s + NK - 1) / NK;
+      if (!mbar_wait(full(s), (cnt - 1) & 1)) set_device_error(a.err, KVSEL_ERR_TIMEOUT, kWhereDrain);
+    }
+  }
+  if (n_q > 0 && !mbar_wait(q_full, (n_q - 1) & 1)) set_device_error(a.err, KVSEL_ERR_TIMEOUT, kWhereDrain);
+}
+
+// ---------------------------------------------------------------- MMA issuer (one thread)
+template <bool PASS2, int RT, int D, int NK>
+__device__ void issue_mma(const TcArgs& a, const SeqTable& t, uint32_t base, uint32_t tmem,
+                          volatile uint32_t* flag) {
+  using P = Plan<RT, D, NK>;
+  const uint32_t bars = base + P::kBarOff;
+  auto full = [&](int s) { return bars + 8u * s; };
+  auto empty = [&](int s) { return bars + 8u * (NK + s); };
+  auto tfull = [&](int s) { return bars + 8u * (2 * NK + s); };
+  auto tempty = [&](int s) { return bars + 8u * (2 * NK + P::kNT + s); };
+  const uint32_t q_full = bars + 8u * (2 * NK + 2 * P::kNT);
+  const uint32_t q_empty = q_full + 8;
+  const uint32_t drain = q_empty + 8;
+  // pass 1: M = 128 window rows (per M block), N = 128 keys;  pass 2: M = 128 keys, N = RT rows
+  constexpr uint32_t idesc = PASS2 ? umma_idesc_bf16(128, RT) : umma_idesc_bf16(128, 128);
+  int ks = 0, ts = 0;
+  uint32_t kph = 0, tph = 0, qph = 0;
+  int prev_unit = -1;
+  bool issued = false;
+  const int i1 = item_end(t.n_items);
+  for (int item = item_begin(t.n_items); item < i1 && !aborted(flag); ++item) {
+    const Item it = decode<PASS2>(t, a.sh, item);
+    if (it.unit != prev_unit) {
+      if (prev_unit >= 0) umma_commit(q_empty);     // previous unit's Q is free once its MMAs finish
+      if (!mbar_wait(q_full, qph)) { fail(a, flag, kWhereMma); break; }
+      qph ^= 1;
+      prev_unit = it.unit;
+    }
+    bool ok = true;
+    for (int t0 = it.ta; t0 < it.tb; t0 += kTileKeys) {
+      if (!mbar_wait(full(ks), kph) || !mbar_wait(tempty(ts), tph ^ 1)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t kbase = base + P::kKOff + ks * P::kKBytes;
+      const uint32_t qbase = base + P::kQOff;
+      const uint32_t d_tmem = tmem + ts * RT;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t db = kk >> 2, off = (kk & 3) * 32;
+        if (PASS2) {
+          umma_bf16(d_tmem, umma_desc_sw128(kbase + db * P::kKBlock + off),
+                    umma_desc_sw128(qbase + db * P::kQBlock + off), idesc, kk > 0);
+        } else {
+#pragma unroll
+          for (int m = 0; m < RT / 128; ++m)
+            umma_bf16(d_tmem + m * 128, umma_desc_sw128(qbase + db * P::kQBlock + m * 16384 + off),
+                      umma_desc_sw128(kbase + db * P::kKBlock + off), idesc, kk > 0);
+        }
+      }
+      issued = true;
+      umma_commit(empty(ks));     // K stage free once these MMAs have read it
+      umma_commit(tfull(ts));     // accumulator ready for the epilogue
+      if (++ks == NK) { ks = 0; kph ^= 1; }
+      if (++ts == (int)P::kNT) { ts = 0; tph ^= 1; }
+    }
+    if (!ok) { fail(a, flag, kWhereMma); break; }
+  }
+  // Every MMA issued must be complete before TMEM is released.
+  if (issued) {
+    umma_commit(drain);
+    if (!mbar_wait(drain, 0)) set_device_error(a.err, KVSEL_ERR_TIMEOUT, kWhereDrain);
+  }
+}
+
+// ---------------------------------------------------------------- epilogue helpers
+__device__ __forceinline__ void epi_sync() {
+  asm volatile("bar.sync %0, %1;" ::"r"(kEpiBarrier), "r"(kEpiThreads) : "memory");
+}
+
+__device__ __forceinline__ float fast_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Epilogue thread geometry: warps 2..9; warp w may read TMEM lanes 32*(w%4) .. +31.
+struct EpiThread {
+  int wg;        // epilogue warpgroup 0 / 1
+  int quarter;   // TMEM lane quarter
+  int lane;
+  int lrow;      // TMEM lane = quarter * 32 + lane
+  int etid;      // 0 .. kEpiThreads-1
+};
+
+__device__ __forceinline__ EpiThread epi_thread() {
+  EpiThread e;
+  const int warp = threadIdx.x / 32;
+  e.wg = (warp - 2) / 4;
+  e.quarter = warp % 4;
+  e.lane = threadIdx.x % 32;
+  e.lrow = e.quarter * 32 + e.lane;
+  e.etid = threadIdx.x - 64;
+  return e;
+}
+
+// ---------------------------------------------------------------- pass 1 epilogue
+// RT = 128: both warpgroups see all 128 rows, warpgroup e takes tile columns [64e, 64e + 64).
+// RT = 256: warpgroup e takes rows 128e .. 128e + 127 (its own accumulator), all 128 columns.
+template <int RT, int D, int NK>
+__device__ void epilogue_pass1(const TcArgs& a, const SeqTable& t, uint32_t base, uint8_t* sbase,
+                               uint32_t tmem, volatile uint32_t* flag) {
+  using P = Plan<RT, D, NK>;
+  constexpr int kChunks = RT == 256 ? 4 : 2;
+  constexpr int kCols = kChunks * 32;
+  const EpiThread e = epi_thread();
+  const uint32_t bars = base + P::kBarOff;
+  auto tfull = [&](int s) { return bars + 8u * (2 * NK + s); };
+  auto tempty = [&](int s) { return bars + 8u * (2 * NK + P::kNT + s); };
+  const int row = RT == 256 ? e.lrow + 128 * e.wg : e.lrow;
+  const uint32_t col0 = RT == 256 ? 128u * e.wg : 64u * e.wg;   // TMEM column within a stage
+  const int key0 = RT == 256 ? 0 : 64 * e.wg;                    // tile key of that column
+  float* red = reinterpret_cast<float*>(sbase + P::kRedOff);
+  const float scale = a.sh.scale_log2;
+  const bool rvalid = row < a.sh.R;
+  int ts = 0;
+  uint32_t tph = 0;
+  const int i1 = item_end(t.n_items);
+  for (int item = item_begin(t.n_items); item < i1; ++item) {
+    const Item it = decode<false>(t, a.sh, item);
+    const int row_last = it.L + (rvalid ? row % a.sh.W : 0);     // last key this row sees
+    const int vis_end = min(it.tb, row_last + 1);
+    float m = -INFINITY, l = 0.f;
+    for (int t0 = it.ta; t0 < it.tb; t0 += kTileKeys) {
+      float v[kChunks][32];
+      // the tensor-memory loads below are warp-collective: decide per warp
+      const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(tfull(ts), tph));
+      if (!ok && e.lane == 0) fail(a, flag, kWhereEpilogue);
+      if (ok) {
+        tc_fence_after();
+        const uint32_t taddr = tmem + ((uint32_t)(e.quarter * 32) << 16) + ts * RT + col0;
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) tmem_ld32(taddr + c * 32, v[c]);
+        tc_fence_before();
+        __syncwarp();
+        if (e.lane == 0) mbar_arrive(tempty(ts));
+        if (rvalid) {
+          const int nvis = vis_end - (t0 + key0);    // columns [0, nvis) of mine are visible
+          float mx = -INFINITY;
+          if (nvis >= kCols) {
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c)
+#pragma unroll
+              for (int i = 0; i < 32; ++i) mx = fmaxf(mx, v[c][i]);
+          } else {
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c)
+#pragma unroll
+              for (int i = 0; i < 32; ++i) mx = (c * 32 + i < nvis) ? fmaxf(mx, v[c][i]) : mx;
+          }
+          if (mx > -INFINITY) {
+            const float nm = fmaxf(m, mx * scale);
+            float acc = l * fast_ex2(m - nm);
+            if (nvis >= kCols) {
+#pragma unroll
+              for (int c = 0; c < kChunks; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) acc += fast_ex2(fmaf(v[c][i], scale, -nm));
+            } else {
+#pragma unroll
+              for (int c = 0; c < kChunks; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (c * 32 + i < nvis) acc += fast_ex2(fmaf(v[c][i], scale, -nm));
+            }
+            l = acc;
+            m = nm;
+          }
+        }
+      }
+      if (++ts == (int)P::kNT) { ts = 0; tph ^= 1; }
+    }
+    // per-row partial (m, l) of this segment
+    if (RT == 128) {
+      epi_sync();
+      if (e.wg == 1) {
+        red[2 * e.lrow] = m;
+        red[2 * e.lrow + 1] = l;
+      }
+      epi_sync();
+      if (e.wg == 0 && rvalid) {
+        const float m2 = red[2 * e.lrow], l2 = red[2 * e.lrow + 1];
+        const float M = fmaxf(m, m2);
+        float S = 0.f;
+        if (M > -INFINITY) S = (m > -INFINITY ? l * fast_ex2(m - M) : 0.f) + (m2 > -INFINITY ? l2 * fast_ex2(m2 - M) : 0.f);
+        a.part[(int64_t)item * a.sh.R + row] = make_float2(M, S);
+      }
+    } else if (rvalid) {
+      a.part[(int64_t)item * a.sh.R + row] = make_float2(m, l);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- pass 2 epilogue
+// Thread = key (TMEM lane); warpgroup e takes rows [e RT/2, (e+1) RT/2) (TMEM columns).
+// MAXW = 0: group sum (every row summed); otherwise group max with head width MAXW.
+template <int RT, int D, int NK, int MAXW>
+__device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base, uint8_t* sbase,
+                               uint32_t tmem, volatile uint32_t* flag) {
+  using P = Plan<RT, D, NK>;
+  constexpr int kHalf = RT / 2;
+  constexpr int kChunks = kHalf / 32;
+  const EpiThread e = epi_thread();
+  const uint32_t bars = base + P::kBarOff;
+  auto tfull = [&](int s) { return bars + 8u * (2 * NK + s); };
+  auto tempty = [&](int s) { return bars + 8u * (2 * NK + P::kNT + s); };
+  float* Ss = reinterpret_cast<float*>(sbase + P::kSsOff);
+  float* lse_s = reinterpret_cast<float*>(sbase + P::kLseOff);
+  const float scale = a.sh.scale_log2;
+  const int col0 = e.wg * kHalf;
+  const int pr = (a.sh.pool_k - 1) / 2;
+  const int P_ = a.sh.page_size;
+  int ts = 0;
+  uint32_t tph = 0;
+  const int i1 = item_end(t.n_items);
+  for (int item = item_begin(t.n_items); item < i1; ++item) {
+    const Item it = decode<true>(t, a.sh, item);
+    epi_sync();                                          // readers of the previous item are done
+    for (int i = e.etid; i < it.tb - it.ta; i += kEpiThreads) Ss[i] = 0.f;
+    for (int i = e.etid; i < RT; i += kEpiThreads)
+      lse_s[i] = i < a.sh.R ? a.lse[(int64_t)it.unit * a.sh.R + i] : INFINITY;   // padding rows give p = 0
+    epi_sync();
+    for (int t0 = it.ta; t0 < it.tb; t0 += kTileKeys) {
+      float v[kChunks][32];
+      // the tensor-memory loads below are warp-collective: decide per warp
+      const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(tfull(ts), tph));
+      if (!ok && e.lane == 0) fail(a, flag, kWhereEpilogue);
+      if (ok) {
+        tc_fence_after();
+        const uint32_t taddr = tmem + ((uint32_t)(e.quarter * 32) << 16) + ts * RT + col0;
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) tmem_ld32(taddr + c * 32, v[c]);
+        tc_fence_before();
+        __syncwarp();
+        if (e.lane == 0) mbar_arrive(tempty(ts));
+        float red = 0.f;
+        if constexpr (MAXW == 0) {
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) red += fast_ex2(fmaf(v[c][i], scale, -lse_s[col0 + c * 32 + i]));
+        } else if constexpr (MAXW >= 32) {
+#pragma unroll
+          for (int h = 0; h < kHalf / MAXW; ++h) {
+            float hs = 0.f;
+#pragma unroll
+            for (int c = h * (MAXW / 32); c < (h + 1) * (MAXW / 32); ++c)
+#pragma unroll
+              for (int i = 0; i < 32; ++i) hs += fast_ex2(fmaf(v[c][i], scale, -lse_s[col0 + c * 32 + i]));
+            red = fmaxf(red, hs);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c)
+#pragma unroll
+            for (int h = 0; h < 32 / MAXW; ++h) {
+              float hs = 0.f;
+#pragma unroll
+              for (int i = h * MAXW; i < (h + 1) * MAXW; ++i)
+                hs += fast_ex2(fmaf(v[c][i], scale, -lse_s[col0 + c * 32 + i]));
+              red = fmaxf(red, hs);
+            }
+        }
+        const int key = t0 + e.lrow;
+        if (key < it.tb) {
+          // two addends per key (one per warpgroup): the result does not depend on their order
+          if constexpr (MAXW == 0) atomicAdd(&Ss[key - it.ta], red);
+          else atomicMax(reinterpret_cast<int*>(&Ss[key - it.ta]), __float_as_int(red));
+        }
+      }
+      if (++ts == (int)P::kNT) { ts = 0; tph ^= 1; }
+    }
+    epi_sync();
+    if (aborted(flag)) continue;
+    // max-pool over prefix positions, then page reduce (DELTA key designs 2-3)
+    const SeqInfo& si = t.s[it.b];
+    float* out = a.scores + si.s_off + ((int64_t)it.layer * a.sh.h_kv + it.g) * it.L;
+    auto pooled = [&](int tt) {
+      const int lo = max(tt - pr, it.ta), hi = min(tt + pr, it.tb - 1);
+      float u = Ss[lo - it.ta];
+      for (int x = lo + 1; x <= hi; ++x) u = fmaxf(u, Ss[x - it.ta]);
+      return u;
+    };
+    if (P_ == 1) {
+      for (int tt = it.a0 + e.etid; tt < it.a1; tt += kEpiThreads) out[tt] = pooled(tt);
+    } else {
+      const int n_pages = (it.L + P_ - 1) / P_;
+      float* pout = a.page_scores + si.p_off + ((int64_t)it.layer * a.sh.h_kv + it.g) * n_pages;
+      for (int p = it.a0 / P_ + e.etid; p * P_ < it.a1; p += kEpiThreads) {
+        const int lo = p * P_, hi = min(it.a1, lo + P_);
+        float pv = 0.f;
+        for (int tt = lo; tt < hi; ++tt) {
+          const float u = pooled(tt);
+          out[tt] = u;
+          pv = (tt == lo) ? u : (a.sh.page_reduce == KVSEL_REDUCE_MAX ? fmaxf(pv, u) : pv + u);
+        }
+        pout[p] = pv;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- kernels
+template <bool PASS2, int RT, int D, int NK, int MAXW>
+__global__ void __launch_bounds__(kThreadsTc, 1) score_tc_kernel(const __grid_constant__ CUtensorMap tq,
+                                                                 const __grid_constant__ CUtensorMap tk,
+                                                                 const __grid_constant__ TcArgs a,
+                                                                 const __grid_constant__ SeqTable t) {
+  using P = Plan<RT, D, NK>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t base = smem_addr(sbase);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sbase + P::kMiscOff);
+  volatile uint32_t* flag = reinterpret_cast<volatile uint32_t*>(sbase + P::kMiscOff + 4);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    const uint32_t bars = base + P::kBarOff;
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(bars + 8u * s, 1);                     // full: producer arrival + TMA bytes
+      mbar_init(bars + 8u * (NK + s), 1);              // empty: MMA commit
+    }
+    for (uint32_t s = 0; s < P::kNT; ++s) {
+      mbar_init(bars + 8u * (2 * NK + s), 1);          // tfull: MMA commit
+      mbar_init(bars + 8u * (2 * NK + P::kNT + s), kEpiWarps);   // tempty: one arrival per epilogue warp
+    }
+    for (int s = 0; s < 3; ++s) mbar_init(bars + 8u * (2 * NK + 2 * P::kNT + s), 1);   // q_full, q_empty, drain
+    *flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(smem_addr(tslot), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  if (warp == 0) {
+    if (lane == 0) produce<PASS2, RT, D, NK>(&tq, &tk, a, t, base, flag);
+  } else if (warp == 1) {
+    if (lane == 0) issue_mma<PASS2, RT, D, NK>(a, t, base, tmem, flag);
+  } else if (PASS2) {
+    epilogue_pass2<RT, D, NK, MAXW>(a, t, base, sbase, tmem, flag);
+  } else {
+    epilogue_pass1<RT, D, NK>(a, t, base, sbase, tmem, flag);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D view [rows][D] bf16, boxes of 64 x 128 with 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int D) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct DevInfo {
+  int sms = 0;
+  int major = 0;
+};
+
+DevInfo device_info() {
+  static std::mutex mu;
+  static DevInfo cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DevInfo{};
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache[dev].sms == 0) {
+    cudaDeviceGetAttribute(&cache[dev].sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&cache[dev].major, cudaDevAttrComputeCapabilityMajor, dev);
+  }
+  return cache[dev];
+}
+
+template <bool PASS2, int RT, int D, int NK, int MAXW>
+kvsel_status launch_one(const char* name, const CUtensorMap& tq, const CUtensorMap& tk, const TcArgs& a,
+                        const SeqTable& t, int sms, cudaStream_t s) {
+  using P = Plan<RT, D, NK>;
+  auto kern = score_tc_kernel<PASS2, RT, D, NK, MAXW>;
+  if (set_smem((const void*)kern, P::kSmem) != cudaSuccess) return KVSEL_ERR_CUDA;
+  const int grid = t.n_items < sms ? t.n_items : sms;
+  TraceScope ts(name, s);
+  kern<<<grid, kThreadsTc, P::kSmem, s>>>(tq, tk, a, t);
+  return launch_status();
+}
+
+template <int RT, int D>
+kvsel_status run_tc(const TcArgs& a, const SeqTable& t1, const SeqTable& t2, const CUtensorMap& tq,
+                    const CUtensorMap& tk, int sms, cudaStream_t s) {
+  constexpr int NK = (RT == 256 && D == 128) ? 3 : 4;
+  kvsel_status st = launch_one<false, RT, D, NK, 0>("score_pass1_tc", tq, tk, a, t1, sms, s);
+  if (st != KVSEL_OK) return st;
+  if ((st = launch_lse_combine(a.sh, t1, a.part, a.lse, s)) != KVSEL_OK) return st;
+  if (a.sh.group_reduce == KVSEL_REDUCE_SUM) return launch_one<true, RT, D, NK, 0>("score_pass2_tc", tq, tk, a, t2, sms, s);
+  switch (a.sh.W) {
+    case 8: return launch_one<true, RT, D, NK, 8>("score_pass2_tc", tq, tk, a, t2, sms, s);
+    case 16: return launch_one<true, RT, D, NK, 16>("score_pass2_tc", tq, tk, a, t2, sms, s);
+    case 32: return launch_one<true, RT, D, NK, 32>("score_pass2_tc", tq, tk, a, t2, sms, s);
+    case 64: return launch_one<true, RT, D, NK, 64>("score_pass2_tc", tq, tk, a, t2, sms, s);
+  }
+  return KVSEL_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+kvsel_status launch_score(const ScoreShape& sh_in, const SeqTable& base, const void* q, const void* k,
+                          float* scores, float* page_scores, float* lse, float2* part, DeviceError* err,
+                          cudaStream_t s) {
+  ScoreShape sh = sh_in;
+  const int64_t ups = (int64_t)sh.n_layers * sh.h_kv;
+  int64_t k_rows = 0;
+  for (int b = 0; b < base.batch; ++b) k_rows += ups * base.s[b].n_keys;
+  const int64_t q_rows = (int64_t)base.batch * sh.n_layers * sh.h_q * sh.W;
+  const DevInfo dev = device_info();
+  const bool w_ok = sh.group_reduce == KVSEL_REDUCE_SUM ||
+                    (sh.W == 8 || sh.W == 16 || sh.W == 32 || sh.W == 64);
+  const bool tc = dev.major == 10 && dev.sms > 0 && sh.R <= 256 && w_ok && k_rows + 256 < (int64_t(1) << 31) &&
+                  q_rows + 256 < (int64_t(1) << 31) && encode_fn() != nullptr;
+  sh.seg1 = (int32_t)kScoreSeg1;
+  const SeqTable t1 = with_items(base, ups, kScoreSeg1, true, sh.W);
+  if (!tc) {
+    sh.seg2 = (int32_t)(sh.page_size * ((1024 + sh.page_size - 1) / sh.page_size));
+    const SeqTable t2 = with_items(base, ups, sh.seg2, false, sh.W);
+    return launch_score_simt(sh, t1, t2, q, k, scores, page_scores, lse, part, err, s);
+  }
+  sh.seg2 = (int32_t)(sh.page_size * (kSeg2Max / sh.page_size));
+  const SeqTable t2 = with_items(base, ups, sh.seg2, false, sh.W);
+  CUtensorMap tq, tk;
+  if (!make_map(&tq, q, q_rows, sh.d) || !make_map(&tk, k, k_rows, sh.d)) return KVSEL_ERR_CUDA;
+  TcArgs a;
+  a.sh = sh;
+  a.scores = scores;
+  a.page_scores = page_scores;
+  a.lse = lse;
+  a.part = part;
+  a.err = err;
+  if (sh.R <= 128) return sh.d == 64 ? run_tc<128, 64>(a, t1, t2, tq, tk, dev.sms, s)
+                                     : run_tc<128, 128>(a, t1, t2, tq, tk, dev.sms, s);
+  return sh.d == 64 ? run_tc<256, 64>(a, t1, t2, tq, tk, dev.sms, s) : run_tc<256, 128>(a, t1, t2, tq, tk, dev.sms, s);
+}
+
+}  // namespace kvsel
