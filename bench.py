@@ -38,6 +38,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="kvsel", choices=["kvsel", "reference"])
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--layers", type=int, default=0,
+                   help="run only this many layers of the workload (small cases for profiler captures)")
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--cpu-units", type=int, default=0,
                    help="(layer, KV head) units in the CPU-baseline sample (default: one per host core)")
@@ -157,9 +159,11 @@ def kernel_bytes(w, n_sel_rows):
     sel_read = page_w if P > 1 else score_w
     idx_w = w.batch * w.n_layers * w.h_kv * w.n_sel() * 4
     gather = 2 * 2 * w.batch * w.n_layers * w.h_kv * n_sel_rows * d * 2
+    pass1 = k_all + q_bytes
+    pass2 = k_prefix + q_bytes + score_w + page_w
     return {
-        "score_pass1_simt": k_all + q_bytes,
-        "score_pass2_simt": k_prefix + q_bytes + score_w + page_w,
+        "score_pass1_simt": pass1, "score_pass1_tc": pass1,
+        "score_pass2_simt": pass2, "score_pass2_tc": pass2,
         "topk_radix": sel_read + idx_w,
         "kv_compact": gather + idx_w,
     }
@@ -222,6 +226,8 @@ def run_kvsel(args):
 
     rank, world, local = dist_setup()
     w = S.by_name(args.workload)
+    if args.layers:
+        w = w.with_(n_layers=args.layers)
     n_cpu_units = args.cpu_units or (os.cpu_count() or 1)
     cores = min(os.cpu_count() or 1, n_cpu_units)
     pool = make_pool(cores) if (rank == 0 and world == 1 and not args.no_cpu) else None  # before any GPU call
