@@ -531,6 +531,519 @@ __global__ void __launch_bounds__(kThreadsTc, 1) score_tc_kernel(const __grid_co
   }
 }
 
+// ================================================================ single-read (fused) scoring
+//
+// The CTAs form groups of gs; group q takes units q, q + n_groups, ...  Every
+// unit is split across the gs CTAs of its group.  In step s a CTA runs pass 1
+// over its share of unit U[s] (reading K from HBM) and then pass 2 over its
+// share of unit U[s-1], whose keys the group read one step earlier and which
+// are still in L2, so each key row crosses HBM once.  The row log-sum-exp of a
+// unit needs every CTA of the group: each CTA writes its per-row partial
+// (max, sum) into a ring slot and counts itself in; the last one to arrive
+// merges the gs partials and publishes the unit's log-sum-exp.  Between a
+// unit's pass 1 and its pass 2 every CTA has the next unit's pass 1 to do, so
+// the merge is off the critical path.  The launch is cooperative (all CTAs
+// resident), and every cross-CTA wait is bounded.
+constexpr int kFusedSsMax = 4096;   // prefix keys (+ halo) of one CTA's pass-2 share
+
+template <int D, int NK>
+struct FPlan {
+  static constexpr int RT = 128;
+  static constexpr int kDBlocks = D / 64;
+  static constexpr uint32_t kQBlock = RT * 128;
+  static constexpr uint32_t kQBytes = kQBlock * kDBlocks;
+  static constexpr uint32_t kKBlock = kTileKeys * 128;
+  static constexpr uint32_t kKBytes = kKBlock * kDBlocks;
+  static constexpr int kQSlots = 3;                                      // Q of units s, s-1 and s+1
+  static constexpr uint32_t kQOff = 0;
+  static constexpr uint32_t kKOff = kQSlots * kQBytes;
+  static constexpr uint32_t kSsOff = kKOff + NK * kKBytes;
+  static constexpr uint32_t kSsFloats = kFusedSsMax + 192;
+  static constexpr uint32_t kLseOff = kSsOff + kSsFloats * 4;
+  static constexpr uint32_t kRedOff = kLseOff + RT * 4;
+  static constexpr uint32_t kNT = kTmemCols / RT;
+  static constexpr uint32_t kBarOff = kRedOff + 128 * 8;
+  // full[NK], empty[NK], tfull[NT], tempty[NT], q_full[3], q_empty[3], drain
+  static constexpr uint32_t kNumBars = 2 * NK + 2 * kNT + 2 * kQSlots + 1;
+  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;           // tmem slot, abort flag, last flag
+  static constexpr uint32_t kBytes = kMiscOff + 16;
+  static constexpr size_t kSmem = kBytes + 1024;
+  static_assert(kSmem <= 227 * 1024, "shared memory plan too large");
+  __device__ static uint32_t full(uint32_t bars, int s) { return bars + 8u * s; }
+  __device__ static uint32_t empty(uint32_t bars, int s) { return bars + 8u * (NK + s); }
+  __device__ static uint32_t tfull(uint32_t bars, int s) { return bars + 8u * (2 * NK + s); }
+  __device__ static uint32_t tempty(uint32_t bars, int s) { return bars + 8u * (2 * NK + kNT + s); }
+  __device__ static uint32_t qfull(uint32_t bars, int q) { return bars + 8u * (2 * NK + 2 * kNT + q); }
+  __device__ static uint32_t qempty(uint32_t bars, int q) { return bars + 8u * (2 * NK + 2 * kNT + kQSlots + q); }
+  __device__ static uint32_t drain(uint32_t bars) { return bars + 8u * (2 * NK + 2 * kNT + 2 * kQSlots); }
+};
+
+struct FusedArgs {
+  ScoreShape sh;
+  float* scores;
+  float* page_scores;
+  DeviceError* err;
+  float2* part_ring;   // [n_groups][kFusedSlots][gs][R]
+  float* lse_ring;     // [n_groups][kFusedSlots][R]
+  uint32_t* arrive;    // [n_groups][kFusedSlots]
+  uint32_t* ready;     // [n_groups][kFusedSlots]
+  int32_t gs, n_groups, n_units;
+};
+
+// One CTA's share of one unit.
+struct Share {
+  int b, layer, g, unit, L, n_keys;
+  int32_t q_row0, k_row0;
+  int ta1, tb1;          // pass-1 keys [ta1, tb1) (prefix and window)
+  int a0, a1;            // pass-2 prefix keys whose scores this CTA emits
+  int ta2, tb2;          // pass-2 keys computed, with the pooling halo
+};
+
+__device__ __forceinline__ void fail_f(const FusedArgs& a, volatile uint32_t* flag, uint32_t where) {
+  set_device_error(a.err, KVSEL_ERR_TIMEOUT, where);
+  *flag = 1;
+}
+
+__device__ __forceinline__ int group_of_cta(const FusedArgs& a) { return blockIdx.x / a.gs; }
+__device__ __forceinline__ int rank_in_group(const FusedArgs& a) { return blockIdx.x % a.gs; }
+__device__ __forceinline__ int units_of_group(const FusedArgs& a, int q) {
+  return q < a.n_units ? (a.n_units - q + a.n_groups - 1) / a.n_groups : 0;
+}
+
+__device__ __forceinline__ Share share_of(const FusedArgs& a, const SeqTable& t, int q, int s) {
+  const ScoreShape& sh = a.sh;
+  Share x;
+  x.unit = q + s * a.n_groups;
+  const int ups = sh.n_layers * sh.h_kv;
+  x.b = x.unit / ups;
+  const int ul = x.unit % ups;
+  x.layer = ul / sh.h_kv;
+  x.g = ul % sh.h_kv;
+  const SeqInfo& si = t.s[x.b];
+  x.L = si.L;
+  x.n_keys = si.n_keys;
+  x.q_row0 = (int32_t)((((int64_t)x.b * sh.n_layers + x.layer) * sh.h_q + (int64_t)x.g * sh.G) * sh.W);
+  x.k_row0 = (int32_t)(si.k_off / sh.d + ((int64_t)x.layer * sh.h_kv + x.g) * si.n_keys);
+  const int r = rank_in_group(a), gs = a.gs;
+  x.ta1 = (int)(((int64_t)r * x.n_keys) / gs);
+  x.tb1 = (int)(((int64_t)(r + 1) * x.n_keys) / gs);
+  const int P = sh.page_size, pr = (sh.pool_k - 1) / 2;
+  const int n_pages = (x.L + P - 1) / P;
+  x.a0 = (int)min((int64_t)x.L, (int64_t)P * (((int64_t)r * n_pages) / gs));
+  x.a1 = (int)min((int64_t)x.L, (int64_t)P * (((int64_t)(r + 1) * n_pages) / gs));
+  if (x.a1 > x.a0) {
+    x.ta2 = max(0, x.a0 - pr);
+    x.tb2 = min(x.L, x.a1 + pr);
+  } else {
+    x.ta2 = x.tb2 = 0;
+  }
+  return x;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ bool wait_at_least(const uint32_t* p, uint32_t target) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (ld_acquire(p) >= target) return true;
+    __nanosleep(128);
+  }
+  return false;
+}
+
+// ---------------------------------------------------------------- fused producer
+template <int D, int NK>
+__device__ void fused_produce(const CUtensorMap* tq, const CUtensorMap* tk, const FusedArgs& a, const SeqTable& t,
+                              uint32_t base, volatile uint32_t* flag) {
+  using P = FPlan<D, NK>;
+  const uint32_t bars = base + P::kBarOff;
+  tma_prefetch_desc(tq);
+  tma_prefetch_desc(tk);
+  const int q = group_of_cta(a);
+  const int nu = units_of_group(a, q);
+  int ks = 0;
+  uint32_t kph = 0, n_fills = 0;
+  uint32_t qph[P::kQSlots] = {0, 0, 0}, n_q[P::kQSlots] = {0, 0, 0};
+  bool ok = true;
+  for (int s = 0; s <= nu && ok && !aborted(flag); ++s) {
+    for (int pass = 0; pass < 2 && ok; ++pass) {
+      if ((pass == 0 && s == nu) || (pass == 1 && s == 0)) continue;
+      const Share x = share_of(a, t, q, pass == 0 ? s : s - 1);
+      if (pass == 0) {
+        const int qs = s % P::kQSlots;
+        if (!mbar_wait(P::qempty(bars, qs), qph[qs] ^ 1)) { ok = false; break; }
+        mbar_expect_tx(P::qfull(bars, qs), P::kQBytes);
+#pragma unroll
+        for (int db = 0; db < P::kDBlocks; ++db)
+          tma_load_2d(base + P::kQOff + qs * P::kQBytes + db * P::kQBlock, tq, db * 64, x.q_row0, P::qfull(bars, qs));
+        qph[qs] ^= 1;
+        ++n_q[qs];
+      }
+      const int ta = pass == 0 ? x.ta1 : x.ta2, tb = pass == 0 ? x.tb1 : x.tb2;
+      for (int t0 = ta; t0 < tb; t0 += kTileKeys) {
+        if (!mbar_wait(P::empty(bars, ks), kph ^ 1)) { ok = false; break; }
+        mbar_expect_tx(P::full(bars, ks), P::kKBytes);
+        const uint32_t dst = base + P::kKOff + ks * P::kKBytes;
+#pragma unroll
+        for (int db = 0; db < P::kDBlocks; ++db)
+          tma_load_2d(dst + db * P::kKBlock, tk, db * 64, x.k_row0 + t0, P::full(bars, ks));
+        ++n_fills;
+        if (++ks == NK) { ks = 0; kph ^= 1; }
+      }
+    }
+  }
+  if (!ok) fail_f(a, flag, kWhereProducer);
+  for (int s = 0; s < NK; ++s)
+    if (n_fills > (uint32_t)s) {
+      const uint32_t cnt = (n_fills - s + NK - 1) / NK;
+      if (!mbar_wait(P::full(bars, s), (cnt - 1) & 1)) set_device_error(a.err, KVSEL_ERR_TIMEOUT, kWhereDrain);
+    }
+  for (int qs = 0; qs < P::kQSlots; ++qs)
+    if (n_q[qs] > 0 && !mbar_wait(P::qfull(bars, qs), (n_q[qs] - 1) & 1))
+      set_device_error(a.err, KVSEL_ERR_TIMEOUT, kWhereDrain);
+}
+
+// ---------------------------------------------------------------- fused MMA issuer
+template <int D, int NK>
+__device__ void fused_mma(const FusedArgs& a, const SeqTable& t, uint32_t base, uint32_t tmem, volatile uint32_t* flag) {
+  using P = FPlan<D, NK>;
+  constexpr int RT = P::RT;
+  const uint32_t bars = base + P::kBarOff;
+  constexpr uint32_t idesc1 = umma_idesc_bf16(128, 128);   // rows x keys
+  constexpr uint32_t idesc2 = umma_idesc_bf16(128, RT);    // keys x rows
+  const int q = group_of_cta(a);
+  const int nu = units_of_group(a, q);
+  int ks = 0, ts = 0;
+  uint32_t kph = 0, tph = 0;
+  uint32_t qph[P::kQSlots] = {0, 0, 0};
+  bool ok = true, issued = false;
+  for (int s = 0; s <= nu && ok && !aborted(flag); ++s) {
+    for (int pass = 0; pass < 2 && ok; ++pass) {
+      if ((pass == 0 && s == nu) || (pass == 1 && s == 0)) continue;
+      const Share x = share_of(a, t, q, pass == 0 ? s : s - 1);
+      const int qs = (pass == 0 ? s : s - 1) % P::kQSlots;
+      if (pass == 0) {
+        if (!mbar_wait(P::qfull(bars, qs), qph[qs])) { ok = false; break; }
+        qph[qs] ^= 1;
+      }
+      const uint32_t qbase = base + P::kQOff + qs * P::kQBytes;
+      const int ta = pass == 0 ? x.ta1 : x.ta2, tb = pass == 0 ? x.tb1 : x.tb2;
+      for (int t0 = ta; t0 < tb; t0 += kTileKeys) {
+        if (!mbar_wait(P::full(bars, ks), kph) || !mbar_wait(P::tempty(bars, ts), tph ^ 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t kbase = base + P::kKOff + ks * P::kKBytes;
+        const uint32_t d_tmem = tmem + ts * RT;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t db = kk >> 2, off = (kk & 3) * 32;
+          if (pass == 0)
+            umma_bf16(d_tmem, umma_desc_sw128(qbase + db * P::kQBlock + off),
+                      umma_desc_sw128(kbase + db * P::kKBlock + off), idesc1, kk > 0);
+          else
+            umma_bf16(d_tmem, umma_desc_sw128(kbase + db * P::kKBlock + off),
+                      umma_desc_sw128(qbase + db * P::kQBlock + off), idesc2, kk > 0);
+        }
+        issued = true;
+        umma_commit(P::empty(bars, ks));
+        umma_commit(P::tfull(bars, ts));
+        if (++ks == NK) { ks = 0; kph ^= 1; }
+        if (++ts == (int)P::kNT) { ts = 0; tph ^= 1; }
+      }
+      if (pass == 1) umma_commit(P::qempty(bars, qs));   // this Q slot is free once these MMAs finish
+    }
+  }
+  if (!ok) fail_f(a, flag, kWhereMma);
+  if (issued) {
+    umma_commit(P::drain(bars));
+    if (!mbar_wait(P::drain(bars), 0)) set_device_error(a.err, KVSEL_ERR_TIMEOUT, kWhereDrain);
+  }
+}
+
+// ---------------------------------------------------------------- fused epilogue
+// Merge of one unit's gs partials by the last CTA to arrive: warp per row, lanes over CTAs.
+__device__ void merge_unit_lse(const FusedArgs& a, int q, int slot, int etid) {
+  const int R = a.sh.R;
+  const int ew = etid / 32, lane = etid % 32;
+  const float2* part = a.part_ring + ((size_t)q * kFusedSlots + slot) * a.gs * R;
+  float* lse = a.lse_ring + ((size_t)q * kFusedSlots + slot) * R;
+  for (int r = ew; r < R; r += kEpiWarps) {
+    float m = -INFINITY, l = 0.f;
+    for (int c = lane; c < a.gs; c += 32) {
+      const float2 p = __ldcg(part + (size_t)c * R + r);
+      if (p.x > -INFINITY) {
+        const float nm = fmaxf(m, p.x);
+        l = l * exp2f(m - nm) + p.y * exp2f(p.x - nm);
+        m = nm;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+      const float nm = fmaxf(m, m2);
+      if (nm > -INFINITY) {
+        l = (m > -INFINITY ? l * exp2f(m - nm) : 0.f) + (m2 > -INFINITY ? l2 * exp2f(m2 - nm) : 0.f);
+        m = nm;
+      }
+    }
+    if (lane == 0) lse[r] = m + log2f(l);
+  }
+}
+
+template <int D, int NK, int MAXW>
+__device__ void fused_epilogue(const FusedArgs& a, const SeqTable& t, uint32_t base, uint8_t* sbase, uint32_t tmem,
+                               volatile uint32_t* flag) {
+  using P = FPlan<D, NK>;
+  constexpr int RT = P::RT;
+  const uint32_t bars = base + P::kBarOff;
+  const EpiThread e = epi_thread();
+  float* Ss = reinterpret_cast<float*>(sbase + P::kSsOff);
+  float* lse_s = reinterpret_cast<float*>(sbase + P::kLseOff);
+  float* red = reinterpret_cast<float*>(sbase + P::kRedOff);
+  volatile uint32_t* last_flag = reinterpret_cast<volatile uint32_t*>(sbase + P::kMiscOff + 8);
+  const float scale = a.sh.scale_log2;
+  const int R = a.sh.R;
+  const int q = group_of_cta(a), rank = rank_in_group(a);
+  const int nu = units_of_group(a, q);
+  const int pr = (a.sh.pool_k - 1) / 2;
+  const int Pg = a.sh.page_size;
+  int ts = 0;
+  uint32_t tph = 0;
+  for (int s = 0; s <= nu; ++s) {
+    // ------------------------------------------------ pass 1 of unit s
+    if (s < nu) {
+      const Share x = share_of(a, t, q, s);
+      const bool rvalid = e.lrow < R;
+      const int vis_end = min(x.tb1, x.L + (rvalid ? e.lrow % a.sh.W : 0) + 1);
+      const int key0 = 64 * e.wg;
+      float m = -INFINITY, l = 0.f;
+      for (int t0 = x.ta1; t0 < x.tb1; t0 += kTileKeys) {
+        float v[2][32];
+        const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(P::tfull(bars, ts), tph));
+        if (!ok && e.lane == 0) fail_f(a, flag, kWhereEpilogue);
+        if (ok) {
+          tc_fence_after();
+          const uint32_t taddr = tmem + ((uint32_t)(e.quarter * 32) << 16) + ts * RT + key0;
+          tmem_ld32(taddr, v[0]);
+          tmem_ld32(taddr + 32, v[1]);
+          tc_fence_before();
+          __syncwarp();
+          if (e.lane == 0) mbar_arrive(P::tempty(bars, ts));
+          if (rvalid) {
+            const int nvis = vis_end - (t0 + key0);
+            float mx = -INFINITY;
+            if (nvis >= 64) {
+#pragma unroll
+              for (int c = 0; c < 2; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, v[c][i]);
+            } else {
+#pragma unroll
+              for (int c = 0; c < 2; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) mx = (c * 32 + i < nvis) ? fmaxf(mx, v[c][i]) : mx;
+            }
+            if (mx > -INFINITY) {
+              const float nm = fmaxf(m, mx * scale);
+              float acc = l * fast_ex2(m - nm);
+              if (nvis >= 64) {
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+#pragma unroll
+                  for (int i = 0; i < 32; ++i) acc += fast_ex2(fmaf(v[c][i], scale, -nm));
+              } else {
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+#pragma unroll
+                  for (int i = 0; i < 32; ++i)
+                    if (c * 32 + i < nvis) acc += fast_ex2(fmaf(v[c][i], scale, -nm));
+              }
+              l = acc;
+              m = nm;
+            }
+          }
+        }
+        if (++ts == (int)P::kNT) { ts = 0; tph ^= 1; }
+      }
+      // this CTA's partial (max, sum) per row of unit s, then count in
+      const int slot = s % kFusedSlots;
+      const uint32_t use = (uint32_t)(s / kFusedSlots);
+      epi_sync();
+      if (e.wg == 1) {
+        red[2 * e.lrow] = m;
+        red[2 * e.lrow + 1] = l;
+      }
+      epi_sync();
+      if (e.wg == 0 && rvalid) {
+        const float m2 = red[2 * e.lrow], l2 = red[2 * e.lrow + 1];
+        const float M = fmaxf(m, m2);
+        float S = 0.f;
+        if (M > -INFINITY)
+          S = (m > -INFINITY ? l * fast_ex2(m - M) : 0.f) + (m2 > -INFINITY ? l2 * fast_ex2(m2 - M) : 0.f);
+        a.part_ring[(((size_t)q * kFusedSlots + slot) * a.gs + rank) * R + e.lrow] = make_float2(M, S);
+      }
+      epi_sync();
+      if (e.etid == 0) {
+        __threadfence();
+        const uint32_t old = atomicAdd(&a.arrive[q * kFusedSlots + slot], 1u);
+        *last_flag = (old + 1 == (uint32_t)a.gs * (use + 1)) ? 1u : 0u;
+      }
+      epi_sync();
+      if (*last_flag) {
+        __threadfence();
+        merge_unit_lse(a, q, slot, e.etid);
+        epi_sync();
+        if (e.etid == 0) {
+          __threadfence();
+          atomicExch(&a.ready[q * kFusedSlots + slot], use + 1);
+        }
+      }
+    }
+    // ------------------------------------------------ pass 2 of unit s - 1
+    if (s >= 1) {
+      const Share x = share_of(a, t, q, s - 1);
+      const int slot = (s - 1) % kFusedSlots;
+      const uint32_t use = (uint32_t)((s - 1) / kFusedSlots);
+      if (e.etid == 0 && !aborted(flag) && !wait_at_least(&a.ready[q * kFusedSlots + slot], use + 1))
+        fail_f(a, flag, kWhereEpilogue);
+      epi_sync();
+      for (int i = e.etid; i < x.tb2 - x.ta2; i += kEpiThreads) Ss[i] = 0.f;
+      for (int i = e.etid; i < RT; i += kEpiThreads)
+        lse_s[i] = i < R ? __ldcg(a.lse_ring + ((size_t)q * kFusedSlots + slot) * R + i) : INFINITY;
+      epi_sync();
+      const int col0 = e.wg * (RT / 2);
+      for (int t0 = x.ta2; t0 < x.tb2; t0 += kTileKeys) {
+        float v[2][32];
+        const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(P::tfull(bars, ts), tph));
+        if (!ok && e.lane == 0) fail_f(a, flag, kWhereEpilogue);
+        if (ok) {
+          tc_fence_after();
+          const uint32_t taddr = tmem + ((uint32_t)(e.quarter * 32) << 16) + ts * RT + col0;
+          tmem_ld32(taddr, v[0]);
+          tmem_ld32(taddr + 32, v[1]);
+          tc_fence_before();
+          __syncwarp();
+          if (e.lane == 0) mbar_arrive(P::tempty(bars, ts));
+          float redv = 0.f;
+          if constexpr (MAXW == 0) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+              for (int i = 0; i < 32; ++i) redv += fast_ex2(fmaf(v[c][i], scale, -lse_s[col0 + c * 32 + i]));
+          } else if constexpr (MAXW >= 32) {
+#pragma unroll
+            for (int h = 0; h < 64 / MAXW; ++h) {
+              float hs = 0.f;
+#pragma unroll
+              for (int c = h * (MAXW / 32); c < (h + 1) * (MAXW / 32); ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) hs += fast_ex2(fmaf(v[c][i], scale, -lse_s[col0 + c * 32 + i]));
+              redv = fmaxf(redv, hs);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+              for (int h = 0; h < 32 / MAXW; ++h) {
+                float hs = 0.f;
+#pragma unroll
+                for (int i = h * MAXW; i < (h + 1) * MAXW; ++i)
+                  hs += fast_ex2(fmaf(v[c][i], scale, -lse_s[col0 + c * 32 + i]));
+                redv = fmaxf(redv, hs);
+              }
+          }
+          const int key = t0 + e.lrow;
+          if (key < x.tb2) {
+            if constexpr (MAXW == 0) atomicAdd(&Ss[key - x.ta2], redv);
+            else atomicMax(reinterpret_cast<int*>(&Ss[key - x.ta2]), __float_as_int(redv));
+          }
+        }
+        if (++ts == (int)P::kNT) { ts = 0; tph ^= 1; }
+      }
+      epi_sync();
+      if (!aborted(flag) && x.a1 > x.a0) {
+        const SeqInfo& si = t.s[x.b];
+        float* out = a.scores + si.s_off + ((int64_t)x.layer * a.sh.h_kv + x.g) * x.L;
+        auto pooled = [&](int tt) {
+          const int lo = max(tt - pr, x.ta2), hi = min(tt + pr, x.tb2 - 1);
+          float u = Ss[lo - x.ta2];
+          for (int y = lo + 1; y <= hi; ++y) u = fmaxf(u, Ss[y - x.ta2]);
+          return u;
+        };
+        if (Pg == 1) {
+          for (int tt = x.a0 + e.etid; tt < x.a1; tt += kEpiThreads) out[tt] = pooled(tt);
+        } else {
+          const int n_pages = (x.L + Pg - 1) / Pg;
+          float* pout = a.page_scores + si.p_off + ((int64_t)x.layer * a.sh.h_kv + x.g) * n_pages;
+          for (int p = x.a0 / Pg + e.etid; p * Pg < x.a1; p += kEpiThreads) {
+            const int lo = p * Pg, hi = min(x.a1, lo + Pg);
+            float pv = 0.f;
+            for (int tt = lo; tt < hi; ++tt) {
+              const float u = pooled(tt);
+              out[tt] = u;
+              pv = (tt == lo) ? u : (a.sh.page_reduce == KVSEL_REDUCE_MAX ? fmaxf(pv, u) : pv + u);
+            }
+            pout[p] = pv;
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int D, int NK, int MAXW>
+__global__ void __launch_bounds__(kThreadsTc, 1) score_fused_kernel(const __grid_constant__ CUtensorMap tq,
+                                                                    const __grid_constant__ CUtensorMap tk,
+                                                                    const __grid_constant__ FusedArgs a,
+                                                                    const __grid_constant__ SeqTable t) {
+  using P = FPlan<D, NK>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t base = smem_addr(sbase);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sbase + P::kMiscOff);
+  volatile uint32_t* flag = reinterpret_cast<volatile uint32_t*>(sbase + P::kMiscOff + 4);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    const uint32_t bars = base + P::kBarOff;
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(P::full(bars, s), 1);
+      mbar_init(P::empty(bars, s), 1);
+    }
+    for (uint32_t s = 0; s < P::kNT; ++s) {
+      mbar_init(P::tfull(bars, s), 1);
+      mbar_init(P::tempty(bars, s), kEpiWarps);
+    }
+    for (int s = 0; s < P::kQSlots; ++s) {
+      mbar_init(P::qfull(bars, s), 1);
+      mbar_init(P::qempty(bars, s), 1);
+    }
+    mbar_init(P::drain(bars), 1);
+    *flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(smem_addr(tslot), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  if (warp == 0) {
+    if (lane == 0) fused_produce<D, NK>(&tq, &tk, a, t, base, flag);
+  } else if (warp == 1) {
+    if (lane == 0) fused_mma<D, NK>(a, t, base, tmem, flag);
+  } else {
+    fused_epilogue<D, NK, MAXW>(a, t, base, sbase, tmem, flag);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static std::once_flag once;
@@ -606,11 +1119,83 @@ kvsel_status run_tc(const TcArgs& a, const SeqTable& t1, const SeqTable& t2, con
   return KVSEL_ERR_UNSUPPORTED;
 }
 
+// Groups of gs CTAs share each unit.  Two units per group are live in L2 at a time (pass 1 of
+// one, pass 2 of the previous), so the number of groups is bounded by the L2 budget; each CTA's
+// pass-2 share (+ halo) must fit the shared-memory score buffer.
+bool plan_fused(const ScoreShape& sh, const SeqTable& base, int sms, int* gs_out, int* ng_out) {
+  if (sh.R > 128) return false;
+  const int ctas = sms < kFusedMaxCtas ? sms : kFusedMaxCtas;
+  const int64_t units = (int64_t)base.batch * sh.n_layers * sh.h_kv;
+  int64_t max_keys = 0, max_L = 0;
+  for (int b = 0; b < base.batch; ++b) {
+    max_keys = base.s[b].n_keys > max_keys ? base.s[b].n_keys : max_keys;
+    max_L = base.s[b].L > max_L ? base.s[b].L : max_L;
+  }
+  const double l2_budget = 72e6;
+  const double unit_bytes = (double)max_keys * sh.d * 2;
+  int64_t ng = (int64_t)(l2_budget / (2.0 * unit_bytes));
+  if (ng < 1) ng = 1;
+  if (ng > units) ng = units;
+  if (ng > ctas) ng = ctas;
+  const int P = sh.page_size, pr = (sh.pool_k - 1) / 2;
+  const int64_t pages = (max_L + P - 1) / P;
+  for (; ng >= 1; --ng) {
+    const int64_t gs = ctas / ng;
+    const int64_t share = (int64_t)P * ((pages + gs - 1) / gs) + 2 * pr;
+    if (share <= kFusedSsMax + 64) {
+      *gs_out = (int)gs;
+      *ng_out = (int)ng;
+      return true;
+    }
+  }
+  return false;
+}
+
+template <int D, int NK, int MAXW>
+kvsel_status launch_fused_one(const CUtensorMap& tq, const CUtensorMap& tk, const FusedArgs& a, const SeqTable& t,
+                              cudaStream_t s) {
+  using P = FPlan<D, NK>;
+  auto kern = score_fused_kernel<D, NK, MAXW>;
+  if (set_smem((const void*)kern, P::kSmem) != cudaSuccess) return KVSEL_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(a.gs * a.n_groups));
+  cfg.blockDim = dim3(kThreadsTc);
+  cfg.dynamicSmemBytes = P::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;   // every CTA resident: they wait on one another
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  TraceScope ts("score_fused_tc", s);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tq, tk, a, t);
+  count_launch();
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return KVSEL_ERR_CUDA;
+  }
+  return cudaGetLastError() == cudaSuccess ? KVSEL_OK : KVSEL_ERR_CUDA;
+}
+
+template <int D>
+kvsel_status run_fused(const FusedArgs& a, const SeqTable& t, const CUtensorMap& tq, const CUtensorMap& tk,
+                       cudaStream_t s) {
+  constexpr int NK = D == 128 ? 3 : 4;
+  if (a.sh.group_reduce == KVSEL_REDUCE_SUM) return launch_fused_one<D, NK, 0>(tq, tk, a, t, s);
+  switch (a.sh.W) {
+    case 8: return launch_fused_one<D, NK, 8>(tq, tk, a, t, s);
+    case 16: return launch_fused_one<D, NK, 16>(tq, tk, a, t, s);
+    case 32: return launch_fused_one<D, NK, 32>(tq, tk, a, t, s);
+    case 64: return launch_fused_one<D, NK, 64>(tq, tk, a, t, s);
+  }
+  return KVSEL_ERR_UNSUPPORTED;
+}
+
 }  // namespace
 
 kvsel_status launch_score(const ScoreShape& sh_in, const SeqTable& base, const void* q, const void* k,
-                          float* scores, float* page_scores, float* lse, float2* part, DeviceError* err,
-                          cudaStream_t s) {
+                          float* scores, float* page_scores, float* lse, float2* part, void* fused_ws,
+                          DeviceError* err, cudaStream_t s) {
   ScoreShape sh = sh_in;
   const int64_t ups = (int64_t)sh.n_layers * sh.h_kv;
   int64_t k_rows = 0;
@@ -628,10 +1213,28 @@ kvsel_status launch_score(const ScoreShape& sh_in, const SeqTable& base, const v
     const SeqTable t2 = with_items(base, ups, sh.seg2, false, sh.W);
     return launch_score_simt(sh, t1, t2, q, k, scores, page_scores, lse, part, err, s);
   }
-  sh.seg2 = (int32_t)(sh.page_size * (kSeg2Max / sh.page_size));
-  const SeqTable t2 = with_items(base, ups, sh.seg2, false, sh.W);
   CUtensorMap tq, tk;
   if (!make_map(&tq, q, q_rows, sh.d) || !make_map(&tk, k, k_rows, sh.d)) return KVSEL_ERR_CUDA;
+  int gs = 0, ng = 0;
+  if (plan_fused(sh, base, dev.sms, &gs, &ng)) {
+    FusedArgs f;
+    f.sh = sh;
+    f.scores = scores;
+    f.page_scores = page_scores;
+    f.err = err;
+    char* fw = static_cast<char*>(fused_ws);
+    f.part_ring = reinterpret_cast<float2*>(fw);
+    f.lse_ring = reinterpret_cast<float*>(fw + fused_part_bytes(sh.R));
+    f.arrive = reinterpret_cast<uint32_t*>(fw + fused_part_bytes(sh.R) + fused_lse_bytes(sh.R));
+    f.ready = f.arrive + kFusedSlots * kFusedMaxCtas;
+    f.gs = gs;
+    f.n_groups = ng;
+    f.n_units = (int32_t)(ups * base.batch);
+    if (cudaMemsetAsync(f.arrive, 0, fused_flag_bytes(), s) != cudaSuccess) return KVSEL_ERR_CUDA;
+    return sh.d == 64 ? run_fused<64>(f, base, tq, tk, s) : run_fused<128>(f, base, tq, tk, s);
+  }
+  sh.seg2 = (int32_t)(sh.page_size * (kSeg2Max / sh.page_size));
+  const SeqTable t2 = with_items(base, ups, sh.seg2, false, sh.W);
   TcArgs a;
   a.sh = sh;
   a.scores = scores;

@@ -97,6 +97,25 @@ def test_path_matches_oracle(name, cuda):
         np.testing.assert_array_equal(got, indices)
 
 
+def test_long_context_two_pass_path(cuda):
+    """640K-token prefix: each CTA's share no longer fits the single-read kernel's score buffer,
+    so the two-pass tensor-core kernels run; checked against the oracle on the one unit."""
+    from attention_kv_cache_gb300.pipeline import Pipeline, pack
+    w = S.Workload("long_640k", 96, 1, 4, 1, 128, 32, (655360,), group_reduce="max", pool_k=7, page_size=16,
+                   k_keep=128, n_recent=4, n_clusters=16)
+    inp = S.make_inputs(w, "cpu")
+    q, k, v = pack(inp, cuda)
+    pipe = Pipeline(w, cuda)
+    pipe.run(q, k, v)
+    torch.cuda.synchronize()
+    ref = O.run_sequence(w, inp.q[0], inp.k[0], with_gather=False)
+    assert_scores_close(pipe.token_scores(0), ref["pooled"], "long pooled")
+    assert_scores_close(pipe.page_view(0), ref["pages"], "long pages")
+    n_cand = -(-w.prefix_lens[0] // 16) - w.n_recent
+    assert_selection_equivalent(pipe.idx[0, 0, 0].cpu().numpy(), ref["idx"][0, 0], ref["pages"][0, 0][:n_cand],
+                                w.k_keep, "long selection")
+
+
 def test_unpooled_raw_scores(cuda):
     """pool_k = 1 gives the raw group column mass; sum mode mass of a group is at most G * W."""
     from attention_kv_cache_gb300 import kvsel as K
