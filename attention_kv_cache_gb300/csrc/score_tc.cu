@@ -38,7 +38,7 @@ constexpr int kSeg2Max = 8192;     // prefix keys per pass-2 segment (rounded do
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kEpiBarrier = 1;   // named barrier id of the epilogue warps
 
-enum : uint32_t { kWhereProducer = 1, kWhereMma = 2, kWhereEpilogue = 3, kWhereDrain = 4 };
+enum : uint32_t { kWhereProducer = 1, kWhereMma = 2, kWhereEpilogue = 3, kWhereDrain = 4, kWhereMerge = 5 };
 
 // Shared-memory plan (offsets from a 1024-byte aligned base).
 template <int RT, int D, int NK>
@@ -539,10 +539,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) score_tc_kernel(const __grid_co
 // share of unit U[s-1], whose keys the group read one step earlier and which
 // are still in L2, so each key row crosses HBM once.  The row log-sum-exp of a
 // unit needs every CTA of the group: each CTA writes its per-row partial
-// (max, sum) into a ring slot and counts itself in; the last one to arrive
-// merges the gs partials and publishes the unit's log-sum-exp.  Between a
-// unit's pass 1 and its pass 2 every CTA has the next unit's pass 1 to do, so
-// the merge is off the critical path.  The launch is cooperative (all CTAs
+// (max, sum) into a ring slot and counts itself in; a merge warp in every CTA
+// then merges the rows that CTA owns (about one row each) and publishes them.
+// Between a unit's pass 1 and its pass 2 every CTA has the next unit's pass 1
+// to do, so the merge is off the critical path.  The launch is cooperative (all CTAs
 // resident), and every cross-CTA wait is bounded.
 constexpr int kFusedSsMax = 4096;   // prefix keys (+ halo) of one CTA's pass-2 share
 
@@ -583,10 +583,10 @@ struct FusedArgs {
   float* scores;
   float* page_scores;
   DeviceError* err;
-  float2* part_ring;   // [n_groups][kFusedSlots][gs][R]
+  float2* part_ring;   // [n_groups][kFusedSlots][R][gs]  per-row partials, CTAs contiguous
   float* lse_ring;     // [n_groups][kFusedSlots][R]
-  uint32_t* arrive;    // [n_groups][kFusedSlots]
-  uint32_t* ready;     // [n_groups][kFusedSlots]
+  uint32_t* arrive;    // [n_groups][kFusedSlots]  CTAs that wrote their partials (cumulative)
+  uint32_t* merged;    // [n_groups][kFusedSlots]  rows whose log-sum-exp is published (cumulative)
   int32_t gs, n_groups, n_units;
 };
 
@@ -763,33 +763,55 @@ __device__ void fused_mma(const FusedArgs& a, const SeqTable& t, uint32_t base, 
 }
 
 // ---------------------------------------------------------------- fused epilogue
-// Merge of one unit's gs partials by the last CTA to arrive: warp per row, lanes over CTAs.
-__device__ void merge_unit_lse(const FusedArgs& a, int q, int slot, int etid) {
+// Merge warp (one per CTA): for each unit of the group, once all gs CTAs have written their
+// partials, merge the rows this CTA owns (rows rank, rank + gs, ...) in a fixed order and
+// publish them.  It runs ahead of the epilogue, so the merge overlaps the next unit's pass 1.
+__device__ void fused_merge(const FusedArgs& a, volatile uint32_t* flag) {
+  const int lane = threadIdx.x % 32;
+  const int q = group_of_cta(a), rank = rank_in_group(a);
+  const int nu = units_of_group(a, q);
   const int R = a.sh.R;
-  const int ew = etid / 32, lane = etid % 32;
-  const float2* part = a.part_ring + ((size_t)q * kFusedSlots + slot) * a.gs * R;
-  float* lse = a.lse_ring + ((size_t)q * kFusedSlots + slot) * R;
-  for (int r = ew; r < R; r += kEpiWarps) {
-    float m = -INFINITY, l = 0.f;
-    for (int c = lane; c < a.gs; c += 32) {
-      const float2 p = __ldcg(part + (size_t)c * R + r);
-      if (p.x > -INFINITY) {
-        const float nm = fmaxf(m, p.x);
-        l = l * exp2f(m - nm) + p.y * exp2f(p.x - nm);
-        m = nm;
-      }
+  for (int s = 0; s < nu; ++s) {
+    const int slot = s % kFusedSlots;
+    const uint32_t use = (uint32_t)(s / kFusedSlots);
+    bool ok = true;
+    if (lane == 0) ok = !aborted(flag) && wait_at_least(&a.arrive[q * kFusedSlots + slot], (uint32_t)a.gs * (use + 1));
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    if (!ok) {
+      if (lane == 0) fail_f(a, flag, kWhereMerge);
+      return;
     }
+    const float2* part = a.part_ring + ((size_t)q * kFusedSlots + slot) * R * a.gs;
+    float* lse = a.lse_ring + ((size_t)q * kFusedSlots + slot) * R;
+    uint32_t mine = 0;
+    for (int r = rank; r < R; r += a.gs) {
+      float m = -INFINITY, l = 0.f;
+      for (int c = lane; c < a.gs; c += 32) {
+        const float2 p = __ldcg(part + (size_t)r * a.gs + c);
+        if (p.x > -INFINITY) {
+          const float nm = fmaxf(m, p.x);
+          l = l * exp2f(m - nm) + p.y * exp2f(p.x - nm);
+          m = nm;
+        }
+      }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-      const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
-      const float nm = fmaxf(m, m2);
-      if (nm > -INFINITY) {
-        l = (m > -INFINITY ? l * exp2f(m - nm) : 0.f) + (m2 > -INFINITY ? l2 * exp2f(m2 - nm) : 0.f);
-        m = nm;
+      for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
+        const float nm = fmaxf(m, m2);
+        if (nm > -INFINITY) {
+          l = (m > -INFINITY ? l * exp2f(m - nm) : 0.f) + (m2 > -INFINITY ? l2 * exp2f(m2 - nm) : 0.f);
+          m = nm;
+        }
       }
+      if (lane == 0) lse[r] = m + log2f(l);
+      ++mine;
     }
-    if (lane == 0) lse[r] = m + log2f(l);
+    __syncwarp();
+    if (lane == 0 && mine > 0) {
+      __threadfence();
+      atomicAdd(&a.merged[q * kFusedSlots + slot], mine);
+    }
   }
 }
 
@@ -803,7 +825,6 @@ __device__ void fused_epilogue(const FusedArgs& a, const SeqTable& t, uint32_t b
   float* Ss = reinterpret_cast<float*>(sbase + P::kSsOff);
   float* lse_s = reinterpret_cast<float*>(sbase + P::kLseOff);
   float* red = reinterpret_cast<float*>(sbase + P::kRedOff);
-  volatile uint32_t* last_flag = reinterpret_cast<volatile uint32_t*>(sbase + P::kMiscOff + 8);
   const float scale = a.sh.scale_log2;
   const int R = a.sh.R;
   const int q = group_of_cta(a), rank = rank_in_group(a);
@@ -883,23 +904,12 @@ __device__ void fused_epilogue(const FusedArgs& a, const SeqTable& t, uint32_t b
         float S = 0.f;
         if (M > -INFINITY)
           S = (m > -INFINITY ? l * fast_ex2(m - M) : 0.f) + (m2 > -INFINITY ? l2 * fast_ex2(m2 - M) : 0.f);
-        a.part_ring[(((size_t)q * kFusedSlots + slot) * a.gs + rank) * R + e.lrow] = make_float2(M, S);
+        a.part_ring[(((size_t)q * kFusedSlots + slot) * R + e.lrow) * a.gs + rank] = make_float2(M, S);
       }
       epi_sync();
       if (e.etid == 0) {
         __threadfence();
-        const uint32_t old = atomicAdd(&a.arrive[q * kFusedSlots + slot], 1u);
-        *last_flag = (old + 1 == (uint32_t)a.gs * (use + 1)) ? 1u : 0u;
-      }
-      epi_sync();
-      if (*last_flag) {
-        __threadfence();
-        merge_unit_lse(a, q, slot, e.etid);
-        epi_sync();
-        if (e.etid == 0) {
-          __threadfence();
-          atomicExch(&a.ready[q * kFusedSlots + slot], use + 1);
-        }
+        atomicAdd(&a.arrive[q * kFusedSlots + slot], 1u);
       }
     }
     // ------------------------------------------------ pass 2 of unit s - 1
@@ -907,7 +917,7 @@ __device__ void fused_epilogue(const FusedArgs& a, const SeqTable& t, uint32_t b
       const Share x = share_of(a, t, q, s - 1);
       const int slot = (s - 1) % kFusedSlots;
       const uint32_t use = (uint32_t)((s - 1) / kFusedSlots);
-      if (e.etid == 0 && !aborted(flag) && !wait_at_least(&a.ready[q * kFusedSlots + slot], use + 1))
+      if (e.etid == 0 && !aborted(flag) && !wait_at_least(&a.merged[q * kFusedSlots + slot], (uint32_t)R * (use + 1)))
         fail_f(a, flag, kWhereEpilogue);
       epi_sync();
       for (int i = e.etid; i < x.tb2 - x.ta2; i += kEpiThreads) Ss[i] = 0.f;
@@ -994,8 +1004,10 @@ __device__ void fused_epilogue(const FusedArgs& a, const SeqTable& t, uint32_t b
   }
 }
 
+constexpr int kThreadsFused = kThreadsTc + 32;   // + the merge warp
+
 template <int D, int NK, int MAXW>
-__global__ void __launch_bounds__(kThreadsTc, 1) score_fused_kernel(const __grid_constant__ CUtensorMap tq,
+__global__ void __launch_bounds__(kThreadsFused, 1) score_fused_kernel(const __grid_constant__ CUtensorMap tq,
                                                                     const __grid_constant__ CUtensorMap tk,
                                                                     const __grid_constant__ FusedArgs a,
                                                                     const __grid_constant__ SeqTable t) {
@@ -1033,8 +1045,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) score_fused_kernel(const __grid
     if (lane == 0) fused_produce<D, NK>(&tq, &tk, a, t, base, flag);
   } else if (warp == 1) {
     if (lane == 0) fused_mma<D, NK>(a, t, base, tmem, flag);
-  } else {
+  } else if (warp < 2 + kEpiWarps) {
     fused_epilogue<D, NK, MAXW>(a, t, base, sbase, tmem, flag);
+  } else {
+    fused_merge(a, flag);
   }
   tc_fence_before();
   __syncthreads();
@@ -1159,7 +1173,7 @@ kvsel_status launch_fused_one(const CUtensorMap& tq, const CUtensorMap& tk, cons
   if (set_smem((const void*)kern, P::kSmem) != cudaSuccess) return KVSEL_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(a.gs * a.n_groups));
-  cfg.blockDim = dim3(kThreadsTc);
+  cfg.blockDim = dim3(kThreadsFused);
   cfg.dynamicSmemBytes = P::kSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -1226,7 +1240,7 @@ kvsel_status launch_score(const ScoreShape& sh_in, const SeqTable& base, const v
     f.part_ring = reinterpret_cast<float2*>(fw);
     f.lse_ring = reinterpret_cast<float*>(fw + fused_part_bytes(sh.R));
     f.arrive = reinterpret_cast<uint32_t*>(fw + fused_part_bytes(sh.R) + fused_lse_bytes(sh.R));
-    f.ready = f.arrive + kFusedSlots * kFusedMaxCtas;
+    f.merged = f.arrive + kFusedSlots * kFusedMaxCtas;
     f.gs = gs;
     f.n_groups = ng;
     f.n_units = (int32_t)(ups * base.batch);
