@@ -256,6 +256,84 @@ __device__ __forceinline__ float fast_ex2(float x) {
   return y;
 }
 
+// Epilogue arithmetic on 64 accumulator columns, written for instruction-level parallelism:
+// eight independent partial results combined by a fixed pairwise tree (so results do not
+// depend on scheduling), invisible columns entered as -inf.
+template <int N>
+__device__ __forceinline__ float tree_sum(float* a) {
+#pragma unroll
+  for (int w = N / 2; w >= 1; w /= 2)
+#pragma unroll
+    for (int i = 0; i < w; ++i) a[i] += a[i + w];
+  return a[0];
+}
+
+__device__ __forceinline__ float max64(const float* v) {
+  float m[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) m[k] = v[k];
+#pragma unroll
+  for (int i = 8; i < 64; ++i) m[i & 7] = fmaxf(m[i & 7], v[i]);
+#pragma unroll
+  for (int w = 4; w >= 1; w /= 2)
+#pragma unroll
+    for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+  return m[0];
+}
+
+// sum_i 2^(v_i * scale + off)
+__device__ __forceinline__ float expsum64(const float* v, float scale, float off) {
+  float a[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) a[k] = 0.f;
+#pragma unroll
+  for (int i = 0; i < 64; ++i) a[i & 7] += fast_ex2(fmaf(v[i], scale, off));
+  return tree_sum<8>(a);
+}
+
+// Column mass of 64 rows for one key: sum (MAXW = 0) or max over heads of MAXW rows of
+// sum_i 2^(v_i * scale + nl_i), nl = -lse of each row.
+template <int MAXW>
+__device__ __forceinline__ float colmass64(const float* v, const float* nl, float scale) {
+  if constexpr (MAXW == 0) {
+    float a[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) a[k] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) a[i & 7] += fast_ex2(fmaf(v[i], scale, nl[i]));
+    return tree_sum<8>(a);
+  } else {
+    constexpr int HW = MAXW < 64 ? MAXW : 64;
+    constexpr int NA = HW < 8 ? HW : 8;
+    float red = 0.f;
+#pragma unroll
+    for (int h = 0; h < 64 / HW; ++h) {
+      float a[NA];
+#pragma unroll
+      for (int k = 0; k < NA; ++k) a[k] = 0.f;
+#pragma unroll
+      for (int i = 0; i < HW; ++i) a[i % NA] += fast_ex2(fmaf(v[h * HW + i], scale, nl[h * HW + i]));
+      red = fmaxf(red, tree_sum<NA>(a));
+    }
+    return red;
+  }
+}
+
+// Online (max, sum) update of one row with 64 new columns, the first nvis of them visible.
+__device__ __forceinline__ void online_update64(float* v, int nvis, float scale, float& m, float& l) {
+  if (nvis < 64) {
+#pragma unroll
+    for (int i = 0; i < 64; ++i)
+      if (i >= nvis) v[i] = -INFINITY;
+  }
+  const float mx = max64(v);
+  if (mx > -INFINITY) {
+    const float nm = fmaxf(m, mx * scale);
+    l = l * fast_ex2(m - nm) + expsum64(v, scale, -nm);
+    m = nm;
+  }
+}
+
 // Epilogue thread geometry: warps 2..9; warp w may read TMEM lanes 32*(w%4) .. +31.
 struct EpiThread {
   int wg;        // epilogue warpgroup 0 / 1
@@ -304,49 +382,29 @@ __device__ void epilogue_pass1(const TcArgs& a, const SeqTable& t, uint32_t base
     const int vis_end = min(it.tb, row_last + 1);
     float m = -INFINITY, l = 0.f;
     for (int t0 = it.ta; t0 < it.tb; t0 += kTileKeys) {
-      float v[kChunks][32];
       // the tensor-memory loads below are warp-collective: decide per warp
       const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(tfull(ts), tph));
       if (!ok && e.lane == 0) fail(a, flag, kWhereEpilogue);
       if (ok) {
         tc_fence_after();
         const uint32_t taddr = tmem + ((uint32_t)(e.quarter * 32) << 16) + ts * RT + col0;
-#pragma unroll
-        for (int c = 0; c < kChunks; ++c) tmem_ld32(taddr + c * 32, v[c]);
-        tc_fence_before();
-        __syncwarp();
-        if (e.lane == 0) mbar_arrive(tempty(ts));
-        if (rvalid) {
-          const int nvis = vis_end - (t0 + key0);    // columns [0, nvis) of mine are visible
-          float mx = -INFINITY;
-          if (nvis >= kCols) {
-#pragma unroll
-            for (int c = 0; c < kChunks; ++c)
-#pragma unroll
-              for (int i = 0; i < 32; ++i) mx = fmaxf(mx, v[c][i]);
-          } else {
-#pragma unroll
-            for (int c = 0; c < kChunks; ++c)
-#pragma unroll
-              for (int i = 0; i < 32; ++i) mx = (c * 32 + i < nvis) ? fmaxf(mx, v[c][i]) : mx;
-          }
-          if (mx > -INFINITY) {
-            const float nm = fmaxf(m, mx * scale);
-            float acc = l * fast_ex2(m - nm);
-            if (nvis >= kCols) {
-#pragma unroll
-              for (int c = 0; c < kChunks; ++c)
-#pragma unroll
-                for (int i = 0; i < 32; ++i) acc += fast_ex2(fmaf(v[c][i], scale, -nm));
-            } else {
-#pragma unroll
-              for (int c = 0; c < kChunks; ++c)
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  if (c * 32 + i < nvis) acc += fast_ex2(fmaf(v[c][i], scale, -nm));
-            }
-            l = acc;
-            m = nm;
+        float v[64];
+        if (kChunks == 2) {
+          tmem_ld64(taddr, v);
+          tc_fence_before();
+          __syncwarp();
+          if (e.lane == 0) mbar_arrive(tempty(ts));
+          if (rvalid) online_update64(v, vis_end - (t0 + key0), scale, m, l);
+        } else {
+          float v2[64];
+          tmem_ld64(taddr, v);
+          tmem_ld64(taddr + 64, v2);
+          tc_fence_before();
+          __syncwarp();
+          if (e.lane == 0) mbar_arrive(tempty(ts));
+          if (rvalid) {
+            online_update64(v, vis_end - (t0 + key0), scale, m, l);
+            online_update64(v2, vis_end - (t0 + key0 + 64), scale, m, l);
           }
         }
       }
@@ -387,7 +445,8 @@ __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base
   auto tfull = [&](int s) { return bars + 8u * (2 * NK + s); };
   auto tempty = [&](int s) { return bars + 8u * (2 * NK + P::kNT + s); };
   float* Ss = reinterpret_cast<float*>(sbase + P::kSsOff);
-  float* lse_s = reinterpret_cast<float*>(sbase + P::kLseOff);
+  float* lse_s = reinterpret_cast<float*>(sbase + P::kLseOff);   // holds -lse per row
+  const float* nlse = lse_s;
   const float scale = a.sh.scale_log2;
   const int col0 = e.wg * kHalf;
   const int pr = (a.sh.pool_k - 1) / 2;
@@ -400,48 +459,33 @@ __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base
     epi_sync();                                          // readers of the previous item are done
     for (int i = e.etid; i < it.tb - it.ta; i += kEpiThreads) Ss[i] = 0.f;
     for (int i = e.etid; i < RT; i += kEpiThreads)
-      lse_s[i] = i < a.sh.R ? a.lse[(int64_t)it.unit * a.sh.R + i] : INFINITY;   // padding rows give p = 0
+      lse_s[i] = i < a.sh.R ? -a.lse[(int64_t)it.unit * a.sh.R + i] : -INFINITY;   // padding rows give p = 0
     epi_sync();
     for (int t0 = it.ta; t0 < it.tb; t0 += kTileKeys) {
-      float v[kChunks][32];
       // the tensor-memory loads below are warp-collective: decide per warp
       const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(tfull(ts), tph));
       if (!ok && e.lane == 0) fail(a, flag, kWhereEpilogue);
       if (ok) {
         tc_fence_after();
         const uint32_t taddr = tmem + ((uint32_t)(e.quarter * 32) << 16) + ts * RT + col0;
-#pragma unroll
-        for (int c = 0; c < kChunks; ++c) tmem_ld32(taddr + c * 32, v[c]);
-        tc_fence_before();
-        __syncwarp();
-        if (e.lane == 0) mbar_arrive(tempty(ts));
-        float red = 0.f;
-        if constexpr (MAXW == 0) {
-#pragma unroll
-          for (int c = 0; c < kChunks; ++c)
-#pragma unroll
-            for (int i = 0; i < 32; ++i) red += fast_ex2(fmaf(v[c][i], scale, -lse_s[col0 + c * 32 + i]));
-        } else if constexpr (MAXW >= 32) {
-#pragma unroll
-          for (int h = 0; h < kHalf / MAXW; ++h) {
-            float hs = 0.f;
-#pragma unroll
-            for (int c = h * (MAXW / 32); c < (h + 1) * (MAXW / 32); ++c)
-#pragma unroll
-              for (int i = 0; i < 32; ++i) hs += fast_ex2(fmaf(v[c][i], scale, -lse_s[col0 + c * 32 + i]));
-            red = fmaxf(red, hs);
-          }
+        float red;
+        if (kChunks == 2) {
+          float v64[64];
+          tmem_ld64(taddr, v64);
+          tc_fence_before();
+          __syncwarp();
+          if (e.lane == 0) mbar_arrive(tempty(ts));
+          red = colmass64<MAXW>(v64, nlse + col0, scale);
         } else {
-#pragma unroll
-          for (int c = 0; c < kChunks; ++c)
-#pragma unroll
-            for (int h = 0; h < 32 / MAXW; ++h) {
-              float hs = 0.f;
-#pragma unroll
-              for (int i = h * MAXW; i < (h + 1) * MAXW; ++i)
-                hs += fast_ex2(fmaf(v[c][i], scale, -lse_s[col0 + c * 32 + i]));
-              red = fmaxf(red, hs);
-            }
+          float v64[64], w64[64];
+          tmem_ld64(taddr, v64);
+          tmem_ld64(taddr + 64, w64);
+          tc_fence_before();
+          __syncwarp();
+          if (e.lane == 0) mbar_arrive(tempty(ts));
+          const float r0 = colmass64<MAXW>(v64, nlse + col0, scale);
+          const float r1 = colmass64<MAXW>(w64, nlse + col0 + 64, scale);
+          red = MAXW == 0 ? r0 + r1 : fmaxf(r0, r1);
         }
         const int key = t0 + e.lrow;
         if (key < it.tb) {
@@ -664,6 +708,7 @@ __device__ void fused_produce(const CUtensorMap* tq, const CUtensorMap* tk, cons
   tma_prefetch_desc(tk);
   const int q = group_of_cta(a);
   const int nu = units_of_group(a, q);
+  const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
   int ks = 0;
   uint32_t kph = 0, n_fills = 0;
   uint32_t qph[P::kQSlots] = {0, 0, 0}, n_q[P::kQSlots] = {0, 0, 0};
@@ -683,13 +728,15 @@ __device__ void fused_produce(const CUtensorMap* tq, const CUtensorMap* tk, cons
         ++n_q[qs];
       }
       const int ta = pass == 0 ? x.ta1 : x.ta2, tb = pass == 0 ? x.tb1 : x.tb2;
+      // pass-1 tiles stay in L2 for the pass-2 re-read one step later; pass-2 tiles are done
+      const uint64_t policy = pass == 0 ? keep : drop;
       for (int t0 = ta; t0 < tb; t0 += kTileKeys) {
         if (!mbar_wait(P::empty(bars, ks), kph ^ 1)) { ok = false; break; }
         mbar_expect_tx(P::full(bars, ks), P::kKBytes);
         const uint32_t dst = base + P::kKOff + ks * P::kKBytes;
 #pragma unroll
         for (int db = 0; db < P::kDBlocks; ++db)
-          tma_load_2d(dst + db * P::kKBlock, tk, db * 64, x.k_row0 + t0, P::full(bars, ks));
+          tma_load_2d_hint(dst + db * P::kKBlock, tk, db * 64, x.k_row0 + t0, P::full(bars, ks), policy);
         ++n_fills;
         if (++ks == NK) { ks = 0; kph ^= 1; }
       }
@@ -842,50 +889,16 @@ __device__ void fused_epilogue(const FusedArgs& a, const SeqTable& t, uint32_t b
       const int key0 = 64 * e.wg;
       float m = -INFINITY, l = 0.f;
       for (int t0 = x.ta1; t0 < x.tb1; t0 += kTileKeys) {
-        float v[2][32];
         const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(P::tfull(bars, ts), tph));
         if (!ok && e.lane == 0) fail_f(a, flag, kWhereEpilogue);
         if (ok) {
           tc_fence_after();
-          const uint32_t taddr = tmem + ((uint32_t)(e.quarter * 32) << 16) + ts * RT + key0;
-          tmem_ld32(taddr, v[0]);
-          tmem_ld32(taddr + 32, v[1]);
+          float v[64];
+          tmem_ld64(tmem + ((uint32_t)(e.quarter * 32) << 16) + ts * RT + key0, v);
           tc_fence_before();
           __syncwarp();
           if (e.lane == 0) mbar_arrive(P::tempty(bars, ts));
-          if (rvalid) {
-            const int nvis = vis_end - (t0 + key0);
-            float mx = -INFINITY;
-            if (nvis >= 64) {
-#pragma unroll
-              for (int c = 0; c < 2; ++c)
-#pragma unroll
-                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, v[c][i]);
-            } else {
-#pragma unroll
-              for (int c = 0; c < 2; ++c)
-#pragma unroll
-                for (int i = 0; i < 32; ++i) mx = (c * 32 + i < nvis) ? fmaxf(mx, v[c][i]) : mx;
-            }
-            if (mx > -INFINITY) {
-              const float nm = fmaxf(m, mx * scale);
-              float acc = l * fast_ex2(m - nm);
-              if (nvis >= 64) {
-#pragma unroll
-                for (int c = 0; c < 2; ++c)
-#pragma unroll
-                  for (int i = 0; i < 32; ++i) acc += fast_ex2(fmaf(v[c][i], scale, -nm));
-              } else {
-#pragma unroll
-                for (int c = 0; c < 2; ++c)
-#pragma unroll
-                  for (int i = 0; i < 32; ++i)
-                    if (c * 32 + i < nvis) acc += fast_ex2(fmaf(v[c][i], scale, -nm));
-              }
-              l = acc;
-              m = nm;
-            }
-          }
+          if (rvalid) online_update64(v, vis_end - (t0 + key0), scale, m, l);
         }
         if (++ts == (int)P::kNT) { ts = 0; tph ^= 1; }
       }
@@ -922,49 +935,23 @@ __device__ void fused_epilogue(const FusedArgs& a, const SeqTable& t, uint32_t b
       epi_sync();
       for (int i = e.etid; i < x.tb2 - x.ta2; i += kEpiThreads) Ss[i] = 0.f;
       for (int i = e.etid; i < RT; i += kEpiThreads)
-        lse_s[i] = i < R ? __ldcg(a.lse_ring + ((size_t)q * kFusedSlots + slot) * R + i) : INFINITY;
+        lse_s[i] = i < R ? -__ldcg(a.lse_ring + ((size_t)q * kFusedSlots + slot) * R + i) : -INFINITY;
       epi_sync();
       const int col0 = e.wg * (RT / 2);
+      float nl[64];                        // -lse of this warpgroup's 64 rows (padding rows: -inf)
+#pragma unroll
+      for (int i = 0; i < 64; ++i) nl[i] = lse_s[col0 + i];
       for (int t0 = x.ta2; t0 < x.tb2; t0 += kTileKeys) {
-        float v[2][32];
         const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(P::tfull(bars, ts), tph));
         if (!ok && e.lane == 0) fail_f(a, flag, kWhereEpilogue);
         if (ok) {
           tc_fence_after();
-          const uint32_t taddr = tmem + ((uint32_t)(e.quarter * 32) << 16) + ts * RT + col0;
-          tmem_ld32(taddr, v[0]);
-          tmem_ld32(taddr + 32, v[1]);
+          float v[64];
+          tmem_ld64(tmem + ((uint32_t)(e.quarter * 32) << 16) + ts * RT + col0, v);
           tc_fence_before();
           __syncwarp();
           if (e.lane == 0) mbar_arrive(P::tempty(bars, ts));
-          float redv = 0.f;
-          if constexpr (MAXW == 0) {
-#pragma unroll
-            for (int c = 0; c < 2; ++c)
-#pragma unroll
-              for (int i = 0; i < 32; ++i) redv += fast_ex2(fmaf(v[c][i], scale, -lse_s[col0 + c * 32 + i]));
-          } else if constexpr (MAXW >= 32) {
-#pragma unroll
-            for (int h = 0; h < 64 / MAXW; ++h) {
-              float hs = 0.f;
-#pragma unroll
-              for (int c = h * (MAXW / 32); c < (h + 1) * (MAXW / 32); ++c)
-#pragma unroll
-                for (int i = 0; i < 32; ++i) hs += fast_ex2(fmaf(v[c][i], scale, -lse_s[col0 + c * 32 + i]));
-              redv = fmaxf(redv, hs);
-            }
-          } else {
-#pragma unroll
-            for (int c = 0; c < 2; ++c)
-#pragma unroll
-              for (int h = 0; h < 32 / MAXW; ++h) {
-                float hs = 0.f;
-#pragma unroll
-                for (int i = h * MAXW; i < (h + 1) * MAXW; ++i)
-                  hs += fast_ex2(fmaf(v[c][i], scale, -lse_s[col0 + c * 32 + i]));
-                redv = fmaxf(redv, hs);
-              }
-          }
+          const float redv = colmass64<MAXW>(v, nl, scale);
           const int key = t0 + e.lrow;
           if (key < x.tb2) {
             if constexpr (MAXW == 0) atomicAdd(&Ss[key - x.ta2], redv);
