@@ -603,12 +603,13 @@ struct FPlan {
   static constexpr uint32_t kKOff = kQSlots * kQBytes;
   static constexpr uint32_t kSsOff = kKOff + NK * kKBytes;
   static constexpr uint32_t kSsFloats = kFusedSsMax + 192;
-  static constexpr uint32_t kLseOff = kSsOff + kSsFloats * 4;
-  static constexpr uint32_t kRedOff = kLseOff + RT * 4;
+  static constexpr uint32_t kLseOff = kSsOff + kSsFloats * 4;          // two staged buffers of -lse
+  static constexpr uint32_t kRedOff = kLseOff + 2 * RT * 4;
   static constexpr uint32_t kNT = kTmemCols / RT;
   static constexpr uint32_t kBarOff = kRedOff + 128 * 8;
-  // full[NK], empty[NK], tfull[NT], tempty[NT], q_full[3], q_empty[3], drain
-  static constexpr uint32_t kNumBars = 2 * NK + 2 * kNT + 2 * kQSlots + 1;
+  // full[NK], empty[NK], tfull[NT], tempty[NT], q_full[3], q_empty[3], drain,
+  // part_done, lse_full[2], lse_free[2]
+  static constexpr uint32_t kNumBars = 2 * NK + 2 * kNT + 2 * kQSlots + 1 + 5;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;           // tmem slot, abort flag, last flag
   static constexpr uint32_t kBytes = kMiscOff + 16;
   static constexpr size_t kSmem = kBytes + 1024;
@@ -620,6 +621,9 @@ struct FPlan {
   __device__ static uint32_t qfull(uint32_t bars, int q) { return bars + 8u * (2 * NK + 2 * kNT + q); }
   __device__ static uint32_t qempty(uint32_t bars, int q) { return bars + 8u * (2 * NK + 2 * kNT + kQSlots + q); }
   __device__ static uint32_t drain(uint32_t bars) { return bars + 8u * (2 * NK + 2 * kNT + 2 * kQSlots); }
+  __device__ static uint32_t part_done(uint32_t bars) { return bars + 8u * (2 * NK + 2 * kNT + 2 * kQSlots + 1); }
+  __device__ static uint32_t lse_full(uint32_t bars, int b) { return bars + 8u * (2 * NK + 2 * kNT + 2 * kQSlots + 2 + b); }
+  __device__ static uint32_t lse_free(uint32_t bars, int b) { return bars + 8u * (2 * NK + 2 * kNT + 2 * kQSlots + 4 + b); }
 };
 
 struct FusedArgs {
@@ -813,20 +817,37 @@ __device__ void fused_mma(const FusedArgs& a, const SeqTable& t, uint32_t base, 
 // Merge warp (one per CTA): for each unit of the group, once all gs CTAs have written their
 // partials, merge the rows this CTA owns (rows rank, rank + gs, ...) in a fixed order and
 // publish them.  It runs ahead of the epilogue, so the merge overlaps the next unit's pass 1.
-__device__ void fused_merge(const FusedArgs& a, volatile uint32_t* flag) {
+template <int D, int NK>
+__device__ void fused_merge(const FusedArgs& a, uint32_t base, uint8_t* sbase, volatile uint32_t* flag) {
+  using P = FPlan<D, NK>;
+  const uint32_t bars = base + P::kBarOff;
+  float* lse_buf = reinterpret_cast<float*>(sbase + P::kLseOff);
   const int lane = threadIdx.x % 32;
   const int q = group_of_cta(a), rank = rank_in_group(a);
   const int nu = units_of_group(a, q);
   const int R = a.sh.R;
+  auto lane0_ok = [&](bool ok) { return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0; };
   for (int s = 0; s < nu; ++s) {
     const int slot = s % kFusedSlots;
     const uint32_t use = (uint32_t)(s / kFusedSlots);
+    uint32_t* arrive = &a.arrive[q * kFusedSlots + slot];
+    uint32_t* merged = &a.merged[q * kFusedSlots + slot];
+    // 1. count this CTA in once its epilogue has written the unit's partials
     bool ok = true;
-    if (lane == 0) ok = !aborted(flag) && wait_at_least(&a.arrive[q * kFusedSlots + slot], (uint32_t)a.gs * (use + 1));
-    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-    if (!ok) {
+    if (lane == 0) ok = !aborted(flag) && mbar_wait(P::part_done(bars), s & 1);
+    if (!lane0_ok(ok)) {
       if (lane == 0) fail_f(a, flag, kWhereMerge);
-      return;
+      break;
+    }
+    if (lane == 0) {
+      __threadfence();
+      atomicAdd(arrive, 1u);
+    }
+    // 2. once every CTA of the group is in, merge the rows this CTA owns
+    if (lane == 0) ok = wait_at_least(arrive, (uint32_t)a.gs * (use + 1));
+    if (!lane0_ok(ok)) {
+      if (lane == 0) fail_f(a, flag, kWhereMerge);
+      break;
     }
     const float2* part = a.part_ring + ((size_t)q * kFusedSlots + slot) * R * a.gs;
     float* lse = a.lse_ring + ((size_t)q * kFusedSlots + slot) * R;
@@ -834,10 +855,10 @@ __device__ void fused_merge(const FusedArgs& a, volatile uint32_t* flag) {
     for (int r = rank; r < R; r += a.gs) {
       float m = -INFINITY, l = 0.f;
       for (int c = lane; c < a.gs; c += 32) {
-        const float2 p = __ldcg(part + (size_t)r * a.gs + c);
-        if (p.x > -INFINITY) {
-          const float nm = fmaxf(m, p.x);
-          l = l * exp2f(m - nm) + p.y * exp2f(p.x - nm);
+        const float2 pv = __ldcg(part + (size_t)r * a.gs + c);
+        if (pv.x > -INFINITY) {
+          const float nm = fmaxf(m, pv.x);
+          l = l * exp2f(m - nm) + pv.y * exp2f(pv.x - nm);
           m = nm;
         }
       }
@@ -857,8 +878,19 @@ __device__ void fused_merge(const FusedArgs& a, volatile uint32_t* flag) {
     __syncwarp();
     if (lane == 0 && mine > 0) {
       __threadfence();
-      atomicAdd(&a.merged[q * kFusedSlots + slot], mine);
+      atomicAdd(merged, mine);
     }
+    // 3. once every row is published, stage -lse into shared memory for this CTA's pass 2
+    const int b = s & 1;
+    if (lane == 0) ok = wait_at_least(merged, (uint32_t)R * (use + 1)) &&
+                        mbar_wait(P::lse_free(bars, b), ((s >> 1) & 1) ^ 1);
+    if (!lane0_ok(ok)) {
+      if (lane == 0) fail_f(a, flag, kWhereMerge);
+      break;
+    }
+    for (int i = lane; i < P::RT; i += 32) lse_buf[b * P::RT + i] = i < R ? -__ldcg(lse + i) : -INFINITY;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(P::lse_full(bars, b));
   }
 }
 
@@ -902,45 +934,42 @@ __device__ void fused_epilogue(const FusedArgs& a, const SeqTable& t, uint32_t b
         }
         if (++ts == (int)P::kNT) { ts = 0; tph ^= 1; }
       }
-      // this CTA's partial (max, sum) per row of unit s, then count in
+      // this CTA's partial (max, sum) per row of unit s; the merge warp counts the CTA in
       const int slot = s % kFusedSlots;
-      const uint32_t use = (uint32_t)(s / kFusedSlots);
       epi_sync();
       if (e.wg == 1) {
         red[2 * e.lrow] = m;
         red[2 * e.lrow + 1] = l;
       }
       epi_sync();
-      if (e.wg == 0 && rvalid) {
-        const float m2 = red[2 * e.lrow], l2 = red[2 * e.lrow + 1];
-        const float M = fmaxf(m, m2);
-        float S = 0.f;
-        if (M > -INFINITY)
-          S = (m > -INFINITY ? l * fast_ex2(m - M) : 0.f) + (m2 > -INFINITY ? l2 * fast_ex2(m2 - M) : 0.f);
-        a.part_ring[(((size_t)q * kFusedSlots + slot) * R + e.lrow) * a.gs + rank] = make_float2(M, S);
-      }
-      epi_sync();
-      if (e.etid == 0) {
-        __threadfence();
-        atomicAdd(&a.arrive[q * kFusedSlots + slot], 1u);
+      if (e.wg == 0) {
+        if (rvalid) {
+          const float m2 = red[2 * e.lrow], l2 = red[2 * e.lrow + 1];
+          const float M = fmaxf(m, m2);
+          float S = 0.f;
+          if (M > -INFINITY)
+            S = (m > -INFINITY ? l * fast_ex2(m - M) : 0.f) + (m2 > -INFINITY ? l2 * fast_ex2(m2 - M) : 0.f);
+          a.part_ring[(((size_t)q * kFusedSlots + slot) * R + e.lrow) * a.gs + rank] = make_float2(M, S);
+        }
+        __syncwarp();
+        if (e.lane == 0) mbar_arrive(P::part_done(bars));
       }
     }
     // ------------------------------------------------ pass 2 of unit s - 1
     if (s >= 1) {
       const Share x = share_of(a, t, q, s - 1);
-      const int slot = (s - 1) % kFusedSlots;
-      const uint32_t use = (uint32_t)((s - 1) / kFusedSlots);
-      if (e.etid == 0 && !aborted(flag) && !wait_at_least(&a.merged[q * kFusedSlots + slot], (uint32_t)R * (use + 1)))
-        fail_f(a, flag, kWhereEpilogue);
-      epi_sync();
-      for (int i = e.etid; i < x.tb2 - x.ta2; i += kEpiThreads) Ss[i] = 0.f;
-      for (int i = e.etid; i < RT; i += kEpiThreads)
-        lse_s[i] = i < R ? -__ldcg(a.lse_ring + ((size_t)q * kFusedSlots + slot) * R + i) : -INFINITY;
-      epi_sync();
+      const int b = (s - 1) & 1;
+      // -lse of the unit, staged in shared memory by the merge warp
+      const bool ready = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(P::lse_full(bars, b), ((s - 1) >> 1) & 1));
+      if (!ready && e.lane == 0) fail_f(a, flag, kWhereEpilogue);
       const int col0 = e.wg * (RT / 2);
       float nl[64];                        // -lse of this warpgroup's 64 rows (padding rows: -inf)
 #pragma unroll
-      for (int i = 0; i < 64; ++i) nl[i] = lse_s[col0 + i];
+      for (int i = 0; i < 64; ++i) nl[i] = lse_s[b * RT + col0 + i];
+      __syncwarp();
+      if (e.lane == 0) mbar_arrive(P::lse_free(bars, b));
+      for (int i = e.etid; i < x.tb2 - x.ta2; i += kEpiThreads) Ss[i] = 0.f;
+      epi_sync();
       for (int t0 = x.ta2; t0 < x.tb2; t0 += kTileKeys) {
         const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(P::tfull(bars, ts), tph));
         if (!ok && e.lane == 0) fail_f(a, flag, kWhereEpilogue);
@@ -961,28 +990,40 @@ __device__ void fused_epilogue(const FusedArgs& a, const SeqTable& t, uint32_t b
         if (++ts == (int)P::kNT) { ts = 0; tph ^= 1; }
       }
       epi_sync();
-      if (!aborted(flag) && x.a1 > x.a0) {
-        const SeqInfo& si = t.s[x.b];
-        float* out = a.scores + si.s_off + ((int64_t)x.layer * a.sh.h_kv + x.g) * x.L;
-        auto pooled = [&](int tt) {
+      // max-pool (thread per token, values kept in registers), then page reduce (thread per page)
+      constexpr int kTok = (kFusedSsMax + 64 + kEpiThreads - 1) / kEpiThreads;
+      const bool live = !aborted(flag);
+      const SeqInfo& si = t.s[x.b];
+      float* out = a.scores + si.s_off + ((int64_t)x.layer * a.sh.h_kv + x.g) * x.L;
+      float u[kTok];
+#pragma unroll
+      for (int k = 0; k < kTok; ++k) {
+        const int tt = x.a0 + e.etid + k * kEpiThreads;
+        u[k] = 0.f;
+        if (live && tt < x.a1) {
           const int lo = max(tt - pr, x.ta2), hi = min(tt + pr, x.tb2 - 1);
-          float u = Ss[lo - x.ta2];
-          for (int y = lo + 1; y <= hi; ++y) u = fmaxf(u, Ss[y - x.ta2]);
-          return u;
-        };
-        if (Pg == 1) {
-          for (int tt = x.a0 + e.etid; tt < x.a1; tt += kEpiThreads) out[tt] = pooled(tt);
-        } else {
+          float v = Ss[lo - x.ta2];
+          for (int y = lo + 1; y <= hi; ++y) v = fmaxf(v, Ss[y - x.ta2]);
+          u[k] = v;
+          out[tt] = v;
+        }
+      }
+      if (Pg > 1) {
+        epi_sync();
+#pragma unroll
+        for (int k = 0; k < kTok; ++k) {
+          const int tt = x.a0 + e.etid + k * kEpiThreads;
+          if (live && tt < x.a1) Ss[tt - x.ta2] = u[k];
+        }
+        epi_sync();
+        if (live) {
           const int n_pages = (x.L + Pg - 1) / Pg;
           float* pout = a.page_scores + si.p_off + ((int64_t)x.layer * a.sh.h_kv + x.g) * n_pages;
           for (int p = x.a0 / Pg + e.etid; p * Pg < x.a1; p += kEpiThreads) {
             const int lo = p * Pg, hi = min(x.a1, lo + Pg);
-            float pv = 0.f;
-            for (int tt = lo; tt < hi; ++tt) {
-              const float u = pooled(tt);
-              out[tt] = u;
-              pv = (tt == lo) ? u : (a.sh.page_reduce == KVSEL_REDUCE_MAX ? fmaxf(pv, u) : pv + u);
-            }
+            float pv = Ss[lo - x.ta2];
+            for (int tt = lo + 1; tt < hi; ++tt)
+              pv = a.sh.page_reduce == KVSEL_REDUCE_MAX ? fmaxf(pv, Ss[tt - x.ta2]) : pv + Ss[tt - x.ta2];
             pout[p] = pv;
           }
         }
@@ -1020,6 +1061,11 @@ __global__ void __launch_bounds__(kThreadsFused, 1) score_fused_kernel(const __g
       mbar_init(P::qempty(bars, s), 1);
     }
     mbar_init(P::drain(bars), 1);
+    mbar_init(P::part_done(bars), 4);            // one arrival per warp of epilogue warpgroup 0
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(P::lse_full(bars, b), 1);        // merge warp staged -lse
+      mbar_init(P::lse_free(bars, b), kEpiWarps);  // every epilogue warp read it
+    }
     *flag = 0;
     fence_barrier_init();
   }
@@ -1035,7 +1081,7 @@ __global__ void __launch_bounds__(kThreadsFused, 1) score_fused_kernel(const __g
   } else if (warp < 2 + kEpiWarps) {
     fused_epilogue<D, NK, MAXW>(a, t, base, sbase, tmem, flag);
   } else {
-    fused_merge(a, flag);
+    fused_merge<D, NK>(a, base, sbase, flag);
   }
   tc_fence_before();
   __syncthreads();
