@@ -38,7 +38,7 @@ constexpr int kSeg2Max = 8192;     // prefix keys per pass-2 segment (rounded do
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kEpiBarrier = 1;   // named barrier id of the epilogue warps
 
-enum : uint32_t { kWhereProducer = 1, kWhereMma = 2, kWhereEpilogue = 3, kWhereDrain = 4, kWhereMerge = 5 };
+enum : uint32_t { kWhereProducer = 1, kWhereMma = 2, kWhereEpilogue = 3, kWhereDrain = 4, kWhereMerge = 5, kWherePool = 6 };
 
 // Shared-memory plan (offsets from a 1024-byte aligned base).
 template <int RT, int D, int NK>
@@ -588,7 +588,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) score_tc_kernel(const __grid_co
 // Between a unit's pass 1 and its pass 2 every CTA has the next unit's pass 1
 // to do, so the merge is off the critical path.  The launch is cooperative (all CTAs
 // resident), and every cross-CTA wait is bounded.
-constexpr int kFusedSsMax = 4096;   // prefix keys (+ halo) of one CTA's pass-2 share
+constexpr int kFusedSsMax = 2048;   // prefix keys (+ halo) of one CTA's pass-2 share
 
 template <int D, int NK>
 struct FPlan {
@@ -602,14 +602,14 @@ struct FPlan {
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kKOff = kQSlots * kQBytes;
   static constexpr uint32_t kSsOff = kKOff + NK * kKBytes;
-  static constexpr uint32_t kSsFloats = kFusedSsMax + 192;
-  static constexpr uint32_t kLseOff = kSsOff + kSsFloats * 4;          // two staged buffers of -lse
+  static constexpr uint32_t kSsFloats = kFusedSsMax + 192;                // one score buffer; two are kept
+  static constexpr uint32_t kLseOff = kSsOff + 2 * kSsFloats * 4;      // two staged buffers of -lse
   static constexpr uint32_t kRedOff = kLseOff + 2 * RT * 4;
   static constexpr uint32_t kNT = kTmemCols / RT;
   static constexpr uint32_t kBarOff = kRedOff + 128 * 8;
   // full[NK], empty[NK], tfull[NT], tempty[NT], q_full[3], q_empty[3], drain,
-  // part_done, lse_full[2], lse_free[2]
-  static constexpr uint32_t kNumBars = 2 * NK + 2 * kNT + 2 * kQSlots + 1 + 5;
+  // part_done, lse_full[2], lse_free[2], ss_full[2], ss_free[2]
+  static constexpr uint32_t kNumBars = 2 * NK + 2 * kNT + 2 * kQSlots + 1 + 9;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;           // tmem slot, abort flag, last flag
   static constexpr uint32_t kBytes = kMiscOff + 16;
   static constexpr size_t kSmem = kBytes + 1024;
@@ -624,6 +624,8 @@ struct FPlan {
   __device__ static uint32_t part_done(uint32_t bars) { return bars + 8u * (2 * NK + 2 * kNT + 2 * kQSlots + 1); }
   __device__ static uint32_t lse_full(uint32_t bars, int b) { return bars + 8u * (2 * NK + 2 * kNT + 2 * kQSlots + 2 + b); }
   __device__ static uint32_t lse_free(uint32_t bars, int b) { return bars + 8u * (2 * NK + 2 * kNT + 2 * kQSlots + 4 + b); }
+  __device__ static uint32_t ss_full(uint32_t bars, int b) { return bars + 8u * (2 * NK + 2 * kNT + 2 * kQSlots + 6 + b); }
+  __device__ static uint32_t ss_free(uint32_t bars, int b) { return bars + 8u * (2 * NK + 2 * kNT + 2 * kQSlots + 8 + b); }
 };
 
 struct FusedArgs {
@@ -968,7 +970,11 @@ __device__ void fused_epilogue(const FusedArgs& a, const SeqTable& t, uint32_t b
       for (int i = 0; i < 64; ++i) nl[i] = lse_s[b * RT + col0 + i];
       __syncwarp();
       if (e.lane == 0) mbar_arrive(P::lse_free(bars, b));
-      for (int i = e.etid; i < x.tb2 - x.ta2; i += kEpiThreads) Ss[i] = 0.f;
+      // score buffer b, once the pool warp is done with its previous unit
+      float* Ssb = Ss + b * P::kSsFloats;
+      const bool free_ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(P::ss_free(bars, b), (((s - 1) >> 1) & 1) ^ 1));
+      if (!free_ok && e.lane == 0) fail_f(a, flag, kWhereEpilogue);
+      for (int i = e.etid; i < x.tb2 - x.ta2; i += kEpiThreads) Ssb[i] = 0.f;
       epi_sync();
       for (int t0 = x.ta2; t0 < x.tb2; t0 += kTileKeys) {
         const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(P::tfull(bars, ts), tph));
@@ -983,56 +989,71 @@ __device__ void fused_epilogue(const FusedArgs& a, const SeqTable& t, uint32_t b
           const float redv = colmass64<MAXW>(v, nl, scale);
           const int key = t0 + e.lrow;
           if (key < x.tb2) {
-            if constexpr (MAXW == 0) atomicAdd(&Ss[key - x.ta2], redv);
-            else atomicMax(reinterpret_cast<int*>(&Ss[key - x.ta2]), __float_as_int(redv));
+            if constexpr (MAXW == 0) atomicAdd(&Ssb[key - x.ta2], redv);
+            else atomicMax(reinterpret_cast<int*>(&Ssb[key - x.ta2]), __float_as_int(redv));
           }
         }
         if (++ts == (int)P::kNT) { ts = 0; tph ^= 1; }
       }
-      epi_sync();
-      // max-pool (thread per token, values kept in registers), then page reduce (thread per page)
-      constexpr int kTok = (kFusedSsMax + 64 + kEpiThreads - 1) / kEpiThreads;
-      const bool live = !aborted(flag);
-      const SeqInfo& si = t.s[x.b];
-      float* out = a.scores + si.s_off + ((int64_t)x.layer * a.sh.h_kv + x.g) * x.L;
-      float u[kTok];
-#pragma unroll
-      for (int k = 0; k < kTok; ++k) {
-        const int tt = x.a0 + e.etid + k * kEpiThreads;
-        u[k] = 0.f;
-        if (live && tt < x.a1) {
-          const int lo = max(tt - pr, x.ta2), hi = min(tt + pr, x.tb2 - 1);
-          float v = Ss[lo - x.ta2];
-          for (int y = lo + 1; y <= hi; ++y) v = fmaxf(v, Ss[y - x.ta2]);
-          u[k] = v;
-          out[tt] = v;
-        }
-      }
-      if (Pg > 1) {
-        epi_sync();
-#pragma unroll
-        for (int k = 0; k < kTok; ++k) {
-          const int tt = x.a0 + e.etid + k * kEpiThreads;
-          if (live && tt < x.a1) Ss[tt - x.ta2] = u[k];
-        }
-        epi_sync();
-        if (live) {
-          const int n_pages = (x.L + Pg - 1) / Pg;
-          float* pout = a.page_scores + si.p_off + ((int64_t)x.layer * a.sh.h_kv + x.g) * n_pages;
-          for (int p = x.a0 / Pg + e.etid; p * Pg < x.a1; p += kEpiThreads) {
-            const int lo = p * Pg, hi = min(x.a1, lo + Pg);
-            float pv = Ss[lo - x.ta2];
-            for (int tt = lo + 1; tt < hi; ++tt)
-              pv = a.sh.page_reduce == KVSEL_REDUCE_MAX ? fmaxf(pv, Ss[tt - x.ta2]) : pv + Ss[tt - x.ta2];
-            pout[p] = pv;
-          }
-        }
-      }
+      // hand the unit's group scores to the pool warp
+      __syncwarp();
+      if (e.lane == 0) mbar_arrive(P::ss_full(bars, b));
     }
   }
 }
 
-constexpr int kThreadsFused = kThreadsTc + 32;   // + the merge warp
+// Pool warp: max-pool and page reduce of each unit's pass-2 share from the score buffer, while
+// the epilogue goes on with the next unit (DELTA, 'Key designs' 2-3; CLAA, pooling kernel 7).
+template <int D, int NK>
+__device__ void fused_pool(const FusedArgs& a, const SeqTable& t, uint32_t base, uint8_t* sbase,
+                           volatile uint32_t* flag) {
+  using P = FPlan<D, NK>;
+  const uint32_t bars = base + P::kBarOff;
+  const float* Ss = reinterpret_cast<const float*>(sbase + P::kSsOff);
+  const int lane = threadIdx.x % 32;
+  const int q = group_of_cta(a);
+  const int nu = units_of_group(a, q);
+  const int pr = (a.sh.pool_k - 1) / 2;
+  const int Pg = a.sh.page_size;
+  for (int u = 0; u < nu; ++u) {
+    const int b = u & 1;
+    const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(P::ss_full(bars, b), (u >> 1) & 1));
+    if (!ok) {
+      if (lane == 0) fail_f(a, flag, kWherePool);
+      return;
+    }
+    const Share x = share_of(a, t, q, u);
+    const float* Sb = Ss + b * P::kSsFloats;
+    const SeqInfo& si = t.s[x.b];
+    float* out = a.scores + si.s_off + ((int64_t)x.layer * a.sh.h_kv + x.g) * x.L;
+    auto pooled = [&](int tt) {
+      const int lo = max(tt - pr, x.ta2), hi = min(tt + pr, x.tb2 - 1);
+      float v = Sb[lo - x.ta2];
+      for (int y = lo + 1; y <= hi; ++y) v = fmaxf(v, Sb[y - x.ta2]);
+      return v;
+    };
+    if (Pg == 1) {
+      for (int tt = x.a0 + lane; tt < x.a1; tt += 32) out[tt] = pooled(tt);
+    } else {
+      const int n_pages = (x.L + Pg - 1) / Pg;
+      float* pout = a.page_scores + si.p_off + ((int64_t)x.layer * a.sh.h_kv + x.g) * n_pages;
+      for (int p = x.a0 / Pg + lane; p * Pg < x.a1; p += 32) {
+        const int lo = p * Pg, hi = min(x.a1, lo + Pg);
+        float pv = 0.f;
+        for (int tt = lo; tt < hi; ++tt) {
+          const float v = pooled(tt);
+          out[tt] = v;
+          pv = (tt == lo) ? v : (a.sh.page_reduce == KVSEL_REDUCE_MAX ? fmaxf(pv, v) : pv + v);
+        }
+        pout[p] = pv;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(P::ss_free(bars, b));
+  }
+}
+
+constexpr int kThreadsFused = kThreadsTc + 64;   // + the merge warp and the pool warp
 
 template <int D, int NK, int MAXW>
 __global__ void __launch_bounds__(kThreadsFused, 1) score_fused_kernel(const __grid_constant__ CUtensorMap tq,
@@ -1063,8 +1084,10 @@ __global__ void __launch_bounds__(kThreadsFused, 1) score_fused_kernel(const __g
     mbar_init(P::drain(bars), 1);
     mbar_init(P::part_done(bars), 4);            // one arrival per warp of epilogue warpgroup 0
     for (int b = 0; b < 2; ++b) {
-      mbar_init(P::lse_full(bars, b), 1);        // merge warp staged -lse
+      mbar_init(P::lse_full(bars, b), 1);          // merge warp staged -lse
       mbar_init(P::lse_free(bars, b), kEpiWarps);  // every epilogue warp read it
+      mbar_init(P::ss_full(bars, b), kEpiWarps);   // every epilogue warp added its column mass
+      mbar_init(P::ss_free(bars, b), 1);           // pool warp wrote the scores out
     }
     *flag = 0;
     fence_barrier_init();
@@ -1080,8 +1103,10 @@ __global__ void __launch_bounds__(kThreadsFused, 1) score_fused_kernel(const __g
     if (lane == 0) fused_mma<D, NK>(a, t, base, tmem, flag);
   } else if (warp < 2 + kEpiWarps) {
     fused_epilogue<D, NK, MAXW>(a, t, base, sbase, tmem, flag);
-  } else {
+  } else if (warp == 2 + kEpiWarps) {
     fused_merge<D, NK>(a, base, sbase, flag);
+  } else {
+    fused_pool<D, NK>(a, t, base, sbase, flag);
   }
   tc_fence_before();
   __syncthreads();
