@@ -896,6 +896,11 @@ __device__ void fused_merge(const FusedArgs& a, uint32_t base, uint8_t* sbase, v
   }
 }
 
+// Epilogue: the two warpgroups take alternate tiles of the stream (warpgroup e takes tiles whose
+// running index is e mod 2), each covering all 128 TMEM columns of its tiles, so the two warps that
+// share a scheduler sit in different phases.  Pass 1: online (max, sum) per row, merged across the
+// warpgroups at the end of the unit.  Pass 2: every key's group score written by the one thread that
+// owns it.
 template <int D, int NK, int MAXW>
 __device__ void fused_epilogue(const FusedArgs& a, const SeqTable& t, uint32_t base, uint8_t* sbase, uint32_t tmem,
                                volatile uint32_t* flag) {
@@ -904,37 +909,40 @@ __device__ void fused_epilogue(const FusedArgs& a, const SeqTable& t, uint32_t b
   const uint32_t bars = base + P::kBarOff;
   const EpiThread e = epi_thread();
   float* Ss = reinterpret_cast<float*>(sbase + P::kSsOff);
-  float* lse_s = reinterpret_cast<float*>(sbase + P::kLseOff);
+  const float* lse_s = reinterpret_cast<const float*>(sbase + P::kLseOff);
   float* red = reinterpret_cast<float*>(sbase + P::kRedOff);
   const float scale = a.sh.scale_log2;
   const int R = a.sh.R;
   const int q = group_of_cta(a), rank = rank_in_group(a);
   const int nu = units_of_group(a, q);
-  const int pr = (a.sh.pool_k - 1) / 2;
-  const int Pg = a.sh.page_size;
-  int ts = 0;
-  uint32_t tph = 0;
+  const uint32_t lane_base = (uint32_t)(e.quarter * 32) << 16;
+  uint32_t tile = 0;          // running index of the tile stream (both warpgroups count every tile)
   for (int s = 0; s <= nu; ++s) {
     // ------------------------------------------------ pass 1 of unit s
     if (s < nu) {
       const Share x = share_of(a, t, q, s);
       const bool rvalid = e.lrow < R;
       const int vis_end = min(x.tb1, x.L + (rvalid ? e.lrow % a.sh.W : 0) + 1);
-      const int key0 = 64 * e.wg;
       float m = -INFINITY, l = 0.f;
-      for (int t0 = x.ta1; t0 < x.tb1; t0 += kTileKeys) {
+      for (int t0 = x.ta1; t0 < x.tb1; t0 += kTileKeys, ++tile) {
+        if ((int)(tile & 1) != e.wg) continue;
+        const int ts = (int)(tile % P::kNT);
+        const uint32_t tph = (tile / P::kNT) & 1;
         const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(P::tfull(bars, ts), tph));
         if (!ok && e.lane == 0) fail_f(a, flag, kWhereEpilogue);
         if (ok) {
           tc_fence_after();
-          float v[64];
-          tmem_ld64(tmem + ((uint32_t)(e.quarter * 32) << 16) + ts * RT + key0, v);
+          float v[64], w[64];
+          tmem_ld64(tmem + lane_base + ts * RT, v);
+          tmem_ld64(tmem + lane_base + ts * RT + 64, w);
           tc_fence_before();
           __syncwarp();
           if (e.lane == 0) mbar_arrive(P::tempty(bars, ts));
-          if (rvalid) online_update64(v, vis_end - (t0 + key0), scale, m, l);
+          if (rvalid) {
+            online_update64(v, vis_end - t0, scale, m, l);
+            online_update64(w, vis_end - (t0 + 64), scale, m, l);
+          }
         }
-        if (++ts == (int)P::kNT) { ts = 0; tph ^= 1; }
       }
       // this CTA's partial (max, sum) per row of unit s; the merge warp counts the CTA in
       const int slot = s % kFusedSlots;
@@ -961,43 +969,45 @@ __device__ void fused_epilogue(const FusedArgs& a, const SeqTable& t, uint32_t b
     if (s >= 1) {
       const Share x = share_of(a, t, q, s - 1);
       const int b = (s - 1) & 1;
-      // -lse of the unit, staged in shared memory by the merge warp
-      const bool ready = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(P::lse_full(bars, b), ((s - 1) >> 1) & 1));
+      // -lse of the unit (staged by the merge warp) and a free score buffer (released by the pool warp)
+      const bool ready = __all_sync(0xffffffffu, !aborted(flag) &&
+                                                     mbar_wait(P::lse_full(bars, b), ((s - 1) >> 1) & 1) &&
+                                                     mbar_wait(P::ss_free(bars, b), (((s - 1) >> 1) & 1) ^ 1));
       if (!ready && e.lane == 0) fail_f(a, flag, kWhereEpilogue);
-      const int col0 = e.wg * (RT / 2);
-      float nl[64];                        // -lse of this warpgroup's 64 rows (padding rows: -inf)
-#pragma unroll
-      for (int i = 0; i < 64; ++i) nl[i] = lse_s[b * RT + col0 + i];
-      __syncwarp();
-      if (e.lane == 0) mbar_arrive(P::lse_free(bars, b));
-      // score buffer b, once the pool warp is done with its previous unit
+      const float* nlse = lse_s + b * RT;
       float* Ssb = Ss + b * P::kSsFloats;
-      const bool free_ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(P::ss_free(bars, b), (((s - 1) >> 1) & 1) ^ 1));
-      if (!free_ok && e.lane == 0) fail_f(a, flag, kWhereEpilogue);
-      for (int i = e.etid; i < x.tb2 - x.ta2; i += kEpiThreads) Ssb[i] = 0.f;
-      epi_sync();
-      for (int t0 = x.ta2; t0 < x.tb2; t0 += kTileKeys) {
+      for (int t0 = x.ta2; t0 < x.tb2; t0 += kTileKeys, ++tile) {
+        if ((int)(tile & 1) != e.wg) continue;
+        const int ts = (int)(tile % P::kNT);
+        const uint32_t tph = (tile / P::kNT) & 1;
         const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(P::tfull(bars, ts), tph));
         if (!ok && e.lane == 0) fail_f(a, flag, kWhereEpilogue);
         if (ok) {
           tc_fence_after();
           float v[64];
-          tmem_ld64(tmem + ((uint32_t)(e.quarter * 32) << 16) + ts * RT + col0, v);
+          float nl[64];
+          tmem_ld64(tmem + lane_base + ts * RT, v);
+#pragma unroll
+          for (int i = 0; i < 64; i += 4) *reinterpret_cast<float4*>(nl + i) = *reinterpret_cast<const float4*>(nlse + i);
+          const float r0 = colmass64<MAXW>(v, nl, scale);
+          tmem_ld64(tmem + lane_base + ts * RT + 64, v);
           tc_fence_before();
           __syncwarp();
           if (e.lane == 0) mbar_arrive(P::tempty(bars, ts));
-          const float redv = colmass64<MAXW>(v, nl, scale);
+#pragma unroll
+          for (int i = 0; i < 64; i += 4) *reinterpret_cast<float4*>(nl + i) = *reinterpret_cast<const float4*>(nlse + 64 + i);
+          const float r1 = colmass64<MAXW>(v, nl, scale);
+          const float redv = MAXW == 0 ? r0 + r1 : fmaxf(r0, r1);
           const int key = t0 + e.lrow;
-          if (key < x.tb2) {
-            if constexpr (MAXW == 0) atomicAdd(&Ssb[key - x.ta2], redv);
-            else atomicMax(reinterpret_cast<int*>(&Ssb[key - x.ta2]), __float_as_int(redv));
-          }
+          if (key < x.tb2) Ssb[key - x.ta2] = redv;
         }
-        if (++ts == (int)P::kNT) { ts = 0; tph ^= 1; }
       }
-      // hand the unit's group scores to the pool warp
+      // hand the unit's group scores to the pool warp; the staged -lse is no longer needed
       __syncwarp();
-      if (e.lane == 0) mbar_arrive(P::ss_full(bars, b));
+      if (e.lane == 0) {
+        mbar_arrive(P::ss_full(bars, b));
+        mbar_arrive(P::lse_free(bars, b));
+      }
     }
   }
 }
@@ -1075,7 +1085,7 @@ __global__ void __launch_bounds__(kThreadsFused, 1) score_fused_kernel(const __g
     }
     for (uint32_t s = 0; s < P::kNT; ++s) {
       mbar_init(P::tfull(bars, s), 1);
-      mbar_init(P::tempty(bars, s), kEpiWarps);
+      mbar_init(P::tempty(bars, s), kEpiWarps / 2);   // the warpgroup that owns the tile
     }
     for (int s = 0; s < P::kQSlots; ++s) {
       mbar_init(P::qfull(bars, s), 1);
