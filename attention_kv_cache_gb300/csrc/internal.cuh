@@ -81,17 +81,8 @@ inline kvsel_status launch_status() {
 // cover and the CUDA-core kernels otherwise.  `base` carries the per-sequence geometry;
 // the launchers add their own work-item tables.
 kvsel_status launch_score(const ScoreShape& sh, const SeqTable& base, const void* q, const void* k,
-                          float* scores, float* page_scores, float* lse, float2* part, void* fused_ws,
-                          DeviceError* err, cudaStream_t s);
-
-// Single-read scoring: per-unit synchronisation ring in the workspace (sized for up to
-// kFusedMaxCtas cooperating CTAs and R rows): partials, log-sum-exp, arrival and ready words.
-constexpr int kFusedSlots = 4;
-constexpr int kFusedMaxCtas = 256;
-inline size_t fused_part_bytes(int R) { return (size_t)kFusedSlots * kFusedMaxCtas * R * 8; }
-inline size_t fused_lse_bytes(int R) { return (size_t)kFusedSlots * kFusedMaxCtas * R * 4; }
-inline size_t fused_flag_bytes() { return (size_t)2 * kFusedSlots * kFusedMaxCtas * 4; }
-inline size_t fused_sync_bytes(int R) { return fused_part_bytes(R) + fused_lse_bytes(R) + fused_flag_bytes(); }
+                          float* scores, float* page_scores, float* lse, float2* part, DeviceError* err,
+                          cudaStream_t s);
 kvsel_status launch_score_simt(const ScoreShape& sh, const SeqTable& t1, const SeqTable& t2,
                                const void* q, const void* k, float* scores, float* page_scores,
                                float* lse, float2* part, DeviceError* err, cudaStream_t s);

@@ -77,7 +77,7 @@ static int64_t total_units(const kvsel_desc& d) { return (int64_t)d.batch * d.n_
 static int64_t nseg1(const kvsel_desc& d, int b) { return cdiv(d.prefix_lens[b] + d.window, kScoreSeg1); }
 
 struct WsLayout {
-  size_t lse_off, part_off, norm_off, cnt_off, fused_off, total;
+  size_t lse_off, part_off, norm_off, cnt_off, total;
 };
 
 static WsLayout ws_layout(const kvsel_desc& d) {
@@ -95,8 +95,6 @@ static WsLayout ws_layout(const kvsel_desc& d) {
   off = align_up(off + (size_t)units * sizeof(float), KVSEL_WS_ALIGN);
   w.cnt_off = off;
   off = align_up(off + (size_t)units * sizeof(int32_t), KVSEL_WS_ALIGN);
-  w.fused_off = off;
-  off = align_up(off + fused_sync_bytes((int)R), KVSEL_WS_ALIGN);
   w.total = off;
   return w;
 }
@@ -201,8 +199,8 @@ kvsel_status kvsel_score(const kvsel_desc* desc, const void* q, const void* k, f
   sh.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.head_dim));
   const SeqTable base = make_table(d, d.n_layers);
   return launch_score(sh, base, q, k, scores, page_scores, reinterpret_cast<float*>(ws_base(ws) + w.lse_off),
-                      reinterpret_cast<float2*>(ws_base(ws) + w.part_off), ws_base(ws) + w.fused_off,
-                      reinterpret_cast<DeviceError*>(ws), stream);
+                      reinterpret_cast<float2*>(ws_base(ws) + w.part_off), reinterpret_cast<DeviceError*>(ws),
+                      stream);
 }
 
 kvsel_status kvsel_combine_layers(const kvsel_desc* desc, const float* scores, int32_t layer_lo,

@@ -34,11 +34,12 @@ constexpr int kTileKeys = 128;
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kThreadsTc = 32 * (2 + kEpiWarps);
-constexpr int kSeg2Max = 8192;     // prefix keys per pass-2 segment (rounded down to whole pages)
+constexpr int kThreadsTc2 = kThreadsTc + 32;      // pass 2 adds the helper warp
+constexpr int kSeg2Max = 4096;     // keys per pass-2 segment, pooling halo included
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kEpiBarrier = 1;   // named barrier id of the epilogue warps
 
-enum : uint32_t { kWhereProducer = 1, kWhereMma = 2, kWhereEpilogue = 3, kWhereDrain = 4, kWhereMerge = 5, kWherePool = 6 };
+enum : uint32_t { kWhereProducer = 1, kWhereMma = 2, kWhereEpilogue = 3, kWhereDrain = 4, kWherePool = 5 };
 
 // Shared-memory plan (offsets from a 1024-byte aligned base).
 template <int RT, int D, int NK>
@@ -50,14 +51,16 @@ struct Plan {
   static constexpr uint32_t kKBytes = kKBlock * kDBlocks;
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kKOff = kQOff + kQBytes;
-  static constexpr uint32_t kSsOff = kKOff + NK * kKBytes;                 // pass-2 segment scores
-  static constexpr uint32_t kSsFloats = kSeg2Max + 128;
-  static constexpr uint32_t kLseOff = kSsOff + kSsFloats * 4;             // pass-2 row lse (RT floats)
-  static constexpr uint32_t kRedOff = kLseOff + RT * 4;                   // pass-1 (m, l) exchange
+  static constexpr uint32_t kSsOff = kKOff + NK * kKBytes;                 // pass 2: two segment score buffers
+  static constexpr uint32_t kSsFloats = kSeg2Max + 32;
+  static constexpr uint32_t kLseOff = kSsOff + 2 * kSsFloats * 4;         // pass 2: two buffers of -lse (RT each)
+  static constexpr uint32_t kRedOff = kLseOff + 2 * RT * 4;               // pass-1 (m, l) exchange
   static constexpr uint32_t kNT = kTmemCols / RT;                         // TMEM accumulator stages
   static constexpr uint32_t kBarOff = kRedOff + 128 * 8;
-  // barriers: full[NK], empty[NK], tfull[NT], tempty[NT], q_full, q_empty, drain
-  static constexpr uint32_t kNumBars = 2 * NK + 2 * kNT + 3;
+  // barriers: full[NK], empty[NK], tfull[NT], tempty[NT], q_full, q_empty, drain,
+  // pass 2: lse_full[2], lse_free[2], ss_full[2], ss_free[2]
+  static constexpr uint32_t kNumBars = 2 * NK + 2 * kNT + 3 + 8;
+  static constexpr uint32_t kBar2 = 2 * NK + 2 * kNT + 3;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;            // tmem slot, abort flag
   static constexpr uint32_t kBytes = kMiscOff + 16;
   static constexpr size_t kSmem = kBytes + 1024;                          // + alignment slack
@@ -432,88 +435,124 @@ __device__ void epilogue_pass1(const TcArgs& a, const SeqTable& t, uint32_t base
 }
 
 // ---------------------------------------------------------------- pass 2 epilogue
-// Thread = key (TMEM lane); warpgroup e takes rows [e RT/2, (e+1) RT/2) (TMEM columns).
+// Thread = key (TMEM lane).  The two warpgroups take alternate tiles of the stream (warpgroup e the
+// tiles whose running index is e mod 2) and each covers all RT rows of its tiles, so every key's group
+// score is written by exactly one thread.  -lse arrives staged in shared memory from the helper warp,
+// and the helper warp pools each finished segment while the epilogue goes on with the next one.
 // MAXW = 0: group sum (every row summed); otherwise group max with head width MAXW.
 template <int RT, int D, int NK, int MAXW>
 __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base, uint8_t* sbase,
                                uint32_t tmem, volatile uint32_t* flag) {
   using P = Plan<RT, D, NK>;
-  constexpr int kHalf = RT / 2;
-  constexpr int kChunks = kHalf / 32;
   const EpiThread e = epi_thread();
   const uint32_t bars = base + P::kBarOff;
   auto tfull = [&](int s) { return bars + 8u * (2 * NK + s); };
   auto tempty = [&](int s) { return bars + 8u * (2 * NK + P::kNT + s); };
+  auto lse_full = [&](int b) { return bars + 8u * (P::kBar2 + b); };
+  auto lse_free = [&](int b) { return bars + 8u * (P::kBar2 + 2 + b); };
+  auto ss_full = [&](int b) { return bars + 8u * (P::kBar2 + 4 + b); };
+  auto ss_free = [&](int b) { return bars + 8u * (P::kBar2 + 6 + b); };
   float* Ss = reinterpret_cast<float*>(sbase + P::kSsOff);
-  float* lse_s = reinterpret_cast<float*>(sbase + P::kLseOff);   // holds -lse per row
-  const float* nlse = lse_s;
+  const float* lse_s = reinterpret_cast<const float*>(sbase + P::kLseOff);
   const float scale = a.sh.scale_log2;
-  const int col0 = e.wg * kHalf;
-  const int pr = (a.sh.pool_k - 1) / 2;
-  const int P_ = a.sh.page_size;
-  int ts = 0;
-  uint32_t tph = 0;
-  const int i1 = item_end(t.n_items);
-  for (int item = item_begin(t.n_items); item < i1; ++item) {
+  const uint32_t lane_base = (uint32_t)(e.quarter * 32) << 16;
+  uint32_t tile = 0;
+  const int i0 = item_begin(t.n_items), i1 = item_end(t.n_items);
+  for (int item = i0; item < i1; ++item) {
     const Item it = decode<true>(t, a.sh, item);
-    epi_sync();                                          // readers of the previous item are done
-    for (int i = e.etid; i < it.tb - it.ta; i += kEpiThreads) Ss[i] = 0.f;
-    for (int i = e.etid; i < RT; i += kEpiThreads)
-      lse_s[i] = i < a.sh.R ? -a.lse[(int64_t)it.unit * a.sh.R + i] : -INFINITY;   // padding rows give p = 0
-    epi_sync();
-    for (int t0 = it.ta; t0 < it.tb; t0 += kTileKeys) {
+    const int li = item - i0, b = li & 1;
+    const bool ready = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(lse_full(b), (li >> 1) & 1) &&
+                                                   mbar_wait(ss_free(b), ((li >> 1) & 1) ^ 1));
+    if (!ready && e.lane == 0) fail(a, flag, kWhereEpilogue);
+    const float* nlse = lse_s + b * RT;
+    float* Ssb = Ss + b * P::kSsFloats;
+    for (int t0 = it.ta; t0 < it.tb; t0 += kTileKeys, ++tile) {
+      if ((int)(tile & 1) != e.wg) continue;
+      const int ts = (int)(tile % P::kNT);
+      const uint32_t tph = (tile / P::kNT) & 1;
       // the tensor-memory loads below are warp-collective: decide per warp
       const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(tfull(ts), tph));
       if (!ok && e.lane == 0) fail(a, flag, kWhereEpilogue);
-      if (ok) {
-        tc_fence_after();
-        const uint32_t taddr = tmem + ((uint32_t)(e.quarter * 32) << 16) + ts * RT + col0;
-        float red;
-        if (kChunks == 2) {
-          float v64[64];
-          tmem_ld64(taddr, v64);
+      if (!ok) continue;
+      tc_fence_after();
+      float red = 0.f;
+#pragma unroll
+      for (int c = 0; c < RT / 64; ++c) {
+        float v[64], nl[64];
+        tmem_ld64(tmem + lane_base + ts * RT + c * 64, v);
+        if (c == RT / 64 - 1) {
           tc_fence_before();
           __syncwarp();
           if (e.lane == 0) mbar_arrive(tempty(ts));
-          red = colmass64<MAXW>(v64, nlse + col0, scale);
-        } else {
-          float v64[64], w64[64];
-          tmem_ld64(taddr, v64);
-          tmem_ld64(taddr + 64, w64);
-          tc_fence_before();
-          __syncwarp();
-          if (e.lane == 0) mbar_arrive(tempty(ts));
-          const float r0 = colmass64<MAXW>(v64, nlse + col0, scale);
-          const float r1 = colmass64<MAXW>(w64, nlse + col0 + 64, scale);
-          red = MAXW == 0 ? r0 + r1 : fmaxf(r0, r1);
         }
-        const int key = t0 + e.lrow;
-        if (key < it.tb) {
-          // two addends per key (one per warpgroup): the result does not depend on their order
-          if constexpr (MAXW == 0) atomicAdd(&Ss[key - it.ta], red);
-          else atomicMax(reinterpret_cast<int*>(&Ss[key - it.ta]), __float_as_int(red));
-        }
+#pragma unroll
+        for (int i = 0; i < 64; i += 4)
+          *reinterpret_cast<float4*>(nl + i) = *reinterpret_cast<const float4*>(nlse + c * 64 + i);
+        const float r = colmass64<MAXW>(v, nl, scale);
+        red = (c == 0) ? r : (MAXW == 0 ? red + r : fmaxf(red, r));
       }
-      if (++ts == (int)P::kNT) { ts = 0; tph ^= 1; }
+      const int key = t0 + e.lrow;
+      if (key < it.tb) Ssb[key - it.ta] = red;
     }
-    epi_sync();
-    if (aborted(flag)) continue;
-    // max-pool over prefix positions, then page reduce (DELTA key designs 2-3)
+    // the segment's group scores go to the helper warp; the staged -lse is no longer needed
+    __syncwarp();
+    if (e.lane == 0) {
+      mbar_arrive(ss_full(b));
+      mbar_arrive(lse_free(b));
+    }
+  }
+}
+
+// Helper warp of pass 2: stages each segment's -lse (two segments ahead) and max-pools / page-reduces
+// each finished segment (CLAA, pooling with kernel 7; DELTA, 'Key designs' 2-3).
+template <int RT, int D, int NK>
+__device__ void pass2_helper(const TcArgs& a, const SeqTable& t, uint32_t base, uint8_t* sbase,
+                             volatile uint32_t* flag) {
+  using P = Plan<RT, D, NK>;
+  const int lane = threadIdx.x % 32;
+  const uint32_t bars = base + P::kBarOff;
+  auto lse_full = [&](int b) { return bars + 8u * (P::kBar2 + b); };
+  auto lse_free = [&](int b) { return bars + 8u * (P::kBar2 + 2 + b); };
+  auto ss_full = [&](int b) { return bars + 8u * (P::kBar2 + 4 + b); };
+  auto ss_free = [&](int b) { return bars + 8u * (P::kBar2 + 6 + b); };
+  const float* Ss = reinterpret_cast<const float*>(sbase + P::kSsOff);
+  float* lse_s = reinterpret_cast<float*>(sbase + P::kLseOff);
+  const int R = a.sh.R, pr = (a.sh.pool_k - 1) / 2, Pg = a.sh.page_size;
+  const int i0 = item_begin(t.n_items), i1 = item_end(t.n_items), n = i1 - i0;
+  auto stage = [&](int li) {
+    const int b = li & 1;
+    const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(lse_free(b), ((li >> 1) & 1) ^ 1));
+    if (!ok) return false;
+    const Item it = decode<true>(t, a.sh, i0 + li);
+    for (int i = lane; i < RT; i += 32)
+      lse_s[b * RT + i] = i < R ? -a.lse[(int64_t)it.unit * R + i] : -INFINITY;   // padding rows give p = 0
+    __syncwarp();
+    if (lane == 0) mbar_arrive(lse_full(b));
+    return true;
+  };
+  bool ok = true;
+  for (int li = 0; li < 2 && li < n && ok; ++li) ok = stage(li);
+  for (int li = 0; li < n && ok; ++li) {
+    const int b = li & 1;
+    ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(ss_full(b), (li >> 1) & 1));
+    if (!ok) break;
+    const Item it = decode<true>(t, a.sh, i0 + li);
+    const float* Sb = Ss + b * P::kSsFloats;
     const SeqInfo& si = t.s[it.b];
     float* out = a.scores + si.s_off + ((int64_t)it.layer * a.sh.h_kv + it.g) * it.L;
     auto pooled = [&](int tt) {
       const int lo = max(tt - pr, it.ta), hi = min(tt + pr, it.tb - 1);
-      float u = Ss[lo - it.ta];
-      for (int x = lo + 1; x <= hi; ++x) u = fmaxf(u, Ss[x - it.ta]);
+      float u = Sb[lo - it.ta];
+      for (int x = lo + 1; x <= hi; ++x) u = fmaxf(u, Sb[x - it.ta]);
       return u;
     };
-    if (P_ == 1) {
-      for (int tt = it.a0 + e.etid; tt < it.a1; tt += kEpiThreads) out[tt] = pooled(tt);
+    if (Pg == 1) {
+      for (int tt = it.a0 + lane; tt < it.a1; tt += 32) out[tt] = pooled(tt);
     } else {
-      const int n_pages = (it.L + P_ - 1) / P_;
+      const int n_pages = (it.L + Pg - 1) / Pg;
       float* pout = a.page_scores + si.p_off + ((int64_t)it.layer * a.sh.h_kv + it.g) * n_pages;
-      for (int p = it.a0 / P_ + e.etid; p * P_ < it.a1; p += kEpiThreads) {
-        const int lo = p * P_, hi = min(it.a1, lo + P_);
+      for (int p = it.a0 / Pg + lane; p * Pg < it.a1; p += 32) {
+        const int lo = p * Pg, hi = min(it.a1, lo + Pg);
         float pv = 0.f;
         for (int tt = lo; tt < hi; ++tt) {
           const float u = pooled(tt);
@@ -523,12 +562,16 @@ __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base
         pout[p] = pv;
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(ss_free(b));
+    if (li + 2 < n) ok = stage(li + 2);
   }
+  if (!ok && lane == 0) fail(a, flag, kWherePool);
 }
 
 // ---------------------------------------------------------------- kernels
 template <bool PASS2, int RT, int D, int NK, int MAXW>
-__global__ void __launch_bounds__(kThreadsTc, 1) score_tc_kernel(const __grid_constant__ CUtensorMap tq,
+__global__ void __launch_bounds__(PASS2 ? kThreadsTc2 : kThreadsTc, 1) score_tc_kernel(const __grid_constant__ CUtensorMap tq,
                                                                  const __grid_constant__ CUtensorMap tk,
                                                                  const __grid_constant__ TcArgs a,
                                                                  const __grid_constant__ SeqTable t) {
@@ -547,9 +590,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1) score_tc_kernel(const __grid_co
     }
     for (uint32_t s = 0; s < P::kNT; ++s) {
       mbar_init(bars + 8u * (2 * NK + s), 1);          // tfull: MMA commit
-      mbar_init(bars + 8u * (2 * NK + P::kNT + s), kEpiWarps);   // tempty: one arrival per epilogue warp
+      // tempty: every epilogue warp (pass 1) or the warpgroup that owns the tile (pass 2)
+      mbar_init(bars + 8u * (2 * NK + P::kNT + s), PASS2 ? kEpiWarps / 2 : kEpiWarps);
     }
     for (int s = 0; s < 3; ++s) mbar_init(bars + 8u * (2 * NK + 2 * P::kNT + s), 1);   // q_full, q_empty, drain
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bars + 8u * (P::kBar2 + b), 1);                // lse_full: helper staged -lse
+      mbar_init(bars + 8u * (P::kBar2 + 2 + b), kEpiWarps);    // lse_free: every epilogue warp is done with it
+      mbar_init(bars + 8u * (P::kBar2 + 4 + b), kEpiWarps);    // ss_full: every epilogue warp wrote its keys
+      mbar_init(bars + 8u * (P::kBar2 + 6 + b), 1);            // ss_free: helper wrote the segment out
+    }
     *flag = 0;
     fence_barrier_init();
   }
@@ -562,561 +612,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1) score_tc_kernel(const __grid_co
     if (lane == 0) produce<PASS2, RT, D, NK>(&tq, &tk, a, t, base, flag);
   } else if (warp == 1) {
     if (lane == 0) issue_mma<PASS2, RT, D, NK>(a, t, base, tmem, flag);
+  } else if (PASS2 && warp == 2 + kEpiWarps) {
+    pass2_helper<RT, D, NK>(a, t, base, sbase, flag);
   } else if (PASS2) {
     epilogue_pass2<RT, D, NK, MAXW>(a, t, base, sbase, tmem, flag);
   } else {
     epilogue_pass1<RT, D, NK>(a, t, base, sbase, tmem, flag);
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
-  }
-}
-
-// ================================================================ single-read (fused) scoring
-//
-// The CTAs form groups of gs; group q takes units q, q + n_groups, ...  Every
-// unit is split across the gs CTAs of its group.  In step s a CTA runs pass 1
-// over its share of unit U[s] (reading K from HBM) and then pass 2 over its
-// share of unit U[s-1], whose keys the group read one step earlier and which
-// are still in L2, so each key row crosses HBM once.  The row log-sum-exp of a
-// unit needs every CTA of the group: each CTA writes its per-row partial
-// (max, sum) into a ring slot and counts itself in; a merge warp in every CTA
-// then merges the rows that CTA owns (about one row each) and publishes them.
-// Between a unit's pass 1 and its pass 2 every CTA has the next unit's pass 1
-// to do, so the merge is off the critical path.  The launch is cooperative (all CTAs
-// resident), and every cross-CTA wait is bounded.
-constexpr int kFusedSsMax = 2048;   // prefix keys (+ halo) of one CTA's pass-2 share
-
-template <int D, int NK>
-struct FPlan {
-  static constexpr int RT = 128;
-  static constexpr int kDBlocks = D / 64;
-  static constexpr uint32_t kQBlock = RT * 128;
-  static constexpr uint32_t kQBytes = kQBlock * kDBlocks;
-  static constexpr uint32_t kKBlock = kTileKeys * 128;
-  static constexpr uint32_t kKBytes = kKBlock * kDBlocks;
-  static constexpr int kQSlots = 3;                                      // Q of units s, s-1 and s+1
-  static constexpr uint32_t kQOff = 0;
-  static constexpr uint32_t kKOff = kQSlots * kQBytes;
-  static constexpr uint32_t kSsOff = kKOff + NK * kKBytes;
-  static constexpr uint32_t kSsFloats = kFusedSsMax + 192;                // one score buffer; two are kept
-  static constexpr uint32_t kLseOff = kSsOff + 2 * kSsFloats * 4;      // two staged buffers of -lse
-  static constexpr uint32_t kRedOff = kLseOff + 2 * RT * 4;
-  static constexpr uint32_t kNT = kTmemCols / RT;
-  static constexpr uint32_t kBarOff = kRedOff + 128 * 8;
-  // full[NK], empty[NK], tfull[NT], tempty[NT], q_full[3], q_empty[3], drain,
-  // part_done, lse_full[2], lse_free[2], ss_full[2], ss_free[2]
-  static constexpr uint32_t kNumBars = 2 * NK + 2 * kNT + 2 * kQSlots + 1 + 9;
-  static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;           // tmem slot, abort flag, last flag
-  static constexpr uint32_t kBytes = kMiscOff + 16;
-  static constexpr size_t kSmem = kBytes + 1024;
-  static_assert(kSmem <= 227 * 1024, "shared memory plan too large");
-  __device__ static uint32_t full(uint32_t bars, int s) { return bars + 8u * s; }
-  __device__ static uint32_t empty(uint32_t bars, int s) { return bars + 8u * (NK + s); }
-  __device__ static uint32_t tfull(uint32_t bars, int s) { return bars + 8u * (2 * NK + s); }
-  __device__ static uint32_t tempty(uint32_t bars, int s) { return bars + 8u * (2 * NK + kNT + s); }
-  __device__ static uint32_t qfull(uint32_t bars, int q) { return bars + 8u * (2 * NK + 2 * kNT + q); }
-  __device__ static uint32_t qempty(uint32_t bars, int q) { return bars + 8u * (2 * NK + 2 * kNT + kQSlots + q); }
-  __device__ static uint32_t drain(uint32_t bars) { return bars + 8u * (2 * NK + 2 * kNT + 2 * kQSlots); }
-  __device__ static uint32_t part_done(uint32_t bars) { return bars + 8u * (2 * NK + 2 * kNT + 2 * kQSlots + 1); }
-  __device__ static uint32_t lse_full(uint32_t bars, int b) { return bars + 8u * (2 * NK + 2 * kNT + 2 * kQSlots + 2 + b); }
-  __device__ static uint32_t lse_free(uint32_t bars, int b) { return bars + 8u * (2 * NK + 2 * kNT + 2 * kQSlots + 4 + b); }
-  __device__ static uint32_t ss_full(uint32_t bars, int b) { return bars + 8u * (2 * NK + 2 * kNT + 2 * kQSlots + 6 + b); }
-  __device__ static uint32_t ss_free(uint32_t bars, int b) { return bars + 8u * (2 * NK + 2 * kNT + 2 * kQSlots + 8 + b); }
-};
-
-struct FusedArgs {
-  ScoreShape sh;
-  float* scores;
-  float* page_scores;
-  DeviceError* err;
-  float2* part_ring;   // [n_groups][kFusedSlots][R][gs]  per-row partials, CTAs contiguous
-  float* lse_ring;     // [n_groups][kFusedSlots][R]
-  uint32_t* arrive;    // [n_groups][kFusedSlots]  CTAs that wrote their partials (cumulative)
-  uint32_t* merged;    // [n_groups][kFusedSlots]  rows whose log-sum-exp is published (cumulative)
-  int32_t gs, n_groups, n_units;
-};
-
-// One CTA's share of one unit.
-struct Share {
-  int b, layer, g, unit, L, n_keys;
-  int32_t q_row0, k_row0;
-  int ta1, tb1;          // pass-1 keys [ta1, tb1) (prefix and window)
-  int a0, a1;            // pass-2 prefix keys whose scores this CTA emits
-  int ta2, tb2;          // pass-2 keys computed, with the pooling halo
-};
-
-__device__ __forceinline__ void fail_f(const FusedArgs& a, volatile uint32_t* flag, uint32_t where) {
-  set_device_error(a.err, KVSEL_ERR_TIMEOUT, where);
-  *flag = 1;
-}
-
-__device__ __forceinline__ int group_of_cta(const FusedArgs& a) { return blockIdx.x / a.gs; }
-__device__ __forceinline__ int rank_in_group(const FusedArgs& a) { return blockIdx.x % a.gs; }
-__device__ __forceinline__ int units_of_group(const FusedArgs& a, int q) {
-  return q < a.n_units ? (a.n_units - q + a.n_groups - 1) / a.n_groups : 0;
-}
-
-__device__ __forceinline__ Share share_of(const FusedArgs& a, const SeqTable& t, int q, int s) {
-  const ScoreShape& sh = a.sh;
-  Share x;
-  x.unit = q + s * a.n_groups;
-  const int ups = sh.n_layers * sh.h_kv;
-  x.b = x.unit / ups;
-  const int ul = x.unit % ups;
-  x.layer = ul / sh.h_kv;
-  x.g = ul % sh.h_kv;
-  const SeqInfo& si = t.s[x.b];
-  x.L = si.L;
-  x.n_keys = si.n_keys;
-  x.q_row0 = (int32_t)((((int64_t)x.b * sh.n_layers + x.layer) * sh.h_q + (int64_t)x.g * sh.G) * sh.W);
-  x.k_row0 = (int32_t)(si.k_off / sh.d + ((int64_t)x.layer * sh.h_kv + x.g) * si.n_keys);
-  const int r = rank_in_group(a), gs = a.gs;
-  x.ta1 = (int)(((int64_t)r * x.n_keys) / gs);
-  x.tb1 = (int)(((int64_t)(r + 1) * x.n_keys) / gs);
-  const int P = sh.page_size, pr = (sh.pool_k - 1) / 2;
-  const int n_pages = (x.L + P - 1) / P;
-  x.a0 = (int)min((int64_t)x.L, (int64_t)P * (((int64_t)r * n_pages) / gs));
-  x.a1 = (int)min((int64_t)x.L, (int64_t)P * (((int64_t)(r + 1) * n_pages) / gs));
-  if (x.a1 > x.a0) {
-    x.ta2 = max(0, x.a0 - pr);
-    x.tb2 = min(x.L, x.a1 + pr);
-  } else {
-    x.ta2 = x.tb2 = 0;
-  }
-  return x;
-}
-
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ bool wait_at_least(const uint32_t* p, uint32_t target) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
-    if (ld_acquire(p) >= target) return true;
-    __nanosleep(128);
-  }
-  return false;
-}
-
-// ---------------------------------------------------------------- fused producer
-template <int D, int NK>
-__device__ void fused_produce(const CUtensorMap* tq, const CUtensorMap* tk, const FusedArgs& a, const SeqTable& t,
-                              uint32_t base, volatile uint32_t* flag) {
-  using P = FPlan<D, NK>;
-  const uint32_t bars = base + P::kBarOff;
-  tma_prefetch_desc(tq);
-  tma_prefetch_desc(tk);
-  const int q = group_of_cta(a);
-  const int nu = units_of_group(a, q);
-  const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
-  int ks = 0;
-  uint32_t kph = 0, n_fills = 0;
-  uint32_t qph[P::kQSlots] = {0, 0, 0}, n_q[P::kQSlots] = {0, 0, 0};
-  bool ok = true;
-  for (int s = 0; s <= nu && ok && !aborted(flag); ++s) {
-    for (int pass = 0; pass < 2 && ok; ++pass) {
-      if ((pass == 0 && s == nu) || (pass == 1 && s == 0)) continue;
-      const Share x = share_of(a, t, q, pass == 0 ? s : s - 1);
-      if (pass == 0) {
-        const int qs = s % P::kQSlots;
-        if (!mbar_wait(P::qempty(bars, qs), qph[qs] ^ 1)) { ok = false; break; }
-        mbar_expect_tx(P::qfull(bars, qs), P::kQBytes);
-#pragma unroll
-        for (int db = 0; db < P::kDBlocks; ++db)
-          tma_load_2d(base + P::kQOff + qs * P::kQBytes + db * P::kQBlock, tq, db * 64, x.q_row0, P::qfull(bars, qs));
-        qph[qs] ^= 1;
-        ++n_q[qs];
-      }
-      const int ta = pass == 0 ? x.ta1 : x.ta2, tb = pass == 0 ? x.tb1 : x.tb2;
-      // pass-1 tiles stay in L2 for the pass-2 re-read one step later; pass-2 tiles are done
-      const uint64_t policy = pass == 0 ? keep : drop;
-      for (int t0 = ta; t0 < tb; t0 += kTileKeys) {
-        if (!mbar_wait(P::empty(bars, ks), kph ^ 1)) { ok = false; break; }
-        mbar_expect_tx(P::full(bars, ks), P::kKBytes);
-        const uint32_t dst = base + P::kKOff + ks * P::kKBytes;
-#pragma unroll
-        for (int db = 0; db < P::kDBlocks; ++db)
-          tma_load_2d_hint(dst + db * P::kKBlock, tk, db * 64, x.k_row0 + t0, P::full(bars, ks), policy);
-        ++n_fills;
-        if (++ks == NK) { ks = 0; kph ^= 1; }
-      }
-    }
-  }
-  if (!ok) fail_f(a, flag, kWhereProducer);
-  for (int s = 0; s < NK; ++s)
-    if (n_fills > (uint32_t)s) {
-      const uint32_t cnt = (n_fills - s + NK - 1) / NK;
-      if (!mbar_wait(P::full(bars, s), (cnt - 1) & 1)) set_device_error(a.err, KVSEL_ERR_TIMEOUT, kWhereDrain);
-    }
-  for (int qs = 0; qs < P::kQSlots; ++qs)
-    if (n_q[qs] > 0 && !mbar_wait(P::qfull(bars, qs), (n_q[qs] - 1) & 1))
-      set_device_error(a.err, KVSEL_ERR_TIMEOUT, kWhereDrain);
-}
-
-// ---------------------------------------------------------------- fused MMA issuer
-template <int D, int NK>
-__device__ void fused_mma(const FusedArgs& a, const SeqTable& t, uint32_t base, uint32_t tmem, volatile uint32_t* flag) {
-  using P = FPlan<D, NK>;
-  constexpr int RT = P::RT;
-  const uint32_t bars = base + P::kBarOff;
-  constexpr uint32_t idesc1 = umma_idesc_bf16(128, 128);   // rows x keys
-  constexpr uint32_t idesc2 = umma_idesc_bf16(128, RT);    // keys x rows
-  const int q = group_of_cta(a);
-  const int nu = units_of_group(a, q);
-  int ks = 0, ts = 0;
-  uint32_t kph = 0, tph = 0;
-  uint32_t qph[P::kQSlots] = {0, 0, 0};
-  bool ok = true, issued = false;
-  for (int s = 0; s <= nu && ok && !aborted(flag); ++s) {
-    for (int pass = 0; pass < 2 && ok; ++pass) {
-      if ((pass == 0 && s == nu) || (pass == 1 && s == 0)) continue;
-      const Share x = share_of(a, t, q, pass == 0 ? s : s - 1);
-      const int qs = (pass == 0 ? s : s - 1) % P::kQSlots;
-      if (pass == 0) {
-        if (!mbar_wait(P::qfull(bars, qs), qph[qs])) { ok = false; break; }
-        qph[qs] ^= 1;
-      }
-      const uint32_t qbase = base + P::kQOff + qs * P::kQBytes;
-      const int ta = pass == 0 ? x.ta1 : x.ta2, tb = pass == 0 ? x.tb1 : x.tb2;
-      for (int t0 = ta; t0 < tb; t0 += kTileKeys) {
-        if (!mbar_wait(P::full(bars, ks), kph) || !mbar_wait(P::tempty(bars, ts), tph ^ 1)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t kbase = base + P::kKOff + ks * P::kKBytes;
-        const uint32_t d_tmem = tmem + ts * RT;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t db = kk >> 2, off = (kk & 3) * 32;
-          if (pass == 0)
-            umma_bf16(d_tmem, umma_desc_sw128(qbase + db * P::kQBlock + off),
-                      umma_desc_sw128(kbase + db * P::kKBlock + off), idesc1, kk > 0);
-          else
-            umma_bf16(d_tmem, umma_desc_sw128(kbase + db * P::kKBlock + off),
-                      umma_desc_sw128(qbase + db * P::kQBlock + off), idesc2, kk > 0);
-        }
-        issued = true;
-        umma_commit(P::empty(bars, ks));
-        umma_commit(P::tfull(bars, ts));
-        if (++ks == NK) { ks = 0; kph ^= 1; }
-        if (++ts == (int)P::kNT) { ts = 0; tph ^= 1; }
-      }
-      if (pass == 1) umma_commit(P::qempty(bars, qs));   // this Q slot is free once these MMAs finish
-    }
-  }
-  if (!ok) fail_f(a, flag, kWhereMma);
-  if (issued) {
-    umma_commit(P::drain(bars));
-    if (!mbar_wait(P::drain(bars), 0)) set_device_error(a.err, KVSEL_ERR_TIMEOUT, kWhereDrain);
-  }
-}
-
-// ---------------------------------------------------------------- fused epilogue
-// Merge warp (one per CTA): for each unit of the group, once all gs CTAs have written their
-// partials, merge the rows this CTA owns (rows rank, rank + gs, ...) in a fixed order and
-// publish them.  It runs ahead of the epilogue, so the merge overlaps the next unit's pass 1.
-template <int D, int NK>
-__device__ void fused_merge(const FusedArgs& a, uint32_t base, uint8_t* sbase, volatile uint32_t* flag) {
-  using P = FPlan<D, NK>;
-  const uint32_t bars = base + P::kBarOff;
-  float* lse_buf = reinterpret_cast<float*>(sbase + P::kLseOff);
-  const int lane = threadIdx.x % 32;
-  const int q = group_of_cta(a), rank = rank_in_group(a);
-  const int nu = units_of_group(a, q);
-  const int R = a.sh.R;
-  auto lane0_ok = [&](bool ok) { return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0; };
-  for (int s = 0; s < nu; ++s) {
-    const int slot = s % kFusedSlots;
-    const uint32_t use = (uint32_t)(s / kFusedSlots);
-    uint32_t* arrive = &a.arrive[q * kFusedSlots + slot];
-    uint32_t* merged = &a.merged[q * kFusedSlots + slot];
-    // 1. count this CTA in once its epilogue has written the unit's partials
-    bool ok = true;
-    if (lane == 0) ok = !aborted(flag) && mbar_wait(P::part_done(bars), s & 1);
-    if (!lane0_ok(ok)) {
-      if (lane == 0) fail_f(a, flag, kWhereMerge);
-      break;
-    }
-    if (lane == 0) {
-      __threadfence();
-      atomicAdd(arrive, 1u);
-    }
-    // 2. once every CTA of the group is in, merge the rows this CTA owns
-    if (lane == 0) ok = wait_at_least(arrive, (uint32_t)a.gs * (use + 1));
-    if (!lane0_ok(ok)) {
-      if (lane == 0) fail_f(a, flag, kWhereMerge);
-      break;
-    }
-    const float2* part = a.part_ring + ((size_t)q * kFusedSlots + slot) * R * a.gs;
-    float* lse = a.lse_ring + ((size_t)q * kFusedSlots + slot) * R;
-    uint32_t mine = 0;
-    for (int r = rank; r < R; r += a.gs) {
-      float m = -INFINITY, l = 0.f;
-      for (int c = lane; c < a.gs; c += 32) {
-        const float2 pv = __ldcg(part + (size_t)r * a.gs + c);
-        if (pv.x > -INFINITY) {
-          const float nm = fmaxf(m, pv.x);
-          l = l * exp2f(m - nm) + pv.y * exp2f(pv.x - nm);
-          m = nm;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-        const float l2 = __shfl_xor_sync(0xffffffffu, l, o);
-        const float nm = fmaxf(m, m2);
-        if (nm > -INFINITY) {
-          l = (m > -INFINITY ? l * exp2f(m - nm) : 0.f) + (m2 > -INFINITY ? l2 * exp2f(m2 - nm) : 0.f);
-          m = nm;
-        }
-      }
-      if (lane == 0) lse[r] = m + log2f(l);
-      ++mine;
-    }
-    __syncwarp();
-    if (lane == 0 && mine > 0) {
-      __threadfence();
-      atomicAdd(merged, mine);
-    }
-    // 3. once every row is published, stage -lse into shared memory for this CTA's pass 2
-    const int b = s & 1;
-    if (lane == 0) ok = wait_at_least(merged, (uint32_t)R * (use + 1)) &&
-                        mbar_wait(P::lse_free(bars, b), ((s >> 1) & 1) ^ 1);
-    if (!lane0_ok(ok)) {
-      if (lane == 0) fail_f(a, flag, kWhereMerge);
-      break;
-    }
-    for (int i = lane; i < P::RT; i += 32) lse_buf[b * P::RT + i] = i < R ? -__ldcg(lse + i) : -INFINITY;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(P::lse_full(bars, b));
-  }
-}
-
-// Epilogue: the two warpgroups take alternate tiles of the stream (warpgroup e takes tiles whose
-// running index is e mod 2), each covering all 128 TMEM columns of its tiles, so the two warps that
-// share a scheduler sit in different phases.  Pass 1: online (max, sum) per row, merged across the
-// warpgroups at the end of the unit.  Pass 2: every key's group score written by the one thread that
-// owns it.
-template <int D, int NK, int MAXW>
-__device__ void fused_epilogue(const FusedArgs& a, const SeqTable& t, uint32_t base, uint8_t* sbase, uint32_t tmem,
-                               volatile uint32_t* flag) {
-  using P = FPlan<D, NK>;
-  constexpr int RT = P::RT;
-  const uint32_t bars = base + P::kBarOff;
-  const EpiThread e = epi_thread();
-  float* Ss = reinterpret_cast<float*>(sbase + P::kSsOff);
-  const float* lse_s = reinterpret_cast<const float*>(sbase + P::kLseOff);
-  float* red = reinterpret_cast<float*>(sbase + P::kRedOff);
-  const float scale = a.sh.scale_log2;
-  const int R = a.sh.R;
-  const int q = group_of_cta(a), rank = rank_in_group(a);
-  const int nu = units_of_group(a, q);
-  const uint32_t lane_base = (uint32_t)(e.quarter * 32) << 16;
-  uint32_t tile = 0;          // running index of the tile stream (both warpgroups count every tile)
-  for (int s = 0; s <= nu; ++s) {
-    // ------------------------------------------------ pass 1 of unit s
-    if (s < nu) {
-      const Share x = share_of(a, t, q, s);
-      const bool rvalid = e.lrow < R;
-      const int vis_end = min(x.tb1, x.L + (rvalid ? e.lrow % a.sh.W : 0) + 1);
-      float m = -INFINITY, l = 0.f;
-      for (int t0 = x.ta1; t0 < x.tb1; t0 += kTileKeys, ++tile) {
-        if ((int)(tile & 1) != e.wg) continue;
-        const int ts = (int)(tile % P::kNT);
-        const uint32_t tph = (tile / P::kNT) & 1;
-        const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(P::tfull(bars, ts), tph));
-        if (!ok && e.lane == 0) fail_f(a, flag, kWhereEpilogue);
-        if (ok) {
-          tc_fence_after();
-          float v[64], w[64];
-          tmem_ld64(tmem + lane_base + ts * RT, v);
-          tmem_ld64(tmem + lane_base + ts * RT + 64, w);
-          tc_fence_before();
-          __syncwarp();
-          if (e.lane == 0) mbar_arrive(P::tempty(bars, ts));
-          if (rvalid) {
-            online_update64(v, vis_end - t0, scale, m, l);
-            online_update64(w, vis_end - (t0 + 64), scale, m, l);
-          }
-        }
-      }
-      // this CTA's partial (max, sum) per row of unit s; the merge warp counts the CTA in
-      const int slot = s % kFusedSlots;
-      epi_sync();
-      if (e.wg == 1) {
-        red[2 * e.lrow] = m;
-        red[2 * e.lrow + 1] = l;
-      }
-      epi_sync();
-      if (e.wg == 0) {
-        if (rvalid) {
-          const float m2 = red[2 * e.lrow], l2 = red[2 * e.lrow + 1];
-          const float M = fmaxf(m, m2);
-          float S = 0.f;
-          if (M > -INFINITY)
-            S = (m > -INFINITY ? l * fast_ex2(m - M) : 0.f) + (m2 > -INFINITY ? l2 * fast_ex2(m2 - M) : 0.f);
-          a.part_ring[(((size_t)q * kFusedSlots + slot) * R + e.lrow) * a.gs + rank] = make_float2(M, S);
-        }
-        __syncwarp();
-        if (e.lane == 0) mbar_arrive(P::part_done(bars));
-      }
-    }
-    // ------------------------------------------------ pass 2 of unit s - 1
-    if (s >= 1) {
-      const Share x = share_of(a, t, q, s - 1);
-      const int b = (s - 1) & 1;
-      // -lse of the unit (staged by the merge warp) and a free score buffer (released by the pool warp)
-      const bool ready = __all_sync(0xffffffffu, !aborted(flag) &&
-                                                     mbar_wait(P::lse_full(bars, b), ((s - 1) >> 1) & 1) &&
-                                                     mbar_wait(P::ss_free(bars, b), (((s - 1) >> 1) & 1) ^ 1));
-      if (!ready && e.lane == 0) fail_f(a, flag, kWhereEpilogue);
-      const float* nlse = lse_s + b * RT;
-      float* Ssb = Ss + b * P::kSsFloats;
-      for (int t0 = x.ta2; t0 < x.tb2; t0 += kTileKeys, ++tile) {
-        if ((int)(tile & 1) != e.wg) continue;
-        const int ts = (int)(tile % P::kNT);
-        const uint32_t tph = (tile / P::kNT) & 1;
-        const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(P::tfull(bars, ts), tph));
-        if (!ok && e.lane == 0) fail_f(a, flag, kWhereEpilogue);
-        if (ok) {
-          tc_fence_after();
-          float v[64];
-          float nl[64];
-          tmem_ld64(tmem + lane_base + ts * RT, v);
-#pragma unroll
-          for (int i = 0; i < 64; i += 4) *reinterpret_cast<float4*>(nl + i) = *reinterpret_cast<const float4*>(nlse + i);
-          const float r0 = colmass64<MAXW>(v, nl, scale);
-          tmem_ld64(tmem + lane_base + ts * RT + 64, v);
-          tc_fence_before();
-          __syncwarp();
-          if (e.lane == 0) mbar_arrive(P::tempty(bars, ts));
-#pragma unroll
-          for (int i = 0; i < 64; i += 4) *reinterpret_cast<float4*>(nl + i) = *reinterpret_cast<const float4*>(nlse + 64 + i);
-          const float r1 = colmass64<MAXW>(v, nl, scale);
-          const float redv = MAXW == 0 ? r0 + r1 : fmaxf(r0, r1);
-          const int key = t0 + e.lrow;
-          if (key < x.tb2) Ssb[key - x.ta2] = redv;
-        }
-      }
-      // hand the unit's group scores to the pool warp; the staged -lse is no longer needed
-      __syncwarp();
-      if (e.lane == 0) {
-        mbar_arrive(P::ss_full(bars, b));
-        mbar_arrive(P::lse_free(bars, b));
-      }
-    }
-  }
-}
-
-// Pool warp: max-pool and page reduce of each unit's pass-2 share from the score buffer, while
-// the epilogue goes on with the next unit (DELTA, 'Key designs' 2-3; CLAA, pooling kernel 7).
-template <int D, int NK>
-__device__ void fused_pool(const FusedArgs& a, const SeqTable& t, uint32_t base, uint8_t* sbase,
-                           volatile uint32_t* flag) {
-  using P = FPlan<D, NK>;
-  const uint32_t bars = base + P::kBarOff;
-  const float* Ss = reinterpret_cast<const float*>(sbase + P::kSsOff);
-  const int lane = threadIdx.x % 32;
-  const int q = group_of_cta(a);
-  const int nu = units_of_group(a, q);
-  const int pr = (a.sh.pool_k - 1) / 2;
-  const int Pg = a.sh.page_size;
-  for (int u = 0; u < nu; ++u) {
-    const int b = u & 1;
-    const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(P::ss_full(bars, b), (u >> 1) & 1));
-    if (!ok) {
-      if (lane == 0) fail_f(a, flag, kWherePool);
-      return;
-    }
-    const Share x = share_of(a, t, q, u);
-    const float* Sb = Ss + b * P::kSsFloats;
-    const SeqInfo& si = t.s[x.b];
-    float* out = a.scores + si.s_off + ((int64_t)x.layer * a.sh.h_kv + x.g) * x.L;
-    auto pooled = [&](int tt) {
-      const int lo = max(tt - pr, x.ta2), hi = min(tt + pr, x.tb2 - 1);
-      float v = Sb[lo - x.ta2];
-      for (int y = lo + 1; y <= hi; ++y) v = fmaxf(v, Sb[y - x.ta2]);
-      return v;
-    };
-    if (Pg == 1) {
-      for (int tt = x.a0 + lane; tt < x.a1; tt += 32) out[tt] = pooled(tt);
-    } else {
-      const int n_pages = (x.L + Pg - 1) / Pg;
-      float* pout = a.page_scores + si.p_off + ((int64_t)x.layer * a.sh.h_kv + x.g) * n_pages;
-      for (int p = x.a0 / Pg + lane; p * Pg < x.a1; p += 32) {
-        const int lo = p * Pg, hi = min(x.a1, lo + Pg);
-        float pv = 0.f;
-        for (int tt = lo; tt < hi; ++tt) {
-          const float v = pooled(tt);
-          out[tt] = v;
-          pv = (tt == lo) ? v : (a.sh.page_reduce == KVSEL_REDUCE_MAX ? fmaxf(pv, v) : pv + v);
-        }
-        pout[p] = pv;
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(P::ss_free(bars, b));
-  }
-}
-
-constexpr int kThreadsFused = kThreadsTc + 64;   // + the merge warp and the pool warp
-
-template <int D, int NK, int MAXW>
-__global__ void __launch_bounds__(kThreadsFused, 1) score_fused_kernel(const __grid_constant__ CUtensorMap tq,
-                                                                    const __grid_constant__ CUtensorMap tk,
-                                                                    const __grid_constant__ FusedArgs a,
-                                                                    const __grid_constant__ SeqTable t) {
-  using P = FPlan<D, NK>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t base = smem_addr(sbase);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(sbase + P::kMiscOff);
-  volatile uint32_t* flag = reinterpret_cast<volatile uint32_t*>(sbase + P::kMiscOff + 4);
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  if (threadIdx.x == 0) {
-    const uint32_t bars = base + P::kBarOff;
-    for (int s = 0; s < NK; ++s) {
-      mbar_init(P::full(bars, s), 1);
-      mbar_init(P::empty(bars, s), 1);
-    }
-    for (uint32_t s = 0; s < P::kNT; ++s) {
-      mbar_init(P::tfull(bars, s), 1);
-      mbar_init(P::tempty(bars, s), kEpiWarps / 2);   // the warpgroup that owns the tile
-    }
-    for (int s = 0; s < P::kQSlots; ++s) {
-      mbar_init(P::qfull(bars, s), 1);
-      mbar_init(P::qempty(bars, s), 1);
-    }
-    mbar_init(P::drain(bars), 1);
-    mbar_init(P::part_done(bars), 4);            // one arrival per warp of epilogue warpgroup 0
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(P::lse_full(bars, b), 1);          // merge warp staged -lse
-      mbar_init(P::lse_free(bars, b), kEpiWarps);  // every epilogue warp read it
-      mbar_init(P::ss_full(bars, b), kEpiWarps);   // every epilogue warp added its column mass
-      mbar_init(P::ss_free(bars, b), 1);           // pool warp wrote the scores out
-    }
-    *flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) tmem_alloc(smem_addr(tslot), kTmemCols);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tslot;
-  if (warp == 0) {
-    if (lane == 0) fused_produce<D, NK>(&tq, &tk, a, t, base, flag);
-  } else if (warp == 1) {
-    if (lane == 0) fused_mma<D, NK>(a, t, base, tmem, flag);
-  } else if (warp < 2 + kEpiWarps) {
-    fused_epilogue<D, NK, MAXW>(a, t, base, sbase, tmem, flag);
-  } else if (warp == 2 + kEpiWarps) {
-    fused_merge<D, NK>(a, base, sbase, flag);
-  } else {
-    fused_pool<D, NK>(a, t, base, sbase, flag);
   }
   tc_fence_before();
   __syncthreads();
@@ -1180,7 +681,7 @@ kvsel_status launch_one(const char* name, const CUtensorMap& tq, const CUtensorM
   if (set_smem((const void*)kern, P::kSmem) != cudaSuccess) return KVSEL_ERR_CUDA;
   const int grid = t.n_items < sms ? t.n_items : sms;
   TraceScope ts(name, s);
-  kern<<<grid, kThreadsTc, P::kSmem, s>>>(tq, tk, a, t);
+  kern<<<grid, PASS2 ? kThreadsTc2 : kThreadsTc, P::kSmem, s>>>(tq, tk, a, t);
   return launch_status();
 }
 
@@ -1201,83 +702,11 @@ kvsel_status run_tc(const TcArgs& a, const SeqTable& t1, const SeqTable& t2, con
   return KVSEL_ERR_UNSUPPORTED;
 }
 
-// Groups of gs CTAs share each unit.  Two units per group are live in L2 at a time (pass 1 of
-// one, pass 2 of the previous), so the number of groups is bounded by the L2 budget; each CTA's
-// pass-2 share (+ halo) must fit the shared-memory score buffer.
-bool plan_fused(const ScoreShape& sh, const SeqTable& base, int sms, int* gs_out, int* ng_out) {
-  if (sh.R > 128) return false;
-  const int ctas = sms < kFusedMaxCtas ? sms : kFusedMaxCtas;
-  const int64_t units = (int64_t)base.batch * sh.n_layers * sh.h_kv;
-  int64_t max_keys = 0, max_L = 0;
-  for (int b = 0; b < base.batch; ++b) {
-    max_keys = base.s[b].n_keys > max_keys ? base.s[b].n_keys : max_keys;
-    max_L = base.s[b].L > max_L ? base.s[b].L : max_L;
-  }
-  const double l2_budget = 72e6;
-  const double unit_bytes = (double)max_keys * sh.d * 2;
-  int64_t ng = (int64_t)(l2_budget / (2.0 * unit_bytes));
-  if (ng < 1) ng = 1;
-  if (ng > units) ng = units;
-  if (ng > ctas) ng = ctas;
-  const int P = sh.page_size, pr = (sh.pool_k - 1) / 2;
-  const int64_t pages = (max_L + P - 1) / P;
-  for (; ng >= 1; --ng) {
-    const int64_t gs = ctas / ng;
-    const int64_t share = (int64_t)P * ((pages + gs - 1) / gs) + 2 * pr;
-    if (share <= kFusedSsMax + 64) {
-      *gs_out = (int)gs;
-      *ng_out = (int)ng;
-      return true;
-    }
-  }
-  return false;
-}
-
-template <int D, int NK, int MAXW>
-kvsel_status launch_fused_one(const CUtensorMap& tq, const CUtensorMap& tk, const FusedArgs& a, const SeqTable& t,
-                              cudaStream_t s) {
-  using P = FPlan<D, NK>;
-  auto kern = score_fused_kernel<D, NK, MAXW>;
-  if (set_smem((const void*)kern, P::kSmem) != cudaSuccess) return KVSEL_ERR_CUDA;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(a.gs * a.n_groups));
-  cfg.blockDim = dim3(kThreadsFused);
-  cfg.dynamicSmemBytes = P::kSmem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;   // every CTA resident: they wait on one another
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  TraceScope ts("score_fused_tc", s);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tq, tk, a, t);
-  count_launch();
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return KVSEL_ERR_CUDA;
-  }
-  return cudaGetLastError() == cudaSuccess ? KVSEL_OK : KVSEL_ERR_CUDA;
-}
-
-template <int D>
-kvsel_status run_fused(const FusedArgs& a, const SeqTable& t, const CUtensorMap& tq, const CUtensorMap& tk,
-                       cudaStream_t s) {
-  constexpr int NK = D == 128 ? 3 : 4;
-  if (a.sh.group_reduce == KVSEL_REDUCE_SUM) return launch_fused_one<D, NK, 0>(tq, tk, a, t, s);
-  switch (a.sh.W) {
-    case 8: return launch_fused_one<D, NK, 8>(tq, tk, a, t, s);
-    case 16: return launch_fused_one<D, NK, 16>(tq, tk, a, t, s);
-    case 32: return launch_fused_one<D, NK, 32>(tq, tk, a, t, s);
-    case 64: return launch_fused_one<D, NK, 64>(tq, tk, a, t, s);
-  }
-  return KVSEL_ERR_UNSUPPORTED;
-}
-
 }  // namespace
 
 kvsel_status launch_score(const ScoreShape& sh_in, const SeqTable& base, const void* q, const void* k,
-                          float* scores, float* page_scores, float* lse, float2* part, void* fused_ws,
-                          DeviceError* err, cudaStream_t s) {
+                          float* scores, float* page_scores, float* lse, float2* part, DeviceError* err,
+                          cudaStream_t s) {
   ScoreShape sh = sh_in;
   const int64_t ups = (int64_t)sh.n_layers * sh.h_kv;
   int64_t k_rows = 0;
@@ -1297,25 +726,8 @@ kvsel_status launch_score(const ScoreShape& sh_in, const SeqTable& base, const v
   }
   CUtensorMap tq, tk;
   if (!make_map(&tq, q, q_rows, sh.d) || !make_map(&tk, k, k_rows, sh.d)) return KVSEL_ERR_CUDA;
-  int gs = 0, ng = 0;
-  if (plan_fused(sh, base, dev.sms, &gs, &ng)) {
-    FusedArgs f;
-    f.sh = sh;
-    f.scores = scores;
-    f.page_scores = page_scores;
-    f.err = err;
-    char* fw = static_cast<char*>(fused_ws);
-    f.part_ring = reinterpret_cast<float2*>(fw);
-    f.lse_ring = reinterpret_cast<float*>(fw + fused_part_bytes(sh.R));
-    f.arrive = reinterpret_cast<uint32_t*>(fw + fused_part_bytes(sh.R) + fused_lse_bytes(sh.R));
-    f.merged = f.arrive + kFusedSlots * kFusedMaxCtas;
-    f.gs = gs;
-    f.n_groups = ng;
-    f.n_units = (int32_t)(ups * base.batch);
-    if (cudaMemsetAsync(f.arrive, 0, fused_flag_bytes(), s) != cudaSuccess) return KVSEL_ERR_CUDA;
-    return sh.d == 64 ? run_fused<64>(f, base, tq, tk, s) : run_fused<128>(f, base, tq, tk, s);
-  }
-  sh.seg2 = (int32_t)(sh.page_size * (kSeg2Max / sh.page_size));
+  // whole pages, and the segment plus its pooling halo fills whole tiles of the score buffer
+  sh.seg2 = (int32_t)(sh.page_size * ((kSeg2Max - (sh.pool_k - 1)) / sh.page_size));
   const SeqTable t2 = with_items(base, ups, sh.seg2, false, sh.W);
   TcArgs a;
   a.sh = sh;

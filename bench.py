@@ -164,8 +164,6 @@ def kernel_bytes(w, n_sel_rows):
     return {
         "score_pass1_simt": pass1, "score_pass1_tc": pass1,
         "score_pass2_simt": pass2, "score_pass2_tc": pass2,
-        # single-read kernel: K once (pass 2 re-reads each unit from L2), plus Q and the outputs
-        "score_fused_tc": k_all + q_bytes + score_w + page_w,
         "topk_radix": sel_read + idx_w,
         "kv_compact": gather + idx_w,
     }
