@@ -34,12 +34,11 @@ constexpr int kTileKeys = 128;
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kThreadsTc = 32 * (2 + kEpiWarps);
-constexpr int kThreadsTc2 = kThreadsTc + 32;      // pass 2 adds the helper warp
-constexpr int kSeg2Max = 4096;     // keys per pass-2 segment, pooling halo included
+constexpr int kSeg2Max = 8192;     // prefix keys per pass-2 segment (rounded down to whole pages)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kEpiBarrier = 1;   // named barrier id of the epilogue warps
 
-enum : uint32_t { kWhereProducer = 1, kWhereMma = 2, kWhereEpilogue = 3, kWhereDrain = 4, kWherePool = 5 };
+enum : uint32_t { kWhereProducer = 1, kWhereMma = 2, kWhereEpilogue = 3, kWhereDrain = 4 };
 
 // Shared-memory plan (offsets from a 1024-byte aligned base).
 template <int RT, int D, int NK>
@@ -51,16 +50,14 @@ struct Plan {
   static constexpr uint32_t kKBytes = kKBlock * kDBlocks;
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kKOff = kQOff + kQBytes;
-  static constexpr uint32_t kSsOff = kKOff + NK * kKBytes;                 // pass 2: two segment score buffers
-  static constexpr uint32_t kSsFloats = kSeg2Max + 32;
-  static constexpr uint32_t kLseOff = kSsOff + 2 * kSsFloats * 4;         // pass 2: two buffers of -lse (RT each)
-  static constexpr uint32_t kRedOff = kLseOff + 2 * RT * 4;               // pass-1 (m, l) exchange
+  static constexpr uint32_t kSsOff = kKOff + NK * kKBytes;                 // pass-2 segment scores
+  static constexpr uint32_t kSsFloats = kSeg2Max + 128;
+  static constexpr uint32_t kLseOff = kSsOff + kSsFloats * 4;             // pass-2 row lse (RT floats)
+  static constexpr uint32_t kRedOff = kLseOff + RT * 4;                   // pass-1 (m, l) exchange
   static constexpr uint32_t kNT = kTmemCols / RT;                         // TMEM accumulator stages
   static constexpr uint32_t kBarOff = kRedOff + 128 * 8;
-  // barriers: full[NK], empty[NK], tfull[NT], tempty[NT], q_full, q_empty, drain,
-  // pass 2: lse_full[2], lse_free[2], ss_full[2], ss_free[2]
-  static constexpr uint32_t kNumBars = 2 * NK + 2 * kNT + 3 + 8;
-  static constexpr uint32_t kBar2 = 2 * NK + 2 * kNT + 3;
+  // barriers: full[NK], empty[NK], tfull[NT], tempty[NT], q_full, q_empty, drain
+  static constexpr uint32_t kNumBars = 2 * NK + 2 * kNT + 3;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;            // tmem slot, abort flag
   static constexpr uint32_t kBytes = kMiscOff + 16;
   static constexpr size_t kSmem = kBytes + 1024;                          // + alignment slack
@@ -434,144 +431,131 @@ __device__ void epilogue_pass1(const TcArgs& a, const SeqTable& t, uint32_t base
   }
 }
 
+// Max-pool of a segment's group scores S[ta..tb) (the pooling halo included) into out[a0..a1), and,
+// with P > 1, page reduce into pout over the pages of [a0, a1).  Window loads are independent of one
+// another, so they overlap instead of forming a chain of shared-memory latencies.
+__device__ __forceinline__ float window_max(const float* S, int ta, int tb, int tt, int pr) {
+  float u = -INFINITY;
+  if (pr <= 3) {
+    float w[7];
+#pragma unroll
+    for (int x = 0; x < 7; ++x) {
+      const int y = tt - 3 + x;
+      w[x] = (x >= 3 - pr && x <= 3 + pr && y >= ta && y < tb) ? S[y - ta] : -INFINITY;
+    }
+    u = fmaxf(fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3])), fmaxf(fmaxf(w[4], w[5]), w[6]));
+  } else {
+    const int lo = max(tt - pr, ta), hi = min(tt + pr, tb - 1);
+#pragma unroll 8
+    for (int y = lo; y <= hi; ++y) u = fmaxf(u, S[y - ta]);
+  }
+  return u;
+}
+
+__device__ void pool_segment(const float* S, int ta, int tb, int a0, int a1, int pr, int P, int page_reduce,
+                             float* out, float* pout, int tid, int nthreads) {
+#pragma unroll 4
+  for (int tt = a0 + tid; tt < a1; tt += nthreads) out[tt] = window_max(S, ta, tb, tt, pr);
+  if (P == 1) return;
+  for (int p = a0 / P + tid; p * P < a1; p += nthreads) {
+    const int lo = p * P, hi = min(a1, lo + P);
+    float pv;
+    if (page_reduce == KVSEL_REDUCE_MAX) {
+      // the max over the page of the pooled scores is the max over the page widened by the window
+      const int wlo = max(lo - pr, ta), whi = min(hi - 1 + pr, tb - 1);
+      pv = -INFINITY;
+#pragma unroll 8
+      for (int y = wlo; y <= whi; ++y) pv = fmaxf(pv, S[y - ta]);
+    } else {
+      pv = 0.f;
+      for (int tt = lo; tt < hi; ++tt) pv += window_max(S, ta, tb, tt, pr);
+    }
+    pout[p] = pv;
+  }
+}
+
 // ---------------------------------------------------------------- pass 2 epilogue
-// Thread = key (TMEM lane).  The two warpgroups take alternate tiles of the stream (warpgroup e the
-// tiles whose running index is e mod 2) and each covers all RT rows of its tiles, so every key's group
-// score is written by exactly one thread.  -lse arrives staged in shared memory from the helper warp,
-// and the helper warp pools each finished segment while the epilogue goes on with the next one.
+// Thread = key (TMEM lane); warpgroup e takes rows [e RT/2, (e+1) RT/2) (TMEM columns).
 // MAXW = 0: group sum (every row summed); otherwise group max with head width MAXW.
 template <int RT, int D, int NK, int MAXW>
 __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base, uint8_t* sbase,
                                uint32_t tmem, volatile uint32_t* flag) {
   using P = Plan<RT, D, NK>;
+  constexpr int kHalf = RT / 2;
+  constexpr int kChunks = kHalf / 32;
   const EpiThread e = epi_thread();
   const uint32_t bars = base + P::kBarOff;
   auto tfull = [&](int s) { return bars + 8u * (2 * NK + s); };
   auto tempty = [&](int s) { return bars + 8u * (2 * NK + P::kNT + s); };
-  auto lse_full = [&](int b) { return bars + 8u * (P::kBar2 + b); };
-  auto lse_free = [&](int b) { return bars + 8u * (P::kBar2 + 2 + b); };
-  auto ss_full = [&](int b) { return bars + 8u * (P::kBar2 + 4 + b); };
-  auto ss_free = [&](int b) { return bars + 8u * (P::kBar2 + 6 + b); };
   float* Ss = reinterpret_cast<float*>(sbase + P::kSsOff);
-  const float* lse_s = reinterpret_cast<const float*>(sbase + P::kLseOff);
+  float* lse_s = reinterpret_cast<float*>(sbase + P::kLseOff);   // holds -lse per row
+  const float* nlse = lse_s;
   const float scale = a.sh.scale_log2;
-  const uint32_t lane_base = (uint32_t)(e.quarter * 32) << 16;
-  uint32_t tile = 0;
-  const int i0 = item_begin(t.n_items), i1 = item_end(t.n_items);
-  for (int item = i0; item < i1; ++item) {
+  const int col0 = e.wg * kHalf;
+  const int pr = (a.sh.pool_k - 1) / 2;
+  const int P_ = a.sh.page_size;
+  int ts = 0;
+  uint32_t tph = 0;
+  const int i1 = item_end(t.n_items);
+  for (int item = item_begin(t.n_items); item < i1; ++item) {
     const Item it = decode<true>(t, a.sh, item);
-    const int li = item - i0, b = li & 1;
-    const bool ready = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(lse_full(b), (li >> 1) & 1) &&
-                                                   mbar_wait(ss_free(b), ((li >> 1) & 1) ^ 1));
-    if (!ready && e.lane == 0) fail(a, flag, kWhereEpilogue);
-    const float* nlse = lse_s + b * RT;
-    float* Ssb = Ss + b * P::kSsFloats;
-    for (int t0 = it.ta; t0 < it.tb; t0 += kTileKeys, ++tile) {
-      if ((int)(tile & 1) != e.wg) continue;
-      const int ts = (int)(tile % P::kNT);
-      const uint32_t tph = (tile / P::kNT) & 1;
+    epi_sync();                                          // readers of the previous item are done
+    for (int i = e.etid; i < it.tb - it.ta; i += kEpiThreads) Ss[i] = 0.f;
+    for (int i = e.etid; i < RT; i += kEpiThreads)
+      lse_s[i] = i < a.sh.R ? -a.lse[(int64_t)it.unit * a.sh.R + i] : -INFINITY;   // padding rows give p = 0
+    epi_sync();
+    for (int t0 = it.ta; t0 < it.tb; t0 += kTileKeys) {
       // the tensor-memory loads below are warp-collective: decide per warp
       const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(tfull(ts), tph));
       if (!ok && e.lane == 0) fail(a, flag, kWhereEpilogue);
-      if (!ok) continue;
-      tc_fence_after();
-      float red = 0.f;
-#pragma unroll
-      for (int c = 0; c < RT / 64; ++c) {
-        float v[64], nl[64];
-        tmem_ld64(tmem + lane_base + ts * RT + c * 64, v);
-        if (c == RT / 64 - 1) {
+      if (ok) {
+        tc_fence_after();
+        const uint32_t taddr = tmem + ((uint32_t)(e.quarter * 32) << 16) + ts * RT + col0;
+        float red;
+        if (kChunks == 2) {
+          float v64[64];
+          tmem_ld64(taddr, v64);
           tc_fence_before();
           __syncwarp();
           if (e.lane == 0) mbar_arrive(tempty(ts));
+          red = colmass64<MAXW>(v64, nlse + col0, scale);
+        } else {
+          float v64[64], w64[64];
+          tmem_ld64(taddr, v64);
+          tmem_ld64(taddr + 64, w64);
+          tc_fence_before();
+          __syncwarp();
+          if (e.lane == 0) mbar_arrive(tempty(ts));
+          const float r0 = colmass64<MAXW>(v64, nlse + col0, scale);
+          const float r1 = colmass64<MAXW>(w64, nlse + col0 + 64, scale);
+          red = MAXW == 0 ? r0 + r1 : fmaxf(r0, r1);
         }
-#pragma unroll
-        for (int i = 0; i < 64; i += 4)
-          *reinterpret_cast<float4*>(nl + i) = *reinterpret_cast<const float4*>(nlse + c * 64 + i);
-        const float r = colmass64<MAXW>(v, nl, scale);
-        red = (c == 0) ? r : (MAXW == 0 ? red + r : fmaxf(red, r));
+        const int key = t0 + e.lrow;
+        if (key < it.tb) {
+          // two addends per key (one per warpgroup): the result does not depend on their order
+          if constexpr (MAXW == 0) atomicAdd(&Ss[key - it.ta], red);
+          else atomicMax(reinterpret_cast<int*>(&Ss[key - it.ta]), __float_as_int(red));
+        }
       }
-      const int key = t0 + e.lrow;
-      if (key < it.tb) Ssb[key - it.ta] = red;
+      if (++ts == (int)P::kNT) { ts = 0; tph ^= 1; }
     }
-    // the segment's group scores go to the helper warp; the staged -lse is no longer needed
-    __syncwarp();
-    if (e.lane == 0) {
-      mbar_arrive(ss_full(b));
-      mbar_arrive(lse_free(b));
-    }
-  }
-}
-
-// Helper warp of pass 2: stages each segment's -lse (two segments ahead) and max-pools / page-reduces
-// each finished segment (CLAA, pooling with kernel 7; DELTA, 'Key designs' 2-3).
-template <int RT, int D, int NK>
-__device__ void pass2_helper(const TcArgs& a, const SeqTable& t, uint32_t base, uint8_t* sbase,
-                             volatile uint32_t* flag) {
-  using P = Plan<RT, D, NK>;
-  const int lane = threadIdx.x % 32;
-  const uint32_t bars = base + P::kBarOff;
-  auto lse_full = [&](int b) { return bars + 8u * (P::kBar2 + b); };
-  auto lse_free = [&](int b) { return bars + 8u * (P::kBar2 + 2 + b); };
-  auto ss_full = [&](int b) { return bars + 8u * (P::kBar2 + 4 + b); };
-  auto ss_free = [&](int b) { return bars + 8u * (P::kBar2 + 6 + b); };
-  const float* Ss = reinterpret_cast<const float*>(sbase + P::kSsOff);
-  float* lse_s = reinterpret_cast<float*>(sbase + P::kLseOff);
-  const int R = a.sh.R, pr = (a.sh.pool_k - 1) / 2, Pg = a.sh.page_size;
-  const int i0 = item_begin(t.n_items), i1 = item_end(t.n_items), n = i1 - i0;
-  auto stage = [&](int li) {
-    const int b = li & 1;
-    const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(lse_free(b), ((li >> 1) & 1) ^ 1));
-    if (!ok) return false;
-    const Item it = decode<true>(t, a.sh, i0 + li);
-    for (int i = lane; i < RT; i += 32)
-      lse_s[b * RT + i] = i < R ? -a.lse[(int64_t)it.unit * R + i] : -INFINITY;   // padding rows give p = 0
-    __syncwarp();
-    if (lane == 0) mbar_arrive(lse_full(b));
-    return true;
-  };
-  bool ok = true;
-  for (int li = 0; li < 2 && li < n && ok; ++li) ok = stage(li);
-  for (int li = 0; li < n && ok; ++li) {
-    const int b = li & 1;
-    ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(ss_full(b), (li >> 1) & 1));
-    if (!ok) break;
-    const Item it = decode<true>(t, a.sh, i0 + li);
-    const float* Sb = Ss + b * P::kSsFloats;
+    epi_sync();
+    if (aborted(flag)) continue;
+    // max-pool over prefix positions, then page reduce (DELTA key designs 2-3)
     const SeqInfo& si = t.s[it.b];
     float* out = a.scores + si.s_off + ((int64_t)it.layer * a.sh.h_kv + it.g) * it.L;
-    auto pooled = [&](int tt) {
-      const int lo = max(tt - pr, it.ta), hi = min(tt + pr, it.tb - 1);
-      float u = Sb[lo - it.ta];
-      for (int x = lo + 1; x <= hi; ++x) u = fmaxf(u, Sb[x - it.ta]);
-      return u;
-    };
-    if (Pg == 1) {
-      for (int tt = it.a0 + lane; tt < it.a1; tt += 32) out[tt] = pooled(tt);
-    } else {
-      const int n_pages = (it.L + Pg - 1) / Pg;
-      float* pout = a.page_scores + si.p_off + ((int64_t)it.layer * a.sh.h_kv + it.g) * n_pages;
-      for (int p = it.a0 / Pg + lane; p * Pg < it.a1; p += 32) {
-        const int lo = p * Pg, hi = min(it.a1, lo + Pg);
-        float pv = 0.f;
-        for (int tt = lo; tt < hi; ++tt) {
-          const float u = pooled(tt);
-          out[tt] = u;
-          pv = (tt == lo) ? u : (a.sh.page_reduce == KVSEL_REDUCE_MAX ? fmaxf(pv, u) : pv + u);
-        }
-        pout[p] = pv;
-      }
+    float* pout = nullptr;
+    if (P_ > 1) {
+      const int n_pages = (it.L + P_ - 1) / P_;
+      pout = a.page_scores + si.p_off + ((int64_t)it.layer * a.sh.h_kv + it.g) * n_pages;
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(ss_free(b));
-    if (li + 2 < n) ok = stage(li + 2);
+    pool_segment(Ss, it.ta, it.tb, it.a0, it.a1, pr, P_, a.sh.page_reduce, out, pout, e.etid, kEpiThreads);
   }
-  if (!ok && lane == 0) fail(a, flag, kWherePool);
 }
 
 // ---------------------------------------------------------------- kernels
 template <bool PASS2, int RT, int D, int NK, int MAXW>
-__global__ void __launch_bounds__(PASS2 ? kThreadsTc2 : kThreadsTc, 1) score_tc_kernel(const __grid_constant__ CUtensorMap tq,
+__global__ void __launch_bounds__(kThreadsTc, 1) score_tc_kernel(const __grid_constant__ CUtensorMap tq,
                                                                  const __grid_constant__ CUtensorMap tk,
                                                                  const __grid_constant__ TcArgs a,
                                                                  const __grid_constant__ SeqTable t) {
@@ -590,16 +574,9 @@ __global__ void __launch_bounds__(PASS2 ? kThreadsTc2 : kThreadsTc, 1) score_tc_
     }
     for (uint32_t s = 0; s < P::kNT; ++s) {
       mbar_init(bars + 8u * (2 * NK + s), 1);          // tfull: MMA commit
-      // tempty: every epilogue warp (pass 1) or the warpgroup that owns the tile (pass 2)
-      mbar_init(bars + 8u * (2 * NK + P::kNT + s), PASS2 ? kEpiWarps / 2 : kEpiWarps);
+      mbar_init(bars + 8u * (2 * NK + P::kNT + s), kEpiWarps);   // tempty: one arrival per epilogue warp
     }
     for (int s = 0; s < 3; ++s) mbar_init(bars + 8u * (2 * NK + 2 * P::kNT + s), 1);   // q_full, q_empty, drain
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bars + 8u * (P::kBar2 + b), 1);                // lse_full: helper staged -lse
-      mbar_init(bars + 8u * (P::kBar2 + 2 + b), kEpiWarps);    // lse_free: every epilogue warp is done with it
-      mbar_init(bars + 8u * (P::kBar2 + 4 + b), kEpiWarps);    // ss_full: every epilogue warp wrote its keys
-      mbar_init(bars + 8u * (P::kBar2 + 6 + b), 1);            // ss_free: helper wrote the segment out
-    }
     *flag = 0;
     fence_barrier_init();
   }
@@ -612,8 +589,6 @@ __global__ void __launch_bounds__(PASS2 ? kThreadsTc2 : kThreadsTc, 1) score_tc_
     if (lane == 0) produce<PASS2, RT, D, NK>(&tq, &tk, a, t, base, flag);
   } else if (warp == 1) {
     if (lane == 0) issue_mma<PASS2, RT, D, NK>(a, t, base, tmem, flag);
-  } else if (PASS2 && warp == 2 + kEpiWarps) {
-    pass2_helper<RT, D, NK>(a, t, base, sbase, flag);
   } else if (PASS2) {
     epilogue_pass2<RT, D, NK, MAXW>(a, t, base, sbase, tmem, flag);
   } else {
@@ -681,7 +656,7 @@ kvsel_status launch_one(const char* name, const CUtensorMap& tq, const CUtensorM
   if (set_smem((const void*)kern, P::kSmem) != cudaSuccess) return KVSEL_ERR_CUDA;
   const int grid = t.n_items < sms ? t.n_items : sms;
   TraceScope ts(name, s);
-  kern<<<grid, PASS2 ? kThreadsTc2 : kThreadsTc, P::kSmem, s>>>(tq, tk, a, t);
+  kern<<<grid, kThreadsTc, P::kSmem, s>>>(tq, tk, a, t);
   return launch_status();
 }
 
@@ -726,8 +701,7 @@ kvsel_status launch_score(const ScoreShape& sh_in, const SeqTable& base, const v
   }
   CUtensorMap tq, tk;
   if (!make_map(&tq, q, q_rows, sh.d) || !make_map(&tk, k, k_rows, sh.d)) return KVSEL_ERR_CUDA;
-  // whole pages, and the segment plus its pooling halo fills whole tiles of the score buffer
-  sh.seg2 = (int32_t)(sh.page_size * ((kSeg2Max - (sh.pool_k - 1)) / sh.page_size));
+  sh.seg2 = (int32_t)(sh.page_size * (kSeg2Max / sh.page_size));
   const SeqTable t2 = with_items(base, ups, sh.seg2, false, sh.W);
   TcArgs a;
   a.sh = sh;
