@@ -62,6 +62,7 @@ def _load():
         "kvsel_compact": (I32, [D, VP, VP, VP, I32, I32, VP, VP, VP, VP]),
         "kvsel_pagetable": (I32, [D, VP, I32, I32, P(I32), VP, VP, VP, SZ, VP]),
         "kvsel_read_device_error": (I32, [VP, VP]),
+        "kvsel_selftest_bounded_wait": (I32, [VP, ctypes.c_uint32, I32, VP]),
         "kvsel_status_string": (ctypes.c_char_p, [I32]),
         "kvsel_version": (ctypes.c_char_p, []),
         "kvsel_trace_enable": (None, [I32]),
@@ -77,7 +78,7 @@ def _load():
 
 _lib = _load()
 EXPORTED = ("kvsel_workspace_size", "kvsel_score", "kvsel_score_noalloc", "kvsel_combine_layers", "kvsel_topk",
-            "kvsel_compact", "kvsel_pagetable", "kvsel_read_device_error", "kvsel_status_string", "kvsel_version",
+            "kvsel_compact", "kvsel_pagetable", "kvsel_read_device_error", "kvsel_selftest_bounded_wait", "kvsel_status_string", "kvsel_version",
             "kvsel_trace_enable", "kvsel_trace_read", "kvsel_launch_count")
 
 
@@ -171,6 +172,11 @@ def kvsel_pagetable(desc, mask, n_qblk: int, n_kvblk_max: int, n_kvblk: Sequence
 def kvsel_read_device_error(ws, stream=None) -> int:
     """Status recorded by the device in the workspace's error word (clears it)."""
     return _lib.kvsel_read_device_error(_ptr(ws), _stream(stream))
+
+
+def kvsel_selftest_bounded_wait(ws, polls: int, arrive: bool, stream=None):
+    _check(_lib.kvsel_selftest_bounded_wait(_ptr(ws), polls, 1 if arrive else 0, _stream(stream)),
+           "kvsel_selftest_bounded_wait")
 
 
 def kvsel_trace_enable(on: bool):

@@ -205,6 +205,18 @@ KVSEL_API kvsel_status kvsel_pagetable(const kvsel_desc* desc, const uint8_t* ma
 KVSEL_API kvsel_status kvsel_score_noalloc(const kvsel_desc* desc, const void* q, const void* k,
                                            float* scores, float* page_scores, cudaStream_t stream);
 
+/*
+ * kvsel_selftest_bounded_wait — exercises the bounded device wait used by every pipelined kernel.
+ *
+ * The pages have no counterpart to this call; it exists so that failure reporting can be tested
+ * without a real fault.  It launches one CTA that waits on a shared-memory mbarrier with the same
+ * wait routine the scoring kernels use.  With arrive == 0 nothing completes the barrier, the wait
+ * gives up after `polls` polls (1 .. 2^22) and KVSEL_ERR_TIMEOUT is recorded in the error word of
+ * `ws` (read it with kvsel_read_device_error); with arrive != 0 a second thread completes the
+ * barrier and nothing is recorded.
+ */
+KVSEL_API kvsel_status kvsel_selftest_bounded_wait(void* ws, uint32_t polls, int32_t arrive, cudaStream_t stream);
+
 /* Reads (stream-synchronising) and clears the device error word of a workspace. */
 KVSEL_API kvsel_status kvsel_read_device_error(void* ws, cudaStream_t stream);
 

@@ -96,3 +96,5 @@ def test_selection_arguments_rejected():
     nk = (ctypes.c_int32 * 1)(9)
     assert K.raw_call("kvsel_pagetable", ctypes.byref(d), 16, 4, 8, nk, 16, 16, 256, big, None) == K.ERR_INVALID_ARG
     assert K.raw_call("kvsel_combine_layers", ctypes.byref(d), 16, 1, 2, 16, 256, big, None) == K.ERR_INVALID_ARG
+    assert K.raw_call("kvsel_selftest_bounded_wait", None, 10, 0, None) == K.ERR_WORKSPACE
+    assert K.raw_call("kvsel_selftest_bounded_wait", 256, 0, 0, None) == K.ERR_INVALID_ARG

@@ -103,3 +103,21 @@ def test_pagetable_full_size_ragged(cuda):
     np.testing.assert_array_equal(indices.cpu().numpy()[: ref_ptr[-1]], ref_idx)
     density = M.float().mean().item()
     assert 0.05 < density < 0.2
+
+
+def test_bounded_wait_reports_timeout(cuda):
+    """A device wait that nothing completes gives up and reports KVSEL_ERR_TIMEOUT; the context stays usable."""
+    from attention_kv_cache_gb300 import kvsel as K
+    desc = K.make_desc(n_layers=1, h_q=4, h_kv=2, head_dim=64, window=16, prefix_lens=[512])
+    ws = _ws(K, desc, cuda)
+    K.kvsel_selftest_bounded_wait(ws, 2000, arrive=False)
+    assert K.kvsel_read_device_error(ws) == K.ERR_TIMEOUT
+    K.kvsel_selftest_bounded_wait(ws, 2000, arrive=True)
+    assert K.kvsel_read_device_error(ws) == K.OK
+    # the device still computes after the timeout
+    s = S.random_scores(2, 300, seed=5, ties=True)
+    idx = torch.empty((2, 10 + 16), dtype=torch.int32, device=cuda)
+    d2 = K.make_desc(n_layers=2, h_q=1, h_kv=1, head_dim=64, window=16, prefix_lens=[300])
+    K.kvsel_topk(d2, s.to(cuda), 2, 10, 0, idx, _ws(K, d2, cuda))
+    for r in range(2):
+        np.testing.assert_array_equal(idx[r].cpu().numpy(), O.select_tokens(s[r].double().numpy(), 10, 300, 16))
