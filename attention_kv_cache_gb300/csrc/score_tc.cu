@@ -256,9 +256,18 @@ __device__ __forceinline__ float fast_ex2(float x) {
   return y;
 }
 
-// Epilogue arithmetic on 64 accumulator columns, written for instruction-level parallelism:
-// eight independent partial results combined by a fixed pairwise tree (so results do not
-// depend on scheduling), invisible columns entered as -inf.
+// Epilogue arithmetic on 64 accumulator columns, written for instruction-level parallelism and
+// issue economy: packed fp32x2 FMA / add (two columns per instruction), three-input max, and
+// independent partial results combined by a fixed pairwise tree (so results do not depend on
+// scheduling); invisible columns enter as -inf.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+__device__ __forceinline__ float2 ex2x2(float2 x) { return make_float2(fast_ex2(x.x), fast_ex2(x.y)); }
+
 template <int N>
 __device__ __forceinline__ float tree_sum(float* a) {
 #pragma unroll
@@ -268,52 +277,66 @@ __device__ __forceinline__ float tree_sum(float* a) {
   return a[0];
 }
 
+template <int N>
+__device__ __forceinline__ float tree_sum2(float2* a) {
+#pragma unroll
+  for (int w = N / 2; w >= 1; w /= 2)
+#pragma unroll
+    for (int i = 0; i < w; ++i) a[i] = __fadd2_rn(a[i], a[i + w]);
+  return a[0].x + a[0].y;
+}
+
 __device__ __forceinline__ float max64(const float* v) {
   float m[8];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) m[k] = v[k];
-#pragma unroll
-  for (int i = 8; i < 64; ++i) m[i & 7] = fmaxf(m[i & 7], v[i]);
-#pragma unroll
-  for (int w = 4; w >= 1; w /= 2)
-#pragma unroll
-    for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
-  return m[0];
+  for (int k = 0; k < 8; ++k) {
+    const float* c = v + 8 * k;
+    m[k] = fmaxf(fmax3(fmax3(c[0], c[1], c[2]), c[3], c[4]), fmax3(c[5], c[6], c[7]));
+  }
+  return fmax3(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
 }
 
 // sum_i 2^(v_i * scale + off)
 __device__ __forceinline__ float expsum64(const float* v, float scale, float off) {
-  float a[8];
+  const float2 sc = make_float2(scale, scale), of = make_float2(off, off);
+  float2 a[4];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) a[k] = 0.f;
+  for (int k = 0; k < 4; ++k) a[k] = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int i = 0; i < 64; ++i) a[i & 7] += fast_ex2(fmaf(v[i], scale, off));
-  return tree_sum<8>(a);
+  for (int i = 0; i < 32; ++i)
+    a[i & 3] = __fadd2_rn(a[i & 3], ex2x2(__ffma2_rn(make_float2(v[2 * i], v[2 * i + 1]), sc, of)));
+  return tree_sum2<4>(a);
 }
 
 // Column mass of 64 rows for one key: sum (MAXW = 0) or max over heads of MAXW rows of
-// sum_i 2^(v_i * scale + nl_i), nl = -lse of each row.
+// sum_i 2^(v_i * scale + nl_i), nl = -lse of each row, held in registers as pairs.
 template <int MAXW>
-__device__ __forceinline__ float colmass64(const float* v, const float* nl, float scale) {
+__device__ __forceinline__ float colmass64(const float* v, const float2* nl, float scale) {
+  const float2 sc = make_float2(scale, scale);
   if constexpr (MAXW == 0) {
-    float a[8];
+    float2 a[4];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) a[k] = 0.f;
+    for (int k = 0; k < 4; ++k) a[k] = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < 64; ++i) a[i & 7] += fast_ex2(fmaf(v[i], scale, nl[i]));
-    return tree_sum<8>(a);
+    for (int i = 0; i < 32; ++i)
+      a[i & 3] = __fadd2_rn(a[i & 3], ex2x2(__ffma2_rn(make_float2(v[2 * i], v[2 * i + 1]), sc, nl[i])));
+    return tree_sum2<4>(a);
   } else {
-    constexpr int HW = MAXW < 64 ? MAXW : 64;
-    constexpr int NA = HW < 8 ? HW : 8;
+    constexpr int HW = MAXW < 64 ? MAXW : 64;      // rows per head
+    constexpr int NP = HW / 2;                     // pairs per head
+    constexpr int NA = NP < 4 ? NP : 4;
     float red = 0.f;
 #pragma unroll
     for (int h = 0; h < 64 / HW; ++h) {
-      float a[NA];
+      float2 a[NA];
 #pragma unroll
-      for (int k = 0; k < NA; ++k) a[k] = 0.f;
+      for (int k = 0; k < NA; ++k) a[k] = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int i = 0; i < HW; ++i) a[i % NA] += fast_ex2(fmaf(v[h * HW + i], scale, nl[h * HW + i]));
-      red = fmaxf(red, tree_sum<NA>(a));
+      for (int i = 0; i < NP; ++i) {
+        const int c = h * NP + i;
+        a[i % NA] = __fadd2_rn(a[i % NA], ex2x2(__ffma2_rn(make_float2(v[2 * c], v[2 * c + 1]), sc, nl[c])));
+      }
+      red = fmaxf(red, tree_sum2<NA>(a));
     }
     return red;
   }
@@ -504,6 +527,13 @@ __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base
     for (int i = e.etid; i < RT; i += kEpiThreads)
       lse_s[i] = i < a.sh.R ? -a.lse[(int64_t)it.unit * a.sh.R + i] : -INFINITY;   // padding rows give p = 0
     epi_sync();
+    // -lse of this warpgroup's 64 rows in registers (column pairs); with 128 rows per warpgroup
+    // they are read from shared memory instead (the registers would not fit)
+    float2 nl[kChunks == 2 ? 32 : 1];
+    if constexpr (kChunks == 2) {
+#pragma unroll
+      for (int c = 0; c < 32; ++c) nl[c] = make_float2(nlse[col0 + 2 * c], nlse[col0 + 2 * c + 1]);
+    }
     for (int t0 = it.ta; t0 < it.tb; t0 += kTileKeys) {
       // the tensor-memory loads below are warp-collective: decide per warp
       const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(tfull(ts), tph));
@@ -518,7 +548,7 @@ __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base
           tc_fence_before();
           __syncwarp();
           if (e.lane == 0) mbar_arrive(tempty(ts));
-          red = colmass64<MAXW>(v64, nlse + col0, scale);
+          red = colmass64<MAXW>(v64, nl, scale);
         } else {
           float v64[64], w64[64];
           tmem_ld64(taddr, v64);
@@ -526,8 +556,9 @@ __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base
           tc_fence_before();
           __syncwarp();
           if (e.lane == 0) mbar_arrive(tempty(ts));
-          const float r0 = colmass64<MAXW>(v64, nlse + col0, scale);
-          const float r1 = colmass64<MAXW>(w64, nlse + col0 + 64, scale);
+          const float2* nls = reinterpret_cast<const float2*>(nlse + col0);
+          const float r0 = colmass64<MAXW>(v64, nls, scale);
+          const float r1 = colmass64<MAXW>(w64, nls + 32, scale);
           red = MAXW == 0 ? r0 + r1 : fmaxf(r0, r1);
         }
         const int key = t0 + e.lrow;
