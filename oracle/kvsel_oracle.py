@@ -30,6 +30,15 @@ Sources (page title, then the section / equation the step follows):
 * CompactAttention: Accelerating Chunked Prefill with Block-Union KV Selection,
   'Core method' and 'Method steps' (2): Q-block union, intra-group union and
   the per-group table T_{b,g} = { j | G_{b,g,j} = 1 }.
+* CLAA, 'Three representative token-ranking methods' (GemFilter): the
+  pre-softmax attention of the last prompt token, summed over all heads;
+  'Three design decisions' (m = 4 deferred layers, per-layer window scores in
+  a rolling buffer of n = 4, token-wise max at the pruning layer l_p = 15) and
+  'Complete flow and cost' (per-layer top-k by keep rate and gather of the
+  cache; a sequence prune index at l_p); 'Experimental setup': average pooling
+  with kernel 7 for every method.
+* LookaheadKV, 'Method steps': the lookahead rows' attention to the prompt is
+  averaged, pooled, and the top K kept.
 
 Readings taken where the pages are silent or garbled (each is also listed in
 the design notes):
@@ -50,6 +59,20 @@ the design notes):
   observation window (token mode) or its pages (page mode) is appended.
 * Cross-layer: each layer's group score is L1-normalised over t < L, then the
   mean over an inclusive layer range is taken, then pooled.
+* Average pooling divides by the number of in-range neighbours (out-of-range
+  neighbours are ignored, as for the max).
+* Pre-softmax scores sum the scaled logits of the window rows (W = 1 is
+  GemFilter's last token); the keys stay those of the prefix.
+* 'mean' group reduce = the group sum divided by G * W (the mean over the
+  group's window rows and heads).
+* A keep rate r maps to k = floor(r * L + 1/2) prefix tokens (round half up),
+  clipped to [0, L]; the observation window is appended as in token mode.
+* CLAA over an offline prompt: layers m .. l_p are scored with the window
+  (sum over window rows and all heads, softmax), each layer's pooled scores give
+  its own top-k, and the token-wise max over the last n buffered layers (up to
+  and including l_p, not before m), pooled, gives the sequence prune index.
+  Layers after l_p run on the pruned sequence, which only a model forward
+  produces; they are scored like any other layer on their own inputs.
 """
 
 from __future__ import annotations
@@ -108,18 +131,35 @@ def column_mass(p: np.ndarray, L: int) -> np.ndarray:
     return p[:, :, :L].sum(axis=1)
 
 
-def group_reduce(c: np.ndarray, mode: str) -> np.ndarray:
-    """Reduce the per-head column mass [G, L] over the heads of one group: 'sum' or 'max'."""
+def logit_mass(q_group: np.ndarray, k_head: np.ndarray, L: int) -> np.ndarray:
+    """Pre-softmax column sum c[h, t] = sum_j z[h, j, t] over prefix keys t < L.
+
+    CLAA 'Three representative token-ranking methods' (GemFilter): the raw
+    attention logit of the last prompt token (W = 1) for every prompt key.
+    q_group: [G, W, d], k_head: [L + W, d] -> [G, L].  Prefix keys are visible
+    to every window row, so no mask applies.
+    """
+    G, W, d = q_group.shape
+    z = window_logits(q_group.reshape(G * W, d), k_head[:L]).reshape(G, W, L)
+    return z.sum(axis=1)
+
+
+def group_reduce(c: np.ndarray, mode: str, W: int = 1) -> np.ndarray:
+    """Reduce the per-head column mass [G, L] over the heads of one group: 'sum', 'max' or 'mean'
+    (the sum divided by G * W, the mean over the group's W window rows and G heads)."""
     if mode == "sum":
         return c.sum(axis=0)
     if mode == "max":
         return c.max(axis=0)
+    if mode == "mean":
+        return c.sum(axis=0) / (c.shape[0] * W)
     raise ValueError(mode)
 
 
-def group_scores(q_group, k_head, L: int, mode: str) -> np.ndarray:
-    """s[t], t < L, for one (layer, KV head): probabilities -> column mass -> group reduce."""
-    return group_reduce(column_mass(window_probs(q_group, k_head, L), L), mode)
+def group_scores(q_group, k_head, L: int, mode: str, softmax: bool = True) -> np.ndarray:
+    """s[t], t < L, for one (layer, KV head): probabilities (or raw logits) -> column mass -> group reduce."""
+    c = column_mass(window_probs(q_group, k_head, L), L) if softmax else logit_mass(q_group, k_head, L)
+    return group_reduce(c, mode, q_group.shape[1])
 
 
 def max_pool(s: np.ndarray, k: int) -> np.ndarray:
@@ -135,6 +175,37 @@ def max_pool(s: np.ndarray, k: int) -> np.ndarray:
         out[..., :-off] = np.maximum(out[..., :-off], s[..., off:])
         out[..., off:] = np.maximum(out[..., off:], s[..., :-off])
     return out
+
+
+def avg_pool(s: np.ndarray, k: int) -> np.ndarray:
+    """u[t] = mean of s over [t - r, t + r] intersected with [0, len), r = (k - 1) / 2 (last axis).
+
+    CLAA 'Oracle construction' and 'Experimental setup': 1-D average pooling,
+    kernel 7.  Only in-range neighbours are counted.
+    """
+    if k % 2 != 1 or k < 1:
+        raise ValueError("pool width must be odd")
+    r = (k - 1) // 2
+    n = s.shape[-1]
+    tot = s.copy()
+    cnt = np.ones(n)
+    for off in range(1, r + 1):
+        if off >= n:
+            break
+        tot[..., :-off] += s[..., off:]
+        tot[..., off:] += s[..., :-off]
+        cnt[:-off] += 1
+        cnt[off:] += 1
+    return tot / cnt
+
+
+def pool(s: np.ndarray, k: int, kind: str = "max") -> np.ndarray:
+    """Max or average pooling of width k along the last axis."""
+    if kind == "max":
+        return max_pool(s, k)
+    if kind == "avg":
+        return avg_pool(s, k)
+    raise ValueError(kind)
 
 
 def page_reduce(u: np.ndarray, P: int, mode: str = "max") -> np.ndarray:
@@ -160,6 +231,22 @@ def l1_normalise(s: np.ndarray) -> np.ndarray:
 def cross_layer_mean(s_layers: np.ndarray, lo: int, hi: int) -> np.ndarray:
     """Mean over layers lo..hi (inclusive) of the L1-normalised scores.  s_layers: [n_layers, ..., L]."""
     return l1_normalise(s_layers[lo:hi + 1]).mean(axis=0)
+
+
+def head_sum(s: np.ndarray) -> np.ndarray:
+    """Sum over every KV head of a layer's group scores [..., H_kv, L] -> [..., L]: the sum over
+    all attention heads that FastKV, CLAA and GemFilter score with (CLAA, decision 2)."""
+    return s.sum(axis=-2)
+
+
+def layer_max(s_layers: np.ndarray, lo: int, hi: int) -> np.ndarray:
+    """Token-wise max over layers lo..hi (inclusive) of s_layers [n_layers, ..., L] (CLAA Eq. 6)."""
+    return s_layers[lo:hi + 1].max(axis=0)
+
+
+def keep_count(keep_rate: float, L: int) -> int:
+    """Prefix tokens kept for a keep rate: floor(r * L + 1/2), clipped to [0, L]."""
+    return int(min(L, max(0, np.floor(keep_rate * L + 0.5))))
 
 
 # --------------------------------------------------------------------------- selection
@@ -237,11 +324,37 @@ def block_union_csr(mask: np.ndarray, h_kv: int, n_kv: list):
 
 # --------------------------------------------------------------------------- whole workload
 
-def score_unit(q_layer, k_layer, g: int, G: int, L: int, mode: str) -> np.ndarray:
+def score_unit(q_layer, k_layer, g: int, G: int, L: int, mode: str, softmax: bool = True) -> np.ndarray:
     """Raw group scores of (layer, KV head g): q_layer [H_q, W, d], k_layer [H_kv, L+W, d] (any dtype)."""
     qg = _f64(q_layer[g * G:(g + 1) * G])
     kh = _f64(k_layer[g])
-    return group_scores(qg, kh, L, mode)
+    return group_scores(qg, kh, L, mode, softmax)
+
+
+def claa_sequence(q, k, L: int, W: int, G: int, h_kv: int, defer: int, prune_layer: int, agg_window: int,
+                  keep_rate: float, pool_k: int = 7, pool_kind: str = "avg"):
+    """CLAA selection for one prompt, following 'Three design decisions' and 'Complete flow and cost'.
+
+    q [n_layers, H_q, W, d], k [n_layers, H_kv, L + W, d].  For every layer l in
+    defer .. prune_layer: the window score of each prefix token (softmax
+    probabilities summed over the window rows and all heads), its pooled form,
+    and the layer's own top-k (k from the keep rate) followed by the window.
+    At prune_layer: the token-wise max over the buffered layers
+    max(defer, prune_layer - agg_window + 1) .. prune_layer, pooled, and its
+    top-k followed by the window: the sequence prune index.
+    """
+    kc = keep_count(keep_rate, L)
+    layer_s, layer_idx = {}, {}
+    for l in range(defer, prune_layer + 1):
+        s = head_sum(np.stack([score_unit(q[l], k[l], g, G, L, "sum") for g in range(h_kv)]))
+        layer_s[l] = s
+        layer_idx[l] = select_tokens(pool(s, pool_k, pool_kind), kc, L, W)
+    lo = max(defer, prune_layer - agg_window + 1)
+    buf = np.stack([layer_s[l] for l in range(lo, prune_layer + 1)])
+    agg = layer_max(buf, 0, buf.shape[0] - 1)
+    u = pool(agg, pool_k, pool_kind)
+    return {"layer_scores": layer_s, "layer_idx": layer_idx, "agg": agg, "prune_scores": u,
+            "prune_idx": select_tokens(u, kc, L, W), "k": kc, "buffer": (lo, prune_layer)}
 
 
 def run_sequence(w, q, k, v=None, with_gather: bool = True, layers=None):

@@ -287,6 +287,136 @@ def check_block_union(o):
     assert row == B * Lyr * Hkv and indptr[-1] == len(indices)
 
 
+# --------------------------------------------------------------------------- scoring variants
+
+def _sdpa_probs(q, k, L, W):
+    """Window-row attention weights from torch SDPA with identity values: [Hq, W, L + W]."""
+    N = L + W
+    Hkv = k.shape[0]
+    vis = torch.zeros((W, N), dtype=torch.bool)
+    for j in range(W):
+        vis[j, : L + j + 1] = True
+    eye = torch.eye(N, dtype=torch.float64).expand(Hkv, N, N)
+    return torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[None], torch.from_numpy(k)[None], eye[None], attn_mask=vis, enable_gqa=True)[0].numpy()
+
+
+def check_logits_mode_sdpa_log_ratios(o):
+    """Pre-softmax scores: per row, z[t] - z[0] = log p[t] - log p[0] with p from torch SDPA (the GQA map and
+    scale included), summed over the window rows; the level is fixed by a hand-worked logit."""
+    rng = _rng(13)
+    Hq, Hkv, W, L, d = 6, 2, 3, 11, 8
+    G = Hq // Hkv
+    q = _bf16_values(rng.standard_normal((Hq, W, d)))
+    k = _bf16_values(rng.standard_normal((Hkv, L + W, d)))
+    p = _sdpa_probs(q, k, L, W)
+    lr = np.log(p[:, :, :L]) - np.log(p[:, :, :1])              # [Hq, W, L]
+    for g in range(Hkv):
+        heads = lr[g * G:(g + 1) * G].sum(axis=1)                # [G, L]
+        for mode in ("sum", "max"):
+            s = o.score_unit(q, k, g, G, L, mode, softmax=False)
+            want_diff = heads.sum(axis=0) if mode == "sum" else None
+            if mode == "sum":
+                np.testing.assert_allclose(s - s[0], want_diff, atol=1e-10)
+            else:
+                # each head's logit mass differs from its own first column by the SDPA log ratios
+                c = np.stack([o.score_unit(q[g * G + h:g * G + h + 1], k[g:g + 1], 0, 1, L, "sum", softmax=False)
+                              for h in range(G)])
+                np.testing.assert_allclose(c - c[:, :1], heads, atol=1e-10)
+                np.testing.assert_allclose(s, c.max(axis=0), rtol=0, atol=0)
+    # level: d = 4, q = (1, 1, 1, 1), k_t = (1, 0, 0, 0) gives z = 1/2; W = 2 equal rows give 1
+    q1 = np.ones((1, 2, 4))
+    k1 = np.zeros((5, 4)); k1[:, 0] = 1.0
+    np.testing.assert_allclose(o.group_scores(q1, k1, 3, "sum", softmax=False), [1.0, 1.0, 1.0], rtol=1e-15)
+
+
+def check_mean_reduce_and_head_sum(o):
+    """'mean' = the group's probabilities averaged over its G*W rows; the sum over all KV heads of the
+    group sums is the sum over every query head's rows (torch SDPA)."""
+    rng = _rng(14)
+    Hq, Hkv, W, L, d = 8, 2, 4, 9, 8
+    G = Hq // Hkv
+    q = _bf16_values(rng.standard_normal((Hq, W, d)) * 1.5)
+    k = _bf16_values(rng.standard_normal((Hkv, L + W, d)))
+    p = _sdpa_probs(q, k, L, W)[:, :, :L]
+    for g in range(Hkv):
+        np.testing.assert_allclose(o.score_unit(q, k, g, G, L, "mean"), p[g * G:(g + 1) * G].mean(axis=(0, 1)),
+                                   rtol=1e-12)
+    per_group = np.stack([o.score_unit(q, k, g, G, L, "sum") for g in range(Hkv)])
+    np.testing.assert_allclose(o.head_sum(per_group), p.sum(axis=(0, 1)), rtol=1e-12)
+    np.testing.assert_allclose(o.head_sum(per_group[None])[0], p.sum(axis=(0, 1)), rtol=1e-12)
+
+
+def _avg_loop(s, k):
+    r = (k - 1) // 2
+    n = len(s)
+    return np.array([np.mean(s[max(0, t - r):min(n, t + r + 1)]) for t in range(n)])
+
+
+def check_avg_pool_definition(o):
+    """Average pool equals its loop definition (in-range neighbours counted); constants stay constant;
+    a unit spike spreads as 1 / (number of in-range neighbours)."""
+    rng = _rng(15)
+    for n in (1, 2, 3, 7, 8, 41):
+        s = rng.random(n)
+        for kk in (1, 3, 7, 9):
+            np.testing.assert_allclose(o.avg_pool(s, kk), _avg_loop(s, kk), rtol=1e-14)
+            np.testing.assert_allclose(o.pool(s, kk, "avg"), _avg_loop(s, kk), rtol=1e-14)
+        np.testing.assert_allclose(o.avg_pool(np.full(n, 2.5), 7), 2.5, rtol=1e-15)
+    s = np.zeros(20); s[0] = 1.0
+    np.testing.assert_allclose(o.avg_pool(s, 7)[:5], [1 / 4, 1 / 5, 1 / 6, 1 / 7, 0.0], rtol=1e-15)
+    x = rng.random((2, 3, 17))
+    np.testing.assert_allclose(o.avg_pool(x, 5)[1, 2], _avg_loop(x[1, 2], 5), rtol=1e-14)
+    np.testing.assert_array_equal(o.pool(x, 5, "max"), o.max_pool(x, 5))
+
+
+def check_layer_max_and_keep_count(o):
+    """Token-wise max over an inclusive layer range by brute force; keep counts round half up."""
+    rng = _rng(16)
+    s = rng.random((7, 3, 13))
+    m = o.layer_max(s, 2, 5)
+    for i in range(3):
+        for t in range(13):
+            assert m[i, t] == max(s[l, i, t] for l in range(2, 6))
+    assert np.all(m >= s[2:6]) and not np.all(m >= s[6])
+    table = {(0.2, 32768): 6554, (0.1, 30): 3, (0.25, 10): 3, (0.15, 10): 2, (1.0, 7): 7, (0.0, 5): 0,
+             (0.5, 1): 1, (0.4, 3): 1, (0.1, 32768): 3277}
+    for (r, L), want in table.items():
+        assert o.keep_count(r, L) == want, (r, L, o.keep_count(r, L))
+
+
+def check_claa_max_buffer(o):
+    """CLAA: a key that only one buffered layer attends to strongly enters the prune index (token-wise
+    max, not a mean), a key attended only just before the buffer does not, and every layer's own
+    index is the top-k of its pooled all-head window score."""
+    rng = _rng(17)
+    n_layers, Hq, Hkv, W, L, d = 8, 4, 2, 2, 40, 16
+    G = Hq // Hkv
+    q = rng.standard_normal((n_layers, Hq, W, d))
+    k = rng.standard_normal((n_layers, Hkv, L + W, d)) * 0.3
+    defer, lp, nbuf = 2, 6, 3                       # buffer = layers 4, 5, 6
+    u = q.sum(axis=(1, 2))
+    u /= np.linalg.norm(u, axis=-1, keepdims=True)
+    for g in range(Hkv):
+        k[5, g, 10] = 6.0 * np.sqrt(d) * u[5]      # inside the buffer, one layer only
+        k[3, g, 30] = 6.0 * np.sqrt(d) * u[3]      # a layer before the buffer
+    res = o.claa_sequence(q, k, L, W, G, Hkv, defer, lp, nbuf, keep_rate=0.1, pool_k=1)
+    assert res["buffer"] == (4, 6) and res["k"] == 4
+    assert 10 in res["prune_idx"] and 30 not in res["prune_idx"]
+    assert 30 in res["layer_idx"][3] and 10 in res["layer_idx"][5]
+    for l in range(defer, lp + 1):
+        s = sum(o.score_unit(q[l], k[l], g, G, L, "sum") for g in range(Hkv))
+        np.testing.assert_allclose(res["layer_scores"][l], s, rtol=1e-13)
+    # with identical layers the aggregate is that layer and the prune index is its index
+    q2 = np.repeat(q[:1], n_layers, axis=0)
+    k2 = np.repeat(k[:1], n_layers, axis=0)
+    r2 = o.claa_sequence(q2, k2, L, W, G, Hkv, 1, 5, 4, keep_rate=0.2)
+    np.testing.assert_array_equal(r2["prune_idx"], r2["layer_idx"][5])
+    assert r2["buffer"] == (2, 5)
+    # the buffer never reaches below the deferred layers
+    assert o.claa_sequence(q, k, L, W, G, Hkv, 5, 6, 4, keep_rate=0.1)["buffer"] == (5, 6)
+
+
 ALL_CHECKS = [
     check_probs_match_sdpa,
     check_row_mass_invariant,
@@ -301,4 +431,9 @@ ALL_CHECKS = [
     check_gather,
     check_l1_cross_layer,
     check_block_union,
+    check_logits_mode_sdpa_log_ratios,
+    check_mean_reduce_and_head_sum,
+    check_avg_pool_definition,
+    check_layer_max_and_keep_count,
+    check_claa_max_buffer,
 ]

@@ -50,15 +50,15 @@ def _mass_includes_window_shift(o):
 def _wrong_group_map(o):
     orig = o.group_scores
 
-    def score_unit(q_layer, k_layer, g, G, L, mode):
+    def score_unit(q_layer, k_layer, g, G, L, mode, softmax=True):
         Hkv = q_layer.shape[0] // G
-        return orig(o._f64(q_layer[g::Hkv]), o._f64(k_layer[g]), L, mode)
+        return orig(o._f64(q_layer[g::Hkv]), o._f64(k_layer[g]), L, mode, softmax)
     o.score_unit = score_unit
 
 
 def _reduce_swapped(o):
     orig = o.group_reduce
-    o.group_reduce = lambda c, mode: orig(c, "max" if mode == "sum" else "sum")
+    o.group_reduce = lambda c, mode, W=1: orig(c, "max" if mode == "sum" else "sum" if mode == "max" else mode, W)
 
 
 def _transposed_rows(o):
@@ -142,11 +142,66 @@ def _gather_page_offset(o):
     o.gather_rows = lambda x, idx, page_size=1: orig(x, idx + (1 if page_size > 1 else 0), page_size)
 
 
+def _logits_unscaled(o):
+    def logit_mass(q_group, k_head, L):
+        G, W, d = q_group.shape
+        return (q_group.reshape(G * W, d) @ k_head[:L].T).reshape(G, W, L).sum(axis=1)
+    o.logit_mass = logit_mass
+
+
+def _logits_include_window_key(o):
+    def logit_mass(q_group, k_head, L):
+        G, W, d = q_group.shape
+        z = o.window_logits(q_group.reshape(G * W, d), k_head[1:L + 1]).reshape(G, W, L)
+        return z.sum(axis=1)
+    o.logit_mass = logit_mass
+
+
+def _mean_over_heads_only(o):
+    orig = o.group_reduce
+    o.group_reduce = lambda c, mode, W=1: c.sum(axis=0) / c.shape[0] if mode == "mean" else orig(c, mode, W)
+
+
+def _head_sum_is_max(o):
+    o.head_sum = lambda s: s.max(axis=-2)
+
+
+def _avg_pool_counts_padding(o):
+    def avg_pool(s, k):
+        r = (k - 1) // 2
+        n = s.shape[-1]
+        tot = s.copy()
+        for off in range(1, r + 1):
+            if off < n:
+                tot[..., :-off] += s[..., off:]
+                tot[..., off:] += s[..., :-off]
+        return tot / k
+    o.avg_pool = avg_pool
+
+
+def _layer_max_is_mean(o):
+    o.layer_max = lambda s, lo, hi: s[lo:hi + 1].mean(axis=0)
+
+
+def _keep_count_floor(o):
+    o.keep_count = lambda r, L: int(min(L, max(0, np.floor(r * L))))
+
+
+def _claa_buffer_short(o):
+    orig = o.claa_sequence
+
+    def claa_sequence(q, k, L, W, G, h_kv, defer, prune_layer, agg_window, keep_rate, pool_k=7, pool_kind="avg"):
+        return orig(q, k, L, W, G, h_kv, defer, prune_layer, max(1, agg_window - 1), keep_rate, pool_k, pool_kind)
+    o.claa_sequence = claa_sequence
+
+
 MUTANTS = [_no_scale, _mask_off_by_one, _prefix_only_softmax, _mass_max_over_rows,
            _mass_includes_window_shift, _wrong_group_map, _reduce_swapped, _transposed_rows,
            _pool_radius, _pool_one_sided, _page_sum_for_max, _tie_to_higher, _rank_ascending,
            _recency_off_by_one, _no_l1, _layer_range_exclusive, _union_wrong_group,
-           _union_first_qblock_only, _gather_page_offset]
+           _union_first_qblock_only, _gather_page_offset, _logits_unscaled, _logits_include_window_key,
+           _mean_over_heads_only, _head_sum_is_max, _avg_pool_counts_padding, _layer_max_is_mean,
+           _keep_count_floor, _claa_buffer_short]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda m: m.__name__.strip("_"))
