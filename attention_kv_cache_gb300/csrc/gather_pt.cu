@@ -5,6 +5,9 @@ namespace kvsel {
 namespace {
 
 // ------------------------------------------------------------------------ compaction
+constexpr int kCompactThreads = 256;
+constexpr int kCompactRows = 128;     // output rows per CTA
+
 struct CompactArgs {
   const uint4* k;
   const uint4* v;
@@ -12,41 +15,64 @@ struct CompactArgs {
   uint4* k_out;
   uint4* v_out;
   DeviceError* err;
-  int32_t n_layers, h_kv, vpr, n_sel, P, idx_layers;
-  int64_t rows_per_seq;   // n_layers * h_kv * n_sel * P
-  int64_t total_vecs;     // batch * rows_per_seq * vpr
+  int32_t n_layers, h_kv, vpr, vpr_shift, n_sel, P, idx_layers, idx_heads, layer_lo, n_out;
+  int32_t rows_per_unit;   // n_sel * P
+  int32_t chunks;          // CTAs per (sequence, output layer, KV head) unit
 };
 
-// One thread moves one 16-byte vector of K and of V.  Consecutive threads cover
-// consecutive vectors of a row, so every row is read and written as whole
-// 128-byte lines.
-__global__ void __launch_bounds__(256) compact_kernel(const __grid_constant__ CompactArgs a,
-                                                      const __grid_constant__ SeqTable t) {
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  const int64_t per_sel = (int64_t)a.n_sel * a.P;
-  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < a.total_vecs; v += stride) {
-    const int64_t row = v / a.vpr;
-    const int c = (int)(v % a.vpr);
-    const int b = (int)(row / a.rows_per_seq);
-    const int64_t rr = row % a.rows_per_seq;
-    const int lg = (int)(rr / per_sel);
-    const int within = (int)(rr % per_sel);
-    const int layer = lg / a.h_kv, g = lg % a.h_kv;
-    const int il = a.idx_layers == 1 ? 0 : layer;
-    const SeqInfo& si = t.s[b];
-    const int32_t id = a.idx[(((int64_t)b * a.idx_layers + il) * a.h_kv + g) * a.n_sel + within / a.P];
-    const int64_t src_row = (int64_t)id * a.P + within % a.P;
-    const int64_t lim = a.P == 1 ? si.n_keys : ((int64_t)si.n_keys + a.P - 1) / a.P;
-    uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
-    if (id < 0 || id >= lim) {
-      if (c == 0) set_device_error(a.err, KVSEL_ERR_DEVICE, (uint32_t)row);
-    } else if (src_row < si.n_keys) {
-      const int64_t off = (si.k_off / 8) + (((int64_t)layer * a.h_kv + g) * si.n_keys + src_row) * a.vpr + c;
-      kv = a.k[off];
-      vv = a.v[off];
+// One CTA copies up to kCompactRows consecutive output rows of one unit.  A row of d bf16 is
+// vpr 16-byte vectors; consecutive threads take consecutive vectors, so every row is read and
+// written as whole 128-byte lines, and the unit's geometry is decoded once per CTA.
+__global__ void __launch_bounds__(kCompactThreads) compact_kernel(const __grid_constant__ CompactArgs a,
+                                                                  const __grid_constant__ SeqTable t) {
+  const int unit = blockIdx.x / a.chunks;
+  const int chunk = blockIdx.x % a.chunks;
+  const int per_seq = a.n_out * a.h_kv;
+  const int b = unit / per_seq;
+  const int rem = unit % per_seq;
+  const int lo = rem / a.h_kv, g = rem % a.h_kv;
+  const int layer = a.layer_lo + lo;
+  const SeqInfo& si = t.s[b];
+  const int il = a.idx_layers == 1 ? 0 : lo;
+  const int ih = a.idx_heads == 1 ? 0 : g;
+  const int32_t* idx = a.idx + (((int64_t)b * a.idx_layers + il) * a.idx_heads + ih) * a.n_sel;
+  const int64_t lim = a.P == 1 ? si.n_keys : ((int64_t)si.n_keys + a.P - 1) / a.P;
+  const uint4* ksrc = a.k + si.k_off / 8 + ((int64_t)layer * a.h_kv + g) * si.n_keys * a.vpr;
+  const uint4* vsrc = a.v + si.k_off / 8 + ((int64_t)layer * a.h_kv + g) * si.n_keys * a.vpr;
+  const int64_t out0 = (int64_t)unit * a.rows_per_unit * a.vpr;
+  const int r0 = chunk * kCompactRows;
+  const int r1 = min(a.rows_per_unit, r0 + kCompactRows);
+  const int n_vec = (r1 - r0) * a.vpr;
+  constexpr int kUnroll = 4;
+  for (int base = 0; base < n_vec; base += kCompactThreads * kUnroll) {
+    uint4 kv[kUnroll], vv[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int vi = base + u * kCompactThreads + threadIdx.x;
+      kv[u] = make_uint4(0, 0, 0, 0);
+      vv[u] = make_uint4(0, 0, 0, 0);
+      if (vi < n_vec) {
+        const int row = r0 + (vi >> a.vpr_shift);
+        const int c = vi & (a.vpr - 1);
+        const int sel = row / a.P;
+        const int32_t id = idx[sel];
+        const int64_t src_row = (int64_t)id * a.P + (row - sel * a.P);
+        if (id < 0 || id >= lim) {
+          if (c == 0) set_device_error(a.err, KVSEL_ERR_DEVICE, (uint32_t)((int64_t)unit * a.rows_per_unit + row));
+        } else if (src_row < si.n_keys) {
+          kv[u] = ksrc[src_row * a.vpr + c];
+          vv[u] = vsrc[src_row * a.vpr + c];
+        }
+      }
     }
-    a.k_out[v] = kv;
-    a.v_out[v] = vv;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int vi = base + u * kCompactThreads + threadIdx.x;
+      if (vi < n_vec) {
+        a.k_out[out0 + (int64_t)r0 * a.vpr + vi] = kv[u];
+        a.v_out[out0 + (int64_t)r0 * a.vpr + vi] = vv[u];
+      }
+    }
   }
 }
 
@@ -153,8 +179,8 @@ __global__ void __launch_bounds__(kPtThreads) pt_write(const __grid_constant__ P
 }  // namespace
 
 kvsel_status launch_compact(const kvsel_desc& d, const SeqTable& t, const void* k, const void* v,
-                            const int32_t* idx, int idx_layers, int n_sel, void* k_out, void* v_out,
-                            DeviceError* err, cudaStream_t s) {
+                            const int32_t* idx, int idx_layers, int idx_heads, int layer_lo, int n_layers_out,
+                            int n_sel, void* k_out, void* v_out, DeviceError* err, cudaStream_t s) {
   CompactArgs a;
   a.k = static_cast<const uint4*>(k);
   a.v = static_cast<const uint4*>(v);
@@ -165,15 +191,19 @@ kvsel_status launch_compact(const kvsel_desc& d, const SeqTable& t, const void* 
   a.n_layers = d.n_layers;
   a.h_kv = d.h_kv;
   a.vpr = d.head_dim / 8;
+  a.vpr_shift = a.vpr == 16 ? 4 : 3;
   a.n_sel = n_sel;
   a.P = d.page_size;
   a.idx_layers = idx_layers;
-  a.rows_per_seq = (int64_t)d.n_layers * d.h_kv * n_sel * d.page_size;
-  a.total_vecs = (int64_t)d.batch * a.rows_per_seq * a.vpr;
-  const int64_t blocks = (a.total_vecs + 255) / 256;
-  const unsigned grid = (unsigned)(blocks < 152 * 32 ? blocks : 152 * 32);
+  a.idx_heads = idx_heads;
+  a.layer_lo = layer_lo;
+  a.n_out = n_layers_out;
+  a.rows_per_unit = n_sel * d.page_size;
+  a.chunks = (a.rows_per_unit + kCompactRows - 1) / kCompactRows;
+  const int64_t units = (int64_t)d.batch * n_layers_out * d.h_kv;
+  if (units * a.chunks >= (int64_t(1) << 31)) return KVSEL_ERR_UNSUPPORTED;
   TraceScope ts("kv_compact", s);
-  compact_kernel<<<grid, 256, 0, s>>>(a, t);
+  compact_kernel<<<(unsigned)(units * a.chunks), kCompactThreads, 0, s>>>(a, t);
   return launch_status();
 }
 

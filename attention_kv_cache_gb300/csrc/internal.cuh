@@ -55,9 +55,16 @@ constexpr int64_t kScoreSeg1 = 2048;
 struct ScoreShape {
   int32_t n_layers, h_q, h_kv, d, W, G, R;   // R = G * W rows per unit
   int32_t group_reduce, pool_k, page_size, page_reduce;
+  int32_t pool_type;                         // KVSEL_POOL_MAX / KVSEL_POOL_AVG
+  int32_t logits;                            // 1: pre-softmax scaled logits (one pass, no lse)
   int32_t seg1, seg2;                        // keys per pass-1 / pass-2 segment
   float scale_log2;                          // log2(e) / sqrt(d)
+  float scale_nat;                           // 1 / sqrt(d)
+  float gscale;                              // factor on the group score: 1, or 1 / (G * W) for the mean
 };
+
+// Score shape of a checked descriptor (kvsel_api.cu).
+ScoreShape make_shape(const kvsel_desc& d);
 
 // ---- launch plumbing (kvsel_api.cu) ------------------------------------------------
 struct TraceScope {
@@ -107,15 +114,17 @@ inline SeqTable with_items(const SeqTable& base, int64_t units_per_seq, int64_t 
   return t;
 }
 
-kvsel_status launch_topk(const kvsel_desc& desc, const SeqTable& t, int layers, int k, int n_recent,
-                         const float* scores, int32_t* idx, cudaStream_t s);
+// Top-k over `rows` score rows per sequence; sequence b's rows start at element
+// rows * (sum of n over earlier sequences), n = L_b or ceil(L_b / P).
+kvsel_status launch_topk(const kvsel_desc& desc, const SeqTable& t, int rows, int k, int n_recent,
+                         bool append_window, const float* scores, int32_t* idx, cudaStream_t s);
 
-kvsel_status launch_combine_layers(const kvsel_desc& desc, const SeqTable& t, const float* scores,
-                                   int lo, int hi, float* norms, float* combined, cudaStream_t s);
+kvsel_status launch_aggregate(const kvsel_desc& desc, const SeqTable& t, const float* scores, int lo, int hi,
+                              int layer_op, int head_op, float* norms, float* out, cudaStream_t s);
 
 kvsel_status launch_compact(const kvsel_desc& desc, const SeqTable& t, const void* k, const void* v,
-                            const int32_t* idx, int idx_layers, int n_sel, void* k_out, void* v_out,
-                            DeviceError* err, cudaStream_t s);
+                            const int32_t* idx, int idx_layers, int idx_heads, int layer_lo, int n_layers_out,
+                            int n_sel, void* k_out, void* v_out, DeviceError* err, cudaStream_t s);
 
 kvsel_status launch_pagetable(const kvsel_desc& desc, const SeqTable& t, const uint8_t* mask,
                               int n_qblk, int n_kvblk_max, int32_t* counts, int32_t* kv_indptr,

@@ -105,8 +105,12 @@ static kvsel_status check_desc(const kvsel_desc* d) {
   if (d->n_layers < 1 || d->h_kv < 1 || d->h_q < 1 || d->h_q % d->h_kv != 0) return KVSEL_ERR_INVALID_ARG;
   if (d->batch < 1 || d->batch > KVSEL_MAX_BATCH) return KVSEL_ERR_INVALID_ARG;
   if (d->window < 1 || d->window > KVSEL_MAX_WINDOW) return KVSEL_ERR_INVALID_ARG;
-  if (d->group_reduce != KVSEL_REDUCE_SUM && d->group_reduce != KVSEL_REDUCE_MAX) return KVSEL_ERR_INVALID_ARG;
+  if (d->group_reduce != KVSEL_REDUCE_SUM && d->group_reduce != KVSEL_REDUCE_MAX &&
+      d->group_reduce != KVSEL_REDUCE_MEAN)
+    return KVSEL_ERR_INVALID_ARG;
   if (d->page_reduce != KVSEL_REDUCE_SUM && d->page_reduce != KVSEL_REDUCE_MAX) return KVSEL_ERR_INVALID_ARG;
+  if (d->pool_type != KVSEL_POOL_MAX && d->pool_type != KVSEL_POOL_AVG) return KVSEL_ERR_INVALID_ARG;
+  if (d->score_mode != KVSEL_SCORE_SOFTMAX && d->score_mode != KVSEL_SCORE_LOGITS) return KVSEL_ERR_INVALID_ARG;
   if (d->pool_k < 1 || d->pool_k % 2 == 0 || d->pool_k > 63) return KVSEL_ERR_INVALID_ARG;
   if (d->page_size < 1 || d->page_size > KVSEL_MAX_PAGE) return KVSEL_ERR_INVALID_ARG;
   for (int b = 0; b < d->batch; ++b) {
@@ -125,6 +129,21 @@ static kvsel_status check_ws(const kvsel_desc& d, void* ws, size_t ws_bytes) {
   if (ws == nullptr || ((uintptr_t)ws % KVSEL_WS_ALIGN) != 0) return KVSEL_ERR_WORKSPACE;
   if (ws_bytes < ws_layout(d).total) return KVSEL_ERR_WORKSPACE;
   return KVSEL_OK;
+}
+
+ScoreShape make_shape(const kvsel_desc& d) {
+  ScoreShape sh;
+  sh.n_layers = d.n_layers; sh.h_q = d.h_q; sh.h_kv = d.h_kv; sh.d = d.head_dim; sh.W = d.window;
+  sh.G = d.h_q / d.h_kv; sh.R = sh.G * d.window;
+  sh.group_reduce = d.group_reduce; sh.pool_k = d.pool_k; sh.page_size = d.page_size;
+  sh.page_reduce = d.page_reduce;
+  sh.pool_type = d.pool_type;
+  sh.logits = d.score_mode == KVSEL_SCORE_LOGITS ? 1 : 0;
+  sh.seg1 = sh.seg2 = 0;    // set by the launcher
+  sh.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.head_dim));
+  sh.scale_nat = (float)(1.0 / std::sqrt((double)d.head_dim));
+  sh.gscale = d.group_reduce == KVSEL_REDUCE_MEAN ? (float)(1.0 / ((double)sh.R)) : 1.0f;
+  return sh;
 }
 
 // Sequence table: element offsets of each sequence in the packed layouts.
@@ -148,6 +167,40 @@ static SeqTable make_table(const kvsel_desc& d, int32_t layers_in_scores) {
   return t;
 }
 
+// Sequence table for `rows` score rows per sequence (top-k inputs): s_off / p_off become the
+// offsets of each sequence's [rows][L_b] token scores / [rows][ceil(L_b / P)] page scores.
+static SeqTable make_table_rows(const kvsel_desc& d, int32_t rows) {
+  SeqTable t = make_table(d, d.n_layers);
+  int64_t s_off = 0, p_off = 0;
+  for (int b = 0; b < d.batch; ++b) {
+    t.s[b].s_off = s_off;
+    t.s[b].p_off = p_off;
+    s_off += (int64_t)rows * t.s[b].L;
+    p_off += (int64_t)rows * cdiv(t.s[b].L, d.page_size);
+  }
+  return t;
+}
+
+// Shared checks of a top-k request (token or page mode).
+static kvsel_status check_topk(const kvsel_desc& d, int32_t k, int32_t n_recent) {
+  if (k < 0 || n_recent < 0) return KVSEL_ERR_INVALID_ARG;
+  const int P = d.page_size;
+  if (P == 1) {
+    if (n_recent != 0) return KVSEL_ERR_INVALID_ARG;
+    for (int b = 0; b < d.batch; ++b)
+      if (k > d.prefix_lens[b]) return KVSEL_ERR_INVALID_ARG;
+  } else {
+    if (d.window % P != 0) return KVSEL_ERR_UNSUPPORTED;
+    for (int b = 0; b < d.batch; ++b) {
+      const int64_t L = d.prefix_lens[b];
+      const int64_t n_pages = cdiv(L, P);
+      if (n_recent > n_pages || k > n_pages - n_recent) return KVSEL_ERR_INVALID_ARG;
+      if (L % P != 0 && n_recent < 1) return KVSEL_ERR_INVALID_ARG;
+    }
+  }
+  return KVSEL_OK;
+}
+
 }  // namespace kvsel
 
 using namespace kvsel;
@@ -155,7 +208,7 @@ using namespace kvsel;
 // ============================================================================= C ABI
 extern "C" {
 
-const char* kvsel_version(void) { return "kvsel 0.1 (sm_103a)"; }
+const char* kvsel_version(void) { return "kvsel 0.2 (sm_103a)"; }
 
 const char* kvsel_status_string(kvsel_status s) {
   switch (s) {
@@ -190,13 +243,7 @@ kvsel_status kvsel_score(const kvsel_desc* desc, const void* q, const void* k, f
   const WsLayout w = ws_layout(d);
   auto ws_base = [](void* p) { return static_cast<char*>(p); };
 
-  ScoreShape sh;
-  sh.n_layers = d.n_layers; sh.h_q = d.h_q; sh.h_kv = d.h_kv; sh.d = d.head_dim; sh.W = d.window;
-  sh.G = d.h_q / d.h_kv; sh.R = sh.G * d.window;
-  sh.group_reduce = d.group_reduce; sh.pool_k = d.pool_k; sh.page_size = d.page_size;
-  sh.page_reduce = d.page_reduce;
-  sh.seg1 = sh.seg2 = 0;    // set by the launcher
-  sh.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.head_dim));
+  const ScoreShape sh = make_shape(d);
   const SeqTable base = make_table(d, d.n_layers);
   return launch_score(sh, base, q, k, scores, page_scores, reinterpret_cast<float*>(ws_base(ws) + w.lse_off),
                       reinterpret_cast<float2*>(ws_base(ws) + w.part_off), reinterpret_cast<DeviceError*>(ws),
@@ -214,9 +261,40 @@ kvsel_status kvsel_combine_layers(const kvsel_desc* desc, const float* scores, i
   if ((st = check_ws(d, ws, ws_bytes)) != KVSEL_OK) return st;
   SeqTable t = make_table(d, d.n_layers);
   const WsLayout w = ws_layout(d);
-  return launch_combine_layers(d, t, scores, layer_lo, layer_hi,
-                               reinterpret_cast<float*>(static_cast<char*>(ws) + w.norm_off), combined,
-                               stream);
+  return launch_aggregate(d, t, scores, layer_lo, layer_hi, KVSEL_LAYERS_L1_MEAN, KVSEL_HEADS_EACH,
+                          reinterpret_cast<float*>(static_cast<char*>(ws) + w.norm_off), combined, stream);
+}
+
+kvsel_status kvsel_aggregate(const kvsel_desc* desc, const float* scores, int32_t layer_lo, int32_t layer_hi,
+                             int32_t layer_op, int32_t head_op, float* out, void* ws, size_t ws_bytes,
+                             cudaStream_t stream) {
+  kvsel_status st = check_desc(desc);
+  if (st != KVSEL_OK) return st;
+  const kvsel_desc& d = *desc;
+  if (scores == nullptr || out == nullptr) return KVSEL_ERR_INVALID_ARG;
+  if (layer_lo < 0 || layer_hi < layer_lo || layer_hi >= d.n_layers) return KVSEL_ERR_INVALID_ARG;
+  if (layer_op != KVSEL_LAYERS_EACH && layer_op != KVSEL_LAYERS_L1_MEAN && layer_op != KVSEL_LAYERS_MAX)
+    return KVSEL_ERR_INVALID_ARG;
+  if (head_op != KVSEL_HEADS_EACH && head_op != KVSEL_HEADS_SUM) return KVSEL_ERR_INVALID_ARG;
+  if ((st = check_ws(d, ws, ws_bytes)) != KVSEL_OK) return st;
+  SeqTable t = make_table(d, d.n_layers);
+  const WsLayout w = ws_layout(d);
+  return launch_aggregate(d, t, scores, layer_lo, layer_hi, layer_op, head_op,
+                          reinterpret_cast<float*>(static_cast<char*>(ws) + w.norm_off), out, stream);
+}
+
+kvsel_status kvsel_select(const kvsel_desc* desc, const float* scores, int32_t rows, int32_t k, int32_t n_recent,
+                          int32_t append_window, int32_t* idx_out, void* ws, size_t ws_bytes,
+                          cudaStream_t stream) {
+  kvsel_status st = check_desc(desc);
+  if (st != KVSEL_OK) return st;
+  const kvsel_desc& d = *desc;
+  if (scores == nullptr || idx_out == nullptr) return KVSEL_ERR_INVALID_ARG;
+  if (rows < 1 || (int64_t)rows * d.batch >= (int64_t(1) << 31)) return KVSEL_ERR_INVALID_ARG;
+  if ((st = check_topk(d, k, n_recent)) != KVSEL_OK) return st;
+  if ((st = check_ws(d, ws, ws_bytes)) != KVSEL_OK) return st;
+  SeqTable t = make_table_rows(d, rows);
+  return launch_topk(d, t, rows, k, n_recent, append_window != 0, scores, idx_out, stream);
 }
 
 kvsel_status kvsel_topk(const kvsel_desc* desc, const float* scores, int32_t layers, int32_t k,
@@ -227,24 +305,11 @@ kvsel_status kvsel_topk(const kvsel_desc* desc, const float* scores, int32_t lay
   const kvsel_desc& d = *desc;
   if (scores == nullptr || idx_out == nullptr) return KVSEL_ERR_INVALID_ARG;
   if (layers != 1 && layers != d.n_layers) return KVSEL_ERR_INVALID_ARG;
-  if (k < 0 || n_recent < 0) return KVSEL_ERR_INVALID_ARG;
+  if ((st = check_topk(d, k, n_recent)) != KVSEL_OK) return st;
   if ((st = check_ws(d, ws, ws_bytes)) != KVSEL_OK) return st;
-  const int P = d.page_size;
-  if (P == 1) {
-    if (n_recent != 0) return KVSEL_ERR_INVALID_ARG;
-    for (int b = 0; b < d.batch; ++b)
-      if (k > d.prefix_lens[b]) return KVSEL_ERR_INVALID_ARG;
-  } else {
-    if (d.window % P != 0) return KVSEL_ERR_UNSUPPORTED;
-    for (int b = 0; b < d.batch; ++b) {
-      const int64_t L = d.prefix_lens[b];
-      const int64_t n_pages = cdiv(L, P);
-      if (n_recent > n_pages || k > n_pages - n_recent) return KVSEL_ERR_INVALID_ARG;
-      if (L % P != 0 && n_recent < 1) return KVSEL_ERR_INVALID_ARG;
-    }
-  }
-  SeqTable t = make_table(d, layers);
-  return launch_topk(d, t, layers, k, n_recent, scores, idx_out, stream);
+  const int32_t rows = layers * d.h_kv;
+  SeqTable t = make_table_rows(d, rows);
+  return launch_topk(d, t, rows, k, n_recent, true, scores, idx_out, stream);
 }
 
 kvsel_status kvsel_compact(const kvsel_desc* desc, const void* k, const void* v, const int32_t* idx,
@@ -262,8 +327,29 @@ kvsel_status kvsel_compact(const kvsel_desc* desc, const void* k, const void* v,
   if (ws != nullptr && ((uintptr_t)ws % KVSEL_WS_ALIGN) != 0) return KVSEL_ERR_WORKSPACE;
   if (n_sel == 0) return KVSEL_OK;
   SeqTable t = make_table(d, d.n_layers);
-  return launch_compact(d, t, k, v, idx, idx_layers, n_sel, k_out, v_out, reinterpret_cast<DeviceError*>(ws),
-                        stream);
+  return launch_compact(d, t, k, v, idx, idx_layers, d.h_kv, 0, d.n_layers, n_sel, k_out, v_out,
+                        reinterpret_cast<DeviceError*>(ws), stream);
+}
+
+kvsel_status kvsel_compact_layers(const kvsel_desc* desc, const void* k, const void* v, const int32_t* idx,
+                                  int32_t idx_layers, int32_t idx_heads, int32_t layer_lo, int32_t n_layers_out,
+                                  int32_t n_sel, void* k_out, void* v_out, void* ws, cudaStream_t stream) {
+  kvsel_status st = check_desc(desc);
+  if (st != KVSEL_OK) return st;
+  const kvsel_desc& d = *desc;
+  if (k == nullptr || v == nullptr || idx == nullptr || k_out == nullptr || v_out == nullptr)
+    return KVSEL_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_out) || !aligned16(v_out)) return KVSEL_ERR_INVALID_ARG;
+  if (layer_lo < 0 || n_layers_out < 1 || layer_lo + n_layers_out > d.n_layers) return KVSEL_ERR_INVALID_ARG;
+  if (idx_layers != 1 && idx_layers != n_layers_out) return KVSEL_ERR_INVALID_ARG;
+  if (idx_heads != 1 && idx_heads != d.h_kv) return KVSEL_ERR_INVALID_ARG;
+  if (n_sel < 0) return KVSEL_ERR_INVALID_ARG;
+  if ((int64_t)n_sel * d.page_size >= (int64_t(1) << 31)) return KVSEL_ERR_INVALID_ARG;
+  if (ws != nullptr && ((uintptr_t)ws % KVSEL_WS_ALIGN) != 0) return KVSEL_ERR_WORKSPACE;
+  if (n_sel == 0) return KVSEL_OK;
+  SeqTable t = make_table(d, d.n_layers);
+  return launch_compact(d, t, k, v, idx, idx_layers, idx_heads, layer_lo, n_layers_out, n_sel, k_out, v_out,
+                        reinterpret_cast<DeviceError*>(ws), stream);
 }
 
 kvsel_status kvsel_pagetable(const kvsel_desc* desc, const uint8_t* mask, int32_t n_qblk,

@@ -8,9 +8,11 @@
 //   pass 1  — per (unit, key segment): online max / sum of 2^(z - m) per row
 //   combine — per row: lse = M + log2(sum_s l_s 2^(m_s - M))
 //   pass 2  — per (unit, prefix segment): p = 2^(z - lse), column mass per
-//             head, group sum / max, max-pool (halo keys recomputed), page
-//             reduce.
+//             head, group sum / max / mean, max or average pool (halo keys
+//             recomputed), page reduce.
 // Logits are never stored.  Exponentials are base 2 on z * log2(e)/sqrt(d).
+// In logits mode (GemFilter's pre-softmax scores) pass 2 alone runs and sums
+// z / sqrt(d) over the window rows instead of probabilities.
 #include "internal.cuh"
 
 namespace kvsel {
@@ -220,7 +222,7 @@ __global__ void __launch_bounds__(kThreads) score_pass2_simt(const __grid_consta
   load_q<D, RP>(Qs, a, b, layer, g);
   const int r = threadIdx.x % RP, s = threadIdx.x / RP;
   const bool rvalid = r < sh.R;
-  const float lse_r = rvalid ? a.lse[(int64_t)(si.unit0 + ul) * sh.R + r] : 0.f;
+  const float lse_r = (rvalid && !sh.logits) ? a.lse[(int64_t)(si.unit0 + ul) * sh.R + r] : 0.f;
   float acc[KPT];
   for (int t0 = ea; t0 < eb; t0 += kTile) {
     __syncthreads();
@@ -231,7 +233,8 @@ __global__ void __launch_bounds__(kThreads) score_pass2_simt(const __grid_consta
     for (int i = 0; i < KPT; ++i) {
       const int tl = s + i * TPR;
       // prefix keys are visible to every window row
-      const float p = (rvalid && t0 + tl < eb) ? fast_ex2(acc[i] * sh.scale_log2 - lse_r) : 0.f;
+      float p = 0.f;
+      if (rvalid && t0 + tl < eb) p = sh.logits ? acc[i] * sh.scale_nat : fast_ex2(acc[i] * sh.scale_log2 - lse_r);
       Ps[r * LDP + tl] = p;
     }
     __syncthreads();
@@ -240,7 +243,7 @@ __global__ void __launch_bounds__(kThreads) score_pass2_simt(const __grid_consta
       for (int h = 0; h < sh.G; ++h) {
         float cs = 0.f;
         for (int j = 0; j < sh.W; ++j) cs += Ps[(h * sh.W + j) * LDP + threadIdx.x];
-        red = (h == 0) ? cs : (sh.group_reduce == KVSEL_REDUCE_SUM ? red + cs : fmaxf(red, cs));
+        red = (h == 0) ? cs : (sh.group_reduce == KVSEL_REDUCE_MAX ? fmaxf(red, cs) : red + cs);
       }
       Ss[t0 + threadIdx.x - ea] = red;
     }
@@ -250,7 +253,13 @@ __global__ void __launch_bounds__(kThreads) score_pass2_simt(const __grid_consta
   for (int tt = a0 + threadIdx.x; tt < a1; tt += kThreads) {
     const int lo = max(tt - pr, ea), hi = min(tt + pr, eb - 1);
     float u = Ss[lo - ea];
-    for (int x = lo + 1; x <= hi; ++x) u = fmaxf(u, Ss[x - ea]);
+    if (sh.pool_type == KVSEL_POOL_AVG) {
+      for (int x = lo + 1; x <= hi; ++x) u += Ss[x - ea];
+      u /= (float)(hi - lo + 1);
+    } else {
+      for (int x = lo + 1; x <= hi; ++x) u = fmaxf(u, Ss[x - ea]);
+    }
+    u *= sh.gscale;
     out[tt] = u;
     Us[tt - a0] = u;
   }
@@ -278,14 +287,14 @@ kvsel_status run(const ScoreArgs& args, const SeqTable& t1, const SeqTable& t2, 
   if (set_smem((const void*)score_pass1_simt<D, RP>, smem1) != cudaSuccess) return KVSEL_ERR_CUDA;
   if (set_smem((const void*)score_pass2_simt<D, RP>, smem2) != cudaSuccess) return KVSEL_ERR_CUDA;
   kvsel_status st;
-  {
-    TraceScope ts("score_pass1_simt", s);
-    score_pass1_simt<D, RP><<<t1.n_items, kThreads, smem1, s>>>(args, t1);
-    if ((st = launch_status()) != KVSEL_OK) return st;
-  }
-  const int64_t units = (int64_t)t1.batch * args.sh.n_layers * args.sh.h_kv;
-  const int64_t n_rows = units * args.sh.R;
-  {
+  if (!args.sh.logits) {   // the softmax needs each row's log-sum-exp first
+    {
+      TraceScope ts("score_pass1_simt", s);
+      score_pass1_simt<D, RP><<<t1.n_items, kThreads, smem1, s>>>(args, t1);
+      if ((st = launch_status()) != KVSEL_OK) return st;
+    }
+    const int64_t units = (int64_t)t1.batch * args.sh.n_layers * args.sh.h_kv;
+    const int64_t n_rows = units * args.sh.R;
     TraceScope ts("score_lse_combine", s);
     score_lse_combine<<<(unsigned)((n_rows + kThreads - 1) / kThreads), kThreads, 0, s>>>(args, t1, n_rows);
     if ((st = launch_status()) != KVSEL_OK) return st;

@@ -342,6 +342,38 @@ __device__ __forceinline__ float colmass64(const float* v, const float2* nl, flo
   }
 }
 
+// Logits mode: the same reductions over sum_i v_i * w_i, w = 1/sqrt(d) for real rows and 0 for
+// the padding rows (GemFilter's pre-softmax score; no exponentials).
+template <int MAXW>
+__device__ __forceinline__ float linmass64(const float* v, const float2* w) {
+  if constexpr (MAXW == 0) {
+    float2 a[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) a[k] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) a[i & 3] = __ffma2_rn(make_float2(v[2 * i], v[2 * i + 1]), w[i], a[i & 3]);
+    return tree_sum2<4>(a);
+  } else {
+    constexpr int HW = MAXW < 64 ? MAXW : 64;
+    constexpr int NP = HW / 2;
+    constexpr int NA = NP < 4 ? NP : 4;
+    float red = -INFINITY;
+#pragma unroll
+    for (int h = 0; h < 64 / HW; ++h) {
+      float2 a[NA];
+#pragma unroll
+      for (int k = 0; k < NA; ++k) a[k] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < NP; ++i) {
+        const int c = h * NP + i;
+        a[i % NA] = __ffma2_rn(make_float2(v[2 * c], v[2 * c + 1]), w[c], a[i % NA]);
+      }
+      red = fmaxf(red, tree_sum2<NA>(a));
+    }
+    return red;
+  }
+}
+
 // Online (max, sum) update of one row with 64 new columns, the first nvis of them visible.
 __device__ __forceinline__ void online_update64(float* v, int nvis, float scale, float& m, float& l) {
   if (nvis < 64) {
@@ -454,9 +486,10 @@ __device__ void epilogue_pass1(const TcArgs& a, const SeqTable& t, uint32_t base
   }
 }
 
-// Max-pool of a segment's group scores S[ta..tb) (the pooling halo included) into out[a0..a1), and,
-// with P > 1, page reduce into pout over the pages of [a0, a1).  Window loads are independent of one
-// another, so they overlap instead of forming a chain of shared-memory latencies.
+// Pooling of a segment's group scores S[ta..tb) (the pooling halo included) into out[a0..a1), and,
+// with P > 1, page reduce into pout over the pages of [a0, a1); every output is scaled by gscale
+// (the 1 / (G W) of the mean reduce).  Window loads are independent of one another, so they
+// overlap instead of forming a chain of shared-memory latencies.
 __device__ __forceinline__ float window_max(const float* S, int ta, int tb, int tt, int pr) {
   float u = -INFINITY;
   if (pr <= 3) {
@@ -475,25 +508,49 @@ __device__ __forceinline__ float window_max(const float* S, int ta, int tb, int 
   return u;
 }
 
+// Mean over the in-range neighbours (the segment's halo reaches every in-range neighbour).
+__device__ __forceinline__ float window_avg(const float* S, int ta, int tb, int tt, int pr) {
+  const int lo = max(tt - pr, ta), hi = min(tt + pr, tb - 1);
+  float acc = 0.f;
+  if (pr <= 3) {
+    float w[7];
+#pragma unroll
+    for (int x = 0; x < 7; ++x) {
+      const int y = tt - 3 + x;
+      w[x] = (y >= lo && y <= hi) ? S[y - ta] : 0.f;
+    }
+    acc = ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + w[6]);
+  } else {
+#pragma unroll 8
+    for (int y = lo; y <= hi; ++y) acc += S[y - ta];
+  }
+  return acc / (float)(hi - lo + 1);
+}
+
 __device__ void pool_segment(const float* S, int ta, int tb, int a0, int a1, int pr, int P, int page_reduce,
-                             float* out, float* pout, int tid, int nthreads) {
+                             int pool_type, float gscale, float* out, float* pout, int tid, int nthreads) {
+  const bool avg = pool_type == KVSEL_POOL_AVG;
 #pragma unroll 4
-  for (int tt = a0 + tid; tt < a1; tt += nthreads) out[tt] = window_max(S, ta, tb, tt, pr);
+  for (int tt = a0 + tid; tt < a1; tt += nthreads)
+    out[tt] = gscale * (avg ? window_avg(S, ta, tb, tt, pr) : window_max(S, ta, tb, tt, pr));
   if (P == 1) return;
   for (int p = a0 / P + tid; p * P < a1; p += nthreads) {
     const int lo = p * P, hi = min(a1, lo + P);
     float pv;
-    if (page_reduce == KVSEL_REDUCE_MAX) {
-      // the max over the page of the pooled scores is the max over the page widened by the window
+    if (page_reduce == KVSEL_REDUCE_MAX && !avg) {
+      // the max over the page of the max-pooled scores is the max over the page widened by the window
       const int wlo = max(lo - pr, ta), whi = min(hi - 1 + pr, tb - 1);
       pv = -INFINITY;
 #pragma unroll 8
       for (int y = wlo; y <= whi; ++y) pv = fmaxf(pv, S[y - ta]);
+    } else if (page_reduce == KVSEL_REDUCE_MAX) {
+      pv = -INFINITY;
+      for (int tt = lo; tt < hi; ++tt) pv = fmaxf(pv, window_avg(S, ta, tb, tt, pr));
     } else {
       pv = 0.f;
-      for (int tt = lo; tt < hi; ++tt) pv += window_max(S, ta, tb, tt, pr);
+      for (int tt = lo; tt < hi; ++tt) pv += avg ? window_avg(S, ta, tb, tt, pr) : window_max(S, ta, tb, tt, pr);
     }
-    pout[p] = pv;
+    pout[p] = gscale * pv;
   }
 }
 
@@ -524,8 +581,10 @@ __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base
     const Item it = decode<true>(t, a.sh, item);
     epi_sync();                                          // readers of the previous item are done
     for (int i = e.etid; i < it.tb - it.ta; i += kEpiThreads) Ss[i] = 0.f;
-    for (int i = e.etid; i < RT; i += kEpiThreads)
-      lse_s[i] = i < a.sh.R ? -a.lse[(int64_t)it.unit * a.sh.R + i] : -INFINITY;   // padding rows give p = 0
+    for (int i = e.etid; i < RT; i += kEpiThreads) {
+      if (a.sh.logits) lse_s[i] = i < a.sh.R ? a.sh.scale_nat : 0.f;    // row weights of the logit sum
+      else lse_s[i] = i < a.sh.R ? -a.lse[(int64_t)it.unit * a.sh.R + i] : -INFINITY;   // padding rows: p = 0
+    }
     epi_sync();
     // -lse of this warpgroup's 64 rows in registers (column pairs); with 128 rows per warpgroup
     // they are read from shared memory instead (the registers would not fit)
@@ -548,7 +607,7 @@ __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base
           tc_fence_before();
           __syncwarp();
           if (e.lane == 0) mbar_arrive(tempty(ts));
-          red = colmass64<MAXW>(v64, nl, scale);
+          red = a.sh.logits ? linmass64<MAXW>(v64, nl) : colmass64<MAXW>(v64, nl, scale);
         } else {
           float v64[64], w64[64];
           tmem_ld64(taddr, v64);
@@ -557,13 +616,14 @@ __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base
           __syncwarp();
           if (e.lane == 0) mbar_arrive(tempty(ts));
           const float2* nls = reinterpret_cast<const float2*>(nlse + col0);
-          const float r0 = colmass64<MAXW>(v64, nls, scale);
-          const float r1 = colmass64<MAXW>(w64, nls + 32, scale);
+          const float r0 = a.sh.logits ? linmass64<MAXW>(v64, nls) : colmass64<MAXW>(v64, nls, scale);
+          const float r1 = a.sh.logits ? linmass64<MAXW>(w64, nls + 32) : colmass64<MAXW>(w64, nls + 32, scale);
           red = MAXW == 0 ? r0 + r1 : fmaxf(r0, r1);
         }
         const int key = t0 + e.lrow;
         if (key < it.tb) {
           // two addends per key (one per warpgroup): the result does not depend on their order
+          // (group max runs here with probabilities only, which are >= 0, so the int order is the float order)
           if constexpr (MAXW == 0) atomicAdd(&Ss[key - it.ta], red);
           else atomicMax(reinterpret_cast<int*>(&Ss[key - it.ta]), __float_as_int(red));
         }
@@ -580,7 +640,8 @@ __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base
       const int n_pages = (it.L + P_ - 1) / P_;
       pout = a.page_scores + si.p_off + ((int64_t)it.layer * a.sh.h_kv + it.g) * n_pages;
     }
-    pool_segment(Ss, it.ta, it.tb, it.a0, it.a1, pr, P_, a.sh.page_reduce, out, pout, e.etid, kEpiThreads);
+    pool_segment(Ss, it.ta, it.tb, it.a0, it.a1, pr, P_, a.sh.page_reduce, a.sh.pool_type, a.sh.gscale, out, pout,
+                 e.etid, kEpiThreads);
   }
 }
 
@@ -695,10 +756,13 @@ template <int RT, int D>
 kvsel_status run_tc(const TcArgs& a, const SeqTable& t1, const SeqTable& t2, const CUtensorMap& tq,
                     const CUtensorMap& tk, int sms, cudaStream_t s) {
   constexpr int NK = (RT == 256 && D == 128) ? 3 : 4;
-  kvsel_status st = launch_one<false, RT, D, NK, 0>("score_pass1_tc", tq, tk, a, t1, sms, s);
-  if (st != KVSEL_OK) return st;
-  if ((st = launch_lse_combine(a.sh, t1, a.part, a.lse, s)) != KVSEL_OK) return st;
-  if (a.sh.group_reduce == KVSEL_REDUCE_SUM) return launch_one<true, RT, D, NK, 0>("score_pass2_tc", tq, tk, a, t2, sms, s);
+  kvsel_status st;
+  if (!a.sh.logits) {   // the softmax needs each row's log-sum-exp first
+    if ((st = launch_one<false, RT, D, NK, 0>("score_pass1_tc", tq, tk, a, t1, sms, s)) != KVSEL_OK) return st;
+    if ((st = launch_lse_combine(a.sh, t1, a.part, a.lse, s)) != KVSEL_OK) return st;
+  }
+  if (a.sh.group_reduce != KVSEL_REDUCE_MAX)
+    return launch_one<true, RT, D, NK, 0>("score_pass2_tc", tq, tk, a, t2, sms, s);
   switch (a.sh.W) {
     case 8: return launch_one<true, RT, D, NK, 8>("score_pass2_tc", tq, tk, a, t2, sms, s);
     case 16: return launch_one<true, RT, D, NK, 16>("score_pass2_tc", tq, tk, a, t2, sms, s);
@@ -719,8 +783,9 @@ kvsel_status launch_score(const ScoreShape& sh_in, const SeqTable& base, const v
   for (int b = 0; b < base.batch; ++b) k_rows += ups * base.s[b].n_keys;
   const int64_t q_rows = (int64_t)base.batch * sh.n_layers * sh.h_q * sh.W;
   const DevInfo dev = device_info();
-  const bool w_ok = sh.group_reduce == KVSEL_REDUCE_SUM ||
-                    (sh.W == 8 || sh.W == 16 || sh.W == 32 || sh.W == 64);
+  // group max: register-resident heads of 8 .. 64 rows, probabilities only (logit sums may be negative)
+  const bool w_ok = sh.group_reduce != KVSEL_REDUCE_MAX ||
+                    (!sh.logits && (sh.W == 8 || sh.W == 16 || sh.W == 32 || sh.W == 64));
   const bool tc = dev.major == 10 && dev.sms > 0 && sh.R <= 256 && w_ok && k_rows + 256 < (int64_t(1) << 31) &&
                   q_rows + 256 < (int64_t(1) << 31) && encode_fn() != nullptr;
   sh.seg1 = (int32_t)kScoreSeg1;

@@ -1,5 +1,5 @@
 // Top-k selection with ties to the lower index, recency / window append, and the
-// cross-layer L1-normalised mean.
+// aggregation of group scores across KV heads and layers (L1-normalised mean or max), pooled.
 //
 // Top-k: one CTA per (sequence, layer, KV head) row.  Scores map to order-
 // preserving uint32 keys; a 4-pass 8-bit radix select finds the k-th largest
@@ -54,7 +54,7 @@ __device__ unsigned long long block_scan_u64(unsigned long long v, unsigned long
 struct TopkArgs {
   const float* scores;
   int32_t* idx;
-  int32_t layers, h_kv, k, n_recent, P, W, n_sel;
+  int32_t rows, k, n_recent, P, n_sel;
 };
 
 template <bool SMEM>
@@ -66,9 +66,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
   __shared__ uint32_t sel_digit, sel_gt;
 
   const int row = blockIdx.x;
-  const int rows_per_seq = a.layers * a.h_kv;
-  const int b = row / rows_per_seq;
-  const int lg = row % rows_per_seq;
+  const int b = row / a.rows;
+  const int lg = row % a.rows;
   const SeqInfo& si = t.s[b];
   const int n = a.P == 1 ? si.L : (si.L + a.P - 1) / a.P;
   const int n_cand = n - a.n_recent;
@@ -144,111 +143,154 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
       }
     }
   }
-  // recency pages and window pages (page mode) or window tokens (token mode) follow n_cand
+  // recency pages, then (when appended) window pages or window tokens: the indices from n_cand on
   for (int i = tid; i < a.n_sel - a.k; i += kTopkThreads) out[a.k + i] = n_cand + i;
 }
 
-// ------------------------------------------------------------------------ cross-layer mean
+// ------------------------------------------------------------------------ aggregation
 constexpr int kCombThreads = 256;
 constexpr int kCombChunk = 1024;
 
-__global__ void __launch_bounds__(kCombThreads) layer_norms(const float* scores, float* norms,
-                                                            const __grid_constant__ SeqTable t, int n_layers,
-                                                            int h_kv) {
-  __shared__ float red[kCombThreads];
-  const int row = blockIdx.x;                       // (b, layer, g)
-  const int per_seq = n_layers * h_kv;
-  const int b = row / per_seq, lg = row % per_seq;
-  const SeqInfo& si = t.s[b];
-  const float* s = scores + si.s_off + (int64_t)lg * si.L;
+struct AggArgs {
+  const float* scores;      // raw group scores, per sequence [n_layers][h_kv][L]
+  float* norms;             // [batch][hi - lo + 1][n_h] L1 norms (L1 mean only)
+  float* out;               // per sequence [n_l][n_h][L]
+  int32_t n_layers, h_kv, lo, hi, layer_op, head_op, n_l, n_h, pool_k, pool_type;
+};
+
+// Value of (layer, output head oh) at token tt: one KV head, or the sum over all of them.
+__device__ __forceinline__ float head_value(const AggArgs& a, const SeqInfo& si, int layer, int oh, int tt) {
+  const float* base = a.scores + si.s_off + (int64_t)layer * a.h_kv * si.L + tt;
+  if (a.head_op == KVSEL_HEADS_EACH) return base[(int64_t)oh * si.L];
   float acc = 0.f;
-  for (int i = threadIdx.x; i < si.L; i += kCombThreads) acc += fabsf(s[i]);
+  for (int g = 0; g < a.h_kv; ++g) acc += base[(int64_t)g * si.L];
+  return acc;
+}
+
+// L1 norm over the prefix of each (sequence, layer of the range, output head) row.
+__global__ void __launch_bounds__(kCombThreads) agg_norms(const __grid_constant__ AggArgs a,
+                                                          const __grid_constant__ SeqTable t) {
+  __shared__ float red[kCombThreads];
+  const int nr = a.hi - a.lo + 1;
+  const int row = blockIdx.x;                        // (b, layer - lo, oh)
+  const int b = row / (nr * a.n_h);
+  const int rem = row % (nr * a.n_h);
+  const int layer = a.lo + rem / a.n_h, oh = rem % a.n_h;
+  const SeqInfo& si = t.s[b];
+  float acc = 0.f;
+  for (int i = threadIdx.x; i < si.L; i += kCombThreads) acc += fabsf(head_value(a, si, layer, oh, i));
   red[threadIdx.x] = acc;
   __syncthreads();
   for (int w = kCombThreads / 2; w > 0; w >>= 1) {
     if ((int)threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
     __syncthreads();
   }
-  if (threadIdx.x == 0) norms[row] = red[0];
+  if (threadIdx.x == 0) a.norms[row] = red[0];
 }
 
-__global__ void __launch_bounds__(kCombThreads) layer_mean_pool(const float* scores, const float* norms,
-                                                                float* combined,
-                                                                const __grid_constant__ SeqTable t,
-                                                                int n_layers, int h_kv, int lo, int hi,
-                                                                int pool_k) {
+// One chunk of one output row: the aggregated value of every token of the chunk and its pooling
+// halo, then the pooled outputs of the chunk.
+__global__ void __launch_bounds__(kCombThreads) agg_pool(const __grid_constant__ AggArgs a,
+                                                         const __grid_constant__ SeqTable t) {
   __shared__ float S[kCombChunk + 64];
-  const int b = blockIdx.z, g = blockIdx.y;
+  const int b = blockIdx.z;
+  const int ol = blockIdx.y / a.n_h, oh = blockIdx.y % a.n_h;
   const SeqInfo& si = t.s[b];
   const int a0 = blockIdx.x * kCombChunk;
   if (a0 >= si.L) return;
   const int a1 = min(si.L, a0 + kCombChunk);
-  const int pr = (pool_k - 1) / 2;
+  const int pr = (a.pool_k - 1) / 2;
   const int ea = max(0, a0 - pr), eb = min(si.L, a1 + pr);
-  const float inv_n = 1.0f / (float)(hi - lo + 1);
+  const int nr = a.hi - a.lo + 1;
+  const float inv_n = 1.0f / (float)nr;
   for (int tt = ea + threadIdx.x; tt < eb; tt += kCombThreads) {
-    float acc = 0.f;
-    for (int layer = lo; layer <= hi; ++layer) {
-      const int64_t row = ((int64_t)b * n_layers + layer) * h_kv + g;
-      const float v = scores[si.s_off + ((int64_t)layer * h_kv + g) * si.L + tt];
-      acc += v / norms[row];
+    float v;
+    if (a.layer_op == KVSEL_LAYERS_EACH) {
+      v = head_value(a, si, a.lo + ol, oh, tt);
+    } else if (a.layer_op == KVSEL_LAYERS_MAX) {
+      v = head_value(a, si, a.lo, oh, tt);
+      for (int layer = a.lo + 1; layer <= a.hi; ++layer) v = fmaxf(v, head_value(a, si, layer, oh, tt));
+    } else {
+      float acc = 0.f;
+      for (int layer = a.lo; layer <= a.hi; ++layer)
+        acc += head_value(a, si, layer, oh, tt) / a.norms[((int64_t)b * nr + (layer - a.lo)) * a.n_h + oh];
+      v = acc * inv_n;
     }
-    S[tt - ea] = acc * inv_n;
+    S[tt - ea] = v;
   }
   __syncthreads();
-  float* out = combined + si.s_off / n_layers + (int64_t)g * si.L;
+  const int64_t tok_off = si.s_off / ((int64_t)a.n_layers * a.h_kv);   // tokens of earlier sequences
+  float* out = a.out + tok_off * a.n_l * a.n_h + ((int64_t)ol * a.n_h + oh) * si.L;
   for (int tt = a0 + threadIdx.x; tt < a1; tt += kCombThreads) {
     const int l0 = max(tt - pr, ea), l1 = min(tt + pr, eb - 1);
     float u = S[l0 - ea];
-    for (int x = l0 + 1; x <= l1; ++x) u = fmaxf(u, S[x - ea]);
+    if (a.pool_type == KVSEL_POOL_AVG) {
+      for (int x = l0 + 1; x <= l1; ++x) u += S[x - ea];
+      u /= (float)(l1 - l0 + 1);
+    } else {
+      for (int x = l0 + 1; x <= l1; ++x) u = fmaxf(u, S[x - ea]);
+    }
     out[tt] = u;
   }
 }
 
 }  // namespace
 
-kvsel_status launch_topk(const kvsel_desc& d, const SeqTable& t, int layers, int k, int n_recent,
-                         const float* scores, int32_t* idx, cudaStream_t s) {
+kvsel_status launch_topk(const kvsel_desc& d, const SeqTable& t, int rows, int k, int n_recent,
+                         bool append_window, const float* scores, int32_t* idx, cudaStream_t s) {
   TopkArgs a;
   a.scores = scores;
   a.idx = idx;
-  a.layers = layers;
-  a.h_kv = d.h_kv;
+  a.rows = rows;
   a.k = k;
   a.n_recent = n_recent;
   a.P = d.page_size;
-  a.W = d.window;
-  a.n_sel = d.page_size == 1 ? k + d.window : k + n_recent + d.window / d.page_size;
+  a.n_sel = d.page_size == 1 ? k + (append_window ? d.window : 0)
+                             : k + n_recent + (append_window ? d.window / d.page_size : 0);
   int64_t nmax = 0;
   for (int b = 0; b < d.batch; ++b) {
     const int64_t n = d.page_size == 1 ? d.prefix_lens[b] : (d.prefix_lens[b] + d.page_size - 1) / d.page_size;
     nmax = n > nmax ? n : nmax;
   }
-  const int rows = d.batch * layers * d.h_kv;
+  const int grid = d.batch * rows;
   TraceScope ts("topk_radix", s);
   if (nmax <= kSmemKeysMax) {
     const size_t smem = (size_t)nmax * sizeof(uint32_t);
     if (set_smem((const void*)topk_kernel<true>, smem) != cudaSuccess) return KVSEL_ERR_CUDA;
-    topk_kernel<true><<<rows, kTopkThreads, smem, s>>>(a, t);
+    topk_kernel<true><<<grid, kTopkThreads, smem, s>>>(a, t);
   } else {
-    topk_kernel<false><<<rows, kTopkThreads, 0, s>>>(a, t);
+    topk_kernel<false><<<grid, kTopkThreads, 0, s>>>(a, t);
   }
   return launch_status();
 }
 
-kvsel_status launch_combine_layers(const kvsel_desc& d, const SeqTable& t, const float* scores, int lo, int hi,
-                                   float* norms, float* combined, cudaStream_t s) {
+kvsel_status launch_aggregate(const kvsel_desc& d, const SeqTable& t, const float* scores, int lo, int hi,
+                              int layer_op, int head_op, float* norms, float* out, cudaStream_t s) {
+  AggArgs a;
+  a.scores = scores;
+  a.norms = norms;
+  a.out = out;
+  a.n_layers = d.n_layers;
+  a.h_kv = d.h_kv;
+  a.lo = lo;
+  a.hi = hi;
+  a.layer_op = layer_op;
+  a.head_op = head_op;
+  a.n_l = layer_op == KVSEL_LAYERS_EACH ? hi - lo + 1 : 1;
+  a.n_h = head_op == KVSEL_HEADS_EACH ? d.h_kv : 1;
+  a.pool_k = d.pool_k;
+  a.pool_type = d.pool_type;
   kvsel_status st;
-  {
+  if (layer_op == KVSEL_LAYERS_L1_MEAN) {
     TraceScope ts("layer_norms", s);
-    layer_norms<<<d.batch * d.n_layers * d.h_kv, kCombThreads, 0, s>>>(scores, norms, t, d.n_layers, d.h_kv);
+    agg_norms<<<d.batch * (hi - lo + 1) * a.n_h, kCombThreads, 0, s>>>(a, t);
     if ((st = launch_status()) != KVSEL_OK) return st;
   }
   int64_t lmax = 0;
   for (int b = 0; b < d.batch; ++b) lmax = d.prefix_lens[b] > lmax ? d.prefix_lens[b] : lmax;
-  dim3 grid((unsigned)((lmax + kCombChunk - 1) / kCombChunk), d.h_kv, d.batch);
-  TraceScope ts("layer_mean_pool", s);
-  layer_mean_pool<<<grid, kCombThreads, 0, s>>>(scores, norms, combined, t, d.n_layers, d.h_kv, lo, hi, d.pool_k);
+  dim3 grid((unsigned)((lmax + kCombChunk - 1) / kCombChunk), (unsigned)(a.n_l * a.n_h), d.batch);
+  TraceScope ts("aggregate_pool", s);
+  agg_pool<<<grid, kCombThreads, 0, s>>>(a, t);
   return launch_status();
 }
 

@@ -17,7 +17,11 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "_build", "libkvsel.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = range(7)
-REDUCE_SUM, REDUCE_MAX = 0, 1
+REDUCE_SUM, REDUCE_MAX, REDUCE_MEAN = 0, 1, 2
+POOL_MAX, POOL_AVG = 0, 1
+SCORE_SOFTMAX, SCORE_LOGITS = 0, 1
+LAYERS_EACH, LAYERS_L1_MEAN, LAYERS_MAX = 0, 1, 2
+HEADS_EACH, HEADS_SUM = 0, 1
 MAX_BATCH, MAX_WINDOW, MAX_ROWS, MAX_PAGE, WS_ALIGN = 128, 64, 256, 256, 256
 
 
@@ -40,6 +44,8 @@ class Desc(ctypes.Structure):
         ("pool_k", ctypes.c_int32),
         ("page_size", ctypes.c_int32),
         ("page_reduce", ctypes.c_int32),
+        ("pool_type", ctypes.c_int32),
+        ("score_mode", ctypes.c_int32),
     ]
 
 
@@ -58,8 +64,11 @@ def _load():
         "kvsel_score": (I32, [D, VP, VP, VP, VP, VP, SZ, VP]),
         "kvsel_score_noalloc": (I32, [D, VP, VP, VP, VP, VP]),
         "kvsel_combine_layers": (I32, [D, VP, I32, I32, VP, VP, SZ, VP]),
+        "kvsel_aggregate": (I32, [D, VP, I32, I32, I32, I32, VP, VP, SZ, VP]),
+        "kvsel_select": (I32, [D, VP, I32, I32, I32, I32, VP, VP, SZ, VP]),
         "kvsel_topk": (I32, [D, VP, I32, I32, I32, VP, VP, SZ, VP]),
         "kvsel_compact": (I32, [D, VP, VP, VP, I32, I32, VP, VP, VP, VP]),
+        "kvsel_compact_layers": (I32, [D, VP, VP, VP, I32, I32, I32, I32, I32, VP, VP, VP, VP]),
         "kvsel_pagetable": (I32, [D, VP, I32, I32, P(I32), VP, VP, VP, SZ, VP]),
         "kvsel_read_device_error": (I32, [VP, VP]),
         "kvsel_selftest_bounded_wait": (I32, [VP, ctypes.c_uint32, I32, VP]),
@@ -77,9 +86,10 @@ def _load():
 
 
 _lib = _load()
-EXPORTED = ("kvsel_workspace_size", "kvsel_score", "kvsel_score_noalloc", "kvsel_combine_layers", "kvsel_topk",
-            "kvsel_compact", "kvsel_pagetable", "kvsel_read_device_error", "kvsel_selftest_bounded_wait", "kvsel_status_string", "kvsel_version",
-            "kvsel_trace_enable", "kvsel_trace_read", "kvsel_launch_count")
+EXPORTED = ("kvsel_workspace_size", "kvsel_score", "kvsel_score_noalloc", "kvsel_combine_layers",
+            "kvsel_aggregate", "kvsel_select", "kvsel_topk", "kvsel_compact", "kvsel_compact_layers",
+            "kvsel_pagetable", "kvsel_read_device_error", "kvsel_selftest_bounded_wait", "kvsel_status_string",
+            "kvsel_version", "kvsel_trace_enable", "kvsel_trace_read", "kvsel_launch_count")
 
 
 def status_string(status: int) -> str:
@@ -114,11 +124,12 @@ def _stream(stream) -> Optional[int]:
 
 def make_desc(*, n_layers: int, h_q: int, h_kv: int, head_dim: int, window: int,
               prefix_lens: Sequence[int], group_reduce: int = REDUCE_SUM, pool_k: int = 7,
-              page_size: int = 1, page_reduce: int = REDUCE_MAX) -> Desc:
+              page_size: int = 1, page_reduce: int = REDUCE_MAX, pool_type: int = POOL_MAX,
+              score_mode: int = SCORE_SOFTMAX) -> Desc:
     """A descriptor; it keeps its own host copy of prefix_lens alive."""
     lens = (ctypes.c_int64 * len(prefix_lens))(*[int(x) for x in prefix_lens])
     d = Desc(n_layers, h_q, h_kv, head_dim, window, len(prefix_lens), lens, group_reduce, pool_k,
-             page_size, page_reduce)
+             page_size, page_reduce, pool_type, score_mode)
     d._lens = lens
     return d
 
@@ -150,6 +161,20 @@ def kvsel_combine_layers(desc, scores, layer_lo: int, layer_hi: int, combined, w
                                      _ptr(ws), nb, _stream(stream)), "kvsel_combine_layers")
 
 
+def kvsel_aggregate(desc, scores, layer_lo: int, layer_hi: int, layer_op: int, head_op: int, out, ws,
+                    ws_bytes=None, stream=None):
+    nb = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    _check(_lib.kvsel_aggregate(ctypes.byref(desc), _ptr(scores), layer_lo, layer_hi, layer_op, head_op, _ptr(out),
+                                _ptr(ws), nb, _stream(stream)), "kvsel_aggregate")
+
+
+def kvsel_select(desc, scores, rows: int, k: int, n_recent: int, append_window: bool, idx_out, ws, ws_bytes=None,
+                 stream=None):
+    nb = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    _check(_lib.kvsel_select(ctypes.byref(desc), _ptr(scores), rows, k, n_recent, 1 if append_window else 0,
+                             _ptr(idx_out), _ptr(ws), nb, _stream(stream)), "kvsel_select")
+
+
 def kvsel_topk(desc, scores, layers: int, k: int, n_recent: int, idx_out, ws, ws_bytes=None, stream=None):
     nb = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
     _check(_lib.kvsel_topk(ctypes.byref(desc), _ptr(scores), layers, k, n_recent, _ptr(idx_out), _ptr(ws), nb,
@@ -159,6 +184,13 @@ def kvsel_topk(desc, scores, layers: int, k: int, n_recent: int, idx_out, ws, ws
 def kvsel_compact(desc, k, v, idx, idx_layers: int, n_sel: int, k_out, v_out, ws=None, stream=None):
     _check(_lib.kvsel_compact(ctypes.byref(desc), _ptr(k), _ptr(v), _ptr(idx), idx_layers, n_sel, _ptr(k_out),
                               _ptr(v_out), _ptr(ws), _stream(stream)), "kvsel_compact")
+
+
+def kvsel_compact_layers(desc, k, v, idx, idx_layers: int, idx_heads: int, layer_lo: int, n_layers_out: int,
+                         n_sel: int, k_out, v_out, ws=None, stream=None):
+    _check(_lib.kvsel_compact_layers(ctypes.byref(desc), _ptr(k), _ptr(v), _ptr(idx), idx_layers, idx_heads,
+                                     layer_lo, n_layers_out, n_sel, _ptr(k_out), _ptr(v_out), _ptr(ws),
+                                     _stream(stream)), "kvsel_compact_layers")
 
 
 def kvsel_pagetable(desc, mask, n_qblk: int, n_kvblk_max: int, n_kvblk: Sequence[int], kv_indptr, kv_indices,

@@ -1,25 +1,37 @@
 """The whole selection path for one workload: buffers (torch) plus the C-ABI call sequence.
 
-score -> [combine_layers] -> topk -> compact, and the block-union page table
-when the workload has a block mask.  Every step runs in libkvsel's kernels;
-this module only allocates device memory and orders the calls on one stream.
+score -> [aggregate over layers / heads] -> top-k -> compact, and the block-union
+page table when the workload has a block mask; the CLAA schedule (per-layer
+selections plus a prune index from the token-wise max over a layer buffer) for
+workloads that carry one.  Every step runs in libkvsel's kernels; this module
+only allocates device memory and orders the calls on one stream.
 """
 
 from __future__ import annotations
 
+import math
 from typing import Optional
 
 import torch
 
 from . import kvsel as K
 
+_REDUCE = {"sum": K.REDUCE_SUM, "max": K.REDUCE_MAX, "mean": K.REDUCE_MEAN}
 
-def desc_for(w, pool_k: Optional[int] = None):
-    return K.make_desc(n_layers=w.n_layers, h_q=w.h_q, h_kv=w.h_kv, head_dim=w.head_dim, window=w.window,
-                       prefix_lens=w.prefix_lens,
-                       group_reduce=K.REDUCE_SUM if w.group_reduce == "sum" else K.REDUCE_MAX,
+
+def keep_count(keep_rate: float, L: int) -> int:
+    """Prefix tokens kept for a keep rate r (CLAA's keep_rate): floor(r * L + 1/2), clipped to [0, L]."""
+    return int(min(L, max(0, math.floor(keep_rate * L + 0.5))))
+
+
+def desc_for(w, pool_k: Optional[int] = None, n_layers: Optional[int] = None):
+    return K.make_desc(n_layers=w.n_layers if n_layers is None else n_layers, h_q=w.h_q, h_kv=w.h_kv,
+                       head_dim=w.head_dim, window=w.window, prefix_lens=w.prefix_lens,
+                       group_reduce=_REDUCE[w.group_reduce],
                        pool_k=w.pool_k if pool_k is None else pool_k, page_size=w.page_size,
-                       page_reduce=K.REDUCE_MAX if w.page_reduce == "max" else K.REDUCE_SUM)
+                       page_reduce=K.REDUCE_MAX if w.page_reduce == "max" else K.REDUCE_SUM,
+                       pool_type=K.POOL_AVG if w.pool_type == "avg" else K.POOL_MAX,
+                       score_mode=K.SCORE_LOGITS if w.score_mode == "logits" else K.SCORE_SOFTMAX)
 
 
 def pack(inputs, device="cuda"):
@@ -33,14 +45,25 @@ def pack(inputs, device="cuda"):
 
 
 class Pipeline:
-    """Buffers and descriptors of one workload ``w`` (a synth.Workload) on ``device``."""
+    """Buffers and descriptors of one workload ``w`` (a synth.Workload) on ``device``.
+
+    Per-KV-head selection (``head_reduce == "group"``): scores are pooled by the
+    scoring kernel, or combined across a layer range first.  All-head selection
+    (``"all"``): raw group scores are summed over every KV head of a layer and
+    pooled by kvsel_aggregate, and one selection per layer serves every KV head.
+    """
 
     def __init__(self, w, device="cuda", n_qblk: Optional[int] = None, n_kvblk_max: Optional[int] = None):
+        if w.claa is not None:
+            raise ValueError("CLAA workloads run through ClaaPipeline")
         self.w = w
         self.device = device
         xl = w.layer_range is not None
+        self.all_heads = w.head_reduce == "all"
+        if self.all_heads and (xl or w.page_size != 1):
+            raise ValueError("all-head selection is a token-mode, per-layer path")
         self.desc = desc_for(w)
-        self.desc_score = desc_for(w, pool_k=1) if xl else self.desc
+        self.desc_score = desc_for(w, pool_k=1) if (xl or self.all_heads) else self.desc
         ws_bytes = max(K.kvsel_workspace_size(self.desc), K.kvsel_workspace_size(self.desc_score))
         ws = torch.zeros(ws_bytes + K.WS_ALIGN, dtype=torch.uint8, device=device)
         off = (-ws.data_ptr()) % K.WS_ALIGN
@@ -53,9 +76,12 @@ class Pipeline:
         self.scores = torch.empty(n_tok, **f32)
         self.page_scores = torch.empty(n_pg, **f32) if P > 1 else None
         self.combined = torch.empty(sum(w.h_kv * L for L in w.prefix_lens), **f32) if xl else None
+        self.agg = torch.empty(sum(w.n_layers * L for L in w.prefix_lens), **f32) if self.all_heads else None
         self.idx_layers = 1 if xl else w.n_layers
+        self.idx_heads = 1 if self.all_heads else w.h_kv
         self.n_sel = w.n_sel()
-        self.idx = torch.empty((w.batch, self.idx_layers, w.h_kv, self.n_sel), dtype=torch.int32, device=device)
+        self.idx = torch.empty((w.batch, self.idx_layers, self.idx_heads, self.n_sel), dtype=torch.int32,
+                               device=device)
         rows = self.n_sel * P
         self.k_out = torch.empty((w.batch, w.n_layers, w.h_kv, rows, w.head_dim), dtype=torch.bfloat16,
                                  device=device)
@@ -73,17 +99,29 @@ class Pipeline:
 
     def select(self, stream=None):
         w = self.w
-        if w.layer_range is not None:
+        app = w.append_window
+        if self.all_heads:
+            K.kvsel_aggregate(self.desc, self.scores, 0, w.n_layers - 1, K.LAYERS_EACH, K.HEADS_SUM, self.agg,
+                              self.ws, self.ws_bytes, stream)
+            K.kvsel_select(self.desc, self.agg, w.n_layers, w.k_keep, 0, app, self.idx, self.ws, self.ws_bytes,
+                           stream)
+        elif w.layer_range is not None:
             lo, hi = w.layer_range
             K.kvsel_combine_layers(self.desc, self.scores, lo, hi, self.combined, self.ws, self.ws_bytes, stream)
-            K.kvsel_topk(self.desc, self.combined, 1, w.k_keep, w.n_recent, self.idx, self.ws, self.ws_bytes, stream)
+            K.kvsel_select(self.desc, self.combined, w.h_kv, w.k_keep, w.n_recent, app, self.idx, self.ws,
+                           self.ws_bytes, stream)
         else:
             src = self.scores if w.page_size == 1 else self.page_scores
-            K.kvsel_topk(self.desc, src, w.n_layers, w.k_keep, w.n_recent, self.idx, self.ws, self.ws_bytes, stream)
+            K.kvsel_select(self.desc, src, w.n_layers * w.h_kv, w.k_keep, w.n_recent, app, self.idx, self.ws,
+                           self.ws_bytes, stream)
 
     def compact(self, k, v, stream=None):
-        K.kvsel_compact(self.desc, k, v, self.idx, self.idx_layers, self.n_sel, self.k_out, self.v_out, self.ws,
-                        stream)
+        if self.idx_heads == self.w.h_kv:
+            K.kvsel_compact(self.desc, k, v, self.idx, self.idx_layers, self.n_sel, self.k_out, self.v_out, self.ws,
+                            stream)
+        else:
+            K.kvsel_compact_layers(self.desc, k, v, self.idx, self.idx_layers, 1, 0, self.w.n_layers, self.n_sel,
+                                   self.k_out, self.v_out, self.ws, stream)
 
     def pagetable(self, mask, n_kvblk, stream=None):
         K.kvsel_pagetable(self.desc, mask, self.n_qblk, self.n_kvblk_max, n_kvblk, self.kv_indptr,
@@ -117,3 +155,66 @@ class Pipeline:
         off = sum(w.h_kv * L for L in w.prefix_lens[:b])
         L = w.prefix_lens[b]
         return self.combined[off:off + w.h_kv * L].view(w.h_kv, L)
+
+
+class ClaaPipeline:
+    """CLAA selection of one prompt (CLAA, 'Three design decisions' and 'Complete flow and cost').
+
+    Layers m .. l_p are scored with the observation window (softmax mass summed
+    over the window rows and every head), each layer's pooled score picks that
+    layer's kept tokens (k from the keep rate) and its cache is compacted with
+    them for every KV head; at l_p the token-wise max over the buffered layers
+    max(m, l_p - n + 1) .. l_p, pooled, picks the sequence prune index.  Layers
+    below m keep their full cache.  Layers after l_p run on the pruned prompt,
+    which the model produces; a second pipeline scores them.
+    """
+
+    def __init__(self, w, device="cuda"):
+        if w.claa is None or w.batch != 1:
+            raise ValueError("a CLAA workload of one prompt")
+        self.w = w
+        self.device = device
+        m, lp, nbuf, rate = w.claa
+        self.m, self.lp = m, lp
+        self.n_sc = lp - m + 1                              # layers scored and compacted
+        self.buf_lo = max(m, lp - nbuf + 1) - m             # buffer, relative to layer m
+        L = w.prefix_lens[0]
+        self.k = keep_count(rate, L)
+        # the scored layers are a contiguous slice of the one prompt's q and k
+        self.desc = desc_for(w, n_layers=self.n_sc)
+        self.desc_score = desc_for(w, pool_k=1, n_layers=self.n_sc)
+        self.desc_full = desc_for(w)
+        ws_bytes = max(K.kvsel_workspace_size(self.desc), K.kvsel_workspace_size(self.desc_full))
+        ws = torch.zeros(ws_bytes + K.WS_ALIGN, dtype=torch.uint8, device=device)
+        off = (-ws.data_ptr()) % K.WS_ALIGN
+        self.ws = ws[off:off + ws_bytes]
+        self.ws_bytes = ws_bytes
+        f32 = dict(dtype=torch.float32, device=device)
+        self.scores = torch.empty((self.n_sc, w.h_kv, L), **f32)       # raw group scores
+        self.layer_scores = torch.empty((self.n_sc, L), **f32)          # pooled all-head score per layer
+        self.prune_scores = torch.empty((1, L), **f32)                  # pooled max over the buffer
+        self.n_sel = self.k + (w.window if w.append_window else 0)
+        self.idx = torch.empty((1, self.n_sc, 1, self.n_sel), dtype=torch.int32, device=device)
+        self.prune_idx = torch.empty((1, 1, self.n_sel), dtype=torch.int32, device=device)
+        self.k_out = torch.empty((1, self.n_sc, w.h_kv, self.n_sel, w.head_dim), dtype=torch.bfloat16, device=device)
+        self.v_out = torch.empty_like(self.k_out)
+
+    def run(self, q, k, v, stream=None):
+        """q [1, n_layers, h_q, W, d]; k, v the prompt's caches (flat, layout of the library)."""
+        w = self.w
+        L = w.prefix_lens[0]
+        per_layer = w.h_kv * (L + w.window) * w.head_dim
+        q_sc = q[:, self.m:self.lp + 1].contiguous() if q.dim() == 5 else q
+        k_sc = k.reshape(-1)[self.m * per_layer:(self.lp + 1) * per_layer]
+        app = w.append_window
+        K.kvsel_score(self.desc_score, q_sc, k_sc, self.scores, None, self.ws, self.ws_bytes, stream)
+        K.kvsel_aggregate(self.desc, self.scores, 0, self.n_sc - 1, K.LAYERS_EACH, K.HEADS_SUM, self.layer_scores,
+                          self.ws, self.ws_bytes, stream)
+        K.kvsel_select(self.desc, self.layer_scores, self.n_sc, self.k, 0, app, self.idx, self.ws, self.ws_bytes,
+                       stream)
+        K.kvsel_compact_layers(self.desc_full, k, v, self.idx, self.n_sc, 1, self.m, self.n_sc, self.n_sel,
+                               self.k_out, self.v_out, self.ws, stream)
+        K.kvsel_aggregate(self.desc, self.scores, self.buf_lo, self.n_sc - 1, K.LAYERS_MAX, K.HEADS_SUM,
+                          self.prune_scores, self.ws, self.ws_bytes, stream)
+        K.kvsel_select(self.desc, self.prune_scores, 1, self.k, 0, app, self.prune_idx, self.ws, self.ws_bytes,
+                       stream)

@@ -54,8 +54,8 @@ class Workload:
     head_dim: int
     window: int
     prefix_lens: tuple
-    group_reduce: str = "sum"          # "sum" | "max" over the query heads of a group
-    pool_k: int = 7                    # odd max-pool width, 1 = off
+    group_reduce: str = "sum"          # "sum" | "max" | "mean" over the query heads of a group
+    pool_k: int = 7                    # odd pool width, 1 = off
     page_size: int = 1                 # 1 = token mode, P > 1 = page mode
     page_reduce: str = "max"           # "max" | "sum" over the tokens of a page
     k_keep: int = 64
@@ -68,6 +68,13 @@ class Workload:
     q_chunk: int = 1024
     block: int = 64
     mask_density: float = 0.10
+    # scoring variants
+    pool_type: str = "max"             # "max" | "avg" pooling
+    score_mode: str = "softmax"        # "softmax" | "logits" (pre-softmax, GemFilter)
+    head_reduce: str = "group"         # "group": one selection per KV head; "all": sum over every KV head
+    append_window: bool = True         # False: the window rows are not kept (LookaheadKV's lookahead rows)
+    # CLAA schedule: (defer m, pruning layer l_p, buffer n, keep rate); k_keep then comes from the rate
+    claa: Optional[tuple] = None
 
     @property
     def batch(self) -> int:
@@ -86,9 +93,10 @@ class Workload:
 
     def n_sel(self) -> int:
         """Selected entries per (sequence, layer, KV head) row of the index output."""
+        win = self.window if self.append_window else 0
         if self.page_size == 1:
-            return self.k_keep + self.window
-        return self.k_keep + self.n_recent + self.window // self.page_size
+            return self.k_keep + win
+        return self.k_keep + self.n_recent + win // self.page_size
 
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -116,9 +124,28 @@ LLAMA70B_64K_XLAYER = Workload("llama70b_80l_h64x8_d128_L65536_W32_xlayer", 4, 8
 
 WORKLOADS = (TINY, LLAMA8B_32K, LLAMA8B_128K_PAGED, RAGGED_B8, LLAMA70B_64K_XLAYER)
 
+# Scoring variants of the pages on the LLaMA-8B 32K shape.
+# CLAA: W = 8 window, softmax mass summed over the window and all heads, average pool 7, m = 4
+# deferred layers, a buffer of n = 4 layers, pruning layer l_p = 15, keep rate 0.2 ('Three design
+# decisions'; 'Experimental setup').
+CLAA_LLAMA8B_32K = Workload("claa_llama8b_32l_h32x8_d128_L32768_W8_keep0.2", 5, 32, 32, 8, 128, 8, (32768,),
+                            group_reduce="sum", pool_k=7, pool_type="avg", head_reduce="all", n_clusters=8,
+                            claa=(4, 15, 4, 0.2))
+# GemFilter: the last prompt token's pre-softmax logits summed over all heads, average pool 7, 1024 kept.
+GEMFILTER_LLAMA8B_32K = Workload("gemfilter_llama8b_32l_h32x8_d128_L32768_W1", 6, 32, 32, 8, 128, 1, (32768,),
+                                 group_reduce="sum", pool_k=7, pool_type="avg", score_mode="logits",
+                                 head_reduce="all", k_keep=1024, n_clusters=8)
+# LookaheadKV: 32 lookahead rows averaged per KV head, pooled, top 128 per head; the lookahead rows
+# themselves are not kept.
+LOOKAHEAD_LLAMA8B_32K = Workload("lookahead_llama8b_32l_h32x8_d128_L32768_W32_C128", 7, 32, 32, 8, 128, 32,
+                                 (32768,), group_reduce="mean", pool_k=7, pool_type="avg", k_keep=128,
+                                 append_window=False, n_clusters=8)
+
+VARIANTS = (CLAA_LLAMA8B_32K, GEMFILTER_LLAMA8B_32K, LOOKAHEAD_LLAMA8B_32K)
+
 
 def by_name(name: str) -> Workload:
-    for w in WORKLOADS:
+    for w in WORKLOADS + VARIANTS:
         if w.name == name:
             return w
     raise KeyError(name)

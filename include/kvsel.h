@@ -51,7 +51,15 @@ typedef enum {
   KVSEL_ERR_DEVICE = 6         /* the device found an index out of range */
 } kvsel_status;
 
-enum { KVSEL_REDUCE_SUM = 0, KVSEL_REDUCE_MAX = 1 };
+/* group_reduce / page_reduce: sum, max, or (group_reduce only) the mean over the G * W rows of a group */
+enum { KVSEL_REDUCE_SUM = 0, KVSEL_REDUCE_MAX = 1, KVSEL_REDUCE_MEAN = 2 };
+/* pool_type: max-pooling or average pooling (the mean over the in-range neighbours) */
+enum { KVSEL_POOL_MAX = 0, KVSEL_POOL_AVG = 1 };
+/* score_mode: post-softmax window probabilities, or the pre-softmax scaled logits */
+enum { KVSEL_SCORE_SOFTMAX = 0, KVSEL_SCORE_LOGITS = 1 };
+/* kvsel_aggregate: what happens across layers and across KV heads */
+enum { KVSEL_LAYERS_EACH = 0, KVSEL_LAYERS_L1_MEAN = 1, KVSEL_LAYERS_MAX = 2 };
+enum { KVSEL_HEADS_EACH = 0, KVSEL_HEADS_SUM = 1 };
 
 #define KVSEL_MAX_BATCH 128
 #define KVSEL_MAX_WINDOW 64
@@ -68,10 +76,12 @@ typedef struct {
   int32_t window;              /* W: 1 .. KVSEL_MAX_WINDOW; (h_q / h_kv) * W <= KVSEL_MAX_ROWS */
   int32_t batch;               /* sequences: 1 .. KVSEL_MAX_BATCH */
   const int64_t* prefix_lens;  /* [host] [batch] prefix lengths L_b >= 1, L_b + W < 2^31 */
-  int32_t group_reduce;        /* KVSEL_REDUCE_SUM or KVSEL_REDUCE_MAX over the query heads of a group */
-  int32_t pool_k;              /* odd max-pool width, 1 (none) .. 63 */
+  int32_t group_reduce;        /* KVSEL_REDUCE_SUM, _MAX or _MEAN over the query heads of a group */
+  int32_t pool_k;              /* odd pool width, 1 (none) .. 63 */
   int32_t page_size;           /* P: 1 = token mode, 2 .. KVSEL_MAX_PAGE = page mode */
   int32_t page_reduce;         /* KVSEL_REDUCE_MAX or KVSEL_REDUCE_SUM over the tokens of a page */
+  int32_t pool_type;           /* KVSEL_POOL_MAX (0) or KVSEL_POOL_AVG */
+  int32_t score_mode;          /* KVSEL_SCORE_SOFTMAX (0) or KVSEL_SCORE_LOGITS */
 } kvsel_desc;
 
 /* Bytes of device workspace the calls below need for this descriptor (any of them). */
@@ -87,10 +97,15 @@ KVSEL_API kvsel_status kvsel_workspace_size(const kvsel_desc* desc, size_t* byte
  * the full row, then the post-softmax mass is summed over the window rows for
  * each prefix column.  The per-head column mass is reduced over the query
  * heads of each GQA group (sum as in CLAA's FastKV-style window scoring,
- * max as in DELTA's head-aware scoring), max-pooled with width pool_k over
- * prefix positions (CLAA, 'Oracle construction': 1-D pooling, kernel 7), and,
- * in page mode, reduced to page scores over P consecutive tokens (DELTA,
- * 'Key designs' 2 and 3).
+ * max as in DELTA's head-aware scoring, or the mean over the group's rows as
+ * LookaheadKV averages its lookahead rows), pooled with width pool_k over
+ * prefix positions (CLAA, 'Oracle construction': 1-D pooling, kernel 7; max
+ * or average, out-of-range neighbours ignored), and, in page mode, reduced to
+ * page scores over P consecutive tokens (DELTA, 'Key designs' 2 and 3).
+ * With score_mode KVSEL_SCORE_LOGITS the softmax is skipped and the scaled
+ * logits are summed instead (CLAA, 'Three representative token-ranking
+ * methods': GemFilter's pre-softmax score of the last prompt token, W = 1);
+ * that mode makes one pass over K instead of two.
  *
  *   q, k         [device] bf16, layouts above; 16-byte aligned
  *   scores       [device] fp32 out: pooled token scores (raw group scores when pool_k == 1)
@@ -107,8 +122,9 @@ KVSEL_API kvsel_status kvsel_score(const kvsel_desc* desc, const void* q, const 
  * Each layer's scores of a (sequence, KV head) row are L1-normalised over the
  * prefix (LookaheadKV, 'KL divergence and ListNet': s / ||s||_1), the mean is
  * taken over layers layer_lo..layer_hi inclusive (CLAA, decision 3: one score
- * per token aggregated over several layers), and the result is max-pooled
- * with desc->pool_k.
+ * per token aggregated over several layers), and the result is pooled with
+ * desc->pool_k / desc->pool_type.  Same as kvsel_aggregate with
+ * KVSEL_LAYERS_L1_MEAN and KVSEL_HEADS_EACH.
  *
  *   scores    [device] fp32 raw group scores (kvsel_score with pool_k = 1), layout above
  *   combined  [device] fp32 out, per sequence b: [h_kv][L_b]
@@ -117,6 +133,47 @@ KVSEL_API kvsel_status kvsel_score(const kvsel_desc* desc, const void* q, const 
 KVSEL_API kvsel_status kvsel_combine_layers(const kvsel_desc* desc, const float* scores,
                                   int32_t layer_lo, int32_t layer_hi, float* combined,
                                   void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * kvsel_aggregate — reduce raw group scores across KV heads and layers, then pool.
+ *
+ * For each sequence, over layers layer_lo..layer_hi (inclusive) of raw group
+ * scores (kvsel_score with pool_k = 1):
+ *   head_op  KVSEL_HEADS_EACH keeps every KV head; KVSEL_HEADS_SUM sums all KV
+ *            heads of a layer (the sum over all attention heads that FastKV,
+ *            CLAA and GemFilter rank with; CLAA, decision 2);
+ *   layer_op KVSEL_LAYERS_EACH keeps every layer of the range;
+ *            KVSEL_LAYERS_L1_MEAN L1-normalises each layer's row over the prefix
+ *            (LookaheadKV, 'KL divergence and ListNet') and averages the range;
+ *            KVSEL_LAYERS_MAX takes the token-wise max over the range (CLAA,
+ *            decision 3, Eq. 6, at the pruning layer);
+ * then pools with desc->pool_k / desc->pool_type.  Token scores only.
+ *
+ *   scores  [device] fp32 raw group scores, per sequence b: [n_layers][h_kv][L_b]
+ *   out     [device] fp32, per sequence b: [n_l][n_h][L_b], n_l = layer_hi - layer_lo + 1
+ *           (EACH) or 1, n_h = h_kv (EACH) or 1; sequences packed in batch order
+ *   ws      [device] workspace (holds the L1 norms)
+ */
+KVSEL_API kvsel_status kvsel_aggregate(const kvsel_desc* desc, const float* scores, int32_t layer_lo,
+                                       int32_t layer_hi, int32_t layer_op, int32_t head_op, float* out,
+                                       void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * kvsel_select — top-k selection over any rows of scores, ties to the lower index.
+ *
+ * As kvsel_topk (below), over `rows` score rows per sequence: per sequence b,
+ * scores [rows][n] with n = L_b (token mode) or ceil(L_b / P) (page mode),
+ * sequences packed in batch order.  With append_window == 0 the window
+ * positions (or window pages) are not appended — for windows whose keys are
+ * not part of the prompt to keep, such as LookaheadKV's lookahead rows,
+ * which take no part in decoding ('Method steps').
+ *
+ *   idx_out  [device] int32 out [batch][rows][n_sel], n_sel = k (+ W with the
+ *            window, token mode) or k + n_recent (+ W / P with the window, page mode)
+ */
+KVSEL_API kvsel_status kvsel_select(const kvsel_desc* desc, const float* scores, int32_t rows, int32_t k,
+                                    int32_t n_recent, int32_t append_window, int32_t* idx_out,
+                                    void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * kvsel_topk — top-k selection per (sequence, layer, KV head) row, ties to the lower index.
@@ -160,6 +217,25 @@ KVSEL_API kvsel_status kvsel_topk(const kvsel_desc* desc, const float* scores, i
 KVSEL_API kvsel_status kvsel_compact(const kvsel_desc* desc, const void* k, const void* v,
                            const int32_t* idx, int32_t idx_layers, int32_t n_sel,
                            void* k_out, void* v_out, void* ws, cudaStream_t stream);
+
+/*
+ * kvsel_compact_layers — kvsel_compact over a range of layers, with selections shared by heads.
+ *
+ * Compacts layers layer_lo .. layer_lo + n_layers_out - 1 of the caches (CLAA,
+ * 'Three design decisions', decision 1: the first m layers keep their full
+ * cache and are not compacted).  idx is [batch][idx_layers][idx_heads][n_sel]:
+ * idx_layers == 1 applies one selection to every compacted layer, otherwise
+ * idx_layers == n_layers_out and row i serves layer layer_lo + i; idx_heads == 1
+ * applies one selection to every KV head (the all-head scores of CLAA,
+ * FastKV and GemFilter rank tokens once per layer), otherwise idx_heads == h_kv.
+ *
+ *   k_out, v_out  [device] bf16 out [batch][n_layers_out][h_kv][n_sel * P][d]
+ *   ws            [device] workspace or NULL (errors as for kvsel_compact)
+ */
+KVSEL_API kvsel_status kvsel_compact_layers(const kvsel_desc* desc, const void* k, const void* v,
+                                            const int32_t* idx, int32_t idx_layers, int32_t idx_heads,
+                                            int32_t layer_lo, int32_t n_layers_out, int32_t n_sel,
+                                            void* k_out, void* v_out, void* ws, cudaStream_t stream);
 
 /*
  * kvsel_pagetable — per-group KV block table from a 2-D block mask.

@@ -362,32 +362,41 @@ def run_sequence(w, q, k, v=None, with_gather: bool = True, layers=None):
     Workload fields).  q [n_layers, H_q, W, d], k/v [n_layers, H_kv, L+W, d].
 
     Returns a dict: 'raw' [n_layers, H_kv, L] group scores, 'pooled' (per layer
-    or, with a layer range, [H_kv, L] after the cross-layer mean), 'pages'
-    [.., n_pages] in page mode, 'idx' selected positions (or pages), and, with
+    or, with a layer range, [H_kv, L] after the cross-layer mean; with all-head
+    selection [n_layers, L] after the sum over KV heads), 'pages' [.., n_pages]
+    in page mode, 'idx' selected positions (or pages), and, with
     ``with_gather``, 'k_c' / 'v_c' compacted rows.
     """
     L = int(k.shape[2]) - w.window
     W, G, Hkv = w.window, w.h_q // w.h_kv, w.h_kv
+    Wapp = W if getattr(w, "append_window", True) else 0
+    softmax = getattr(w, "score_mode", "softmax") == "softmax"
+    kind = getattr(w, "pool_type", "max")
+    all_heads = getattr(w, "head_reduce", "group") == "all"
     layers = range(w.n_layers) if layers is None else layers
-    raw = np.stack([np.stack([score_unit(q[l], k[l], g, G, L, w.group_reduce) for g in range(Hkv)])
+    raw = np.stack([np.stack([score_unit(q[l], k[l], g, G, L, w.group_reduce, softmax) for g in range(Hkv)])
                     for l in layers])
     out = {"raw": raw}
-    if w.layer_range is not None:
+    if all_heads:
+        u = pool(head_sum(raw), w.pool_k, kind)                  # [layers, L]
+        out["pooled"] = u
+        out["idx"] = np.stack([select_tokens(u[i], w.k_keep, L, Wapp) for i in range(u.shape[0])])
+    elif w.layer_range is not None:
         lo, hi = w.layer_range
         s = cross_layer_mean(raw, lo, hi)                       # [H_kv, L]
-        u = max_pool(s, w.pool_k)
-        idx = np.stack([select_tokens(u[g], w.k_keep, L, W) for g in range(Hkv)])
+        u = pool(s, w.pool_k, kind)
+        idx = np.stack([select_tokens(u[g], w.k_keep, L, Wapp) for g in range(Hkv)])
         out.update(combined=s, pooled=u, idx=idx)
     else:
-        u = max_pool(raw, w.pool_k)                              # [layers, H_kv, L]
+        u = pool(raw, w.pool_k, kind)                            # [layers, H_kv, L]
         out["pooled"] = u
         if w.page_size == 1:
-            idx = np.stack([np.stack([select_tokens(u[i, g], w.k_keep, L, W) for g in range(Hkv)])
+            idx = np.stack([np.stack([select_tokens(u[i, g], w.k_keep, L, Wapp) for g in range(Hkv)])
                             for i in range(u.shape[0])])
         else:
             U = page_reduce(u, w.page_size, w.page_reduce)
             out["pages"] = U
-            idx = np.stack([np.stack([select_pages(U[i, g], w.k_keep, w.n_recent, L, W, w.page_size)
+            idx = np.stack([np.stack([select_pages(U[i, g], w.k_keep, w.n_recent, L, Wapp, w.page_size)
                                       for g in range(Hkv)]) for i in range(u.shape[0])])
         out["idx"] = idx
     if with_gather and v is not None:
@@ -396,7 +405,12 @@ def run_sequence(w, q, k, v=None, with_gather: bool = True, layers=None):
         for i, l in enumerate(layers):
             kl, vl = [], []
             for g in range(Hkv):
-                ii = out["idx"][g] if w.layer_range is not None else out["idx"][i, g]
+                if all_heads:
+                    ii = out["idx"][i]
+                elif w.layer_range is not None:
+                    ii = out["idx"][g]
+                else:
+                    ii = out["idx"][i, g]
                 kl.append(gather_rows(_f64(k[l, g]), ii, P))
                 vl.append(gather_rows(_f64(v[l, g]), ii, P))
             kc.append(np.stack(kl)); vc.append(np.stack(vl))

@@ -1,6 +1,10 @@
 """Comparison rules between the CUDA path and the fp64 oracle.
 
 * fp32 scores: |gpu - oracle| <= 1e-3 * |oracle| + 1e-6 element by element.
+  Pre-softmax (logit) scores are signed sums that can cancel to near zero, so
+  their absolute term scales with the row: 1e-4 * RMS of the oracle row.  (The
+  fp32 accumulation of one 128-term bf16 dot product is off by about
+  sqrt(d) * 2^-24 * sum |q_i k_i| ~ 1e-6 of a logit of order one.)
 * Selected sets: equal, except that an index may be swapped for another when
   the oracle score of each lies within 1e-5 (relative) of the oracle's k-th
   score — a near tie that fp32 and fp64 may order differently.  The appended
@@ -17,11 +21,16 @@ import torch
 RTOL, ATOL, TIE_RTOL = 1e-3, 1e-6, 1e-5
 
 
-def assert_scores_close(gpu, ref, what="scores"):
+LOGIT_ATOL_RMS = 1e-4
+
+
+def assert_scores_close(gpu, ref, what="scores", signed=False):
+    """signed=True for pre-softmax (logit) scores: the absolute term is 1e-4 * RMS of each last-axis row."""
     g = gpu.detach().float().cpu().double().numpy() if hasattr(gpu, "detach") else np.asarray(gpu, np.float64)
     r = np.asarray(ref, np.float64)
     assert g.shape == r.shape, (what, g.shape, r.shape)
-    bad = np.abs(g - r) > RTOL * np.abs(r) + ATOL
+    atol = LOGIT_ATOL_RMS * np.sqrt((r * r).mean(axis=-1, keepdims=True)) if signed else ATOL
+    bad = np.abs(g - r) > RTOL * np.abs(r) + atol
     if bad.any():
         i = np.argwhere(bad)[0]
         raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside tolerance; first at {tuple(i)}: "

@@ -58,7 +58,10 @@ def test_workspace_size_grows_with_length():
     (dict(prefix_lens=[0]), K.ERR_INVALID_ARG),
     (dict(prefix_lens=[2 ** 31]), K.ERR_INVALID_ARG),
     (dict(prefix_lens=[10] * 129), K.ERR_INVALID_ARG),
-    (dict(group_reduce=2), K.ERR_INVALID_ARG),
+    (dict(group_reduce=3), K.ERR_INVALID_ARG),
+    (dict(pool_type=2), K.ERR_INVALID_ARG),
+    (dict(score_mode=2), K.ERR_INVALID_ARG),
+    (dict(page_reduce=2), K.ERR_INVALID_ARG),
 ])
 def test_bad_descriptor_rejected(kw, status):
     d = _desc(**kw)
@@ -98,3 +101,28 @@ def test_selection_arguments_rejected():
     assert K.raw_call("kvsel_combine_layers", ctypes.byref(d), 16, 1, 2, 16, 256, big, None) == K.ERR_INVALID_ARG
     assert K.raw_call("kvsel_selftest_bounded_wait", None, 10, 0, None) == K.ERR_WORKSPACE
     assert K.raw_call("kvsel_selftest_bounded_wait", 256, 0, 0, None) == K.ERR_INVALID_ARG
+
+
+def test_new_entry_arguments_rejected():
+    """kvsel_aggregate / kvsel_select / kvsel_compact_layers check their arguments before any launch."""
+    d = _desc(prefix_lens=[100])
+    big = 1 << 40
+    agg = lambda lo, hi, lop, hop: K.raw_call("kvsel_aggregate", ctypes.byref(d), 16, lo, hi, lop, hop, 16, 256,
+                                              big, None)
+    assert agg(0, 2, K.LAYERS_MAX, K.HEADS_SUM) == K.ERR_INVALID_ARG        # layer beyond n_layers
+    assert agg(1, 0, K.LAYERS_MAX, K.HEADS_SUM) == K.ERR_INVALID_ARG        # empty range
+    assert agg(0, 1, 3, K.HEADS_SUM) == K.ERR_INVALID_ARG
+    assert agg(0, 1, K.LAYERS_EACH, 2) == K.ERR_INVALID_ARG
+    assert K.raw_call("kvsel_aggregate", ctypes.byref(d), None, 0, 1, 0, 0, 16, 256, big, None) == K.ERR_INVALID_ARG
+    sel = lambda rows, k, nr, app: K.raw_call("kvsel_select", ctypes.byref(d), 16, rows, k, nr, app, 16, 256, big,
+                                              None)
+    assert sel(0, 5, 0, 1) == K.ERR_INVALID_ARG
+    assert sel(3, 101, 0, 0) == K.ERR_INVALID_ARG
+    assert sel(3, 5, 1, 1) == K.ERR_INVALID_ARG                             # recency is a page-mode option
+    cl = lambda il, ih, lo, n: K.raw_call("kvsel_compact_layers", ctypes.byref(d), 16, 16, 16, il, ih, lo, n, 10,
+                                          16, 16, None, None)
+    assert cl(1, 1, 1, 2) == K.ERR_INVALID_ARG                              # layers 1..2 of 2
+    assert cl(2, 1, 1, 1) == K.ERR_INVALID_ARG                              # idx rows != compacted layers
+    assert cl(1, 3, 0, 2) == K.ERR_INVALID_ARG                              # idx heads neither 1 nor h_kv
+    assert K.raw_call("kvsel_compact_layers", ctypes.byref(d), 16, 16, 16, 1, 1, 0, 2, 10, 8, 16, None,
+                      None) == K.ERR_INVALID_ARG                            # misaligned output
