@@ -51,18 +51,34 @@ def parse():
 # ----------------------------------------------------------------------------- oracle (CPU) leg
 
 def _oracle_unit(args):
-    """The oracle's whole path for one (layer, KV head) unit; returns seconds spent."""
+    """The oracle's whole path for one unit; returns seconds spent.
+
+    A unit is one (layer, KV head) — or, for selections shared by every KV head,
+    one layer with all its KV heads (q_group [h_kv, G, W, d], k_unit / v_unit
+    [h_kv, L + W, d]).
+    """
     wd, q_group, k_unit, v_unit = args
+    import numpy as np
     from oracle import kvsel_oracle as O
     t0 = time.perf_counter()
     L, W, P = wd["L"], wd["W"], wd["P"]
-    s = O.group_scores(O._f64(q_group), O._f64(k_unit), L, wd["reduce"])
-    u = O.max_pool(s, wd["pool_k"])
+    Wapp = W if wd["append"] else 0
+    if wd["all_heads"]:
+        raw = [O.group_scores(O._f64(q_group[g]), O._f64(k_unit[g]), L, wd["reduce"], wd["softmax"])
+               for g in range(len(q_group))]
+        u = O.pool(O.head_sum(np.stack(raw)), wd["pool_k"], wd["pool_type"])
+        sel = O.select_tokens(u, wd["k"], L, Wapp)
+        for g in range(len(q_group)):
+            O.gather_rows(O._f64(k_unit[g]), sel, P)
+            O.gather_rows(O._f64(v_unit[g]), sel, P)
+        return time.perf_counter() - t0
+    s = O.group_scores(O._f64(q_group), O._f64(k_unit), L, wd["reduce"], wd["softmax"])
+    u = O.pool(s, wd["pool_k"], wd["pool_type"])
     if P > 1:
         U = O.page_reduce(u, P, wd["page_reduce"])
-        sel = O.select_pages(U, wd["k"], wd["n_recent"], L, W, P)
+        sel = O.select_pages(U, wd["k"], wd["n_recent"], L, Wapp, P)
     else:
-        sel = O.select_tokens(u, wd["k"], L, W)
+        sel = O.select_tokens(u, wd["k"], L, Wapp)
     O.gather_rows(O._f64(k_unit), sel, P)
     O.gather_rows(O._f64(v_unit), sel, P)
     return time.perf_counter() - t0
@@ -73,15 +89,47 @@ def _pool_init():
     os.environ["OMP_NUM_THREADS"] = "1"
 
 
+def _all_heads(w):
+    return w.head_reduce == "all" or w.claa is not None
+
+
+def _k_keep(w):
+    return keep_count(w.claa[3], w.prefix_lens[0]) if w.claa is not None else w.k_keep
+
+
+def keep_count(rate, L):
+    from attention_kv_cache_gb300.pipeline import keep_count as kc
+    return kc(rate, L)
+
+
 def oracle_rate(w, units, pool, cores):
     """Prefix tokens per second per layer of the oracle over ``units`` = [(q_group, k_unit, v_unit)]."""
     wd = dict(L=w.prefix_lens[0], W=w.window, P=w.page_size, G=w.group, h_kv=w.h_kv, reduce=w.group_reduce,
-              pool_k=w.pool_k, page_reduce=w.page_reduce, k=w.k_keep, n_recent=w.n_recent)
+              pool_k=w.pool_k, page_reduce=w.page_reduce, k=_k_keep(w), n_recent=w.n_recent,
+              softmax=w.score_mode == "softmax", pool_type=w.pool_type, append=w.append_window,
+              all_heads=_all_heads(w))
     t0 = time.perf_counter()
     pool.map(_oracle_unit, [(wd, q, k, v) for (q, k, v) in units], chunksize=1)
     wall = time.perf_counter() - t0
-    tokens_layers = len(units) / w.h_kv * w.prefix_lens[0]
+    per_unit_layers = 1.0 if _all_heads(w) else 1.0 / w.h_kv
+    tokens_layers = len(units) * per_unit_layers * w.prefix_lens[0]
     return tokens_layers / wall, wall
+
+
+def oracle_units(w, q, kk, vv, layers, count):
+    """``count`` oracle units cycled over ``layers`` (per-sequence q [n_layers, ...], kk / vv per layer)."""
+    G = w.group
+    units = []
+    for i in range(count):
+        if _all_heads(w):
+            layer = layers[i % len(layers)]
+            qg = q[layer].reshape(w.h_kv, G, w.window, w.head_dim)
+            units.append((qg.cpu(), kk(layer).cpu(), vv(layer).cpu()))
+        else:
+            layer, g = divmod(i, w.h_kv)
+            layer = layers[layer % len(layers)]
+            units.append((q[layer, g * G:(g + 1) * G].cpu(), kk(layer)[g].cpu(), vv(layer)[g].cpu()))
+    return units
 
 
 def make_pool(cores):
@@ -146,19 +194,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def kernel_bytes(w, n_sel_rows):
-    """Algorithmic HBM bytes of one launch of each kernel (the whole workload per launch)."""
+def kernel_bytes(w, n_sel_rows, n_layers=None):
+    """Algorithmic HBM bytes of one launch of each kernel (the whole workload per launch); n_layers = the
+    layers one launch covers (default: all of the workload's)."""
     d, W = w.head_dim, w.window
-    units = [(w.n_layers * w.h_kv, L) for L in w.prefix_lens]
-    q_bytes = w.batch * w.n_layers * w.h_q * W * d * 2
+    nl = w.n_layers if n_layers is None else n_layers
+    units = [(nl * w.h_kv, L) for L in w.prefix_lens]
+    q_bytes = w.batch * nl * w.h_q * W * d * 2
     k_all = sum(u * (L + W) * d * 2 for u, L in units)
     k_prefix = sum(u * L * d * 2 for u, L in units)
     score_w = sum(u * L * 4 for u, L in units)
     P = w.page_size
     page_w = sum(u * (-(-L // P)) * 4 for u, L in units) if P > 1 else 0
     sel_read = page_w if P > 1 else score_w
-    idx_w = w.batch * w.n_layers * w.h_kv * w.n_sel() * 4
-    gather = 2 * 2 * w.batch * w.n_layers * w.h_kv * n_sel_rows * d * 2
+    idx_w = w.batch * nl * w.h_kv * w.n_sel() * 4
+    gather = 2 * 2 * w.batch * nl * w.h_kv * n_sel_rows * d * 2
     pass1 = k_all + q_bytes
     pass2 = k_prefix + q_bytes + score_w + page_w
     return {
@@ -222,12 +272,15 @@ def run_kvsel(args):
     import torch
     from attention_kv_cache_gb300 import kvsel as K
     from attention_kv_cache_gb300 import synth as S
-    from attention_kv_cache_gb300.pipeline import Pipeline, pack
+    from attention_kv_cache_gb300.pipeline import ClaaPipeline, Pipeline, pack
 
     rank, world, local = dist_setup()
     w = S.by_name(args.workload)
     if args.layers:
         w = w.with_(n_layers=args.layers)
+        if w.claa is not None:
+            m, lp, nbuf, rate = w.claa
+            w = w.with_(claa=(min(m, args.layers - 1), args.layers - 1, nbuf, rate))
     n_cpu_units = args.cpu_units or (os.cpu_count() or 1)
     cores = min(os.cpu_count() or 1, n_cpu_units)
     pool = make_pool(cores) if (rank == 0 and world == 1 and not args.no_cpu) else None  # before any GPU call
@@ -238,11 +291,19 @@ def run_kvsel(args):
     q, k, v = pack(inp, dev)
     mask = inp.mask
     nkv = inp.n_kvblk
-    pipe = Pipeline(w, dev)
+    claa = w.claa is not None
+    pipe = ClaaPipeline(w, dev) if claa else Pipeline(w, dev)
     stream = torch.cuda.current_stream(dev)
+    scored_layers = pipe.n_sc if claa else w.n_layers
+
+    def run_step():
+        if claa:
+            pipe.run(q, k, v)
+        else:
+            pipe.run(q, k, v, mask, nkv)
 
     for _ in range(args.warmup):
-        pipe.run(q, k, v, mask, nkv)
+        run_step()
     torch.cuda.synchronize()
     assert K.kvsel_read_device_error(pipe.ws) == K.OK
 
@@ -256,7 +317,7 @@ def run_kvsel(args):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        pipe.run(q, k, v, mask, nkv)
+        run_step()
     e1.record(stream)
     torch.cuda.synchronize()
     launches = K.kvsel_launch_count() - n0
@@ -267,12 +328,12 @@ def run_kvsel(args):
     ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     assert K.kvsel_read_device_error(pipe.ws) == K.OK
 
-    tokens_per_step = sum(L for L in w.prefix_lens) * w.n_layers
+    tokens_per_step = sum(L for L in w.prefix_lens) * scored_layers
     value = world * tokens_per_step * args.steps / (ms / 1e3)
 
     # ---- roofline of the dominant kernel (largest share of the timed region)
     name, (n_launch, k_ms) = max(trace.items(), key=lambda kv: kv[1][1])
-    bytes_per_launch = kernel_bytes(w, pipe.n_sel * w.page_size).get(name)
+    bytes_per_launch = kernel_bytes(w, pipe.n_sel * w.page_size, scored_layers).get(name)
     peak, peak_src = measured_peaks()
     roof = None
     if bytes_per_launch is not None:
@@ -291,6 +352,8 @@ def run_kvsel(args):
         vh = torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
         vh.copy_(v)
         outs = [pipe.idx, pipe.k_out, pipe.v_out] + ([pipe.kv_indptr, pipe.kv_indices] if mask is not None else [])
+        if claa:
+            outs.append(pipe.prune_idx)
         outs_h = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
         mask_h = mask.cpu().pin_memory() if mask is not None else None
 
@@ -300,7 +363,7 @@ def run_kvsel(args):
             v.copy_(vh, non_blocking=True)
             if mask is not None:
                 mask.copy_(mask_h, non_blocking=True)
-            pipe.run(q, k, v, mask, nkv)
+            run_step()
             for o, oh in zip(outs, outs_h):
                 oh.copy_(o, non_blocking=True)
 
@@ -321,26 +384,25 @@ def run_kvsel(args):
     # ---- CPU baseline: the oracle on a bounded sample of the same workload (rank 0, N = 1)
     cpu = None
     if pool is not None:
-        units = []
-        G = w.group
-        for i in range(n_cpu_units):
-            layer, g = divmod(i, w.h_kv)
-            layer %= w.n_layers
-            units.append((inp.q[0][layer, g * G:(g + 1) * G].cpu(), inp.k[0][layer, g].cpu(), inp.v[0][layer, g].cpu()))
+        layers = list(range(pipe.m, pipe.lp + 1)) if claa else list(range(w.n_layers))
+        units = oracle_units(w, inp.q[0], lambda l: inp.k[0][l], lambda l: inp.v[0][l], layers, n_cpu_units)
         rate, wall = oracle_rate(w, units, pool, cores)
+        what = "layers (all KV heads)" if _all_heads(w) else "(layer, KV head) units"
         cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": f"{len(units)} (layer, KV head) units of the same workload ({len(units) / w.h_kv:g} layers), "
-                         f"full path per unit, {wall:.1f} s wall on {cores} worker processes (1 BLAS thread each)"}
+               "sample": f"{len(units)} {what} of the same workload, full path per unit, "
+                         f"{wall:.1f} s wall on {cores} worker processes (1 BLAS thread each)"}
         pool.close()
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "metric": metric_for(w), "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16 inputs, f32 arithmetic", "data": "synthetic",
             "config": {"workload": w.name, "layers": w.n_layers, "h_q": w.h_q, "h_kv": w.h_kv, "d": w.head_dim,
                        "prefix_len": list(w.prefix_lens), "window": w.window, "group_reduce": w.group_reduce,
-                       "pool_k": w.pool_k, "page_size": w.page_size, "k_keep": w.k_keep, "n_recent": w.n_recent,
+                       "pool_k": w.pool_k, "pool_type": w.pool_type, "score_mode": w.score_mode,
+                       "head_reduce": w.head_reduce, "claa": w.claa, "scored_layers": scored_layers,
+                       "page_size": w.page_size, "k_keep": _k_keep(w), "n_recent": w.n_recent,
                        "l2": "inputs exceed L2 (K+V %.1f GB per step)" % ((k.numel() + v.numel()) * 2 / 1e9),
                        "parallelism": f"replicas x{world}"},
             "clocks": clocks, "gpu_launches": launches, "kernels": {n: {"launches": c, "ms": round(t, 3)}
@@ -351,6 +413,12 @@ def run_kvsel(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def metric_for(w):
+    if w.name == DEFAULT_WORKLOAD:
+        return METRIC
+    return f"prefix tokens scored+selected/s (per layer, {w.prefix_lens[0] // 1024}K ctx, {w.name})"
 
 
 # ----------------------------------------------------------------------------- the oracle arm
@@ -366,21 +434,21 @@ def run_reference(args):
     cores = min(os.cpu_count() or 1, max(1, args.steps))
     pool = make_pool(cores)
     q = S.make_queries(w, 0, "cpu")
-    kk, vv, _ = S.make_layer(w, 0, 0, q, "cpu")
-    G = w.group
-    units = [(q[0, g * G:(g + 1) * G], kk[g], vv[g]) for g in range(w.h_kv)]
+    layer0 = w.claa[0] if w.claa is not None else 0
+    kk, vv, _ = S.make_layer(w, 0, layer0, q, "cpu")
+    units = oracle_units(w, q, lambda l: kk, lambda l: vv, [layer0], max(args.steps, args.warmup, 1))
     if args.warmup > 0:
-        oracle_rate(w, [units[i % len(units)] for i in range(min(args.warmup, cores))], pool, cores)
-    value, wall = oracle_rate(w, [units[i % len(units)] for i in range(args.steps)], pool, cores)
+        oracle_rate(w, units[:min(args.warmup, cores)], pool, cores)
+    value, wall = oracle_rate(w, units[:args.steps], pool, cores)
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 0,
+        "impl": "reference", "metric": metric_for(w), "value": value, "unit": "tokens/s", "n_gpus": 0,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / max(1, args.steps),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name,
                    "sample_per_step": "one (layer, KV head) unit: scores, pooling, page scores, selection, gather"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{args.steps} units of layer 0 (cycled over its {w.h_kv} KV heads), "
-                                   f"{wall:.1f} s wall on {cores} worker processes"},
+                         "sample": f"{args.steps} units of layer {layer0} (cycled over its {w.h_kv} KV heads, or the "
+                                   f"whole layer for all-head selection), {wall:.1f} s wall on {cores} worker processes"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     pool.close()
