@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
                                                             const __grid_constant__ SeqTable t) {
   extern __shared__ __align__(16) uint32_t keys_sm[];
   __shared__ uint32_t hist[256];
+  __shared__ uint32_t hist_w[kTopkThreads / 32][256];   // one histogram per warp: no cross-warp atomics
   __shared__ unsigned long long scan_sh[32];
   __shared__ uint32_t sel_digit, sel_gt;
 
@@ -85,8 +86,9 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
   if (a.k > 0) {
     for (int pass = 0; pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
-      if (tid < 256) hist[tid] = 0;
-      __syncthreads();
+      uint32_t* hw = hist_w[tid >> 5];
+      for (int j = tid & 31; j < 256; j += 32) hw[j] = 0;
+      __syncwarp();
       for (int base = 0; base < n_cand; base += kTopkThreads) {
         const int i = base + tid;
         uint32_t key = 0;
@@ -99,8 +101,15 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
         if (ok) {
           const uint32_t digit = (key >> shift) & 255u;
           const unsigned peers = __match_any_sync(m, digit);
-          if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(peers));
+          if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hw[digit], (uint32_t)__popc(peers));
         }
+      }
+      __syncthreads();
+      if (tid < 256) {
+        uint32_t c = 0;
+#pragma unroll 8
+        for (int w = 0; w < kTopkThreads / 32; ++w) c += hist_w[w][tid];
+        hist[tid] = c;
       }
       __syncthreads();
       // digits from the top: count of candidates whose digit is above d
@@ -118,29 +127,25 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
       krem -= sel_gt;
       __syncthreads();
     }
-    // ordered emission: every key > T, then the first krem keys == T
+    // ordered emission: every key > T and the first krem keys == T, in index order.  Rounds of one key
+    // per thread (consecutive threads, consecutive keys); a block scan gives each selected key the
+    // number of selected keys before it: (keys > T before it) + min(keys == T before it, krem).
     const uint32_t T = prefix;
-    const int chunk = (n_cand + kTopkThreads - 1) / kTopkThreads;
-    const int beg = min(n_cand, tid * chunk), end = min(n_cand, beg + chunk);
-    uint32_t gt = 0, eq = 0;
-    for (int i = beg; i < end; ++i) {
-      const uint32_t key = key_at(i);
-      gt += key > T;
-      eq += key == T;
-    }
-    unsigned long long tot;
-    const unsigned long long pre = block_scan_u64(((unsigned long long)gt << 32) | eq, scan_sh, &tot);
-    const uint32_t gt_before = (uint32_t)(pre >> 32), eq_before = (uint32_t)(pre & 0xffffffffu);
-    uint32_t pos = gt_before + min(eq_before, krem);
-    uint32_t eq_seen = eq_before;
-    for (int i = beg; i < end; ++i) {
-      const uint32_t key = key_at(i);
-      if (key > T) {
-        out[pos++] = i;
-      } else if (key == T) {
-        if (eq_seen < krem) out[pos++] = i;
-        ++eq_seen;
-      }
+    uint32_t gt_run = 0, eq_run = 0;
+    for (int base = 0; base < n_cand; base += kTopkThreads) {
+      const int i = base + tid;
+      const uint32_t key = i < n_cand ? key_at(i) : 0u;
+      const bool is_gt = i < n_cand && key > T;
+      const bool is_eq = i < n_cand && key == T;
+      unsigned long long tot;
+      const unsigned long long pre =
+          block_scan_u64(((unsigned long long)is_gt << 32) | (unsigned long long)is_eq, scan_sh, &tot);
+      const uint32_t gt_before = gt_run + (uint32_t)(pre >> 32);
+      const uint32_t eq_before = eq_run + (uint32_t)(pre & 0xffffffffu);
+      if (is_gt) out[gt_before + min(eq_before, krem)] = i;
+      else if (is_eq && eq_before < krem) out[gt_before + eq_before] = i;
+      gt_run += (uint32_t)(tot >> 32);
+      eq_run += (uint32_t)(tot & 0xffffffffu);
     }
   }
   // recency pages, then (when appended) window pages or window tokens: the indices from n_cand on
