@@ -39,6 +39,10 @@ Sources (page title, then the section / equation the step follows):
   with kernel 7 for every method.
 * LookaheadKV, 'Method steps': the lookahead rows' attention to the prompt is
   averaged, pooled, and the top K kept.
+* CompactAttention, 'Method steps' (3): the selected KV blocks are read in
+  place by a paged dense-attention kernel through kv_indptr / kv_indices;
+  DELTA, 'Overall framework': sparse layers attend only over the selected page
+  set.  The attention itself is softmax(q K^T / sqrt(d)) V over those rows.
 
 Readings taken where the pages are silent or garbled (each is also listed in
 the design notes):
@@ -67,6 +71,10 @@ the design notes):
   group's window rows and heads).
 * A keep rate r maps to k = floor(r * L + 1/2) prefix tokens (round half up),
   clipped to [0, L]; the observation window is appended as in token mode.
+* Attention over a page / block table: a query row attends to every row of
+  every listed block (block b covers rows bP .. bP + P - 1, rows past the
+  cache's end do not exist), with no causal mask (decode-style queries come
+  after every selected key).
 * CLAA over an offline prompt: layers m .. l_p are scored with the window
   (sum over window rows and all heads, softmax), each layer's pooled scores give
   its own top-k, and the token-wise max over the last n buffered layers (up to
@@ -287,6 +295,23 @@ def gather_rows(x: np.ndarray, idx: np.ndarray, page_size: int = 1) -> np.ndarra
     ok = rows < x.shape[0]
     out[ok] = x[rows[ok]]
     return out
+
+
+# --------------------------------------------------------------------------- attention over a table
+
+def table_rows(blocks: np.ndarray, P: int, n_rows: int) -> np.ndarray:
+    """Cache rows named by a block list: rows bP .. bP + P - 1 of each block b, in list order, < n_rows."""
+    rows = (np.asarray(blocks, np.int64)[:, None] * P + np.arange(P)[None, :]).reshape(-1)
+    return rows[rows < n_rows]
+
+
+def attend(q: np.ndarray, k: np.ndarray, v: np.ndarray, rows: np.ndarray) -> np.ndarray:
+    """o[r] = softmax_t(<q_r, k_t> / sqrt(d)) v_t over the given cache rows t.  q [R, d] -> [R, d]."""
+    z = window_logits(q, k[rows])
+    z = z - z.max(axis=-1, keepdims=True)
+    p = np.exp(z)
+    p /= p.sum(axis=-1, keepdims=True)
+    return p @ v[rows]
 
 
 # --------------------------------------------------------------------------- block union

@@ -417,6 +417,31 @@ def check_claa_max_buffer(o):
     assert o.claa_sequence(q, k, L, W, G, Hkv, 5, 6, 4, keep_rate=0.1)["buffer"] == (5, 6)
 
 
+# --------------------------------------------------------------------------- attention over a table
+
+def check_table_attention_sdpa(o):
+    """Attention over table rows equals torch SDPA on the gathered rows (scale, softmax, weighted V);
+    identical keys give the plain mean of the V rows; block rows past the cache end do not exist."""
+    rng = _rng(18)
+    N, d, R, P = 70, 16, 5, 8
+    k = _bf16_values(rng.standard_normal((N, d)) * 1.3)
+    v = _bf16_values(rng.standard_normal((N, d)))
+    q = _bf16_values(rng.standard_normal((R, d)))
+    blocks = np.array([8, 0, 3, 5])                     # block 8 covers rows 64..71: only 64..69 exist
+    rows = o.table_rows(blocks, P, N)
+    assert list(rows) == list(range(64, 70)) + list(range(0, 8)) + list(range(24, 32)) + list(range(40, 48))
+    got = o.attend(q, k, v, rows)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[None, None], torch.from_numpy(k[rows])[None, None], torch.from_numpy(v[rows])[None, None]
+    )[0, 0].numpy()
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+    same = np.repeat(k[:1], N, axis=0)
+    np.testing.assert_allclose(o.attend(q, same, v, rows), np.repeat(v[rows].mean(axis=0, keepdims=True), R, 0),
+                               rtol=1e-12)
+    # the row order of the table does not matter
+    np.testing.assert_allclose(o.attend(q, k, v, rows[::-1].copy()), got, rtol=1e-12)
+
+
 ALL_CHECKS = [
     check_probs_match_sdpa,
     check_row_mass_invariant,
@@ -436,4 +461,5 @@ ALL_CHECKS = [
     check_avg_pool_definition,
     check_layer_max_and_keep_count,
     check_claa_max_buffer,
+    check_table_attention_sdpa,
 ]

@@ -195,13 +195,28 @@ def _claa_buffer_short(o):
     o.claa_sequence = claa_sequence
 
 
+def _attend_no_scale(o):
+    def attend(q, k, v, rows):
+        z = q @ k[rows].T
+        p = np.exp(z - z.max(axis=-1, keepdims=True))
+        return (p / p.sum(axis=-1, keepdims=True)) @ v[rows]
+    o.attend = attend
+
+
+def _table_rows_off_by_one(o):
+    def table_rows(blocks, P, n_rows):
+        rows = (np.asarray(blocks, np.int64)[:, None] * P + np.arange(1, P + 1)[None, :]).reshape(-1)
+        return rows[rows < n_rows]
+    o.table_rows = table_rows
+
+
 MUTANTS = [_no_scale, _mask_off_by_one, _prefix_only_softmax, _mass_max_over_rows,
            _mass_includes_window_shift, _wrong_group_map, _reduce_swapped, _transposed_rows,
            _pool_radius, _pool_one_sided, _page_sum_for_max, _tie_to_higher, _rank_ascending,
            _recency_off_by_one, _no_l1, _layer_range_exclusive, _union_wrong_group,
            _union_first_qblock_only, _gather_page_offset, _logits_unscaled, _logits_include_window_key,
            _mean_over_heads_only, _head_sum_is_max, _avg_pool_counts_padding, _layer_max_is_mean,
-           _keep_count_floor, _claa_buffer_short]
+           _keep_count_floor, _claa_buffer_short, _attend_no_scale, _table_rows_off_by_one]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda m: m.__name__.strip("_"))
