@@ -126,6 +126,12 @@ kvsel_status launch_compact(const kvsel_desc& desc, const SeqTable& t, const voi
                             const int32_t* idx, int idx_layers, int idx_heads, int layer_lo, int n_layers_out,
                             int n_sel, void* k_out, void* v_out, DeviceError* err, cudaStream_t s);
 
+// Attention over a page / block table (attend.cu).
+int64_t attend_splits(int64_t rows, int64_t max_rows_per_list, int R);   // R = query rows per table row
+kvsel_status launch_attend(const kvsel_desc& d, const SeqTable& t, const void* q, int n_q, const void* k,
+                           const void* v, const int32_t* indptr, const int32_t* indices, int n_per_row, int P,
+                           int64_t S, float* part, float* o, DeviceError* err, cudaStream_t s);
+
 kvsel_status launch_pagetable(const kvsel_desc& desc, const SeqTable& t, const uint8_t* mask,
                               int n_qblk, int n_kvblk_max, int32_t* counts, int32_t* kv_indptr,
                               int32_t* kv_indices, cudaStream_t s);

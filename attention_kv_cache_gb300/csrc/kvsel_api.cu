@@ -1,5 +1,6 @@
 // C ABI of libkvsel: argument checks, workspace layout, per-call sequence tables,
 // tracing, and the order of kernel launches for each entry point.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
@@ -64,9 +65,26 @@ TraceScope::~TraceScope() {
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+// Raises a kernel's dynamic shared-memory limit to `bytes` when a launch needs more than it was
+// last given.  The default limit counts static and dynamic shared memory together against 48 KB,
+// so a kernel with a large static footprint needs the attribute for small dynamic sizes too; the
+// attribute is per device, so the cache is too.
 cudaError_t set_smem(const void* func, size_t bytes) {
-  if (bytes <= 48 * 1024) return cudaSuccess;
-  return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  static std::mutex mu;
+  static std::vector<std::pair<std::pair<int, const void*>, size_t>> given;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(mu);
+  for (auto& e : given)
+    if (e.first.first == dev && e.first.second == func) {
+      if (e.second >= bytes) return cudaSuccess;
+      const cudaError_t st = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+      if (st == cudaSuccess) e.second = bytes;
+      return st;
+    }
+  const cudaError_t st = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (st == cudaSuccess) given.push_back({{dev, func}, bytes});
+  return st;
 }
 
 // ----------------------------------------------------------------------------- geometry
@@ -350,6 +368,51 @@ kvsel_status kvsel_compact_layers(const kvsel_desc* desc, const void* k, const v
   SeqTable t = make_table(d, d.n_layers);
   return launch_compact(d, t, k, v, idx, idx_layers, idx_heads, layer_lo, n_layers_out, n_sel, k_out, v_out,
                         reinterpret_cast<DeviceError*>(ws), stream);
+}
+
+static kvsel_status attend_plan(const kvsel_desc& d, int32_t n_q, int32_t block, int32_t max_blocks,
+                                int64_t* S, size_t* bytes) {
+  if (n_q < 1 || (int64_t)(d.h_q / d.h_kv) * n_q > 32) return KVSEL_ERR_UNSUPPORTED;
+  if (block < 1 || block > KVSEL_MAX_PAGE || max_blocks < 0) return KVSEL_ERR_INVALID_ARG;
+  const int64_t rows = total_units(d);
+  const int64_t R = (int64_t)(d.h_q / d.h_kv) * n_q;
+  *S = attend_splits(rows, std::max<int64_t>(1, (int64_t)max_blocks * block), (int)R);
+  if (rows * *S >= (int64_t(1) << 31)) return KVSEL_ERR_UNSUPPORTED;
+  *bytes = align_up(sizeof(DeviceError) + (size_t)(rows * *S * R * (d.head_dim + 2)) * sizeof(float), KVSEL_WS_ALIGN);
+  return KVSEL_OK;
+}
+
+kvsel_status kvsel_attend_workspace_size(const kvsel_desc* desc, int32_t n_q, int32_t block, int32_t max_blocks,
+                                         size_t* bytes) {
+  kvsel_status st = check_desc(desc);
+  if (st != KVSEL_OK) return st;
+  if (bytes == nullptr) return KVSEL_ERR_INVALID_ARG;
+  int64_t S = 0;
+  return attend_plan(*desc, n_q, block, max_blocks, &S, bytes);
+}
+
+kvsel_status kvsel_attend(const kvsel_desc* desc, const void* q, int32_t n_q, const void* k, const void* v,
+                          const int32_t* kv_indptr, const int32_t* kv_indices, int32_t n_per_row, int32_t block,
+                          int32_t max_blocks, float* o, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  kvsel_status st = check_desc(desc);
+  if (st != KVSEL_OK) return st;
+  const kvsel_desc& d = *desc;
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return KVSEL_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return KVSEL_ERR_INVALID_ARG;
+  if (kv_indices == nullptr && kv_indptr != nullptr) return KVSEL_ERR_INVALID_ARG;
+  if (kv_indices != nullptr && kv_indptr == nullptr && (n_per_row < 0 || n_per_row > max_blocks))
+    return KVSEL_ERR_INVALID_ARG;
+  int64_t S = 0;
+  size_t need = 0;
+  if ((st = attend_plan(d, n_q, block, max_blocks, &S, &need)) != KVSEL_OK) return st;
+  if (ws == nullptr || ((uintptr_t)ws % KVSEL_WS_ALIGN) != 0 || ws_bytes < need) return KVSEL_ERR_WORKSPACE;
+  if (kv_indices == nullptr)
+    for (int b = 0; b < d.batch; ++b)
+      if (cdiv(d.prefix_lens[b] + d.window, block) > max_blocks) return KVSEL_ERR_INVALID_ARG;
+  SeqTable t = make_table(d, d.n_layers);
+  return launch_attend(d, t, q, n_q, k, v, kv_indptr, kv_indices, n_per_row, block, S,
+                       reinterpret_cast<float*>(static_cast<char*>(ws) + sizeof(DeviceError)), o,
+                       reinterpret_cast<DeviceError*>(ws), stream);
 }
 
 kvsel_status kvsel_pagetable(const kvsel_desc* desc, const uint8_t* mask, int32_t n_qblk,

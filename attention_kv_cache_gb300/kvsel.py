@@ -70,6 +70,8 @@ def _load():
         "kvsel_compact": (I32, [D, VP, VP, VP, I32, I32, VP, VP, VP, VP]),
         "kvsel_compact_layers": (I32, [D, VP, VP, VP, I32, I32, I32, I32, I32, VP, VP, VP, VP]),
         "kvsel_pagetable": (I32, [D, VP, I32, I32, P(I32), VP, VP, VP, SZ, VP]),
+        "kvsel_attend_workspace_size": (I32, [D, I32, I32, I32, P(SZ)]),
+        "kvsel_attend": (I32, [D, VP, I32, VP, VP, VP, VP, I32, I32, I32, VP, VP, SZ, VP]),
         "kvsel_read_device_error": (I32, [VP, VP]),
         "kvsel_selftest_bounded_wait": (I32, [VP, ctypes.c_uint32, I32, VP]),
         "kvsel_status_string": (ctypes.c_char_p, [I32]),
@@ -88,7 +90,7 @@ def _load():
 _lib = _load()
 EXPORTED = ("kvsel_workspace_size", "kvsel_score", "kvsel_score_noalloc", "kvsel_combine_layers",
             "kvsel_aggregate", "kvsel_select", "kvsel_topk", "kvsel_compact", "kvsel_compact_layers",
-            "kvsel_pagetable", "kvsel_read_device_error", "kvsel_selftest_bounded_wait", "kvsel_status_string",
+            "kvsel_pagetable", "kvsel_attend_workspace_size", "kvsel_attend", "kvsel_read_device_error", "kvsel_selftest_bounded_wait", "kvsel_status_string",
             "kvsel_version", "kvsel_trace_enable", "kvsel_trace_read", "kvsel_launch_count")
 
 
@@ -199,6 +201,20 @@ def kvsel_pagetable(desc, mask, n_qblk: int, n_kvblk_max: int, n_kvblk: Sequence
     nk = (ctypes.c_int32 * len(n_kvblk))(*[int(x) for x in n_kvblk])
     _check(_lib.kvsel_pagetable(ctypes.byref(desc), _ptr(mask), n_qblk, n_kvblk_max, nk, _ptr(kv_indptr),
                                 _ptr(kv_indices), _ptr(ws), nb, _stream(stream)), "kvsel_pagetable")
+
+
+def kvsel_attend_workspace_size(desc, n_q: int, block: int, max_blocks: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.kvsel_attend_workspace_size(ctypes.byref(desc), n_q, block, max_blocks, ctypes.byref(n)),
+           "kvsel_attend_workspace_size")
+    return n.value
+
+
+def kvsel_attend(desc, q, n_q: int, k, v, kv_indptr, kv_indices, n_per_row: int, block: int, max_blocks: int, o,
+                 ws, ws_bytes=None, stream=None):
+    nb = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    _check(_lib.kvsel_attend(ctypes.byref(desc), _ptr(q), n_q, _ptr(k), _ptr(v), _ptr(kv_indptr), _ptr(kv_indices),
+                             n_per_row, block, max_blocks, _ptr(o), _ptr(ws), nb, _stream(stream)), "kvsel_attend")
 
 
 def kvsel_read_device_error(ws, stream=None) -> int:

@@ -282,6 +282,14 @@ def make_inputs(w: Workload, device="cpu", with_mask: Optional[bool] = None) -> 
     return Inputs(w, qs, ks, vs, cs, mask, n_kv)
 
 
+def make_decode_queries(w: Workload, n_q: int, device="cpu", seed_offset: int = 0) -> torch.Tensor:
+    """Queries of n_q new tokens per head for attention over the selected cache:
+    [batch, n_layers, h_q, n_q, d] bf16, N(0, 1)."""
+    g = torch.Generator(device=device).manual_seed(w.seed * 7_919 + 0xDEC0DE + seed_offset)
+    q = torch.randn((w.batch, w.n_layers, w.h_q, n_q, w.head_dim), generator=g, device=device, dtype=torch.float32)
+    return q.to(torch.bfloat16)
+
+
 def random_scores(rows: int, n: int, seed: int, ties: bool = False, device="cpu") -> torch.Tensor:
     """Non-negative fp32 score rows for selection tests.
 

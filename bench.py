@@ -45,6 +45,9 @@ def parse():
                    help="(layer, KV head) units in the CPU-baseline sample (default: one per host core)")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--attend", action="store_true",
+                   help="time attention over the selected pages in place (page table) against compact + dense")
+    p.add_argument("--n-q", type=int, default=1, help="query rows per head for --attend")
     return p.parse_args()
 
 
@@ -421,6 +424,99 @@ def metric_for(w):
     return f"prefix tokens scored+selected/s (per layer, {w.prefix_lens[0] // 1024}K ctx, {w.name})"
 
 
+# ----------------------------------------------------------------------------- attention over the selection
+
+def run_attend(args):
+    """Decode-style attention over the selected pages: read in place through the page table
+    (CompactAttention's zero-copy execution, DELTA's sparse layers) against the copy path (compact,
+    then dense attention over the compacted cache)."""
+    import torch
+    from attention_kv_cache_gb300 import kvsel as K
+    from attention_kv_cache_gb300 import synth as S
+    from attention_kv_cache_gb300.pipeline import Pipeline, pack
+
+    w = S.by_name(args.workload)
+    if args.layers:
+        w = w.with_(n_layers=args.layers)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    inp = S.make_inputs(w, str(dev))
+    q, k, v = pack(inp, dev)
+    pipe = Pipeline(w, dev)
+    pipe.run(q, k, v, inp.mask, inp.n_kvblk)
+    n_q = args.n_q
+    qd = S.make_decode_queries(w, n_q, str(dev))
+    P, n_sel = w.page_size, pipe.n_sel
+    o = torch.empty((w.batch, w.n_layers, w.h_q, n_q, w.head_dim), dtype=torch.float32, device=dev)
+
+    def ws_for(desc, max_blocks):
+        n = K.kvsel_attend_workspace_size(desc, n_q, P, max_blocks)
+        buf = torch.zeros(n + K.WS_ALIGN, dtype=torch.uint8, device=dev)
+        off = (-buf.data_ptr()) % K.WS_ALIGN
+        return buf[off:off + n]
+
+    ws_a = ws_for(pipe.desc, n_sel)
+    rows = n_sel * P
+    dc = K.make_desc(n_layers=w.n_layers, h_q=w.h_q, h_kv=w.h_kv, head_dim=w.head_dim, window=w.window,
+                     prefix_lens=[rows - w.window])
+    ws_c = ws_for(dc, n_sel)
+    oc = torch.empty_like(o)
+    kc, vc = pipe.k_out.reshape(-1), pipe.v_out.reshape(-1)
+
+    def in_place():
+        K.kvsel_attend(pipe.desc, qd, n_q, k, v, None, pipe.idx, n_sel, P, n_sel, o, ws_a)
+
+    def copy_path():
+        pipe.compact(k, v)
+        K.kvsel_attend(dc, qd, n_q, kc, vc, None, None, 0, P, n_sel, oc, ws_c)
+
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    for name, fn in (("in_place", in_place), ("copy", copy_path)):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        sampler = ClockSampler(0)
+        K.kvsel_trace_enable(True)
+        K.kvsel_trace_read()
+        n0 = K.kvsel_launch_count()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        trace = K.kvsel_trace_read()
+        K.kvsel_trace_enable(False)
+        res[name] = {"ms": e0.elapsed_time(e1) / args.steps, "launches": K.kvsel_launch_count() - n0,
+                     "clocks": sampler.stop(),
+                     "kernels": {n: {"launches": c, "ms": round(t, 4)} for n, (c, t) in trace.items()}}
+    assert K.kvsel_read_device_error(ws_a) == K.OK
+    units = w.batch * w.n_layers * w.h_kv
+    kv_rows = units * rows                                  # selected cache rows attended per step
+    att_bytes = kv_rows * 2 * w.head_dim * 2 + qd.numel() * 2
+    c_att = res["in_place"]["kernels"]["attend_split"]
+    att_ms = c_att["ms"] / c_att["launches"]
+    peak, peak_src = measured_peaks()
+    achieved = att_bytes / (att_ms / 1e3) / 1e9
+    line = {
+        "metric": f"selected KV rows attended/s (decode, n_q={n_q}, in place through the page table)",
+        "value": kv_rows / (res["in_place"]["ms"] / 1e3), "unit": "rows/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["in_place"]["ms"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 inputs, f32 arithmetic", "data": "synthetic",
+        "config": {"workload": w.name, "layers": w.n_layers, "pages_per_row": n_sel, "page_size": P,
+                   "rows_per_step": kv_rows, "l2": "selected K+V %.0f MB per step" % (kv_rows * 512 / 1e6)},
+        "clocks": res["in_place"]["clocks"], "gpu_launches": res["in_place"]["launches"],
+        "kernels": res["in_place"]["kernels"],
+        "roofline": {"bound": "hbm", "kernel": "attend_split", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_source": peak_src, "traffic": None,
+                     "algorithmic_bytes": att_bytes},
+        "copy_path": {"ms_per_step": res["copy"]["ms"], "kernels": res["copy"]["kernels"],
+                      "in_place_speedup": res["copy"]["ms"] / res["in_place"]["ms"]},
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- the oracle arm
 
 def run_reference(args):
@@ -459,5 +555,7 @@ if __name__ == "__main__":
     a = parse()
     if a.impl == "reference":
         run_reference(a)
+    elif a.attend:
+        run_attend(a)
     else:
         run_kvsel(a)

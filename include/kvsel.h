@@ -238,6 +238,38 @@ KVSEL_API kvsel_status kvsel_compact_layers(const kvsel_desc* desc, const void* 
                                             void* k_out, void* v_out, void* ws, cudaStream_t stream);
 
 /*
+ * kvsel_attend — attention of a few query rows per head over the KV rows a table selects, in place.
+ *
+ * CompactAttention, 'Method steps' (3): the per-group block list T[b,g] (kv_indptr / kv_indices,
+ * as kvsel_pagetable writes it) goes to a paged dense-attention kernel that reads the selected
+ * blocks of the KV-head-major cache where they are, with no copy; DELTA, 'Overall framework':
+ * sparse layers attend only over the selected page set (the dense page table of kvsel_topk in page
+ * mode).  For each table row (b, layer, g) and each of the n_q query rows of each of the G query
+ * heads of group g: o = softmax(q K_sel^T / sqrt(d)) V_sel over every row of every listed block
+ * (block j covers rows j*block .. j*block + block - 1; rows past L_b + W do not exist), with no
+ * causal mask (decode-style queries come after every selected key).  A row that selects nothing
+ * gives o = 0.
+ *
+ *   q           [device] bf16 [batch][n_layers][h_q][n_q][d]; (h_q / h_kv) * n_q <= 32
+ *   k, v        [device] bf16 caches, layout above
+ *   kv_indptr   [device] int32 [batch * n_layers * h_kv + 1] (CSR), or NULL: row r's list is
+ *               kv_indices[r * n_per_row .. (r + 1) * n_per_row) (a dense table)
+ *   kv_indices  [device] int32 block ids, or NULL together with kv_indptr: every block of the
+ *               row's cache in order (dense attention over the whole cache)
+ *   block       rows per block, 1 .. KVSEL_MAX_PAGE
+ *   max_blocks  upper bound of any row's list length (sizes the split of each row's work)
+ *   o           [device] fp32 out [batch][n_layers][h_q][n_q][d]
+ *   ws          [device] workspace of kvsel_attend_workspace_size() bytes (partials of the splits);
+ *               a block id whose first row does not exist is skipped and KVSEL_ERR_DEVICE recorded
+ */
+KVSEL_API kvsel_status kvsel_attend_workspace_size(const kvsel_desc* desc, int32_t n_q, int32_t block,
+                                                   int32_t max_blocks, size_t* bytes);
+KVSEL_API kvsel_status kvsel_attend(const kvsel_desc* desc, const void* q, int32_t n_q, const void* k,
+                                    const void* v, const int32_t* kv_indptr, const int32_t* kv_indices,
+                                    int32_t n_per_row, int32_t block, int32_t max_blocks, float* o, void* ws,
+                                    size_t ws_bytes, cudaStream_t stream);
+
+/*
  * kvsel_pagetable — per-group KV block table from a 2-D block mask.
  *
  * CompactAttention: Accelerating Chunked Prefill with Block-Union KV

@@ -121,3 +121,25 @@ def test_bounded_wait_reports_timeout(cuda):
     K.kvsel_topk(d2, s.to(cuda), 2, 10, 0, idx, _ws(K, d2, cuda))
     for r in range(2):
         np.testing.assert_array_equal(idx[r].cpu().numpy(), O.select_tokens(s[r].double().numpy(), 10, 300, 16))
+
+
+def test_topk_first_call_in_fresh_process(cuda):
+    """The first top-k launch of a process, on rows whose keys fit shared memory, launches (the kernel's
+    static shared memory counts against the default limit too)."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = (
+        "import sys, torch; sys.path.insert(0, %r)\n"
+        "from attention_kv_cache_gb300 import kvsel as K\n"
+        "d = K.make_desc(n_layers=1, h_q=1, h_kv=1, head_dim=128, window=8, prefix_lens=[8192])\n"
+        "n = K.kvsel_workspace_size(d); ws = torch.zeros(n + 256, dtype=torch.uint8, device='cuda')\n"
+        "ws = ws[(-ws.data_ptr()) %% 256:][:n]\n"
+        "s = torch.rand(8192, device='cuda'); idx = torch.empty(18, dtype=torch.int32, device='cuda')\n"
+        "K.kvsel_topk(d, s, 1, 10, 0, idx, ws); torch.cuda.synchronize()\n"
+        "ref = torch.sort(torch.topk(s, 10).indices).values.int()\n"
+        "assert torch.equal(idx[:10], ref), (idx, ref)\n"
+        "print('ok')\n" % root)
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0 and out.stdout.strip().endswith("ok"), out.stderr[-2000:]
