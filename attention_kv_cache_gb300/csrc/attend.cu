@@ -224,26 +224,45 @@ __global__ void __launch_bounds__(kAttThreads) attend_split(const __grid_constan
 }
 
 // Decode-sized groups (R <= 8 query rows per table row): one warp per split, no block-wide
-// synchronisation in the loop.  Per step of 32 key positions of its split, lane i takes position i:
-// it loads that key's K row (256 contiguous bytes) and, for V, the 8 bytes of dims 4i..4i+3 of every
-// one of the 32 keys (32 coalesced row reads), all issued before any arithmetic so that 16 KB per
-// warp are in flight; the logits use the query rows from shared memory (broadcast reads), the
-// online softmax runs across the lanes with shuffles, and the weighted V sum keeps each lane's dims.
+// synchronisation in the loop.  A step covers 16 key positions of the split: the lanes copy the
+// step's K and V rows into the warp's shared-memory stage with cp.async (whole rows per copy
+// instruction; zero-filled where a position selects no row), and the next step's copies are issued
+// before this step's arithmetic.  Lane i takes key i % 16 and half i / 16 of the head dim for the
+// logits (K chunks XOR-swizzled by the key, so the lanes' reads hit distinct banks; query rows read
+// from shared memory as broadcasts), the online softmax runs across the 16 keys with shuffles, and in
+// the weighted V sum lane i owns dims DPL*i .. DPL*i + DPL - 1.  Small stages keep 12 warps per SM.
+constexpr int kWarpsPerCta = 4;
+constexpr int kStep = 16;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  const uint32_t n = valid ? 16u : 0u;   // 0 source bytes: the 16 destination bytes are zero-filled
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 template <int D, int R>
-__global__ void __launch_bounds__(128) attend_warp(const __grid_constant__ AttArgs a,
-                                                   const __grid_constant__ SeqTable t) {
-  constexpr int VPR = D / 8;          // 16-byte vectors per K row
-  constexpr int DPL = D / 32;         // dims per lane in the V sum (4 for d = 128, 2 for d = 64)
-  __shared__ __align__(16) float Qs[R * D];
+__global__ void __launch_bounds__(32 * kWarpsPerCta) attend_warp(const __grid_constant__ AttArgs a,
+                                                                 const __grid_constant__ SeqTable t) {
+  constexpr int VPR = D / 8;          // 16-byte chunks per row
+  constexpr int DPL = D / 32;         // dims per lane in the V sum
+  constexpr int STAGE = kStep * D;    // bf16 elements of one K (or V) stage
+  constexpr int HC = VPR / 2;         // chunks per half row
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  float* Qs = reinterpret_cast<float*>(smem_raw);                                   // [R][D]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = blockIdx.x / (a.S / 4);
-  const int s = (blockIdx.x % (a.S / 4)) * 4 + warp;
+  __nv_bfloat16* Kb = reinterpret_cast<__nv_bfloat16*>(smem_raw + R * D * 4) + warp * 4 * STAGE;   // [2][16][D]
+  __nv_bfloat16* Vb = Kb + 2 * STAGE;                                                              // [2][16][D]
+  const int per_cta = a.S / kWarpsPerCta;
+  const int r = blockIdx.x / per_cta;
+  const int s = (blockIdx.x % per_cta) * kWarpsPerCta + warp;
   const int per_seq = a.n_layers * a.h_kv;
   const int b = r / per_seq, lg = r % per_seq;
   const int layer = lg / a.h_kv, g = lg % a.h_kv;
   const SeqInfo& si = t.s[b];
   // query rows j < a.R of the group (rows up to the template's R beyond them are zero and unused)
-  for (int x = threadIdx.x; x < R * D; x += 128) {
+  for (int x = threadIdx.x; x < R * D; x += 32 * kWarpsPerCta) {
     const int j = x / D, c = x % D;
     float qv = 0.f;
     if (j < a.R) {
@@ -258,9 +277,45 @@ __global__ void __launch_bounds__(128) attend_warp(const __grid_constant__ AttAr
   row_list(a, si, r, beg, end);
   const int64_t n_pos = (int64_t)(end - beg) * a.P;                  // key positions of the row
   const int64_t p0 = (s * n_pos) / a.S, p1 = ((s + 1) * n_pos) / a.S;
-  const uint4* kbase = a.k + si.k_off / 8 + ((int64_t)layer * a.h_kv + g) * si.n_keys * VPR;
+  const __nv_bfloat16* kbase =
+      reinterpret_cast<const __nv_bfloat16*>(a.k) + si.k_off + ((int64_t)layer * a.h_kv + g) * si.n_keys * D;
   const __nv_bfloat16* vbase =
       reinterpret_cast<const __nv_bfloat16*>(a.v) + si.k_off + ((int64_t)layer * a.h_kv + g) * si.n_keys * D;
+  const uint32_t kb_s = (uint32_t)__cvta_generic_to_shared(Kb), vb_s = (uint32_t)__cvta_generic_to_shared(Vb);
+  const int key = lane & (kStep - 1), half = lane >> 4;
+
+  // Block id of this lane's key position (fetched a step ahead of its use), and its cache row or -1.
+  auto id_at = [&](int64_t pos) -> int32_t {
+    if (pos >= p1) return -1;
+    const int bi = (int)(pos / a.P);
+    return a.indices == nullptr ? bi : __ldg(a.indices + beg + bi);
+  };
+  auto row_of = [&](int64_t pos, int32_t id) -> int32_t {
+    if (pos >= p1) return -1;
+    const int bi = (int)(pos / a.P), within = (int)(pos - (int64_t)bi * a.P);
+    const int64_t rr = (int64_t)id * a.P + within;
+    if (id >= 0 && rr < si.n_keys) return (int32_t)rr;
+    if (within == 0 && half == 0) set_device_error(a.err, KVSEL_ERR_DEVICE, (uint32_t)(beg + bi));
+    return -1;
+  };
+  // Copy of one stage: lane takes 16-byte chunk lane % VPR of key lane / VPR + (32 / VPR) * i, so each
+  // copy instruction reads whole rows (512 contiguous bytes per two rows at d = 128).
+  auto issue = [&](int32_t row, int buf) {
+    constexpr int KPI = 32 / VPR;                   // keys per instruction
+    const int c = lane % VPR;
+#pragma unroll
+    for (int i = 0; i < kStep / KPI; ++i) {
+      const int x = i * KPI + lane / VPR;
+      const int32_t rx = __shfl_sync(0xffffffffu, row, x);
+      const int64_t src = (int64_t)(rx < 0 ? 0 : rx) * D + c * 8;
+      const uint32_t kd = kb_s + (uint32_t)((buf * STAGE + x * D) * 2 + ((c ^ (x & (VPR - 1))) * 16));
+      const uint32_t vd = vb_s + (uint32_t)((buf * STAGE + x * D) * 2 + c * 16);
+      cp_async16(kd, kbase + src, rx >= 0);
+      cp_async16(vd, vbase + src, rx >= 0);
+    }
+    cp_async_commit();
+  };
+
   float m[R], l[R], acc[R][DPL];
 #pragma unroll
   for (int j = 0; j < R; ++j) {
@@ -269,77 +324,77 @@ __global__ void __launch_bounds__(128) attend_warp(const __grid_constant__ AttAr
 #pragma unroll
     for (int c = 0; c < DPL; ++c) acc[j][c] = 0.f;
   }
-  for (int64_t base = p0; base < p1; base += 32) {
-    // this lane's key position -> cache row (or -1: past the split, an invalid block, past the cache)
-    const int64_t pos = base + lane;
-    int32_t row = -1;
-    if (pos < p1) {
-      const int bi = (int)(pos / a.P), within = (int)(pos - (int64_t)bi * a.P);
-      const int id = a.indices == nullptr ? bi : a.indices[beg + bi];
-      const int64_t rr = (int64_t)id * a.P + within;
-      if (id >= 0 && rr < si.n_keys) row = (int32_t)rr;
-      else if (within == 0) set_device_error(a.err, KVSEL_ERR_DEVICE, (uint32_t)(beg + bi));
+  int32_t row = row_of(p0 + key, id_at(p0 + key));
+  int32_t id_next = id_at(p0 + kStep + key);
+  if (p0 < p1) issue(row, 0);
+  int buf = 0;
+  for (int64_t base = p0; base < p1; base += kStep) {
+    const bool more = base + kStep < p1;
+    int32_t row_next = -1;
+    const int32_t id_after = id_at(base + 2 * kStep + key);
+    if (more) {
+      row_next = row_of(base + kStep + key, id_next);
+      issue(row_next, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
-    // loads: own K row; dims DPL*lane .. of every key's V row
-    uint4 kv[VPR];
+    id_next = id_after;
+    __syncwarp();
+    // logits: this lane's key, half of the head dim, two partial sums per row for ILP
+    const __nv_bfloat16* krow = Kb + buf * STAGE + key * D;
+    float z[R], z2[R];
 #pragma unroll
-    for (int c = 0; c < VPR; ++c) kv[c] = row >= 0 ? kbase[(int64_t)row * VPR + c] : make_uint4(0, 0, 0, 0);
-    uint32_t vv[32][DPL / 2];
+    for (int j = 0; j < R; ++j) z[j] = z2[j] = 0.f;
 #pragma unroll
-    for (int x = 0; x < 32; ++x) {
-      const int32_t rx = __shfl_sync(0xffffffffu, row, x);
-      const __nv_bfloat16* vp = vbase + (int64_t)(rx < 0 ? 0 : rx) * D + DPL * lane;
-      if constexpr (DPL == 4) {
-        const uint2 u = rx >= 0 ? *reinterpret_cast<const uint2*>(vp) : make_uint2(0, 0);
-        vv[x][0] = u.x;
-        vv[x][1] = u.y;
-      } else {
-        vv[x][0] = rx >= 0 ? *reinterpret_cast<const uint32_t*>(vp) : 0u;
-      }
-    }
-    // logits of this lane's key for the R query rows
-    float z[R];
-#pragma unroll
-    for (int j = 0; j < R; ++j) z[j] = 0.f;
-#pragma unroll
-    for (int c = 0; c < VPR; ++c) {
+    for (int cc = 0; cc < HC; ++cc) {
+      const int c = half * HC + cc;
       float kf[8];
-      bf16x8_to_f32(kv[c], kf);
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(krow + ((c ^ (key & (VPR - 1))) * 8)), kf);
 #pragma unroll
       for (int j = 0; j < R; ++j) {
         const float4 q0 = *reinterpret_cast<const float4*>(Qs + j * D + c * 8);
         const float4 q1 = *reinterpret_cast<const float4*>(Qs + j * D + c * 8 + 4);
         z[j] = fmaf(q0.x, kf[0], fmaf(q0.y, kf[1], fmaf(q0.z, kf[2], fmaf(q0.w, kf[3], z[j]))));
-        z[j] = fmaf(q1.x, kf[4], fmaf(q1.y, kf[5], fmaf(q1.z, kf[6], fmaf(q1.w, kf[7], z[j]))));
+        z2[j] = fmaf(q1.x, kf[4], fmaf(q1.y, kf[5], fmaf(q1.z, kf[6], fmaf(q1.w, kf[7], z2[j]))));
       }
     }
-    // online softmax across the 32 keys of the step
+    // online softmax across the 16 keys of the step (both halves hold the same values)
     float p[R];
 #pragma unroll
     for (int j = 0; j < R; ++j) {
-      const float zj = row >= 0 ? z[j] : -INFINITY;
+      float zj = z[j] + z2[j];
+      zj += __shfl_xor_sync(0xffffffffu, zj, 16);
+      zj = row >= 0 ? zj : -INFINITY;
       float mx = zj;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       const float m_new = fmaxf(m[j], mx);
       const float f = m[j] == -INFINITY ? 0.f : fast_ex2(m[j] - m_new);
       p[j] = m_new == -INFINITY ? 0.f : fast_ex2(zj - m_new);
       float sum = p[j];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
       l[j] = l[j] * f + sum;
       m[j] = m_new;
 #pragma unroll
       for (int c = 0; c < DPL; ++c) acc[j][c] *= f;
     }
-    // weighted V sum over the 32 keys
+    // weighted V sum over the 16 keys (zero-filled rows carry p = 0)
+    const __nv_bfloat16* vst = Vb + buf * STAGE + DPL * lane;
 #pragma unroll
-    for (int x = 0; x < 32; ++x) {
+    for (int x = 0; x < kStep; ++x) {
       float vf[DPL];
-#pragma unroll
-      for (int c = 0; c < DPL / 2; ++c) {
-        vf[2 * c] = __uint_as_float(vv[x][c] << 16);
-        vf[2 * c + 1] = __uint_as_float(vv[x][c] & 0xffff0000u);
+      if constexpr (DPL == 4) {
+        const uint2 u = *reinterpret_cast<const uint2*>(vst + x * D);
+        vf[0] = __uint_as_float(u.x << 16);
+        vf[1] = __uint_as_float(u.x & 0xffff0000u);
+        vf[2] = __uint_as_float(u.y << 16);
+        vf[3] = __uint_as_float(u.y & 0xffff0000u);
+      } else {
+        const uint32_t u = *reinterpret_cast<const uint32_t*>(vst + x * D);
+        vf[0] = __uint_as_float(u << 16);
+        vf[1] = __uint_as_float(u & 0xffff0000u);
       }
 #pragma unroll
       for (int j = 0; j < R; ++j) {
@@ -348,6 +403,9 @@ __global__ void __launch_bounds__(128) attend_warp(const __grid_constant__ AttAr
         for (int c = 0; c < DPL; ++c) acc[j][c] = fmaf(px, vf[c], acc[j][c]);
       }
     }
+    __syncwarp();          // the stage is read before it is refilled
+    row = row_next;
+    buf ^= 1;
   }
   float* out = a.part + ((int64_t)r * a.S + s) * a.R * (D + 2);
 #pragma unroll
@@ -362,24 +420,35 @@ __global__ void __launch_bounds__(128) attend_warp(const __grid_constant__ AttAr
   }
 }
 
+size_t attend_warp_smem(int d, int R) {
+  return (size_t)R * d * 4 + (size_t)kWarpsPerCta * 4 * kStep * d * 2;
+}
+
 // o[row j of table row r] = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M) l_s; rows with no key give 0.
 template <int D>
 __global__ void __launch_bounds__(D) attend_combine(const __grid_constant__ AttArgs a) {
+  __shared__ float ms[256], ws_[256];
   const int rj = blockIdx.x;
   const int r = rj / a.R, j = rj % a.R;
   const int c = threadIdx.x;
   const float* p = a.part + (int64_t)r * a.S * a.R * (D + 2) + j * (D + 2);
   const int64_t stride = (int64_t)a.R * (D + 2);
+  // the splits' maxima and sums, loaded in parallel
+  for (int s = c; s < a.S; s += D) {
+    ms[s] = p[s * stride + D];
+    ws_[s] = p[s * stride + D + 1];
+  }
+  __syncthreads();
   float M = -INFINITY;
-  for (int s = 0; s < a.S; ++s) M = fmaxf(M, p[s * stride + D]);
+  for (int s = 0; s < a.S; ++s) M = fmaxf(M, ms[s]);
   float num = 0.f, den = 0.f;
   if (M > -INFINITY) {
+#pragma unroll 4
     for (int s = 0; s < a.S; ++s) {
-      const float m = p[s * stride + D];
-      if (m == -INFINITY) continue;
-      const float w = exp2f(m - M);
+      const float m = ms[s];
+      const float w = m == -INFINITY ? 0.f : exp2f(m - M);
       num = fmaf(w, p[s * stride + c], num);
-      den = fmaf(w, p[s * stride + D + 1], den);
+      den = fmaf(w, ws_[s], den);
     }
   }
   const int per_seq = a.n_layers * a.h_kv;
@@ -394,12 +463,13 @@ __global__ void __launch_bounds__(D) attend_combine(const __grid_constant__ AttA
 
 int64_t attend_splits(int64_t rows, int64_t max_rows_per_list, int R) {
   if (R <= 8) {
-    // warp splits: about 4096 warps over the GPU, no split shorter than 64 positions; a multiple of 4
+    // warp splits: about 4096 warps over the GPU, no split shorter than 64 positions; a multiple of
+    // the warps per CTA
     int64_t s = (4096 + rows - 1) / rows;
     const int64_t cap = (max_rows_per_list + 63) / 64;
     if (s > cap) s = cap;
-    s = (s + 3) / 4 * 4;
-    if (s < 4) s = 4;
+    s = (s + kWarpsPerCta - 1) / kWarpsPerCta * kWarpsPerCta;
+    if (s < kWarpsPerCta) s = kWarpsPerCta;
     if (s > 256) s = 256;
     return s;
   }
@@ -445,8 +515,13 @@ kvsel_status launch_attend(const kvsel_desc& d, const SeqTable& t, const void* q
   kvsel_status st;
   if (a.R <= 8) {
     TraceScope ts("attend_split", s);
-    const unsigned grid = (unsigned)(rows * S / 4);
-    auto go = [&](auto kern) { kern<<<grid, 128, 0, s>>>(a, t); };
+    const unsigned grid = (unsigned)(rows * S / kWarpsPerCta);
+    const int Rt = a.R == 1 ? 1 : a.R == 2 ? 2 : a.R <= 4 ? 4 : 8;
+    const size_t wsm = attend_warp_smem(d.head_dim, Rt);
+    cudaError_t ce = cudaSuccess;
+    auto go = [&](auto kern) {
+      if ((ce = set_smem((const void*)kern, wsm)) == cudaSuccess) kern<<<grid, 32 * kWarpsPerCta, wsm, s>>>(a, t);
+    };
     if (d.head_dim == 64) {
       if (a.R == 1) go(attend_warp<64, 1>);
       else if (a.R == 2) go(attend_warp<64, 2>);
@@ -458,6 +533,7 @@ kvsel_status launch_attend(const kvsel_desc& d, const SeqTable& t, const void* q
       else if (a.R <= 4) go(attend_warp<128, 4>);
       else go(attend_warp<128, 8>);
     }
+    if (ce != cudaSuccess) return KVSEL_ERR_CUDA;
     if ((st = launch_status()) != KVSEL_OK) return st;
   } else {
     TraceScope ts("attend_split", s);

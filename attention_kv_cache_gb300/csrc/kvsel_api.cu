@@ -378,6 +378,7 @@ static kvsel_status attend_plan(const kvsel_desc& d, int32_t n_q, int32_t block,
   const int64_t R = (int64_t)(d.h_q / d.h_kv) * n_q;
   *S = attend_splits(rows, std::max<int64_t>(1, (int64_t)max_blocks * block), (int)R);
   if (rows * *S >= (int64_t(1) << 31)) return KVSEL_ERR_UNSUPPORTED;
+  // error word, partials of the splits
   *bytes = align_up(sizeof(DeviceError) + (size_t)(rows * *S * R * (d.head_dim + 2)) * sizeof(float), KVSEL_WS_ALIGN);
   return KVSEL_OK;
 }
