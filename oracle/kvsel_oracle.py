@@ -39,6 +39,10 @@ Sources (page title, then the section / equation the step follows):
   with kernel 7 for every method.
 * LookaheadKV, 'Method steps': the lookahead rows' attention to the prompt is
   averaged, pooled, and the top K kept.
+* CLAA, 'Complete flow and cost' (engineering detail 1): the keys that score the
+  window are the prefill's own intermediate results; the prefill attention is
+  causal softmax attention over the prompt, o_i = sum_{t <= i} softmax_t(q_i k_t /
+  sqrt(d)) v_t, and its per-row log-sum-exp is what the window scores need.
 * CompactAttention, 'Method steps' (3): the selected KV blocks are read in
   place by a paged dense-attention kernel through kv_indptr / kv_indices;
   DELTA, 'Overall framework': sparse layers attend only over the selected page
@@ -312,6 +316,27 @@ def attend(q: np.ndarray, k: np.ndarray, v: np.ndarray, rows: np.ndarray) -> np.
     p = np.exp(z)
     p /= p.sum(axis=-1, keepdims=True)
     return p @ v[rows]
+
+
+def prefill_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray):
+    """Causal attention of every prompt row.  q [H_q, N, d], k / v [H_kv, N, d] (GQA map h -> h // G).
+
+    Returns o [H_q, N, d] and lse [H_q, N], the natural-log log-sum-exp of each row's scaled logits
+    over its visible keys t <= i.
+    """
+    Hq, N, d = q.shape
+    G = Hq // k.shape[0]
+    vis = np.arange(N)[None, :] <= np.arange(N)[:, None]
+    o = np.zeros_like(q)
+    lse = np.zeros((Hq, N))
+    for h in range(Hq):
+        z = np.where(vis, window_logits(q[h], k[h // G]), -np.inf)
+        m = z.max(axis=-1, keepdims=True)
+        e = np.exp(z - m)
+        ssum = e.sum(axis=-1, keepdims=True)
+        o[h] = (e / ssum) @ v[h // G]
+        lse[h] = (m + np.log(ssum))[:, 0]
+    return o, lse
 
 
 # --------------------------------------------------------------------------- block union

@@ -442,6 +442,34 @@ def check_table_attention_sdpa(o):
     np.testing.assert_allclose(o.attend(q, k, v, rows[::-1].copy()), got, rtol=1e-12)
 
 
+def check_prefill_attention_sdpa(o):
+    """Causal prefill attention equals torch SDPA (is_causal, enable_gqa); its lse reproduces the row
+    weights (exp(z - lse) sums to one) and the window rows' softmax of the window scoring."""
+    rng = _rng(19)
+    Hq, Hkv, N, d = 4, 2, 23, 8
+    q = _bf16_values(rng.standard_normal((Hq, N, d)) * 1.4)
+    k = _bf16_values(rng.standard_normal((Hkv, N, d)))
+    v = _bf16_values(rng.standard_normal((Hkv, N, d)))
+    out, lse = o.prefill_attention(q, k, v)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[None], torch.from_numpy(k)[None], torch.from_numpy(v)[None], is_causal=True,
+        enable_gqa=True)[0].numpy()
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-13)
+    G = Hq // Hkv
+    for h in range(Hq):
+        z = (q[h] @ k[h // G].T) / np.sqrt(d)
+        for i in range(N):
+            np.testing.assert_allclose(np.exp(z[i, :i + 1] - lse[h, i]).sum(), 1.0, rtol=1e-13)
+    # the last W rows are the observation window: their probabilities are the window softmax
+    W = 5
+    L = N - W
+    p = o.window_probs(q[:G, L:], k[0], L)
+    for hl in range(G):
+        for j in range(W):
+            zz = (q[hl, L + j] @ k[0].T) / np.sqrt(d)
+            np.testing.assert_allclose(p[hl, j, :L + j + 1], np.exp(zz[:L + j + 1] - lse[hl, L + j]), rtol=1e-12)
+
+
 ALL_CHECKS = [
     check_probs_match_sdpa,
     check_row_mass_invariant,
@@ -462,4 +490,5 @@ ALL_CHECKS = [
     check_layer_max_and_keep_count,
     check_claa_max_buffer,
     check_table_attention_sdpa,
+    check_prefill_attention_sdpa,
 ]

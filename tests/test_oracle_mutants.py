@@ -210,13 +210,30 @@ def _table_rows_off_by_one(o):
     o.table_rows = table_rows
 
 
+def _prefill_not_causal(o):
+    def prefill_attention(q, k, v):
+        Hq, N, d = q.shape
+        G = Hq // k.shape[0]
+        out = np.zeros_like(q)
+        lse = np.zeros((Hq, N))
+        for h in range(Hq):
+            z = o.window_logits(q[h], k[h // G])
+            m = z.max(axis=-1, keepdims=True)
+            e = np.exp(z - m)
+            out[h] = (e / e.sum(-1, keepdims=True)) @ v[h // G]
+            lse[h] = (m + np.log(e.sum(-1, keepdims=True)))[:, 0]
+        return out, lse
+    o.prefill_attention = prefill_attention
+
+
 MUTANTS = [_no_scale, _mask_off_by_one, _prefix_only_softmax, _mass_max_over_rows,
            _mass_includes_window_shift, _wrong_group_map, _reduce_swapped, _transposed_rows,
            _pool_radius, _pool_one_sided, _page_sum_for_max, _tie_to_higher, _rank_ascending,
            _recency_off_by_one, _no_l1, _layer_range_exclusive, _union_wrong_group,
            _union_first_qblock_only, _gather_page_offset, _logits_unscaled, _logits_include_window_key,
            _mean_over_heads_only, _head_sum_is_max, _avg_pool_counts_padding, _layer_max_is_mean,
-           _keep_count_floor, _claa_buffer_short, _attend_no_scale, _table_rows_off_by_one]
+           _keep_count_floor, _claa_buffer_short, _attend_no_scale, _table_rows_off_by_one,
+           _prefill_not_causal]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda m: m.__name__.strip("_"))
