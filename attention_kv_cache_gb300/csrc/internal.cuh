@@ -57,6 +57,7 @@ struct ScoreShape {
   int32_t group_reduce, pool_k, page_size, page_reduce;
   int32_t pool_type;                         // KVSEL_POOL_MAX / KVSEL_POOL_AVG
   int32_t logits;                            // 1: pre-softmax scaled logits (one pass, no lse)
+  int32_t lse_given;                         // 1: the rows' lse is an input (the prefill's); pass 2 only
   int32_t seg1, seg2;                        // keys per pass-1 / pass-2 segment
   float scale_log2;                          // log2(e) / sqrt(d)
   float scale_nat;                           // 1 / sqrt(d)
@@ -125,6 +126,10 @@ kvsel_status launch_aggregate(const kvsel_desc& desc, const SeqTable& t, const f
 kvsel_status launch_compact(const kvsel_desc& desc, const SeqTable& t, const void* k, const void* v,
                             const int32_t* idx, int idx_layers, int idx_heads, int layer_lo, int n_layers_out,
                             int n_sel, void* k_out, void* v_out, DeviceError* err, cudaStream_t s);
+
+// Causal prefill attention with the window rows' lse and queries (prefill.cu).
+kvsel_status launch_prefill(const kvsel_desc& d, const SeqTable& t, const void* q, const void* k, const void* v,
+                            void* o, float* lse, float* lse_win, void* q_win, DeviceError* err, cudaStream_t s);
 
 // Attention over a page / block table (attend.cu).
 int64_t attend_splits(int64_t rows, int64_t max_rows_per_list, int R);   // R = query rows per table row

@@ -157,6 +157,7 @@ ScoreShape make_shape(const kvsel_desc& d) {
   sh.page_reduce = d.page_reduce;
   sh.pool_type = d.pool_type;
   sh.logits = d.score_mode == KVSEL_SCORE_LOGITS ? 1 : 0;
+  sh.lse_given = 0;
   sh.seg1 = sh.seg2 = 0;    // set by the launcher
   sh.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)d.head_dim));
   sh.scale_nat = (float)(1.0 / std::sqrt((double)d.head_dim));
@@ -266,6 +267,39 @@ kvsel_status kvsel_score(const kvsel_desc* desc, const void* q, const void* k, f
   return launch_score(sh, base, q, k, scores, page_scores, reinterpret_cast<float*>(ws_base(ws) + w.lse_off),
                       reinterpret_cast<float2*>(ws_base(ws) + w.part_off), reinterpret_cast<DeviceError*>(ws),
                       stream);
+}
+
+kvsel_status kvsel_score_from_lse(const kvsel_desc* desc, const void* q_win, const void* k, const float* lse_win,
+                                  float* scores, float* page_scores, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  kvsel_status st = check_desc(desc);
+  if (st != KVSEL_OK) return st;
+  const kvsel_desc& d = *desc;
+  if (q_win == nullptr || k == nullptr || scores == nullptr || lse_win == nullptr) return KVSEL_ERR_INVALID_ARG;
+  if (!aligned16(q_win) || !aligned16(k) || !aligned16(scores)) return KVSEL_ERR_INVALID_ARG;
+  if (d.page_size > 1 && page_scores == nullptr) return KVSEL_ERR_INVALID_ARG;
+  if (d.score_mode != KVSEL_SCORE_SOFTMAX) return KVSEL_ERR_INVALID_ARG;
+  if ((st = check_ws(d, ws, ws_bytes)) != KVSEL_OK) return st;
+  const WsLayout w = ws_layout(d);
+  ScoreShape sh = make_shape(d);
+  sh.lse_given = 1;
+  const SeqTable base = make_table(d, d.n_layers);
+  return launch_score(sh, base, q_win, k, scores, page_scores, const_cast<float*>(lse_win),
+                      reinterpret_cast<float2*>(static_cast<char*>(ws) + w.part_off), reinterpret_cast<DeviceError*>(ws),
+                      stream);
+}
+
+kvsel_status kvsel_prefill_attention(const kvsel_desc* desc, const void* q, const void* k, const void* v, void* o,
+                                     float* lse, float* lse_win, void* q_win, void* ws, cudaStream_t stream) {
+  kvsel_status st = check_desc(desc);
+  if (st != KVSEL_OK) return st;
+  const kvsel_desc& d = *desc;
+  if (d.head_dim != 128) return KVSEL_ERR_UNSUPPORTED;
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || lse_win == nullptr || q_win == nullptr)
+    return KVSEL_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(q_win)) return KVSEL_ERR_INVALID_ARG;
+  if (ws != nullptr && ((uintptr_t)ws % KVSEL_WS_ALIGN) != 0) return KVSEL_ERR_WORKSPACE;
+  const SeqTable t = make_table(d, d.n_layers);
+  return launch_prefill(d, t, q, k, v, o, lse, lse_win, q_win, reinterpret_cast<DeviceError*>(ws), stream);
 }
 
 kvsel_status kvsel_combine_layers(const kvsel_desc* desc, const float* scores, int32_t layer_lo,

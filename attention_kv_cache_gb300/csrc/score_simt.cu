@@ -287,7 +287,7 @@ kvsel_status run(const ScoreArgs& args, const SeqTable& t1, const SeqTable& t2, 
   if (set_smem((const void*)score_pass1_simt<D, RP>, smem1) != cudaSuccess) return KVSEL_ERR_CUDA;
   if (set_smem((const void*)score_pass2_simt<D, RP>, smem2) != cudaSuccess) return KVSEL_ERR_CUDA;
   kvsel_status st;
-  if (!args.sh.logits) {   // the softmax needs each row's log-sum-exp first
+  if (!args.sh.logits && !args.sh.lse_given) {   // the softmax needs each row's log-sum-exp first
     {
       TraceScope ts("score_pass1_simt", s);
       score_pass1_simt<D, RP><<<t1.n_items, kThreads, smem1, s>>>(args, t1);

@@ -757,7 +757,7 @@ kvsel_status run_tc(const TcArgs& a, const SeqTable& t1, const SeqTable& t2, con
                     const CUtensorMap& tk, int sms, cudaStream_t s) {
   constexpr int NK = (RT == 256 && D == 128) ? 3 : 4;
   kvsel_status st;
-  if (!a.sh.logits) {   // the softmax needs each row's log-sum-exp first
+  if (!a.sh.logits && !a.sh.lse_given) {   // the softmax needs each row's log-sum-exp first
     if ((st = launch_one<false, RT, D, NK, 0>("score_pass1_tc", tq, tk, a, t1, sms, s)) != KVSEL_OK) return st;
     if ((st = launch_lse_combine(a.sh, t1, a.part, a.lse, s)) != KVSEL_OK) return st;
   }

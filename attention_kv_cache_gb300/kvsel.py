@@ -64,6 +64,8 @@ def _load():
         "kvsel_score": (I32, [D, VP, VP, VP, VP, VP, SZ, VP]),
         "kvsel_score_noalloc": (I32, [D, VP, VP, VP, VP, VP]),
         "kvsel_combine_layers": (I32, [D, VP, I32, I32, VP, VP, SZ, VP]),
+        "kvsel_prefill_attention": (I32, [D, VP, VP, VP, VP, VP, VP, VP, VP, VP]),
+        "kvsel_score_from_lse": (I32, [D, VP, VP, VP, VP, VP, VP, SZ, VP]),
         "kvsel_aggregate": (I32, [D, VP, I32, I32, I32, I32, VP, VP, SZ, VP]),
         "kvsel_select": (I32, [D, VP, I32, I32, I32, I32, VP, VP, SZ, VP]),
         "kvsel_topk": (I32, [D, VP, I32, I32, I32, VP, VP, SZ, VP]),
@@ -88,7 +90,8 @@ def _load():
 
 
 _lib = _load()
-EXPORTED = ("kvsel_workspace_size", "kvsel_score", "kvsel_score_noalloc", "kvsel_combine_layers",
+EXPORTED = ("kvsel_workspace_size", "kvsel_score", "kvsel_score_noalloc", "kvsel_prefill_attention",
+            "kvsel_score_from_lse", "kvsel_combine_layers",
             "kvsel_aggregate", "kvsel_select", "kvsel_topk", "kvsel_compact", "kvsel_compact_layers",
             "kvsel_pagetable", "kvsel_attend_workspace_size", "kvsel_attend", "kvsel_read_device_error", "kvsel_selftest_bounded_wait", "kvsel_status_string",
             "kvsel_version", "kvsel_trace_enable", "kvsel_trace_read", "kvsel_launch_count")
@@ -155,6 +158,18 @@ def kvsel_score_noalloc(desc, q, k, scores, page_scores, stream=None):
 
 
 NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def kvsel_prefill_attention(desc, q, k, v, o, lse, lse_win, q_win, ws=None, stream=None):
+    _check(_lib.kvsel_prefill_attention(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                        _ptr(lse_win), _ptr(q_win), _ptr(ws), _stream(stream)),
+           "kvsel_prefill_attention")
+
+
+def kvsel_score_from_lse(desc, q_win, k, lse_win, scores, page_scores, ws, ws_bytes=None, stream=None):
+    nb = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    _check(_lib.kvsel_score_from_lse(ctypes.byref(desc), _ptr(q_win), _ptr(k), _ptr(lse_win), _ptr(scores),
+                                     _ptr(page_scores), _ptr(ws), nb, _stream(stream)), "kvsel_score_from_lse")
 
 
 def kvsel_combine_layers(desc, scores, layer_lo: int, layer_hi: int, combined, ws, ws_bytes=None, stream=None):

@@ -282,6 +282,16 @@ def make_inputs(w: Workload, device="cpu", with_mask: Optional[bool] = None) -> 
     return Inputs(w, qs, ks, vs, cs, mask, n_kv)
 
 
+def make_prompt_queries(w: Workload, b: int, device="cpu") -> torch.Tensor:
+    """Queries of every prompt row of sequence b for the prefill: [n_layers, h_q, L_b + W, d] bf16.
+    The last W rows are the observation-window queries of make_queries (same values); the prefix rows
+    are drawn from their own stream."""
+    L = w.prefix_lens[b]
+    g = torch.Generator(device=device).manual_seed(w.seed * 1_000_003 + b * 10_007 + 0x51A7)
+    pre = torch.randn((w.n_layers, w.h_q, L, w.head_dim), generator=g, device=device, dtype=torch.float32)
+    return torch.cat([pre.to(torch.bfloat16), make_queries(w, b, device).to(device)], dim=2)
+
+
 def make_decode_queries(w: Workload, n_q: int, device="cpu", seed_offset: int = 0) -> torch.Tensor:
     """Queries of n_q new tokens per head for attention over the selected cache:
     [batch, n_layers, h_q, n_q, d] bf16, N(0, 1)."""

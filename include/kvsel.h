@@ -117,6 +117,42 @@ KVSEL_API kvsel_status kvsel_score(const kvsel_desc* desc, const void* q, const 
                          void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * kvsel_prefill_attention — causal attention of every prompt row, with what the window scoring needs.
+ *
+ * o_i = sum over keys t <= i of softmax(q_i k_t / sqrt(d)) v_t for every row i of every query head
+ * (GQA map h -> h / (h_q / h_kv)), on the tensor cores.  CLAA, 'Complete flow and cost' (engineering
+ * detail 1): the keys that score the observation window are the prefill's own; the prefill's softmax
+ * forms each row's log-sum-exp, which is the first of the scoring's two passes for the window rows.
+ * So the call also writes the window rows' lse (base 2, units of z log2(e) / sqrt(d), in the order
+ * kvsel_score_from_lse reads) and the window queries; kvsel_score_from_lse then scores with one pass.
+ *
+ *   q, o     [device] bf16, per sequence b: [n_layers][h_q][L_b + W][d]; d = 128
+ *   k, v     [device] bf16 caches, layout above
+ *   lse      [device] fp32 out, natural-log lse of every row, layout of q without d (nullable)
+ *   lse_win  [device] fp32 out [batch][n_layers][h_kv][(h_q / h_kv) * W], row (h_local, j)
+ *   q_win    [device] bf16 out [batch][n_layers][h_q][W][d] (the layout kvsel_score reads)
+ *   ws       [device] workspace or NULL (error word for bounded waits)
+ */
+KVSEL_API kvsel_status kvsel_prefill_attention(const kvsel_desc* desc, const void* q, const void* k, const void* v,
+                                               void* o, float* lse, float* lse_win, void* q_win, void* ws,
+                                               cudaStream_t stream);
+
+/*
+ * kvsel_score_from_lse — kvsel_score with the window rows' lse given (from kvsel_prefill_attention).
+ *
+ * Computes what kvsel_score computes (softmax mode) with the second pass only: the column mass of
+ * the window probabilities 2^(z log2(e) / sqrt(d) - lse) for every prefix key, the group reduce,
+ * pooling and page reduce.  One read of the prefix keys instead of two.
+ *
+ *   q_win    [device] bf16 window queries, layout above
+ *   lse_win  [device] fp32, as kvsel_prefill_attention writes it
+ *   other arguments as for kvsel_score
+ */
+KVSEL_API kvsel_status kvsel_score_from_lse(const kvsel_desc* desc, const void* q_win, const void* k,
+                                            const float* lse_win, float* scores, float* page_scores, void* ws,
+                                            size_t ws_bytes, cudaStream_t stream);
+
+/*
  * kvsel_combine_layers — cross-layer aggregation of raw group scores.
  *
  * Each layer's scores of a (sequence, KV head) row are L1-normalised over the

@@ -1,0 +1,97 @@
+"""Causal prefill attention on the tensor cores against the fp64 oracle, and the window scores taken
+from its log-sum-exp (one pass over the prefix keys) against the oracle's scores.
+
+Tolerances: P is rounded to bf16 before the P V product and o is stored as bf16, so
+|o - oracle| <= 2^-9 * max|v| + 2^-8 * |oracle| (+1e-5); the lse is accumulated in fp32 from unrounded
+probabilities, |lse - oracle| <= 1e-4; scores as everywhere (1e-3 relative + 1e-6).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from attention_kv_cache_gb300 import synth as S
+from oracle import kvsel_oracle as O
+from tests.parity import assert_scores_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _ws(K, n, cuda):
+    buf = torch.zeros(n + K.WS_ALIGN, dtype=torch.uint8, device=cuda)
+    off = (-buf.data_ptr()) % K.WS_ALIGN
+    return buf[off:off + n]
+
+
+def _run_prefill(w, cuda):
+    from attention_kv_cache_gb300 import kvsel as K
+    from attention_kv_cache_gb300.pipeline import desc_for, pack
+    inp = S.make_inputs(w, "cpu")
+    qf = [S.make_prompt_queries(w, b, "cpu") for b in range(w.batch)]
+    _, k, v = pack(inp, cuda)
+    q = torch.cat([x.reshape(-1) for x in qf]).to(cuda)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.numel() // w.head_dim, dtype=torch.float32, device=cuda)
+    G, W = w.group, w.window
+    lse_win = torch.empty((w.batch, w.n_layers, w.h_kv, G * W), dtype=torch.float32, device=cuda)
+    q_win = torch.empty((w.batch, w.n_layers, w.h_q, W, w.head_dim), dtype=torch.bfloat16, device=cuda)
+    desc = desc_for(w)
+    ws = _ws(K, K.kvsel_workspace_size(desc), cuda)
+    K.kvsel_prefill_attention(desc, q, k, v, o, lse, lse_win, q_win, ws)
+    torch.cuda.synchronize()
+    assert K.kvsel_read_device_error(ws) == K.OK
+    return inp, qf, k, v, o, lse, lse_win, q_win, desc, ws
+
+
+def _check_prefill(w, inp, qf, o, lse, lse_win, q_win):
+    off = 0
+    for b in range(w.batch):
+        N = w.prefix_lens[b] + w.window
+        n = w.n_layers * w.h_q * N
+        ob = o[off * w.head_dim:(off + n) * w.head_dim].view(w.n_layers, w.h_q, N, w.head_dim).double().cpu().numpy()
+        lb = lse[off:off + n].view(w.n_layers, w.h_q, N).double().cpu().numpy()
+        for layer in range(w.n_layers):
+            qq = O._f64(qf[b][layer])
+            kk = O._f64(inp.k[b][layer])
+            vv = O._f64(inp.v[b][layer])
+            ref_o, ref_l = O.prefill_attention(qq, kk, vv)
+            bound = 2.0 ** -9 * np.abs(vv).max() + 2.0 ** -8 * np.abs(ref_o) + 1e-5
+            bad = np.abs(ob[layer] - ref_o) > bound
+            assert not bad.any(), f"o b{b} l{layer}: {bad.sum()} off, first {np.argwhere(bad)[0]}"
+            np.testing.assert_allclose(lb[layer], ref_l, rtol=0, atol=1e-4, err_msg=f"lse b{b} l{layer}")
+            L, W, G = w.prefix_lens[b], w.window, w.group
+            want_win = (ref_l[:, L:] / np.log(2.0)).reshape(w.h_kv, G * W)
+            np.testing.assert_allclose(lse_win[b, layer].double().cpu().numpy(), want_win, rtol=0, atol=2e-4)
+            assert torch.equal(q_win[b, layer].cpu(), qf[b][layer][:, L:])
+        off += n
+
+
+@pytest.mark.parametrize("name,w", [
+    ("one_seq_3_tiles", S.Workload("pf_small", 110, 2, 8, 2, 128, 16, (300,), k_keep=20)),
+    ("eleven_tiles_g4", S.Workload("pf_long", 111, 1, 4, 1, 128, 32, (1300,), k_keep=40, n_clusters=4)),
+    ("ragged_batch", S.Workload("pf_ragged", 112, 1, 4, 2, 128, 8, (200, 700), k_keep=16)),
+])
+def test_prefill_matches_oracle(name, w, cuda):
+    inp, qf, k, v, o, lse, lse_win, q_win, desc, ws = _run_prefill(w, cuda)
+    _check_prefill(w, inp, qf, o, lse, lse_win, q_win)
+
+
+def test_scores_from_prefill_lse(cuda):
+    """Window scores from the prefill's lse (one pass) equal the oracle's and the two-pass scores."""
+    from attention_kv_cache_gb300 import kvsel as K
+    w = S.scaled(S.LLAMA8B_128K_PAGED, n_layers=2, prefix_lens=[2560], n_clusters=8)
+    inp, qf, k, v, o, lse, lse_win, q_win, desc, ws = _run_prefill(w, cuda)
+    L, P = w.prefix_lens[0], w.page_size
+    scores = torch.empty(w.n_layers * w.h_kv * L, dtype=torch.float32, device=cuda)
+    pages = torch.empty(w.n_layers * w.h_kv * (-(-L // P)), dtype=torch.float32, device=cuda)
+    K.kvsel_score_from_lse(desc, q_win, k, lse_win, scores, pages, ws)
+    s2 = torch.empty_like(scores)
+    p2 = torch.empty_like(pages)
+    K.kvsel_score(desc, q_win, k, s2, p2, ws)
+    torch.cuda.synchronize()
+    assert K.kvsel_read_device_error(ws) == K.OK
+    ref = O.run_sequence(w, inp.q[0], inp.k[0], with_gather=False)
+    assert_scores_close(scores.view(w.n_layers, w.h_kv, L), ref["pooled"], "scores from the prefill lse")
+    assert_scores_close(pages.view(w.n_layers, w.h_kv, -1), ref["pages"], "pages from the prefill lse")
+    assert_scores_close(scores.view(w.n_layers, w.h_kv, L), s2.view(w.n_layers, w.h_kv, L).double().cpu().numpy(),
+                        "one pass against two passes")
