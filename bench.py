@@ -48,6 +48,9 @@ def parse():
     p.add_argument("--attend", action="store_true",
                    help="time attention over the selected pages in place (page table) against compact + dense")
     p.add_argument("--n-q", type=int, default=1, help="query rows per head for --attend")
+    p.add_argument("--prefill", action="store_true",
+                   help="time causal prefill attention and the selection scored from its lse (one pass) "
+                        "against the selection scored with two passes")
     return p.parse_args()
 
 
@@ -517,6 +520,104 @@ def run_attend(args):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- prefill with the window scores
+
+def measured_tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["bf16_tflops_sustained"]), "measured (sustained)"
+    return 1700.0, "fallback (sustained)"
+
+
+def run_prefill(args):
+    """Causal prefill attention of every prompt row (tensor cores), then the selection path scored from
+    the prefill's lse (one pass over the prefix keys), against the same selection scored with its own
+    two passes."""
+    import torch
+    from attention_kv_cache_gb300 import kvsel as K
+    from attention_kv_cache_gb300 import synth as S
+    from attention_kv_cache_gb300.pipeline import Pipeline, pack
+
+    w = S.by_name(args.workload if args.workload != DEFAULT_WORKLOAD else "llama8b_32l_h32x8_d128_L32768_W32")
+    w = w.with_(n_layers=args.layers or 4)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    inp = S.make_inputs(w, str(dev))
+    _, k, v = pack(inp, dev)
+    q = torch.cat([S.make_prompt_queries(w, b, str(dev)).reshape(-1) for b in range(w.batch)])
+    o = torch.empty_like(q)
+    G, W = w.group, w.window
+    lse_win = torch.empty((w.batch, w.n_layers, w.h_kv, G * W), dtype=torch.float32, device=dev)
+    q_win = torch.empty((w.batch, w.n_layers, w.h_q, W, w.head_dim), dtype=torch.bfloat16, device=dev)
+    pipe = Pipeline(w, dev)
+
+    def prefill():
+        K.kvsel_prefill_attention(pipe.desc, q, k, v, o, None, lse_win, q_win, pipe.ws)
+
+    def fused():
+        prefill()
+        K.kvsel_score_from_lse(pipe.desc_score, q_win, k, lse_win, pipe.scores, pipe.page_scores, pipe.ws,
+                               pipe.ws_bytes)
+        pipe.select()
+        pipe.compact(k, v)
+
+    def unfused():
+        prefill()
+        pipe.run(q_win, k, v)
+
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    for name, fn in (("prefill", prefill), ("fused", fused), ("unfused", unfused)):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        sampler = ClockSampler(0)
+        K.kvsel_trace_enable(True)
+        K.kvsel_trace_read()
+        n0 = K.kvsel_launch_count()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        trace = K.kvsel_trace_read()
+        K.kvsel_trace_enable(False)
+        res[name] = {"ms": e0.elapsed_time(e1) / args.steps, "launches": K.kvsel_launch_count() - n0,
+                     "clocks": sampler.stop(),
+                     "kernels": {n: {"launches": c, "ms": round(t, 4)} for n, (c, t) in trace.items()}}
+    assert K.kvsel_read_device_error(pipe.ws) == K.OK
+    # causal flops: Q K^T and P V over keys t <= i, 2 flops per multiply-add
+    flops = sum(4.0 * w.n_layers * w.h_q * (L + W) * (L + W + 1) / 2 * w.head_dim for L in w.prefix_lens)
+    pf = res["prefill"]["kernels"]["prefill_tc"]
+    pf_ms = pf["ms"] / pf["launches"]
+    peak, peak_src = measured_tensor_peak()
+    achieved = flops / (pf_ms / 1e3) / 1e12
+    tokens = sum(L for L in w.prefix_lens) * w.n_layers
+    line = {
+        "metric": "causal prefill attention TFLOP/s (bf16 in, fp32 accumulate), with the window scores' lse",
+        "value": achieved, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": res["prefill"]["ms"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 inputs, f32 accumulate", "data": "synthetic",
+        "config": {"workload": w.name, "layers": w.n_layers, "h_q": w.h_q, "h_kv": w.h_kv, "d": w.head_dim,
+                   "prompt_len": [L + W for L in w.prefix_lens], "causal_flops_per_step": flops},
+        "clocks": res["prefill"]["clocks"], "gpu_launches": res["prefill"]["launches"],
+        "kernels": res["prefill"]["kernels"],
+        "roofline": {"bound": "tensor", "kernel": "prefill_tc", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                     "traffic": None, "algorithmic_flops": flops},
+        "selection_after_prefill": {
+            "fused_ms_per_step": res["fused"]["ms"], "unfused_ms_per_step": res["unfused"]["ms"],
+            "fused_kernels": res["fused"]["kernels"], "unfused_kernels": res["unfused"]["kernels"],
+            "selection_ms_fused": res["fused"]["ms"] - res["prefill"]["ms"],
+            "selection_ms_unfused": res["unfused"]["ms"] - res["prefill"]["ms"],
+            "prefix_tokens_per_s_fused": tokens / ((res["fused"]["ms"] - res["prefill"]["ms"]) / 1e3)},
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- the oracle arm
 
 def run_reference(args):
@@ -557,5 +658,7 @@ if __name__ == "__main__":
         run_reference(a)
     elif a.attend:
         run_attend(a)
+    elif a.prefill:
+        run_prefill(a)
     else:
         run_kvsel(a)
