@@ -30,8 +30,8 @@ constexpr int kPfThreads = 192;
 constexpr int kPfTile = 128;
 constexpr uint32_t kQOff = 0, kPOff = 32768, kKVOff = 65536, kStageBytes = 65536;
 constexpr uint32_t kBarOff = kKVOff + 2 * kStageBytes;               // 196608
-// barriers: kv_full[2], kv_empty[2], s_full[2], s_empty[2], p_full, pv_done, q_full, drain
-constexpr uint32_t kNumBars = 12;
+// barriers: k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2], p_full, pv_done, q_full, drain
+constexpr uint32_t kNumBars = 16;
 constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
 constexpr size_t kPfSmem = kMiscOff + 16 + 1024;
 constexpr uint32_t kSCol = 0, kOCol = 256;                          // TMEM: S buffers 0..255, O 256..383
@@ -50,6 +50,12 @@ struct PfArgs {
   int32_t n_qt_max;
   int64_t q_row0[KVSEL_MAX_BATCH];   // first row of each sequence in the q / o row view
 };
+
+__device__ __forceinline__ float fast_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ bool pf_aborted(const volatile uint32_t* f) { return *f != 0; }
 __device__ __forceinline__ void pf_fail(const PfArgs& a, volatile uint32_t* f, uint32_t where) {
@@ -79,19 +85,23 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t base = smem_addr(sbase);
   const uint32_t bars = base + kBarOff;
-  auto kv_full = [&](int s) { return bars + 8u * s; };
-  auto kv_empty = [&](int s) { return bars + 8u * (2 + s); };
-  auto s_full = [&](int s) { return bars + 8u * (4 + s); };
-  auto s_empty = [&](int s) { return bars + 8u * (6 + s); };
-  const uint32_t p_full = bars + 64, pv_done = bars + 72, q_full = bars + 80, drain = bars + 88;
+  auto k_full = [&](int s) { return bars + 8u * s; };
+  auto k_empty = [&](int s) { return bars + 8u * (2 + s); };
+  auto v_full = [&](int s) { return bars + 8u * (4 + s); };
+  auto v_empty = [&](int s) { return bars + 8u * (6 + s); };
+  auto s_full = [&](int s) { return bars + 8u * (8 + s); };
+  auto s_empty = [&](int s) { return bars + 8u * (10 + s); };
+  const uint32_t p_full = bars + 96, pv_done = bars + 104, q_full = bars + 112, drain = bars + 120;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sbase + kMiscOff);
   volatile uint32_t* flag = reinterpret_cast<volatile uint32_t*>(sbase + kMiscOff + 4);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
-      mbar_init(kv_full(s), 1);
-      mbar_init(kv_empty(s), 1);
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), 1);
       mbar_init(s_full(s), 1);
       mbar_init(s_empty(s), 4);           // one arrival per softmax warp
     }
@@ -119,25 +129,31 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       mbar_expect_tx(q_full, 32768);
       tma_load_2d(base + kQOff, &tq, 0, (int32_t)qrow0, q_full);
       tma_load_2d(base + kQOff + 16384, &tq, 64, (int32_t)qrow0, q_full);
-      int fills = 0;
+      // K tiles are freed by their S product, V tiles by their P V product: two rings, filled in
+      // tile order (K_j, V_j, K_j+1, ...)
+      int kfills = 0, vfills = 0;
       for (int j = 0; j < nt; ++j) {
         const int s = j & 1;
-        if (pf_aborted(flag) || !mbar_wait(kv_empty(s), ((j >> 1) & 1) ^ 1)) { pf_fail(a, flag, kPfProducer); break; }
         const uint32_t st = base + kKVOff + s * kStageBytes;
         const int32_t kr = (int32_t)(krow0 + (int64_t)j * kPfTile);
-        mbar_expect_tx(kv_full(s), 65536);
-        tma_load_2d(st, &tk, 0, kr, kv_full(s));
-        tma_load_2d(st + 16384, &tk, 64, kr, kv_full(s));
-        tma_load_2d(st + 32768, &tv, 0, kr, kv_full(s));
-        tma_load_2d(st + 49152, &tv, 64, kr, kv_full(s));
-        ++fills;
+        if (pf_aborted(flag) || !mbar_wait(k_empty(s), ((j >> 1) & 1) ^ 1)) { pf_fail(a, flag, kPfProducer); break; }
+        mbar_expect_tx(k_full(s), 32768);
+        tma_load_2d(st, &tk, 0, kr, k_full(s));
+        tma_load_2d(st + 16384, &tk, 64, kr, k_full(s));
+        ++kfills;
+        if (pf_aborted(flag) || !mbar_wait(v_empty(s), ((j >> 1) & 1) ^ 1)) { pf_fail(a, flag, kPfProducer); break; }
+        mbar_expect_tx(v_full(s), 32768);
+        tma_load_2d(st + 32768, &tv, 0, kr, v_full(s));
+        tma_load_2d(st + 49152, &tv, 64, kr, v_full(s));
+        ++vfills;
       }
       // copies still in flight (only after an abort) land before the CTA exits
-      for (int s = 0; s < 2; ++s)
-        if (fills > s) {
-          const int cnt = (fills - s + 1) / 2;
-          if (!mbar_wait(kv_full(s), (cnt - 1) & 1)) set_device_error(a.err, KVSEL_ERR_TIMEOUT, kPfDrain);
-        }
+      for (int s = 0; s < 2; ++s) {
+        if (kfills > s && !mbar_wait(k_full(s), (((kfills - s + 1) / 2) - 1) & 1))
+          set_device_error(a.err, KVSEL_ERR_TIMEOUT, kPfDrain);
+        if (vfills > s && !mbar_wait(v_full(s), (((vfills - s + 1) / 2) - 1) & 1))
+          set_device_error(a.err, KVSEL_ERR_TIMEOUT, kPfDrain);
+      }
       if (!mbar_wait(q_full, 0)) set_device_error(a.err, KVSEL_ERR_TIMEOUT, kPfDrain);
     }
   } else if (warp == 1) {
@@ -148,7 +164,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       bool issued = false;
       auto issue_s = [&](int j) -> bool {
         const int s = j & 1;
-        if (pf_aborted(flag) || !mbar_wait(kv_full(s), (j >> 1) & 1) || !mbar_wait(s_empty(s), ((j >> 1) & 1) ^ 1))
+        if (pf_aborted(flag) || !mbar_wait(k_full(s), (j >> 1) & 1) || !mbar_wait(s_empty(s), ((j >> 1) & 1) ^ 1))
           return false;
         tc_fence_after();
         const uint32_t sk = base + kKVOff + s * kStageBytes;
@@ -159,13 +175,19 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                     umma_desc_sw128(sk + kb * 16384 + off), idesc_s, kk > 0);
         }
         umma_commit(s_full(s));
+        umma_commit(k_empty(s));
         issued = true;
         return true;
       };
+      // S for the next two tiles is always in flight; the P V product of tile j comes first once its
+      // P is ready, then S of tile j + 2 (whose K tile was loading meanwhile)
       if (ok) ok = issue_s(0);
+      if (ok && nt > 1) ok = issue_s(1);
       for (int j = 0; j < nt && ok; ++j) {
-        if (j + 1 < nt && !issue_s(j + 1)) { ok = false; break; }
-        if (pf_aborted(flag) || !mbar_wait(p_full, j & 1)) { ok = false; break; }
+        if (pf_aborted(flag) || !mbar_wait(p_full, j & 1) || !mbar_wait(v_full(j & 1), (j >> 1) & 1)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t sv = base + kKVOff + (j & 1) * kStageBytes + 32768;
 #pragma unroll
@@ -174,8 +196,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
           umma_bf16(tmem + kOCol, umma_desc_sw128(base + kPOff + kb * 16384 + off),
                     umma_desc_sw128_mn(sv + kk * 2048, 16384), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(kv_empty(j & 1));
+        umma_commit(v_empty(j & 1));
         umma_commit(pv_done);
+        if (j + 2 < nt && !issue_s(j + 2)) { ok = false; break; }
       }
       if (!ok) pf_fail(a, flag, kPfMma);
       if (issued) {
@@ -206,28 +229,43 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_empty(s));
-      // causal mask: key j * 128 + c is visible to row i when it is not after it
-      const int vis = i - j * kPfTile + 1;                          // visible columns (>= 128 off the diagonal)
-      float mt = -INFINITY;
+      // scale; causal mask on the diagonal tile (key j * 128 + c is visible to row i when c < i - 128 j + 1)
+      if (j == nt - 1) {
+        const int vis = i - j * kPfTile + 1;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        v[c] = c < vis ? v[c] * scale : -INFINITY;
-        mt = fmaxf(mt, v[c]);
+        for (int c = 0; c < 128; ++c) v[c] = c < vis ? v[c] * scale : -INFINITY;
+      } else {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) v[c] *= scale;
       }
-      const float m_new = fmaxf(m, mt);
-      const float alpha = m == -INFINITY ? 0.f : exp2f(m - m_new);
-      float sum = 0.f;
+      float mp[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mp[k] = v[k];
+#pragma unroll
+      for (int c = 8; c < 128; ++c) mp[c & 7] = fmaxf(mp[c & 7], v[c]);
+      const float mt = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+      // lazy rescale: the exponent offset m moves only when the tile's max exceeds it by more than
+      // 2^8, so O is rescaled in TMEM rarely (the probabilities stay below 256; the lse is m + log2 l
+      // whatever m is)
+      float alpha = 1.f;
+      if (mt > m + 8.f) {
+        alpha = m == -INFINITY ? 0.f : fast_ex2(m - mt);
+        m = mt;
+      }
+      float sp[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) sp[k] = 0.f;
       uint32_t pk[64];
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        const float p0 = m_new == -INFINITY ? 0.f : exp2f(v[2 * c] - m_new);
-        const float p1 = m_new == -INFINITY ? 0.f : exp2f(v[2 * c + 1] - m_new);
-        sum += p0 + p1;
+        const float p0 = fast_ex2(v[2 * c] - m);
+        const float p1 = fast_ex2(v[2 * c + 1] - m);
+        sp[c & 7] += p0 + p1;
         const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
         pk[c] = *reinterpret_cast<const uint32_t*>(&pb);
       }
+      const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
       l = l * alpha + sum;
-      m = m_new;
       // P and O may be touched once the previous tile's P V product is done
       if (j > 0) {
         ok = __all_sync(0xffffffffu, !pf_aborted(flag) && mbar_wait(pv_done, (j - 1) & 1));
