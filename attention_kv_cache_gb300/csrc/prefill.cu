@@ -7,12 +7,20 @@
 // this kernel writes, besides o and the lse of every row, the window rows' lse (in the scoring's
 // layout, base-2 units) and their queries, and the scoring then needs its second pass only.
 //
-// One CTA per (sequence, layer, query head, 128-row query tile), heaviest tiles first.  Warp 0
-// issues TMA (the Q tile once; K and V tiles through a two-stage ring), warp 1 issues UMMA
-// (S = Q K^T into one of two TMEM buffers; O += P V into a TMEM accumulator, V as an MN-major
-// operand), warps 2..5 own one query row per thread: they read S from TMEM, apply the causal mask,
-// keep the online (max, sum), write P as bf16 into shared memory in the swizzled K-major layout the
-// UMMA reads, and rescale O in TMEM when a row's max grows.  All waits are bounded.
+// One CTA per (sequence, layer, query head, pair of consecutive 128-row query tiles A and B),
+// heaviest pairs first.  The two tiles share every K and V tile; while one tile's softmax runs, the
+// tensor cores work on the other's products.  Warp 0 issues TMA (both Q tiles once; K and V tiles
+// through two-stage rings); warp 1 issues UMMA: S_X = Q_X K^T into TMEM, O_X += P_X V with P_X read
+// from TMEM (written there over S_X by the softmax) and V as an MN-major shared-memory operand.
+// The eight steps of one product form a dependent accumulation chain, which the tensor pipe runs
+// well below its rate; two independent products issued step by step in alternation run near it.
+// Tile B trails tile A by one S product, so that B's P V of step j becomes ready when A's P V of
+// step j completes, i.e. when A's next S may start: those two are issued interleaved, and the
+// order per step is P_A V, (P_B V | S_A of the next step), S_B of the next step.  Warps 2..5
+// (tile A) and 6..9 (tile B) own one query row per thread: they read S from TMEM, apply the causal
+// mask, keep an exponent offset that moves only past 2^8 (so O is rescaled in TMEM rarely), and
+// store P as bf16 pairs.  A tile's next S is issued only after its P V product has completed, which
+// orders every reuse of its TMEM columns.  All waits are bounded.
 #include <cudaTypedefs.h>
 
 #include <cstring>
@@ -26,15 +34,17 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kPfThreads = 192;
+constexpr int kPfThreads = 320;
 constexpr int kPfTile = 128;
-constexpr uint32_t kQOff = 0, kPOff = 32768, kKVOff = 65536, kStageBytes = 65536;
-constexpr uint32_t kBarOff = kKVOff + 2 * kStageBytes;               // 196608
-// barriers: k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2], p_full, pv_done, q_full, drain
+// shared memory: Q_A | Q_B | K stages | V stages (32 KB each), then barriers
+constexpr uint32_t kQOff = 0, kKOff = 65536, kVOff = 131072, kTileBytes = 32768;
+constexpr uint32_t kBarOff = 196608;
+// barriers: k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done[2], q_full, drain
 constexpr uint32_t kNumBars = 16;
 constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
 constexpr size_t kPfSmem = kMiscOff + 16 + 1024;
-constexpr uint32_t kSCol = 0, kOCol = 256;                          // TMEM: S buffers 0..255, O 256..383
+// TMEM: tile X in {0, 1}: S (P over its first 64 columns) at 256 X, O at 256 X + 128
+constexpr uint32_t kSCol = 0, kOCol = 128, kTileCols = 256;
 
 enum : uint32_t { kPfProducer = 11, kPfMma = 12, kPfSoftmax = 13, kPfDrain = 14 };
 
@@ -47,7 +57,7 @@ struct PfArgs {
   float* lse_win;               // base-2 lse of the window rows, [batch][layers][h_kv][G * W]
   __nv_bfloat16* q_win;         // window queries, [batch][layers][h_q][W][d]
   DeviceError* err;
-  int32_t n_qt_max;
+  int32_t n_pairs;              // query-tile pairs of the longest sequence
   int64_t q_row0[KVSEL_MAX_BATCH];   // first row of each sequence in the q / o row view
 };
 
@@ -63,6 +73,49 @@ __device__ __forceinline__ void pf_fail(const PfArgs& a, volatile uint32_t* f, u
   *f = 1;
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Largest of 64 raw logits (three-input max: 36 instructions).
+__device__ __forceinline__ float max64(const float* v) {
+  float mp[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float* c = v + 8 * k;
+    mp[k] = fmaxf(fmax3(fmax3(c[0], c[1], c[2]), c[3], c[4]), fmax3(c[5], c[6], c[7]));
+  }
+  return fmax3(fmax3(mp[0], mp[1], mp[2]), fmax3(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
+}
+
+// Causal mask of 64 raw logits of keys key0 .. key0 + 63 for row i: keys after i become -inf.
+__device__ __forceinline__ void mask64(float* v, int key0, int i) {
+  const int vis = i - key0 + 1;
+#pragma unroll
+  for (int c = 0; c < 64; ++c) v[c] = c < vis ? v[c] : -INFINITY;
+}
+
+// 2^(scale v - m) of 64 raw logits, two per packed fma: their sum, and the bf16 pairs in 32 words
+// (even key in the low half).  pk may be v's own registers: word c is written after v[2c] and
+// v[2c + 1] are read.
+__device__ __forceinline__ float exp_pack64(const float* v, float2 sc, float2 nm, uint32_t* pk) {
+  float2 sp[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) sp[k] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    const float2 t = __ffma2_rn(make_float2(v[2 * c], v[2 * c + 1]), sc, nm);
+    const float2 p = make_float2(fast_ex2(t.x), fast_ex2(t.y));
+    sp[c & 3] = __fadd2_rn(sp[c & 3], p);
+    const __nv_bfloat162 pb = __floats2bfloat162_rn(p.x, p.y);
+    pk[c] = *reinterpret_cast<const uint32_t*>(&pb);
+  }
+  const float2 s = __fadd2_rn(__fadd2_rn(sp[0], sp[1]), __fadd2_rn(sp[2], sp[3]));
+  return s.x + s.y;
+}
+
 __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap tq,
                                                                 const __grid_constant__ CUtensorMap tk,
                                                                 const __grid_constant__ CUtensorMap tv,
@@ -70,7 +123,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                                                                 const __grid_constant__ SeqTable t) {
   constexpr int D = 128;
   const int heads_total = a.batch * a.n_layers * a.h_q;
-  const int qt = a.n_qt_max - 1 - (int)(blockIdx.x / heads_total);   // heaviest tiles first
+  const int pair = a.n_pairs - 1 - (int)(blockIdx.x / heads_total);   // heaviest pairs first
   const int hrem = (int)(blockIdx.x % heads_total);
   const int b = hrem / (a.n_layers * a.h_q);
   const int layer = (hrem / a.h_q) % a.n_layers;
@@ -78,8 +131,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   const int g = h / a.G;
   const SeqInfo& si = t.s[b];
   const int N = si.n_keys;
-  if (qt * kPfTile >= N) return;                                      // this sequence is shorter
-  const int nt = qt + 1;                                               // causal: K tiles 0 .. qt
+  const int qa = 2 * pair;
+  if (qa * kPfTile >= N) return;                                       // this sequence is shorter
+  const int nq = (qa + 1) * kPfTile < N ? 2 : 1;                        // query tiles in this CTA
+  const int nt_x[2] = {qa + 1, qa + 2};                                 // K tiles of tile A, B (causal)
+  const int nt = nt_x[nq - 1];
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -89,9 +145,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   auto k_empty = [&](int s) { return bars + 8u * (2 + s); };
   auto v_full = [&](int s) { return bars + 8u * (4 + s); };
   auto v_empty = [&](int s) { return bars + 8u * (6 + s); };
-  auto s_full = [&](int s) { return bars + 8u * (8 + s); };
-  auto s_empty = [&](int s) { return bars + 8u * (10 + s); };
-  const uint32_t p_full = bars + 96, pv_done = bars + 104, q_full = bars + 112, drain = bars + 120;
+  auto s_full = [&](int x) { return bars + 8u * (8 + x); };
+  auto p_full = [&](int x) { return bars + 8u * (10 + x); };
+  auto pv_done = [&](int x) { return bars + 8u * (12 + x); };
+  const uint32_t q_full = bars + 112, drain = bars + 120;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(sbase + kMiscOff);
   volatile uint32_t* flag = reinterpret_cast<volatile uint32_t*>(sbase + kMiscOff + 4);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -99,14 +156,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
       mbar_init(k_full(s), 1);
-      mbar_init(k_empty(s), 1);
+      mbar_init(k_empty(s), nq);          // freed by the S product of every tile that reads it
       mbar_init(v_full(s), 1);
-      mbar_init(v_empty(s), 1);
+      mbar_init(v_empty(s), nq);          // freed by the P V product of every tile that reads it
       mbar_init(s_full(s), 1);
-      mbar_init(s_empty(s), 4);           // one arrival per softmax warp
+      mbar_init(p_full(s), 4);            // one arrival per softmax warp of the tile
+      mbar_init(pv_done(s), 1);
     }
-    mbar_init(p_full, 4);
-    mbar_init(pv_done, 1);
     mbar_init(q_full, 1);
     mbar_init(drain, 1);
     *flag = 0;
@@ -118,7 +174,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tmem = *tslot;
 
-  const int64_t qrow0 = a.q_row0[b] + ((int64_t)layer * a.h_q + h) * N + (int64_t)qt * kPfTile;
+  const int64_t qrow_base = a.q_row0[b] + ((int64_t)layer * a.h_q + h) * N;
   const int64_t krow0 = si.k_off / D + ((int64_t)layer * a.h_kv + g) * N;
 
   if (warp == 0) {
@@ -126,25 +182,27 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
-      mbar_expect_tx(q_full, 32768);
-      tma_load_2d(base + kQOff, &tq, 0, (int32_t)qrow0, q_full);
-      tma_load_2d(base + kQOff + 16384, &tq, 64, (int32_t)qrow0, q_full);
-      // K tiles are freed by their S product, V tiles by their P V product: two rings, filled in
+      mbar_expect_tx(q_full, 32768u * nq);
+      for (int x = 0; x < nq; ++x) {
+        const int32_t qr = (int32_t)(qrow_base + (int64_t)(qa + x) * kPfTile);
+        tma_load_2d(base + kQOff + x * kTileBytes, &tq, 0, qr, q_full);
+        tma_load_2d(base + kQOff + x * kTileBytes + 16384, &tq, 64, qr, q_full);
+      }
+      // K tiles are freed by their S products, V tiles by their P V products: two rings, filled in
       // tile order (K_j, V_j, K_j+1, ...)
       int kfills = 0, vfills = 0;
       for (int j = 0; j < nt; ++j) {
         const int s = j & 1;
-        const uint32_t st = base + kKVOff + s * kStageBytes;
         const int32_t kr = (int32_t)(krow0 + (int64_t)j * kPfTile);
         if (pf_aborted(flag) || !mbar_wait(k_empty(s), ((j >> 1) & 1) ^ 1)) { pf_fail(a, flag, kPfProducer); break; }
         mbar_expect_tx(k_full(s), 32768);
-        tma_load_2d(st, &tk, 0, kr, k_full(s));
-        tma_load_2d(st + 16384, &tk, 64, kr, k_full(s));
+        tma_load_2d(base + kKOff + s * kTileBytes, &tk, 0, kr, k_full(s));
+        tma_load_2d(base + kKOff + s * kTileBytes + 16384, &tk, 64, kr, k_full(s));
         ++kfills;
         if (pf_aborted(flag) || !mbar_wait(v_empty(s), ((j >> 1) & 1) ^ 1)) { pf_fail(a, flag, kPfProducer); break; }
         mbar_expect_tx(v_full(s), 32768);
-        tma_load_2d(st + 32768, &tv, 0, kr, v_full(s));
-        tma_load_2d(st + 49152, &tv, 64, kr, v_full(s));
+        tma_load_2d(base + kVOff + s * kTileBytes, &tv, 0, kr, v_full(s));
+        tma_load_2d(base + kVOff + s * kTileBytes + 16384, &tv, 64, kr, v_full(s));
         ++vfills;
       }
       // copies still in flight (only after an abort) land before the CTA exits
@@ -157,48 +215,77 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       if (!mbar_wait(q_full, 0)) set_device_error(a.err, KVSEL_ERR_TIMEOUT, kPfDrain);
     }
   } else if (warp == 1) {
+    // The K (V) tile of the last step is read by tile B alone: its stage sees one of nq releases,
+    // and is never refilled.
     if (lane == 0) {
       constexpr uint32_t idesc_s = umma_idesc_bf16(128, 128);
       constexpr uint32_t idesc_o = umma_idesc_bf16(128, 128) | kUmmaBMajorMN;
-      bool ok = mbar_wait(q_full, 0);
+      const int ntA = nt_x[0], ntB = nq == 2 ? nt_x[1] : 0;
+      bool ok = mbar_wait_spin(q_full, 0);
       bool issued = false;
-      auto issue_s = [&](int j) -> bool {
-        const int s = j & 1;
-        if (pf_aborted(flag) || !mbar_wait(k_full(s), (j >> 1) & 1) || !mbar_wait(s_empty(s), ((j >> 1) & 1) ^ 1))
-          return false;
-        tc_fence_after();
-        const uint32_t sk = base + kKVOff + s * kStageBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t kb = kk >> 2, off = (kk & 3) * 32;
-          umma_bf16(tmem + kSCol + s * 128, umma_desc_sw128(base + kQOff + kb * 16384 + off),
-                    umma_desc_sw128(sk + kb * 16384 + off), idesc_s, kk > 0);
-        }
-        umma_commit(s_full(s));
-        umma_commit(k_empty(s));
+      // S_x(j) may start once the tile's P V product of step j - 1 (which reads the same TMEM
+      // columns) has completed and K_j has landed; P_x(j) V_j once the softmax has written P_x(j)
+      // and V_j has landed.
+      auto s_ready = [&](int x, int j) {
+        return !pf_aborted(flag) && (j == 0 || mbar_wait_spin(pv_done(x), (j - 1) & 1)) &&
+               mbar_wait_spin(k_full(j & 1), (j >> 1) & 1);
+      };
+      auto pv_ready = [&](int x, int j) {
+        return !pf_aborted(flag) && mbar_wait_spin(p_full(x), j & 1) && mbar_wait_spin(v_full(j & 1), (j >> 1) & 1);
+      };
+      auto s_step = [&](int x, int j, int kk) {
+        const uint32_t sq = base + kQOff + x * kTileBytes, sk = base + kKOff + (j & 1) * kTileBytes;
+        const uint32_t kb = kk >> 2, off = (kk & 3) * 32;
+        umma_bf16(tmem + x * kTileCols + kSCol, umma_desc_sw128(sq + kb * 16384 + off),
+                  umma_desc_sw128(sk + kb * 16384 + off), idesc_s, kk > 0);
+      };
+      auto pv_step = [&](int x, int j, int kk) {
+        const uint32_t sv = base + kVOff + (j & 1) * kTileBytes;
+        umma_bf16_ta(tmem + x * kTileCols + kOCol, tmem + x * kTileCols + kSCol + kk * 8,
+                     umma_desc_sw128_mn(sv + kk * 2048, 16384), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+      };
+      // a commit tracks every product issued before it, so each signals no earlier than its own
+      auto s_issued = [&](int x, int j) {
+        umma_commit(s_full(x));
+        umma_commit(k_empty(j & 1));
         issued = true;
+      };
+      auto pv_issued = [&](int x, int j) {
+        umma_commit(pv_done(x));
+        umma_commit(v_empty(j & 1));
+      };
+      auto s_alone = [&](int x, int j) -> bool {
+        if (!s_ready(x, j)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) s_step(x, j, kk);
+        s_issued(x, j);
         return true;
       };
-      // S for the next two tiles is always in flight; the P V product of tile j comes first once its
-      // P is ready, then S of tile j + 2 (whose K tile was loading meanwhile)
-      if (ok) ok = issue_s(0);
-      if (ok && nt > 1) ok = issue_s(1);
+      ok = ok && s_alone(0, 0);
+      if (ntB > 0) ok = ok && s_alone(1, 0);
       for (int j = 0; j < nt && ok; ++j) {
-        if (pf_aborted(flag) || !mbar_wait(p_full, j & 1) || !mbar_wait(v_full(j & 1), (j >> 1) & 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t sv = base + kKVOff + (j & 1) * kStageBytes + 32768;
+        if (j < ntA) {
+          if (!(ok = pv_ready(0, j))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kPfTile / 16; ++kk) {
-          const uint32_t kb = kk >> 2, off = (kk & 3) * 32;
-          umma_bf16(tmem + kOCol, umma_desc_sw128(base + kPOff + kb * 16384 + off),
-                    umma_desc_sw128_mn(sv + kk * 2048, 16384), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kPfTile / 16; ++kk) pv_step(0, j, kk);
+          pv_issued(0, j);
         }
-        umma_commit(v_empty(j & 1));
-        umma_commit(pv_done);
-        if (j + 2 < nt && !issue_s(j + 2)) { ok = false; break; }
+        const bool pvb = j < ntB, sa = j + 1 < ntA;
+        if (pvb && !(ok = pv_ready(1, j))) break;
+        if (sa && !(ok = s_ready(0, j + 1))) break;
+        if (pvb || sa) {
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            if (pvb) pv_step(1, j, kk);
+            if (sa) s_step(0, j + 1, kk);
+          }
+          if (pvb) pv_issued(1, j);
+          if (sa) s_issued(0, j + 1);
+        }
+        if (j + 1 < ntB) ok = s_alone(1, j + 1);
       }
       if (!ok) pf_fail(a, flag, kPfMma);
       if (issued) {
@@ -207,101 +294,70 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       }
     }
   } else {
-    // softmax / epilogue: thread = query row of the tile
+    // softmax / epilogue: warpgroup x = tile, thread = query row of the tile
+    const int x = (warp - 2) / 4;
     const int quarter = warp % 4;
     const int row = quarter * 32 + lane;
+    const int qt = qa + x;
     const int i = qt * kPfTile + row;                               // row index in the sequence
-    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + x * kTileCols;
     const float scale = a.scale_log2;
+    const int ntx = x < nq ? nt_x[x] : 0;
     float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < nt; ++j) {
-      const int s = j & 1;
-      ok = __all_sync(0xffffffffu, ok && !pf_aborted(flag) && mbar_wait(s_full(s), (j >> 1) & 1));
+    bool ok = x < nq;
+    for (int j = 0; j < ntx; ++j) {
+      ok = __all_sync(0xffffffffu, ok && !pf_aborted(flag) && mbar_wait_spin(s_full(x), j & 1));
       if (!ok) {
         if (lane == 0) pf_fail(a, flag, kPfSoftmax);
         break;
       }
       tc_fence_after();
-      float v[128];
-      tmem_ld64(lane_base + kSCol + s * 128, v);
-      tmem_ld64(lane_base + kSCol + s * 128 + 64, v + 64);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_empty(s));
-      // scale; causal mask on the diagonal tile (key j * 128 + c is visible to row i when c < i - 128 j + 1)
-      if (j == nt - 1) {
-        const int vis = i - j * kPfTile + 1;
-#pragma unroll
-        for (int c = 0; c < 128; ++c) v[c] = c < vis ? v[c] * scale : -INFINITY;
-      } else {
-#pragma unroll
-        for (int c = 0; c < 128; ++c) v[c] *= scale;
+      const bool diag = j == ntx - 1;
+      // both halves of the S row; P then goes over the columns already read (keys 0..63 into
+      // columns 0..31, keys 64..127 into 32..63), packed in place into the same registers
+      uint32_t rv[64], rw[64];
+      tmem_ld64_async(lane_base + kSCol + 64, rv);
+      tmem_wait_ld64(rv);
+      tmem_ld64_async(lane_base + kSCol, rw);
+      tmem_wait_ld64(rw);
+      float* v = reinterpret_cast<float*>(rv);
+      float* w = reinterpret_cast<float*>(rw);
+      if (diag) {
+        mask64(v, j * kPfTile + 64, i);
+        mask64(w, j * kPfTile, i);
       }
-      float mp[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) mp[k] = v[k];
-#pragma unroll
-      for (int c = 8; c < 128; ++c) mp[c & 7] = fmaxf(mp[c & 7], v[c]);
-      const float mt = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])), fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
-      // lazy rescale: the exponent offset m moves only when the tile's max exceeds it by more than
-      // 2^8, so O is rescaled in TMEM rarely (the probabilities stay below 256; the lse is m + log2 l
-      // whatever m is)
+      const float mt = fmaxf(max64(v), max64(w)) * scale;         // scale > 0: max commutes
+      // lazy rescale: the exponent offset moves only when the tile's max exceeds it by more than 2^8
       float alpha = 1.f;
       if (mt > m + 8.f) {
         alpha = m == -INFINITY ? 0.f : fast_ex2(m - mt);
         m = mt;
       }
-      float sp[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) sp[k] = 0.f;
-      uint32_t pk[64];
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float p0 = fast_ex2(v[2 * c] - m);
-        const float p1 = fast_ex2(v[2 * c + 1] - m);
-        sp[c & 7] += p0 + p1;
-        const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-        pk[c] = *reinterpret_cast<const uint32_t*>(&pb);
-      }
-      const float sum = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+      const float2 sc = make_float2(scale, scale), nm = make_float2(-m, -m);
+      float sum = exp_pack64(w, sc, nm, rw);
+      tmem_st32(lane_base + kSCol, rw);
+      sum += exp_pack64(v, sc, nm, rv);
+      tmem_st32(lane_base + kSCol + 32, rv);
       l = l * alpha + sum;
-      // P and O may be touched once the previous tile's P V product is done
-      if (j > 0) {
-        ok = __all_sync(0xffffffffu, !pf_aborted(flag) && mbar_wait(pv_done, (j - 1) & 1));
-        if (!ok) {
-          if (lane == 0) pf_fail(a, flag, kPfSoftmax);
-          break;
-        }
-        tc_fence_after();
-      }
-      // P row into the swizzled K-major tile: 64-key block kb at +16 KB, 16-byte chunk c at c ^ (row & 7)
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int kb = c >> 3, cc = c & 7;
-        uint4 w = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        *reinterpret_cast<uint4*>(sbase + kPOff + kb * 16384 + row * 128 + ((cc ^ (row & 7)) * 16)) = w;
-      }
-      // rescale the running O when this row's max grew (warp-wide decision: the TMEM access is collective)
+      // O is final for tile j - 1 here (this tile's S was issued after that P V product completed)
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        uint32_t r[64];
+        uint32_t* r = rv;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          tmem_ld64_async(lane_base + kOCol + half * 64, r);
+        for (int hh = 0; hh < 2; ++hh) {
+          tmem_ld64_async(lane_base + kOCol + hh * 64, r);
           tmem_wait_ld64(r);
 #pragma unroll
           for (int c = 0; c < 64; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * alpha);
-          tmem_st64(lane_base + kOCol + half * 64, r);
+          tmem_st64(lane_base + kOCol + hh * 64, r);
         }
-        tmem_wait_st();
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(p_full(x));
     }
     if (ok) {
-      ok = __all_sync(0xffffffffu, !pf_aborted(flag) && mbar_wait(pv_done, (nt - 1) & 1));
+      ok = __all_sync(0xffffffffu, !pf_aborted(flag) && mbar_wait(pv_done(x), (ntx - 1) & 1));
       if (!ok && lane == 0) pf_fail(a, flag, kPfSoftmax);
     }
     if (ok) {
@@ -309,10 +365,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       uint32_t r[64];
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       const bool live = i < N;
-      __nv_bfloat16* orow = a.o + (qrow0 + row) * D;
+      const int64_t qrow = qrow_base + i;
+      __nv_bfloat16* orow = a.o + qrow * D;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        tmem_ld64_async(lane_base + kOCol + half * 64, r);
+      for (int hh = 0; hh < 2; ++hh) {
+        tmem_ld64_async(lane_base + kOCol + hh * 64, r);
         tmem_wait_ld64(r);
         if (live) {
 #pragma unroll
@@ -324,18 +381,18 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                                                               __uint_as_float(r[8 * c + 2 * e + 1]) * inv_l);
               w[e] = *reinterpret_cast<const uint32_t*>(&pb);
             }
-            *reinterpret_cast<uint4*>(orow + half * 64 + c * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(orow + hh * 64 + c * 8) = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
       }
       if (live) {
         const float lse2 = m + log2f(l);
-        if (a.lse != nullptr) a.lse[qrow0 + row] = lse2 * 0.6931471805599453f;
+        if (a.lse != nullptr) a.lse[qrow] = lse2 * 0.6931471805599453f;
         if (i >= si.L) {                                            // an observation-window row
           const int jw = i - si.L, hl = h - g * a.G;
           const int64_t unit = ((int64_t)b * a.n_layers + layer) * a.h_kv + g;
           a.lse_win[unit * (a.G * a.W) + hl * a.W + jw] = lse2;
-          const uint4* src = reinterpret_cast<const uint4*>(a.q + (qrow0 + row) * D);
+          const uint4* src = reinterpret_cast<const uint4*>(a.q + qrow * D);
           uint4* dst = reinterpret_cast<uint4*>(a.q_win + ((((int64_t)b * a.n_layers + layer) * a.h_q + h) * a.W + jw) * D);
 #pragma unroll
           for (int c = 0; c < D / 8; ++c) dst[c] = src[c];
@@ -405,11 +462,11 @@ kvsel_status launch_prefill(const kvsel_desc& d, const SeqTable& t, const void* 
     nmax = n > nmax ? n : nmax;
   }
   if (q_rows + kPfTile >= (int64_t(1) << 31) || k_rows + kPfTile >= (int64_t(1) << 31)) return KVSEL_ERR_UNSUPPORTED;
-  a.n_qt_max = (int32_t)((nmax + kPfTile - 1) / kPfTile);
+  a.n_pairs = (int32_t)((nmax + 2 * kPfTile - 1) / (2 * kPfTile));
   CUtensorMap tq, tk, tv;
   if (!pf_map(&tq, q, q_rows) || !pf_map(&tk, k, k_rows) || !pf_map(&tv, v, k_rows)) return KVSEL_ERR_CUDA;
   if (set_smem((const void*)prefill_kernel, kPfSmem) != cudaSuccess) return KVSEL_ERR_CUDA;
-  const int64_t grid = (int64_t)a.n_qt_max * d.batch * d.n_layers * d.h_q;
+  const int64_t grid = (int64_t)a.n_pairs * d.batch * d.n_layers * d.h_q;
   if (grid >= (int64_t(1) << 31)) return KVSEL_ERR_UNSUPPORTED;
   TraceScope ts("prefill_tc", s);
   prefill_kernel<<<(unsigned)grid, kPfThreads, kPfSmem, s>>>(tq, tk, tv, a, t);
