@@ -68,6 +68,18 @@ __device__ __forceinline__ float fast_ex2(float x) {
 }
 
 __device__ __forceinline__ bool pf_aborted(const volatile uint32_t* f) { return *f != 0; }
+
+// A wait on the pipeline's critical path: polls without sleeping, and reads the abort flag only every
+// 256 polls (under the tensor pipe's and TMA's shared-memory traffic every shared-memory access of
+// the polling thread costs on the order of a hundred cycles, so a phase that has completed must
+// cost one access, not two).  False after kSpinLimit polls or once another role has aborted.
+__device__ __forceinline__ bool pf_wait(uint32_t bar, uint32_t parity, const volatile uint32_t* f) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255) == 255 && pf_aborted(f)) return false;
+  }
+  return false;
+}
 __device__ __forceinline__ void pf_fail(const PfArgs& a, volatile uint32_t* f, uint32_t where) {
   set_device_error(a.err, KVSEL_ERR_TIMEOUT, where);
   *f = 1;
@@ -221,17 +233,20 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       constexpr uint32_t idesc_s = umma_idesc_bf16(128, 128);
       constexpr uint32_t idesc_o = umma_idesc_bf16(128, 128) | kUmmaBMajorMN;
       const int ntA = nt_x[0], ntB = nq == 2 ? nt_x[1] : 0;
-      bool ok = mbar_wait_spin(q_full, 0);
+      bool ok = pf_wait(q_full, 0, flag);
       bool issued = false;
-      // S_x(j) may start once the tile's P V product of step j - 1 (which reads the same TMEM
-      // columns) has completed and K_j has landed; P_x(j) V_j once the softmax has written P_x(j)
-      // and V_j has landed.
+      // S_x(j) may start once K_j has landed and the tile's P V product of step j - 1 (which reads
+      // the same TMEM columns) has completed; P_x(j) V_j once V_j has landed and the softmax has
+      // written P_x(j).  The tile load is waited for first (it has normally landed long before), and
+      // not again by the second tile that reads it.
       auto s_ready = [&](int x, int j) {
-        return !pf_aborted(flag) && (j == 0 || mbar_wait_spin(pv_done(x), (j - 1) & 1)) &&
-               mbar_wait_spin(k_full(j & 1), (j >> 1) & 1);
+        const bool k_seen = x == 1 && j < ntA;
+        return (k_seen || pf_wait(k_full(j & 1), (j >> 1) & 1, flag)) &&
+               (j == 0 || pf_wait(pv_done(x), (j - 1) & 1, flag));
       };
       auto pv_ready = [&](int x, int j) {
-        return !pf_aborted(flag) && mbar_wait_spin(p_full(x), j & 1) && mbar_wait_spin(v_full(j & 1), (j >> 1) & 1);
+        const bool v_seen = x == 1 && j < ntA;
+        return (v_seen || pf_wait(v_full(j & 1), (j >> 1) & 1, flag)) && pf_wait(p_full(x), j & 1, flag);
       };
       auto s_step = [&](int x, int j, int kk) {
         const uint32_t sq = base + kQOff + x * kTileBytes, sk = base + kKOff + (j & 1) * kTileBytes;
@@ -306,7 +321,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     float m = -INFINITY, l = 0.f;
     bool ok = x < nq;
     for (int j = 0; j < ntx; ++j) {
-      ok = __all_sync(0xffffffffu, ok && !pf_aborted(flag) && mbar_wait_spin(s_full(x), j & 1));
+      ok = __all_sync(0xffffffffu, ok && pf_wait(s_full(x), j & 1, flag));
       if (!ok) {
         if (lane == 0) pf_fail(a, flag, kPfSoftmax);
         break;

@@ -59,14 +59,6 @@ __device__ __forceinline__ bool mbar_wait_n(uint32_t bar, uint32_t parity, uint3
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) { return mbar_wait_n(bar, parity, kSpinLimit); }
 
-// The same wait without the back-off sleep, for waits on a pipeline's critical path (the sleep adds
-// its own length to the latency of every hand-off); still bounded by kSpinLimit polls.
-__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
-}
-
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
