@@ -591,6 +591,9 @@ def run_prefill(args):
     assert K.kvsel_read_device_error(pipe.ws) == K.OK
     # causal flops: Q K^T and P V over keys t <= i, 2 flops per multiply-add
     flops = sum(4.0 * w.n_layers * w.h_q * (L + W) * (L + W + 1) / 2 * w.head_dim for L in w.prefix_lens)
+    # the committed traffic record is per launch of 4 layers of the 32K LLaMA-8B prompt
+    rec = traffic_record("prefill_tc") if w.name == "llama8b_32l_h32x8_d128_L32768_W32" else None
+    prefill_traffic = rec * w.n_layers / 4 if rec is not None else None
     pf = res["prefill"]["kernels"]["prefill_tc"]
     pf_ms = pf["ms"] / pf["launches"]
     peak, peak_src = measured_tensor_peak()
@@ -611,7 +614,7 @@ def run_prefill(args):
         "kernels": res["prefill"]["kernels"],
         "roofline": {"bound": "tensor", "kernel": "prefill_tc", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "peak_source": peak_src,
-                     "traffic": None, "algorithmic_flops": flops},
+                     "traffic": prefill_traffic, "algorithmic_flops": flops},
         "selection_after_prefill": {
             "fused_ms_per_step": res["fused"]["ms"], "unfused_ms_per_step": res["unfused"]["ms"],
             "fused_kernels": res["fused"]["kernels"], "unfused_kernels": res["unfused"]["kernels"],
