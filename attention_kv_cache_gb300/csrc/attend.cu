@@ -30,6 +30,7 @@ struct AttArgs {
   float* o;                   // [batch][n_layers][h_q][n_q][d]
   DeviceError* err;           // a block id outside the cache is skipped and recorded here
   int32_t n_layers, h_q, h_kv, d, G, n_q, R, P, n_per_row, S;
+  int32_t rows;               // table rows (batch x layers x KV heads)
   float scale_log2;
 };
 
@@ -226,11 +227,17 @@ __global__ void __launch_bounds__(kAttThreads) attend_split(const __grid_constan
 // Decode-sized groups (R <= 8 query rows per table row): one warp per split, no block-wide
 // synchronisation in the loop.  A step covers 16 key positions of the split: the lanes copy the
 // step's K and V rows into the warp's shared-memory stage with cp.async (whole rows per copy
-// instruction; zero-filled where a position selects no row), and the next step's copies are issued
-// before this step's arithmetic.  Lane i takes key i % 16 and half i / 16 of the head dim for the
-// logits (K chunks XOR-swizzled by the key, so the lanes' reads hit distinct banks; query rows read
-// from shared memory as broadcasts), the online softmax runs across the 16 keys with shuffles, and in
-// the weighted V sum lane i owns dims DPL*i .. DPL*i + DPL - 1.  Small stages keep 12 warps per SM.
+// instruction; zero-filled where a position selects no row; 16-byte chunks XOR-swizzled by the key so
+// that the matrix loads below hit distinct banks), and the next step's copies are issued before this
+// step's arithmetic.  The arithmetic runs on mma.sync m16n8k16 (bf16 in, fp32 accumulate) with the
+// group's query rows as the 16 rows of the A operand (rows R..15 zero): the logits S = Q K^T with Q
+// held in registers for the whole split and K loaded by ldmatrix (bf16 products are exact, so this is
+// the fp32 dot product up to summation order); P is formed in the logits' accumulator layout, which is
+// the A-operand layout of the next product, and split into bf16 high and low parts so that P V is
+// taken to ~16 significant bits of P; V is loaded transposed by ldmatrix.  The online softmax keeps an
+// exponent offset that moves only when a row's max passes it by 2^8 (then O and l are rescaled).
+// Warp w of the grid takes split w % S of table row w / S (the warps of one CTA may serve different
+// rows), so the split count can be sized to fill exactly one wave of resident warps.
 constexpr int kWarpsPerCta = 4;
 constexpr int kStep = 16;
 
@@ -242,37 +249,63 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-template <int D, int R>
+__device__ __forceinline__ void ldsm_x4(uint32_t* r, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t* r, uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// d += A B for one 16x8x16 tile whose A rows 8..15 are zero (a1 = a3 = 0): only the accumulator
+// elements of rows 0..7 (d[0], d[1]: row gq, columns 2tq and 2tq + 1) are kept.
+__device__ __forceinline__ void mma_rows8(float* d, uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  float x2, x3;
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %10, %10};"
+      : "+f"(d[0]), "+f"(d[1]), "=f"(x2), "=f"(x3)
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&p);
+}
+
+template <int D>
 __global__ void __launch_bounds__(32 * kWarpsPerCta) attend_warp(const __grid_constant__ AttArgs a,
                                                                  const __grid_constant__ SeqTable t) {
   constexpr int VPR = D / 8;          // 16-byte chunks per row
-  constexpr int DPL = D / 32;         // dims per lane in the V sum
   constexpr int STAGE = kStep * D;    // bf16 elements of one K (or V) stage
-  constexpr int HC = VPR / 2;         // chunks per half row
+  constexpr int NT = D / 8;           // 8-wide tiles of the head dim in O
   extern __shared__ __align__(16) uint8_t smem_raw[];
-  float* Qs = reinterpret_cast<float*>(smem_raw);                                   // [R][D]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __nv_bfloat16* Kb = reinterpret_cast<__nv_bfloat16*>(smem_raw + R * D * 4) + warp * 4 * STAGE;   // [2][16][D]
-  __nv_bfloat16* Vb = Kb + 2 * STAGE;                                                              // [2][16][D]
-  const int per_cta = a.S / kWarpsPerCta;
-  const int r = blockIdx.x / per_cta;
-  const int s = (blockIdx.x % per_cta) * kWarpsPerCta + warp;
+  const int gq = lane >> 2, tq = lane & 3;                           // fragment row / column pair
+  __nv_bfloat16* Kb = reinterpret_cast<__nv_bfloat16*>(smem_raw) + warp * 4 * STAGE;   // [2][16][D]
+  __nv_bfloat16* Vb = Kb + 2 * STAGE;                                                   // [2][16][D]
+  const int64_t w = (int64_t)blockIdx.x * kWarpsPerCta + warp;
+  if (w >= (int64_t)a.rows * a.S) return;                            // past the last split (whole warp)
+  const int r = (int)(w / a.S);
+  const int s = (int)(w % a.S);
   const int per_seq = a.n_layers * a.h_kv;
   const int b = r / per_seq, lg = r % per_seq;
   const int layer = lg / a.h_kv, g = lg % a.h_kv;
   const SeqInfo& si = t.s[b];
-  // query rows j < a.R of the group (rows up to the template's R beyond them are zero and unused)
-  for (int x = threadIdx.x; x < R * D; x += 32 * kWarpsPerCta) {
-    const int j = x / D, c = x % D;
-    float qv = 0.f;
-    if (j < a.R) {
-      const int h = g * a.G + j / a.n_q, i = j % a.n_q;
-      const int64_t off = ((((int64_t)b * a.n_layers + layer) * a.h_q + h) * a.n_q + i) * D + c;
-      qv = __bfloat162float(a.q[off]) * a.scale_log2;
+  // A fragments of query row gq (zero for gq >= R): elements 16c + 2tq, +1 and 16c + 8 + 2tq, +1
+  uint32_t qa[D / 16][2];
+  {
+    const bool live = gq < a.R;
+    const int h = g * a.G + gq / a.n_q, i = gq % a.n_q;
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+        a.q + (live ? ((((int64_t)b * a.n_layers + layer) * a.h_q + h) * a.n_q + i) * D : 0));
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) {
+      qa[c][0] = live ? __ldg(qrow + 8 * c + tq) : 0u;
+      qa[c][1] = live ? __ldg(qrow + 8 * c + 4 + tq) : 0u;
     }
-    Qs[x] = qv;
   }
-  __syncthreads();
   int beg, end;
   row_list(a, si, r, beg, end);
   const int64_t n_pos = (int64_t)(end - beg) * a.P;                  // key positions of the row
@@ -308,22 +341,23 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) attend_warp(const __grid_co
       const int x = i * KPI + lane / VPR;
       const int32_t rx = __shfl_sync(0xffffffffu, row, x);
       const int64_t src = (int64_t)(rx < 0 ? 0 : rx) * D + c * 8;
-      const uint32_t kd = kb_s + (uint32_t)((buf * STAGE + x * D) * 2 + ((c ^ (x & (VPR - 1))) * 16));
-      const uint32_t vd = vb_s + (uint32_t)((buf * STAGE + x * D) * 2 + c * 16);
-      cp_async16(kd, kbase + src, rx >= 0);
-      cp_async16(vd, vbase + src, rx >= 0);
+      const uint32_t dst = (uint32_t)((buf * STAGE + x * D) * 2 + ((c ^ (x & (VPR - 1))) * 16));
+      cp_async16(kb_s + dst, kbase + src, rx >= 0);
+      cp_async16(vb_s + dst, vbase + src, rx >= 0);
     }
     cp_async_commit();
   };
+  // ldmatrix row addresses of this lane within a stage (byte offsets, before the chunk swizzle):
+  // K: matrices (keys 0-7 | 8-15) x (low | high 8 of a 16-wide chunk); V (transposed): matrices
+  // (keys 0-7 | 8-15) x (d tile 2p | 2p + 1)
+  const int key_k = ((lane >> 4) << 3) | (lane & 7), hi_k = (lane >> 3) & 1;
+  const int key_v = (((lane >> 3) & 1) << 3) | (lane & 7), hi_v = lane >> 4;
 
-  float m[R], l[R], acc[R][DPL];
+  float o[NT][2];
 #pragma unroll
-  for (int j = 0; j < R; ++j) {
-    m[j] = -INFINITY;
-    l[j] = 0.f;
-#pragma unroll
-    for (int c = 0; c < DPL; ++c) acc[j][c] = 0.f;
-  }
+  for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = 0.f;
+  float m = -INFINITY, l = 0.f;
+  const float scale = a.scale_log2;
   int32_t row = row_of(p0 + key, id_at(p0 + key));
   int32_t id_next = id_at(p0 + kStep + key);
   if (p0 < p1) issue(row, 0);
@@ -341,87 +375,98 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) attend_warp(const __grid_co
     }
     id_next = id_after;
     __syncwarp();
-    // logits: this lane's key, half of the head dim, two partial sums per row for ILP
-    const __nv_bfloat16* krow = Kb + buf * STAGE + key * D;
-    float z[R], z2[R];
+    // logits of row gq: keys 2tq, 2tq + 1 (s0[0..1]) and 8 + 2tq, 9 + 2tq (s1[0..1])
+    const uint32_t kst = kb_s + (uint32_t)(buf * STAGE * 2), vst = vb_s + (uint32_t)(buf * STAGE * 2);
+    float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};
 #pragma unroll
-    for (int j = 0; j < R; ++j) z[j] = z2[j] = 0.f;
+    for (int c = 0; c < D / 16; ++c) {
+      uint32_t kb[4];
+      ldsm_x4(kb, kst + (uint32_t)(key_k * D * 2 + (((2 * c + hi_k) ^ (key_k & (VPR - 1))) << 4)));
+      mma_rows8(s0, qa[c][0], qa[c][1], kb[0], kb[1]);
+      mma_rows8(s1, qa[c][0], qa[c][1], kb[2], kb[3]);
+    }
+    const uint32_t valid = __ballot_sync(0xffffffffu, row >= 0);    // bit x: key x selects a row
+    const int k0 = 2 * tq;
+    float z[4] = {s0[0], s0[1], s1[0], s1[1]};
+    const int kz[4] = {k0, k0 + 1, k0 + 8, k0 + 9};
 #pragma unroll
-    for (int cc = 0; cc < HC; ++cc) {
-      const int c = half * HC + cc;
-      float kf[8];
-      bf16x8_to_f32(*reinterpret_cast<const uint4*>(krow + ((c ^ (key & (VPR - 1))) * 8)), kf);
+    for (int e = 0; e < 4; ++e) z[e] = ((valid >> kz[e]) & 1u) ? z[e] * scale : -INFINITY;
+    float mx = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    float alpha = 1.f;
+    if (mx > m + 8.f) {
+      alpha = m == -INFINITY ? 0.f : fast_ex2(m - mx);
+      m = mx;
+    }
+    if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-      for (int j = 0; j < R; ++j) {
-        const float4 q0 = *reinterpret_cast<const float4*>(Qs + j * D + c * 8);
-        const float4 q1 = *reinterpret_cast<const float4*>(Qs + j * D + c * 8 + 4);
-        z[j] = fmaf(q0.x, kf[0], fmaf(q0.y, kf[1], fmaf(q0.z, kf[2], fmaf(q0.w, kf[3], z[j]))));
-        z2[j] = fmaf(q1.x, kf[4], fmaf(q1.y, kf[5], fmaf(q1.z, kf[6], fmaf(q1.w, kf[7], z2[j]))));
+      for (int n = 0; n < NT; ++n) {
+        o[n][0] *= alpha;
+        o[n][1] *= alpha;
       }
     }
-    // online softmax across the 16 keys of the step (both halves hold the same values)
-    float p[R];
+    float p[4], sum = 0.f;
 #pragma unroll
-    for (int j = 0; j < R; ++j) {
-      float zj = z[j] + z2[j];
-      zj += __shfl_xor_sync(0xffffffffu, zj, 16);
-      zj = row >= 0 ? zj : -INFINITY;
-      float mx = zj;
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      const float m_new = fmaxf(m[j], mx);
-      const float f = m[j] == -INFINITY ? 0.f : fast_ex2(m[j] - m_new);
-      p[j] = m_new == -INFINITY ? 0.f : fast_ex2(zj - m_new);
-      float sum = p[j];
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      l[j] = l[j] * f + sum;
-      m[j] = m_new;
-#pragma unroll
-      for (int c = 0; c < DPL; ++c) acc[j][c] *= f;
+    for (int e = 0; e < 4; ++e) {
+      p[e] = z[e] == -INFINITY ? 0.f : fast_ex2(z[e] - m);
+      sum += p[e];
     }
-    // weighted V sum over the 16 keys (zero-filled rows carry p = 0)
-    const __nv_bfloat16* vst = Vb + buf * STAGE + DPL * lane;
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    l = l * alpha + sum;
+    // P as bf16 high + low parts, in the A-operand layout (keys 2tq.. in a0, 8 + 2tq.. in a2)
+    const uint32_t h01 = pack_bf16(p[0], p[1]), h23 = pack_bf16(p[2], p[3]);
+    const __nv_bfloat162 hb01 = *reinterpret_cast<const __nv_bfloat162*>(&h01);
+    const __nv_bfloat162 hb23 = *reinterpret_cast<const __nv_bfloat162*>(&h23);
+    const uint32_t l01 = pack_bf16(p[0] - __low2float(hb01), p[1] - __high2float(hb01));
+    const uint32_t l23 = pack_bf16(p[2] - __low2float(hb23), p[3] - __high2float(hb23));
 #pragma unroll
-    for (int x = 0; x < kStep; ++x) {
-      float vf[DPL];
-      if constexpr (DPL == 4) {
-        const uint2 u = *reinterpret_cast<const uint2*>(vst + x * D);
-        vf[0] = __uint_as_float(u.x << 16);
-        vf[1] = __uint_as_float(u.x & 0xffff0000u);
-        vf[2] = __uint_as_float(u.y << 16);
-        vf[3] = __uint_as_float(u.y & 0xffff0000u);
-      } else {
-        const uint32_t u = *reinterpret_cast<const uint32_t*>(vst + x * D);
-        vf[0] = __uint_as_float(u << 16);
-        vf[1] = __uint_as_float(u & 0xffff0000u);
-      }
-#pragma unroll
-      for (int j = 0; j < R; ++j) {
-        const float px = __shfl_sync(0xffffffffu, p[j], x);
-#pragma unroll
-        for (int c = 0; c < DPL; ++c) acc[j][c] = fmaf(px, vf[c], acc[j][c]);
-      }
+    for (int pp = 0; pp < NT / 2; ++pp) {
+      uint32_t vb[4];
+      ldsm_x4_t(vb, vst + (uint32_t)(key_v * D * 2 + (((2 * pp + hi_v) ^ (key_v & (VPR - 1))) << 4)));
+      mma_rows8(o[2 * pp], h01, h23, vb[0], vb[1]);
+      mma_rows8(o[2 * pp], l01, l23, vb[0], vb[1]);
+      mma_rows8(o[2 * pp + 1], h01, h23, vb[2], vb[3]);
+      mma_rows8(o[2 * pp + 1], l01, l23, vb[2], vb[3]);
     }
     __syncwarp();          // the stage is read before it is refilled
     row = row_next;
     buf ^= 1;
   }
-  float* out = a.part + ((int64_t)r * a.S + s) * a.R * (D + 2);
+  if (gq < a.R) {
+    float* out = a.part + (((int64_t)r * a.S + s) * a.R + gq) * (D + 2);
 #pragma unroll
-  for (int j = 0; j < R; ++j) {
-    if (j >= a.R) break;
-#pragma unroll
-    for (int c = 0; c < DPL; ++c) out[j * (D + 2) + DPL * lane + c] = acc[j][c];
-    if (lane == 0) {
-      out[j * (D + 2) + D] = m[j];
-      out[j * (D + 2) + D + 1] = l[j];
+    for (int n = 0; n < NT; ++n) {
+      out[8 * n + 2 * tq] = o[n][0];
+      out[8 * n + 2 * tq + 1] = o[n][1];
+    }
+    if (tq == 0) {
+      out[D] = m;
+      out[D + 1] = l;
     }
   }
 }
 
-size_t attend_warp_smem(int d, int R) {
-  return (size_t)R * d * 4 + (size_t)kWarpsPerCta * 4 * kStep * d * 2;
+size_t attend_warp_smem(int d) { return (size_t)kWarpsPerCta * 4 * kStep * d * 2; }
+
+using AttKernel = void (*)(const AttArgs, const SeqTable);
+
+// The warp kernel for head dim d (any R <= 8 query rows per table row).
+AttKernel attend_warp_kernel(int d) { return d == 64 ? attend_warp<64> : attend_warp<128>; }
+
+// Warps of the warp kernel resident at once on the current device; 0 if that cannot be queried.
+int64_t attend_resident_warps(int d) {
+  const size_t wsm = attend_warp_smem(d);
+  const AttKernel kern = attend_warp_kernel(d);
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      set_smem((const void*)kern, wsm) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * kWarpsPerCta, wsm) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return (int64_t)sms * per_sm * kWarpsPerCta;
 }
 
 // o[row j of table row r] = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M) l_s; rows with no key give 0.
@@ -461,15 +506,16 @@ __global__ void __launch_bounds__(D) attend_combine(const __grid_constant__ AttA
 
 }  // namespace
 
-int64_t attend_splits(int64_t rows, int64_t max_rows_per_list, int R) {
+int64_t attend_splits(int64_t rows, int64_t max_rows_per_list, int R, int d) {
   if (R <= 8) {
-    // warp splits: about 4096 warps over the GPU, no split shorter than 64 positions; a multiple of
-    // the warps per CTA
-    int64_t s = (4096 + rows - 1) / rows;
+    // warp splits: as many as fit one wave of resident warps (all rows' splits run at once), no
+    // split shorter than 64 positions
+    int64_t resident = attend_resident_warps(d);
+    if (resident <= 0) resident = 152 * 12;
+    int64_t s = resident / rows;
     const int64_t cap = (max_rows_per_list + 63) / 64;
     if (s > cap) s = cap;
-    s = (s + kWarpsPerCta - 1) / kWarpsPerCta * kWarpsPerCta;
-    if (s < kWarpsPerCta) s = kWarpsPerCta;
+    if (s < 1) s = 1;
     if (s > 256) s = 256;
     return s;
   }
@@ -511,29 +557,16 @@ kvsel_status launch_attend(const kvsel_desc& d, const SeqTable& t, const void* q
   a.S = (int32_t)S;
   a.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)d.head_dim));
   const int64_t rows = (int64_t)d.batch * d.n_layers * d.h_kv;
+  a.rows = (int32_t)rows;
   const size_t smem = attend_smem(d.head_dim);
   kvsel_status st;
   if (a.R <= 8) {
     TraceScope ts("attend_split", s);
-    const unsigned grid = (unsigned)(rows * S / kWarpsPerCta);
-    const int Rt = a.R == 1 ? 1 : a.R == 2 ? 2 : a.R <= 4 ? 4 : 8;
-    const size_t wsm = attend_warp_smem(d.head_dim, Rt);
-    cudaError_t ce = cudaSuccess;
-    auto go = [&](auto kern) {
-      if ((ce = set_smem((const void*)kern, wsm)) == cudaSuccess) kern<<<grid, 32 * kWarpsPerCta, wsm, s>>>(a, t);
-    };
-    if (d.head_dim == 64) {
-      if (a.R == 1) go(attend_warp<64, 1>);
-      else if (a.R == 2) go(attend_warp<64, 2>);
-      else if (a.R <= 4) go(attend_warp<64, 4>);
-      else go(attend_warp<64, 8>);
-    } else {
-      if (a.R == 1) go(attend_warp<128, 1>);
-      else if (a.R == 2) go(attend_warp<128, 2>);
-      else if (a.R <= 4) go(attend_warp<128, 4>);
-      else go(attend_warp<128, 8>);
-    }
-    if (ce != cudaSuccess) return KVSEL_ERR_CUDA;
+    const unsigned grid = (unsigned)((rows * S + kWarpsPerCta - 1) / kWarpsPerCta);
+    const size_t wsm = attend_warp_smem(d.head_dim);
+    const AttKernel kern = attend_warp_kernel(d.head_dim);
+    if (set_smem((const void*)kern, wsm) != cudaSuccess) return KVSEL_ERR_CUDA;
+    kern<<<grid, 32 * kWarpsPerCta, wsm, s>>>(a, t);
     if ((st = launch_status()) != KVSEL_OK) return st;
   } else {
     TraceScope ts("attend_split", s);
