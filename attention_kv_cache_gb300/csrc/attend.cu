@@ -226,10 +226,9 @@ __global__ void __launch_bounds__(kAttThreads) attend_split(const __grid_constan
 
 // Decode-sized groups (R <= 8 query rows per table row): one warp per split, no block-wide
 // synchronisation in the loop.  A step covers 16 key positions of the split: the lanes copy the
-// step's K and V rows into the warp's shared-memory stage with cp.async (whole rows per copy
-// instruction; zero-filled where a position selects no row; 16-byte chunks XOR-swizzled by the key so
-// that the matrix loads below hit distinct banks), and the next step's copies are issued before this
-// step's arithmetic.  The arithmetic runs on mma.sync m16n8k16 (bf16 in, fp32 accumulate) with the
+// step's K and V rows into one of the warp's three shared-memory stages with cp.async (whole rows per
+// copy instruction; zero-filled where a position selects no row; 16-byte chunks XOR-swizzled by the
+// key so that the matrix loads below hit distinct banks), two steps ahead of the step computed.  The arithmetic runs on mma.sync m16n8k16 (bf16 in, fp32 accumulate) with the
 // group's query rows as the 16 rows of the A operand (rows R..15 zero): the logits S = Q K^T with Q
 // held in registers for the whole split and K loaded by ldmatrix (bf16 products are exact, so this is
 // the fp32 dot product up to summation order); P is formed in the logits' accumulator layout, which is
@@ -240,6 +239,7 @@ __global__ void __launch_bounds__(kAttThreads) attend_split(const __grid_constan
 // rows), so the split count can be sized to fill exactly one wave of resident warps.
 constexpr int kWarpsPerCta = 4;
 constexpr int kStep = 16;
+constexpr int kStages = 3;
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
   const uint32_t n = valid ? 16u : 0u;   // 0 source bytes: the 16 destination bytes are zero-filled
@@ -283,8 +283,8 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) attend_warp(const __grid_co
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;                           // fragment row / column pair
-  __nv_bfloat16* Kb = reinterpret_cast<__nv_bfloat16*>(smem_raw) + warp * 4 * STAGE;   // [2][16][D]
-  __nv_bfloat16* Vb = Kb + 2 * STAGE;                                                   // [2][16][D]
+  __nv_bfloat16* Kb = reinterpret_cast<__nv_bfloat16*>(smem_raw) + warp * 2 * kStages * STAGE;   // [3][16][D]
+  __nv_bfloat16* Vb = Kb + kStages * STAGE;                                                     // [3][16][D]
   const int64_t w = (int64_t)blockIdx.x * kWarpsPerCta + warp;
   if (w >= (int64_t)a.rows * a.S) return;                            // past the last split (whole warp)
   const int r = (int)(w / a.S);
@@ -358,21 +358,24 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) attend_warp(const __grid_co
   for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = 0.f;
   float m = -INFINITY, l = 0.f;
   const float scale = a.scale_log2;
+  // every step commits one copy group (empty past the split's end), so waiting for all but the two
+  // newest groups waits for exactly the step about to be computed
   int32_t row = row_of(p0 + key, id_at(p0 + key));
-  int32_t id_next = id_at(p0 + kStep + key);
-  if (p0 < p1) issue(row, 0);
+  if (p0 < p1) issue(row, 0); else cp_async_commit();
+  int32_t row1 = row_of(p0 + kStep + key, id_at(p0 + kStep + key));
+  if (p0 + kStep < p1) issue(row1, 1); else cp_async_commit();
+  int32_t id_next = id_at(p0 + 2 * kStep + key);
   int buf = 0;
   for (int64_t base = p0; base < p1; base += kStep) {
-    const bool more = base + kStep < p1;
-    int32_t row_next = -1;
-    const int32_t id_after = id_at(base + 2 * kStep + key);
-    if (more) {
-      row_next = row_of(base + kStep + key, id_next);
-      issue(row_next, buf ^ 1);
-      cp_async_wait<1>();
+    int32_t row2 = -1;
+    const int32_t id_after = id_at(base + 3 * kStep + key);
+    if (base + 2 * kStep < p1) {
+      row2 = row_of(base + 2 * kStep + key, id_next);
+      issue(row2, buf == 0 ? 2 : buf - 1);
     } else {
-      cp_async_wait<0>();
+      cp_async_commit();
     }
+    cp_async_wait<2>();
     id_next = id_after;
     __syncwarp();
     // logits of row gq: keys 2tq, 2tq + 1 (s0[0..1]) and 8 + 2tq, 9 + 2tq (s1[0..1])
@@ -431,9 +434,11 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) attend_warp(const __grid_co
       mma_rows8(o[2 * pp + 1], l01, l23, vb[2], vb[3]);
     }
     __syncwarp();          // the stage is read before it is refilled
-    row = row_next;
-    buf ^= 1;
+    row = row1;
+    row1 = row2;
+    buf = buf == kStages - 1 ? 0 : buf + 1;
   }
+  cp_async_wait<0>();      // (only empty groups can remain)
   if (gq < a.R) {
     float* out = a.part + (((int64_t)r * a.S + s) * a.R + gq) * (D + 2);
 #pragma unroll
@@ -448,7 +453,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) attend_warp(const __grid_co
   }
 }
 
-size_t attend_warp_smem(int d) { return (size_t)kWarpsPerCta * 4 * kStep * d * 2; }
+size_t attend_warp_smem(int d) { return (size_t)kWarpsPerCta * 2 * kStages * kStep * d * 2; }
 
 using AttKernel = void (*)(const AttArgs, const SeqTable);
 
