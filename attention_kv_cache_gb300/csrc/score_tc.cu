@@ -12,8 +12,10 @@
 //           rows of each head in registers (no cross-lane reduction), then the
 //           group reduce, max-pool and page reduce run on the segment in smem.
 //
-// Persistent CTAs (one per SM), each walking a contiguous range of (unit,
-// segment) work items.  Warp roles: warp 0 issues TMA (Q once per unit, K
+// Persistent CTAs (one per SM).  Pass 1 walks a contiguous range of (unit,
+// segment) work items; pass 2 takes an equal share of all units' prefix pages
+// laid end to end, cut into pieces at unit ends and every kSeg2Max keys, so
+// that every CTA emits the same number of pages however many units there are.  Warp roles: warp 0 issues TMA (Q once per unit, K
 // tiles through an NK-stage ring), warp 1 owns TMEM and issues UMMA into a
 // ring of TMEM accumulators, warps 2..9 are the epilogue.  All hand-offs are
 // mbarriers with bounded waits; a wait that gives up records
@@ -84,41 +86,58 @@ struct Item {
   int a0, a1;          // pass 2: prefix range whose scores are emitted
 };
 
-template <bool PASS2>
-__device__ __forceinline__ Item decode(const SeqTable& t, const ScoreShape& sh, int item) {
-  Item it;
-  it.b = find_seq(t, item);
-  const SeqInfo& si = t.s[it.b];
-  const int local = item - si.item0;
-  it.ul = local / si.n_seg;
-  it.seg = local % si.n_seg;
-  it.layer = it.ul / sh.h_kv;
-  it.g = it.ul % sh.h_kv;
-  it.unit = si.unit0 + it.ul;
+// Unit ul of sequence b: the fields every item of it shares.
+__device__ __forceinline__ void unit_fields(const SeqTable& t, const ScoreShape& sh, int b, int ul, Item& it) {
+  const SeqInfo& si = t.s[b];
+  it.b = b;
+  it.ul = ul;
+  it.layer = ul / sh.h_kv;
+  it.g = ul % sh.h_kv;
+  it.unit = si.unit0 + ul;
   it.L = si.L;
   it.n_keys = si.n_keys;
-  it.q_row0 = (int32_t)((((int64_t)it.b * sh.n_layers + it.layer) * sh.h_q + (int64_t)it.g * sh.G) * sh.W);
+  it.q_row0 = (int32_t)((((int64_t)b * sh.n_layers + it.layer) * sh.h_q + (int64_t)it.g * sh.G) * sh.W);
   it.k_row0 = (int32_t)(si.k_off / sh.d + ((int64_t)it.layer * sh.h_kv + it.g) * si.n_keys);
-  if (!PASS2) {
-    it.ta = it.seg * sh.seg1;
-    it.tb = min(si.n_keys, it.ta + sh.seg1);
-    it.a0 = it.a1 = 0;
-  } else {
-    const int pr = (sh.pool_k - 1) / 2;
-    it.a0 = it.seg * sh.seg2;
-    it.a1 = min(si.L, it.a0 + sh.seg2);
-    it.ta = max(0, it.a0 - pr);
-    it.tb = min(si.L, it.a1 + pr);
-  }
-  return it;
 }
 
-__device__ __forceinline__ int item_begin(int n_items) {
-  return (int)(((int64_t)blockIdx.x * n_items) / gridDim.x);
-}
-__device__ __forceinline__ int item_end(int n_items) {
-  return (int)(((int64_t)(blockIdx.x + 1) * n_items) / gridDim.x);
-}
+// This CTA's work, in order.  Pass 1: items [n*c/grid, n*(c+1)/grid) of the launch's (unit,
+// segment) items.  Pass 2: the launch's units' prefix pages laid end to end (sequence b's units
+// start at page item0, n_seg pages each), pages [n*c/grid, n*(c+1)/grid) of them, cut into
+// pieces that end at a unit's end, at the share's end or after seg2 keys.
+template <bool PASS2>
+struct Work {
+  int pos, end;
+  __device__ __forceinline__ explicit Work(const SeqTable& t)
+      : pos((int)(((int64_t)blockIdx.x * t.n_items) / gridDim.x)),
+        end((int)(((int64_t)(blockIdx.x + 1) * t.n_items) / gridDim.x)) {}
+  __device__ __forceinline__ bool next(const SeqTable& t, const ScoreShape& sh, Item& it) {
+    if (pos >= end) return false;
+    const int b = find_seq(t, pos);
+    const SeqInfo& si = t.s[b];
+    const int local = pos - si.item0;
+    if (!PASS2) {
+      unit_fields(t, sh, b, local / si.n_seg, it);
+      it.seg = local % si.n_seg;
+      it.ta = it.seg * sh.seg1;
+      it.tb = min(si.n_keys, it.ta + sh.seg1);
+      it.a0 = it.a1 = 0;
+      pos += 1;
+    } else {
+      unit_fields(t, sh, b, local / si.n_seg, it);
+      const int pin = local % si.n_seg;                       // first page of the piece in its unit
+      const int n = min(min(si.n_seg - pin, sh.seg2 / sh.page_size), end - pos);
+      const int pr = (sh.pool_k - 1) / 2;
+      it.seg = pin;
+      it.a0 = pin * sh.page_size;
+      it.a1 = min(si.L, (pin + n) * sh.page_size);
+      it.ta = max(0, it.a0 - pr);
+      it.tb = min(si.L, it.a1 + pr);
+      pos += n;
+    }
+    return true;
+  }
+  __device__ __forceinline__ int index() const { return pos - 1; }   // pass 1: the item just taken
+};
 
 __device__ __forceinline__ bool aborted(const volatile uint32_t* flag) { return *flag != 0; }
 
@@ -143,9 +162,8 @@ __device__ void produce(const CUtensorMap* tq, const CUtensorMap* tk, const TcAr
   uint32_t kph = 0, qph = 0;
   uint32_t n_fills = 0, n_q = 0;
   int prev_unit = -1;
-  const int i1 = item_end(t.n_items);
-  for (int item = item_begin(t.n_items); item < i1 && !aborted(flag); ++item) {
-    const Item it = decode<PASS2>(t, a.sh, item);
+  Work<PASS2> work(t);
+  for (Item it; !aborted(flag) && work.next(t, a.sh, it);) {
     if (it.unit != prev_unit) {
       if (!mbar_wait(q_empty, qph ^ 1)) { fail(a, flag, kWhereProducer); break; }
       mbar_expect_tx(q_full, P::kQBytes);
@@ -201,9 +219,8 @@ __device__ void issue_mma(const TcArgs& a, const SeqTable& t, uint32_t base, uin
   uint32_t kph = 0, tph = 0, qph = 0;
   int prev_unit = -1;
   bool issued = false;
-  const int i1 = item_end(t.n_items);
-  for (int item = item_begin(t.n_items); item < i1 && !aborted(flag); ++item) {
-    const Item it = decode<PASS2>(t, a.sh, item);
+  Work<PASS2> work(t);
+  for (Item it; !aborted(flag) && work.next(t, a.sh, it);) {
     if (it.unit != prev_unit) {
       if (prev_unit >= 0) umma_commit(q_empty);     // previous unit's Q is free once its MMAs finish
       if (!mbar_wait(q_full, qph)) { fail(a, flag, kWhereMma); break; }
@@ -430,9 +447,9 @@ __device__ void epilogue_pass1(const TcArgs& a, const SeqTable& t, uint32_t base
   const bool rvalid = row < a.sh.R;
   int ts = 0;
   uint32_t tph = 0;
-  const int i1 = item_end(t.n_items);
-  for (int item = item_begin(t.n_items); item < i1; ++item) {
-    const Item it = decode<false>(t, a.sh, item);
+  Work<false> work(t);
+  for (Item it; work.next(t, a.sh, it);) {
+    const int item = work.index();
     const int row_last = it.L + (rvalid ? row % a.sh.W : 0);     // last key this row sees
     const int vis_end = min(it.tb, row_last + 1);
     float m = -INFINITY, l = 0.f;
@@ -576,9 +593,8 @@ __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base
   const int P_ = a.sh.page_size;
   int ts = 0;
   uint32_t tph = 0;
-  const int i1 = item_end(t.n_items);
-  for (int item = item_begin(t.n_items); item < i1; ++item) {
-    const Item it = decode<true>(t, a.sh, item);
+  Work<true> work(t);
+  for (Item it; work.next(t, a.sh, it);) {
     epi_sync();                                          // readers of the previous item are done
     for (int i = e.etid; i < it.tb - it.ta; i += kEpiThreads) Ss[i] = 0.f;
     for (int i = e.etid; i < RT; i += kEpiThreads) {
@@ -798,7 +814,7 @@ kvsel_status launch_score(const ScoreShape& sh_in, const SeqTable& base, const v
   CUtensorMap tq, tk;
   if (!make_map(&tq, q, q_rows, sh.d) || !make_map(&tk, k, k_rows, sh.d)) return KVSEL_ERR_CUDA;
   sh.seg2 = (int32_t)(sh.page_size * (kSeg2Max / sh.page_size));
-  const SeqTable t2 = with_items(base, ups, sh.seg2, false, sh.W);
+  const SeqTable t2 = with_items(base, ups, sh.page_size, false, sh.W);   // one item per prefix page
   TcArgs a;
   a.sh = sh;
   a.scores = scores;
