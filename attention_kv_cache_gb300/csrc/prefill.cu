@@ -332,9 +332,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       // columns 0..31, keys 64..127 into 32..63), packed in place into the same registers
       uint32_t rv[64], rw[64];
       tmem_ld64_async(lane_base + kSCol + 64, rv);
-      tmem_wait_ld64(rv);
       tmem_ld64_async(lane_base + kSCol, rw);
-      tmem_wait_ld64(rw);
+      tmem_wait_ld64(rv);                                      // one wait covers both loads
+      reg_tie64(rw);
       float* v = reinterpret_cast<float*>(rv);
       float* w = reinterpret_cast<float*>(rw);
       if (diag) {
