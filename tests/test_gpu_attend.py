@@ -151,3 +151,39 @@ def test_attend_group_shapes(h_q, h_kv, n_q, d, cuda):
     assert K.kvsel_read_device_error(ws) == K.OK
     lists = idx.view(2, h_kv, n_per).numpy()
     _close(o[0], _ref(w, qd[0], inp.k[0], inp.v[0], lists, P, n_q), f"R={h_q // h_kv * n_q}")
+
+
+def _climbing(n_keys, d, slope2, a, seed):
+    """Unit direction u, K rows c_t u (+ small noise) whose logit against the query a u grows by slope2
+    (base 2) per key, and random V rows: (u, k [n_keys, d] bf16, v [n_keys, d] bf16)."""
+    g = torch.Generator().manual_seed(seed)
+    u = torch.randn(d, generator=g)
+    u /= u.norm()
+    c = torch.arange(n_keys, dtype=torch.float32) * slope2 * np.log(2.0) * np.sqrt(d) / a
+    k = (c[:, None] * u[None, :] + 0.05 * torch.randn(n_keys, d, generator=g)).to(torch.bfloat16)
+    v = torch.randn(n_keys, d, generator=g).to(torch.bfloat16)
+    return u, k, v
+
+
+@pytest.mark.parametrize("n_q", [1, 3])
+def test_attend_offset_moves(n_q, cuda):
+    """Logits that climb by 12 (base 2) per 128 keys along the cache: within every split the exponent
+    offset moves many times (O and l rescaled), and the splits' offsets differ by far more than 2^8 in
+    the merge.  R = 4 (tensor-core warp kernel) and R = 12 (block kernel)."""
+    from attention_kv_cache_gb300 import kvsel as K
+    h_q, d, L, W, P = 4, 128, 3000, 8, 16
+    n_keys = L + W
+    w = S.Workload("attend_climb", 103, 1, h_q, 1, d, W, (L,), k_keep=10)
+    u, kk, vv = _climbing(n_keys, d, 12.0 / 128, 4.0, seed=7 + n_q)
+    g = torch.Generator().manual_seed(11)
+    qd = (4.0 * u + 0.05 * torch.randn((1, 1, h_q, n_q, d), generator=g)).to(torch.bfloat16)
+    desc = K.make_desc(n_layers=1, h_q=h_q, h_kv=1, head_dim=d, window=W, prefix_lens=[L])
+    nb = -(-n_keys // P)
+    o = torch.empty((1, 1, h_q, n_q, d), dtype=torch.float32, device=cuda)
+    ws = _ws(K, K.kvsel_attend_workspace_size(desc, n_q, P, nb), cuda)
+    K.kvsel_attend(desc, qd.to(cuda), n_q, kk.reshape(-1).to(cuda), vv.reshape(-1).to(cuda), None, None, 0, P, nb,
+                   o, ws)
+    torch.cuda.synchronize()
+    assert K.kvsel_read_device_error(ws) == K.OK
+    want = _ref(w, qd[0], kk[None, None], vv[None, None], [[np.arange(nb)]], P, n_q)
+    _close(o[0], want, f"climbing logits R={h_q * n_q}")

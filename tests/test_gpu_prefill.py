@@ -76,6 +76,38 @@ def test_prefill_matches_oracle(name, w, cuda):
     _check_prefill(w, inp, qf, o, lse, lse_win, q_win)
 
 
+def test_prefill_offset_moves(cuda):
+    """Logits that climb by 10 (base 2) per 128-key tile: every row's exponent offset moves at every
+    tile up to its own, so O is rescaled in TMEM many times; o, lse and the window lse against the
+    oracle as above."""
+    from types import SimpleNamespace
+
+    from attention_kv_cache_gb300 import kvsel as K
+    from attention_kv_cache_gb300.pipeline import desc_for
+    w = S.Workload("pf_climb", 113, 1, 2, 1, 128, 16, (600,), k_keep=16)
+    N, d = 616, 128
+    g = torch.Generator().manual_seed(13)
+    u = torch.randn(d, generator=g)
+    u /= u.norm()
+    a = 4.0
+    c = torch.arange(N, dtype=torch.float32) * (10.0 / 128) * np.log(2.0) * np.sqrt(d) / a
+    kk = (c[:, None] * u[None, :] + 0.05 * torch.randn(N, d, generator=g)).to(torch.bfloat16)
+    vv = torch.randn(N, d, generator=g).to(torch.bfloat16)
+    qq = (a * u + 0.05 * torch.randn((1, 2, N, d), generator=g)).to(torch.bfloat16)    # [layers, h_q, N, d]
+    q = qq.reshape(-1).to(cuda)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.numel() // d, dtype=torch.float32, device=cuda)
+    lse_win = torch.empty((1, 1, 1, 2 * w.window), dtype=torch.float32, device=cuda)
+    q_win = torch.empty((1, 1, 2, w.window, d), dtype=torch.bfloat16, device=cuda)
+    desc = desc_for(w)
+    ws = _ws(K, K.kvsel_workspace_size(desc), cuda)
+    K.kvsel_prefill_attention(desc, q, kk.reshape(-1).to(cuda), vv.reshape(-1).to(cuda), o, lse, lse_win, q_win, ws)
+    torch.cuda.synchronize()
+    assert K.kvsel_read_device_error(ws) == K.OK
+    inp = SimpleNamespace(k=[kk.reshape(1, 1, N, d)], v=[vv.reshape(1, 1, N, d)])
+    _check_prefill(w, inp, [qq], o, lse, lse_win, q_win)
+
+
 def test_scores_from_prefill_lse(cuda):
     """Window scores from the prefill's lse (one pass) equal the oracle's and the two-pass scores."""
     from attention_kv_cache_gb300 import kvsel as K
