@@ -296,7 +296,13 @@ KVSEL_API kvsel_status kvsel_compact_layers(const kvsel_desc* desc, const void* 
  *   max_blocks  upper bound of any row's list length (sizes the split of each row's work)
  *   o           [device] fp32 out [batch][n_layers][h_q][n_q][d]
  *   ws          [device] workspace of kvsel_attend_workspace_size() bytes (partials of the splits);
- *               a block id whose first row does not exist is skipped and KVSEL_ERR_DEVICE recorded
+ *               a block id whose first row does not exist is skipped and KVSEL_ERR_DEVICE recorded.
+ *               The split count, and with it the size, depends on how many warps the current device
+ *               keeps resident: query the size on the device the call runs on.
+ *
+ * Arithmetic: for up to 8 query rows per table row the logits are bf16 products accumulated in fp32
+ * (tensor cores) and P V takes P to ~16 significant bits (a bf16 high and low part); more rows use
+ * fp32 FMA throughout.
  */
 KVSEL_API kvsel_status kvsel_attend_workspace_size(const kvsel_desc* desc, int32_t n_q, int32_t block,
                                                    int32_t max_blocks, size_t* bytes);
