@@ -10,6 +10,8 @@
 // Split-K: the blocks of a row are divided among S CTAs; each CTA walks its blocks in chunks of up to
 // 128 cache rows staged in shared memory, keeps an online (max, sum) and the weighted V sum per query
 // row, and writes a partial; attend_combine merges the S partials of each query row.
+#include <mutex>
+
 #include "internal.cuh"
 
 namespace kvsel {
@@ -268,6 +270,7 @@ __device__ __forceinline__ void mma_rows8(float* d, uint32_t a0, uint32_t a2, ui
       "{%0, %1, %10, %10};"
       : "+f"(d[0]), "+f"(d[1]), "=f"(x2), "=f"(x3)
       : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+  asm volatile("" ::"f"(x2), "f"(x3));   // (rows 8..15 of the product: zero, unused)
 }
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
@@ -461,17 +464,31 @@ using AttKernel = void (*)(const AttArgs, const SeqTable);
 AttKernel attend_warp_kernel(int d) { return d == 64 ? attend_warp<64> : attend_warp<128>; }
 
 // Warps of the warp kernel resident at once on the current device; 0 if that cannot be queried.
+// Queried once per (device, head dim).
 int64_t attend_resident_warps(int d) {
+  constexpr int kMaxDev = 64;
+  static std::mutex mu;
+  static int64_t cache[kMaxDev][2] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  const int di = d == 64 ? 0 : 1;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < kMaxDev && cache[dev][di] > 0) return cache[dev][di];
   const size_t wsm = attend_warp_smem(d);
   const AttKernel kern = attend_warp_kernel(d);
-  int dev = 0, sms = 0, per_sm = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+  int sms = 0, per_sm = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
       set_smem((const void*)kern, wsm) != cudaSuccess ||
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * kWarpsPerCta, wsm) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
-  return (int64_t)sms * per_sm * kWarpsPerCta;
+  const int64_t n = (int64_t)sms * per_sm * kWarpsPerCta;
+  if (dev >= 0 && dev < kMaxDev) cache[dev][di] = n;
+  return n;
 }
 
 // o[row j of table row r] = sum_s 2^(m_s - M) acc_s / sum_s 2^(m_s - M) l_s; rows with no key give 0.
