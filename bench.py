@@ -294,7 +294,7 @@ def run_kvsel(args):
     rank, world, local = dist_setup()
     w = S.by_name(args.workload)
     if args.layers:
-        w = w.with_(n_layers=args.layers)
+        w = S.scaled(w, n_layers=args.layers)
         if w.claa is not None:
             m, lp, nbuf, rate = w.claa
             w = w.with_(claa=(min(m, args.layers - 1), args.layers - 1, nbuf, rate))
@@ -469,7 +469,7 @@ def run_attend(args):
 
     w = S.by_name(args.workload)
     if args.layers:
-        w = w.with_(n_layers=args.layers)
+        w = S.scaled(w, n_layers=args.layers)
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     inp = S.make_inputs(w, str(dev))
