@@ -36,14 +36,17 @@ constexpr int kTileKeys = 128;
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kThreadsTc = 32 * (2 + kEpiWarps);
-constexpr int kSeg2Max = 8192;     // prefix keys per pass-2 segment (rounded down to whole pages)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kEpiBarrier = 1;   // named barrier id of the epilogue warps
 
 enum : uint32_t { kWhereProducer = 1, kWhereMma = 2, kWhereEpilogue = 3, kWhereDrain = 4 };
 
+// Prefix keys per pass-2 segment (rounded down to whole pages): the segment's scores are held in
+// shared memory until it is pooled.
+constexpr int kSeg2Max = 8192;
+
 // Shared-memory plan (offsets from a 1024-byte aligned base).
-template <int RT, int D, int NK>
+template <bool PASS2, int RT, int D, int NK>
 struct Plan {
   static constexpr int kDBlocks = D / 64;                   // 128-byte swizzle atoms along d
   static constexpr uint32_t kQBlock = RT * 128;             // one d-block of Q: RT rows x 128 B
@@ -52,12 +55,17 @@ struct Plan {
   static constexpr uint32_t kKBytes = kKBlock * kDBlocks;
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kKOff = kQOff + kQBytes;
-  static constexpr uint32_t kSsOff = kKOff + NK * kKBytes;                 // pass-2 segment scores
-  static constexpr uint32_t kSsFloats = kSeg2Max + 128;
+  // With 256 rows, pass 2 adds each row's -lse to its logits on the tensor cores: one more K = 16
+  // product of a block of ones (128 keys) with the rows' -lse / scale split into bf16 parts.
+  static constexpr bool kFold = PASS2 && RT == 256;
+  static constexpr uint32_t kOnesOff = kKOff + NK * kKBytes;                // 128 rows x 32 B of bf16 ones
+  static constexpr uint32_t kCOff = kOnesOff + (kFold ? 128 * 32 : 0);     // RT rows x 32 B
+  static constexpr uint32_t kSsOff = kCOff + (kFold ? RT * 32 : 0);        // pass-2 segment scores
+  static constexpr uint32_t kSsFloats = PASS2 ? kSeg2Max + 128 : 0;
   static constexpr uint32_t kLseOff = kSsOff + kSsFloats * 4;             // pass-2 row lse (RT floats)
-  static constexpr uint32_t kRedOff = kLseOff + RT * 4;                   // pass-1 (m, l) exchange
+  static constexpr uint32_t kRedOff = kLseOff + (PASS2 ? RT * 4 : 0);     // pass-1 (m, l) exchange
   static constexpr uint32_t kNT = kTmemCols / RT;                         // TMEM accumulator stages
-  static constexpr uint32_t kBarOff = kRedOff + 128 * 8;
+  static constexpr uint32_t kBarOff = kRedOff + (PASS2 ? 0 : 128 * 8);
   // barriers: full[NK], empty[NK], tfull[NT], tempty[NT], q_full, q_empty, drain
   static constexpr uint32_t kNumBars = 2 * NK + 2 * kNT + 3;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;            // tmem slot, abort flag
@@ -146,49 +154,102 @@ __device__ __forceinline__ void fail(const TcArgs& a, volatile uint32_t* flag, u
   *flag = 1;
 }
 
-// ---------------------------------------------------------------- producer (one thread)
+// ---------------------------------------------------------------- producer (warp 0)
+// The rows' -lse / scale for the extra K = 16 product of pass 2 (256 rows): c / 2 as the sum of
+// three bf16 parts p1 + p2 + p3 (24 significant bits), stored as [p1 p2 p3 0 0 0 0 0] in both
+// 16-byte halves of the row's 32 bytes, so that the product with a row of ones gives c whichever
+// way the 32-byte swizzle permutes the halves.  Padding rows get c = -2^101: their p is 0.
+// Each lane writes rows lane, lane + 32, ...; the writes are made visible to the tensor cores'
+// operand reads before the warp's leader signals the unit's Q tile.
+template <int RT>
+__device__ __forceinline__ void write_fold_rows(const TcArgs& a, int unit, uint8_t* crow, int lane) {
+  const double inv = 1.0 / (double)a.sh.scale_log2;
+  for (int r = lane; r < RT; r += 32) {
+    __nv_bfloat16 p1, p2, p3;
+    if (r < a.sh.R) {
+      const double h = -0.5 * (double)a.lse[(int64_t)unit * a.sh.R + r] * inv;
+      p1 = __float2bfloat16_rn((float)h);
+      const double r1 = h - (double)__bfloat162float(p1);
+      p2 = __float2bfloat16_rn((float)r1);
+      p3 = __float2bfloat16_rn((float)(r1 - (double)__bfloat162float(p2)));
+    } else {
+      p1 = __float2bfloat16_rn(-0x1p100f);
+      p2 = p3 = __float2bfloat16_rn(0.f);
+    }
+    const uint32_t w0 = (uint32_t)__bfloat16_as_ushort(p1) | ((uint32_t)__bfloat16_as_ushort(p2) << 16);
+    const uint32_t w1 = (uint32_t)__bfloat16_as_ushort(p3);
+    uint4* dst = reinterpret_cast<uint4*>(crow + r * 32);
+    dst[0] = make_uint4(w0, w1, 0u, 0u);
+    dst[1] = make_uint4(w0, w1, 0u, 0u);
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+}
+
+// Lane 0 issues every TMA load and does every wait; the whole warp runs the loop (its decisions
+// are lane 0's, broadcast) so that all lanes can write the pass-2 row constants at a unit change.
 template <bool PASS2, int RT, int D, int NK>
 __device__ void produce(const CUtensorMap* tq, const CUtensorMap* tk, const TcArgs& a, const SeqTable& t,
-                        uint32_t base, volatile uint32_t* flag) {
-  using P = Plan<RT, D, NK>;
+                        uint32_t base, uint8_t* sbase, volatile uint32_t* flag) {
+  using P = Plan<PASS2, RT, D, NK>;
+  const int lane = threadIdx.x % 32;
+  const bool leader = lane == 0;
+  const bool fold = P::kFold && PASS2 && !a.sh.logits;
   const uint32_t bars = base + P::kBarOff;
   auto full = [&](int s) { return bars + 8u * s; };
   auto empty = [&](int s) { return bars + 8u * (NK + s); };
   const uint32_t q_full = bars + 8u * (2 * NK + 2 * P::kNT);
   const uint32_t q_empty = q_full + 8;
-  tma_prefetch_desc(tq);
-  tma_prefetch_desc(tk);
+  if (leader) {
+    tma_prefetch_desc(tq);
+    tma_prefetch_desc(tk);
+  }
   int ks = 0;
   uint32_t kph = 0, qph = 0;
   uint32_t n_fills = 0, n_q = 0;
   int prev_unit = -1;
   Work<PASS2> work(t);
-  for (Item it; !aborted(flag) && work.next(t, a.sh, it);) {
+  Item it;
+  while (__shfl_sync(0xffffffffu, leader && !aborted(flag) ? 1 : 0, 0) && work.next(t, a.sh, it)) {
     if (it.unit != prev_unit) {
-      if (!mbar_wait(q_empty, qph ^ 1)) { fail(a, flag, kWhereProducer); break; }
-      mbar_expect_tx(q_full, P::kQBytes);
+      int ok = 1;
+      if (leader) ok = mbar_wait(q_empty, qph ^ 1) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        if (leader) fail(a, flag, kWhereProducer);
+        break;
+      }
+      if (fold) write_fold_rows<RT>(a, it.unit, sbase + P::kCOff, lane);
+      if (leader) {
+        mbar_expect_tx(q_full, P::kQBytes);
 #pragma unroll
-      for (int db = 0; db < P::kDBlocks; ++db)
+        for (int db = 0; db < P::kDBlocks; ++db)
 #pragma unroll
-        for (int m = 0; m < RT / 128; ++m)
-          tma_load_2d(base + P::kQOff + db * P::kQBlock + m * 16384, tq, db * 64, it.q_row0 + m * 128, q_full);
+          for (int m = 0; m < RT / 128; ++m)
+            tma_load_2d(base + P::kQOff + db * P::kQBlock + m * 16384, tq, db * 64, it.q_row0 + m * 128, q_full);
+      }
       qph ^= 1;
       ++n_q;
       prev_unit = it.unit;
     }
-    bool ok = true;
-    for (int t0 = it.ta; t0 < it.tb; t0 += kTileKeys) {
-      if (!mbar_wait(empty(ks), kph ^ 1)) { ok = false; break; }
-      mbar_expect_tx(full(ks), P::kKBytes);
-      const uint32_t dst = base + P::kKOff + ks * P::kKBytes;
+    int ok = 1;
+    if (leader) {
+      for (int t0 = it.ta; t0 < it.tb; t0 += kTileKeys) {
+        if (!mbar_wait(empty(ks), kph ^ 1)) { ok = 0; break; }
+        mbar_expect_tx(full(ks), P::kKBytes);
+        const uint32_t dst = base + P::kKOff + ks * P::kKBytes;
 #pragma unroll
-      for (int db = 0; db < P::kDBlocks; ++db)
-        tma_load_2d(dst + db * P::kKBlock, tk, db * 64, it.k_row0 + t0, full(ks));
-      ++n_fills;
-      if (++ks == NK) { ks = 0; kph ^= 1; }
+        for (int db = 0; db < P::kDBlocks; ++db)
+          tma_load_2d(dst + db * P::kKBlock, tk, db * 64, it.k_row0 + t0, full(ks));
+        ++n_fills;
+        if (++ks == NK) { ks = 0; kph ^= 1; }
+      }
     }
-    if (!ok) { fail(a, flag, kWhereProducer); break; }
+    if (!__shfl_sync(0xffffffffu, ok, 0)) {
+      if (leader) fail(a, flag, kWhereProducer);
+      break;
+    }
   }
+  if (!leader) return;
   // Loads still in flight (possible only after an abort) must land before the CTA exits:
   // wait for the phase of each stage's last fill (returns at once when already complete).
   for (int s = 0; s < NK; ++s) {
@@ -204,7 +265,7 @@ __device__ void produce(const CUtensorMap* tq, const CUtensorMap* tk, const TcAr
 template <bool PASS2, int RT, int D, int NK>
 __device__ void issue_mma(const TcArgs& a, const SeqTable& t, uint32_t base, uint32_t tmem,
                           volatile uint32_t* flag) {
-  using P = Plan<RT, D, NK>;
+  using P = Plan<PASS2, RT, D, NK>;
   const uint32_t bars = base + P::kBarOff;
   auto full = [&](int s) { return bars + 8u * s; };
   auto empty = [&](int s) { return bars + 8u * (NK + s); };
@@ -215,6 +276,7 @@ __device__ void issue_mma(const TcArgs& a, const SeqTable& t, uint32_t base, uin
   const uint32_t drain = q_empty + 8;
   // pass 1: M = 128 window rows (per M block), N = 128 keys;  pass 2: M = 128 keys, N = RT rows
   constexpr uint32_t idesc = PASS2 ? umma_idesc_bf16(128, RT) : umma_idesc_bf16(128, 128);
+  const bool fold = P::kFold && PASS2 && !a.sh.logits;
   int ks = 0, ts = 0;
   uint32_t kph = 0, tph = 0, qph = 0;
   int prev_unit = -1;
@@ -247,6 +309,8 @@ __device__ void issue_mma(const TcArgs& a, const SeqTable& t, uint32_t base, uin
                       umma_desc_sw128(kbase + db * P::kKBlock + off), idesc, kk > 0);
         }
       }
+      if (fold)   // + (-lse / scale) of every row: ones (keys) x the rows' constants
+        umma_bf16(d_tmem, umma_desc_sw32(base + P::kOnesOff), umma_desc_sw32(base + P::kCOff), idesc, 1);
       issued = true;
       umma_commit(empty(ks));     // K stage free once these MMAs have read it
       umma_commit(tfull(ts));     // accumulator ready for the epilogue
@@ -325,9 +389,17 @@ __device__ __forceinline__ float expsum64(const float* v, float scale, float off
   return tree_sum2<4>(a);
 }
 
+// Exponent argument of a column pair: v * scale + nl (FOLDED: the -lse is already in v).
+template <bool FOLDED>
+__device__ __forceinline__ float2 exp_arg2(float v0, float v1, float2 sc, const float2* nl, int i) {
+  if constexpr (FOLDED) return __fmul2_rn(make_float2(v0, v1), sc);
+  else return __ffma2_rn(make_float2(v0, v1), sc, nl[i]);
+}
+
 // Column mass of 64 rows for one key: sum (MAXW = 0) or max over heads of MAXW rows of
-// sum_i 2^(v_i * scale + nl_i), nl = -lse of each row, held in registers as pairs.
-template <int MAXW>
+// sum_i 2^(v_i * scale + nl_i), nl = -lse of each row as pairs (FOLDED: v_i * scale alone,
+// the accumulator already holding z - lse / scale).
+template <int MAXW, bool FOLDED = false>
 __device__ __forceinline__ float colmass64(const float* v, const float2* nl, float scale) {
   const float2 sc = make_float2(scale, scale);
   if constexpr (MAXW == 0) {
@@ -336,7 +408,7 @@ __device__ __forceinline__ float colmass64(const float* v, const float2* nl, flo
     for (int k = 0; k < 4; ++k) a[k] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < 32; ++i)
-      a[i & 3] = __fadd2_rn(a[i & 3], ex2x2(__ffma2_rn(make_float2(v[2 * i], v[2 * i + 1]), sc, nl[i])));
+      a[i & 3] = __fadd2_rn(a[i & 3], ex2x2(exp_arg2<FOLDED>(v[2 * i], v[2 * i + 1], sc, nl, i)));
     return tree_sum2<4>(a);
   } else {
     constexpr int HW = MAXW < 64 ? MAXW : 64;      // rows per head
@@ -351,7 +423,7 @@ __device__ __forceinline__ float colmass64(const float* v, const float2* nl, flo
 #pragma unroll
       for (int i = 0; i < NP; ++i) {
         const int c = h * NP + i;
-        a[i % NA] = __fadd2_rn(a[i % NA], ex2x2(__ffma2_rn(make_float2(v[2 * c], v[2 * c + 1]), sc, nl[c])));
+        a[i % NA] = __fadd2_rn(a[i % NA], ex2x2(exp_arg2<FOLDED>(v[2 * c], v[2 * c + 1], sc, nl, c)));
       }
       red = fmaxf(red, tree_sum2<NA>(a));
     }
@@ -391,18 +463,32 @@ __device__ __forceinline__ float linmass64(const float* v, const float2* w) {
   }
 }
 
-// Online (max, sum) update of one row with 64 new columns, the first nvis of them visible.
+// Online (offset, sum) update of one row with 64 new columns, the first nvis of them visible:
+// l = sum of 2^(z scale - m).  Once the row has an offset m, the exponentials are taken against
+// it without waiting for the new columns' maximum, which is formed beside them; only a column
+// above m + 8 (each term then stays below 2^8) moves the offset and recomputes the sum.  The
+// row's log-sum-exp m + log2 l is the same whichever offset the sum was taken against.
 __device__ __forceinline__ void online_update64(float* v, int nvis, float scale, float& m, float& l) {
   if (nvis < 64) {
 #pragma unroll
     for (int i = 0; i < 64; ++i)
       if (i >= nvis) v[i] = -INFINITY;
   }
-  const float mx = max64(v);
-  if (mx > -INFINITY) {
-    const float nm = fmaxf(m, mx * scale);
-    l = l * fast_ex2(m - nm) + expsum64(v, scale, -nm);
-    m = nm;
+  if (m == -INFINITY) {                     // first visible columns of the row in this segment
+    const float mx = max64(v);
+    if (mx > -INFINITY) {
+      m = mx * scale;
+      l = expsum64(v, scale, -m);
+    }
+    return;
+  }
+  const float s = expsum64(v, scale, -m);
+  const float mx = max64(v) * scale;
+  if (mx > m + 8.f) {
+    l = l * fast_ex2(m - mx) + expsum64(v, scale, -mx);
+    m = mx;
+  } else {
+    l += s;
   }
 }
 
@@ -432,7 +518,7 @@ __device__ __forceinline__ EpiThread epi_thread() {
 template <int RT, int D, int NK>
 __device__ void epilogue_pass1(const TcArgs& a, const SeqTable& t, uint32_t base, uint8_t* sbase,
                                uint32_t tmem, volatile uint32_t* flag) {
-  using P = Plan<RT, D, NK>;
+  using P = Plan<false, RT, D, NK>;
   constexpr int kChunks = RT == 256 ? 4 : 2;
   constexpr int kCols = kChunks * 32;
   const EpiThread e = epi_thread();
@@ -577,7 +663,7 @@ __device__ void pool_segment(const float* S, int ta, int tb, int a0, int a1, int
 template <int RT, int D, int NK, int MAXW>
 __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base, uint8_t* sbase,
                                uint32_t tmem, volatile uint32_t* flag) {
-  using P = Plan<RT, D, NK>;
+  using P = Plan<true, RT, D, NK>;
   constexpr int kHalf = RT / 2;
   constexpr int kChunks = kHalf / 32;
   const EpiThread e = epi_thread();
@@ -588,6 +674,7 @@ __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base
   float* lse_s = reinterpret_cast<float*>(sbase + P::kLseOff);   // holds -lse per row
   const float* nlse = lse_s;
   const float scale = a.sh.scale_log2;
+  const bool fold = P::kFold && !a.sh.logits;
   const int col0 = e.wg * kHalf;
   const int pr = (a.sh.pool_k - 1) / 2;
   const int P_ = a.sh.page_size;
@@ -597,7 +684,7 @@ __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base
   for (Item it; work.next(t, a.sh, it);) {
     epi_sync();                                          // readers of the previous item are done
     for (int i = e.etid; i < it.tb - it.ta; i += kEpiThreads) Ss[i] = 0.f;
-    for (int i = e.etid; i < RT; i += kEpiThreads) {
+    for (int i = e.etid; i < RT && !fold; i += kEpiThreads) {
       if (a.sh.logits) lse_s[i] = i < a.sh.R ? a.sh.scale_nat : 0.f;    // row weights of the logit sum
       else lse_s[i] = i < a.sh.R ? -a.lse[(int64_t)it.unit * a.sh.R + i] : -INFINITY;   // padding rows: p = 0
     }
@@ -631,9 +718,15 @@ __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base
           tc_fence_before();
           __syncwarp();
           if (e.lane == 0) mbar_arrive(tempty(ts));
-          const float2* nls = reinterpret_cast<const float2*>(nlse + col0);
-          const float r0 = a.sh.logits ? linmass64<MAXW>(v64, nls) : colmass64<MAXW>(v64, nls, scale);
-          const float r1 = a.sh.logits ? linmass64<MAXW>(w64, nls + 32) : colmass64<MAXW>(w64, nls + 32, scale);
+          float r0, r1;
+          if (fold) {   // the accumulator holds z - lse / scale (no per-row operand)
+            r0 = colmass64<MAXW, true>(v64, nullptr, scale);
+            r1 = colmass64<MAXW, true>(w64, nullptr, scale);
+          } else {
+            const float2* nls = reinterpret_cast<const float2*>(nlse + col0);
+            r0 = a.sh.logits ? linmass64<MAXW>(v64, nls) : colmass64<MAXW>(v64, nls, scale);
+            r1 = a.sh.logits ? linmass64<MAXW>(w64, nls + 32) : colmass64<MAXW>(w64, nls + 32, scale);
+          }
           red = MAXW == 0 ? r0 + r1 : fmaxf(r0, r1);
         }
         const int key = t0 + e.lrow;
@@ -667,7 +760,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) score_tc_kernel(const __grid_co
                                                                  const __grid_constant__ CUtensorMap tk,
                                                                  const __grid_constant__ TcArgs a,
                                                                  const __grid_constant__ SeqTable t) {
-  using P = Plan<RT, D, NK>;
+  using P = Plan<PASS2, RT, D, NK>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t base = smem_addr(sbase);
@@ -688,19 +781,23 @@ __global__ void __launch_bounds__(kThreadsTc, 1) score_tc_kernel(const __grid_co
     *flag = 0;
     fence_barrier_init();
   }
+  if (P::kFold && PASS2) {   // bf16 ones, the A operand of the -lse product
+    uint32_t* ones = reinterpret_cast<uint32_t*>(sbase + P::kOnesOff);
+    for (int i = threadIdx.x; i < 128 * 32 / 4; i += blockDim.x) ones[i] = 0x3F803F80u;
+    fence_proxy_async_smem();
+  }
   if (warp == 1) tmem_alloc(smem_addr(tslot), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
   if (warp == 0) {
-    if (lane == 0) produce<PASS2, RT, D, NK>(&tq, &tk, a, t, base, flag);
+    produce<PASS2, RT, D, NK>(&tq, &tk, a, t, base, sbase, flag);
   } else if (warp == 1) {
     if (lane == 0) issue_mma<PASS2, RT, D, NK>(a, t, base, tmem, flag);
-  } else if (PASS2) {
-    epilogue_pass2<RT, D, NK, MAXW>(a, t, base, sbase, tmem, flag);
   } else {
-    epilogue_pass1<RT, D, NK>(a, t, base, sbase, tmem, flag);
+    if constexpr (PASS2) epilogue_pass2<RT, D, NK, MAXW>(a, t, base, sbase, tmem, flag);
+    else epilogue_pass1<RT, D, NK>(a, t, base, sbase, tmem, flag);
   }
   tc_fence_before();
   __syncthreads();
@@ -759,7 +856,7 @@ DevInfo device_info() {
 template <bool PASS2, int RT, int D, int NK, int MAXW>
 kvsel_status launch_one(const char* name, const CUtensorMap& tq, const CUtensorMap& tk, const TcArgs& a,
                         const SeqTable& t, int sms, cudaStream_t s) {
-  using P = Plan<RT, D, NK>;
+  using P = Plan<PASS2, RT, D, NK>;
   auto kern = score_tc_kernel<PASS2, RT, D, NK, MAXW>;
   if (set_smem((const void*)kern, P::kSmem) != cudaSuccess) return KVSEL_ERR_CUDA;
   const int grid = t.n_items < sms ? t.n_items : sms;
@@ -771,10 +868,12 @@ kvsel_status launch_one(const char* name, const CUtensorMap& tq, const CUtensorM
 template <int RT, int D>
 kvsel_status run_tc(const TcArgs& a, const SeqTable& t1, const SeqTable& t2, const CUtensorMap& tq,
                     const CUtensorMap& tk, int sms, cudaStream_t s) {
+  // K stages: as many as shared memory holds beside Q (and pass 2's segment buffers)
+  constexpr int NK1 = (RT == 256 && D == 128) ? 5 : 4;
   constexpr int NK = (RT == 256 && D == 128) ? 3 : 4;
   kvsel_status st;
   if (!a.sh.logits && !a.sh.lse_given) {   // the softmax needs each row's log-sum-exp first
-    if ((st = launch_one<false, RT, D, NK, 0>("score_pass1_tc", tq, tk, a, t1, sms, s)) != KVSEL_OK) return st;
+    if ((st = launch_one<false, RT, D, NK1, 0>("score_pass1_tc", tq, tk, a, t1, sms, s)) != KVSEL_OK) return st;
     if ((st = launch_lse_combine(a.sh, t1, a.part, a.lse, s)) != KVSEL_OK) return st;
   }
   if (a.sh.group_reduce != KVSEL_REDUCE_MAX)

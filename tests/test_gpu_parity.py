@@ -35,6 +35,9 @@ CASES = {
     # max over heads whose window is not a power of two: served by the CUDA-core kernels
     "w24_max_cudacore": S.Workload("edge_w24", 93, 2, 8, 2, 128, 24, (3000,), group_reduce="max", pool_k=5,
                                    k_keep=200, n_clusters=4),
+    # group of 6 x 32 rows = 192 rows in a 256-row tile: 64 padding rows must carry no mass
+    "g6_rt256_padded": S.Workload("edge_g6", 98, 1, 12, 2, 128, 32, (2222,), group_reduce="sum", pool_k=7,
+                                  k_keep=100, n_clusters=4),
     # group of 8 with W = 16 and max reduce (256 padded rows, head width below a warp)
     "g16w16_max": S.Workload("edge_g16", 94, 1, 16, 1, 64, 16, (2500,), group_reduce="max", pool_k=3,
                              k_keep=64, page_size=16, n_recent=2, n_clusters=4),
