@@ -17,7 +17,8 @@
 // laid end to end, cut into pieces at unit ends and every kSeg2Max keys, so
 // that every CTA emits the same number of pages however many units there are.  Warp roles: warp 0 issues TMA (Q once per unit, K
 // tiles through an NK-stage ring), warp 1 owns TMEM and issues UMMA into a
-// ring of TMEM accumulators, warps 2..9 are the epilogue.  All hand-offs are
+// ring of TMEM accumulators, warps 2.. are the epilogue (8 warps; 16 in pass 1
+// over 256 rows).  All hand-offs are
 // mbarriers with bounded waits; a wait that gives up records
 // KVSEL_ERR_TIMEOUT in the workspace error word and the CTA unwinds.
 #include <cudaTypedefs.h>
@@ -33,9 +34,6 @@ namespace {
 using namespace sm100;
 
 constexpr int kTileKeys = 128;
-constexpr int kEpiWarps = 8;
-constexpr int kEpiThreads = 32 * kEpiWarps;
-constexpr int kThreadsTc = 32 * (2 + kEpiWarps);
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kEpiBarrier = 1;   // named barrier id of the epilogue warps
 
@@ -58,6 +56,11 @@ struct Plan {
   // With 256 rows, pass 2 adds each row's -lse to its logits on the tensor cores: one more K = 16
   // product of a block of ones (128 keys) with the rows' -lse / scale split into bf16 parts.
   static constexpr bool kFold = PASS2 && RT == 256;
+  // Epilogue warps: 8, or 16 for pass 1 over 256 rows (four warps per TMEM lane quarter, each
+  // taking 64 of the 256 accumulator columns a lane holds, so that every SM sub-partition has four
+  // warps' exponentials in flight).
+  static constexpr int kEW = (!PASS2 && RT == 256) ? 16 : 8;
+  static constexpr int kThreads = 32 * (2 + kEW);
   static constexpr uint32_t kOnesOff = kKOff + NK * kKBytes;                // 128 rows x 32 B of bf16 ones
   static constexpr uint32_t kCOff = kOnesOff + (kFold ? 128 * 32 : 0);     // RT rows x 32 B
   static constexpr uint32_t kSsOff = kCOff + (kFold ? RT * 32 : 0);        // pass-2 segment scores
@@ -65,7 +68,7 @@ struct Plan {
   static constexpr uint32_t kLseOff = kSsOff + kSsFloats * 4;             // pass-2 row lse (RT floats)
   static constexpr uint32_t kRedOff = kLseOff + (PASS2 ? RT * 4 : 0);     // pass-1 (m, l) exchange
   static constexpr uint32_t kNT = kTmemCols / RT;                         // TMEM accumulator stages
-  static constexpr uint32_t kBarOff = kRedOff + (PASS2 ? 0 : 128 * 8);
+  static constexpr uint32_t kBarOff = kRedOff + (PASS2 ? 0 : 128 * 8);   // 128 rows' (m, l) per exchange round
   // barriers: full[NK], empty[NK], tfull[NT], tempty[NT], q_full, q_empty, drain
   static constexpr uint32_t kNumBars = 2 * NK + 2 * kNT + 3;
   static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;            // tmem slot, abort flag
@@ -327,8 +330,9 @@ __device__ void issue_mma(const TcArgs& a, const SeqTable& t, uint32_t base, uin
 }
 
 // ---------------------------------------------------------------- epilogue helpers
+template <int EW>
 __device__ __forceinline__ void epi_sync() {
-  asm volatile("bar.sync %0, %1;" ::"r"(kEpiBarrier), "r"(kEpiThreads) : "memory");
+  asm volatile("bar.sync %0, %1;" ::"r"(kEpiBarrier), "r"(32 * EW) : "memory");
 }
 
 __device__ __forceinline__ float fast_ex2(float x) {
@@ -465,9 +469,11 @@ __device__ __forceinline__ float linmass64(const float* v, const float2* w) {
 
 // Online (offset, sum) update of one row with 64 new columns, the first nvis of them visible:
 // l = sum of 2^(z scale - m).  Once the row has an offset m, the exponentials are taken against
-// it without waiting for the new columns' maximum, which is formed beside them; only a column
-// above m + 8 (each term then stays below 2^8) moves the offset and recomputes the sum.  The
-// row's log-sum-exp m + log2 l is the same whichever offset the sum was taken against.
+// it without forming the new columns' maximum: when their sum s is at most 2^8 every term is, so
+// no column lies more than 8 above the offset and s is added as it is.  A larger (or infinite) s
+// moves the offset to the columns' maximum, which is then at least m + 2 (64 terms of at most
+// 2^(max - m) exceed 2^8), and the sum is rescaled and retaken.  The row's log-sum-exp
+// m + log2 l is the same whichever offset the sum was taken against.
 __device__ __forceinline__ void online_update64(float* v, int nvis, float scale, float& m, float& l) {
   if (nvis < 64) {
 #pragma unroll
@@ -483,22 +489,22 @@ __device__ __forceinline__ void online_update64(float* v, int nvis, float scale,
     return;
   }
   const float s = expsum64(v, scale, -m);
-  const float mx = max64(v) * scale;
-  if (mx > m + 8.f) {
+  if (s <= 256.f) {
+    l += s;
+  } else {
+    const float mx = max64(v) * scale;
     l = l * fast_ex2(m - mx) + expsum64(v, scale, -mx);
     m = mx;
-  } else {
-    l += s;
   }
 }
 
-// Epilogue thread geometry: warps 2..9; warp w may read TMEM lanes 32*(w%4) .. +31.
+// Epilogue thread geometry: warps 2..; warp w may read TMEM lanes 32*(w%4) .. +31.
 struct EpiThread {
-  int wg;        // epilogue warpgroup 0 / 1
+  int wg;        // epilogue warpgroup 0 .. (epilogue warps / 4) - 1
   int quarter;   // TMEM lane quarter
   int lane;
   int lrow;      // TMEM lane = quarter * 32 + lane
-  int etid;      // 0 .. kEpiThreads-1
+  int etid;      // 0 .. (epilogue threads) - 1
 };
 
 __device__ __forceinline__ EpiThread epi_thread() {
@@ -512,22 +518,36 @@ __device__ __forceinline__ EpiThread epi_thread() {
   return e;
 }
 
+// Whether the accumulator stage (bar, parity) may be read.  `ready` is the previous tile's
+// non-blocking probe of it, issued before that tile's arithmetic so that its latency overlaps the
+// arithmetic; otherwise the warp waits (bounded), reading the abort flag only then.  The tensor-
+// memory loads that follow are warp-collective, so the decision is the warp's.
+__device__ __forceinline__ bool tile_ready(bool ready, uint32_t bar, uint32_t parity, volatile uint32_t* flag) {
+  if (__all_sync(0xffffffffu, ready)) return true;
+  return __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(bar, parity));
+}
+
 // ---------------------------------------------------------------- pass 1 epilogue
 // RT = 128: both warpgroups see all 128 rows, warpgroup e takes tile columns [64e, 64e + 64).
-// RT = 256: warpgroup e takes rows 128e .. 128e + 127 (its own accumulator), all 128 columns.
+// RT = 256: warpgroup e takes rows 128 (e % 2) .. + 127 (accumulator block e % 2) and tile columns
+// [64 (e / 2), 64 (e / 2) + 64).  Either way each thread holds one row's (offset, sum) over its
+// 64-column half of every tile, and the halves are merged once per segment through shared memory
+// (one exchange per 128 rows).
 template <int RT, int D, int NK>
 __device__ void epilogue_pass1(const TcArgs& a, const SeqTable& t, uint32_t base, uint8_t* sbase,
                                uint32_t tmem, volatile uint32_t* flag) {
   using P = Plan<false, RT, D, NK>;
-  constexpr int kChunks = RT == 256 ? 4 : 2;
-  constexpr int kCols = kChunks * 32;
+  constexpr int EW = P::kEW;
+  static_assert(EW / 4 * 64 * 128 == RT * kTileKeys, "every (row, column) of a tile has one thread");
   const EpiThread e = epi_thread();
   const uint32_t bars = base + P::kBarOff;
   auto tfull = [&](int s) { return bars + 8u * (2 * NK + s); };
   auto tempty = [&](int s) { return bars + 8u * (2 * NK + P::kNT + s); };
-  const int row = RT == 256 ? e.lrow + 128 * e.wg : e.lrow;
-  const uint32_t col0 = RT == 256 ? 128u * e.wg : 64u * e.wg;   // TMEM column within a stage
-  const int key0 = RT == 256 ? 0 : 64 * e.wg;                    // tile key of that column
+  const int rblk = RT == 256 ? (e.wg & 1) : 0;                 // accumulator block (128 rows)
+  const int chalf = RT == 256 ? (e.wg >> 1) : e.wg;            // 64-column half of the tile
+  const int row = e.lrow + 128 * rblk;
+  const uint32_t col0 = 128u * rblk + 64u * chalf;             // TMEM column within a stage
+  const int key0 = 64 * chalf;                                  // tile key of that column
   float* red = reinterpret_cast<float*>(sbase + P::kRedOff);
   const float scale = a.sh.scale_log2;
   const bool rvalid = row < a.sh.R;
@@ -539,52 +559,38 @@ __device__ void epilogue_pass1(const TcArgs& a, const SeqTable& t, uint32_t base
     const int row_last = it.L + (rvalid ? row % a.sh.W : 0);     // last key this row sees
     const int vis_end = min(it.tb, row_last + 1);
     float m = -INFINITY, l = 0.f;
+    bool ready = false;      // this tile's accumulator was seen complete by the previous tile's probe
     for (int t0 = it.ta; t0 < it.tb; t0 += kTileKeys) {
-      // the tensor-memory loads below are warp-collective: decide per warp
-      const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(tfull(ts), tph));
+      const bool ok = tile_ready(ready, tfull(ts), tph, flag);
       if (!ok && e.lane == 0) fail(a, flag, kWhereEpilogue);
+      float v[64];
       if (ok) {
         tc_fence_after();
-        const uint32_t taddr = tmem + ((uint32_t)(e.quarter * 32) << 16) + ts * RT + col0;
-        float v[64];
-        if (kChunks == 2) {
-          tmem_ld64(taddr, v);
-          tc_fence_before();
-          __syncwarp();
-          if (e.lane == 0) mbar_arrive(tempty(ts));
-          if (rvalid) online_update64(v, vis_end - (t0 + key0), scale, m, l);
-        } else {
-          float v2[64];
-          tmem_ld64(taddr, v);
-          tmem_ld64(taddr + 64, v2);
-          tc_fence_before();
-          __syncwarp();
-          if (e.lane == 0) mbar_arrive(tempty(ts));
-          if (rvalid) {
-            online_update64(v, vis_end - (t0 + key0), scale, m, l);
-            online_update64(v2, vis_end - (t0 + key0 + 64), scale, m, l);
-          }
-        }
+        tmem_ld64(tmem + ((uint32_t)(e.quarter * 32) << 16) + ts * RT + col0, v);
+        tc_fence_before();
+        __syncwarp();
+        if (e.lane == 0) mbar_arrive(tempty(ts));
       }
       if (++ts == (int)P::kNT) { ts = 0; tph ^= 1; }
+      ready = t0 + kTileKeys < it.tb && mbar_test_wait(tfull(ts), tph);   // answer used at the next tile
+      if (ok && rvalid) online_update64(v, vis_end - (t0 + key0), scale, m, l);
     }
-    // per-row partial (m, l) of this segment
-    if (RT == 128) {
-      epi_sync();
-      if (e.wg == 1) {
+    // per-row partial (m, l) of this segment: the second half's threads hand theirs over
+#pragma unroll
+    for (int rb = 0; rb < RT / 128; ++rb) {
+      epi_sync<EW>();
+      if (rblk == rb && chalf == 1) {
         red[2 * e.lrow] = m;
         red[2 * e.lrow + 1] = l;
       }
-      epi_sync();
-      if (e.wg == 0 && rvalid) {
+      epi_sync<EW>();
+      if (rblk == rb && chalf == 0 && rvalid) {
         const float m2 = red[2 * e.lrow], l2 = red[2 * e.lrow + 1];
         const float M = fmaxf(m, m2);
         float S = 0.f;
         if (M > -INFINITY) S = (m > -INFINITY ? l * fast_ex2(m - M) : 0.f) + (m2 > -INFINITY ? l2 * fast_ex2(m2 - M) : 0.f);
         a.part[(int64_t)item * a.sh.R + row] = make_float2(M, S);
       }
-    } else if (rvalid) {
-      a.part[(int64_t)item * a.sh.R + row] = make_float2(m, l);
     }
   }
 }
@@ -664,6 +670,8 @@ template <int RT, int D, int NK, int MAXW>
 __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base, uint8_t* sbase,
                                uint32_t tmem, volatile uint32_t* flag) {
   using P = Plan<true, RT, D, NK>;
+  constexpr int EW = P::kEW;
+  constexpr int kEpiThreads = 32 * EW;
   constexpr int kHalf = RT / 2;
   constexpr int kChunks = kHalf / 32;
   const EpiThread e = epi_thread();
@@ -682,13 +690,13 @@ __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base
   uint32_t tph = 0;
   Work<true> work(t);
   for (Item it; work.next(t, a.sh, it);) {
-    epi_sync();                                          // readers of the previous item are done
+    epi_sync<EW>();                                          // readers of the previous item are done
     for (int i = e.etid; i < it.tb - it.ta; i += kEpiThreads) Ss[i] = 0.f;
     for (int i = e.etid; i < RT && !fold; i += kEpiThreads) {
       if (a.sh.logits) lse_s[i] = i < a.sh.R ? a.sh.scale_nat : 0.f;    // row weights of the logit sum
       else lse_s[i] = i < a.sh.R ? -a.lse[(int64_t)it.unit * a.sh.R + i] : -INFINITY;   // padding rows: p = 0
     }
-    epi_sync();
+    epi_sync<EW>();
     // -lse of this warpgroup's 64 rows in registers (column pairs); with 128 rows per warpgroup
     // they are read from shared memory instead (the registers would not fit)
     float2 nl[kChunks == 2 ? 32 : 1];
@@ -739,7 +747,7 @@ __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base
       }
       if (++ts == (int)P::kNT) { ts = 0; tph ^= 1; }
     }
-    epi_sync();
+    epi_sync<EW>();
     if (aborted(flag)) continue;
     // max-pool over prefix positions, then page reduce (DELTA key designs 2-3)
     const SeqInfo& si = t.s[it.b];
@@ -756,7 +764,7 @@ __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base
 
 // ---------------------------------------------------------------- kernels
 template <bool PASS2, int RT, int D, int NK, int MAXW>
-__global__ void __launch_bounds__(kThreadsTc, 1) score_tc_kernel(const __grid_constant__ CUtensorMap tq,
+__global__ void __launch_bounds__(Plan<PASS2, RT, D, NK>::kThreads, 1) score_tc_kernel(const __grid_constant__ CUtensorMap tq,
                                                                  const __grid_constant__ CUtensorMap tk,
                                                                  const __grid_constant__ TcArgs a,
                                                                  const __grid_constant__ SeqTable t) {
@@ -775,7 +783,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) score_tc_kernel(const __grid_co
     }
     for (uint32_t s = 0; s < P::kNT; ++s) {
       mbar_init(bars + 8u * (2 * NK + s), 1);          // tfull: MMA commit
-      mbar_init(bars + 8u * (2 * NK + P::kNT + s), kEpiWarps);   // tempty: one arrival per epilogue warp
+      mbar_init(bars + 8u * (2 * NK + P::kNT + s), P::kEW);   // tempty: one arrival per epilogue warp
     }
     for (int s = 0; s < 3; ++s) mbar_init(bars + 8u * (2 * NK + 2 * P::kNT + s), 1);   // q_full, q_empty, drain
     *flag = 0;
@@ -861,7 +869,7 @@ kvsel_status launch_one(const char* name, const CUtensorMap& tq, const CUtensorM
   if (set_smem((const void*)kern, P::kSmem) != cudaSuccess) return KVSEL_ERR_CUDA;
   const int grid = t.n_items < sms ? t.n_items : sms;
   TraceScope ts(name, s);
-  kern<<<grid, kThreadsTc, P::kSmem, s>>>(tq, tk, a, t);
+  kern<<<grid, P::kThreads, P::kSmem, s>>>(tq, tk, a, t);
   return launch_status();
 }
 
