@@ -704,9 +704,15 @@ __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base
 #pragma unroll
       for (int c = 0; c < 32; ++c) nl[c] = make_float2(nlse[col0 + 2 * c], nlse[col0 + 2 * c + 1]);
     }
+    // 256 rows (128 columns per thread): the next tile's accumulator is probed before this tile's
+    // arithmetic, as in pass 1
+    bool ready = false;
     for (int t0 = it.ta; t0 < it.tb; t0 += kTileKeys) {
       // the tensor-memory loads below are warp-collective: decide per warp
-      const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(tfull(ts), tph));
+      bool ok;
+      if constexpr (kChunks == 4) ok = tile_ready(ready, tfull(ts), tph, flag);
+      else ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(tfull(ts), tph));
+      ready = false;
       if (!ok && e.lane == 0) fail(a, flag, kWhereEpilogue);
       if (ok) {
         tc_fence_after();
@@ -726,6 +732,8 @@ __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base
           tc_fence_before();
           __syncwarp();
           if (e.lane == 0) mbar_arrive(tempty(ts));
+          const int tn = ts + 1 == (int)P::kNT ? 0 : ts + 1;
+          ready = t0 + kTileKeys < it.tb && mbar_test_wait(tfull(tn), tn == 0 ? tph ^ 1 : tph);
           float r0, r1;
           if (fold) {   // the accumulator holds z - lse / scale (no per-row operand)
             r0 = colmass64<MAXW, true>(v64, nullptr, scale);
