@@ -56,11 +56,13 @@ struct Plan {
   // With 256 rows, pass 2 adds each row's -lse to its logits on the tensor cores: one more K = 16
   // product of a block of ones (128 keys) with the rows' -lse / scale split into bf16 parts.
   static constexpr bool kFold = PASS2 && RT == 256;
-  // Epilogue warps: 8, or 16 for pass 1 over 256 rows (four warps per TMEM lane quarter, each
-  // taking 64 of the 256 accumulator columns a lane holds, so that every SM sub-partition has four
-  // warps' exponentials in flight).
-  static constexpr int kEW = (!PASS2 && RT == 256) ? 16 : 8;
+  // Epilogue warps: 8, or 16 over 256 rows (four warps per TMEM lane quarter, so that every SM
+  // sub-partition has four warps' exponentials in flight).  Pass 1 gives each warp 64 of the 256
+  // accumulator columns of its lanes in every tile; pass 2 gives the two pairs of warpgroups
+  // alternate tiles (one TMEM stage each), so only one pair's warps release a stage.
+  static constexpr int kEW = RT == 256 ? 16 : 8;
   static constexpr int kThreads = 32 * (2 + kEW);
+  static constexpr int kStageReaders = (PASS2 && RT == 256) ? kEW / 2 : kEW;
   static constexpr uint32_t kOnesOff = kKOff + NK * kKBytes;                // 128 rows x 32 B of bf16 ones
   static constexpr uint32_t kCOff = kOnesOff + (kFold ? 128 * 32 : 0);     // RT rows x 32 B
   static constexpr uint32_t kSsOff = kCOff + (kFold ? RT * 32 : 0);        // pass-2 segment scores
@@ -770,6 +772,91 @@ __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base
   }
 }
 
+// Pass 2 over 256 rows with 16 epilogue warps.  The pairs of warpgroups (0, 1) and (2, 3) take
+// alternate tiles: pair p the tiles this CTA takes at positions of parity p, always from TMEM stage
+// p.  Within a pair, warpgroup h takes rows [128 h, 128 h + 128) (TMEM columns), read as two
+// 64-column halves.  The pairs run a tile apart, so one pair's waits and loads overlap the other's
+// arithmetic.  A key's two partials (one per warpgroup of the pair) meet by shared-memory atomics:
+// with two addends the result does not depend on their order.
+template <int RT, int D, int NK, int MAXW>
+__device__ void epilogue_pass2_pairs(const TcArgs& a, const SeqTable& t, uint32_t base, uint8_t* sbase,
+                                     uint32_t tmem, volatile uint32_t* flag) {
+  using P = Plan<true, RT, D, NK>;
+  static_assert(RT == 256 && P::kEW == 16 && P::kNT == 2, "one TMEM stage per pair of warpgroups");
+  constexpr int kEpiThreads = 32 * P::kEW;
+  const EpiThread e = epi_thread();
+  const int pair = e.wg >> 1, half = e.wg & 1;
+  const uint32_t bars = base + P::kBarOff;
+  const uint32_t tfull = bars + 8u * (2 * NK + pair);
+  const uint32_t tempty = bars + 8u * (2 * NK + P::kNT + pair);
+  float* Ss = reinterpret_cast<float*>(sbase + P::kSsOff);
+  float* lse_s = reinterpret_cast<float*>(sbase + P::kLseOff);   // logits mode: row weights
+  const float2* nls = reinterpret_cast<const float2*>(lse_s + 128 * half);
+  const float scale = a.sh.scale_log2;
+  const bool fold = P::kFold && !a.sh.logits;                    // softmax: the accumulator holds z - lse / scale
+  const uint32_t lane_base = tmem + ((uint32_t)(e.quarter * 32) << 16) + pair * RT + 128 * half;
+  const int pr = (a.sh.pool_k - 1) / 2;
+  const int P_ = a.sh.page_size;
+  uint32_t tph = 0;
+  int nt = 0;                                                    // tiles this CTA has taken so far
+  Work<true> work(t);
+  for (Item it; work.next(t, a.sh, it);) {
+    epi_sync<P::kEW>();                                  // readers of the previous item are done
+    for (int i = e.etid; i < it.tb - it.ta; i += kEpiThreads) Ss[i] = 0.f;
+    for (int i = e.etid; i < RT && !fold; i += kEpiThreads) {
+      if (a.sh.logits) lse_s[i] = i < a.sh.R ? a.sh.scale_nat : 0.f;
+      else lse_s[i] = i < a.sh.R ? -a.lse[(int64_t)it.unit * a.sh.R + i] : -INFINITY;
+    }
+    epi_sync<P::kEW>();
+    for (int t0 = it.ta; t0 < it.tb; t0 += kTileKeys, ++nt) {
+      if ((nt & 1) != pair) continue;
+      // the tensor-memory loads below are warp-collective: decide per warp
+      const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(tfull, tph));
+      tph ^= 1;
+      if (!ok) {
+        if (e.lane == 0) fail(a, flag, kWhereEpilogue);
+        continue;
+      }
+      tc_fence_after();
+      float r0, r1;
+      {
+        float v[64];
+        tmem_ld64(lane_base, v);
+        r0 = fold ? colmass64<MAXW, true>(v, nullptr, scale)
+                  : (a.sh.logits ? linmass64<MAXW>(v, nls) : colmass64<MAXW>(v, nls, scale));
+      }
+      {
+        float v[64];
+        tmem_ld64(lane_base + 64, v);
+        tc_fence_before();
+        __syncwarp();
+        if (e.lane == 0) mbar_arrive(tempty);
+        r1 = fold ? colmass64<MAXW, true>(v, nullptr, scale)
+                  : (a.sh.logits ? linmass64<MAXW>(v, nls + 32) : colmass64<MAXW>(v, nls + 32, scale));
+      }
+      const float red = MAXW == 0 ? r0 + r1 : fmaxf(r0, r1);
+      const int key = t0 + e.lrow;
+      if (key < it.tb) {
+        // group max runs here with probabilities only, which are >= 0, so the int order is the float order
+        if constexpr (MAXW == 0) atomicAdd(&Ss[key - it.ta], red);
+        else atomicMax(reinterpret_cast<int*>(&Ss[key - it.ta]), __float_as_int(red));
+      }
+    }
+    epi_sync<P::kEW>();
+    if (aborted(flag)) continue;
+    const SeqInfo& si = t.s[it.b];
+    float* out = a.scores + si.s_off + ((int64_t)it.layer * a.sh.h_kv + it.g) * it.L;
+    float* pout = nullptr;
+    if (P_ > 1) {
+      const int n_pages = (it.L + P_ - 1) / P_;
+      pout = a.page_scores + si.p_off + ((int64_t)it.layer * a.sh.h_kv + it.g) * n_pages;
+    }
+    pool_segment(Ss, it.ta, it.tb, it.a0, it.a1, pr, P_, a.sh.page_reduce, a.sh.pool_type, a.sh.gscale, out, pout,
+                 e.etid, kEpiThreads);
+  }
+}
+
+
 // ---------------------------------------------------------------- kernels
 template <bool PASS2, int RT, int D, int NK, int MAXW>
 __global__ void __launch_bounds__(Plan<PASS2, RT, D, NK>::kThreads, 1) score_tc_kernel(const __grid_constant__ CUtensorMap tq,
@@ -791,7 +878,7 @@ __global__ void __launch_bounds__(Plan<PASS2, RT, D, NK>::kThreads, 1) score_tc_
     }
     for (uint32_t s = 0; s < P::kNT; ++s) {
       mbar_init(bars + 8u * (2 * NK + s), 1);          // tfull: MMA commit
-      mbar_init(bars + 8u * (2 * NK + P::kNT + s), P::kEW);   // tempty: one arrival per epilogue warp
+      mbar_init(bars + 8u * (2 * NK + P::kNT + s), P::kStageReaders);   // tempty: one arrival per reading warp
     }
     for (int s = 0; s < 3; ++s) mbar_init(bars + 8u * (2 * NK + 2 * P::kNT + s), 1);   // q_full, q_empty, drain
     *flag = 0;
@@ -812,7 +899,8 @@ __global__ void __launch_bounds__(Plan<PASS2, RT, D, NK>::kThreads, 1) score_tc_
   } else if (warp == 1) {
     if (lane == 0) issue_mma<PASS2, RT, D, NK>(a, t, base, tmem, flag);
   } else {
-    if constexpr (PASS2) epilogue_pass2<RT, D, NK, MAXW>(a, t, base, sbase, tmem, flag);
+    if constexpr (PASS2 && RT == 256) epilogue_pass2_pairs<RT, D, NK, MAXW>(a, t, base, sbase, tmem, flag);
+    else if constexpr (PASS2) epilogue_pass2<RT, D, NK, MAXW>(a, t, base, sbase, tmem, flag);
     else epilogue_pass1<RT, D, NK>(a, t, base, sbase, tmem, flag);
   }
   tc_fence_before();

@@ -38,7 +38,13 @@ CASES = {
     # group of 6 x 32 rows = 192 rows in a 256-row tile: 64 padding rows must carry no mass
     "g6_rt256_padded": S.Workload("edge_g6", 98, 1, 12, 2, 128, 32, (2222,), group_reduce="sum", pool_k=7,
                                   k_keep=100, n_clusters=4),
-    # group of 8 with W = 16 and max reduce (256 padded rows, head width below a warp)
+    # group of 4 with the full 64-row window and max reduce: 256 rows, one head per 64 columns
+    "g4w64_max_rt256": S.Workload("edge_g4w64", 105, 1, 8, 2, 128, 64, (1999,), group_reduce="max", pool_k=5,
+                                  k_keep=80, n_clusters=4),
+    # group of 32 heads with W = 8, max reduce, d = 64: 256 rows of 8-row heads
+    "g32w8_max_d64_rt256": S.Workload("edge_g32w8", 106, 1, 32, 1, 64, 8, (700,), group_reduce="max", pool_k=3,
+                                      k_keep=30),
+    # group of 16 with W = 16 and max reduce (256 rows, head width below a warp)
     "g16w16_max": S.Workload("edge_g16", 94, 1, 16, 1, 64, 16, (2500,), group_reduce="max", pool_k=3,
                              k_keep=64, page_size=16, n_recent=2, n_clusters=4),
 }

@@ -39,7 +39,7 @@ V = {
     "avg_cudacore_w24": S.Workload("v_avg_w24", 99, 1, 8, 2, 128, 24, (2000,), group_reduce="max", pool_k=7,
                                    pool_type="avg", k_keep=100, n_clusters=4),
     # logits summed over a group of 6 x 32 rows: 192 weighted rows and 64 padding rows in a 256-row tile
-    "logits_rt256_padded": S.Workload("v_logits_256", 102, 1, 12, 2, 128, 32, (1900,), group_reduce="sum",
+    "logits_rt256_padded": S.Workload("v_logits_256", 104, 1, 12, 2, 128, 32, (1900,), group_reduce="sum",
                                       pool_k=7, score_mode="logits", k_keep=64),
     # mean reduce over 256 padded rows (group of 8 x 32 rows), average pool
     "mean_rt256": S.Workload("v_mean_256", 100, 1, 16, 2, 128, 32, (2100,), group_reduce="mean", pool_k=7,
