@@ -57,12 +57,11 @@ struct Plan {
   // product of a block of ones (128 keys) with the rows' -lse / scale split into bf16 parts.
   static constexpr bool kFold = PASS2 && RT == 256;
   // Epilogue warps: 8, or 16 over 256 rows (four warps per TMEM lane quarter, so that every SM
-  // sub-partition has four warps' exponentials in flight).  Pass 1 gives each warp 64 of the 256
-  // accumulator columns of its lanes in every tile; pass 2 gives the two pairs of warpgroups
-  // alternate tiles (one TMEM stage each), so only one pair's warps release a stage.
+  // sub-partition has four warps' exponentials in flight).  Over 256 rows the two pairs of
+  // warpgroups take alternate tiles (one TMEM stage each), so only one pair's warps release a stage.
   static constexpr int kEW = RT == 256 ? 16 : 8;
   static constexpr int kThreads = 32 * (2 + kEW);
-  static constexpr int kStageReaders = (PASS2 && RT == 256) ? kEW / 2 : kEW;
+  static constexpr int kStageReaders = RT == 256 ? kEW / 2 : kEW;
   static constexpr uint32_t kOnesOff = kKOff + NK * kKBytes;                // 128 rows x 32 B of bf16 ones
   static constexpr uint32_t kCOff = kOnesOff + (kFold ? 128 * 32 : 0);     // RT rows x 32 B
   static constexpr uint32_t kSsOff = kCOff + (kFold ? RT * 32 : 0);        // pass-2 segment scores
@@ -530,11 +529,14 @@ __device__ __forceinline__ bool tile_ready(bool ready, uint32_t bar, uint32_t pa
 }
 
 // ---------------------------------------------------------------- pass 1 epilogue
-// RT = 128: both warpgroups see all 128 rows, warpgroup e takes tile columns [64e, 64e + 64).
-// RT = 256: warpgroup e takes rows 128 (e % 2) .. + 127 (accumulator block e % 2) and tile columns
-// [64 (e / 2), 64 (e / 2) + 64).  Either way each thread holds one row's (offset, sum) over its
-// 64-column half of every tile, and the halves are merged once per segment through shared memory
-// (one exchange per 128 rows).
+// RT = 128: both warpgroups see all 128 rows, warpgroup e takes tile columns [64e, 64e + 64) of
+// every tile (the next tile's accumulator probed before this tile's arithmetic).
+// RT = 256: the pairs of warpgroups (0, 1) and (2, 3) take alternate tiles, pair p those this CTA
+// takes at positions of parity p, always from TMEM stage p; warpgroup e takes rows
+// 128 (e % 2) .. + 127 (accumulator block e % 2), all 128 columns as two 64-column halves.  The
+// pairs run a tile apart, so one pair's waits and loads overlap the other's arithmetic.
+// Either way each row has two partial (offset, sum)s, merged once per segment through shared
+// memory (one exchange per 128 rows).
 template <int RT, int D, int NK>
 __device__ void epilogue_pass1(const TcArgs& a, const SeqTable& t, uint32_t base, uint8_t* sbase,
                                uint32_t tmem, volatile uint32_t* flag) {
@@ -545,15 +547,16 @@ __device__ void epilogue_pass1(const TcArgs& a, const SeqTable& t, uint32_t base
   const uint32_t bars = base + P::kBarOff;
   auto tfull = [&](int s) { return bars + 8u * (2 * NK + s); };
   auto tempty = [&](int s) { return bars + 8u * (2 * NK + P::kNT + s); };
-  const int rblk = RT == 256 ? (e.wg & 1) : 0;                 // accumulator block (128 rows)
-  const int chalf = RT == 256 ? (e.wg >> 1) : e.wg;            // 64-column half of the tile
+  constexpr bool kPairs = RT == 256;
+  const int rblk = kPairs ? (e.wg & 1) : 0;                    // accumulator block (128 rows)
+  const int chalf = e.wg >> (kPairs ? 1 : 0);                  // RT = 256: pair; else 64-column half
   const int row = e.lrow + 128 * rblk;
-  const uint32_t col0 = 128u * rblk + 64u * chalf;             // TMEM column within a stage
-  const int key0 = 64 * chalf;                                  // tile key of that column
+  const uint32_t col0 = kPairs ? 128u * rblk : 64u * chalf;    // TMEM column within a stage
+  const int key0 = kPairs ? 0 : 64 * chalf;                    // tile key of that column
   float* red = reinterpret_cast<float*>(sbase + P::kRedOff);
   const float scale = a.sh.scale_log2;
   const bool rvalid = row < a.sh.R;
-  int ts = 0;
+  int ts = 0, nt = 0;                                           // nt: tiles this CTA has taken so far
   uint32_t tph = 0;
   Work<false> work(t);
   for (Item it; work.next(t, a.sh, it);) {
@@ -563,6 +566,32 @@ __device__ void epilogue_pass1(const TcArgs& a, const SeqTable& t, uint32_t base
     float m = -INFINITY, l = 0.f;
     bool ready = false;      // this tile's accumulator was seen complete by the previous tile's probe
     for (int t0 = it.ta; t0 < it.tb; t0 += kTileKeys) {
+      if constexpr (kPairs) {
+        if ((nt++ & 1) != chalf) continue;
+        // the tensor-memory loads below are warp-collective: decide per warp
+        const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(tfull(chalf), tph));
+        tph ^= 1;
+        if (!ok) {
+          if (e.lane == 0) fail(a, flag, kWhereEpilogue);
+          continue;
+        }
+        tc_fence_after();
+        const uint32_t lane_base = tmem + ((uint32_t)(e.quarter * 32) << 16) + chalf * RT + col0;
+        {
+          float v[64];
+          tmem_ld64(lane_base, v);
+          if (rvalid) online_update64(v, vis_end - t0, scale, m, l);
+        }
+        {
+          float v[64];
+          tmem_ld64(lane_base + 64, v);
+          tc_fence_before();
+          __syncwarp();
+          if (e.lane == 0) mbar_arrive(tempty(chalf));
+          if (rvalid) online_update64(v, vis_end - (t0 + 64), scale, m, l);
+        }
+        continue;
+      }
       const bool ok = tile_ready(ready, tfull(ts), tph, flag);
       if (!ok && e.lane == 0) fail(a, flag, kWhereEpilogue);
       float v[64];
@@ -666,87 +695,51 @@ __device__ void pool_segment(const float* S, int ta, int tb, int a0, int a1, int
 }
 
 // ---------------------------------------------------------------- pass 2 epilogue
-// Thread = key (TMEM lane); warpgroup e takes rows [e RT/2, (e+1) RT/2) (TMEM columns).
+// 128 rows, 8 epilogue warps: thread = key (TMEM lane); warpgroup e takes rows [64 e, 64 e + 64)
+// (TMEM columns), whose -lse it holds in registers as column pairs.
 // MAXW = 0: group sum (every row summed); otherwise group max with head width MAXW.
 template <int RT, int D, int NK, int MAXW>
 __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base, uint8_t* sbase,
                                uint32_t tmem, volatile uint32_t* flag) {
   using P = Plan<true, RT, D, NK>;
-  constexpr int EW = P::kEW;
-  constexpr int kEpiThreads = 32 * EW;
-  constexpr int kHalf = RT / 2;
-  constexpr int kChunks = kHalf / 32;
+  static_assert(RT == 128 && P::kEW == 8, "two warpgroups of 64 rows");
+  constexpr int kEpiThreads = 32 * P::kEW;
   const EpiThread e = epi_thread();
   const uint32_t bars = base + P::kBarOff;
   auto tfull = [&](int s) { return bars + 8u * (2 * NK + s); };
   auto tempty = [&](int s) { return bars + 8u * (2 * NK + P::kNT + s); };
   float* Ss = reinterpret_cast<float*>(sbase + P::kSsOff);
   float* lse_s = reinterpret_cast<float*>(sbase + P::kLseOff);   // holds -lse per row
-  const float* nlse = lse_s;
   const float scale = a.sh.scale_log2;
-  const bool fold = P::kFold && !a.sh.logits;
-  const int col0 = e.wg * kHalf;
+  const int col0 = e.wg * 64;
   const int pr = (a.sh.pool_k - 1) / 2;
   const int P_ = a.sh.page_size;
   int ts = 0;
   uint32_t tph = 0;
   Work<true> work(t);
   for (Item it; work.next(t, a.sh, it);) {
-    epi_sync<EW>();                                          // readers of the previous item are done
+    epi_sync<P::kEW>();                                      // readers of the previous item are done
     for (int i = e.etid; i < it.tb - it.ta; i += kEpiThreads) Ss[i] = 0.f;
-    for (int i = e.etid; i < RT && !fold; i += kEpiThreads) {
+    for (int i = e.etid; i < RT; i += kEpiThreads) {
       if (a.sh.logits) lse_s[i] = i < a.sh.R ? a.sh.scale_nat : 0.f;    // row weights of the logit sum
       else lse_s[i] = i < a.sh.R ? -a.lse[(int64_t)it.unit * a.sh.R + i] : -INFINITY;   // padding rows: p = 0
     }
-    epi_sync<EW>();
-    // -lse of this warpgroup's 64 rows in registers (column pairs); with 128 rows per warpgroup
-    // they are read from shared memory instead (the registers would not fit)
-    float2 nl[kChunks == 2 ? 32 : 1];
-    if constexpr (kChunks == 2) {
+    epi_sync<P::kEW>();
+    float2 nl[32];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) nl[c] = make_float2(nlse[col0 + 2 * c], nlse[col0 + 2 * c + 1]);
-    }
-    // 256 rows (128 columns per thread): the next tile's accumulator is probed before this tile's
-    // arithmetic, as in pass 1
-    bool ready = false;
+    for (int c = 0; c < 32; ++c) nl[c] = make_float2(lse_s[col0 + 2 * c], lse_s[col0 + 2 * c + 1]);
     for (int t0 = it.ta; t0 < it.tb; t0 += kTileKeys) {
       // the tensor-memory loads below are warp-collective: decide per warp
-      bool ok;
-      if constexpr (kChunks == 4) ok = tile_ready(ready, tfull(ts), tph, flag);
-      else ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(tfull(ts), tph));
-      ready = false;
+      const bool ok = __all_sync(0xffffffffu, !aborted(flag) && mbar_wait(tfull(ts), tph));
       if (!ok && e.lane == 0) fail(a, flag, kWhereEpilogue);
       if (ok) {
         tc_fence_after();
-        const uint32_t taddr = tmem + ((uint32_t)(e.quarter * 32) << 16) + ts * RT + col0;
-        float red;
-        if (kChunks == 2) {
-          float v64[64];
-          tmem_ld64(taddr, v64);
-          tc_fence_before();
-          __syncwarp();
-          if (e.lane == 0) mbar_arrive(tempty(ts));
-          red = a.sh.logits ? linmass64<MAXW>(v64, nl) : colmass64<MAXW>(v64, nl, scale);
-        } else {
-          float v64[64], w64[64];
-          tmem_ld64(taddr, v64);
-          tmem_ld64(taddr + 64, w64);
-          tc_fence_before();
-          __syncwarp();
-          if (e.lane == 0) mbar_arrive(tempty(ts));
-          const int tn = ts + 1 == (int)P::kNT ? 0 : ts + 1;
-          ready = t0 + kTileKeys < it.tb && mbar_test_wait(tfull(tn), tn == 0 ? tph ^ 1 : tph);
-          float r0, r1;
-          if (fold) {   // the accumulator holds z - lse / scale (no per-row operand)
-            r0 = colmass64<MAXW, true>(v64, nullptr, scale);
-            r1 = colmass64<MAXW, true>(w64, nullptr, scale);
-          } else {
-            const float2* nls = reinterpret_cast<const float2*>(nlse + col0);
-            r0 = a.sh.logits ? linmass64<MAXW>(v64, nls) : colmass64<MAXW>(v64, nls, scale);
-            r1 = a.sh.logits ? linmass64<MAXW>(w64, nls + 32) : colmass64<MAXW>(w64, nls + 32, scale);
-          }
-          red = MAXW == 0 ? r0 + r1 : fmaxf(r0, r1);
-        }
+        float v64[64];
+        tmem_ld64(tmem + ((uint32_t)(e.quarter * 32) << 16) + ts * RT + col0, v64);
+        tc_fence_before();
+        __syncwarp();
+        if (e.lane == 0) mbar_arrive(tempty(ts));
+        const float red = a.sh.logits ? linmass64<MAXW>(v64, nl) : colmass64<MAXW>(v64, nl, scale);
         const int key = t0 + e.lrow;
         if (key < it.tb) {
           // two addends per key (one per warpgroup): the result does not depend on their order
@@ -757,7 +750,7 @@ __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base
       }
       if (++ts == (int)P::kNT) { ts = 0; tph ^= 1; }
     }
-    epi_sync<EW>();
+    epi_sync<P::kEW>();
     if (aborted(flag)) continue;
     // max-pool over prefix positions, then page reduce (DELTA key designs 2-3)
     const SeqInfo& si = t.s[it.b];
