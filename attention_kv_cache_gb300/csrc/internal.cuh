@@ -5,9 +5,20 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "kvsel.h"
 
 namespace kvsel {
+
+// A named range on a profiler's host timeline spanning one entry-point call (NVTX, header-only);
+// a no-op unless a tool that records NVTX ranges is attached.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Error word at the start of every workspace (device side).
 struct DeviceError {

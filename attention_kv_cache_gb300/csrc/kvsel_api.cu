@@ -252,6 +252,7 @@ kvsel_status kvsel_workspace_size(const kvsel_desc* desc, size_t* bytes) {
 
 kvsel_status kvsel_score(const kvsel_desc* desc, const void* q, const void* k, float* scores,
                          float* page_scores, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  NvtxRange nvtx("kvsel_score");
   kvsel_status st = check_desc(desc);
   if (st != KVSEL_OK) return st;
   const kvsel_desc& d = *desc;
@@ -271,6 +272,7 @@ kvsel_status kvsel_score(const kvsel_desc* desc, const void* q, const void* k, f
 
 kvsel_status kvsel_score_from_lse(const kvsel_desc* desc, const void* q_win, const void* k, const float* lse_win,
                                   float* scores, float* page_scores, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  NvtxRange nvtx("kvsel_score_from_lse");
   kvsel_status st = check_desc(desc);
   if (st != KVSEL_OK) return st;
   const kvsel_desc& d = *desc;
@@ -290,6 +292,7 @@ kvsel_status kvsel_score_from_lse(const kvsel_desc* desc, const void* q_win, con
 
 kvsel_status kvsel_prefill_attention(const kvsel_desc* desc, const void* q, const void* k, const void* v, void* o,
                                      float* lse, float* lse_win, void* q_win, void* ws, cudaStream_t stream) {
+  NvtxRange nvtx("kvsel_prefill_attention");
   kvsel_status st = check_desc(desc);
   if (st != KVSEL_OK) return st;
   const kvsel_desc& d = *desc;
@@ -305,6 +308,7 @@ kvsel_status kvsel_prefill_attention(const kvsel_desc* desc, const void* q, cons
 kvsel_status kvsel_combine_layers(const kvsel_desc* desc, const float* scores, int32_t layer_lo,
                                   int32_t layer_hi, float* combined, void* ws, size_t ws_bytes,
                                   cudaStream_t stream) {
+  NvtxRange nvtx("kvsel_combine_layers");
   kvsel_status st = check_desc(desc);
   if (st != KVSEL_OK) return st;
   const kvsel_desc& d = *desc;
@@ -320,6 +324,7 @@ kvsel_status kvsel_combine_layers(const kvsel_desc* desc, const float* scores, i
 kvsel_status kvsel_aggregate(const kvsel_desc* desc, const float* scores, int32_t layer_lo, int32_t layer_hi,
                              int32_t layer_op, int32_t head_op, float* out, void* ws, size_t ws_bytes,
                              cudaStream_t stream) {
+  NvtxRange nvtx("kvsel_aggregate");
   kvsel_status st = check_desc(desc);
   if (st != KVSEL_OK) return st;
   const kvsel_desc& d = *desc;
@@ -338,6 +343,7 @@ kvsel_status kvsel_aggregate(const kvsel_desc* desc, const float* scores, int32_
 kvsel_status kvsel_select(const kvsel_desc* desc, const float* scores, int32_t rows, int32_t k, int32_t n_recent,
                           int32_t append_window, int32_t* idx_out, void* ws, size_t ws_bytes,
                           cudaStream_t stream) {
+  NvtxRange nvtx("kvsel_select");
   kvsel_status st = check_desc(desc);
   if (st != KVSEL_OK) return st;
   const kvsel_desc& d = *desc;
@@ -352,6 +358,7 @@ kvsel_status kvsel_select(const kvsel_desc* desc, const float* scores, int32_t r
 kvsel_status kvsel_topk(const kvsel_desc* desc, const float* scores, int32_t layers, int32_t k,
                         int32_t n_recent, int32_t* idx_out, void* ws, size_t ws_bytes,
                         cudaStream_t stream) {
+  NvtxRange nvtx("kvsel_topk");
   kvsel_status st = check_desc(desc);
   if (st != KVSEL_OK) return st;
   const kvsel_desc& d = *desc;
@@ -367,6 +374,7 @@ kvsel_status kvsel_topk(const kvsel_desc* desc, const float* scores, int32_t lay
 kvsel_status kvsel_compact(const kvsel_desc* desc, const void* k, const void* v, const int32_t* idx,
                            int32_t idx_layers, int32_t n_sel, void* k_out, void* v_out, void* ws,
                            cudaStream_t stream) {
+  NvtxRange nvtx("kvsel_compact");
   kvsel_status st = check_desc(desc);
   if (st != KVSEL_OK) return st;
   const kvsel_desc& d = *desc;
@@ -386,6 +394,7 @@ kvsel_status kvsel_compact(const kvsel_desc* desc, const void* k, const void* v,
 kvsel_status kvsel_compact_layers(const kvsel_desc* desc, const void* k, const void* v, const int32_t* idx,
                                   int32_t idx_layers, int32_t idx_heads, int32_t layer_lo, int32_t n_layers_out,
                                   int32_t n_sel, void* k_out, void* v_out, void* ws, cudaStream_t stream) {
+  NvtxRange nvtx("kvsel_compact_layers");
   kvsel_status st = check_desc(desc);
   if (st != KVSEL_OK) return st;
   const kvsel_desc& d = *desc;
@@ -429,6 +438,7 @@ kvsel_status kvsel_attend_workspace_size(const kvsel_desc* desc, int32_t n_q, in
 kvsel_status kvsel_attend(const kvsel_desc* desc, const void* q, int32_t n_q, const void* k, const void* v,
                           const int32_t* kv_indptr, const int32_t* kv_indices, int32_t n_per_row, int32_t block,
                           int32_t max_blocks, float* o, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  NvtxRange nvtx("kvsel_attend");
   kvsel_status st = check_desc(desc);
   if (st != KVSEL_OK) return st;
   const kvsel_desc& d = *desc;
@@ -453,6 +463,7 @@ kvsel_status kvsel_attend(const kvsel_desc* desc, const void* q, int32_t n_q, co
 kvsel_status kvsel_pagetable(const kvsel_desc* desc, const uint8_t* mask, int32_t n_qblk,
                              int32_t n_kvblk_max, const int32_t* n_kvblk, int32_t* kv_indptr,
                              int32_t* kv_indices, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  NvtxRange nvtx("kvsel_pagetable");
   kvsel_status st = check_desc(desc);
   if (st != KVSEL_OK) return st;
   const kvsel_desc& d = *desc;
