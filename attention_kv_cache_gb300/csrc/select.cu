@@ -64,6 +64,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
   __shared__ uint32_t hist[256];
   __shared__ uint32_t hist_w[kTopkThreads / 32][256];   // one histogram per warp: no cross-warp atomics
   __shared__ unsigned long long scan_sh[32];
+  __shared__ uint2 warp_cnt[kTopkThreads / 32];
   __shared__ uint32_t sel_digit, sel_gt;
 
   const int row = blockIdx.x;
@@ -76,8 +77,23 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
   int32_t* out = a.idx + (int64_t)row * a.n_sel;
   const int tid = threadIdx.x;
 
-  if (SMEM)
-    for (int i = tid; i < n_cand; i += kTopkThreads) keys_sm[i] = f2key(src[i]);
+  if (SMEM) {
+    // stage the row's keys: 16-byte loads when the row is 16-byte aligned, several in flight per thread
+    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+      const int n4 = n_cand >> 2;
+      const float4* s4 = reinterpret_cast<const float4*>(src);
+      uint4* k4 = reinterpret_cast<uint4*>(keys_sm);
+#pragma unroll 4
+      for (int i = tid; i < n4; i += kTopkThreads) {
+        const float4 f = s4[i];
+        k4[i] = make_uint4(f2key(f.x), f2key(f.y), f2key(f.z), f2key(f.w));
+      }
+      for (int i = 4 * n4 + tid; i < n_cand; i += kTopkThreads) keys_sm[i] = f2key(src[i]);
+    } else {
+#pragma unroll 8
+      for (int i = tid; i < n_cand; i += kTopkThreads) keys_sm[i] = f2key(src[i]);
+    }
+  }
   __syncthreads();
   auto key_at = [&](int i) -> uint32_t { return SMEM ? keys_sm[i] : f2key(src[i]); };
 
@@ -89,6 +105,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
       uint32_t* hw = hist_w[tid >> 5];
       for (int j = tid & 31; j < 256; j += 32) hw[j] = 0;
       __syncwarp();
+#pragma unroll 4
       for (int base = 0; base < n_cand; base += kTopkThreads) {
         const int i = base + tid;
         uint32_t key = 0;
@@ -127,25 +144,47 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
       krem -= sel_gt;
       __syncthreads();
     }
-    // ordered emission: every key > T and the first krem keys == T, in index order.  Rounds of one key
-    // per thread (consecutive threads, consecutive keys); a block scan gives each selected key the
-    // number of selected keys before it: (keys > T before it) + min(keys == T before it, krem).
+    // ordered emission: every key > T and the first krem keys == T, in index order.  A selected key's
+    // output position is the number of selected keys before it: (keys > T before it) + min(keys == T
+    // before it, krem).  Each warp owns one contiguous segment of the row: it counts its segment's
+    // keys > T and == T, one barrier makes every warp's counts visible, and the warp then walks its
+    // segment in rounds of 32 consecutive keys, placing each key from its warp's offsets and the
+    // ballots of the lanes before it.
     const uint32_t T = prefix;
-    uint32_t gt_run = 0, eq_run = 0;
-    for (int base = 0; base < n_cand; base += kTopkThreads) {
-      const int i = base + tid;
-      const uint32_t key = i < n_cand ? key_at(i) : 0u;
-      const bool is_gt = i < n_cand && key > T;
-      const bool is_eq = i < n_cand && key == T;
-      unsigned long long tot;
-      const unsigned long long pre =
-          block_scan_u64(((unsigned long long)is_gt << 32) | (unsigned long long)is_eq, scan_sh, &tot);
-      const uint32_t gt_before = gt_run + (uint32_t)(pre >> 32);
-      const uint32_t eq_before = eq_run + (uint32_t)(pre & 0xffffffffu);
-      if (is_gt) out[gt_before + min(eq_before, krem)] = i;
-      else if (is_eq && eq_before < krem) out[gt_before + eq_before] = i;
-      gt_run += (uint32_t)(tot >> 32);
-      eq_run += (uint32_t)(tot & 0xffffffffu);
+    const int warp = tid >> 5, lane = tid & 31;
+    constexpr int kWarps = kTopkThreads / 32;
+    const int seg = (n_cand + kWarps - 1) / kWarps;
+    const int s0 = min(n_cand, warp * seg), s1 = min(n_cand, s0 + seg);
+    uint32_t g = 0, e = 0;
+    for (int i = s0 + lane; i < s1; i += 32) {
+      const uint32_t key = key_at(i);
+      g += key > T ? 1u : 0u;
+      e += key == T ? 1u : 0u;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      g += __shfl_xor_sync(0xffffffffu, g, o);
+      e += __shfl_xor_sync(0xffffffffu, e, o);
+    }
+    if (lane == 0) warp_cnt[warp] = make_uint2(g, e);
+    __syncthreads();
+    uint32_t gt_before = 0, eq_before = 0;
+    for (int w = 0; w < warp; ++w) {
+      gt_before += warp_cnt[w].x;
+      eq_before += warp_cnt[w].y;
+    }
+    const unsigned lower = (1u << lane) - 1u;
+    for (int base = s0; base < s1; base += 32) {
+      const int i = base + lane;
+      const uint32_t key = i < s1 ? key_at(i) : 0u;
+      const bool is_gt = i < s1 && key > T;
+      const bool is_eq = i < s1 && key == T;
+      const unsigned mg = __ballot_sync(0xffffffffu, is_gt), me = __ballot_sync(0xffffffffu, is_eq);
+      const uint32_t gb = gt_before + __popc(mg & lower), eb = eq_before + __popc(me & lower);
+      if (is_gt) out[gb + min(eb, krem)] = i;
+      else if (is_eq && eb < krem) out[gb + eb] = i;
+      gt_before += __popc(mg);
+      eq_before += __popc(me);
     }
   }
   // recency pages, then (when appended) window pages or window tokens: the indices from n_cand on
