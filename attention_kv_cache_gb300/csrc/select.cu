@@ -251,14 +251,28 @@ __global__ void __launch_bounds__(kCombThreads) agg_pool(const __grid_constant__
     float v;
     if (a.layer_op == KVSEL_LAYERS_EACH) {
       v = head_value(a, si, a.lo + ol, oh, tt);
-    } else if (a.layer_op == KVSEL_LAYERS_MAX) {
-      v = head_value(a, si, a.lo, oh, tt);
-      for (int layer = a.lo + 1; layer <= a.hi; ++layer) v = fmaxf(v, head_value(a, si, layer, oh, tt));
     } else {
-      float acc = 0.f;
-      for (int layer = a.lo; layer <= a.hi; ++layer)
-        acc += head_value(a, si, layer, oh, tt) / a.norms[((int64_t)b * nr + (layer - a.lo)) * a.n_h + oh];
-      v = acc * inv_n;
+      // layers in batches of 8 whose loads are all issued before they are combined, in layer order
+      // (the same arithmetic, in the same order, as one layer at a time)
+      const bool mx = a.layer_op == KVSEL_LAYERS_MAX;
+      float acc = mx ? -INFINITY : 0.f;
+      for (int l0 = a.lo; l0 <= a.hi; l0 += 8) {
+        float x[8], nv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int layer = l0 + u;
+          x[u] = 0.f;
+          nv[u] = 1.f;
+          if (layer <= a.hi) {
+            x[u] = head_value(a, si, layer, oh, tt);
+            if (!mx) nv[u] = a.norms[((int64_t)b * nr + (layer - a.lo)) * a.n_h + oh];
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (l0 + u <= a.hi) acc = mx ? fmaxf(acc, x[u]) : acc + x[u] / nv[u];
+      }
+      v = mx ? acc : acc * inv_n;
     }
     S[tt - ea] = v;
   }
