@@ -87,15 +87,17 @@ struct PtArgs {
   int32_t n_layers, h_q, h_kv, n_qblk, nmax, rows;
 };
 
-// OR over the Q blocks and the query heads of group g for KV block j.
+// OR over the Q blocks and the query heads of group g for KV block j.  Every entry is read (no
+// early exit), so the loads are independent and many are in flight at once instead of forming a
+// chain of dependent loads for a block that no head selects.
 __device__ __forceinline__ bool union_hit(const PtArgs& a, int b, int layer, int g, int j) {
   const int G = a.h_q / a.h_kv;
-  for (int h = g * G; h < (g + 1) * G; ++h) {
-    const uint8_t* m = a.mask + ((((int64_t)b * a.n_layers + layer) * a.h_q + h) * a.n_qblk) * a.nmax + j;
-    for (int i = 0; i < a.n_qblk; ++i)
-      if (m[(int64_t)i * a.nmax]) return true;
-  }
-  return false;
+  const int n = G * a.n_qblk;                       // (head, Q block) rows of the group, consecutive
+  const uint8_t* m = a.mask + ((((int64_t)b * a.n_layers + layer) * a.h_q + (int64_t)g * G) * a.n_qblk) * a.nmax + j;
+  uint32_t acc = 0;
+#pragma unroll 8
+  for (int r = 0; r < n; ++r) acc |= m[(int64_t)r * a.nmax];
+  return acc != 0;
 }
 
 __global__ void __launch_bounds__(kPtThreads) pt_count(const __grid_constant__ PtArgs a,
