@@ -450,10 +450,18 @@ def run_kvsel(args):
         dist.destroy_process_group()
 
 
+def _ctx(w):
+    """Prefix length(s) of a workload for its metric name: '64K', '512', or a range for a ragged batch."""
+    def f(L):
+        return f"{L // 1024}K" if L >= 1024 else str(L)
+    lo, hi = min(w.prefix_lens), max(w.prefix_lens)
+    return f(lo) if lo == hi else f"{f(lo)}-{f(hi)}"
+
+
 def metric_for(w):
     if w.name == DEFAULT_WORKLOAD:
         return METRIC
-    return f"prefix tokens scored+selected/s (per layer, {w.prefix_lens[0] // 1024}K ctx, {w.name})"
+    return f"prefix tokens scored+selected/s (per layer, {_ctx(w)} ctx, {w.name})"
 
 
 # ----------------------------------------------------------------------------- attention over the selection
