@@ -470,6 +470,168 @@ def check_prefill_attention_sdpa(o):
             np.testing.assert_allclose(p[hl, j, :L + j + 1], np.exp(zz[:L + j + 1] - lse[hl, L + j]), rtol=1e-12)
 
 
+# --------------------------------------------------------------------------- composition of the steps
+
+def _ref_group_scores(q_l, k_l, L, W, G, mode, softmax):
+    """Raw group scores [H_kv, L] of one layer, built outside the oracle: probabilities from torch SDPA
+    (identity values) or logits by an explicit dot-product loop, then each head's column sum over the
+    window rows, then the reduction over the heads of each group."""
+    Hq, d = q_l.shape[0], q_l.shape[-1]
+    if softmax:
+        c = _sdpa_probs(q_l, k_l, L, W)[:, :, :L].sum(axis=1)            # [Hq, L]
+    else:
+        c = np.zeros((Hq, L))
+        for h in range(Hq):
+            for t in range(L):
+                c[h, t] = sum(float(np.dot(q_l[h, j], k_l[h // G, t])) for j in range(W)) / math.sqrt(d)
+    out = []
+    for g in range(k_l.shape[0]):
+        heads = c[g * G:(g + 1) * G]
+        out.append({"sum": heads.sum(axis=0), "max": heads.max(axis=0),
+                    "mean": heads.sum(axis=0) / (G * W)}[mode])
+    return np.stack(out)
+
+
+def _ref_pool(s, k, kind):
+    return _pool_loop(s, k) if kind == "max" else _avg_loop(s, k)
+
+
+def _ref_top(u, k):
+    """k best positions by (score desc, index asc), returned ascending."""
+    return sorted(sorted(range(len(u)), key=lambda t: (-u[t], t))[:k])
+
+
+def _ref_pages(u, P):
+    n = len(u)
+    return np.array([max(u[p * P:min(n, (p + 1) * P)]) for p in range(-(-n // P))])
+
+
+def _ref_rows(x, idx, P):
+    """Rows x[i] (token mode) or the P rows of page i, zero past the end, in list order."""
+    out = []
+    for i in idx:
+        for r in range(i * P, i * P + P):
+            out.append(x[r] if r < x.shape[0] else np.zeros(x.shape[1]))
+    return np.array(out)
+
+
+def _workload(**kw):
+    import types
+    base = dict(group_reduce="sum", pool_k=3, page_size=1, page_reduce="max", k_keep=4, n_recent=0,
+                layer_range=None, pool_type="max", score_mode="softmax", head_reduce="group",
+                append_window=True)
+    base.update(kw)
+    return types.SimpleNamespace(**base)
+
+
+def check_run_sequence_composition(o):
+    """run_sequence chains the steps in the order the pages give, on tiny inputs, against outputs rebuilt
+    here from SDPA probabilities and loop definitions:
+
+    * token mode: group reduce -> pool -> top k per (layer, KV head) -> window appended -> gather;
+    * page mode: group max -> pool -> page max (DELTA key designs 2-3: token scores first, then the page
+      score) -> last n_recent prefix pages kept, top k of the others, window pages appended;
+    * cross-layer: group sum -> L1 over the prefix per (layer, KV head) -> mean over the inclusive layer
+      range -> pool -> one top k per KV head gathered from every layer (LookaheadKV's L1 normalisation;
+      CLAA decision 3);
+    * all-head: the sum over KV heads of the raw group scores, then the pool, one index per layer
+      (CLAA decision 2), here without the window (LookaheadKV's lookahead rows are not kept);
+    * pre-softmax logits summed over all heads with average pooling (GemFilter).
+    """
+    rng = _rng(20)
+
+    def inputs(n_layers, Hq, Hkv, W, L, d, scale=1.6):
+        q = _bf16_values(rng.standard_normal((n_layers, Hq, W, d)) * scale)
+        k = _bf16_values(rng.standard_normal((n_layers, Hkv, L + W, d)))
+        v = _bf16_values(rng.standard_normal((n_layers, Hkv, L + W, d)))
+        return q, k, v
+
+    def raw_of(w, q, k, L):
+        G = w.h_q // w.h_kv
+        return np.stack([_ref_group_scores(q[l], k[l], L, w.window, G, w.group_reduce,
+                                           w.score_mode == "softmax") for l in range(w.n_layers)])
+
+    # token mode
+    w = _workload(n_layers=2, h_q=4, h_kv=2, window=3, k_keep=5)
+    L = 19
+    q, k, v = inputs(2, 4, 2, 3, L, 8)
+    res = o.run_sequence(w, q, k, v)
+    raw = raw_of(w, q, k, L)
+    np.testing.assert_allclose(res["raw"], raw, rtol=1e-11, atol=1e-14)
+    for l in range(2):
+        for g in range(2):
+            u = _ref_pool(raw[l, g], 3, "max")
+            np.testing.assert_allclose(res["pooled"][l, g], u, rtol=1e-11, atol=1e-14)
+            want = _ref_top(u, 5) + list(range(L, L + 3))
+            assert list(res["idx"][l, g]) == want, (l, g, list(res["idx"][l, g]), want)
+            np.testing.assert_array_equal(res["k_c"][l, g], _ref_rows(k[l, g], want, 1))
+            np.testing.assert_array_equal(res["v_c"][l, g], _ref_rows(v[l, g], want, 1))
+
+    # page mode, partial last page shared by prefix and window
+    P = 4
+    w = _workload(n_layers=2, h_q=4, h_kv=2, window=4, group_reduce="max", page_size=P, k_keep=2, n_recent=1)
+    L = 22
+    q, k, v = inputs(2, 4, 2, 4, L, 8)
+    res = o.run_sequence(w, q, k, v)
+    raw = raw_of(w, q, k, L)
+    np.testing.assert_allclose(res["raw"], raw, rtol=1e-11, atol=1e-14)
+    n_pages = -(-L // P)
+    for l in range(2):
+        for g in range(2):
+            u = _ref_pool(raw[l, g], 3, "max")
+            U = _ref_pages(u, P)
+            np.testing.assert_allclose(res["pages"][l, g], U, rtol=1e-11, atol=1e-14)
+            cand = n_pages - 1
+            want = sorted(_ref_top(U[:cand], 2) + [cand]) + list(range(n_pages, -(-(L + 4) // P)))
+            assert list(res["idx"][l, g]) == want, (l, g, list(res["idx"][l, g]), want)
+            np.testing.assert_array_equal(res["k_c"][l, g], _ref_rows(k[l, g], want, P))
+
+    # cross-layer L1 mean over an inclusive layer range
+    w = _workload(n_layers=5, h_q=4, h_kv=2, window=2, k_keep=4, layer_range=(1, 3))
+    L = 17
+    q, k, v = inputs(5, 4, 2, 2, L, 8)
+    res = o.run_sequence(w, q, k, v)
+    raw = raw_of(w, q, k, L)
+    np.testing.assert_allclose(res["raw"], raw, rtol=1e-11, atol=1e-14)
+    for g in range(2):
+        S = sum(raw[l, g] / sum(abs(x) for x in raw[l, g]) for l in (1, 2, 3)) / 3.0
+        np.testing.assert_allclose(res["combined"][g], S, rtol=1e-11, atol=1e-14)
+        u = _ref_pool(S, 3, "max")
+        np.testing.assert_allclose(res["pooled"][g], u, rtol=1e-11, atol=1e-14)
+        want = _ref_top(u, 4) + [L, L + 1]
+        assert list(res["idx"][g]) == want, (g, list(res["idx"][g]), want)
+        for l in range(5):
+            np.testing.assert_array_equal(res["k_c"][l, g], _ref_rows(k[l, g], want, 1))
+
+    # all-head sum, mean reduce, max pool, window not kept
+    w = _workload(n_layers=2, h_q=4, h_kv=2, window=3, group_reduce="mean", head_reduce="all",
+                  append_window=False, k_keep=4)
+    L = 15
+    q, k, v = inputs(2, 4, 2, 3, L, 8)
+    res = o.run_sequence(w, q, k, v)
+    raw = raw_of(w, q, k, L)
+    np.testing.assert_allclose(res["raw"], raw, rtol=1e-11, atol=1e-14)
+    for l in range(2):
+        u = _ref_pool(raw[l, 0] + raw[l, 1], 3, "max")
+        np.testing.assert_allclose(res["pooled"][l], u, rtol=1e-11, atol=1e-14)
+        want = _ref_top(u, 4)
+        assert list(res["idx"][l]) == want, (l, list(res["idx"][l]), want)
+        for g in range(2):
+            np.testing.assert_array_equal(res["k_c"][l, g], _ref_rows(k[l, g], want, 1))
+
+    # pre-softmax logits over all heads, average pooling, W = 1
+    w = _workload(n_layers=1, h_q=4, h_kv=2, window=1, score_mode="logits", head_reduce="all",
+                  pool_type="avg", k_keep=3)
+    L = 13
+    q, k, v = inputs(1, 4, 2, 1, L, 8)
+    res = o.run_sequence(w, q, k, v, with_gather=False)
+    raw = raw_of(w, q, k, L)
+    np.testing.assert_allclose(res["raw"], raw, rtol=1e-11, atol=1e-13)
+    u = _ref_pool(raw[0, 0] + raw[0, 1], 3, "avg")
+    np.testing.assert_allclose(res["pooled"][0], u, rtol=1e-11, atol=1e-13)
+    assert list(res["idx"][0]) == _ref_top(u, 3) + [L]
+
+
 ALL_CHECKS = [
     check_probs_match_sdpa,
     check_row_mass_invariant,
@@ -491,4 +653,5 @@ ALL_CHECKS = [
     check_claa_max_buffer,
     check_table_attention_sdpa,
     check_prefill_attention_sdpa,
+    check_run_sequence_composition,
 ]

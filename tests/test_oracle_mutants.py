@@ -5,6 +5,7 @@ index, or a swapped operand anywhere in the oracle would be caught.
 """
 
 import importlib.util
+import inspect
 import os
 
 import numpy as np
@@ -226,6 +227,60 @@ def _prefill_not_causal(o):
     o.prefill_attention = prefill_attention
 
 
+def _rewrite_run_sequence(*edits):
+    """A mutant that re-defines run_sequence from its own source with text edits (each must match once)."""
+    def mutate(o):
+        src = inspect.getsource(o.run_sequence)
+        for old, new in edits:
+            assert src.count(old) == 1, f"mutant pattern not found once: {old!r}"
+            src = src.replace(old, new)
+        exec(compile(src, o.__file__, "exec"), o.__dict__)
+    return mutate
+
+
+def _page_max_of_raw_scores(o):
+    """Page scores taken from the unpooled token scores."""
+    _rewrite_run_sequence(("U = page_reduce(u,", "U = page_reduce(raw,"))(o)
+
+
+def _pool_after_page_max(o):
+    """Page max first, then the pool over pages."""
+    _rewrite_run_sequence(("U = page_reduce(u, w.page_size, w.page_reduce)",
+                           "U = pool(page_reduce(raw, w.page_size, w.page_reduce), w.pool_k, kind)"))(o)
+
+
+def _pool_before_l1_mean(o):
+    """Cross-layer: each layer pooled before the L1 normalisation and the layer mean."""
+    _rewrite_run_sequence(("s = cross_layer_mean(raw, lo, hi)", "s = cross_layer_mean(pool(raw, w.pool_k, kind), lo, hi)"),
+                          ("u = pool(s, w.pool_k, kind)", "u = s"))(o)
+
+
+def _run_layer_range_exclusive(o):
+    """The last layer of the range left out inside the composition."""
+    _rewrite_run_sequence(("cross_layer_mean(raw, lo, hi)", "cross_layer_mean(raw, lo, hi - 1)"))(o)
+
+
+def _mean_over_every_layer(o):
+    _rewrite_run_sequence(("cross_layer_mean(raw, lo, hi)", "cross_layer_mean(raw, 0, raw.shape[0] - 1)"))(o)
+
+
+def _window_always_appended(o):
+    _rewrite_run_sequence(('Wapp = W if getattr(w, "append_window", True) else 0', "Wapp = W"))(o)
+
+
+def _head_sum_after_pool(o):
+    _rewrite_run_sequence(("u = pool(head_sum(raw), w.pool_k, kind)", "u = head_sum(pool(raw, w.pool_k, kind))"))(o)
+
+
+def _gather_first_layer_index(o):
+    """Every layer's cache gathered with layer 0's selection."""
+    _rewrite_run_sequence(('ii = out["idx"][i, g]', 'ii = out["idx"][0, g]'))(o)
+
+
+def _pool_kind_ignored(o):
+    _rewrite_run_sequence(('kind = getattr(w, "pool_type", "max")', 'kind = "max"'))(o)
+
+
 MUTANTS = [_no_scale, _mask_off_by_one, _prefix_only_softmax, _mass_max_over_rows,
            _mass_includes_window_shift, _wrong_group_map, _reduce_swapped, _transposed_rows,
            _pool_radius, _pool_one_sided, _page_sum_for_max, _tie_to_higher, _rank_ascending,
@@ -233,7 +288,9 @@ MUTANTS = [_no_scale, _mask_off_by_one, _prefix_only_softmax, _mass_max_over_row
            _union_first_qblock_only, _gather_page_offset, _logits_unscaled, _logits_include_window_key,
            _mean_over_heads_only, _head_sum_is_max, _avg_pool_counts_padding, _layer_max_is_mean,
            _keep_count_floor, _claa_buffer_short, _attend_no_scale, _table_rows_off_by_one,
-           _prefill_not_causal]
+           _prefill_not_causal, _page_max_of_raw_scores, _pool_after_page_max, _pool_before_l1_mean,
+           _run_layer_range_exclusive, _mean_over_every_layer, _window_always_appended, _head_sum_after_pool,
+           _gather_first_layer_index, _pool_kind_ignored]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda m: m.__name__.strip("_"))
