@@ -78,6 +78,10 @@ struct ScoreShape {
 // Score shape of a checked descriptor (kvsel_api.cu).
 ScoreShape make_shape(const kvsel_desc& d);
 
+// The checks kvsel_score makes of its descriptor and pointers, workspace aside (kvsel_api.cu).
+kvsel_status check_score_args(const kvsel_desc* desc, const void* q, const void* k, const float* scores,
+                              const float* page_scores);
+
 // ---- launch plumbing (kvsel_api.cu) ------------------------------------------------
 struct TraceScope {
   TraceScope(const char* name, cudaStream_t s);

@@ -143,6 +143,16 @@ static kvsel_status check_desc(const kvsel_desc* d) {
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+kvsel_status check_score_args(const kvsel_desc* desc, const void* q, const void* k, const float* scores,
+                              const float* page_scores) {
+  kvsel_status st = check_desc(desc);
+  if (st != KVSEL_OK) return st;
+  if (q == nullptr || k == nullptr || scores == nullptr) return KVSEL_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(scores)) return KVSEL_ERR_INVALID_ARG;
+  if (desc->page_size > 1 && page_scores == nullptr) return KVSEL_ERR_INVALID_ARG;
+  return KVSEL_OK;
+}
+
 static kvsel_status check_ws(const kvsel_desc& d, void* ws, size_t ws_bytes) {
   if (ws == nullptr || ((uintptr_t)ws % KVSEL_WS_ALIGN) != 0) return KVSEL_ERR_WORKSPACE;
   if (ws_bytes < ws_layout(d).total) return KVSEL_ERR_WORKSPACE;
@@ -253,12 +263,9 @@ kvsel_status kvsel_workspace_size(const kvsel_desc* desc, size_t* bytes) {
 kvsel_status kvsel_score(const kvsel_desc* desc, const void* q, const void* k, float* scores,
                          float* page_scores, void* ws, size_t ws_bytes, cudaStream_t stream) {
   NvtxRange nvtx("kvsel_score");
-  kvsel_status st = check_desc(desc);
+  kvsel_status st = check_score_args(desc, q, k, scores, page_scores);
   if (st != KVSEL_OK) return st;
   const kvsel_desc& d = *desc;
-  if (q == nullptr || k == nullptr || scores == nullptr) return KVSEL_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(scores)) return KVSEL_ERR_INVALID_ARG;
-  if (d.page_size > 1 && page_scores == nullptr) return KVSEL_ERR_INVALID_ARG;
   if ((st = check_ws(d, ws, ws_bytes)) != KVSEL_OK) return st;
   const WsLayout w = ws_layout(d);
   auto ws_base = [](void* p) { return static_cast<char*>(p); };

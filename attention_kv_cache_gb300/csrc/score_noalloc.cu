@@ -48,12 +48,13 @@ kvsel_status scratch_on_current_device(void** out) {
 extern "C" KVSEL_API kvsel_status kvsel_score_noalloc(const kvsel_desc* desc, const void* q, const void* k,
                                                       float* scores, float* page_scores,
                                                       cudaStream_t stream) {
-  size_t need = 0;
-  kvsel_status st = kvsel_workspace_size(desc, &need);   // checks the descriptor
+  // Every argument check kvsel_score makes comes first, so a rejected call leaves nothing on the
+  // stream and cannot clear the error word of an earlier call still in flight.
+  kvsel_status st = kvsel::check_score_args(desc, q, k, scores, page_scores);
   if (st != KVSEL_OK) return st;
+  size_t need = 0;
+  if ((st = kvsel_workspace_size(desc, &need)) != KVSEL_OK) return st;
   if (need > kScratchBytes) return KVSEL_ERR_WORKSPACE;   // larger than the built-in scratch
-  if (q == nullptr || k == nullptr || scores == nullptr) return KVSEL_ERR_INVALID_ARG;
-  if (desc->page_size > 1 && page_scores == nullptr) return KVSEL_ERR_INVALID_ARG;
   void* ws = nullptr;
   if ((st = scratch_on_current_device(&ws)) != KVSEL_OK) return st;
   // The array keeps the previous call's contents.  The scoring passes rewrite
@@ -61,4 +62,11 @@ extern "C" KVSEL_API kvsel_status kvsel_score_noalloc(const kvsel_desc* desc, co
   // must start at zero.
   if (cudaMemsetAsync(ws, 0, sizeof(kvsel::DeviceError), stream) != cudaSuccess) return KVSEL_ERR_CUDA;
   return kvsel_score(desc, q, k, scores, page_scores, ws, kScratchBytes, stream);
+}
+
+extern "C" KVSEL_API kvsel_status kvsel_noalloc_read_device_error(cudaStream_t stream) {
+  void* ws = nullptr;
+  kvsel_status st = scratch_on_current_device(&ws);
+  if (st != KVSEL_OK) return st;
+  return kvsel_read_device_error(ws, stream);
 }

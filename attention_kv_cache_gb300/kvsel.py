@@ -75,6 +75,7 @@ def _load():
         "kvsel_attend_workspace_size": (I32, [D, I32, I32, I32, P(SZ)]),
         "kvsel_attend": (I32, [D, VP, I32, VP, VP, VP, VP, I32, I32, I32, VP, VP, SZ, VP]),
         "kvsel_read_device_error": (I32, [VP, VP]),
+        "kvsel_noalloc_read_device_error": (I32, [VP]),
         "kvsel_selftest_bounded_wait": (I32, [VP, ctypes.c_uint32, I32, VP]),
         "kvsel_status_string": (ctypes.c_char_p, [I32]),
         "kvsel_version": (ctypes.c_char_p, []),
@@ -93,7 +94,7 @@ _lib = _load()
 EXPORTED = ("kvsel_workspace_size", "kvsel_score", "kvsel_score_noalloc", "kvsel_prefill_attention",
             "kvsel_score_from_lse", "kvsel_combine_layers",
             "kvsel_aggregate", "kvsel_select", "kvsel_topk", "kvsel_compact", "kvsel_compact_layers",
-            "kvsel_pagetable", "kvsel_attend_workspace_size", "kvsel_attend", "kvsel_read_device_error", "kvsel_selftest_bounded_wait", "kvsel_status_string",
+            "kvsel_pagetable", "kvsel_attend_workspace_size", "kvsel_attend", "kvsel_read_device_error", "kvsel_noalloc_read_device_error", "kvsel_selftest_bounded_wait", "kvsel_status_string",
             "kvsel_version", "kvsel_trace_enable", "kvsel_trace_read", "kvsel_launch_count")
 
 
@@ -235,6 +236,11 @@ def kvsel_attend(desc, q, n_q: int, k, v, kv_indptr, kv_indices, n_per_row: int,
 def kvsel_read_device_error(ws, stream=None) -> int:
     """Status recorded by the device in the workspace's error word (clears it)."""
     return _lib.kvsel_read_device_error(_ptr(ws), _stream(stream))
+
+
+def kvsel_noalloc_read_device_error(stream=None) -> int:
+    """Status the device recorded during the last kvsel_score_noalloc call on the current device (clears it)."""
+    return _lib.kvsel_noalloc_read_device_error(_stream(stream))
 
 
 def kvsel_selftest_bounded_wait(ws, polls: int, arrive: bool, stream=None):

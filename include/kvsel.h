@@ -344,16 +344,27 @@ KVSEL_API kvsel_status kvsel_pagetable(const kvsel_desc* desc, const uint8_t* ma
  * frees nothing.
  *
  * The first call made while a device is current looks up that array's device
- * address (cudaGetSymbolAddress) and caches it; make that first call before
- * any stream capture.  The stream must belong to the current device.  All
- * calls share the one array: calls whose work overlaps on the GPU (two
- * streams, or two host threads) race and give undefined results.  A
- * descriptor whose kvsel_workspace_size() exceeds KVSEL_NOALLOC_SCRATCH_BYTES
- * is rejected with KVSEL_ERR_WORKSPACE before anything is launched.
+ * address (cudaGetSymbolAddress) and caches it for the life of the process;
+ * make that first call before any stream capture.  cudaDeviceReset after it
+ * is not supported (the module may then load at another address and the
+ * cached one would be stale).  The stream must belong to the current device.
+ * All calls share the one array: calls whose work overlaps on the GPU (two
+ * streams, or two host threads) race and give undefined results.  Arguments
+ * are checked as kvsel_score checks them, and a descriptor whose
+ * kvsel_workspace_size() exceeds KVSEL_NOALLOC_SCRATCH_BYTES is rejected with
+ * KVSEL_ERR_WORKSPACE; a rejected call launches nothing and enqueues nothing.
+ *
+ * Errors only the device sees (a bounded wait that ran out) go to the error
+ * word at the start of the array, which each call clears first; read it with
+ * kvsel_noalloc_read_device_error() on the call's stream before the next call.
  */
 #define KVSEL_NOALLOC_SCRATCH_BYTES (32u << 20)
 KVSEL_API kvsel_status kvsel_score_noalloc(const kvsel_desc* desc, const void* q, const void* k,
                                            float* scores, float* page_scores, cudaStream_t stream);
+
+/* Reads (stream-synchronising) and clears the error word of the current device's built-in scratch:
+ * the status of the last kvsel_score_noalloc call on that device, or KVSEL_OK. */
+KVSEL_API kvsel_status kvsel_noalloc_read_device_error(cudaStream_t stream);
 
 /*
  * kvsel_selftest_bounded_wait — exercises the bounded device wait used by every pipelined kernel.
