@@ -67,7 +67,8 @@ __device__ __forceinline__ void row_list(const AttArgs& a, const SeqInfo& si, in
 
 template <int D>
 __global__ void __launch_bounds__(kAttThreads) attend_split(const __grid_constant__ AttArgs a,
-                                                            const __grid_constant__ SeqTable t) {
+                                                            const __grid_constant__ SeqTable tp) {
+  const SeqTable& t = real_table(tp);
   constexpr int LDR = D + kRowPad;                 // staged row stride (bf16)
   constexpr int VPR = D / 8;                       // 16-byte vectors per row
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -279,7 +280,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 template <int D>
 __global__ void __launch_bounds__(32 * kWarpsPerCta) attend_warp(const __grid_constant__ AttArgs a,
-                                                                 const __grid_constant__ SeqTable t) {
+                                                                 const __grid_constant__ SeqTable tp) {
+  const SeqTable& t = real_table(tp);
   constexpr int VPR = D / 8;          // 16-byte chunks per row
   constexpr int STAGE = kStep * D;    // bf16 elements of one K (or V) stage
   constexpr int NT = D / 8;           // 8-wide tiles of the head dim in O

@@ -24,7 +24,8 @@ struct CompactArgs {
 // vpr 16-byte vectors; consecutive threads take consecutive vectors, so every row is read and
 // written as whole 128-byte lines, and the unit's geometry is decoded once per CTA.
 __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const __grid_constant__ CompactArgs a,
-                                                                  const __grid_constant__ SeqTable t) {
+                                                                  const __grid_constant__ SeqTable tp) {
+  const SeqTable& t = real_table(tp);
   const int unit = blockIdx.x / a.chunks;
   const int chunk = blockIdx.x % a.chunks;
   const int per_seq = a.n_out * a.h_kv;
@@ -33,6 +34,7 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const __grid_c
   const int lo = rem / a.h_kv, g = rem % a.h_kv;
   const int layer = a.layer_lo + lo;
   const SeqInfo& si = t.s[b];
+  if (si.n_keys == 0) return;            // a table whose device lengths failed the checks
   const int il = a.idx_layers == 1 ? 0 : lo;
   const int ih = a.idx_heads == 1 ? 0 : g;
   const int32_t* idx = a.idx + (((int64_t)b * a.idx_layers + il) * a.idx_heads + ih) * a.n_sel;
@@ -101,7 +103,8 @@ __device__ __forceinline__ bool union_hit(const PtArgs& a, int b, int layer, int
 }
 
 __global__ void __launch_bounds__(kPtThreads) pt_count(const __grid_constant__ PtArgs a,
-                                                       const __grid_constant__ SeqTable t) {
+                                                       const __grid_constant__ SeqTable tp) {
+  const SeqTable& t = real_table(tp);
   const int row = blockIdx.x;
   const int per_seq = a.n_layers * a.h_kv;
   const int b = row / per_seq, lg = row % per_seq;
@@ -152,7 +155,8 @@ __global__ void __launch_bounds__(1024) pt_scan(const __grid_constant__ PtArgs a
 }
 
 __global__ void __launch_bounds__(kPtThreads) pt_write(const __grid_constant__ PtArgs a,
-                                                       const __grid_constant__ SeqTable t) {
+                                                       const __grid_constant__ SeqTable tp) {
+  const SeqTable& t = real_table(tp);
   __shared__ int warp_cnt[kPtThreads / 32];
   const int row = blockIdx.x;
   const int per_seq = a.n_layers * a.h_kv;

@@ -33,9 +33,10 @@ __device__ __forceinline__ void set_device_error(DeviceError* e, uint32_t code, 
   if (atomicCAS(&e->code, 0u, code) == 0u) atomicExch(&e->where, where);
 }
 
-// Per-sequence geometry of one call (lives in kernel parameters).
+// Per-sequence geometry of one call (lives in kernel parameters, or in the workspace when the
+// prefix lengths live on the device).
 struct SeqInfo {
-  int32_t L;            // prefix length L_b
+  int32_t L;            // prefix length L_b (0 in a table whose device lengths failed the checks)
   int32_t n_keys;       // L_b + W
   int64_t k_off;        // element offset of the sequence's K / V block
   int64_t s_off;        // element offset of its token scores ([layers][h_kv][L_b])
@@ -47,16 +48,87 @@ struct SeqInfo {
   int32_t aux;          // launch-specific (KV blocks for the page table)
 };
 
+struct SeqTable;
+
+// How a call whose prefix lengths live on the device rebuilds its tables there (host side only;
+// the kernels never read it).  The host copy of such a table is built from the bound prefix_len_max
+// for every sequence, so the grids and tensor maps sized from it cover every real length.
+struct TablePlan {
+  const int64_t* lens_dev;   // [device] L_b, or nullptr: host lengths, the host table is the real one
+  const int32_t* aux_dev;    // [device] per-sequence aux values (page-table KV blocks), or nullptr
+  SeqTable* slots;           // [device] kTableSlots tables in the workspace
+  DeviceError* err;
+  int64_t lmax;              // every L_b must lie in [1, lmax]
+  int64_t score_rows;        // score rows per sequence (the s_off / p_off strides)
+  int32_t n_layers, h_kv, d, W, P;
+  int32_t aux_max;           // aux_dev entries must lie in [0, aux_max]
+  int32_t chk_topk, topk_k, n_recent;   // per-sequence selection checks (kvsel_topk / kvsel_select)
+};
+
 struct SeqTable {
   int32_t batch;
   int32_t n_items;
+  const SeqTable* dev;       // [device] the real table (built from device lengths), or nullptr
+  TablePlan plan;
   SeqInfo s[KVSEL_MAX_BATCH];
 };
+
+// Tables a call may keep in its workspace, right after the error word.
+constexpr int kTableSlots = 2;
+constexpr size_t kTableArea = (kTableSlots * sizeof(SeqTable) + KVSEL_WS_ALIGN - 1) / KVSEL_WS_ALIGN * KVSEL_WS_ALIGN;
+constexpr size_t kTableOff = sizeof(DeviceError);
+
+// The table a kernel reads: its parameter, or the device-built table the parameter points to.
+__device__ __forceinline__ const SeqTable& real_table(const SeqTable& param) {
+  return param.dev != nullptr ? *param.dev : param;
+}
 
 __device__ __forceinline__ int find_seq(const SeqTable& t, int item) {
   int b = 0;
   while (b + 1 < t.batch && t.s[b + 1].item0 <= item) ++b;
   return b;
+}
+
+// Per-sequence geometry from the prefix lengths (host lengths, bounds, or on the device, the real
+// ones): offsets of each sequence in the packed K / V, score and page-score layouts.  Work items
+// are left empty (with_items fills them).
+__host__ __device__ inline void fill_table(SeqTable& t, int batch, const int64_t* lens, const int32_t* aux,
+                                           int n_layers, int h_kv, int d, int W, int P, int64_t score_rows) {
+  t.batch = batch;
+  t.n_items = 0;
+  int64_t k_off = 0, s_off = 0, p_off = 0;
+  for (int b = 0; b < batch; ++b) {
+    SeqInfo& s = t.s[b];
+    s.L = (int32_t)lens[b];
+    s.n_keys = s.L + W;
+    s.k_off = k_off;
+    s.s_off = s_off;
+    s.p_off = p_off;
+    s.item0 = 0;
+    s.n_seg = 0;
+    s.part_off = 0;
+    s.unit0 = b * n_layers * h_kv;
+    s.aux = aux != nullptr ? aux[b] : 0;
+    k_off += (int64_t)n_layers * h_kv * s.n_keys * d;
+    s_off += score_rows * s.L;
+    p_off += score_rows * ((s.L + P - 1) / P);
+  }
+}
+
+// Work items: n_seg = ceil(len_b / seg) segments for each (layer, KV head) unit of sequence b,
+// where len_b is L_b + W (pass 1) or L_b (pass 2).
+__host__ __device__ inline void fill_items(SeqTable& t, int64_t units_per_seq, int64_t seg, bool include_window,
+                                           int32_t window) {
+  int64_t item = 0;
+  for (int b = 0; b < t.batch; ++b) {
+    const int64_t len = (int64_t)t.s[b].L + (include_window && t.s[b].L > 0 ? window : 0);
+    const int64_t ns = (len + seg - 1) / seg;
+    t.s[b].item0 = (int32_t)item;
+    t.s[b].n_seg = (int32_t)ns;
+    t.s[b].part_off = item;
+    item += units_per_seq * ns;
+  }
+  t.n_items = (int32_t)item;
 }
 
 // Keys per pass-1 segment (fixes the size of the per-segment partials in the workspace).
@@ -112,23 +184,10 @@ kvsel_status launch_score_simt(const ScoreShape& sh, const SeqTable& t1, const S
 kvsel_status launch_lse_combine(const ScoreShape& sh, const SeqTable& t1, float2* part, float* lse,
                                 cudaStream_t s);
 
-// Work items: n_seg = ceil(len_b / seg) segments for each (layer, KV head) unit of sequence b,
-// where len_b is L_b + W (pass 1) or L_b (pass 2).
-inline SeqTable with_items(const SeqTable& base, int64_t units_per_seq, int64_t seg, bool include_window,
-                           int32_t window) {
-  SeqTable t = base;
-  int64_t item = 0;
-  for (int b = 0; b < t.batch; ++b) {
-    const int64_t len = (int64_t)t.s[b].L + (include_window ? window : 0);
-    const int64_t ns = (len + seg - 1) / seg;
-    t.s[b].item0 = (int32_t)item;
-    t.s[b].n_seg = (int32_t)ns;
-    t.s[b].part_off = item;
-    item += units_per_seq * ns;
-  }
-  t.n_items = (int32_t)item;
-  return t;
-}
+// A copy of `base` with work items (fill_items).  With device lengths the same table is also built on
+// the device, into workspace slot `slot`, and the copy points at it (kvsel_api.cu).
+kvsel_status with_items(const SeqTable& base, int64_t units_per_seq, int64_t seg, bool include_window,
+                        int32_t window, int slot, cudaStream_t s, SeqTable* out);
 
 // Top-k over `rows` score rows per sequence; sequence b's rows start at element
 // rows * (sum of n over earlier sequences), n = L_b or ceil(L_b / P).

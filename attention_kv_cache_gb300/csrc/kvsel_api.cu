@@ -92,7 +92,10 @@ static inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 static int64_t total_units(const kvsel_desc& d) { return (int64_t)d.batch * d.n_layers * d.h_kv; }
-static int64_t nseg1(const kvsel_desc& d, int b) { return cdiv(d.prefix_lens[b] + d.window, kScoreSeg1); }
+static bool lens_on_device(const kvsel_desc& d) { return d.prefix_lens_dev != nullptr; }
+// L_b as the host sees it: the real length, or with device lengths the bound (which sizes everything).
+static int64_t len_at(const kvsel_desc& d, int b) { return lens_on_device(d) ? d.prefix_len_max : d.prefix_lens[b]; }
+static int64_t nseg1(const kvsel_desc& d, int b) { return cdiv(len_at(d, b) + d.window, kScoreSeg1); }
 
 struct WsLayout {
   size_t lse_off, part_off, norm_off, cnt_off, total;
@@ -102,7 +105,7 @@ static WsLayout ws_layout(const kvsel_desc& d) {
   WsLayout w{};
   const int64_t R = (int64_t)(d.h_q / d.h_kv) * d.window;
   const int64_t units = total_units(d);
-  size_t off = sizeof(DeviceError);
+  size_t off = kTableOff + kTableArea;           // error word, then the device-built tables
   w.lse_off = off;
   off = align_up(off + (size_t)(units * R) * sizeof(float), KVSEL_WS_ALIGN);
   w.part_off = off;
@@ -119,7 +122,8 @@ static WsLayout ws_layout(const kvsel_desc& d) {
 
 // ----------------------------------------------------------------------------- checks
 static kvsel_status check_desc(const kvsel_desc* d) {
-  if (d == nullptr || d->prefix_lens == nullptr) return KVSEL_ERR_INVALID_ARG;
+  if (d == nullptr) return KVSEL_ERR_INVALID_ARG;
+  if ((d->prefix_lens == nullptr) == (d->prefix_lens_dev == nullptr)) return KVSEL_ERR_INVALID_ARG;  // exactly one
   if (d->n_layers < 1 || d->h_kv < 1 || d->h_q < 1 || d->h_q % d->h_kv != 0) return KVSEL_ERR_INVALID_ARG;
   if (d->batch < 1 || d->batch > KVSEL_MAX_BATCH) return KVSEL_ERR_INVALID_ARG;
   if (d->window < 1 || d->window > KVSEL_MAX_WINDOW) return KVSEL_ERR_INVALID_ARG;
@@ -131,8 +135,8 @@ static kvsel_status check_desc(const kvsel_desc* d) {
   if (d->score_mode != KVSEL_SCORE_SOFTMAX && d->score_mode != KVSEL_SCORE_LOGITS) return KVSEL_ERR_INVALID_ARG;
   if (d->pool_k < 1 || d->pool_k % 2 == 0 || d->pool_k > 63) return KVSEL_ERR_INVALID_ARG;
   if (d->page_size < 1 || d->page_size > KVSEL_MAX_PAGE) return KVSEL_ERR_INVALID_ARG;
-  for (int b = 0; b < d->batch; ++b) {
-    const int64_t L = d->prefix_lens[b];
+  for (int b = 0; b < d->batch; ++b) {     // with device lengths: the bound here, each L_b on the device
+    const int64_t L = len_at(*d, b);
     if (L < 1 || L + d->window >= (int64_t(1) << 31)) return KVSEL_ERR_INVALID_ARG;
   }
   if (total_units(*d) > (int64_t(1) << 24)) return KVSEL_ERR_INVALID_ARG;
@@ -175,39 +179,118 @@ ScoreShape make_shape(const kvsel_desc& d) {
   return sh;
 }
 
-// Sequence table: element offsets of each sequence in the packed layouts.
-static SeqTable make_table(const kvsel_desc& d, int32_t layers_in_scores) {
-  SeqTable t;
-  memset(&t, 0, sizeof(t));
-  t.batch = d.batch;
-  int64_t k_off = 0, s_off = 0, p_off = 0;
-  for (int b = 0; b < d.batch; ++b) {
-    SeqInfo& s = t.s[b];
-    s.L = (int32_t)d.prefix_lens[b];
-    s.n_keys = s.L + d.window;
-    s.k_off = k_off;
-    s.s_off = s_off;
-    s.p_off = p_off;
-    s.unit0 = b * d.n_layers * d.h_kv;
-    k_off += (int64_t)d.n_layers * d.h_kv * s.n_keys * d.head_dim;
-    s_off += (int64_t)layers_in_scores * d.h_kv * s.L;
-    p_off += (int64_t)layers_in_scores * d.h_kv * cdiv(s.L, d.page_size);
+// ----------------------------------------------------------------------------- sequence tables
+// Per-sequence checks a device-built table makes (the host makes them itself with host lengths).
+struct SeqChecks {
+  int32_t topk = 0, k = 0, n_recent = 0;   // kvsel_topk / kvsel_select rules on each L_b
+  const int32_t* aux = nullptr;           // per-sequence aux values ([host] or [device] like the lengths)
+  int32_t aux_max = 0;
+};
+
+struct PlanLaunch {
+  TablePlan p;
+  SeqTable* out;
+  int32_t batch, with_items, include_window;
+  int64_t units, seg;
+};
+
+// Builds one call's sequence table from the device-resident prefix lengths (one thread: a batch is at
+// most KVSEL_MAX_BATCH sequences).  A length outside [1, prefix_len_max], or one that breaks the
+// call's selection rules, records KVSEL_ERR_INVALID_ARG with the sequence as detail and leaves a
+// table of empty sequences (L = 0), which every kernel skips.
+__global__ void __launch_bounds__(32) seq_table_kernel(const __grid_constant__ PlanLaunch a) {
+  if (threadIdx.x != 0) return;
+  const TablePlan& p = a.p;
+  SeqTable& t = *a.out;
+  int bad = -1;
+  for (int b = 0; b < a.batch && bad < 0; ++b) {
+    const int64_t L = p.lens_dev[b];
+    bool ok = L >= 1 && L <= p.lmax;
+    if (ok && p.chk_topk) {
+      if (p.P == 1) {
+        ok = p.topk_k <= L;
+      } else {
+        const int64_t n_pages = (L + p.P - 1) / p.P;
+        ok = p.n_recent <= n_pages && p.topk_k <= n_pages - p.n_recent && (L % p.P == 0 || p.n_recent >= 1);
+      }
+    }
+    if (ok && p.aux_dev != nullptr) ok = p.aux_dev[b] >= 0 && p.aux_dev[b] <= p.aux_max;
+    if (!ok) bad = b;
   }
-  return t;
+  if (bad >= 0) {
+    set_device_error(p.err, KVSEL_ERR_INVALID_ARG, (uint32_t)bad);
+    t.batch = a.batch;
+    t.n_items = 0;
+    t.dev = nullptr;
+    for (int b = 0; b < a.batch; ++b) t.s[b] = SeqInfo{};
+    return;
+  }
+  fill_table(t, a.batch, p.lens_dev, p.aux_dev, p.n_layers, p.h_kv, p.d, p.W, p.P, p.score_rows);
+  t.dev = nullptr;
+  if (a.with_items) fill_items(t, a.units, a.seg, a.include_window != 0, p.W);
 }
 
-// Sequence table for `rows` score rows per sequence (top-k inputs): s_off / p_off become the
-// offsets of each sequence's [rows][L_b] token scores / [rows][ceil(L_b / P)] page scores.
-static SeqTable make_table_rows(const kvsel_desc& d, int32_t rows) {
-  SeqTable t = make_table(d, d.n_layers);
-  int64_t s_off = 0, p_off = 0;
-  for (int b = 0; b < d.batch; ++b) {
-    t.s[b].s_off = s_off;
-    t.s[b].p_off = p_off;
-    s_off += (int64_t)rows * t.s[b].L;
-    p_off += (int64_t)rows * cdiv(t.s[b].L, d.page_size);
+static kvsel_status launch_table(const SeqTable& host, bool with_items_, int64_t units, int64_t seg,
+                                 bool include_window, int slot, cudaStream_t s) {
+  PlanLaunch a;
+  a.p = host.plan;
+  a.out = host.plan.slots + slot;
+  a.batch = host.batch;
+  a.with_items = with_items_ ? 1 : 0;
+  a.include_window = include_window ? 1 : 0;
+  a.units = units;
+  a.seg = seg;
+  TraceScope ts("seq_table", s);
+  seq_table_kernel<<<1, 32, 0, s>>>(a);
+  return launch_status();
+}
+
+// The call's sequence table for score arrays of `score_rows` rows per sequence.  With host lengths it
+// is exact.  With device lengths the host copy holds the bound for every sequence (grids and tensor
+// maps are sized from it) and the real table is built on the device into workspace slot 0, on the
+// call's stream; the copy's `dev` points at it.
+static kvsel_status make_table(const kvsel_desc& d, int64_t score_rows, void* ws, cudaStream_t s, SeqTable* t,
+                               const SeqChecks& chk = SeqChecks{}, bool build = true) {
+  memset(t, 0, sizeof(*t));
+  std::vector<int64_t> lens(d.batch);
+  for (int b = 0; b < d.batch; ++b) lens[b] = len_at(d, b);
+  const bool dev = lens_on_device(d);
+  fill_table(*t, d.batch, lens.data(), dev ? nullptr : chk.aux, d.n_layers, d.h_kv, d.head_dim, d.window,
+             d.page_size, score_rows);
+  if (!dev) return KVSEL_OK;
+  if (ws == nullptr || ((uintptr_t)ws % KVSEL_WS_ALIGN) != 0) return KVSEL_ERR_WORKSPACE;
+  if (chk.aux != nullptr)
+    for (int b = 0; b < d.batch; ++b) t->s[b].aux = chk.aux_max;   // bound for sizing; real values on the device
+  TablePlan& p = t->plan;
+  p.lens_dev = d.prefix_lens_dev;
+  p.aux_dev = chk.aux;
+  p.slots = reinterpret_cast<SeqTable*>(static_cast<char*>(ws) + kTableOff);
+  p.err = reinterpret_cast<DeviceError*>(ws);
+  p.lmax = d.prefix_len_max;
+  p.score_rows = score_rows;
+  p.n_layers = d.n_layers;
+  p.h_kv = d.h_kv;
+  p.d = d.head_dim;
+  p.W = d.window;
+  p.P = d.page_size;
+  p.aux_max = chk.aux_max;
+  p.chk_topk = chk.topk;
+  p.topk_k = chk.k;
+  p.n_recent = chk.n_recent;
+  t->dev = p.slots;
+  return build ? launch_table(*t, false, 0, 0, false, 0, s) : KVSEL_OK;
+}
+
+kvsel_status with_items(const SeqTable& base, int64_t units_per_seq, int64_t seg, bool include_window,
+                        int32_t window, int slot, cudaStream_t s, SeqTable* out) {
+  *out = base;
+  fill_items(*out, units_per_seq, seg, include_window, window);
+  if (base.plan.lens_dev == nullptr) {
+    out->dev = nullptr;
+    return KVSEL_OK;
   }
-  return t;
+  out->dev = base.plan.slots + slot;
+  return launch_table(*out, true, units_per_seq, seg, include_window, slot, s);
 }
 
 // Shared checks of a top-k request (token or page mode).
@@ -217,17 +300,25 @@ static kvsel_status check_topk(const kvsel_desc& d, int32_t k, int32_t n_recent)
   if (P == 1) {
     if (n_recent != 0) return KVSEL_ERR_INVALID_ARG;
     for (int b = 0; b < d.batch; ++b)
-      if (k > d.prefix_lens[b]) return KVSEL_ERR_INVALID_ARG;
+      if (k > len_at(d, b)) return KVSEL_ERR_INVALID_ARG;
   } else {
     if (d.window % P != 0) return KVSEL_ERR_UNSUPPORTED;
     for (int b = 0; b < d.batch; ++b) {
-      const int64_t L = d.prefix_lens[b];
+      const int64_t L = len_at(d, b);
       const int64_t n_pages = cdiv(L, P);
       if (n_recent > n_pages || k > n_pages - n_recent) return KVSEL_ERR_INVALID_ARG;
-      if (L % P != 0 && n_recent < 1) return KVSEL_ERR_INVALID_ARG;
+      if (!lens_on_device(d) && L % P != 0 && n_recent < 1) return KVSEL_ERR_INVALID_ARG;
     }
   }
-  return KVSEL_OK;
+  return KVSEL_OK;   // with device lengths these held for the bound; the device checks each L_b
+}
+
+static SeqChecks topk_checks(int32_t k, int32_t n_recent) {
+  SeqChecks c;
+  c.topk = 1;
+  c.k = k;
+  c.n_recent = n_recent;
+  return c;
 }
 
 }  // namespace kvsel
@@ -271,7 +362,8 @@ kvsel_status kvsel_score(const kvsel_desc* desc, const void* q, const void* k, f
   auto ws_base = [](void* p) { return static_cast<char*>(p); };
 
   const ScoreShape sh = make_shape(d);
-  const SeqTable base = make_table(d, d.n_layers);
+  SeqTable base;
+  if ((st = make_table(d, (int64_t)d.n_layers * d.h_kv, ws, stream, &base, SeqChecks{}, false)) != KVSEL_OK) return st;
   return launch_score(sh, base, q, k, scores, page_scores, reinterpret_cast<float*>(ws_base(ws) + w.lse_off),
                       reinterpret_cast<float2*>(ws_base(ws) + w.part_off), reinterpret_cast<DeviceError*>(ws),
                       stream);
@@ -291,7 +383,8 @@ kvsel_status kvsel_score_from_lse(const kvsel_desc* desc, const void* q_win, con
   const WsLayout w = ws_layout(d);
   ScoreShape sh = make_shape(d);
   sh.lse_given = 1;
-  const SeqTable base = make_table(d, d.n_layers);
+  SeqTable base;
+  if ((st = make_table(d, (int64_t)d.n_layers * d.h_kv, ws, stream, &base, SeqChecks{}, false)) != KVSEL_OK) return st;
   return launch_score(sh, base, q_win, k, scores, page_scores, const_cast<float*>(lse_win),
                       reinterpret_cast<float2*>(static_cast<char*>(ws) + w.part_off), reinterpret_cast<DeviceError*>(ws),
                       stream);
@@ -308,7 +401,11 @@ kvsel_status kvsel_prefill_attention(const kvsel_desc* desc, const void* q, cons
     return KVSEL_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(q_win)) return KVSEL_ERR_INVALID_ARG;
   if (ws != nullptr && ((uintptr_t)ws % KVSEL_WS_ALIGN) != 0) return KVSEL_ERR_WORKSPACE;
-  const SeqTable t = make_table(d, d.n_layers);
+  // The prefill's last K / V tile may reach past the real rows, which must then be finite: with host
+  // lengths the tensor maps end there and fill zeros; bound-sized maps could read unwritten memory.
+  if (lens_on_device(d)) return KVSEL_ERR_UNSUPPORTED;
+  SeqTable t;
+  if ((st = make_table(d, (int64_t)d.n_layers * d.h_kv, ws, stream, &t)) != KVSEL_OK) return st;
   return launch_prefill(d, t, q, k, v, o, lse, lse_win, q_win, reinterpret_cast<DeviceError*>(ws), stream);
 }
 
@@ -322,7 +419,8 @@ kvsel_status kvsel_combine_layers(const kvsel_desc* desc, const float* scores, i
   if (scores == nullptr || combined == nullptr) return KVSEL_ERR_INVALID_ARG;
   if (layer_lo < 0 || layer_hi < layer_lo || layer_hi >= d.n_layers) return KVSEL_ERR_INVALID_ARG;
   if ((st = check_ws(d, ws, ws_bytes)) != KVSEL_OK) return st;
-  SeqTable t = make_table(d, d.n_layers);
+  SeqTable t;
+  if ((st = make_table(d, (int64_t)d.n_layers * d.h_kv, ws, stream, &t)) != KVSEL_OK) return st;
   const WsLayout w = ws_layout(d);
   return launch_aggregate(d, t, scores, layer_lo, layer_hi, KVSEL_LAYERS_L1_MEAN, KVSEL_HEADS_EACH,
                           reinterpret_cast<float*>(static_cast<char*>(ws) + w.norm_off), combined, stream);
@@ -341,7 +439,8 @@ kvsel_status kvsel_aggregate(const kvsel_desc* desc, const float* scores, int32_
     return KVSEL_ERR_INVALID_ARG;
   if (head_op != KVSEL_HEADS_EACH && head_op != KVSEL_HEADS_SUM) return KVSEL_ERR_INVALID_ARG;
   if ((st = check_ws(d, ws, ws_bytes)) != KVSEL_OK) return st;
-  SeqTable t = make_table(d, d.n_layers);
+  SeqTable t;
+  if ((st = make_table(d, (int64_t)d.n_layers * d.h_kv, ws, stream, &t)) != KVSEL_OK) return st;
   const WsLayout w = ws_layout(d);
   return launch_aggregate(d, t, scores, layer_lo, layer_hi, layer_op, head_op,
                           reinterpret_cast<float*>(static_cast<char*>(ws) + w.norm_off), out, stream);
@@ -358,7 +457,8 @@ kvsel_status kvsel_select(const kvsel_desc* desc, const float* scores, int32_t r
   if (rows < 1 || (int64_t)rows * d.batch >= (int64_t(1) << 31)) return KVSEL_ERR_INVALID_ARG;
   if ((st = check_topk(d, k, n_recent)) != KVSEL_OK) return st;
   if ((st = check_ws(d, ws, ws_bytes)) != KVSEL_OK) return st;
-  SeqTable t = make_table_rows(d, rows);
+  SeqTable t;
+  if ((st = make_table(d, rows, ws, stream, &t, topk_checks(k, n_recent))) != KVSEL_OK) return st;
   return launch_topk(d, t, rows, k, n_recent, append_window != 0, scores, idx_out, stream);
 }
 
@@ -374,7 +474,8 @@ kvsel_status kvsel_topk(const kvsel_desc* desc, const float* scores, int32_t lay
   if ((st = check_topk(d, k, n_recent)) != KVSEL_OK) return st;
   if ((st = check_ws(d, ws, ws_bytes)) != KVSEL_OK) return st;
   const int32_t rows = layers * d.h_kv;
-  SeqTable t = make_table_rows(d, rows);
+  SeqTable t;
+  if ((st = make_table(d, rows, ws, stream, &t, topk_checks(k, n_recent))) != KVSEL_OK) return st;
   return launch_topk(d, t, rows, k, n_recent, true, scores, idx_out, stream);
 }
 
@@ -392,8 +493,10 @@ kvsel_status kvsel_compact(const kvsel_desc* desc, const void* k, const void* v,
   if (n_sel < 0) return KVSEL_ERR_INVALID_ARG;
   if ((int64_t)n_sel * d.page_size >= (int64_t(1) << 31)) return KVSEL_ERR_INVALID_ARG;
   if (ws != nullptr && ((uintptr_t)ws % KVSEL_WS_ALIGN) != 0) return KVSEL_ERR_WORKSPACE;
+  if (lens_on_device(d) && ws == nullptr) return KVSEL_ERR_WORKSPACE;
   if (n_sel == 0) return KVSEL_OK;
-  SeqTable t = make_table(d, d.n_layers);
+  SeqTable t;
+  if ((st = make_table(d, (int64_t)d.n_layers * d.h_kv, ws, stream, &t)) != KVSEL_OK) return st;
   return launch_compact(d, t, k, v, idx, idx_layers, d.h_kv, 0, d.n_layers, n_sel, k_out, v_out,
                         reinterpret_cast<DeviceError*>(ws), stream);
 }
@@ -414,8 +517,10 @@ kvsel_status kvsel_compact_layers(const kvsel_desc* desc, const void* k, const v
   if (n_sel < 0) return KVSEL_ERR_INVALID_ARG;
   if ((int64_t)n_sel * d.page_size >= (int64_t(1) << 31)) return KVSEL_ERR_INVALID_ARG;
   if (ws != nullptr && ((uintptr_t)ws % KVSEL_WS_ALIGN) != 0) return KVSEL_ERR_WORKSPACE;
+  if (lens_on_device(d) && ws == nullptr) return KVSEL_ERR_WORKSPACE;
   if (n_sel == 0) return KVSEL_OK;
-  SeqTable t = make_table(d, d.n_layers);
+  SeqTable t;
+  if ((st = make_table(d, (int64_t)d.n_layers * d.h_kv, ws, stream, &t)) != KVSEL_OK) return st;
   return launch_compact(d, t, k, v, idx, idx_layers, idx_heads, layer_lo, n_layers_out, n_sel, k_out, v_out,
                         reinterpret_cast<DeviceError*>(ws), stream);
 }
@@ -428,8 +533,9 @@ static kvsel_status attend_plan(const kvsel_desc& d, int32_t n_q, int32_t block,
   const int64_t R = (int64_t)(d.h_q / d.h_kv) * n_q;
   *S = attend_splits(rows, std::max<int64_t>(1, (int64_t)max_blocks * block), (int)R, d.head_dim);
   if (rows * *S >= (int64_t(1) << 31)) return KVSEL_ERR_UNSUPPORTED;
-  // error word, partials of the splits
-  *bytes = align_up(sizeof(DeviceError) + (size_t)(rows * *S * R * (d.head_dim + 2)) * sizeof(float), KVSEL_WS_ALIGN);
+  // error word, device-built tables, partials of the splits
+  *bytes = align_up(kTableOff + kTableArea + (size_t)(rows * *S * R * (d.head_dim + 2)) * sizeof(float),
+                    KVSEL_WS_ALIGN);
   return KVSEL_OK;
 }
 
@@ -458,12 +564,13 @@ kvsel_status kvsel_attend(const kvsel_desc* desc, const void* q, int32_t n_q, co
   size_t need = 0;
   if ((st = attend_plan(d, n_q, block, max_blocks, &S, &need)) != KVSEL_OK) return st;
   if (ws == nullptr || ((uintptr_t)ws % KVSEL_WS_ALIGN) != 0 || ws_bytes < need) return KVSEL_ERR_WORKSPACE;
-  if (kv_indices == nullptr)
+  if (kv_indices == nullptr)   // whole caches: with device lengths the bound must fit
     for (int b = 0; b < d.batch; ++b)
-      if (cdiv(d.prefix_lens[b] + d.window, block) > max_blocks) return KVSEL_ERR_INVALID_ARG;
-  SeqTable t = make_table(d, d.n_layers);
+      if (cdiv(len_at(d, b) + d.window, block) > max_blocks) return KVSEL_ERR_INVALID_ARG;
+  SeqTable t;
+  if ((st = make_table(d, (int64_t)d.n_layers * d.h_kv, ws, stream, &t)) != KVSEL_OK) return st;
   return launch_attend(d, t, q, n_q, k, v, kv_indptr, kv_indices, n_per_row, block, S,
-                       reinterpret_cast<float*>(static_cast<char*>(ws) + sizeof(DeviceError)), o,
+                       reinterpret_cast<float*>(static_cast<char*>(ws) + kTableOff + kTableArea), o,
                        reinterpret_cast<DeviceError*>(ws), stream);
 }
 
@@ -479,11 +586,14 @@ kvsel_status kvsel_pagetable(const kvsel_desc* desc, const uint8_t* mask, int32_
   if (n_qblk < 1 || n_kvblk_max < 1) return KVSEL_ERR_INVALID_ARG;
   if (total_units(d) * n_kvblk_max >= (int64_t(1) << 31)) return KVSEL_ERR_UNSUPPORTED;
   if ((st = check_ws(d, ws, ws_bytes)) != KVSEL_OK) return st;
-  SeqTable t = make_table(d, d.n_layers);
-  for (int b = 0; b < d.batch; ++b) {
-    if (n_kvblk[b] < 0 || n_kvblk[b] > n_kvblk_max) return KVSEL_ERR_INVALID_ARG;
-    t.s[b].aux = n_kvblk[b];
-  }
+  if (!lens_on_device(d))
+    for (int b = 0; b < d.batch; ++b)
+      if (n_kvblk[b] < 0 || n_kvblk[b] > n_kvblk_max) return KVSEL_ERR_INVALID_ARG;
+  SeqChecks chk;
+  chk.aux = n_kvblk;            // [host], or [device] with device lengths (checked there)
+  chk.aux_max = n_kvblk_max;
+  SeqTable t;
+  if ((st = make_table(d, (int64_t)d.n_layers * d.h_kv, ws, stream, &t, chk)) != KVSEL_OK) return st;
   const WsLayout w = ws_layout(d);
   return launch_pagetable(d, t, mask, n_qblk, n_kvblk_max,
                           reinterpret_cast<int32_t*>(static_cast<char*>(ws) + w.cnt_off), kv_indptr,

@@ -58,7 +58,6 @@ struct PfArgs {
   __nv_bfloat16* q_win;         // window queries, [batch][layers][h_q][W][d]
   DeviceError* err;
   int32_t n_pairs;              // query-tile pairs of the longest sequence
-  int64_t q_row0[KVSEL_MAX_BATCH];   // first row of each sequence in the q / o row view
 };
 
 __device__ __forceinline__ float fast_ex2(float x) {
@@ -132,7 +131,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                                                                 const __grid_constant__ CUtensorMap tk,
                                                                 const __grid_constant__ CUtensorMap tv,
                                                                 const __grid_constant__ PfArgs a,
-                                                                const __grid_constant__ SeqTable t) {
+                                                                const __grid_constant__ SeqTable tp) {
+  const SeqTable& t = real_table(tp);
   constexpr int D = 128;
   const int heads_total = a.batch * a.n_layers * a.h_q;
   const int pair = a.n_pairs - 1 - (int)(blockIdx.x / heads_total);   // heaviest pairs first
@@ -186,7 +186,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tmem = *tslot;
 
-  const int64_t qrow_base = a.q_row0[b] + ((int64_t)layer * a.h_q + h) * N;
+  // the sequence's first q / o row: its K rows (k_off / d) times the G query heads per KV head
+  const int64_t qrow_base = si.k_off / D * a.G + ((int64_t)layer * a.h_q + h) * N;
   const int64_t krow0 = si.k_off / D + ((int64_t)layer * a.h_kv + g) * N;
 
   if (warp == 0) {
@@ -470,7 +471,6 @@ kvsel_status launch_prefill(const kvsel_desc& d, const SeqTable& t, const void* 
   a.err = err;
   int64_t q_rows = 0, k_rows = 0, nmax = 0;
   for (int b = 0; b < d.batch; ++b) {
-    a.q_row0[b] = q_rows;
     const int64_t n = t.s[b].n_keys;
     q_rows += (int64_t)d.n_layers * d.h_q * n;
     k_rows += (int64_t)d.n_layers * d.h_kv * n;

@@ -108,7 +108,8 @@ __device__ __forceinline__ const __nv_bfloat16* unit_keys(const ScoreArgs& a, co
 // ------------------------------------------------------------------------ pass 1
 template <int D, int RP>
 __global__ void __launch_bounds__(kThreads) score_pass1_simt(const __grid_constant__ ScoreArgs a,
-                                                             const __grid_constant__ SeqTable t) {
+                                                             const __grid_constant__ SeqTable tp) {
+  const SeqTable& t = real_table(tp);
   constexpr int KPT = RP / 8, TPR = kTile / KPT, LD = D + 4;
   extern __shared__ __align__(16) float smem[];
   float* Qs = smem;
@@ -118,6 +119,7 @@ __global__ void __launch_bounds__(kThreads) score_pass1_simt(const __grid_consta
 
   const ScoreShape& sh = a.sh;
   const int item = blockIdx.x;
+  if (item >= t.n_items) return;         // the grid is sized for bound lengths
   const int b = find_seq(t, item);
   const SeqInfo& si = t.s[b];
   const int local = item - si.item0;
@@ -173,8 +175,9 @@ __global__ void __launch_bounds__(kThreads) score_pass1_simt(const __grid_consta
 
 // ------------------------------------------------------------------------ combine
 __global__ void __launch_bounds__(kThreads) score_lse_combine(const __grid_constant__ ScoreArgs a,
-                                                              const __grid_constant__ SeqTable t,
+                                                              const __grid_constant__ SeqTable tp,
                                                               int64_t n_rows) {
+  const SeqTable& t = real_table(tp);
   const int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x;
   if (i >= n_rows) return;
   const ScoreShape& sh = a.sh;
@@ -198,7 +201,8 @@ __global__ void __launch_bounds__(kThreads) score_lse_combine(const __grid_const
 // ------------------------------------------------------------------------ pass 2
 template <int D, int RP>
 __global__ void __launch_bounds__(kThreads) score_pass2_simt(const __grid_constant__ ScoreArgs a,
-                                                             const __grid_constant__ SeqTable t) {
+                                                             const __grid_constant__ SeqTable tp) {
+  const SeqTable& t = real_table(tp);
   constexpr int KPT = RP / 8, TPR = kTile / KPT, LD = D + 4, LDP = kTile + 1;
   extern __shared__ __align__(16) float smem[];
   const ScoreShape& sh = a.sh;
@@ -209,6 +213,7 @@ __global__ void __launch_bounds__(kThreads) score_pass2_simt(const __grid_consta
   float* Us = Ss + sh.seg2 + 128;       // pooled scores of [a0, a1)
 
   const int item = blockIdx.x;
+  if (item >= t.n_items) return;         // the grid is sized for bound lengths
   const int b = find_seq(t, item);
   const SeqInfo& si = t.s[b];
   const int local = item - si.item0;

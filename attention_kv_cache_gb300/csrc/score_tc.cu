@@ -855,7 +855,12 @@ template <bool PASS2, int RT, int D, int NK, int MAXW>
 __global__ void __launch_bounds__(Plan<PASS2, RT, D, NK>::kThreads, 1) score_tc_kernel(const __grid_constant__ CUtensorMap tq,
                                                                  const __grid_constant__ CUtensorMap tk,
                                                                  const __grid_constant__ TcArgs a,
-                                                                 const __grid_constant__ SeqTable t) {
+                                                                 const __grid_constant__ SeqTable tp) {
+  const SeqTable& t = real_table(tp);
+  {
+    const Work<PASS2> mine(t);   // a grid sized for bound lengths may hold CTAs with nothing to do
+    if (mine.pos >= mine.end) return;
+  }
   using P = Plan<PASS2, RT, D, NK>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1001,16 +1006,19 @@ kvsel_status launch_score(const ScoreShape& sh_in, const SeqTable& base, const v
   const bool tc = dev.major == 10 && dev.sms > 0 && sh.R <= 256 && w_ok && k_rows + 256 < (int64_t(1) << 31) &&
                   q_rows + 256 < (int64_t(1) << 31) && encode_fn() != nullptr;
   sh.seg1 = (int32_t)kScoreSeg1;
-  const SeqTable t1 = with_items(base, ups, kScoreSeg1, true, sh.W);
+  SeqTable t1, t2;
+  kvsel_status st = with_items(base, ups, kScoreSeg1, true, sh.W, 0, s, &t1);
+  if (st != KVSEL_OK) return st;
   if (!tc) {
     sh.seg2 = (int32_t)(sh.page_size * ((1024 + sh.page_size - 1) / sh.page_size));
-    const SeqTable t2 = with_items(base, ups, sh.seg2, false, sh.W);
+    if ((st = with_items(base, ups, sh.seg2, false, sh.W, 1, s, &t2)) != KVSEL_OK) return st;
     return launch_score_simt(sh, t1, t2, q, k, scores, page_scores, lse, part, err, s);
   }
   CUtensorMap tq, tk;
   if (!make_map(&tq, q, q_rows, sh.d) || !make_map(&tk, k, k_rows, sh.d)) return KVSEL_ERR_CUDA;
   sh.seg2 = (int32_t)(sh.page_size * (kSeg2Max / sh.page_size));
-  const SeqTable t2 = with_items(base, ups, sh.page_size, false, sh.W);   // one item per prefix page
+  // one item per prefix page
+  if ((st = with_items(base, ups, sh.page_size, false, sh.W, 1, s, &t2)) != KVSEL_OK) return st;
   TcArgs a;
   a.sh = sh;
   a.scores = scores;

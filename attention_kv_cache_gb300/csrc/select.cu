@@ -59,7 +59,8 @@ struct TopkArgs {
 
 template <bool SMEM>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constant__ TopkArgs a,
-                                                            const __grid_constant__ SeqTable t) {
+                                                            const __grid_constant__ SeqTable tp) {
+  const SeqTable& t = real_table(tp);
   extern __shared__ __align__(16) uint32_t keys_sm[];
   __shared__ uint32_t hist[256];
   __shared__ uint32_t hist_w[kTopkThreads / 32][256];   // one histogram per warp: no cross-warp atomics
@@ -71,6 +72,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
   const int b = row / a.rows;
   const int lg = row % a.rows;
   const SeqInfo& si = t.s[b];
+  if (si.L == 0) return;                 // a table whose device lengths failed the checks
   const int n = a.P == 1 ? si.L : (si.L + a.P - 1) / a.P;
   const int n_cand = n - a.n_recent;
   const float* src = a.scores + (a.P == 1 ? si.s_off : si.p_off) + (int64_t)lg * n;
@@ -213,7 +215,8 @@ __device__ __forceinline__ float head_value(const AggArgs& a, const SeqInfo& si,
 
 // L1 norm over the prefix of each (sequence, layer of the range, output head) row.
 __global__ void __launch_bounds__(kCombThreads) agg_norms(const __grid_constant__ AggArgs a,
-                                                          const __grid_constant__ SeqTable t) {
+                                                          const __grid_constant__ SeqTable tp) {
+  const SeqTable& t = real_table(tp);
   __shared__ float red[kCombThreads];
   const int nr = a.hi - a.lo + 1;
   const int row = blockIdx.x;                        // (b, layer - lo, oh)
@@ -235,7 +238,8 @@ __global__ void __launch_bounds__(kCombThreads) agg_norms(const __grid_constant_
 // One chunk of one output row: the aggregated value of every token of the chunk and its pooling
 // halo, then the pooled outputs of the chunk.
 __global__ void __launch_bounds__(kCombThreads) agg_pool(const __grid_constant__ AggArgs a,
-                                                         const __grid_constant__ SeqTable t) {
+                                                         const __grid_constant__ SeqTable tp) {
+  const SeqTable& t = real_table(tp);
   __shared__ float S[kCombChunk + 64];
   const int b = blockIdx.z;
   const int ol = blockIdx.y / a.n_h, oh = blockIdx.y % a.n_h;
@@ -305,9 +309,10 @@ kvsel_status launch_topk(const kvsel_desc& d, const SeqTable& t, int rows, int k
   a.P = d.page_size;
   a.n_sel = d.page_size == 1 ? k + (append_window ? d.window : 0)
                              : k + n_recent + (append_window ? d.window / d.page_size : 0);
-  int64_t nmax = 0;
+  int64_t nmax = 0;   // from the host table: the real lengths, or their bound with device lengths
   for (int b = 0; b < d.batch; ++b) {
-    const int64_t n = d.page_size == 1 ? d.prefix_lens[b] : (d.prefix_lens[b] + d.page_size - 1) / d.page_size;
+    const int64_t L = t.s[b].L;
+    const int64_t n = d.page_size == 1 ? L : (L + d.page_size - 1) / d.page_size;
     nmax = n > nmax ? n : nmax;
   }
   const int grid = d.batch * rows;
@@ -344,8 +349,8 @@ kvsel_status launch_aggregate(const kvsel_desc& d, const SeqTable& t, const floa
     agg_norms<<<d.batch * (hi - lo + 1) * a.n_h, kCombThreads, 0, s>>>(a, t);
     if ((st = launch_status()) != KVSEL_OK) return st;
   }
-  int64_t lmax = 0;
-  for (int b = 0; b < d.batch; ++b) lmax = d.prefix_lens[b] > lmax ? d.prefix_lens[b] : lmax;
+  int64_t lmax = 0;   // real lengths, or their bound with device lengths
+  for (int b = 0; b < d.batch; ++b) lmax = t.s[b].L > lmax ? t.s[b].L : lmax;
   dim3 grid((unsigned)((lmax + kCombChunk - 1) / kCombChunk), (unsigned)(a.n_l * a.n_h), d.batch);
   TraceScope ts("aggregate_pool", s);
   agg_pool<<<grid, kCombThreads, 0, s>>>(a, t);

@@ -46,6 +46,8 @@ class Desc(ctypes.Structure):
         ("page_reduce", ctypes.c_int32),
         ("pool_type", ctypes.c_int32),
         ("score_mode", ctypes.c_int32),
+        ("prefix_lens_dev", ctypes.c_void_p),
+        ("prefix_len_max", ctypes.c_int64),
     ]
 
 
@@ -71,7 +73,7 @@ def _load():
         "kvsel_topk": (I32, [D, VP, I32, I32, I32, VP, VP, SZ, VP]),
         "kvsel_compact": (I32, [D, VP, VP, VP, I32, I32, VP, VP, VP, VP]),
         "kvsel_compact_layers": (I32, [D, VP, VP, VP, I32, I32, I32, I32, I32, VP, VP, VP, VP]),
-        "kvsel_pagetable": (I32, [D, VP, I32, I32, P(I32), VP, VP, VP, SZ, VP]),
+        "kvsel_pagetable": (I32, [D, VP, I32, I32, VP, VP, VP, VP, SZ, VP]),
         "kvsel_attend_workspace_size": (I32, [D, I32, I32, I32, P(SZ)]),
         "kvsel_attend": (I32, [D, VP, I32, VP, VP, VP, VP, I32, I32, I32, VP, VP, SZ, VP]),
         "kvsel_read_device_error": (I32, [VP, VP]),
@@ -129,13 +131,21 @@ def _stream(stream) -> Optional[int]:
 
 
 def make_desc(*, n_layers: int, h_q: int, h_kv: int, head_dim: int, window: int,
-              prefix_lens: Sequence[int], group_reduce: int = REDUCE_SUM, pool_k: int = 7,
+              prefix_lens: Optional[Sequence[int]] = None, group_reduce: int = REDUCE_SUM, pool_k: int = 7,
               page_size: int = 1, page_reduce: int = REDUCE_MAX, pool_type: int = POOL_MAX,
-              score_mode: int = SCORE_SOFTMAX) -> Desc:
-    """A descriptor; it keeps its own host copy of prefix_lens alive."""
+              score_mode: int = SCORE_SOFTMAX, prefix_lens_dev=None, prefix_len_max: int = 0) -> Desc:
+    """A descriptor; it keeps its own host copy of prefix_lens (or a reference to the device tensor
+    ``prefix_lens_dev``, int64 on the GPU, with its bound ``prefix_len_max``) alive."""
+    if prefix_lens_dev is not None:
+        if prefix_lens is not None:
+            raise ValueError("give prefix_lens or prefix_lens_dev, not both")
+        d = Desc(n_layers, h_q, h_kv, head_dim, window, int(prefix_lens_dev.numel()), None, group_reduce,
+                 pool_k, page_size, page_reduce, pool_type, score_mode, _ptr(prefix_lens_dev), int(prefix_len_max))
+        d._lens = prefix_lens_dev
+        return d
     lens = (ctypes.c_int64 * len(prefix_lens))(*[int(x) for x in prefix_lens])
     d = Desc(n_layers, h_q, h_kv, head_dim, window, len(prefix_lens), lens, group_reduce, pool_k,
-             page_size, page_reduce, pool_type, score_mode)
+             page_size, page_reduce, pool_type, score_mode, None, 0)
     d._lens = lens
     return d
 
@@ -214,7 +224,11 @@ def kvsel_compact_layers(desc, k, v, idx, idx_layers: int, idx_heads: int, layer
 def kvsel_pagetable(desc, mask, n_qblk: int, n_kvblk_max: int, n_kvblk: Sequence[int], kv_indptr, kv_indices,
                     ws, ws_bytes=None, stream=None):
     nb = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
-    nk = (ctypes.c_int32 * len(n_kvblk))(*[int(x) for x in n_kvblk])
+    if hasattr(n_kvblk, "data_ptr"):            # int32 device tensor (descriptor with device lengths)
+        nk = _ptr(n_kvblk)
+    else:
+        arr = (ctypes.c_int32 * len(n_kvblk))(*[int(x) for x in n_kvblk])
+        nk = ctypes.cast(arr, ctypes.c_void_p)
     _check(_lib.kvsel_pagetable(ctypes.byref(desc), _ptr(mask), n_qblk, n_kvblk_max, nk, _ptr(kv_indptr),
                                 _ptr(kv_indices), _ptr(ws), nb, _stream(stream)), "kvsel_pagetable")
 

@@ -24,9 +24,12 @@ def keep_count(keep_rate: float, L: int) -> int:
     return int(min(L, max(0, math.floor(keep_rate * L + 0.5))))
 
 
-def desc_for(w, pool_k: Optional[int] = None, n_layers: Optional[int] = None):
+def desc_for(w, pool_k: Optional[int] = None, n_layers: Optional[int] = None, lens_dev=None, len_max: int = 0):
+    """Descriptor of workload w: its host prefix lengths, or the device tensor ``lens_dev`` with bound ``len_max``."""
     return K.make_desc(n_layers=w.n_layers if n_layers is None else n_layers, h_q=w.h_q, h_kv=w.h_kv,
-                       head_dim=w.head_dim, window=w.window, prefix_lens=w.prefix_lens,
+                       head_dim=w.head_dim, window=w.window,
+                       prefix_lens=None if lens_dev is not None else w.prefix_lens,
+                       prefix_lens_dev=lens_dev, prefix_len_max=len_max,
                        group_reduce=_REDUCE[w.group_reduce],
                        pool_k=w.pool_k if pool_k is None else pool_k, page_size=w.page_size,
                        page_reduce=K.REDUCE_MAX if w.page_reduce == "max" else K.REDUCE_SUM,
@@ -53,7 +56,10 @@ class Pipeline:
     pooled by kvsel_aggregate, and one selection per layer serves every KV head.
     """
 
-    def __init__(self, w, device="cuda", n_qblk: Optional[int] = None, n_kvblk_max: Optional[int] = None):
+    def __init__(self, w, device="cuda", n_qblk: Optional[int] = None, n_kvblk_max: Optional[int] = None,
+                 lens_dev=None, len_max: int = 0):
+        """With ``lens_dev`` (int64 device tensor of the prefix lengths) the calls read the lengths on the
+        device and every buffer is sized for the bound ``len_max``."""
         if w.claa is not None:
             raise ValueError("CLAA workloads run through ClaaPipeline")
         self.w = w
@@ -62,21 +68,23 @@ class Pipeline:
         self.all_heads = w.head_reduce == "all"
         if self.all_heads and (xl or w.page_size != 1):
             raise ValueError("all-head selection is a token-mode, per-layer path")
-        self.desc = desc_for(w)
-        self.desc_score = desc_for(w, pool_k=1) if (xl or self.all_heads) else self.desc
+        self.desc = desc_for(w, lens_dev=lens_dev, len_max=len_max)
+        self.desc_score = (desc_for(w, pool_k=1, lens_dev=lens_dev, len_max=len_max) if (xl or self.all_heads)
+                           else self.desc)
+        lens = [len_max] * w.batch if lens_dev is not None else list(w.prefix_lens)   # sizes the buffers
         ws_bytes = max(K.kvsel_workspace_size(self.desc), K.kvsel_workspace_size(self.desc_score))
         ws = torch.zeros(ws_bytes + K.WS_ALIGN, dtype=torch.uint8, device=device)
         off = (-ws.data_ptr()) % K.WS_ALIGN
         self.ws = ws[off:off + ws_bytes]
         self.ws_bytes = ws_bytes
         P = w.page_size
-        n_tok = sum(w.n_layers * w.h_kv * L for L in w.prefix_lens)
-        n_pg = sum(w.n_layers * w.h_kv * (-(-L // P)) for L in w.prefix_lens)
+        n_tok = sum(w.n_layers * w.h_kv * L for L in lens)
+        n_pg = sum(w.n_layers * w.h_kv * (-(-L // P)) for L in lens)
         f32 = dict(dtype=torch.float32, device=device)
         self.scores = torch.empty(n_tok, **f32)
         self.page_scores = torch.empty(n_pg, **f32) if P > 1 else None
-        self.combined = torch.empty(sum(w.h_kv * L for L in w.prefix_lens), **f32) if xl else None
-        self.agg = torch.empty(sum(w.n_layers * L for L in w.prefix_lens), **f32) if self.all_heads else None
+        self.combined = torch.empty(sum(w.h_kv * L for L in lens), **f32) if xl else None
+        self.agg = torch.empty(sum(w.n_layers * L for L in lens), **f32) if self.all_heads else None
         self.idx_layers = 1 if xl else w.n_layers
         self.idx_heads = 1 if self.all_heads else w.h_kv
         self.n_sel = w.n_sel()
@@ -89,7 +97,7 @@ class Pipeline:
         self.kv_indptr = self.kv_indices = None
         if w.block_union:
             self.n_qblk = n_qblk or w.q_chunk // w.block
-            self.n_kvblk_max = n_kvblk_max or max(-(-L // w.block) for L in w.prefix_lens)
+            self.n_kvblk_max = n_kvblk_max or max(-(-L // w.block) for L in lens)
             n_rows = w.batch * w.n_layers * w.h_kv
             self.kv_indptr = torch.empty(n_rows + 1, dtype=torch.int32, device=device)
             self.kv_indices = torch.empty(n_rows * self.n_kvblk_max, dtype=torch.int32, device=device)

@@ -11,8 +11,27 @@
  * Arguments are checked on the host before any launch; a rejected call
  * returns a status and launches nothing.  A launch failure returns
  * KVSEL_ERR_CUDA.  Errors that only the device can see (a bounded wait that
- * ran out, an index out of range) are recorded in an error word at the start
- * of the workspace and read back with kvsel_read_device_error().
+ * ran out, an index out of range, a device-resident length out of range) are
+ * recorded in an error word at the start of the workspace and read back with
+ * kvsel_read_device_error().
+ *
+ * Prefix lengths on the device.  A caller whose ragged lengths live in device
+ * memory (CompactAttention, 'Future directions': page-table metadata built on
+ * the kernel side, with no CPU-GPU synchronisation) sets
+ * kvsel_desc.prefix_lens_dev and prefix_len_max instead of prefix_lens.  Each
+ * call then builds its per-sequence offsets on the device (one small kernel
+ * per call, on the call's stream) and sizes its grids for prefix_len_max.
+ * What changes for the caller:
+ *   - the layouts stay packed by the real lengths, but every buffer must have
+ *     room for every sequence at prefix_len_max (the kernels' tensor maps and
+ *     grids are sized for the bound);
+ *   - every call needs a workspace, including kvsel_compact,
+ *     kvsel_compact_layers and kvsel_prefill_attention;
+ *   - checks that depend on a length (1 <= L_b <= prefix_len_max; kvsel_topk's
+ *     k <= L_b and its page rules; kvsel_pagetable's n_kvblk, then read from
+ *     device memory) run on the device: a failed check records
+ *     KVSEL_ERR_INVALID_ARG (detail: the sequence) in the error word and that
+ *     call's kernels leave their outputs unwritten.
  *
  * Layouts (bf16 = IEEE bfloat16 bit pattern in uint16 storage, row-major,
  * sequences of a batch packed one after another in batch order):
@@ -75,13 +94,18 @@ typedef struct {
   int32_t head_dim;            /* d: 64 or 128 */
   int32_t window;              /* W: 1 .. KVSEL_MAX_WINDOW; (h_q / h_kv) * W <= KVSEL_MAX_ROWS */
   int32_t batch;               /* sequences: 1 .. KVSEL_MAX_BATCH */
-  const int64_t* prefix_lens;  /* [host] [batch] prefix lengths L_b >= 1, L_b + W < 2^31 */
+  const int64_t* prefix_lens;  /* [host] [batch] prefix lengths L_b >= 1, L_b + W < 2^31; or NULL with
+                                  prefix_lens_dev */
   int32_t group_reduce;        /* KVSEL_REDUCE_SUM, _MAX or _MEAN over the query heads of a group */
   int32_t pool_k;              /* odd pool width, 1 (none) .. 63 */
   int32_t page_size;           /* P: 1 = token mode, 2 .. KVSEL_MAX_PAGE = page mode */
   int32_t page_reduce;         /* KVSEL_REDUCE_MAX or KVSEL_REDUCE_SUM over the tokens of a page */
   int32_t pool_type;           /* KVSEL_POOL_MAX (0) or KVSEL_POOL_AVG */
   int32_t score_mode;          /* KVSEL_SCORE_SOFTMAX (0) or KVSEL_SCORE_LOGITS */
+  const int64_t* prefix_lens_dev;  /* [device] [batch] prefix lengths, or NULL (prefix_lens is used);
+                                      exactly one of prefix_lens / prefix_lens_dev is set */
+  int64_t prefix_len_max;      /* with prefix_lens_dev: bound of every L_b (>= 1, + W < 2^31); sizes the
+                                  workspace, the grids and the buffers the caller provides */
 } kvsel_desc;
 
 /* Bytes of device workspace the calls below need for this descriptor (any of them). */
@@ -322,7 +346,8 @@ KVSEL_API kvsel_status kvsel_attend(const kvsel_desc* desc, const void* q, int32
  *
  *   mask        [device] uint8 [batch][n_layers][h_q][n_qblk][n_kvblk_max], nonzero = selected
  *   n_kvblk     [host] [batch] KV blocks of each sequence (<= n_kvblk_max); mask
- *               entries at j >= n_kvblk[b] are ignored
+ *               entries at j >= n_kvblk[b] are ignored.  [device] when the descriptor's
+ *               prefix lengths are on the device (prefix_lens_dev)
  *   kv_indptr   [device] int32 out [batch * n_layers * h_kv + 1]
  *   kv_indices  [device] int32 out, capacity batch * n_layers * h_kv * n_kvblk_max
  */

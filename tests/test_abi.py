@@ -126,3 +126,39 @@ def test_new_entry_arguments_rejected():
     assert cl(1, 3, 0, 2) == K.ERR_INVALID_ARG                              # idx heads neither 1 nor h_kv
     assert K.raw_call("kvsel_compact_layers", ctypes.byref(d), 16, 16, 16, 1, 1, 0, 2, 10, 8, 16, None,
                       None) == K.ERR_INVALID_ARG                            # misaligned output
+
+
+def _dev_desc(lmax, **kw):
+    """A descriptor whose lengths are 'on the device' (a fake address: nothing is dereferenced on the host)."""
+    d = _desc(**kw)
+    d.prefix_lens = None
+    d.prefix_lens_dev = 256
+    d.prefix_len_max = lmax
+    return d
+
+
+def test_device_length_descriptor_checks():
+    n = ctypes.c_size_t(0)
+    d = _dev_desc(5000)
+    assert K.raw_call("kvsel_workspace_size", ctypes.byref(d), ctypes.byref(n)) == K.OK
+    # the workspace is sized for the bound
+    assert n.value == K.kvsel_workspace_size(_desc(prefix_lens=[5000]))
+    both = _dev_desc(5000)
+    both.prefix_lens = _desc().prefix_lens
+    assert K.raw_call("kvsel_workspace_size", ctypes.byref(both), ctypes.byref(n)) == K.ERR_INVALID_ARG
+    neither = _desc()
+    neither.prefix_lens = None
+    assert K.raw_call("kvsel_workspace_size", ctypes.byref(neither), ctypes.byref(n)) == K.ERR_INVALID_ARG
+    for lmax in (0, 2 ** 31):
+        assert K.raw_call("kvsel_workspace_size", ctypes.byref(_dev_desc(lmax)), ctypes.byref(n)) == K.ERR_INVALID_ARG
+    big = 1 << 40
+    # checks against the bound still run on the host: k above it, recency beyond its pages
+    assert K.raw_call("kvsel_topk", ctypes.byref(_dev_desc(100)), 16, 2, 101, 0, 16, 256, big, None) == K.ERR_INVALID_ARG
+    assert K.raw_call("kvsel_topk", ctypes.byref(_dev_desc(100, page_size=16)), 16, 2, 7, 1, 16, 256, big,
+                      None) == K.ERR_INVALID_ARG
+    # every call needs a workspace: it holds the table built on the device
+    assert K.raw_call("kvsel_compact", ctypes.byref(_dev_desc(100)), 16, 16, 16, 1, 10, 16, 16, None,
+                      None) == K.ERR_WORKSPACE
+    # the prefill takes host lengths only
+    assert K.raw_call("kvsel_prefill_attention", ctypes.byref(_dev_desc(100)), 16, 16, 16, 16, None, 16, 16, 256,
+                      None) == K.ERR_UNSUPPORTED
