@@ -600,6 +600,81 @@ kvsel_status kvsel_pagetable(const kvsel_desc* desc, const uint8_t* mask, int32_
                           kv_indices, stream);
 }
 
+// ----------------------------------------------------------------------------- CLAA schedule
+static kvsel_status claa_check(const kvsel_desc* desc, const kvsel_claa_params* p) {
+  kvsel_status st = check_desc(desc);
+  if (st != KVSEL_OK) return st;
+  if (p == nullptr) return KVSEL_ERR_INVALID_ARG;
+  const kvsel_desc& d = *desc;
+  if (d.batch != 1 || lens_on_device(d) || d.page_size != 1) return KVSEL_ERR_UNSUPPORTED;
+  if (d.group_reduce != KVSEL_REDUCE_SUM || d.score_mode != KVSEL_SCORE_SOFTMAX) return KVSEL_ERR_INVALID_ARG;
+  if (p->defer < 0 || p->prune_layer < p->defer || p->prune_layer >= d.n_layers || p->n_buffer < 1)
+    return KVSEL_ERR_INVALID_ARG;
+  if (!(p->keep_rate >= 0.0 && p->keep_rate <= 1.0)) return KVSEL_ERR_INVALID_ARG;
+  return KVSEL_OK;
+}
+
+// The scored layers' descriptor: layers m .. l_p of the prompt, pooled or (pool_k = 1) raw.
+static kvsel_desc claa_sub(const kvsel_desc& d, const kvsel_claa_params& p, bool raw) {
+  kvsel_desc s = d;
+  s.n_layers = p.prune_layer - p.defer + 1;
+  if (raw) s.pool_k = 1;
+  return s;
+}
+
+kvsel_status kvsel_claa_shape(const kvsel_desc* desc, const kvsel_claa_params* p, kvsel_claa_shape_t* out) {
+  kvsel_status st = claa_check(desc, p);
+  if (st != KVSEL_OK) return st;
+  if (out == nullptr) return KVSEL_ERR_INVALID_ARG;
+  const int64_t L = desc->prefix_lens[0];
+  out->n_scored = p->prune_layer - p->defer + 1;
+  out->buffer_lo = std::max(p->defer, p->prune_layer - p->n_buffer + 1);
+  // keep_rate -> k: floor(r L + 1/2), clipped to [0, L]
+  const double kk = std::floor(p->keep_rate * (double)L + 0.5);
+  out->k = (int32_t)std::min<double>((double)L, std::max(0.0, kk));
+  out->n_sel = out->k + desc->window;
+  const kvsel_desc sub = claa_sub(*desc, *p, false);
+  out->ws_bytes = std::max(ws_layout(sub).total, ws_layout(*desc).total);
+  return KVSEL_OK;
+}
+
+kvsel_status kvsel_claa_select(const kvsel_desc* desc, const kvsel_claa_params* p, const void* q, const void* k,
+                               const void* v, float* scores, float* layer_scores, float* prune_scores, int32_t* idx,
+                               int32_t* prune_idx, void* k_out, void* v_out, void* ws, size_t ws_bytes,
+                               cudaStream_t stream) {
+  NvtxRange nvtx("kvsel_claa_select");
+  kvsel_claa_shape_t sh;
+  kvsel_status st = kvsel_claa_shape(desc, p, &sh);
+  if (st != KVSEL_OK) return st;
+  const kvsel_desc& d = *desc;
+  if (q == nullptr || k == nullptr || v == nullptr || scores == nullptr || layer_scores == nullptr ||
+      prune_scores == nullptr || idx == nullptr || prune_idx == nullptr || k_out == nullptr || v_out == nullptr)
+    return KVSEL_ERR_INVALID_ARG;
+  if (ws == nullptr || ((uintptr_t)ws % KVSEL_WS_ALIGN) != 0 || ws_bytes < sh.ws_bytes) return KVSEL_ERR_WORKSPACE;
+  const int64_t L = d.prefix_lens[0];
+  const kvsel_desc raw = claa_sub(d, *p, true);
+  const kvsel_desc pooled = claa_sub(d, *p, false);
+  // the scored layers are a contiguous slice of the prompt's q and K
+  const auto* qb = static_cast<const uint16_t*>(q) + (int64_t)p->defer * d.h_q * d.window * d.head_dim;
+  const auto* kb = static_cast<const uint16_t*>(k) + (int64_t)p->defer * d.h_kv * (L + d.window) * d.head_dim;
+  // decision 2: every scored layer's window score, summed over the window rows and all heads, pooled
+  if ((st = kvsel_score(&raw, qb, kb, scores, nullptr, ws, ws_bytes, stream)) != KVSEL_OK) return st;
+  if ((st = kvsel_aggregate(&pooled, scores, 0, sh.n_scored - 1, KVSEL_LAYERS_EACH, KVSEL_HEADS_SUM, layer_scores,
+                            ws, ws_bytes, stream)) != KVSEL_OK)
+    return st;
+  // each scored layer keeps topk(score, keep_rate) plus the window, and its cache is gathered to them
+  if ((st = kvsel_select(&pooled, layer_scores, sh.n_scored, sh.k, 0, 1, idx, ws, ws_bytes, stream)) != KVSEL_OK)
+    return st;
+  if ((st = kvsel_compact_layers(&d, k, v, idx, sh.n_scored, 1, p->defer, sh.n_scored, sh.n_sel, k_out, v_out, ws,
+                                 stream)) != KVSEL_OK)
+    return st;
+  // decision 3 (Eq. 6): the token-wise max over the buffer, pooled, picks the prune index at l_p
+  if ((st = kvsel_aggregate(&pooled, scores, sh.buffer_lo - p->defer, sh.n_scored - 1, KVSEL_LAYERS_MAX,
+                            KVSEL_HEADS_SUM, prune_scores, ws, ws_bytes, stream)) != KVSEL_OK)
+    return st;
+  return kvsel_select(&pooled, prune_scores, 1, sh.k, 0, 1, prune_idx, ws, ws_bytes, stream);
+}
+
 kvsel_status kvsel_read_device_error(void* ws, cudaStream_t stream) {
   if (ws == nullptr || ((uintptr_t)ws % KVSEL_WS_ALIGN) != 0) return KVSEL_ERR_WORKSPACE;
   uint32_t h[2] = {0, 0};

@@ -51,6 +51,16 @@ class Desc(ctypes.Structure):
     ]
 
 
+class ClaaParams(ctypes.Structure):
+    _fields_ = [("defer", ctypes.c_int32), ("prune_layer", ctypes.c_int32), ("n_buffer", ctypes.c_int32),
+                ("keep_rate", ctypes.c_double)]
+
+
+class ClaaShape(ctypes.Structure):
+    _fields_ = [("n_scored", ctypes.c_int32), ("buffer_lo", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("n_sel", ctypes.c_int32), ("ws_bytes", ctypes.c_size_t)]
+
+
 class TraceEntry(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int64), ("ms", ctypes.c_double)]
 
@@ -74,6 +84,8 @@ def _load():
         "kvsel_compact": (I32, [D, VP, VP, VP, I32, I32, VP, VP, VP, VP]),
         "kvsel_compact_layers": (I32, [D, VP, VP, VP, I32, I32, I32, I32, I32, VP, VP, VP, VP]),
         "kvsel_pagetable": (I32, [D, VP, I32, I32, VP, VP, VP, VP, SZ, VP]),
+        "kvsel_claa_shape": (I32, [D, P(ClaaParams), P(ClaaShape)]),
+        "kvsel_claa_select": (I32, [D, P(ClaaParams), VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
         "kvsel_attend_workspace_size": (I32, [D, I32, I32, I32, P(SZ)]),
         "kvsel_attend": (I32, [D, VP, I32, VP, VP, VP, VP, I32, I32, I32, VP, VP, SZ, VP]),
         "kvsel_read_device_error": (I32, [VP, VP]),
@@ -96,7 +108,7 @@ _lib = _load()
 EXPORTED = ("kvsel_workspace_size", "kvsel_score", "kvsel_score_noalloc", "kvsel_prefill_attention",
             "kvsel_score_from_lse", "kvsel_combine_layers",
             "kvsel_aggregate", "kvsel_select", "kvsel_topk", "kvsel_compact", "kvsel_compact_layers",
-            "kvsel_pagetable", "kvsel_attend_workspace_size", "kvsel_attend", "kvsel_read_device_error", "kvsel_noalloc_read_device_error", "kvsel_selftest_bounded_wait", "kvsel_status_string",
+            "kvsel_pagetable", "kvsel_claa_shape", "kvsel_claa_select", "kvsel_attend_workspace_size", "kvsel_attend", "kvsel_read_device_error", "kvsel_noalloc_read_device_error", "kvsel_selftest_bounded_wait", "kvsel_status_string",
             "kvsel_version", "kvsel_trace_enable", "kvsel_trace_read", "kvsel_launch_count")
 
 
@@ -231,6 +243,20 @@ def kvsel_pagetable(desc, mask, n_qblk: int, n_kvblk_max: int, n_kvblk: Sequence
         nk = ctypes.cast(arr, ctypes.c_void_p)
     _check(_lib.kvsel_pagetable(ctypes.byref(desc), _ptr(mask), n_qblk, n_kvblk_max, nk, _ptr(kv_indptr),
                                 _ptr(kv_indices), _ptr(ws), nb, _stream(stream)), "kvsel_pagetable")
+
+
+def kvsel_claa_shape(desc, params: ClaaParams) -> ClaaShape:
+    out = ClaaShape()
+    _check(_lib.kvsel_claa_shape(ctypes.byref(desc), ctypes.byref(params), ctypes.byref(out)), "kvsel_claa_shape")
+    return out
+
+
+def kvsel_claa_select(desc, params: ClaaParams, q, k, v, scores, layer_scores, prune_scores, idx, prune_idx, k_out,
+                      v_out, ws, ws_bytes=None, stream=None):
+    nb = ws_bytes if ws_bytes is not None else ws.numel() * ws.element_size()
+    _check(_lib.kvsel_claa_select(ctypes.byref(desc), ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(scores),
+                                  _ptr(layer_scores), _ptr(prune_scores), _ptr(idx), _ptr(prune_idx), _ptr(k_out),
+                                  _ptr(v_out), _ptr(ws), nb, _stream(stream)), "kvsel_claa_select")
 
 
 def kvsel_attend_workspace_size(desc, n_q: int, block: int, max_blocks: int) -> int:

@@ -9,7 +9,6 @@ only allocates device memory and orders the calls on one stream.
 
 from __future__ import annotations
 
-import math
 from typing import Optional
 
 import torch
@@ -17,11 +16,6 @@ import torch
 from . import kvsel as K
 
 _REDUCE = {"sum": K.REDUCE_SUM, "max": K.REDUCE_MAX, "mean": K.REDUCE_MEAN}
-
-
-def keep_count(keep_rate: float, L: int) -> int:
-    """Prefix tokens kept for a keep rate r (CLAA's keep_rate): floor(r * L + 1/2), clipped to [0, L]."""
-    return int(min(L, max(0, math.floor(keep_rate * L + 0.5))))
 
 
 def desc_for(w, pool_k: Optional[int] = None, n_layers: Optional[int] = None, lens_dev=None, len_max: int = 0):
@@ -166,15 +160,11 @@ class Pipeline:
 
 
 class ClaaPipeline:
-    """CLAA selection of one prompt (CLAA, 'Three design decisions' and 'Complete flow and cost').
-
-    Layers m .. l_p are scored with the observation window (softmax mass summed
-    over the window rows and every head), each layer's pooled score picks that
-    layer's kept tokens (k from the keep rate) and its cache is compacted with
-    them for every KV head; at l_p the token-wise max over the buffered layers
-    max(m, l_p - n + 1) .. l_p, pooled, picks the sequence prune index.  Layers
-    below m keep their full cache.  Layers after l_p run on the pruned prompt,
-    which the model produces; a second pipeline scores them.
+    """CLAA selection of one prompt (CLAA, 'Three design decisions' and 'Complete flow and cost'),
+    run by kvsel_claa_select: layers m .. l_p are scored with the observation window, each keeps
+    its own top-k (k from the keep rate) and its cache is compacted; at l_p the token-wise max over
+    the buffered layers picks the sequence prune index.  The schedule's sizes (scored layers, the
+    buffer, k) come from kvsel_claa_shape; this class only allocates the buffers.
     """
 
     def __init__(self, w, device="cuda"):
@@ -183,25 +173,23 @@ class ClaaPipeline:
         self.w = w
         self.device = device
         m, lp, nbuf, rate = w.claa
+        self.params = K.ClaaParams(m, lp, nbuf, rate)
+        self.desc = desc_for(w)
+        shape = K.kvsel_claa_shape(self.desc, self.params)
         self.m, self.lp = m, lp
-        self.n_sc = lp - m + 1                              # layers scored and compacted
-        self.buf_lo = max(m, lp - nbuf + 1) - m             # buffer, relative to layer m
+        self.n_sc = shape.n_scored                          # layers scored and compacted
+        self.buf_lo = shape.buffer_lo - m                   # buffer, relative to layer m
+        self.k = shape.k
+        self.n_sel = shape.n_sel
         L = w.prefix_lens[0]
-        self.k = keep_count(rate, L)
-        # the scored layers are a contiguous slice of the one prompt's q and k
-        self.desc = desc_for(w, n_layers=self.n_sc)
-        self.desc_score = desc_for(w, pool_k=1, n_layers=self.n_sc)
-        self.desc_full = desc_for(w)
-        ws_bytes = max(K.kvsel_workspace_size(self.desc), K.kvsel_workspace_size(self.desc_full))
-        ws = torch.zeros(ws_bytes + K.WS_ALIGN, dtype=torch.uint8, device=device)
+        ws = torch.zeros(shape.ws_bytes + K.WS_ALIGN, dtype=torch.uint8, device=device)
         off = (-ws.data_ptr()) % K.WS_ALIGN
-        self.ws = ws[off:off + ws_bytes]
-        self.ws_bytes = ws_bytes
+        self.ws = ws[off:off + shape.ws_bytes]
+        self.ws_bytes = shape.ws_bytes
         f32 = dict(dtype=torch.float32, device=device)
         self.scores = torch.empty((self.n_sc, w.h_kv, L), **f32)       # raw group scores
         self.layer_scores = torch.empty((self.n_sc, L), **f32)          # pooled all-head score per layer
         self.prune_scores = torch.empty((1, L), **f32)                  # pooled max over the buffer
-        self.n_sel = self.k + (w.window if w.append_window else 0)
         self.idx = torch.empty((1, self.n_sc, 1, self.n_sel), dtype=torch.int32, device=device)
         self.prune_idx = torch.empty((1, 1, self.n_sel), dtype=torch.int32, device=device)
         self.k_out = torch.empty((1, self.n_sc, w.h_kv, self.n_sel, w.head_dim), dtype=torch.bfloat16, device=device)
@@ -209,20 +197,5 @@ class ClaaPipeline:
 
     def run(self, q, k, v, stream=None):
         """q [1, n_layers, h_q, W, d]; k, v the prompt's caches (flat, layout of the library)."""
-        w = self.w
-        L = w.prefix_lens[0]
-        per_layer = w.h_kv * (L + w.window) * w.head_dim
-        q_sc = q[:, self.m:self.lp + 1].contiguous() if q.dim() == 5 else q
-        k_sc = k.reshape(-1)[self.m * per_layer:(self.lp + 1) * per_layer]
-        app = w.append_window
-        K.kvsel_score(self.desc_score, q_sc, k_sc, self.scores, None, self.ws, self.ws_bytes, stream)
-        K.kvsel_aggregate(self.desc, self.scores, 0, self.n_sc - 1, K.LAYERS_EACH, K.HEADS_SUM, self.layer_scores,
-                          self.ws, self.ws_bytes, stream)
-        K.kvsel_select(self.desc, self.layer_scores, self.n_sc, self.k, 0, app, self.idx, self.ws, self.ws_bytes,
-                       stream)
-        K.kvsel_compact_layers(self.desc_full, k, v, self.idx, self.n_sc, 1, self.m, self.n_sc, self.n_sel,
-                               self.k_out, self.v_out, self.ws, stream)
-        K.kvsel_aggregate(self.desc, self.scores, self.buf_lo, self.n_sc - 1, K.LAYERS_MAX, K.HEADS_SUM,
-                          self.prune_scores, self.ws, self.ws_bytes, stream)
-        K.kvsel_select(self.desc, self.prune_scores, 1, self.k, 0, app, self.prune_idx, self.ws, self.ws_bytes,
-                       stream)
+        K.kvsel_claa_select(self.desc, self.params, q, k, v, self.scores, self.layer_scores, self.prune_scores,
+                            self.idx, self.prune_idx, self.k_out, self.v_out, self.ws, self.ws_bytes, stream)

@@ -104,7 +104,7 @@ def _k_keep(w):
 
 
 def keep_count(rate, L):
-    from attention_kv_cache_gb300.pipeline import keep_count as kc
+    from oracle.kvsel_oracle import keep_count as kc      # the CPU leg takes k from the oracle
     return kc(rate, L)
 
 

@@ -336,6 +336,51 @@ KVSEL_API kvsel_status kvsel_attend(const kvsel_desc* desc, const void* q, int32
                                     size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * kvsel_claa_shape / kvsel_claa_select — the CLAA schedule over one prompt.
+ *
+ * CLAA, 'Three design decisions': decision 1, the first m layers (defer) keep their full cache;
+ * decision 2, every later layer up to the pruning layer l_p scores the prompt with its observation
+ * window (post-softmax probabilities summed over the window rows and all heads); decision 3 (Eq. 6),
+ * the per-layer scores of the last n layers (the rolling buffer, layers max(m, l_p - n + 1) .. l_p)
+ * are aggregated token-wise by their maximum.  'Complete flow and cost': each scored layer keeps
+ * topk(score, keep_rate) of the prefix (k = floor(r L + 1/2), clipped to [0, L]) plus the window and
+ * gathers its cache to those rows; at l_p the pooled aggregate picks the sequence prune index.
+ * Pooling is desc->pool_k / pool_type ('Experimental setup': average pooling, kernel 7).
+ *
+ * The descriptor covers every layer of the prompt (batch 1, host prefix length, token mode,
+ * group_reduce KVSEL_REDUCE_SUM, score_mode KVSEL_SCORE_SOFTMAX).  kvsel_claa_shape returns the
+ * sizes the outputs need; kvsel_claa_select runs the schedule:
+ *   q, k, v        [device] bf16, layouts above, all n_layers layers
+ *   scores         [device] fp32 out [n_scored][h_kv][L]: raw group scores of layers m .. l_p
+ *   layer_scores   [device] fp32 out [n_scored][L]: pooled all-head score of each scored layer
+ *   prune_scores   [device] fp32 out [L]: pooled token-wise max over the buffer
+ *   idx            [device] int32 out [n_scored][n_sel]: each scored layer's kept rows
+ *   prune_idx      [device] int32 out [n_sel]: the prune index
+ *   k_out, v_out   [device] bf16 out [n_scored][h_kv][n_sel][d]: compacted caches of layers m .. l_p
+ *   ws             [device] workspace of at least shape.ws_bytes
+ */
+typedef struct {
+  int32_t defer;          /* m: layers 0 .. m - 1 are neither scored nor compacted */
+  int32_t prune_layer;    /* l_p: m <= l_p < n_layers */
+  int32_t n_buffer;       /* n >= 1: layers in the rolling buffer */
+  double keep_rate;       /* r in [0, 1]: fraction of the prefix kept */
+} kvsel_claa_params;
+
+typedef struct {
+  int32_t n_scored;       /* l_p - m + 1 */
+  int32_t buffer_lo;      /* first buffered layer, max(m, l_p - n + 1); the last is l_p */
+  int32_t k;              /* prefix tokens kept per selection */
+  int32_t n_sel;          /* entries per selection: k + W */
+  size_t ws_bytes;        /* workspace kvsel_claa_select needs */
+} kvsel_claa_shape_t;
+
+KVSEL_API kvsel_status kvsel_claa_shape(const kvsel_desc* desc, const kvsel_claa_params* p, kvsel_claa_shape_t* out);
+KVSEL_API kvsel_status kvsel_claa_select(const kvsel_desc* desc, const kvsel_claa_params* p, const void* q,
+                                         const void* k, const void* v, float* scores, float* layer_scores,
+                                         float* prune_scores, int32_t* idx, int32_t* prune_idx, void* k_out,
+                                         void* v_out, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * kvsel_pagetable — per-group KV block table from a 2-D block mask.
  *
  * CompactAttention: Accelerating Chunked Prefill with Block-Union KV

@@ -162,3 +162,29 @@ def test_device_length_descriptor_checks():
     # the prefill takes host lengths only
     assert K.raw_call("kvsel_prefill_attention", ctypes.byref(_dev_desc(100)), 16, 16, 16, 16, None, 16, 16, 256,
                       None) == K.ERR_UNSUPPORTED
+
+
+def test_claa_shape_matches_the_oracle_schedule():
+    """kvsel_claa_shape's keep count and buffer follow CLAA's schedule as the oracle writes it (host only)."""
+    from oracle import kvsel_oracle as O
+    for rate, L in ((0.2, 32768), (0.1, 30), (0.25, 10), (0.15, 10), (1.0, 7), (0.0, 5), (0.5, 1), (0.4, 3),
+                    (0.1, 32768), (0.33, 1001)):
+        d = _desc(n_layers=16, h_q=32, h_kv=8, window=8, prefix_lens=[L], pool_k=7, pool_type=K.POOL_AVG)
+        for m, lp, n in ((4, 15, 4), (2, 6, 3), (3, 4, 4), (0, 0, 1)):
+            sh = K.kvsel_claa_shape(d, K.ClaaParams(m, lp, n, rate))
+            assert sh.k == O.keep_count(rate, L), (rate, L, sh.k)
+            assert sh.n_sel == sh.k + 8
+            assert sh.n_scored == lp - m + 1
+            assert sh.buffer_lo == max(m, lp - n + 1)
+            assert sh.ws_bytes >= K.kvsel_workspace_size(d)
+    d = _desc(n_layers=16, prefix_lens=[100])
+    bad = [K.ClaaParams(5, 4, 4, 0.2), K.ClaaParams(4, 16, 4, 0.2), K.ClaaParams(4, 15, 0, 0.2),
+           K.ClaaParams(4, 15, 4, 1.5), K.ClaaParams(-1, 15, 4, 0.2)]
+    out = K.ClaaShape()
+    for p in bad:
+        assert K.raw_call("kvsel_claa_shape", ctypes.byref(d), ctypes.byref(p), ctypes.byref(out)) == K.ERR_INVALID_ARG
+    p = K.ClaaParams(4, 15, 4, 0.2)
+    assert K.raw_call("kvsel_claa_shape", ctypes.byref(_desc(n_layers=16, prefix_lens=[100, 200])), ctypes.byref(p),
+                      ctypes.byref(out)) == K.ERR_UNSUPPORTED
+    assert K.raw_call("kvsel_claa_shape", ctypes.byref(_desc(n_layers=16, prefix_lens=[100], group_reduce=K.REDUCE_MAX)),
+                      ctypes.byref(p), ctypes.byref(out)) == K.ERR_INVALID_ARG
