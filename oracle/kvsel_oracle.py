@@ -339,6 +339,28 @@ def prefill_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray):
     return o, lse
 
 
+def prefill_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, rows):
+    """prefill_attention restricted to the listed rows, for prompts whose full N x N logits do not fit:
+    o [H_q, len(rows), d] and lse [H_q, len(rows)], row i attending to keys t <= i.  q [H_q, N, d],
+    k / v [H_kv, N, d] (any dtype)."""
+    Hq, d = q.shape[0], q.shape[-1]
+    G = Hq // k.shape[0]
+    rows = [int(i) for i in rows]
+    o = np.zeros((Hq, len(rows), d))
+    lse = np.zeros((Hq, len(rows)))
+    for h in range(Hq):
+        kh, vh = _f64(k[h // G]), _f64(v[h // G])
+        qh = _f64(q[h])
+        for n, i in enumerate(rows):
+            z = window_logits(qh[i:i + 1], kh[:i + 1])[0]
+            m = z.max()
+            e = np.exp(z - m)
+            ssum = e.sum()
+            o[h, n] = (e / ssum) @ vh[:i + 1]
+            lse[h, n] = m + np.log(ssum)
+    return o, lse
+
+
 # --------------------------------------------------------------------------- block union
 
 def block_union(mask: np.ndarray, h_kv: int, n_kv: int):

@@ -460,6 +460,11 @@ def check_prefill_attention_sdpa(o):
         z = (q[h] @ k[h // G].T) / np.sqrt(d)
         for i in range(N):
             np.testing.assert_allclose(np.exp(z[i, :i + 1] - lse[h, i]).sum(), 1.0, rtol=1e-13)
+    # any subset of rows, computed alone, equals those rows of the whole prompt (and SDPA's causal output)
+    rows = [0, 1, 7, 13, N - 1]
+    o_r, l_r = o.prefill_rows(q, k, v, rows)
+    np.testing.assert_allclose(o_r, ref[:, rows], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(l_r, lse[:, rows], rtol=1e-13, atol=1e-13)
     # the last W rows are the observation window: their probabilities are the window softmax
     W = 5
     L = N - W

@@ -187,3 +187,26 @@ def test_attend_offset_moves(n_q, cuda):
     assert K.kvsel_read_device_error(ws) == K.OK
     want = _ref(w, qd[0], kk[None, None], vv[None, None], [[np.arange(nb)]], P, n_q)
     _close(o[0], want, f"climbing logits R={h_q * n_q}")
+
+
+def test_attend_full_size_page_table_128k(cuda):
+    """One layer of the 128K paged workload at full length: the selection's 134 pages per (KV head) row
+    (128 chosen + 4 recent + 2 window pages of 16 rows) attended in place, against the oracle."""
+    from attention_kv_cache_gb300 import kvsel as K
+    from attention_kv_cache_gb300.pipeline import Pipeline, pack
+    w = S.scaled(S.LLAMA8B_128K_PAGED, n_layers=1)
+    inp = S.make_inputs(w, "cpu")
+    q, k, v = pack(inp, cuda)
+    pipe = Pipeline(w, cuda)
+    pipe.run(q, k, v)
+    n_q = 1
+    qd = S.make_decode_queries(w, n_q, "cpu")
+    o = torch.empty((1, w.n_layers, w.h_q, n_q, w.head_dim), dtype=torch.float32, device=cuda)
+    n_sel, P = pipe.n_sel, w.page_size
+    assert n_sel == 134
+    ws = _ws(K, K.kvsel_attend_workspace_size(pipe.desc, n_q, P, n_sel), cuda)
+    K.kvsel_attend(pipe.desc, qd.to(cuda), n_q, k, v, None, pipe.idx, n_sel, P, n_sel, o, ws)
+    torch.cuda.synchronize()
+    assert K.kvsel_read_device_error(ws) == K.OK
+    idx = pipe.idx[0].cpu().numpy()
+    _close(o[0], _ref(w, qd[0], inp.k[0], inp.v[0], idx, P, n_q), "128K page table in place")

@@ -127,3 +127,34 @@ def test_scores_from_prefill_lse(cuda):
     assert_scores_close(pages.view(w.n_layers, w.h_kv, -1), ref["pages"], "pages from the prefill lse")
     assert_scores_close(scores.view(w.n_layers, w.h_kv, L), s2.view(w.n_layers, w.h_kv, L).double().cpu().numpy(),
                         "one pass against two passes")
+
+
+def test_prefill_full_length_32k(cuda):
+    """One layer of a 32K-token prompt (32768 prefix + 32 window rows: 257 query tiles, a partial last
+    one, heaviest tile pairs first): o of sampled rows (the first tile, a middle tile, the last 160
+    rows) and the lse of every window row against the oracle restricted to those rows; then the window
+    scores from that lse against the oracle's scores of the same prompt."""
+    from attention_kv_cache_gb300 import kvsel as K
+    w = S.Workload("pf_32k", 114, 1, 2, 1, 128, 32, (32768,), group_reduce="sum", pool_k=7, k_keep=1024,
+                   n_clusters=8)
+    inp, qf, k, v, o, lse, lse_win, q_win, desc, ws = _run_prefill(w, cuda)
+    N = w.prefix_lens[0] + w.window
+    L, W, G = w.prefix_lens[0], w.window, w.group
+    rows = list(range(0, 128)) + list(range(16384, 16512)) + list(range(N - 160, N))
+    ob = o.view(w.h_q, N, w.head_dim)[:, rows].double().cpu().numpy()
+    lb = lse.view(w.h_q, N)[:, rows].double().cpu().numpy()
+    vv = O._f64(inp.v[0][0])
+    ref_o, ref_l = O.prefill_rows(qf[0][0], inp.k[0][0], inp.v[0][0], rows)
+    bound = 2.0 ** -9 * np.abs(vv).max() + 2.0 ** -8 * np.abs(ref_o) + 1e-5
+    bad = np.abs(ob - ref_o) > bound
+    assert not bad.any(), f"o: {bad.sum()} off, first {np.argwhere(bad)[0]}"
+    np.testing.assert_allclose(lb, ref_l, rtol=0, atol=1e-4, err_msg="lse of the sampled rows")
+    want_win = (ref_l[:, -W:] / np.log(2.0)).reshape(w.h_kv, G * W)
+    np.testing.assert_allclose(lse_win[0, 0].double().cpu().numpy(), want_win, rtol=0, atol=2e-4)
+    assert torch.equal(q_win[0, 0].cpu(), qf[0][0][:, L:])
+    scores = torch.empty(w.n_layers * w.h_kv * L, dtype=torch.float32, device=cuda)
+    K.kvsel_score_from_lse(desc, q_win, k, lse_win, scores, None, ws)
+    torch.cuda.synchronize()
+    assert K.kvsel_read_device_error(ws) == K.OK
+    ref = O.run_sequence(w, inp.q[0], inp.k[0], with_gather=False)
+    assert_scores_close(scores.view(w.n_layers, w.h_kv, L), ref["pooled"], "32K scores from the prefill lse")

@@ -227,6 +227,16 @@ def _prefill_not_causal(o):
     o.prefill_attention = prefill_attention
 
 
+def _prefill_rows_sees_own_key_late(o):
+    """Row i attends to keys t < i (its own key left out)."""
+    orig = o.prefill_rows
+
+    def prefill_rows(q, k, v, rows):
+        out, lse = orig(q, k, v, [max(0, int(i) - 1) for i in rows])
+        return out, lse
+    o.prefill_rows = prefill_rows
+
+
 def _rewrite_run_sequence(*edits):
     """A mutant that re-defines run_sequence from its own source with text edits (each must match once)."""
     def mutate(o):
@@ -290,7 +300,7 @@ MUTANTS = [_no_scale, _mask_off_by_one, _prefix_only_softmax, _mass_max_over_row
            _keep_count_floor, _claa_buffer_short, _attend_no_scale, _table_rows_off_by_one,
            _prefill_not_causal, _page_max_of_raw_scores, _pool_after_page_max, _pool_before_l1_mean,
            _run_layer_range_exclusive, _mean_over_every_layer, _window_always_appended, _head_sum_after_pool,
-           _gather_first_layer_index, _pool_kind_ignored]
+           _gather_first_layer_index, _pool_kind_ignored, _prefill_rows_sees_own_key_late]
 
 
 @pytest.mark.parametrize("mutate", MUTANTS, ids=lambda m: m.__name__.strip("_"))
