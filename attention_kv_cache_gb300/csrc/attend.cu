@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kAttThreads) attend_split(const __grid_constan
   const int per_seq = a.n_layers * a.h_kv;
   const int b = r / per_seq, lg = r % per_seq;
   const int layer = lg / a.h_kv, g = lg % a.h_kv;
-  const SeqInfo& si = t.s[b];
+  const SeqInfo si = t.s[b];   // a copy: loads once, whatever the table lives in
   int beg, end;
   row_list(a, si, r, beg, end);
   const int nb = end - beg;
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) attend_warp(const __grid_co
   const int per_seq = a.n_layers * a.h_kv;
   const int b = r / per_seq, lg = r % per_seq;
   const int layer = lg / a.h_kv, g = lg % a.h_kv;
-  const SeqInfo& si = t.s[b];
+  const SeqInfo si = t.s[b];   // a copy: loads once, whatever the table lives in
   // A fragments of query row gq (zero for gq >= R): elements 16c + 2tq, +1 and 16c + 8 + 2tq, +1
   uint32_t qa[D / 16][2];
   {

@@ -33,7 +33,7 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const __grid_c
   const int rem = unit % per_seq;
   const int lo = rem / a.h_kv, g = rem % a.h_kv;
   const int layer = a.layer_lo + lo;
-  const SeqInfo& si = t.s[b];
+  const SeqInfo si = t.s[b];   // a copy: loads once, whatever the table lives in
   if (si.n_keys == 0) return;            // a table whose device lengths failed the checks
   const int il = a.idx_layers == 1 ? 0 : lo;
   const int ih = a.idx_heads == 1 ? 0 : g;

@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   const int layer = (hrem / a.h_q) % a.n_layers;
   const int h = hrem % a.h_q;
   const int g = h / a.G;
-  const SeqInfo& si = t.s[b];
+  const SeqInfo si = t.s[b];   // a copy: loads once, whatever the table lives in
   const int N = si.n_keys;
   const int qa = 2 * pair;
   if (qa * kPfTile >= N) return;                                       // this sequence is shorter

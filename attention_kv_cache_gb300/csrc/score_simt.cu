@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kThreads) score_pass1_simt(const __grid_consta
   const int item = blockIdx.x;
   if (item >= t.n_items) return;         // the grid is sized for bound lengths
   const int b = find_seq(t, item);
-  const SeqInfo& si = t.s[b];
+  const SeqInfo si = t.s[b];   // a copy: loads once, whatever the table lives in
   const int local = item - si.item0;
   const int ul = local / si.n_seg, seg = local % si.n_seg;
   const int layer = ul / sh.h_kv, g = ul % sh.h_kv;
@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kThreads) score_lse_combine(const __grid_const
   const int64_t ups = (int64_t)sh.n_layers * sh.h_kv;
   const int b = (int)(u / ups);
   const int ul = (int)(u % ups);
-  const SeqInfo& si = t.s[b];
+  const SeqInfo si = t.s[b];   // a copy: loads once, whatever the table lives in
   const int64_t first = si.item0 + (int64_t)ul * si.n_seg;
   float M = -INFINITY;
   for (int sg = 0; sg < si.n_seg; ++sg) M = fmaxf(M, a.part[(first + sg) * sh.R + r].x);
@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(kThreads) score_pass2_simt(const __grid_consta
   const int item = blockIdx.x;
   if (item >= t.n_items) return;         // the grid is sized for bound lengths
   const int b = find_seq(t, item);
-  const SeqInfo& si = t.s[b];
+  const SeqInfo si = t.s[b];   // a copy: loads once, whatever the table lives in
   const int local = item - si.item0;
   const int ul = local / si.n_seg, seg = local % si.n_seg;
   const int layer = ul / sh.h_kv, g = ul % sh.h_kv;

@@ -100,7 +100,7 @@ struct Item {
 
 // Unit ul of sequence b: the fields every item of it shares.
 __device__ __forceinline__ void unit_fields(const SeqTable& t, const ScoreShape& sh, int b, int ul, Item& it) {
-  const SeqInfo& si = t.s[b];
+  const SeqInfo si = t.s[b];   // a copy: loads once, whatever the table lives in
   it.b = b;
   it.ul = ul;
   it.layer = ul / sh.h_kv;
@@ -125,7 +125,7 @@ struct Work {
   __device__ __forceinline__ bool next(const SeqTable& t, const ScoreShape& sh, Item& it) {
     if (pos >= end) return false;
     const int b = find_seq(t, pos);
-    const SeqInfo& si = t.s[b];
+    const SeqInfo si = t.s[b];   // a copy: loads once, whatever the table lives in
     const int local = pos - si.item0;
     if (!PASS2) {
       unit_fields(t, sh, b, local / si.n_seg, it);
@@ -753,7 +753,7 @@ __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base
     epi_sync<P::kEW>();
     if (aborted(flag)) continue;
     // max-pool over prefix positions, then page reduce (DELTA key designs 2-3)
-    const SeqInfo& si = t.s[it.b];
+    const SeqInfo si = t.s[it.b];   // a copy: loads once, whatever the table lives in
     float* out = a.scores + si.s_off + ((int64_t)it.layer * a.sh.h_kv + it.g) * it.L;
     float* pout = nullptr;
     if (P_ > 1) {
@@ -837,7 +837,7 @@ __device__ void epilogue_pass2_pairs(const TcArgs& a, const SeqTable& t, uint32_
     }
     epi_sync<P::kEW>();
     if (aborted(flag)) continue;
-    const SeqInfo& si = t.s[it.b];
+    const SeqInfo si = t.s[it.b];   // a copy: loads once, whatever the table lives in
     float* out = a.scores + si.s_off + ((int64_t)it.layer * a.sh.h_kv + it.g) * it.L;
     float* pout = nullptr;
     if (P_ > 1) {

@@ -2,12 +2,17 @@
 // aggregation of group scores across KV heads and layers (L1-normalised mean or max), pooled.
 //
 // Top-k: one CTA per (sequence, layer, KV head) row.  Scores map to order-
-// preserving uint32 keys; a 4-pass 8-bit radix select finds the k-th largest
-// key T and how many keys equal to T are taken (krem).  Then one ordered pass
-// emits every index with key > T and the first krem indices with key == T, in
-// ascending index order, which is exactly the first k of the ranking by
-// (score descending, index ascending) sorted back into position order
-// (DELTA, 'Key designs' 2; ClusterAttn, 'Method details').
+// preserving uint32 keys.  The k-th largest key T and how many keys equal to T
+// are taken (krem) come from a 4-pass 8-bit radix select: over a short list of
+// candidates when a sample of the row brackets the k-th key (every key at or
+// above a threshold read off a 1024-key sample, some 1.25 k of them), over the
+// whole row otherwise.  Then one ordered pass emits every index with key > T
+// and the first krem indices with key == T, in ascending index order, which is
+// exactly the first k of the ranking by (score descending, index ascending)
+// sorted back into position order (DELTA, 'Key designs' 2; ClusterAttn,
+// 'Method details').
+#include <algorithm>
+
 #include "internal.cuh"
 
 namespace kvsel {
@@ -55,23 +60,95 @@ struct TopkArgs {
   const float* scores;
   int32_t* idx;
   int32_t rows, k, n_recent, P, n_sel;
+  int32_t stage;    // keys staged in shared memory ahead of the candidate list (0: rows read from global)
+  int32_t cap;      // candidate list capacity (>= kSample), 0: no candidate path
 };
+
+constexpr int kSample = 1024;
+
+struct TopkShared {
+  uint32_t hist[256];
+  uint32_t hist_w[kTopkThreads / 32][256];   // one histogram per warp: no cross-warp atomics
+  unsigned long long scan_sh[32];
+  uint2 warp_cnt[kTopkThreads / 32];
+  uint32_t sel_digit, sel_gt, n_found;
+};
+
+// The k-th largest of arr[0, n) (1 <= k <= n, a short list in shared memory): *T and how many keys
+// equal to *T the top k take (*krem).  Four 8-bit passes from the top digit; each keeps the keys that
+// match the digits chosen so far, counts their next digit (one shared histogram, one atomic per group
+// of lanes with equal digits) and chooses the digit the k-th key has.
+__device__ void select_short(const uint32_t* arr, int n, uint32_t k, TopkShared& sh, uint32_t* T, uint32_t* krem) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  uint32_t prefix = 0, pmask = 0, rem = k;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    if (tid < 256) sh.hist[tid] = 0;
+    __syncthreads();
+    for (int base = 0; base < n; base += kTopkThreads) {
+      const int i = base + tid;
+      uint32_t key = 0;
+      bool ok = false;
+      if (i < n) {
+        key = arr[i];
+        ok = (key & pmask) == prefix;
+      }
+      const unsigned m = __ballot_sync(0xffffffffu, ok);
+      if (ok) {
+        const uint32_t digit = (key >> shift) & 255u;
+        const unsigned peers = __match_any_sync(m, digit);
+        if (lane == __ffs(peers) - 1) atomicAdd(&sh.hist[digit], (uint32_t)__popc(peers));
+      }
+    }
+    __syncthreads();
+    if (tid < 32) {   // one warp: lane l holds digits 255 - 8l .. 248 - 8l, scanned from the top
+      uint32_t c[8], s = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = sh.hist[255 - 8 * lane - j];
+        s += c[j];
+      }
+      uint32_t incl = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      uint32_t above = incl - s;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (above < rem && rem <= above + c[j]) {
+          sh.sel_digit = 255u - 8u * lane - j;
+          sh.sel_gt = above;
+        }
+        above += c[j];
+      }
+    }
+    __syncthreads();
+    prefix |= sh.sel_digit << shift;
+    pmask |= 255u << shift;
+    rem -= sh.sel_gt;
+  }
+  *T = prefix;
+  *krem = rem;
+}
 
 template <bool SMEM>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constant__ TopkArgs a,
                                                             const __grid_constant__ SeqTable tp) {
   const SeqTable& t = real_table(tp);
-  extern __shared__ __align__(16) uint32_t keys_sm[];
-  __shared__ uint32_t hist[256];
-  __shared__ uint32_t hist_w[kTopkThreads / 32][256];   // one histogram per warp: no cross-warp atomics
-  __shared__ unsigned long long scan_sh[32];
-  __shared__ uint2 warp_cnt[kTopkThreads / 32];
-  __shared__ uint32_t sel_digit, sel_gt;
+  extern __shared__ __align__(16) uint32_t keys_sm[];   // [stage] staged keys, then [cap] candidates
+  __shared__ TopkShared sh;
+  uint32_t* hist = sh.hist;
+  auto& hist_w = sh.hist_w;
+  unsigned long long* scan_sh = sh.scan_sh;
+  uint2* warp_cnt = sh.warp_cnt;
+  uint32_t* cand = keys_sm + a.stage;
 
   const int row = blockIdx.x;
   const int b = row / a.rows;
   const int lg = row % a.rows;
-  const SeqInfo& si = t.s[b];
+  const SeqInfo si = t.s[b];   // a copy: loads once, whatever the table lives in
   if (si.L == 0) return;                 // a table whose device lengths failed the checks
   const int n = a.P == 1 ? si.L : (si.L + a.P - 1) / a.P;
   const int n_cand = n - a.n_recent;
@@ -101,8 +178,46 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
 
   uint32_t prefix = 0, pmask = 0;
   uint32_t krem = (uint32_t)a.k;
+  bool have = false;   // T (prefix) and krem found from the candidate list
+  if (a.k > 0 && a.cap >= kSample && n_cand >= 12 * kSample) {   // shorter rows: the whole-row passes are cheaper
+    // A threshold read off an evenly spaced sample: about k * S / n_cand sample keys lie at or above the
+    // row's k-th key; the sample's r0-th largest key, r0 1.25 times that plus three standard deviations,
+    // leaves some 1.25 k keys of the row at or above it, the k-th among them.
+    const float e = (float)a.k * (float)kSample / (float)n_cand;
+    const int r0 = (int)(1.25f * e + 3.0f * sqrtf(e) + 4.0f);
+    if (r0 <= kSample) {
+      for (int s = tid; s < kSample; s += kTopkThreads) cand[s] = key_at((int)(((int64_t)s * n_cand) / kSample));
+      __syncthreads();
+      uint32_t T0, rem0;
+      select_short(cand, kSample, (uint32_t)r0, sh, &T0, &rem0);
+      if (tid == 0) sh.n_found = 0;
+      __syncthreads();
+      // every key >= T0 into the list (positions taken a warp at a time); keys past the capacity are
+      // counted but not stored, and the list is then not used
+      const int lane = tid & 31;
+      const unsigned lower = (1u << lane) - 1u;
+#pragma unroll 4
+      for (int base = 0; base < n_cand; base += kTopkThreads) {
+        const int i = base + tid;
+        const uint32_t key = i < n_cand ? key_at(i) : 0u;
+        const bool p = i < n_cand && key >= T0;
+        const unsigned m = __ballot_sync(0xffffffffu, p);
+        uint32_t wbase = 0;
+        if (lane == 0 && m != 0u) wbase = atomicAdd(&sh.n_found, (uint32_t)__popc(m));
+        wbase = __shfl_sync(0xffffffffu, wbase, 0);
+        const uint32_t pos = wbase + (uint32_t)__popc(m & lower);
+        if (p && pos < (uint32_t)a.cap) cand[pos] = key;
+      }
+      __syncthreads();
+      const uint32_t nf = sh.n_found;
+      if (nf >= (uint32_t)a.k && nf <= (uint32_t)a.cap) {   // the row's k-th key is among them
+        select_short(cand, (int)nf, (uint32_t)a.k, sh, &prefix, &krem);
+        have = true;
+      }
+    }
+  }
   if (a.k > 0) {
-    for (int pass = 0; pass < 4; ++pass) {
+    for (int pass = 0; !have && pass < 4; ++pass) {
       const int shift = 24 - 8 * pass;
       uint32_t* hw = hist_w[tid >> 5];
       for (int j = tid & 31; j < 256; j += 32) hw[j] = 0;
@@ -137,13 +252,13 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
       unsigned long long tot;
       const unsigned long long above = block_scan_u64(c, scan_sh, &tot);
       if (tid < 256 && above < krem && krem <= above + c) {
-        sel_digit = d;
-        sel_gt = (uint32_t)above;
+        sh.sel_digit = d;
+        sh.sel_gt = (uint32_t)above;
       }
       __syncthreads();
-      prefix |= sel_digit << shift;
+      prefix |= sh.sel_digit << shift;
       pmask |= 255u << shift;
-      krem -= sel_gt;
+      krem -= sh.sel_gt;
       __syncthreads();
     }
     // ordered emission: every key > T and the first krem keys == T, in index order.  A selected key's
@@ -223,7 +338,7 @@ __global__ void __launch_bounds__(kCombThreads) agg_norms(const __grid_constant_
   const int b = row / (nr * a.n_h);
   const int rem = row % (nr * a.n_h);
   const int layer = a.lo + rem / a.n_h, oh = rem % a.n_h;
-  const SeqInfo& si = t.s[b];
+  const SeqInfo si = t.s[b];   // a copy: loads once, whatever the table lives in
   float acc = 0.f;
   for (int i = threadIdx.x; i < si.L; i += kCombThreads) acc += fabsf(head_value(a, si, layer, oh, i));
   red[threadIdx.x] = acc;
@@ -243,7 +358,7 @@ __global__ void __launch_bounds__(kCombThreads) agg_pool(const __grid_constant__
   __shared__ float S[kCombChunk + 64];
   const int b = blockIdx.z;
   const int ol = blockIdx.y / a.n_h, oh = blockIdx.y % a.n_h;
-  const SeqInfo& si = t.s[b];
+  const SeqInfo si = t.s[b];   // a copy: loads once, whatever the table lives in
   const int a0 = blockIdx.x * kCombChunk;
   if (a0 >= si.L) return;
   const int a1 = min(si.L, a0 + kCombChunk);
@@ -315,14 +430,26 @@ kvsel_status launch_topk(const kvsel_desc& d, const SeqTable& t, int rows, int k
     const int64_t n = d.page_size == 1 ? L : (L + d.page_size - 1) / d.page_size;
     nmax = n > nmax ? n : nmax;
   }
+  int dev = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return KVSEL_ERR_CUDA;
+  const bool staged = nmax <= kSmemKeysMax;
+  a.stage = staged ? (int32_t)nmax : 0;
+  // candidate list: room for 4 k + 2048 keys (the sample's threshold keeps ~1.25 k) within what shared
+  // memory has left beside the staged row and the kernel's own arrays
+  const int64_t avail = ((int64_t)optin - (int64_t)sizeof(TopkShared) - 256) / 4 - a.stage;
+  const int64_t cap = std::min<int64_t>(std::max<int64_t>(kSample, 4 * (int64_t)k + 2048), avail);
+  a.cap = cap >= kSample ? (int32_t)cap : 0;
+  const size_t smem = (size_t)(a.stage + a.cap) * sizeof(uint32_t);
   const int grid = d.batch * rows;
   TraceScope ts("topk_radix", s);
-  if (nmax <= kSmemKeysMax) {
-    const size_t smem = (size_t)nmax * sizeof(uint32_t);
+  if (staged) {
     if (set_smem((const void*)topk_kernel<true>, smem) != cudaSuccess) return KVSEL_ERR_CUDA;
     topk_kernel<true><<<grid, kTopkThreads, smem, s>>>(a, t);
   } else {
-    topk_kernel<false><<<grid, kTopkThreads, 0, s>>>(a, t);
+    if (set_smem((const void*)topk_kernel<false>, smem) != cudaSuccess) return KVSEL_ERR_CUDA;
+    topk_kernel<false><<<grid, kTopkThreads, smem, s>>>(a, t);
   }
   return launch_status();
 }

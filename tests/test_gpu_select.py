@@ -143,3 +143,30 @@ def test_topk_first_call_in_fresh_process(cuda):
         "print('ok')\n" % root)
     out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
     assert out.returncode == 0 and out.stdout.strip().endswith("ok"), out.stderr[-2000:]
+
+
+@pytest.mark.parametrize("pattern", ["smooth", "top_on_sample_grid", "top_off_sample_grid", "ties_at_threshold",
+                                     "long_row_global"])
+def test_topk_candidate_path_exact(pattern, cuda):
+    """Rows long enough for the sampled threshold: the candidate list (smooth scores; the top keys
+    never sampled; ties around the k-th key) and the fall-back to the whole-row select (the top keys
+    all on the sample's positions, so the threshold keeps fewer than k keys), bit-exact."""
+    from attention_kv_cache_gb300 import kvsel as K
+    rows, W = 3, 4
+    n, k = (65536, 4096) if pattern == "long_row_global" else (32768, 1024)
+    g = torch.Generator().manual_seed(77 + len(pattern))
+    s = torch.rand((rows, n), generator=g, dtype=torch.float64) ** 8
+    stride = n // 1024                                   # the sample's positions are multiples of n / 1024
+    if pattern == "top_on_sample_grid":
+        s[:, ::stride] += 10.0
+    elif pattern == "top_off_sample_grid":
+        s[:, 1::stride] += 10.0
+    elif pattern == "ties_at_threshold":
+        s = torch.round(s * 512) / 512
+    s = s.float()
+    desc = K.make_desc(n_layers=rows, h_q=1, h_kv=1, head_dim=128, window=W, prefix_lens=[n])
+    idx = torch.full((rows, k + W), -7, dtype=torch.int32, device=cuda)
+    K.kvsel_topk(desc, s.to(cuda), rows, k, 0, idx, _ws(K, desc, cuda))
+    got = idx.cpu().numpy()
+    for r in range(rows):
+        np.testing.assert_array_equal(got[r], O.select_tokens(s[r].double().numpy(), k, n, W), err_msg=f"row {r}")
