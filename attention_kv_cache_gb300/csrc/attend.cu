@@ -10,9 +10,12 @@
 // Split-K: the blocks of a row are divided among S CTAs; each CTA walks its blocks in chunks of up to
 // 128 cache rows staged in shared memory, keeps an online (max, sum) and the weighted V sum per query
 // row, and writes a partial; attend_combine merges the S partials of each query row.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "internal.cuh"
+#include "sm100.cuh"
 
 namespace kvsel {
 namespace {
@@ -460,6 +463,263 @@ __global__ void __launch_bounds__(32 * kWarpsPerCta) attend_warp(const __grid_co
 
 size_t attend_warp_smem(int d) { return (size_t)kWarpsPerCta * 2 * kStages * kStep * d * 2; }
 
+// ---------------------------------------------------------------- the same warp kernel, stages by TMA
+// When the 16 rows of every step are consecutive cache rows (whole caches, or blocks of a multiple of
+// 16 rows), each step's K and V rows are one 16-row box of a 2-D tensor map over the cache ([rows][d],
+// 64-column boxes with the 128-byte swizzle): one lane issues the step's box loads, which complete on
+// the stage's mbarrier, instead of 32 lanes issuing 16-byte copies, and the block ids are loaded a
+// step before their loads are issued.  The arithmetic is the warp kernel's (two accumulation chains
+// per logit tile); K and V are addressed in the swizzled layout (16-byte chunk c of row x of a
+// 64-column half at (c ^ (x & 7)) * 16).
+constexpr uint32_t kHalfBytes = kStep * 128;   // one 64-column half of a stage's 16 rows
+constexpr int kTmaStages = 3;   // stages per warp: two steps in flight
+constexpr int kTmaWarps = 4;    // warps per CTA (two CTAs of 4 x 24 KB per SM at d = 128)
+
+template <int D>
+__host__ __device__ constexpr uint32_t tma_stage_bytes() { return (uint32_t)(D / 64) * kHalfBytes; }   // K (or V) of one stage
+
+size_t attend_tma_smem(int d) {
+  const size_t stages = (size_t)kTmaWarps * 2 * kTmaStages * (d / 64) * kHalfBytes;
+  return 1024 + stages + (size_t)kTmaWarps * kTmaStages * 12;   // slack, stages, mbarriers and step rows
+}
+
+template <int D>
+__global__ void __launch_bounds__(32 * kTmaWarps) attend_tma(const __grid_constant__ CUtensorMap tmk,
+                                                                const __grid_constant__ CUtensorMap tmv,
+                                                                const __grid_constant__ AttArgs a,
+                                                                const __grid_constant__ SeqTable tp) {
+  const SeqTable& t = real_table(tp);
+  constexpr int NT = D / 8;
+  constexpr uint32_t KV = tma_stage_bytes<D>();
+  constexpr int NS = kTmaStages;
+  constexpr uint32_t WARP_BYTES = 2 * NS * KV;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sbase = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+  const uint32_t st0 = sm100::smem_addr(sbase) + warp * WARP_BYTES;          // K stages, then V stages
+  const uint32_t bar0 = sm100::smem_addr(sbase) + kTmaWarps * WARP_BYTES + warp * NS * 8;
+  // first cache row of the step in each stage (written by the issuing lane)
+  volatile int32_t* rows_s = reinterpret_cast<volatile int32_t*>(sbase + kTmaWarps * (WARP_BYTES + NS * 8)) + warp * NS;
+  const int64_t w = (int64_t)blockIdx.x * kTmaWarps + warp;
+  if (w >= (int64_t)a.rows * a.S) return;                                    // whole warp
+  if (lane == 0) {
+    for (int i = 0; i < NS; ++i) sm100::mbar_init(bar0 + 8u * i, 1);
+    sm100::fence_barrier_init();
+  }
+  __syncwarp();
+  const int r = (int)(w / a.S);
+  const int s = (int)(w % a.S);
+  const int per_seq = a.n_layers * a.h_kv;
+  const int b = r / per_seq, lg = r % per_seq;
+  const int layer = lg / a.h_kv, g = lg % a.h_kv;
+  const SeqInfo si = t.s[b];
+  uint32_t qa[D / 16][2];
+  {
+    const bool live = gq < a.R;
+    const int h = g * a.G + gq / a.n_q, i = gq % a.n_q;
+    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+        a.q + (live ? ((((int64_t)b * a.n_layers + layer) * a.h_q + h) * a.n_q + i) * D : 0));
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) {
+      qa[c][0] = live ? __ldg(qrow + 8 * c + tq) : 0u;
+      qa[c][1] = live ? __ldg(qrow + 8 * c + 4 + tq) : 0u;
+    }
+  }
+  int beg, end;
+  row_list(a, si, r, beg, end);
+  // positions of the row in steps of 16 (blocks hold whole steps); this split's steps
+  const int64_t n_pos = (int64_t)(end - beg) * a.P;
+  const int64_t n_steps = (n_pos + kStep - 1) / kStep;
+  const int64_t p0 = ((s * n_steps) / a.S) * kStep;
+  const int64_t p1 = min(n_pos, (((s + 1) * n_steps) / a.S) * kStep);
+  const int32_t unit_row0 = (int32_t)(si.k_off / D + ((int64_t)layer * a.h_kv + g) * si.n_keys);
+  const int key = lane & (kStep - 1);
+
+  // Block id of the step at `pos` (loaded a step before it is needed), then the step's first cache
+  // row, or -1 (past the split, or a block outside the cache).
+  auto step_id = [&](int64_t pos) -> int32_t {
+    if (pos >= p1) return -1;
+    const int bi = (int)(pos / a.P);
+    return a.indices == nullptr ? bi : __ldg(a.indices + beg + bi);
+  };
+  auto step_row = [&](int64_t pos, int32_t id) -> int32_t {
+    if (pos >= p1) return -1;
+    const int bi = (int)(pos / a.P), within = (int)(pos - (int64_t)bi * a.P);
+    const int64_t rr = (int64_t)id * a.P + within;
+    if (id >= 0 && rr < si.n_keys) return (int32_t)rr;
+    if (within == 0 && lane == 0) set_device_error(a.err, KVSEL_ERR_DEVICE, (uint32_t)(beg + bi));
+    return -1;
+  };
+  // One lane loads the step's K and V boxes into stage `buf` (a step with no row loads row 0 of the
+  // unit: its keys are masked).
+  auto issue = [&](int32_t row0, int buf) {
+    if (lane == 0) {
+      rows_s[buf] = row0;
+      const uint32_t bar = bar0 + 8u * buf;
+      sm100::mbar_expect_tx(bar, 2 * KV);
+      const int32_t y = unit_row0 + (row0 < 0 ? 0 : row0);
+      const uint32_t kst = st0 + buf * KV, vst = st0 + NS * KV + buf * KV;
+#pragma unroll
+      for (int hh = 0; hh < D / 64; ++hh) {
+        sm100::tma_load_2d(kst + hh * kHalfBytes, &tmk, 64 * hh, y, bar);
+        sm100::tma_load_2d(vst + hh * kHalfBytes, &tmv, 64 * hh, y, bar);
+      }
+    }
+  };
+  // swizzled byte offset of 16-byte chunk cc (0 .. D/8 - 1) of row x within a K or V stage
+  auto chunk_at = [](int x, int cc) -> uint32_t {
+    return (uint32_t)((cc >> 3) * kHalfBytes + x * 128 + (((cc & 7) ^ (x & 7)) << 4));
+  };
+  const int key_k = ((lane >> 4) << 3) | (lane & 7), hi_k = (lane >> 3) & 1;
+  const int key_v = (((lane >> 3) & 1) << 3) | (lane & 7), hi_v = lane >> 4;
+
+  float o[NT][2];
+#pragma unroll
+  for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = 0.f;
+  float m = -INFINITY, l = 0.f;
+  const float scale = a.scale_log2;
+  // steps are issued NS - 1 ahead; step k uses stage k % NS with phase (k / NS) & 1
+#pragma unroll
+  for (int i = 0; i < NS - 1; ++i) {
+    const int64_t pos = p0 + (int64_t)i * kStep;
+    if (pos < p1) issue(step_row(pos, step_id(pos)), i);
+  }
+  int32_t id_c = step_id(p0 + (int64_t)(NS - 1) * kStep);          // block of the next step to issue
+  int64_t k_step = 0;
+  bool ok = true;
+  for (int64_t base = p0; base < p1; base += kStep, ++k_step) {
+    const int buf = (int)(k_step % NS);
+    const int64_t npos = base + (int64_t)(NS - 1) * kStep;
+    const int32_t id_d = step_id(npos + kStep);                    // used at the next step
+    if (npos < p1) {
+      const int32_t row_c = step_row(npos, id_c);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the stage's last reads come first
+      issue(row_c, (int)((k_step + NS - 1) % NS));
+    }
+    id_c = id_d;
+    const uint32_t parity = (uint32_t)((k_step / NS) & 1);
+    if (!__all_sync(0xffffffffu, sm100::mbar_wait(bar0 + 8u * buf, parity))) {
+      if (lane == 0) set_device_error(a.err, KVSEL_ERR_TIMEOUT, 5u);
+      ok = false;
+      break;
+    }
+    const int32_t row0 = rows_s[buf];
+    const uint32_t kst = st0 + buf * KV, vst = st0 + NS * KV + buf * KV;
+    // two accumulation chains per 8-key tile (even / odd 16-wide chunks of d), added at the end
+    float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f}, t0[2] = {0.f, 0.f}, t1[2] = {0.f, 0.f};
+#pragma unroll
+    for (int c = 0; c < D / 16; c += 2) {
+      uint32_t kb[4], kc[4];
+      ldsm_x4(kb, kst + chunk_at(key_k, 2 * c + hi_k));
+      ldsm_x4(kc, kst + chunk_at(key_k, 2 * c + 2 + hi_k));
+      mma_rows8(s0, qa[c][0], qa[c][1], kb[0], kb[1]);
+      mma_rows8(s1, qa[c][0], qa[c][1], kb[2], kb[3]);
+      mma_rows8(t0, qa[c + 1][0], qa[c + 1][1], kc[0], kc[1]);
+      mma_rows8(t1, qa[c + 1][0], qa[c + 1][1], kc[2], kc[3]);
+    }
+    s0[0] += t0[0];
+    s0[1] += t0[1];
+    s1[0] += t1[0];
+    s1[1] += t1[1];
+    // key x of the step is row row0 + x: it exists when the step has a row, the position lies in the
+    // split and the row lies in the cache (a block may end past the cache)
+    const bool kv_ok = row0 >= 0 && base + key < p1 && row0 + key < si.n_keys;
+    const uint32_t valid = __ballot_sync(0xffffffffu, kv_ok && lane < kStep);
+    const int k0 = 2 * tq;
+    float z[4] = {s0[0], s0[1], s1[0], s1[1]};
+    const int kz[4] = {k0, k0 + 1, k0 + 8, k0 + 9};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) z[e] = ((valid >> kz[e]) & 1u) ? z[e] * scale : -INFINITY;
+    float mx = fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    float alpha = 1.f;
+    if (mx > m + 8.f) {
+      alpha = m == -INFINITY ? 0.f : fast_ex2(m - mx);
+      m = mx;
+    }
+    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        o[n][0] *= alpha;
+        o[n][1] *= alpha;
+      }
+    }
+    float p[4], sum = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      p[e] = z[e] == -INFINITY ? 0.f : fast_ex2(z[e] - m);
+      sum += p[e];
+    }
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    l = l * alpha + sum;
+    const uint32_t h01 = pack_bf16(p[0], p[1]), h23 = pack_bf16(p[2], p[3]);
+    const __nv_bfloat162 hb01 = *reinterpret_cast<const __nv_bfloat162*>(&h01);
+    const __nv_bfloat162 hb23 = *reinterpret_cast<const __nv_bfloat162*>(&h23);
+    const uint32_t l01 = pack_bf16(p[0] - __low2float(hb01), p[1] - __high2float(hb01));
+    const uint32_t l23 = pack_bf16(p[2] - __low2float(hb23), p[3] - __high2float(hb23));
+#pragma unroll
+    for (int pp = 0; pp < NT / 2; ++pp) {
+      uint32_t vb[4];
+      ldsm_x4_t(vb, vst + chunk_at(key_v, 2 * pp + hi_v));
+      mma_rows8(o[2 * pp], h01, h23, vb[0], vb[1]);
+      mma_rows8(o[2 * pp], l01, l23, vb[0], vb[1]);
+      mma_rows8(o[2 * pp + 1], h01, h23, vb[2], vb[3]);
+      mma_rows8(o[2 * pp + 1], l01, l23, vb[2], vb[3]);
+    }
+    __syncwarp();          // every lane's reads of the stage precede its next load
+  }
+  if (!ok) {
+    // loads still in flight must land before the warp exits: wait (bounded) for every issued step
+    for (int64_t k2 = k_step; k2 < k_step + NS - 1; ++k2) {
+      if (p0 + k2 * kStep >= p1) break;
+      sm100::mbar_wait(bar0 + 8u * (uint32_t)(k2 % NS), (uint32_t)((k2 / NS) & 1));
+    }
+    return;
+  }
+  if (gq < a.R) {
+    float* out = a.part + (((int64_t)r * a.S + s) * a.R + gq) * (D + 2);
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      out[8 * n + 2 * tq] = o[n][0];
+      out[8 * n + 2 * tq + 1] = o[n][1];
+    }
+    if (tq == 0) {
+      out[D] = m;
+      out[D + 1] = l;
+    }
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 att_encode() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D view [rows][d] bf16 of a cache, boxes of 64 columns x 16 rows with the 128-byte swizzle.
+bool att_map(CUtensorMap* mp, const void* ptr, int64_t rows, int d) {
+  auto fn = att_encode();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kStep};
+  cuuint32_t es[2] = {1, 1};
+  return fn(mp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 using AttKernel = void (*)(const AttArgs, const SeqTable);
 
 // The warp kernel for head dim d (any R <= 8 query rows per table row).
@@ -530,11 +790,38 @@ __global__ void __launch_bounds__(D) attend_combine(const __grid_constant__ AttA
 
 }  // namespace
 
-int64_t attend_splits(int64_t rows, int64_t max_rows_per_list, int R, int d) {
+// Warps of the TMA warp kernel resident at once on the current device (0 if that cannot be queried).
+int64_t attend_tma_resident_warps(int d) {
+  constexpr int kMaxDev = 64;
+  static std::mutex mu;
+  static int64_t cache[kMaxDev][2] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  const int di = d == 64 ? 0 : 1;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < kMaxDev && cache[dev][di] > 0) return cache[dev][di];
+  const size_t wsm = attend_tma_smem(d);
+  const void* kern = d == 64 ? (const void*)attend_tma<64> : (const void*)attend_tma<128>;
+  int sms = 0, per_sm = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      set_smem(kern, wsm) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 32 * kTmaWarps, wsm) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  const int64_t n = (int64_t)sms * per_sm * kTmaWarps;
+  if (dev >= 0 && dev < kMaxDev) cache[dev][di] = n;
+  return n;
+}
+
+int64_t attend_splits(int64_t rows, int64_t max_rows_per_list, int R, int d, int block) {
   if (R <= 8) {
     // warp splits: as many as fit one wave of resident warps (all rows' splits run at once), no
-    // split shorter than 64 positions
-    int64_t resident = attend_resident_warps(d);
+    // split shorter than 64 positions.  Blocks of a multiple of 16 rows run on the TMA kernel.
+    int64_t resident = block % kStep == 0 ? attend_tma_resident_warps(d) : attend_resident_warps(d);
     if (resident <= 0) resident = 152 * 12;
     int64_t s = resident / rows;
     const int64_t cap = (max_rows_per_list + 63) / 64;
@@ -584,7 +871,25 @@ kvsel_status launch_attend(const kvsel_desc& d, const SeqTable& t, const void* q
   a.rows = (int32_t)rows;
   const size_t smem = attend_smem(d.head_dim);
   kvsel_status st;
-  if (a.R <= 8) {
+  // every step's 16 rows consecutive: whole caches, or blocks of a multiple of 16 rows
+  int64_t cache_rows = 0;
+  for (int b = 0; b < d.batch; ++b) cache_rows += (int64_t)d.n_layers * d.h_kv * t.s[b].n_keys;
+  CUtensorMap tmk, tmv;
+  const bool tma = a.R <= 8 && (indices == nullptr || P % kStep == 0) && cache_rows + kStep < (int64_t(1) << 31) &&
+                   att_map(&tmk, k, cache_rows, d.head_dim) && att_map(&tmv, v, cache_rows, d.head_dim);
+  if (tma) {
+    TraceScope ts("attend_split", s);
+    const unsigned grid = (unsigned)((rows * S + kTmaWarps - 1) / kTmaWarps);
+    const size_t wsm = attend_tma_smem(d.head_dim);
+    if (d.head_dim == 64) {
+      if (set_smem((const void*)attend_tma<64>, wsm) != cudaSuccess) return KVSEL_ERR_CUDA;
+      attend_tma<64><<<grid, 32 * kTmaWarps, wsm, s>>>(tmk, tmv, a, t);
+    } else {
+      if (set_smem((const void*)attend_tma<128>, wsm) != cudaSuccess) return KVSEL_ERR_CUDA;
+      attend_tma<128><<<grid, 32 * kTmaWarps, wsm, s>>>(tmk, tmv, a, t);
+    }
+    if ((st = launch_status()) != KVSEL_OK) return st;
+  } else if (a.R <= 8) {
     TraceScope ts("attend_split", s);
     const unsigned grid = (unsigned)((rows * S + kWarpsPerCta - 1) / kWarpsPerCta);
     const size_t wsm = attend_warp_smem(d.head_dim);

@@ -206,7 +206,8 @@ kvsel_status launch_prefill(const kvsel_desc& d, const SeqTable& t, const void* 
                             void* o, float* lse, float* lse_win, void* q_win, DeviceError* err, cudaStream_t s);
 
 // Attention over a page / block table (attend.cu).
-int64_t attend_splits(int64_t rows, int64_t max_rows_per_list, int R, int d);   // R = query rows per table row
+// R = query rows per table row; block = rows per listed block
+int64_t attend_splits(int64_t rows, int64_t max_rows_per_list, int R, int d, int block);
 kvsel_status launch_attend(const kvsel_desc& d, const SeqTable& t, const void* q, int n_q, const void* k,
                            const void* v, const int32_t* indptr, const int32_t* indices, int n_per_row, int P,
                            int64_t S, float* part, float* o, DeviceError* err, cudaStream_t s);

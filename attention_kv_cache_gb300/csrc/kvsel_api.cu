@@ -531,7 +531,7 @@ static kvsel_status attend_plan(const kvsel_desc& d, int32_t n_q, int32_t block,
   if (block < 1 || block > KVSEL_MAX_PAGE || max_blocks < 0) return KVSEL_ERR_INVALID_ARG;
   const int64_t rows = total_units(d);
   const int64_t R = (int64_t)(d.h_q / d.h_kv) * n_q;
-  *S = attend_splits(rows, std::max<int64_t>(1, (int64_t)max_blocks * block), (int)R, d.head_dim);
+  *S = attend_splits(rows, std::max<int64_t>(1, (int64_t)max_blocks * block), (int)R, d.head_dim, block);
   if (rows * *S >= (int64_t(1) << 31)) return KVSEL_ERR_UNSUPPORTED;
   // error word, device-built tables, partials of the splits
   *bytes = align_up(kTableOff + kTableArea + (size_t)(rows * *S * R * (d.head_dim + 2)) * sizeof(float),
