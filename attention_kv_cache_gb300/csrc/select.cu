@@ -18,7 +18,7 @@
 namespace kvsel {
 namespace {
 
-constexpr int kTopkThreads = 1024;
+constexpr int kTopkThreads = 512;     // two CTAs per SM
 constexpr int kSmemKeysMax = 40960;   // rows up to this length are staged in shared memory
 
 __device__ __forceinline__ uint32_t f2key(float f) {
@@ -67,7 +67,7 @@ struct TopkArgs {
 constexpr int kSample = 1024;
 
 struct TopkShared {
-  uint32_t hist[256];
+  uint32_t hist[2][256];                     // select_short: one histogram per pass parity
   uint32_t hist_w[kTopkThreads / 32][256];   // one histogram per warp: no cross-warp atomics
   unsigned long long scan_sh[32];
   uint2 warp_cnt[kTopkThreads / 32];
@@ -75,16 +75,21 @@ struct TopkShared {
 };
 
 // The k-th largest of arr[0, n) (1 <= k <= n, a short list in shared memory): *T and how many keys
-// equal to *T the top k take (*krem).  Four 8-bit passes from the top digit; each keeps the keys that
+// equal to *T the top k take (*krem).  8-bit passes from the top digit; each keeps the keys that
 // match the digits chosen so far, counts their next digit (one shared histogram, one atomic per group
-// of lanes with equal digits) and chooses the digit the k-th key has.
-__device__ void select_short(const uint32_t* arr, int n, uint32_t k, TopkShared& sh, uint32_t* T, uint32_t* krem) {
+// of lanes with equal digits) and chooses the digit the k-th key has.  With `passes` < 4 the result
+// is the k-th key's top 8 * passes bits with the rest zero: a key no larger than the k-th.  The two
+// histograms alternate, so a pass zeroes the next one's while it counts into its own.
+__device__ void select_short(const uint32_t* arr, int n, uint32_t k, TopkShared& sh, uint32_t* T, uint32_t* krem,
+                             int passes = 4) {
   const int tid = threadIdx.x, lane = tid & 31;
   uint32_t prefix = 0, pmask = 0, rem = k;
-  for (int pass = 0; pass < 4; ++pass) {
+  if (tid < 256) sh.hist[0][tid] = 0;
+  __syncthreads();
+  for (int pass = 0; pass < passes; ++pass) {
     const int shift = 24 - 8 * pass;
-    if (tid < 256) sh.hist[tid] = 0;
-    __syncthreads();
+    uint32_t* hist = sh.hist[pass & 1];
+    if (tid < 256) sh.hist[(pass + 1) & 1][tid] = 0;
     for (int base = 0; base < n; base += kTopkThreads) {
       const int i = base + tid;
       uint32_t key = 0;
@@ -97,7 +102,7 @@ __device__ void select_short(const uint32_t* arr, int n, uint32_t k, TopkShared&
       if (ok) {
         const uint32_t digit = (key >> shift) & 255u;
         const unsigned peers = __match_any_sync(m, digit);
-        if (lane == __ffs(peers) - 1) atomicAdd(&sh.hist[digit], (uint32_t)__popc(peers));
+        if (lane == __ffs(peers) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(peers));
       }
     }
     __syncthreads();
@@ -105,7 +110,7 @@ __device__ void select_short(const uint32_t* arr, int n, uint32_t k, TopkShared&
       uint32_t c[8], s = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        c[j] = sh.hist[255 - 8 * lane - j];
+        c[j] = hist[255 - 8 * lane - j];
         s += c[j];
       }
       uint32_t incl = s;
@@ -129,17 +134,18 @@ __device__ void select_short(const uint32_t* arr, int n, uint32_t k, TopkShared&
     pmask |= 255u << shift;
     rem -= sh.sel_gt;
   }
+  __syncthreads();     // every thread has read sel_digit / sel_gt before they are written again
   *T = prefix;
   *krem = rem;
 }
 
 template <bool SMEM>
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constant__ TopkArgs a,
+__global__ void __launch_bounds__(kTopkThreads, 2) topk_kernel(const __grid_constant__ TopkArgs a,
                                                             const __grid_constant__ SeqTable tp) {
   const SeqTable& t = real_table(tp);
   extern __shared__ __align__(16) uint32_t keys_sm[];   // [stage] staged keys, then [cap] candidates
   __shared__ TopkShared sh;
-  uint32_t* hist = sh.hist;
+  uint32_t* hist = sh.hist[0];
   auto& hist_w = sh.hist_w;
   unsigned long long* scan_sh = sh.scan_sh;
   uint2* warp_cnt = sh.warp_cnt;
@@ -179,40 +185,91 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
   uint32_t prefix = 0, pmask = 0;
   uint32_t krem = (uint32_t)a.k;
   bool have = false;   // T (prefix) and krem found from the candidate list
-  if (a.k > 0 && a.cap >= kSample && n_cand >= 12 * kSample) {   // shorter rows: the whole-row passes are cheaper
+  int n_list = -1;     // >= 0: the list holds every candidate in index order and the emission walks it
+  const int lane = tid & 31, warp = tid >> 5;
+  const unsigned lower = (1u << lane) - 1u;
+  constexpr int kWarps = kTopkThreads / 32;
+  if (a.k > 0 && a.cap >= kSample && n_cand >= (SMEM ? 12 : 4) * kSample) {
     // A threshold read off an evenly spaced sample: about k * S / n_cand sample keys lie at or above the
     // row's k-th key; the sample's r0-th largest key, r0 1.25 times that plus three standard deviations,
-    // leaves some 1.25 k keys of the row at or above it, the k-th among them.
+    // leaves some 1.25 k keys of the row at or above it, the k-th among them.  Its top 16 bits suffice
+    // (two passes): the threshold is then a little lower, and the list a little longer.
     const float e = (float)a.k * (float)kSample / (float)n_cand;
     const int r0 = (int)(1.25f * e + 3.0f * sqrtf(e) + 4.0f);
     if (r0 <= kSample) {
       for (int s = tid; s < kSample; s += kTopkThreads) cand[s] = key_at((int)(((int64_t)s * n_cand) / kSample));
       __syncthreads();
       uint32_t T0, rem0;
-      select_short(cand, kSample, (uint32_t)r0, sh, &T0, &rem0);
-      if (tid == 0) sh.n_found = 0;
-      __syncthreads();
-      // every key >= T0 into the list (positions taken a warp at a time); keys past the capacity are
-      // counted but not stored, and the list is then not used
-      const int lane = tid & 31;
-      const unsigned lower = (1u << lane) - 1u;
+      select_short(cand, kSample, (uint32_t)r0, sh, &T0, &rem0, 2);
+      if (!SMEM) {
+        // Rows read from memory: every key >= T0 into the list in index order.  Each warp counts its
+        // contiguous segment's candidates, the counts give each warp its place, and a second read of
+        // the segment (now in L2) writes the keys and their positions.
+        const int seg = (n_cand + kWarps - 1) / kWarps;
+        const int s0 = min(n_cand, warp * seg), s1 = min(n_cand, s0 + seg);
+        uint32_t c = 0;
+#pragma unroll 8
+        for (int i = s0 + lane; i < s1; i += 32) c += key_at(i) >= T0 ? 1u : 0u;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+        if (lane == 0) warp_cnt[warp] = make_uint2(c, 0u);
+        __syncthreads();
+        uint32_t pos = 0, nf = 0;
+        for (int w = 0; w < kWarps; ++w) {
+          if (w < warp) pos += warp_cnt[w].x;
+          nf += warp_cnt[w].x;
+        }
+        if (nf >= (uint32_t)a.k && nf <= (uint32_t)a.cap) {   // the row's k-th key is among them
+          uint32_t* cand_idx = cand + a.cap;
+          constexpr int U = 8;                 // rounds whose loads are issued together
+          for (int base = s0; base < s1; base += 32 * U) {
+            uint32_t keys[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+              const int i = base + 32 * u + lane;
+              keys[u] = i < s1 ? key_at(i) : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+              const int i = base + 32 * u + lane;
+              const bool p = i < s1 && keys[u] >= T0;
+              const unsigned m = __ballot_sync(0xffffffffu, p);
+              if (p) {
+                const uint32_t at = pos + (uint32_t)__popc(m & lower);
+                cand[at] = keys[u];
+                cand_idx[at] = (uint32_t)i;
+              }
+              pos += (uint32_t)__popc(m);
+            }
+          }
+          __syncthreads();
+          select_short(cand, (int)nf, (uint32_t)a.k, sh, &prefix, &krem);
+          n_list = (int)nf;
+          have = true;
+        }
+      } else {
+        if (tid == 0) sh.n_found = 0;
+        __syncthreads();
+        // staged rows: every key >= T0 into the list (positions taken a warp at a time); keys past the
+        // capacity are counted but not stored, and the list is then not used
 #pragma unroll 4
-      for (int base = 0; base < n_cand; base += kTopkThreads) {
-        const int i = base + tid;
-        const uint32_t key = i < n_cand ? key_at(i) : 0u;
-        const bool p = i < n_cand && key >= T0;
-        const unsigned m = __ballot_sync(0xffffffffu, p);
-        uint32_t wbase = 0;
-        if (lane == 0 && m != 0u) wbase = atomicAdd(&sh.n_found, (uint32_t)__popc(m));
-        wbase = __shfl_sync(0xffffffffu, wbase, 0);
-        const uint32_t pos = wbase + (uint32_t)__popc(m & lower);
-        if (p && pos < (uint32_t)a.cap) cand[pos] = key;
-      }
-      __syncthreads();
-      const uint32_t nf = sh.n_found;
-      if (nf >= (uint32_t)a.k && nf <= (uint32_t)a.cap) {   // the row's k-th key is among them
-        select_short(cand, (int)nf, (uint32_t)a.k, sh, &prefix, &krem);
-        have = true;
+        for (int base = 0; base < n_cand; base += kTopkThreads) {
+          const int i = base + tid;
+          const uint32_t key = i < n_cand ? key_at(i) : 0u;
+          const bool p = i < n_cand && key >= T0;
+          const unsigned m = __ballot_sync(0xffffffffu, p);
+          uint32_t wbase = 0;
+          if (lane == 0 && m != 0u) wbase = atomicAdd(&sh.n_found, (uint32_t)__popc(m));
+          wbase = __shfl_sync(0xffffffffu, wbase, 0);
+          const uint32_t at = wbase + (uint32_t)__popc(m & lower);
+          if (p && at < (uint32_t)a.cap) cand[at] = key;
+        }
+        __syncthreads();
+        const uint32_t nf = sh.n_found;
+        if (nf >= (uint32_t)a.k && nf <= (uint32_t)a.cap) {   // the row's k-th key is among them
+          select_short(cand, (int)nf, (uint32_t)a.k, sh, &prefix, &krem);
+          have = true;
+        }
       }
     }
   }
@@ -263,18 +320,22 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
     }
     // ordered emission: every key > T and the first krem keys == T, in index order.  A selected key's
     // output position is the number of selected keys before it: (keys > T before it) + min(keys == T
-    // before it, krem).  Each warp owns one contiguous segment of the row: it counts its segment's
-    // keys > T and == T, one barrier makes every warp's counts visible, and the warp then walks its
-    // segment in rounds of 32 consecutive keys, placing each key from its warp's offsets and the
-    // ballots of the lanes before it.
+    // before it, krem).  Each warp owns one contiguous segment (of the row, or of the candidate list,
+    // which is in index order): it counts its segment's keys > T and == T, one barrier makes every
+    // warp's counts visible, and the warp then walks its segment in rounds of 32 consecutive keys,
+    // placing each key from its warp's offsets and the ballots of the lanes before it.
     const uint32_t T = prefix;
-    const int warp = tid >> 5, lane = tid & 31;
-    constexpr int kWarps = kTopkThreads / 32;
-    const int seg = (n_cand + kWarps - 1) / kWarps;
-    const int s0 = min(n_cand, warp * seg), s1 = min(n_cand, s0 + seg);
+    const uint32_t* cand_idx = cand + a.cap;
+    const bool from_list = n_list >= 0;
+    const int n_em = from_list ? n_list : n_cand;
+    auto em_key = [&](int i) -> uint32_t { return from_list ? cand[i] : key_at(i); };
+    auto em_idx = [&](int i) -> int32_t { return from_list ? (int32_t)cand_idx[i] : i; };
+    const int seg = (n_em + kWarps - 1) / kWarps;
+    const int s0 = min(n_em, warp * seg), s1 = min(n_em, s0 + seg);
     uint32_t g = 0, e = 0;
+#pragma unroll 8
     for (int i = s0 + lane; i < s1; i += 32) {
-      const uint32_t key = key_at(i);
+      const uint32_t key = em_key(i);
       g += key > T ? 1u : 0u;
       e += key == T ? 1u : 0u;
     }
@@ -283,6 +344,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
       g += __shfl_xor_sync(0xffffffffu, g, o);
       e += __shfl_xor_sync(0xffffffffu, e, o);
     }
+    __syncthreads();                       // (warp_cnt may still be read by the list's placement)
     if (lane == 0) warp_cnt[warp] = make_uint2(g, e);
     __syncthreads();
     uint32_t gt_before = 0, eq_before = 0;
@@ -290,18 +352,26 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const __grid_constan
       gt_before += warp_cnt[w].x;
       eq_before += warp_cnt[w].y;
     }
-    const unsigned lower = (1u << lane) - 1u;
-    for (int base = s0; base < s1; base += 32) {
-      const int i = base + lane;
-      const uint32_t key = i < s1 ? key_at(i) : 0u;
-      const bool is_gt = i < s1 && key > T;
-      const bool is_eq = i < s1 && key == T;
-      const unsigned mg = __ballot_sync(0xffffffffu, is_gt), me = __ballot_sync(0xffffffffu, is_eq);
-      const uint32_t gb = gt_before + __popc(mg & lower), eb = eq_before + __popc(me & lower);
-      if (is_gt) out[gb + min(eb, krem)] = i;
-      else if (is_eq && eb < krem) out[gb + eb] = i;
-      gt_before += __popc(mg);
-      eq_before += __popc(me);
+    constexpr int U = 4;                       // rounds whose loads are issued together
+    for (int base = s0; base < s1; base += 32 * U) {
+      uint32_t keys[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = base + 32 * u + lane;
+        keys[u] = i < s1 ? em_key(i) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = base + 32 * u + lane;
+        const bool is_gt = i < s1 && keys[u] > T;
+        const bool is_eq = i < s1 && keys[u] == T;
+        const unsigned mg = __ballot_sync(0xffffffffu, is_gt), me = __ballot_sync(0xffffffffu, is_eq);
+        const uint32_t gb = gt_before + __popc(mg & lower), eb = eq_before + __popc(me & lower);
+        if (is_gt) out[gb + min(eb, krem)] = em_idx(i);
+        else if (is_eq && eb < krem) out[gb + eb] = em_idx(i);
+        gt_before += __popc(mg);
+        eq_before += __popc(me);
+      }
     }
   }
   // recency pages, then (when appended) window pages or window tokens: the indices from n_cand on
@@ -434,14 +504,18 @@ kvsel_status launch_topk(const kvsel_desc& d, const SeqTable& t, int rows, int k
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
     return KVSEL_ERR_CUDA;
-  const bool staged = nmax <= kSmemKeysMax;
+  // rows of 12K keys or more are read from memory and take the ordered candidate list (keys and
+  // positions); shorter rows are staged in shared memory
+  const bool staged = nmax < 12 * kSample && nmax <= kSmemKeysMax;
   a.stage = staged ? (int32_t)nmax : 0;
-  // candidate list: room for 4 k + 2048 keys (the sample's threshold keeps ~1.25 k) within what shared
-  // memory has left beside the staged row and the kernel's own arrays
-  const int64_t avail = ((int64_t)optin - (int64_t)sizeof(TopkShared) - 256) / 4 - a.stage;
-  const int64_t cap = std::min<int64_t>(std::max<int64_t>(kSample, 4 * (int64_t)k + 2048), avail);
+  // candidate list: room for 2 k + 2048 entries (the sample's threshold keeps ~1.25 k; more than 2 k + 2048
+  // is several standard deviations out, and then the whole-row select runs) within what shared memory
+  // has left beside the staged row and the kernel's own arrays
+  const int64_t entry = staged ? 1 : 2;      // a key, or a key and its position
+  const int64_t avail = (((int64_t)optin - (int64_t)sizeof(TopkShared) - 256) / 4 - a.stage) / entry;
+  const int64_t cap = std::min<int64_t>(std::max<int64_t>(kSample, 2 * (int64_t)k + 2048), avail);
   a.cap = cap >= kSample ? (int32_t)cap : 0;
-  const size_t smem = (size_t)(a.stage + a.cap) * sizeof(uint32_t);
+  const size_t smem = (size_t)(a.stage + entry * a.cap) * sizeof(uint32_t);
   const int grid = d.batch * rows;
   TraceScope ts("topk_radix", s);
   if (staged) {
