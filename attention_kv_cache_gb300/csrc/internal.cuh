@@ -137,6 +137,8 @@ constexpr int64_t kScoreSeg1 = 2048;
 // Problem description handed to every scoring kernel.
 struct ScoreShape {
   int32_t n_layers, h_q, h_kv, d, W, G, R;   // R = G * W rows per unit
+  int32_t Wp;                                // tensor-core tile rows per head (a power of two >= W for the
+                                             // group max, so every head fills whole register groups; else W)
   int32_t group_reduce, pool_k, page_size, page_reduce;
   int32_t pool_type;                         // KVSEL_POOL_MAX / KVSEL_POOL_AVG
   int32_t logits;                            // 1: pre-softmax scaled logits (one pass, no lse)

@@ -167,6 +167,7 @@ ScoreShape make_shape(const kvsel_desc& d) {
   ScoreShape sh;
   sh.n_layers = d.n_layers; sh.h_q = d.h_q; sh.h_kv = d.h_kv; sh.d = d.head_dim; sh.W = d.window;
   sh.G = d.h_q / d.h_kv; sh.R = sh.G * d.window;
+  sh.Wp = d.window;         // padded by the tensor-core launcher where it needs it
   sh.group_reduce = d.group_reduce; sh.pool_k = d.pool_k; sh.page_size = d.page_size;
   sh.page_reduce = d.page_reduce;
   sh.pool_type = d.pool_type;

@@ -98,6 +98,22 @@ struct Item {
   int a0, a1;          // pass 2: prefix range whose scores are emitted
 };
 
+// Tile row r of a unit: with heads padded to Wp rows, row r is window row j = r % Wp of head
+// h = r / Wp, a real row when j < W and h < G, whose index among the unit's R = G W rows is h W + j;
+// without padding (Wp == W) tile row r is row r.  -1 for a padding row.
+__device__ __forceinline__ int real_row(const ScoreShape& sh, int r) {
+  if (sh.Wp == sh.W) return r < sh.R ? r : -1;
+  const int h = r / sh.Wp, j = r - h * sh.Wp;
+  return (j < sh.W && h < sh.G) ? h * sh.W + j : -1;
+}
+
+// Heads of the group that start at tile row c0 or later (the head sums of a 64-column block that
+// begins there), for the group max: the blocks' remaining heads are all padding rows.
+__device__ __forceinline__ int heads_from(const ScoreShape& sh, int c0) {
+  const int hw = sh.Wp < 64 ? sh.Wp : 64;
+  return max(0, sh.G - c0 / hw);
+}
+
 // Unit ul of sequence b: the fields every item of it shares.
 __device__ __forceinline__ void unit_fields(const SeqTable& t, const ScoreShape& sh, int b, int ul, Item& it) {
   const SeqInfo si = t.s[b];   // a copy: loads once, whatever the table lives in
@@ -170,8 +186,9 @@ __device__ __forceinline__ void write_fold_rows(const TcArgs& a, int unit, uint8
   const double inv = 1.0 / (double)a.sh.scale_log2;
   for (int r = lane; r < RT; r += 32) {
     __nv_bfloat16 p1, p2, p3;
-    if (r < a.sh.R) {
-      const double h = -0.5 * (double)a.lse[(int64_t)unit * a.sh.R + r] * inv;
+    const int rr = real_row(a.sh, r);
+    if (rr >= 0) {
+      const double h = -0.5 * (double)a.lse[(int64_t)unit * a.sh.R + rr] * inv;
       p1 = __float2bfloat16_rn((float)h);
       const double r1 = h - (double)__bfloat162float(p1);
       p2 = __float2bfloat16_rn((float)r1);
@@ -193,8 +210,8 @@ __device__ __forceinline__ void write_fold_rows(const TcArgs& a, int unit, uint8
 // Lane 0 issues every TMA load and does every wait; the whole warp runs the loop (its decisions
 // are lane 0's, broadcast) so that all lanes can write the pass-2 row constants at a unit change.
 template <bool PASS2, int RT, int D, int NK>
-__device__ void produce(const CUtensorMap* tq, const CUtensorMap* tk, const TcArgs& a, const SeqTable& t,
-                        uint32_t base, uint8_t* sbase, volatile uint32_t* flag) {
+__device__ void produce(const CUtensorMap* tq, const CUtensorMap* tqh, const CUtensorMap* tk, const TcArgs& a,
+                        const SeqTable& t, uint32_t base, uint8_t* sbase, volatile uint32_t* flag) {
   using P = Plan<PASS2, RT, D, NK>;
   const int lane = threadIdx.x % 32;
   const bool leader = lane == 0;
@@ -224,12 +241,24 @@ __device__ void produce(const CUtensorMap* tq, const CUtensorMap* tk, const TcAr
       }
       if (fold) write_fold_rows<RT>(a, it.unit, sbase + P::kCOff, lane);
       if (leader) {
-        mbar_expect_tx(q_full, P::kQBytes);
+        if (a.sh.Wp == a.sh.W) {
+          mbar_expect_tx(q_full, P::kQBytes);
 #pragma unroll
-        for (int db = 0; db < P::kDBlocks; ++db)
+          for (int db = 0; db < P::kDBlocks; ++db)
 #pragma unroll
-          for (int m = 0; m < RT / 128; ++m)
-            tma_load_2d(base + P::kQOff + db * P::kQBlock + m * 16384, tq, db * 64, it.q_row0 + m * 128, q_full);
+            for (int m = 0; m < RT / 128; ++m)
+              tma_load_2d(base + P::kQOff + db * P::kQBlock + m * 16384, tq, db * 64, it.q_row0 + m * 128, q_full);
+        } else {
+          // padded heads: head h's rows land at tile rows h Wp .. (boxes of Wp rows; the rows past a
+          // head's W are the next head's, and count as padding)
+          mbar_expect_tx(q_full, (uint32_t)(a.sh.G * a.sh.Wp * 128 * P::kDBlocks));
+          for (int db = 0; db < P::kDBlocks; ++db)
+            for (int h = 0; h < a.sh.G; ++h) {
+              const int r0 = h * a.sh.Wp;
+              tma_load_2d(base + P::kQOff + db * P::kQBlock + (r0 >> 7) * 16384 + (r0 & 127) * 128, tqh, db * 64,
+                          it.q_row0 + h * a.sh.W, q_full);
+            }
+        }
       }
       qph ^= 1;
       ++n_q;
@@ -439,7 +468,7 @@ __device__ __forceinline__ float colmass64(const float* v, const float2* nl, flo
 // Logits mode: the same reductions over sum_i v_i * w_i, w = 1/sqrt(d) for real rows and 0 for
 // the padding rows (GemFilter's pre-softmax score; no exponentials).
 template <int MAXW>
-__device__ __forceinline__ float linmass64(const float* v, const float2* w) {
+__device__ __forceinline__ float linmass64(const float* v, const float2* w, int nh = 64) {
   if constexpr (MAXW == 0) {
     float2 a[4];
 #pragma unroll
@@ -462,7 +491,8 @@ __device__ __forceinline__ float linmass64(const float* v, const float2* w) {
         const int c = h * NP + i;
         a[i % NA] = __ffma2_rn(make_float2(v[2 * c], v[2 * c + 1]), w[c], a[i % NA]);
       }
-      red = fmaxf(red, tree_sum2<NA>(a));
+      // heads past the group's last (all padding) have no sum: a zero would outrank negative maxima
+      if (h < nh) red = fmaxf(red, tree_sum2<NA>(a));
     }
     return red;
   }
@@ -550,12 +580,13 @@ __device__ void epilogue_pass1(const TcArgs& a, const SeqTable& t, uint32_t base
   constexpr bool kPairs = RT == 256;
   const int rblk = kPairs ? (e.wg & 1) : 0;                    // accumulator block (128 rows)
   const int chalf = e.wg >> (kPairs ? 1 : 0);                  // RT = 256: pair; else 64-column half
-  const int row = e.lrow + 128 * rblk;
+  const int trow = e.lrow + 128 * rblk;                         // tile row
+  const int row = real_row(a.sh, trow);                         // the unit's row (-1: padding)
   const uint32_t col0 = kPairs ? 128u * rblk : 64u * chalf;    // TMEM column within a stage
   const int key0 = kPairs ? 0 : 64 * chalf;                    // tile key of that column
   float* red = reinterpret_cast<float*>(sbase + P::kRedOff);
   const float scale = a.sh.scale_log2;
-  const bool rvalid = row < a.sh.R;
+  const bool rvalid = row >= 0;
   int ts = 0, nt = 0;                                           // nt: tiles this CTA has taken so far
   uint32_t tph = 0;
   Work<false> work(t);
@@ -624,6 +655,21 @@ __device__ void epilogue_pass1(const TcArgs& a, const SeqTable& t, uint32_t base
       }
     }
   }
+}
+
+// The group max of a key's two partials by shared-memory atomics: probabilities (>= 0) compare as
+// their int bit patterns; the signed sums of pre-softmax scores compare through an order-preserving
+// unsigned key (0 lies below every key), decoded in place before the segment is pooled.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float order_key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+__device__ __forceinline__ void max_into(float* slot, float v, bool signed_values) {
+  if (signed_values) atomicMax(reinterpret_cast<unsigned int*>(slot), order_key(v));
+  else atomicMax(reinterpret_cast<int*>(slot), __float_as_int(v));
 }
 
 // Pooling of a segment's group scores S[ta..tb) (the pooling halo included) into out[a0..a1), and,
@@ -721,8 +767,9 @@ __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base
     epi_sync<P::kEW>();                                      // readers of the previous item are done
     for (int i = e.etid; i < it.tb - it.ta; i += kEpiThreads) Ss[i] = 0.f;
     for (int i = e.etid; i < RT; i += kEpiThreads) {
-      if (a.sh.logits) lse_s[i] = i < a.sh.R ? a.sh.scale_nat : 0.f;    // row weights of the logit sum
-      else lse_s[i] = i < a.sh.R ? -a.lse[(int64_t)it.unit * a.sh.R + i] : -INFINITY;   // padding rows: p = 0
+      const int rr = real_row(a.sh, i);
+      if (a.sh.logits) lse_s[i] = rr >= 0 ? a.sh.scale_nat : 0.f;    // row weights of the logit sum
+      else lse_s[i] = rr >= 0 ? -a.lse[(int64_t)it.unit * a.sh.R + rr] : -INFINITY;   // padding rows: p = 0
     }
     epi_sync<P::kEW>();
     float2 nl[32];
@@ -739,18 +786,22 @@ __device__ void epilogue_pass2(const TcArgs& a, const SeqTable& t, uint32_t base
         tc_fence_before();
         __syncwarp();
         if (e.lane == 0) mbar_arrive(tempty(ts));
-        const float red = a.sh.logits ? linmass64<MAXW>(v64, nl) : colmass64<MAXW>(v64, nl, scale);
+        const float red = a.sh.logits ? linmass64<MAXW>(v64, nl, heads_from(a.sh, col0))
+                                       : colmass64<MAXW>(v64, nl, scale);
         const int key = t0 + e.lrow;
         if (key < it.tb) {
           // two addends per key (one per warpgroup): the result does not depend on their order
-          // (group max runs here with probabilities only, which are >= 0, so the int order is the float order)
           if constexpr (MAXW == 0) atomicAdd(&Ss[key - it.ta], red);
-          else atomicMax(reinterpret_cast<int*>(&Ss[key - it.ta]), __float_as_int(red));
+          else max_into(&Ss[key - it.ta], red, a.sh.logits != 0);
         }
       }
       if (++ts == (int)P::kNT) { ts = 0; tph ^= 1; }
     }
     epi_sync<P::kEW>();
+    if (MAXW > 0 && a.sh.logits) {   // signed group maxima: keys back to values
+      for (int i = e.etid; i < it.tb - it.ta; i += kEpiThreads) Ss[i] = order_key_value(__float_as_uint(Ss[i]));
+      epi_sync<P::kEW>();
+    }
     if (aborted(flag)) continue;
     // max-pool over prefix positions, then page reduce (DELTA key designs 2-3)
     const SeqInfo si = t.s[it.b];   // a copy: loads once, whatever the table lives in
@@ -797,8 +848,9 @@ __device__ void epilogue_pass2_pairs(const TcArgs& a, const SeqTable& t, uint32_
     epi_sync<P::kEW>();                                  // readers of the previous item are done
     for (int i = e.etid; i < it.tb - it.ta; i += kEpiThreads) Ss[i] = 0.f;
     for (int i = e.etid; i < RT && !fold; i += kEpiThreads) {
-      if (a.sh.logits) lse_s[i] = i < a.sh.R ? a.sh.scale_nat : 0.f;
-      else lse_s[i] = i < a.sh.R ? -a.lse[(int64_t)it.unit * a.sh.R + i] : -INFINITY;
+      const int rr = real_row(a.sh, i);
+      if (a.sh.logits) lse_s[i] = rr >= 0 ? a.sh.scale_nat : 0.f;
+      else lse_s[i] = rr >= 0 ? -a.lse[(int64_t)it.unit * a.sh.R + rr] : -INFINITY;
     }
     epi_sync<P::kEW>();
     for (int t0 = it.ta; t0 < it.tb; t0 += kTileKeys, ++nt) {
@@ -816,7 +868,8 @@ __device__ void epilogue_pass2_pairs(const TcArgs& a, const SeqTable& t, uint32_
         float v[64];
         tmem_ld64(lane_base, v);
         r0 = fold ? colmass64<MAXW, true>(v, nullptr, scale)
-                  : (a.sh.logits ? linmass64<MAXW>(v, nls) : colmass64<MAXW>(v, nls, scale));
+                  : (a.sh.logits ? linmass64<MAXW>(v, nls, heads_from(a.sh, 128 * half))
+                                 : colmass64<MAXW>(v, nls, scale));
       }
       {
         float v[64];
@@ -825,17 +878,21 @@ __device__ void epilogue_pass2_pairs(const TcArgs& a, const SeqTable& t, uint32_
         __syncwarp();
         if (e.lane == 0) mbar_arrive(tempty);
         r1 = fold ? colmass64<MAXW, true>(v, nullptr, scale)
-                  : (a.sh.logits ? linmass64<MAXW>(v, nls + 32) : colmass64<MAXW>(v, nls + 32, scale));
+                  : (a.sh.logits ? linmass64<MAXW>(v, nls + 32, heads_from(a.sh, 128 * half + 64))
+                                 : colmass64<MAXW>(v, nls + 32, scale));
       }
       const float red = MAXW == 0 ? r0 + r1 : fmaxf(r0, r1);
       const int key = t0 + e.lrow;
       if (key < it.tb) {
-        // group max runs here with probabilities only, which are >= 0, so the int order is the float order
         if constexpr (MAXW == 0) atomicAdd(&Ss[key - it.ta], red);
-        else atomicMax(reinterpret_cast<int*>(&Ss[key - it.ta]), __float_as_int(red));
+        else max_into(&Ss[key - it.ta], red, a.sh.logits != 0);
       }
     }
     epi_sync<P::kEW>();
+    if (MAXW > 0 && a.sh.logits) {   // signed group maxima: keys back to values
+      for (int i = e.etid; i < it.tb - it.ta; i += kEpiThreads) Ss[i] = order_key_value(__float_as_uint(Ss[i]));
+      epi_sync<P::kEW>();
+    }
     if (aborted(flag)) continue;
     const SeqInfo si = t.s[it.b];   // a copy: loads once, whatever the table lives in
     float* out = a.scores + si.s_off + ((int64_t)it.layer * a.sh.h_kv + it.g) * it.L;
@@ -853,6 +910,7 @@ __device__ void epilogue_pass2_pairs(const TcArgs& a, const SeqTable& t, uint32_
 // ---------------------------------------------------------------- kernels
 template <bool PASS2, int RT, int D, int NK, int MAXW>
 __global__ void __launch_bounds__(Plan<PASS2, RT, D, NK>::kThreads, 1) score_tc_kernel(const __grid_constant__ CUtensorMap tq,
+                                                                 const __grid_constant__ CUtensorMap tqh,
                                                                  const __grid_constant__ CUtensorMap tk,
                                                                  const __grid_constant__ TcArgs a,
                                                                  const __grid_constant__ SeqTable tp) {
@@ -887,13 +945,18 @@ __global__ void __launch_bounds__(Plan<PASS2, RT, D, NK>::kThreads, 1) score_tc_
     for (int i = threadIdx.x; i < 128 * 32 / 4; i += blockDim.x) ones[i] = 0x3F803F80u;
     fence_proxy_async_smem();
   }
+  if (a.sh.Wp != a.sh.W) {   // padded heads: tile rows past the last head are never loaded; keep them zero
+    uint4* qz = reinterpret_cast<uint4*>(sbase + P::kQOff);
+    for (int i = threadIdx.x; i < (int)(P::kQBytes / 16); i += blockDim.x) qz[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
   if (warp == 1) tmem_alloc(smem_addr(tslot), kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
   if (warp == 0) {
-    produce<PASS2, RT, D, NK>(&tq, &tk, a, t, base, sbase, flag);
+    produce<PASS2, RT, D, NK>(&tq, &tqh, &tk, a, t, base, sbase, flag);
   } else if (warp == 1) {
     if (lane == 0) issue_mma<PASS2, RT, D, NK>(a, t, base, tmem, flag);
   } else {
@@ -924,13 +987,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D view [rows][D] bf16, boxes of 64 x 128 with 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int D) {
+// 2-D view [rows][D] bf16, boxes of 64 x box_rows with 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, int64_t rows, int D, int box_rows = 128) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -956,35 +1019,35 @@ DevInfo device_info() {
 }
 
 template <bool PASS2, int RT, int D, int NK, int MAXW>
-kvsel_status launch_one(const char* name, const CUtensorMap& tq, const CUtensorMap& tk, const TcArgs& a,
-                        const SeqTable& t, int sms, cudaStream_t s) {
+kvsel_status launch_one(const char* name, const CUtensorMap& tq, const CUtensorMap& tqh, const CUtensorMap& tk,
+                        const TcArgs& a, const SeqTable& t, int sms, cudaStream_t s) {
   using P = Plan<PASS2, RT, D, NK>;
   auto kern = score_tc_kernel<PASS2, RT, D, NK, MAXW>;
   if (set_smem((const void*)kern, P::kSmem) != cudaSuccess) return KVSEL_ERR_CUDA;
   const int grid = t.n_items < sms ? t.n_items : sms;
   TraceScope ts(name, s);
-  kern<<<grid, P::kThreads, P::kSmem, s>>>(tq, tk, a, t);
+  kern<<<grid, P::kThreads, P::kSmem, s>>>(tq, tqh, tk, a, t);
   return launch_status();
 }
 
 template <int RT, int D>
 kvsel_status run_tc(const TcArgs& a, const SeqTable& t1, const SeqTable& t2, const CUtensorMap& tq,
-                    const CUtensorMap& tk, int sms, cudaStream_t s) {
+                    const CUtensorMap& tqh, const CUtensorMap& tk, int sms, cudaStream_t s) {
   // K stages: as many as shared memory holds beside Q (and pass 2's segment buffers)
   constexpr int NK1 = (RT == 256 && D == 128) ? 5 : 4;
   constexpr int NK = (RT == 256 && D == 128) ? 3 : 4;
   kvsel_status st;
   if (!a.sh.logits && !a.sh.lse_given) {   // the softmax needs each row's log-sum-exp first
-    if ((st = launch_one<false, RT, D, NK1, 0>("score_pass1_tc", tq, tk, a, t1, sms, s)) != KVSEL_OK) return st;
+    if ((st = launch_one<false, RT, D, NK1, 0>("score_pass1_tc", tq, tqh, tk, a, t1, sms, s)) != KVSEL_OK) return st;
     if ((st = launch_lse_combine(a.sh, t1, a.part, a.lse, s)) != KVSEL_OK) return st;
   }
   if (a.sh.group_reduce != KVSEL_REDUCE_MAX)
-    return launch_one<true, RT, D, NK, 0>("score_pass2_tc", tq, tk, a, t2, sms, s);
-  switch (a.sh.W) {
-    case 8: return launch_one<true, RT, D, NK, 8>("score_pass2_tc", tq, tk, a, t2, sms, s);
-    case 16: return launch_one<true, RT, D, NK, 16>("score_pass2_tc", tq, tk, a, t2, sms, s);
-    case 32: return launch_one<true, RT, D, NK, 32>("score_pass2_tc", tq, tk, a, t2, sms, s);
-    case 64: return launch_one<true, RT, D, NK, 64>("score_pass2_tc", tq, tk, a, t2, sms, s);
+    return launch_one<true, RT, D, NK, 0>("score_pass2_tc", tq, tqh, tk, a, t2, sms, s);
+  switch (a.sh.Wp) {
+    case 8: return launch_one<true, RT, D, NK, 8>("score_pass2_tc", tq, tqh, tk, a, t2, sms, s);
+    case 16: return launch_one<true, RT, D, NK, 16>("score_pass2_tc", tq, tqh, tk, a, t2, sms, s);
+    case 32: return launch_one<true, RT, D, NK, 32>("score_pass2_tc", tq, tqh, tk, a, t2, sms, s);
+    case 64: return launch_one<true, RT, D, NK, 64>("score_pass2_tc", tq, tqh, tk, a, t2, sms, s);
   }
   return KVSEL_ERR_UNSUPPORTED;
 }
@@ -1000,10 +1063,14 @@ kvsel_status launch_score(const ScoreShape& sh_in, const SeqTable& base, const v
   for (int b = 0; b < base.batch; ++b) k_rows += ups * base.s[b].n_keys;
   const int64_t q_rows = (int64_t)base.batch * sh.n_layers * sh.h_q * sh.W;
   const DevInfo dev = device_info();
-  // group max: register-resident heads of 8 .. 64 rows, probabilities only (logit sums may be negative)
-  const bool w_ok = sh.group_reduce != KVSEL_REDUCE_MAX ||
-                    (!sh.logits && (sh.W == 8 || sh.W == 16 || sh.W == 32 || sh.W == 64));
-  const bool tc = dev.major == 10 && dev.sms > 0 && sh.R <= 256 && w_ok && k_rows + 256 < (int64_t(1) << 31) &&
+  // group max: register-resident heads of 8 .. 64 tile rows; a window that is not a power of two is
+  // padded to one (the padding rows carry no mass), so the group is G Wp tile rows
+  if (sh.group_reduce == KVSEL_REDUCE_MAX) {
+    sh.Wp = 8;
+    while (sh.Wp < sh.W) sh.Wp *= 2;
+  }
+  const int rows_tile = sh.G * sh.Wp;
+  const bool tc = dev.major == 10 && dev.sms > 0 && rows_tile <= 256 && sh.Wp <= 64 && k_rows + 256 < (int64_t(1) << 31) &&
                   q_rows + 256 < (int64_t(1) << 31) && encode_fn() != nullptr;
   sh.seg1 = (int32_t)kScoreSeg1;
   SeqTable t1, t2;
@@ -1014,8 +1081,13 @@ kvsel_status launch_score(const ScoreShape& sh_in, const SeqTable& base, const v
     if ((st = with_items(base, ups, sh.seg2, false, sh.W, 1, s, &t2)) != KVSEL_OK) return st;
     return launch_score_simt(sh, t1, t2, q, k, scores, page_scores, lse, part, err, s);
   }
-  CUtensorMap tq, tk;
+  CUtensorMap tq, tqh, tk;
   if (!make_map(&tq, q, q_rows, sh.d) || !make_map(&tk, k, k_rows, sh.d)) return KVSEL_ERR_CUDA;
+  if (sh.Wp != sh.W) {   // per-head boxes of Wp rows for the padded layout
+    if (!make_map(&tqh, q, q_rows, sh.d, sh.Wp)) return KVSEL_ERR_CUDA;
+  } else {
+    tqh = tq;
+  }
   sh.seg2 = (int32_t)(sh.page_size * (kSeg2Max / sh.page_size));
   // one item per prefix page
   if ((st = with_items(base, ups, sh.page_size, false, sh.W, 1, s, &t2)) != KVSEL_OK) return st;
@@ -1026,9 +1098,10 @@ kvsel_status launch_score(const ScoreShape& sh_in, const SeqTable& base, const v
   a.lse = lse;
   a.part = part;
   a.err = err;
-  if (sh.R <= 128) return sh.d == 64 ? run_tc<128, 64>(a, t1, t2, tq, tk, dev.sms, s)
-                                     : run_tc<128, 128>(a, t1, t2, tq, tk, dev.sms, s);
-  return sh.d == 64 ? run_tc<256, 64>(a, t1, t2, tq, tk, dev.sms, s) : run_tc<256, 128>(a, t1, t2, tq, tk, dev.sms, s);
+  if (rows_tile <= 128) return sh.d == 64 ? run_tc<128, 64>(a, t1, t2, tq, tqh, tk, dev.sms, s)
+                                          : run_tc<128, 128>(a, t1, t2, tq, tqh, tk, dev.sms, s);
+  return sh.d == 64 ? run_tc<256, 64>(a, t1, t2, tq, tqh, tk, dev.sms, s)
+                    : run_tc<256, 128>(a, t1, t2, tq, tqh, tk, dev.sms, s);
 }
 
 }  // namespace kvsel

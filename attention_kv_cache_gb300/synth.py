@@ -141,7 +141,12 @@ LOOKAHEAD_LLAMA8B_32K = Workload("lookahead_llama8b_32l_h32x8_d128_L32768_W32_C1
                                  (32768,), group_reduce="mean", pool_k=7, pool_type="avg", k_keep=128,
                                  append_window=False, n_clusters=8)
 
-VARIANTS = (CLAA_LLAMA8B_32K, GEMFILTER_LLAMA8B_32K, LOOKAHEAD_LLAMA8B_32K)
+# The group max over heads of 24 window rows (a window that is not a power of two): the shape the
+# tensor-core scoring does not cover, served by the CUDA-core kernels.
+MAXW24_LLAMA8B_32K = Workload("maxw24_llama8b_32l_h32x8_d128_L32768_W24", 8, 32, 32, 8, 128, 24, (32768,),
+                              group_reduce="max", pool_k=7, k_keep=1024, n_clusters=8)
+
+VARIANTS = (CLAA_LLAMA8B_32K, GEMFILTER_LLAMA8B_32K, LOOKAHEAD_LLAMA8B_32K, MAXW24_LLAMA8B_32K)
 
 
 def by_name(name: str) -> Workload:

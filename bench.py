@@ -236,6 +236,17 @@ def kernel_flops(w, n_layers=None):
     return {"score_pass1_tc": pass1, "score_pass2_tc": pass2}
 
 
+def alu_peak_tflops():
+    """fp32 FMA peak of the CUDA-core scoring kernels: 152 SMs x 128 FMA lanes x 2 flops x the maximum SM
+    clock in MEASURED_PEAKS.json (2070 MHz when absent): 80.5 TFLOP/s on a GB300."""
+    mhz = 2070.0
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            mhz = float(json.load(f).get("sm_max_mhz", mhz))
+    return 152 * 128 * 2 * mhz * 1e6 / 1e12
+
+
 def traffic_record(kernel):
     """dram bytes per launch from the committed ncu summary, if taken on the kernel's current source."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
@@ -358,7 +369,17 @@ def run_kvsel(args):
     t_launch = k_ms / n_launch / 1e3
     # the roofline is the larger of the HBM time and the tensor time at the measured peaks (with 256
     # window rows per unit, as in the 70B-shaped workload, the two are about equal)
-    if (bytes_per_launch is not None and flops_per_launch is not None
+    alu_flops = kernel_flops(w, scored_layers).get(name.replace("_simt", "_tc")) if name.endswith("_simt") else None
+    if alu_flops is not None and bytes_per_launch is not None and \
+            alu_flops / (alu_peak_tflops() * 1e12) > bytes_per_launch / (peak * 1e9):
+        # the CUDA-core kernels make the logits with fp32 FMA: bound by that rate, not by HBM
+        achieved = alu_flops / t_launch / 1e12
+        roof = {"bound": "alu", "kernel": name, "achieved": round(achieved, 1), "peak": round(alu_peak_tflops(), 1),
+                "unit": "TFLOP/s", "frac": round(achieved / alu_peak_tflops(), 4),
+                "peak_source": "fp32 FMA lanes x SM clock", "traffic": None, "algorithmic_flops": alu_flops,
+                "algorithmic_bytes": bytes_per_launch, "hbm_frac": round(bytes_per_launch / t_launch / 1e9 / peak, 4),
+                "share": round(k_ms / sum(x[1] for x in trace.values()), 4)}
+    elif (bytes_per_launch is not None and flops_per_launch is not None
             and flops_per_launch / (tc_peak * 1e12) > bytes_per_launch / (peak * 1e9)):
         achieved = flops_per_launch / t_launch / 1e12
         roof = {"bound": "tensor", "kernel": name, "achieved": round(achieved, 1), "peak": tc_peak,

@@ -32,9 +32,19 @@ CASES = {
                              k_keep=100, n_clusters=4),
     # prefix of one token
     "L1": S.Workload("edge_L1", 92, 1, 4, 1, 128, 8, (1,), pool_k=7, k_keep=1),
-    # max over heads whose window is not a power of two: served by the CUDA-core kernels
-    "w24_max_cudacore": S.Workload("edge_w24", 93, 2, 8, 2, 128, 24, (3000,), group_reduce="max", pool_k=5,
-                                   k_keep=200, n_clusters=4),
+    # max over heads whose window is not a power of two: each head padded to 32 tile rows (4 x 32 = 128)
+    "w24_max_padded": S.Workload("edge_w24", 93, 2, 8, 2, 128, 24, (3000,), group_reduce="max", pool_k=5,
+                                 k_keep=200, n_clusters=4),
+    # W = 40 padded to 64 rows per head, group of 4: a 256-row tile with 24 dead rows in every head
+    "w40_max_padded_rt256": S.Workload("edge_w40", 107, 1, 8, 2, 128, 40, (2345,), group_reduce="max", pool_k=7,
+                                       k_keep=90, n_clusters=4),
+    # W = 5 padded to 8 rows, group of 4, d = 64
+    "w5_max_padded_d64": S.Workload("edge_w5", 108, 1, 8, 2, 64, 5, (3001,), group_reduce="max", pool_k=3,
+                                    k_keep=40, n_clusters=4),
+    # group of 10 with W = 24: 240 rows, but 10 x 32 padded rows exceed a 256-row tile, so the
+    # CUDA-core kernels serve it
+    "g10w24_max_cudacore": S.Workload("edge_g10w24", 109, 1, 20, 2, 128, 24, (1500,), group_reduce="max",
+                                      pool_k=5, k_keep=100, n_clusters=4),
     # group of 6 x 32 rows = 192 rows in a 256-row tile: 64 padding rows must carry no mass
     "g6_rt256_padded": S.Workload("edge_g6", 98, 1, 12, 2, 128, 32, (2222,), group_reduce="sum", pool_k=7,
                                   k_keep=100, n_clusters=4),

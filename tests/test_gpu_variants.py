@@ -29,16 +29,22 @@ V = {
     # logits per KV head, max pool, group sum
     "logits_group_w4": S.Workload("v_logits", 97, 2, 8, 2, 128, 4, (2777,), group_reduce="sum", pool_k=5,
                                   score_mode="logits", k_keep=50),
-    # logits with the group max (the CUDA-core path), d = 64
+    # logits with the group max (signed maxima through order-preserving keys), d = 64
     "logits_groupmax_d64": S.Workload("v_logits_max", 98, 1, 8, 2, 64, 8, (1500,), group_reduce="max", pool_k=3,
                                       score_mode="logits", k_keep=40),
     # average pool in page mode: page max and page sum of the averaged scores
     "avg_pages_max": S.scaled(S.LLAMA8B_128K_PAGED, n_layers=2, prefix_lens=[8200], pool_type="avg"),
     "avg_pages_sum": S.scaled(S.LLAMA8B_128K_PAGED, n_layers=1, prefix_lens=[4100], pool_type="avg",
                               page_reduce="sum", k_keep=40),
-    # average pool on the CUDA-core kernels (group max with a window that is not a power of two)
-    "avg_cudacore_w24": S.Workload("v_avg_w24", 99, 1, 8, 2, 128, 24, (2000,), group_reduce="max", pool_k=7,
-                                   pool_type="avg", k_keep=100, n_clusters=4),
+    # average pool, group max with a window that is not a power of two (heads padded to 32 rows)
+    "avg_padded_w24": S.Workload("v_avg_w24", 99, 1, 8, 2, 128, 24, (2000,), group_reduce="max", pool_k=7,
+                                 pool_type="avg", k_keep=100, n_clusters=4),
+    # logits, group max, W = 12 padded to 16 rows, group of 8
+    "logits_groupmax_padded_w12": S.Workload("v_logits_max12", 110, 1, 16, 2, 128, 12, (2600,),
+                                             group_reduce="max", pool_k=5, score_mode="logits", k_keep=60),
+    # the CUDA-core kernels: group of 10 x 24 rows (padded beyond a 256-row tile), logits and average pool
+    "logits_avg_cudacore_g10w24": S.Workload("v_cc_g10", 111, 1, 20, 2, 128, 24, (1300,), group_reduce="max",
+                                             pool_k=7, pool_type="avg", score_mode="logits", k_keep=64),
     # logits summed over a group of 6 x 32 rows: 192 weighted rows and 64 padding rows in a 256-row tile
     "logits_rt256_padded": S.Workload("v_logits_256", 104, 1, 12, 2, 128, 32, (1900,), group_reduce="sum",
                                       pool_k=7, score_mode="logits", k_keep=64),
