@@ -76,8 +76,9 @@ struct TopkShared {
 
 // The k-th largest of arr[0, n) (1 <= k <= n, a short list in shared memory): *T and how many keys
 // equal to *T the top k take (*krem).  8-bit passes from the top digit; each keeps the keys that
-// match the digits chosen so far, counts their next digit (one shared histogram, one atomic per group
-// of lanes with equal digits) and chooses the digit the k-th key has.  With `passes` < 4 the result
+// match the digits chosen so far, counts their next digit (one shared histogram, one atomic per key:
+// on this GPU that beats grouping the lanes of equal digits by a warp match, even when every key of a
+// warp has the same digit) and chooses the digit the k-th key has.  With `passes` < 4 the result
 // is the k-th key's top 8 * passes bits with the rest zero: a key no larger than the k-th.  The two
 // histograms alternate, so a pass zeroes the next one's while it counts into its own.
 __device__ void select_short(const uint32_t* arr, int n, uint32_t k, TopkShared& sh, uint32_t* T, uint32_t* krem,
@@ -98,12 +99,7 @@ __device__ void select_short(const uint32_t* arr, int n, uint32_t k, TopkShared&
         key = arr[i];
         ok = (key & pmask) == prefix;
       }
-      const unsigned m = __ballot_sync(0xffffffffu, ok);
-      if (ok) {
-        const uint32_t digit = (key >> shift) & 255u;
-        const unsigned peers = __match_any_sync(m, digit);
-        if (lane == __ffs(peers) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(peers));
-      }
+      if (ok) atomicAdd(&hist[(key >> shift) & 255u], 1u);
     }
     __syncthreads();
     if (tid < 32) {   // one warp: lane l holds digits 255 - 8l .. 248 - 8l, scanned from the top
@@ -288,12 +284,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_kernel(const __grid_cons
           key = key_at(i);
           ok = (key & pmask) == prefix;
         }
-        const unsigned m = __ballot_sync(0xffffffffu, ok);
-        if (ok) {
-          const uint32_t digit = (key >> shift) & 255u;
-          const unsigned peers = __match_any_sync(m, digit);
-          if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hw[digit], (uint32_t)__popc(peers));
-        }
+        if (ok) atomicAdd(&hw[(key >> shift) & 255u], 1u);
       }
       __syncthreads();
       if (tid < 256) {
