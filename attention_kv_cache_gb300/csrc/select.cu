@@ -200,12 +200,23 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_kernel(const __grid_cons
       if (!SMEM) {
         // Rows read from memory: every key >= T0 into the list in index order.  Each warp counts its
         // contiguous segment's candidates, the counts give each warp its place, and a second read of
-        // the segment (now in L2) writes the keys and their positions.
-        const int seg = (n_cand + kWarps - 1) / kWarps;
-        const int s0 = min(n_cand, warp * seg), s1 = min(n_cand, s0 + seg);
+        // the segment (now in L2) writes the keys and their positions.  The segments are runs of
+        // 16-byte units of the row (the keys before the first 16-byte boundary go to warp 0, the last
+        // 0-3 keys to the last warp), four keys per lane and load.
+        const int head = min(n_cand, (int)((4u - (uint32_t)((reinterpret_cast<uintptr_t>(src) >> 2) & 3u)) & 3u));
+        const int m4 = (n_cand - head) >> 2;
+        const int tail0 = head + 4 * m4;
+        const float4* s4 = reinterpret_cast<const float4*>(src + head);
+        const int u0 = (int)(((int64_t)warp * m4) / kWarps), u1 = (int)(((int64_t)(warp + 1) * m4) / kWarps);
         uint32_t c = 0;
-#pragma unroll 8
-        for (int i = s0 + lane; i < s1; i += 32) c += key_at(i) >= T0 ? 1u : 0u;
+        if (warp == 0 && lane < head) c += f2key(src[lane]) >= T0 ? 1u : 0u;
+        if (warp == kWarps - 1 && lane < n_cand - tail0) c += f2key(src[tail0 + lane]) >= T0 ? 1u : 0u;
+#pragma unroll 4
+        for (int u = u0 + lane; u < u1; u += 32) {
+          const float4 f = s4[u];
+          c += (f2key(f.x) >= T0 ? 1u : 0u) + (f2key(f.y) >= T0 ? 1u : 0u) + (f2key(f.z) >= T0 ? 1u : 0u) +
+               (f2key(f.w) >= T0 ? 1u : 0u);
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
         if (lane == 0) warp_cnt[warp] = make_uint2(c, 0u);
@@ -217,27 +228,54 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_kernel(const __grid_cons
         }
         if (nf >= (uint32_t)a.k && nf <= (uint32_t)a.cap) {   // the row's k-th key is among them
           uint32_t* cand_idx = cand + a.cap;
-          constexpr int U = 8;                 // rounds whose loads are issued together
-          for (int base = s0; base < s1; base += 32 * U) {
-            uint32_t keys[U];
+          auto put1 = [&](bool live, int i) {     // one key per lane, lanes in index order
+            const uint32_t key = live ? f2key(src[i]) : 0u;
+            const bool p = live && key >= T0;
+            const unsigned m = __ballot_sync(0xffffffffu, p);
+            if (p) {
+              const uint32_t at = pos + (uint32_t)__popc(m & lower);
+              cand[at] = key;
+              cand_idx[at] = (uint32_t)i;
+            }
+            pos += (uint32_t)__popc(m);
+          };
+          if (warp == 0) put1(lane < head, lane);
+          constexpr int U = 4;                 // rounds of 32 units whose loads are issued together
+          for (int base = u0; base < u1; base += 32 * U) {
+            float4 f[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-              const int i = base + 32 * u + lane;
-              keys[u] = i < s1 ? key_at(i) : 0u;
+            for (int r = 0; r < U; ++r) {
+              const int u = base + 32 * r + lane;
+              f[r] = u < u1 ? s4[u] : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-              const int i = base + 32 * u + lane;
-              const bool p = i < s1 && keys[u] >= T0;
-              const unsigned m = __ballot_sync(0xffffffffu, p);
-              if (p) {
-                const uint32_t at = pos + (uint32_t)__popc(m & lower);
-                cand[at] = keys[u];
-                cand_idx[at] = (uint32_t)i;
+            for (int r = 0; r < U; ++r) {
+              const int u = base + 32 * r + lane;
+              const bool live = u < u1;
+              const uint32_t kk[4] = {f2key(f[r].x), f2key(f[r].y), f2key(f[r].z), f2key(f[r].w)};
+              bool p[4];
+              uint32_t before = 0, all = 0;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                p[q] = live && kk[q] >= T0;
+                const unsigned m = __ballot_sync(0xffffffffu, p[q]);
+                before += (uint32_t)__popc(m & lower);
+                all += (uint32_t)__popc(m);
               }
-              pos += (uint32_t)__popc(m);
+              // the lane's four keys follow every key of the lanes before it
+              uint32_t at = pos + before;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                if (p[q]) {
+                  cand[at] = kk[q];
+                  cand_idx[at] = (uint32_t)(head + 4 * u + q);
+                  ++at;
+                }
+              }
+              pos += all;
             }
           }
+          if (warp == kWarps - 1) put1(lane < n_cand - tail0, tail0 + lane);
           __syncthreads();
           select_short(cand, (int)nf, (uint32_t)a.k, sh, &prefix, &krem);
           n_list = (int)nf;
