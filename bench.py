@@ -40,7 +40,7 @@ def parse():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--layers", type=int, default=0,
                    help="run only this many layers of the workload (small cases for profiler captures)")
-    p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--cpu-units", type=int, default=0,
                    help="(layer, KV head) units in the CPU-baseline sample (default: one per host core)")
     p.add_argument("--no-cpu", action="store_true")
