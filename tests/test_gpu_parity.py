@@ -38,6 +38,10 @@ CASES = {
     # W = 40 padded to 64 rows per head, group of 4: a 256-row tile with 24 dead rows in every head
     "w40_max_padded_rt256": S.Workload("edge_w40", 107, 1, 8, 2, 128, 40, (2345,), group_reduce="max", pool_k=7,
                                        k_keep=90, n_clusters=4),
+    # W = 48 padded to 64 rows, group of 4 (256 tile rows), page mode with P = 16: the paired
+    # epilogue over padded heads, page max of the pooled scores, recency pages
+    "w48_max_padded_pages_rt256": S.Workload("edge_w48p", 112, 1, 8, 2, 128, 48, (4100,), group_reduce="max",
+                                             pool_k=5, k_keep=24, page_size=16, n_recent=3, n_clusters=4),
     # W = 5 padded to 8 rows, group of 4, d = 64
     "w5_max_padded_d64": S.Workload("edge_w5", 108, 1, 8, 2, 64, 5, (3001,), group_reduce="max", pool_k=3,
                                     k_keep=40, n_clusters=4),

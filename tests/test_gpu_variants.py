@@ -42,6 +42,11 @@ V = {
     # logits, group max, W = 12 padded to 16 rows, group of 8
     "logits_groupmax_padded_w12": S.Workload("v_logits_max12", 110, 1, 16, 2, 128, 12, (2600,),
                                              group_reduce="max", pool_k=5, score_mode="logits", k_keep=60),
+    # logits, group max, W = 40 padded to 64 rows, group of 3: 192 of 256 tile rows, so the paired
+    # epilogue's last 64 columns are a head that exists only as padding and must be left out of the
+    # signed maxima
+    "logits_groupmax_padded_rt256": S.Workload("v_logits_max40", 113, 1, 6, 2, 128, 40, (2300,),
+                                               group_reduce="max", pool_k=3, score_mode="logits", k_keep=48),
     # the CUDA-core kernels: group of 10 x 24 rows (padded beyond a 256-row tile), logits and average pool
     "logits_avg_cudacore_g10w24": S.Workload("v_cc_g10", 111, 1, 20, 2, 128, 24, (1300,), group_reduce="max",
                                              pool_k=7, pool_type="avg", score_mode="logits", k_keep=64),
