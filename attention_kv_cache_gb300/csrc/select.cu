@@ -409,7 +409,8 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_kernel(const __grid_cons
 
 // ------------------------------------------------------------------------ aggregation
 constexpr int kCombThreads = 256;
-constexpr int kCombChunk = 1024;
+constexpr int kCombChunk = 256;    // tokens per pooling CTA: about one per thread, so that a row's
+                                    // layers are read by many threads at once
 
 struct AggArgs {
   const float* scores;      // raw group scores, per sequence [n_layers][h_kv][L]
@@ -470,14 +471,14 @@ __global__ void __launch_bounds__(kCombThreads) agg_pool(const __grid_constant__
     if (a.layer_op == KVSEL_LAYERS_EACH) {
       v = head_value(a, si, a.lo + ol, oh, tt);
     } else {
-      // layers in batches of 8 whose loads are all issued before they are combined, in layer order
+      // layers in batches of 16 whose loads are all issued before they are combined, in layer order
       // (the same arithmetic, in the same order, as one layer at a time)
       const bool mx = a.layer_op == KVSEL_LAYERS_MAX;
       float acc = mx ? -INFINITY : 0.f;
-      for (int l0 = a.lo; l0 <= a.hi; l0 += 8) {
-        float x[8], nv[8];
+      for (int l0 = a.lo; l0 <= a.hi; l0 += 16) {
+        float x[16], nv[16];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < 16; ++u) {
           const int layer = l0 + u;
           x[u] = 0.f;
           nv[u] = 1.f;
@@ -487,7 +488,7 @@ __global__ void __launch_bounds__(kCombThreads) agg_pool(const __grid_constant__
           }
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
+        for (int u = 0; u < 16; ++u)
           if (l0 + u <= a.hi) acc = mx ? fmaxf(acc, x[u]) : acc + x[u] / nv[u];
       }
       v = mx ? acc : acc * inv_n;
