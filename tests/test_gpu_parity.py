@@ -85,6 +85,12 @@ def run_case(w, cuda):
 def test_path_matches_oracle(name, cuda):
     w = CASES[name]
     inp, pipe = run_case(w, cuda)
+    check_against_oracle(name, w, inp, pipe)
+
+
+def check_against_oracle(name, w, inp, pipe):
+    """Scores (pooled, raw, combined, pages), selections, compacted rows and the block-union table
+    of one run of the pipeline against the oracle."""
     for b in range(w.batch):
         L = w.prefix_lens[b]
         ref = O.run_sequence(w, inp.q[b], inp.k[b], inp.v[b], with_gather=False)
