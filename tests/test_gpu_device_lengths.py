@@ -133,3 +133,15 @@ def test_device_length_out_of_range_reported(cuda):
     pipe.run(q, k, v)
     assert K.kvsel_read_device_error(pipe.ws) == K.OK
     assert bool((pipe.idx >= 0).all())
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_shapes_device_lengths_bit_equal(seed, cuda):
+    """The random shapes of the fuzz tests with their lengths only on the device (bound a little above
+    the longest): every output bit-equal to the host-length call's."""
+    import random
+    from tests.test_gpu_fuzz import draw
+    w = draw(seed)
+    len_max = max(w.prefix_lens) + random.Random(seed).choice([0, 1, 17, 300])
+    inp, host, dev = _run_both(w, len_max, cuda)
+    _assert_same(host, dev, w)
