@@ -409,22 +409,33 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_kernel(const __grid_cons
 
 // ------------------------------------------------------------------------ aggregation
 constexpr int kCombThreads = 256;
-constexpr int kCombChunk = 256;    // tokens per pooling CTA: about one per thread, so that a row's
-                                    // layers are read by many threads at once
+// Tokens per pooling CTA: about one per thread when every token reads many layers (so that they are
+// read by many threads at once), four per thread when each token reads one layer's heads.
+constexpr int kCombChunkLayers = 256;
+constexpr int kCombChunkMax = 1024;
 
 struct AggArgs {
   const float* scores;      // raw group scores, per sequence [n_layers][h_kv][L]
   float* norms;             // [batch][hi - lo + 1][n_h] L1 norms (L1 mean only)
   float* out;               // per sequence [n_l][n_h][L]
   int32_t n_layers, h_kv, lo, hi, layer_op, head_op, n_l, n_h, pool_k, pool_type;
+  int32_t chunk;            // tokens per pooling CTA (kCombChunkLayers or kCombChunkMax)
 };
 
 // Value of (layer, output head oh) at token tt: one KV head, or the sum over all of them.
 __device__ __forceinline__ float head_value(const AggArgs& a, const SeqInfo& si, int layer, int oh, int tt) {
   const float* base = a.scores + si.s_off + (int64_t)layer * a.h_kv * si.L + tt;
   if (a.head_op == KVSEL_HEADS_EACH) return base[(int64_t)oh * si.L];
+  // heads in batches of 8 whose loads are all issued before they are added, in head order
   float acc = 0.f;
-  for (int g = 0; g < a.h_kv; ++g) acc += base[(int64_t)g * si.L];
+  for (int g0 = 0; g0 < a.h_kv; g0 += 8) {
+    float x[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) x[u] = g0 + u < a.h_kv ? base[(int64_t)(g0 + u) * si.L] : 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (g0 + u < a.h_kv) acc += x[u];
+  }
   return acc;
 }
 
@@ -455,13 +466,13 @@ __global__ void __launch_bounds__(kCombThreads) agg_norms(const __grid_constant_
 __global__ void __launch_bounds__(kCombThreads) agg_pool(const __grid_constant__ AggArgs a,
                                                          const __grid_constant__ SeqTable tp) {
   const SeqTable& t = real_table(tp);
-  __shared__ float S[kCombChunk + 64];
+  __shared__ float S[kCombChunkMax + 64];
   const int b = blockIdx.z;
   const int ol = blockIdx.y / a.n_h, oh = blockIdx.y % a.n_h;
   const SeqInfo si = t.s[b];   // a copy: loads once, whatever the table lives in
-  const int a0 = blockIdx.x * kCombChunk;
+  const int a0 = blockIdx.x * a.chunk;
   if (a0 >= si.L) return;
-  const int a1 = min(si.L, a0 + kCombChunk);
+  const int a1 = min(si.L, a0 + a.chunk);
   const int pr = (a.pool_k - 1) / 2;
   const int ea = max(0, a0 - pr), eb = min(si.L, a1 + pr);
   const int nr = a.hi - a.lo + 1;
@@ -582,7 +593,8 @@ kvsel_status launch_aggregate(const kvsel_desc& d, const SeqTable& t, const floa
   }
   int64_t lmax = 0;   // real lengths, or their bound with device lengths
   for (int b = 0; b < d.batch; ++b) lmax = t.s[b].L > lmax ? t.s[b].L : lmax;
-  dim3 grid((unsigned)((lmax + kCombChunk - 1) / kCombChunk), (unsigned)(a.n_l * a.n_h), d.batch);
+  a.chunk = layer_op == KVSEL_LAYERS_EACH ? kCombChunkMax : kCombChunkLayers;
+  dim3 grid((unsigned)((lmax + a.chunk - 1) / a.chunk), (unsigned)(a.n_l * a.n_h), d.batch);
   TraceScope ts("aggregate_pool", s);
   agg_pool<<<grid, kCombThreads, 0, s>>>(a, t);
   return launch_status();
