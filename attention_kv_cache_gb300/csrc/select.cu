@@ -18,7 +18,9 @@
 namespace kvsel {
 namespace {
 
-constexpr int kTopkThreads = 512;     // two CTAs per SM
+// Threads per top-k CTA: 512 (two CTAs per SM) when the rows fit one wave of them; 256 (four per SM,
+// each row's passes longer) when there are more rows than that, so that more rows run at once.
+constexpr int kTopkThreadsMax = 512;
 constexpr int kSmemKeysMax = 40960;   // rows up to this length are staged in shared memory
 
 __device__ __forceinline__ uint32_t f2key(float f) {
@@ -66,11 +68,12 @@ struct TopkArgs {
 
 constexpr int kSample = 1024;
 
+template <int NT>
 struct TopkShared {
   uint32_t hist[2][256];                     // select_short: one histogram per pass parity
-  uint32_t hist_w[kTopkThreads / 32][256];   // one histogram per warp: no cross-warp atomics
+  uint32_t hist_w[NT / 32][256];             // one histogram per warp: no cross-warp atomics
   unsigned long long scan_sh[32];
-  uint2 warp_cnt[kTopkThreads / 32];
+  uint2 warp_cnt[NT / 32];
   uint32_t sel_digit, sel_gt, n_found;
 };
 
@@ -81,7 +84,8 @@ struct TopkShared {
 // warp has the same digit) and chooses the digit the k-th key has.  With `passes` < 4 the result
 // is the k-th key's top 8 * passes bits with the rest zero: a key no larger than the k-th.  The two
 // histograms alternate, so a pass zeroes the next one's while it counts into its own.
-__device__ void select_short(const uint32_t* arr, int n, uint32_t k, TopkShared& sh, uint32_t* T, uint32_t* krem,
+template <int NT>
+__device__ void select_short(const uint32_t* arr, int n, uint32_t k, TopkShared<NT>& sh, uint32_t* T, uint32_t* krem,
                              int passes = 4) {
   const int tid = threadIdx.x, lane = tid & 31;
   uint32_t prefix = 0, pmask = 0, rem = k;
@@ -91,7 +95,7 @@ __device__ void select_short(const uint32_t* arr, int n, uint32_t k, TopkShared&
     const int shift = 24 - 8 * pass;
     uint32_t* hist = sh.hist[pass & 1];
     if (tid < 256) sh.hist[(pass + 1) & 1][tid] = 0;
-    for (int base = 0; base < n; base += kTopkThreads) {
+    for (int base = 0; base < n; base += NT) {
       const int i = base + tid;
       uint32_t key = 0;
       bool ok = false;
@@ -135,12 +139,12 @@ __device__ void select_short(const uint32_t* arr, int n, uint32_t k, TopkShared&
   *krem = rem;
 }
 
-template <bool SMEM>
-__global__ void __launch_bounds__(kTopkThreads, 2) topk_kernel(const __grid_constant__ TopkArgs a,
+template <bool SMEM, int NT>
+__global__ void __launch_bounds__(NT, 1024 / NT) topk_kernel(const __grid_constant__ TopkArgs a,
                                                             const __grid_constant__ SeqTable tp) {
   const SeqTable& t = real_table(tp);
   extern __shared__ __align__(16) uint32_t keys_sm[];   // [stage] staged keys, then [cap] candidates
-  __shared__ TopkShared sh;
+  __shared__ TopkShared<NT> sh;
   uint32_t* hist = sh.hist[0];
   auto& hist_w = sh.hist_w;
   unsigned long long* scan_sh = sh.scan_sh;
@@ -165,14 +169,14 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_kernel(const __grid_cons
       const float4* s4 = reinterpret_cast<const float4*>(src);
       uint4* k4 = reinterpret_cast<uint4*>(keys_sm);
 #pragma unroll 4
-      for (int i = tid; i < n4; i += kTopkThreads) {
+      for (int i = tid; i < n4; i += NT) {
         const float4 f = s4[i];
         k4[i] = make_uint4(f2key(f.x), f2key(f.y), f2key(f.z), f2key(f.w));
       }
-      for (int i = 4 * n4 + tid; i < n_cand; i += kTopkThreads) keys_sm[i] = f2key(src[i]);
+      for (int i = 4 * n4 + tid; i < n_cand; i += NT) keys_sm[i] = f2key(src[i]);
     } else {
 #pragma unroll 8
-      for (int i = tid; i < n_cand; i += kTopkThreads) keys_sm[i] = f2key(src[i]);
+      for (int i = tid; i < n_cand; i += NT) keys_sm[i] = f2key(src[i]);
     }
   }
   __syncthreads();
@@ -184,7 +188,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_kernel(const __grid_cons
   int n_list = -1;     // >= 0: the list holds every candidate in index order and the emission walks it
   const int lane = tid & 31, warp = tid >> 5;
   const unsigned lower = (1u << lane) - 1u;
-  constexpr int kWarps = kTopkThreads / 32;
+  constexpr int kWarps = NT / 32;
   if (a.k > 0 && a.cap >= kSample && n_cand >= (SMEM ? 12 : 4) * kSample) {
     // A threshold read off an evenly spaced sample: about k * S / n_cand sample keys lie at or above the
     // row's k-th key; the sample's r0-th largest key, r0 1.25 times that plus three standard deviations,
@@ -193,7 +197,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_kernel(const __grid_cons
     const float e = (float)a.k * (float)kSample / (float)n_cand;
     const int r0 = (int)(1.25f * e + 3.0f * sqrtf(e) + 4.0f);
     if (r0 <= kSample) {
-      for (int s = tid; s < kSample; s += kTopkThreads) cand[s] = key_at((int)(((int64_t)s * n_cand) / kSample));
+      for (int s = tid; s < kSample; s += NT) cand[s] = key_at((int)(((int64_t)s * n_cand) / kSample));
       __syncthreads();
       uint32_t T0, rem0;
       select_short(cand, kSample, (uint32_t)r0, sh, &T0, &rem0, 2);
@@ -287,7 +291,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_kernel(const __grid_cons
         // staged rows: every key >= T0 into the list (positions taken a warp at a time); keys past the
         // capacity are counted but not stored, and the list is then not used
 #pragma unroll 4
-        for (int base = 0; base < n_cand; base += kTopkThreads) {
+        for (int base = 0; base < n_cand; base += NT) {
           const int i = base + tid;
           const uint32_t key = i < n_cand ? key_at(i) : 0u;
           const bool p = i < n_cand && key >= T0;
@@ -314,7 +318,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_kernel(const __grid_cons
       for (int j = tid & 31; j < 256; j += 32) hw[j] = 0;
       __syncwarp();
 #pragma unroll 4
-      for (int base = 0; base < n_cand; base += kTopkThreads) {
+      for (int base = 0; base < n_cand; base += NT) {
         const int i = base + tid;
         uint32_t key = 0;
         bool ok = false;
@@ -328,7 +332,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_kernel(const __grid_cons
       if (tid < 256) {
         uint32_t c = 0;
 #pragma unroll 8
-        for (int w = 0; w < kTopkThreads / 32; ++w) c += hist_w[w][tid];
+        for (int w = 0; w < NT / 32; ++w) c += hist_w[w][tid];
         hist[tid] = c;
       }
       __syncthreads();
@@ -404,7 +408,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) topk_kernel(const __grid_cons
     }
   }
   // recency pages, then (when appended) window pages or window tokens: the indices from n_cand on
-  for (int i = tid; i < a.n_sel - a.k; i += kTopkThreads) out[a.k + i] = n_cand + i;
+  for (int i = tid; i < a.n_sel - a.k; i += NT) out[a.k + i] = n_cand + i;
 }
 
 // ------------------------------------------------------------------------ aggregation
@@ -553,18 +557,32 @@ kvsel_status launch_topk(const kvsel_desc& d, const SeqTable& t, int rows, int k
   // is several standard deviations out, and then the whole-row select runs) within what shared memory
   // has left beside the staged row and the kernel's own arrays
   const int64_t entry = staged ? 1 : 2;      // a key, or a key and its position
-  const int64_t avail = (((int64_t)optin - (int64_t)sizeof(TopkShared) - 256) / 4 - a.stage) / entry;
+  const int64_t avail = (((int64_t)optin - (int64_t)sizeof(TopkShared<kTopkThreadsMax>) - 256) / 4 - a.stage) / entry;
   const int64_t cap = std::min<int64_t>(std::max<int64_t>(kSample, 2 * (int64_t)k + 2048), avail);
   a.cap = cap >= kSample ? (int32_t)cap : 0;
   const size_t smem = (size_t)(a.stage + entry * a.cap) * sizeof(uint32_t);
   const int grid = d.batch * rows;
+  // more rows than one wave of 512-thread CTAs (two per SM): 256-thread CTAs, four per SM
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KVSEL_ERR_CUDA;
+  const bool many = grid > 2 * sms;
   TraceScope ts("topk_radix", s);
   if (staged) {
-    if (set_smem((const void*)topk_kernel<true>, smem) != cudaSuccess) return KVSEL_ERR_CUDA;
-    topk_kernel<true><<<grid, kTopkThreads, smem, s>>>(a, t);
+    if (many) {
+      if (set_smem((const void*)topk_kernel<true, 256>, smem) != cudaSuccess) return KVSEL_ERR_CUDA;
+      topk_kernel<true, 256><<<grid, 256, smem, s>>>(a, t);
+    } else {
+      if (set_smem((const void*)topk_kernel<true, 512>, smem) != cudaSuccess) return KVSEL_ERR_CUDA;
+      topk_kernel<true, 512><<<grid, 512, smem, s>>>(a, t);
+    }
   } else {
-    if (set_smem((const void*)topk_kernel<false>, smem) != cudaSuccess) return KVSEL_ERR_CUDA;
-    topk_kernel<false><<<grid, kTopkThreads, smem, s>>>(a, t);
+    if (many) {
+      if (set_smem((const void*)topk_kernel<false, 256>, smem) != cudaSuccess) return KVSEL_ERR_CUDA;
+      topk_kernel<false, 256><<<grid, 256, smem, s>>>(a, t);
+    } else {
+      if (set_smem((const void*)topk_kernel<false, 512>, smem) != cudaSuccess) return KVSEL_ERR_CUDA;
+      topk_kernel<false, 512><<<grid, 512, smem, s>>>(a, t);
+    }
   }
   return launch_status();
 }

@@ -19,7 +19,9 @@ def _ws(K, desc, cuda):
 
 @pytest.mark.parametrize("rows,n,k,ties", [(3, 100, 7, True), (5, 4097, 1000, True), (2, 33000, 1024, False),
                                            (2, 50000, 4096, True), (4, 300, 300, True), (2, 64, 0, False),
-                                           (3, 70000, 1, True)])
+                                           (3, 70000, 1, True),
+                                           # more rows than one wave of 512-thread CTAs: the 256-thread kernels
+                                           (400, 3000, 200, True), (330, 16384, 1024, True)])
 def test_topk_token_mode_exact(rows, n, k, ties, cuda):
     """Top-k with ties to the lower index, both decided in fp32 (the kernel's precision)."""
     from attention_kv_cache_gb300 import kvsel as K
