@@ -710,7 +710,10 @@ __device__ __forceinline__ float window_avg(const float* S, int ta, int tb, int 
 #pragma unroll 8
     for (int y = lo; y <= hi; ++y) acc += S[y - ta];
   }
-  return acc / (float)(hi - lo + 1);
+  // a full window divides by the constant 2 pr + 1 (one multiply by its reciprocal); the segment's
+  // first and last r positions by their own count
+  const int cnt = hi - lo + 1;
+  return cnt == 2 * pr + 1 ? acc * (1.0f / (float)(2 * pr + 1)) : acc / (float)cnt;
 }
 
 __device__ void pool_segment(const float* S, int ta, int tb, int a0, int a1, int pr, int P, int page_reduce,
