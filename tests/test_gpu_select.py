@@ -148,6 +148,7 @@ def test_topk_first_call_in_fresh_process(cuda):
 
 
 @pytest.mark.parametrize("pattern", ["smooth", "top_on_sample_grid", "top_off_sample_grid", "ties_at_threshold",
+                                     "top_in_one_segment",
                                      "long_row_global"])
 def test_topk_candidate_path_exact(pattern, cuda):
     """Rows long enough for the sampled threshold: the candidate list (smooth scores; the top keys
@@ -165,6 +166,8 @@ def test_topk_candidate_path_exact(pattern, cuda):
         s[:, 1::stride] += 10.0
     elif pattern == "ties_at_threshold":
         s = torch.round(s * 512) / 512
+    elif pattern == "top_in_one_segment":                # one warp's segment holds a third of the
+        s[:, :600] += 10.0                               # candidates: its placement offsets dominate
     s = s.float()
     desc = K.make_desc(n_layers=rows, h_q=1, h_kv=1, head_dim=128, window=W, prefix_lens=[n])
     idx = torch.full((rows, k + W), -7, dtype=torch.int32, device=cuda)
