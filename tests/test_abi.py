@@ -71,6 +71,19 @@ def test_bad_descriptor_rejected(kw, status):
     assert K.raw_call("kvsel_score", ctypes.byref(d), 16, 16, 16, 16, 256, 1 << 40, None) == status
 
 
+@pytest.mark.parametrize("h_q,h_kv,window,reduce", [
+    (8, 2, 24, K.REDUCE_MAX),      # heads padded to 32 rows: 128 tile rows
+    (8, 2, 40, K.REDUCE_MAX),      # padded to 64 rows: 256 tile rows
+    (20, 2, 24, K.REDUCE_MAX),     # 240 rows, 320 once padded: the CUDA-core kernels
+    (64, 2, 8, K.REDUCE_SUM),      # 256 rows of 8-row heads
+    (2, 2, 64, K.REDUCE_MEAN),     # one head of the widest window
+])
+def test_supported_group_shapes_accepted(h_q, h_kv, window, reduce):
+    """Every shape within (h_q / h_kv) W <= 256 has a kernel, whatever its padding."""
+    d = _desc(h_q=h_q, h_kv=h_kv, window=window, group_reduce=reduce)
+    assert K.kvsel_workspace_size(d) > 0
+
+
 def test_null_and_misaligned_pointers_rejected():
     d = _desc()
     ws = K.kvsel_workspace_size(d)
