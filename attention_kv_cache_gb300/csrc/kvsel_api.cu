@@ -147,6 +147,24 @@ static kvsel_status check_desc(const kvsel_desc* d) {
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+// A source the gather kernel may read: memory of the current device (or managed), or pinned host
+// memory mapped at the same address (on a Grace-Blackwell node the kernel then reads only the kept
+// rows over the host link).  Anything else — pageable or foreign memory, another device's — is
+// refused on the host instead of being dereferenced by a kernel.
+static bool device_readable(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (at.type == cudaMemoryTypeDevice) return at.device == dev;
+  if (at.type == cudaMemoryTypeManaged) return true;
+  if (at.type == cudaMemoryTypeHost) return at.devicePointer == p;
+  return false;
+}
+
 kvsel_status check_score_args(const kvsel_desc* desc, const void* q, const void* k, const float* scores,
                               const float* page_scores) {
   kvsel_status st = check_desc(desc);
@@ -496,6 +514,7 @@ kvsel_status kvsel_compact(const kvsel_desc* desc, const void* k, const void* v,
   if (ws != nullptr && ((uintptr_t)ws % KVSEL_WS_ALIGN) != 0) return KVSEL_ERR_WORKSPACE;
   if (lens_on_device(d) && ws == nullptr) return KVSEL_ERR_WORKSPACE;
   if (n_sel == 0) return KVSEL_OK;
+  if (!device_readable(k) || !device_readable(v)) return KVSEL_ERR_INVALID_ARG;
   SeqTable t;
   if ((st = make_table(d, (int64_t)d.n_layers * d.h_kv, ws, stream, &t)) != KVSEL_OK) return st;
   return launch_compact(d, t, k, v, idx, idx_layers, d.h_kv, 0, d.n_layers, n_sel, k_out, v_out,
@@ -520,6 +539,7 @@ kvsel_status kvsel_compact_layers(const kvsel_desc* desc, const void* k, const v
   if (ws != nullptr && ((uintptr_t)ws % KVSEL_WS_ALIGN) != 0) return KVSEL_ERR_WORKSPACE;
   if (lens_on_device(d) && ws == nullptr) return KVSEL_ERR_WORKSPACE;
   if (n_sel == 0) return KVSEL_OK;
+  if (!device_readable(k) || !device_readable(v)) return KVSEL_ERR_INVALID_ARG;
   SeqTable t;
   if ((st = make_table(d, (int64_t)d.n_layers * d.h_kv, ws, stream, &t)) != KVSEL_OK) return st;
   return launch_compact(d, t, k, v, idx, idx_layers, idx_heads, layer_lo, n_layers_out, n_sel, k_out, v_out,
@@ -652,6 +672,7 @@ kvsel_status kvsel_claa_select(const kvsel_desc* desc, const kvsel_claa_params* 
       prune_scores == nullptr || idx == nullptr || prune_idx == nullptr || k_out == nullptr || v_out == nullptr)
     return KVSEL_ERR_INVALID_ARG;
   if (ws == nullptr || ((uintptr_t)ws % KVSEL_WS_ALIGN) != 0 || ws_bytes < sh.ws_bytes) return KVSEL_ERR_WORKSPACE;
+  if (sh.n_sel > 0 && (!device_readable(k) || !device_readable(v))) return KVSEL_ERR_INVALID_ARG;  // before any launch
   const int64_t L = d.prefix_lens[0];
   const kvsel_desc raw = claa_sub(d, *p, true);
   const kvsel_desc pooled = claa_sub(d, *p, false);

@@ -266,7 +266,13 @@ KVSEL_API kvsel_status kvsel_topk(const kvsel_desc* desc, const float* scores, i
  * of page idx[r] (rows past L_b + W are written as zero).  A bit copy:
  * outputs equal inputs exactly.
  *
- *   k, v          [device] bf16 caches, layout above
+ *   k, v          [device] bf16 caches, layout above; either may instead be pinned
+ *                 host memory mapped at the same address (cudaHostAlloc, or
+ *                 cudaHostRegister with cudaHostRegisterMapped): the kernel then
+ *                 reads only the kept rows over the host link, so a cache held on
+ *                 the host never has to be copied whole.  Any other pointer (pageable
+ *                 host memory, another device's memory) is rejected with
+ *                 KVSEL_ERR_INVALID_ARG before the launch.
  *   idx           [device] int32 [batch][idx_layers][h_kv][n_sel] as written by kvsel_topk;
  *                 idx_layers == 1 applies one selection to every layer
  *   k_out, v_out  [device] bf16 out [batch][n_layers][h_kv][n_sel * P][d]
@@ -289,6 +295,7 @@ KVSEL_API kvsel_status kvsel_compact(const kvsel_desc* desc, const void* k, cons
  * applies one selection to every KV head (the all-head scores of CLAA,
  * FastKV and GemFilter rank tokens once per layer), otherwise idx_heads == h_kv.
  *
+ *   k, v          as for kvsel_compact (device, or mapped pinned host memory)
  *   k_out, v_out  [device] bf16 out [batch][n_layers_out][h_kv][n_sel * P][d]
  *   ws            [device] workspace or NULL (errors as for kvsel_compact)
  */
@@ -350,7 +357,8 @@ KVSEL_API kvsel_status kvsel_attend(const kvsel_desc* desc, const void* q, int32
  * The descriptor covers every layer of the prompt (batch 1, host prefix length, token mode,
  * group_reduce KVSEL_REDUCE_SUM, score_mode KVSEL_SCORE_SOFTMAX).  kvsel_claa_shape returns the
  * sizes the outputs need; kvsel_claa_select runs the schedule:
- *   q, k, v        [device] bf16, layouts above, all n_layers layers
+ *   q, k, v        [device] bf16, layouts above, all n_layers layers; v is only gathered, so it
+ *                  may be mapped pinned host memory (as for kvsel_compact)
  *   scores         [device] fp32 out [n_scored][h_kv][L]: raw group scores of layers m .. l_p
  *   layer_scores   [device] fp32 out [n_scored][L]: pooled all-head score of each scored layer
  *   prune_scores   [device] fp32 out [L]: pooled token-wise max over the buffer

@@ -88,6 +88,41 @@ def test_compact_bit_exact_and_bounds(P, cuda):
     assert torch.all(ko[0, 1, 0, 5 * P:6 * P] == 0) and torch.all(ko[0, 2, 1, 0:P] == 0)
 
 
+@pytest.mark.parametrize("P", [1, 16])
+def test_compact_from_pinned_host_memory(P, cuda):
+    """K and V in mapped pinned host memory: the gather reads the kept rows over the host link and
+    writes exactly what it writes from device memory; pageable memory is refused before any launch."""
+    from attention_kv_cache_gb300 import kvsel as K
+    w = S.Workload("gather_host", 96, 3, 4, 2, 128, 16, (2000,), k_keep=20, page_size=P, n_recent=1 if P > 1 else 0)
+    inp = S.make_inputs(w, "cpu")
+    n_keys = 2000 + 16
+    lim = n_keys if P == 1 else -(-n_keys // P)
+    n_sel = 37
+    idx = torch.randint(0, lim, (1, w.n_layers, w.h_kv, n_sel), generator=torch.Generator().manual_seed(5),
+                        dtype=torch.int32).to(cuda)
+    desc = K.make_desc(n_layers=w.n_layers, h_q=w.h_q, h_kv=w.h_kv, head_dim=128, window=16, prefix_lens=[2000],
+                       page_size=P)
+    kd, vd = inp.k[0].to(cuda), inp.v[0].to(cuda)
+    kh, vh = inp.k[0].contiguous().pin_memory(), inp.v[0].contiguous().pin_memory()
+    ws = _ws(K, desc, cuda)
+    out = lambda: torch.full((1, w.n_layers, w.h_kv, n_sel * P, 128), 7.0, dtype=torch.bfloat16, device=cuda)
+    ko, vo, ko2, vo2 = out(), out(), out(), out()
+    K.kvsel_compact(desc, kd, vd, idx, w.n_layers, n_sel, ko, vo, ws)
+    K.kvsel_compact(desc, kd, vh, idx, w.n_layers, n_sel, ko2, vo2, ws)         # V on the host
+    torch.cuda.synchronize()
+    assert K.kvsel_read_device_error(ws) == K.OK
+    assert torch.equal(ko, ko2) and torch.equal(vo, vo2)
+    K.kvsel_compact(desc, kh, vh, idx, w.n_layers, n_sel, ko2, vo2, ws)         # both on the host
+    assert K.kvsel_read_device_error(ws) == K.OK
+    assert torch.equal(ko, ko2) and torch.equal(vo, vo2)
+    pageable = inp.v[0].contiguous()
+    assert not pageable.is_pinned()
+    n0 = K.kvsel_launch_count()
+    with pytest.raises(K.KvselError) as e:
+        K.kvsel_compact(desc, kd, pageable, idx, w.n_layers, n_sel, ko2, vo2, ws)
+    assert e.value.status == K.ERR_INVALID_ARG and K.kvsel_launch_count() == n0
+
+
 def test_pagetable_full_size_ragged(cuda):
     """Block union over the ragged batch's full mask (8 sequences, 32 layers, 16 Q blocks)."""
     from attention_kv_cache_gb300 import kvsel as K
