@@ -151,18 +151,23 @@ static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 // memory mapped at the same address (on a Grace-Blackwell node the kernel then reads only the kept
 // rows over the host link).  Anything else — pageable or foreign memory, another device's — is
 // refused on the host instead of being dereferenced by a kernel.
+// The queries are host-side and not stream-ordered: while a stream capture is under way they run
+// with this thread's capture mode relaxed, so that they neither fail nor invalidate the capture.
 static bool device_readable(const void* p) {
+  cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+  const bool swapped = cudaThreadExchangeStreamCaptureMode(&mode) == cudaSuccess;
   cudaPointerAttributes at;
+  int dev = -1;
+  bool ok = false;
   if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
     (void)cudaGetLastError();
-    return false;
+  } else if (cudaGetDevice(&dev) == cudaSuccess) {
+    if (at.type == cudaMemoryTypeDevice) ok = at.device == dev;
+    else if (at.type == cudaMemoryTypeManaged) ok = true;
+    else if (at.type == cudaMemoryTypeHost) ok = at.devicePointer == p;
   }
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  if (at.type == cudaMemoryTypeDevice) return at.device == dev;
-  if (at.type == cudaMemoryTypeManaged) return true;
-  if (at.type == cudaMemoryTypeHost) return at.devicePointer == p;
-  return false;
+  if (swapped) (void)cudaThreadExchangeStreamCaptureMode(&mode);
+  return ok;
 }
 
 kvsel_status check_score_args(const kvsel_desc* desc, const void* q, const void* k, const float* scores,

@@ -8,6 +8,14 @@
  * on the stream passed in; the library keeps no per-call state, so calls with
  * distinct workspaces may run concurrently from several host threads.
  *
+ * Stream capture.  The calls of a step (scoring, aggregation, selection,
+ * compaction, page table, attention) enqueue only kernels and memsets on the
+ * stream and read host arguments at call time, so a step can be captured into
+ * a CUDA graph (in any capture mode) and replayed; a replay reads the device
+ * buffers as they are then, with the host arguments of the captured call.
+ * kvsel_read_device_error() and kvsel_trace_read() synchronise and are not
+ * for capture.
+ *
  * Arguments are checked on the host before any launch; a rejected call
  * returns a status and launches nothing.  A launch failure returns
  * KVSEL_ERR_CUDA.  Errors that only the device can see (a bounded wait that
